@@ -1,0 +1,402 @@
+/*
+ * la_oracle.c -- plain fp64 restatement of normalized causal linear attention
+ * (ELU+1 feature map) and of the delta-rule memory.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg, never by the product library.  It shares no
+ * code, header or constant with the CUDA path.  Every function is written to
+ * be checked against the pages by eye: no blocking, fusion or reordering
+ * beyond what the cited definition states.  Threads split the independent
+ * (batch, head) pairs and nothing else.
+ *
+ * Citations (page title, section):
+ *   P1 = "AIGC 基本功|线性、循环与记忆架构-LinearMem" (jefxiong.cn)
+ *   P3 = "线性注意力与SSM" (ggaaooppeenngg.github.io)
+ *   P5 = "sequence-models" practice notes (wineandchord.com)
+ */
+#define _GNU_SOURCE
+#include "la_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <sched.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Feature map.  P1 section 03 "从检索权重开始": phi(u) = u + 1 when u > 0 and
+ * exp(u) when u <= 0 (so phi(0) = 1, continuous, always positive). */
+static double phi(double u) { return u > 0.0 ? u + 1.0 : exp(u); }
+
+int orc_phi(const double* u, double* out, int64_t n) {
+  if (n < 0 || (n > 0 && (!u || !out))) return -1;
+  for (int64_t i = 0; i < n; ++i) out[i] = phi(u[i]);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Work split over heads.  Each job gets a contiguous range of head indices. */
+typedef void (*head_fn)(void* ctx, int64_t head);
+
+typedef struct {
+  head_fn fn;
+  void* ctx;
+  int64_t begin, end;
+} range_job;
+
+static void* run_range(void* p) {
+  range_job* j = (range_job*)p;
+  for (int64_t h = j->begin; h < j->end; ++h) j->fn(j->ctx, h);
+  return NULL;
+}
+
+int orc_default_threads(void) {
+  cpu_set_t set;
+  CPU_ZERO(&set);
+  if (sched_getaffinity(0, sizeof(set), &set) == 0) {
+    int c = CPU_COUNT(&set);
+    if (c > 0) return c;
+  }
+  return 1;
+}
+
+static void for_each_head(int64_t nheads, int nthreads, head_fn fn, void* ctx) {
+  if (nthreads <= 0) nthreads = orc_default_threads();
+  if (nthreads > nheads) nthreads = (int)nheads;
+  if (nthreads <= 1) {
+    for (int64_t h = 0; h < nheads; ++h) fn(ctx, h);
+    return;
+  }
+  pthread_t* tid = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+  range_job* jobs = (range_job*)malloc(sizeof(range_job) * nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t].fn = fn;
+    jobs[t].ctx = ctx;
+    jobs[t].begin = nheads * t / nthreads;
+    jobs[t].end = nheads * (t + 1) / nthreads;
+  }
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&tid[t], NULL, run_range, &jobs[t]) != 0) break;
+    started = t;
+  }
+  run_range(&jobs[0]);
+  for (int t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
+  /* any range whose thread could not be created runs here */
+  for (int t = started + 1; t < nthreads; ++t) run_range(&jobs[t]);
+  free(jobs);
+  free(tid);
+}
+
+/* Common argument bundle for the linear-attention forms. */
+typedef struct {
+  const double *q, *k, *v, *S0, *z0;
+  int N, dk, dv, C;
+  double eps;
+  double *o, *S_N, *z_N;
+} la_args;
+
+static int la_check(const double* q, const double* k, const double* v, int B,
+                    int H, int N, int dk, int dv, double eps, const double* o) {
+  if (B < 1 || H < 1 || N < 0 || dk < 1 || dv < 1 || !(eps >= 0.0)) return -1;
+  if (N > 0 && (!q || !k || !v || !o)) return -1;
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* (1) Recurrence, P1 section 03: S_0 = 0, z_0 = 0 (here: S0, z0), and for each
+ * token first write  S_t = S_{t-1} + phi(k_t) v_t^T,  z_t = z_{t-1} + phi(k_t),
+ * then read  o_t^T = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps).
+ * Returns o, and the final S and z (P1 appendix: recurrent_linear returns
+ * out, S, z). */
+static void recurrent_head(void* p, int64_t h) {
+  const la_args* a = (const la_args*)p;
+  const int N = a->N, dk = a->dk, dv = a->dv;
+  double* S = a->S_N + h * (int64_t)dk * dv;
+  double* z = a->z_N + h * (int64_t)dk;
+  if (a->S0) memcpy(S, a->S0 + h * (int64_t)dk * dv, sizeof(double) * dk * dv);
+  else memset(S, 0, sizeof(double) * dk * dv);
+  if (a->z0) memcpy(z, a->z0 + h * (int64_t)dk, sizeof(double) * dk);
+  else memset(z, 0, sizeof(double) * dk);
+
+  double* fk = (double*)malloc(sizeof(double) * dk);
+  double* fq = (double*)malloc(sizeof(double) * dk);
+  for (int t = 0; t < N; ++t) {
+    const double* qt = a->q + (h * (int64_t)N + t) * dk;
+    const double* kt = a->k + (h * (int64_t)N + t) * dk;
+    const double* vt = a->v + (h * (int64_t)N + t) * dv;
+    double* ot = a->o + (h * (int64_t)N + t) * dv;
+    for (int i = 0; i < dk; ++i) fk[i] = phi(kt[i]);
+    for (int i = 0; i < dk; ++i) fq[i] = phi(qt[i]);
+    /* write */
+    for (int i = 0; i < dk; ++i) {
+      for (int j = 0; j < dv; ++j) S[i * dv + j] += fk[i] * vt[j];
+      z[i] += fk[i];
+    }
+    /* read */
+    double den = 0.0;
+    for (int i = 0; i < dk; ++i) den += fq[i] * z[i];
+    den += a->eps;
+    for (int j = 0; j < dv; ++j) {
+      double num = 0.0;
+      for (int i = 0; i < dk; ++i) num += fq[i] * S[i * dv + j];
+      ot[j] = num / den;
+    }
+  }
+  free(fk);
+  free(fq);
+}
+
+int orc_la_recurrent(const double* q, const double* k, const double* v, int B,
+                     int H, int N, int dk, int dv, double eps, const double* S0,
+                     const double* z0, double* o, double* S_N, double* z_N,
+                     int nthreads) {
+  if (la_check(q, k, v, B, H, N, dk, dv, eps, o) || !S_N || !z_N) return -1;
+  la_args a = {q, k, v, S0, z0, N, dk, dv, 0, eps, o, S_N, z_N};
+  for_each_head((int64_t)B * H, nthreads, recurrent_head, &a);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* (2) Quadratic masked form, P1 section 03 (the normalized sum over i <= t)
+ * and P1 appendix explicit_linear: W = phi(Q) phi(K)^T with everything above
+ * the diagonal removed, o = W V / (row sums of W + eps).  Extended with a
+ * nonzero initial state: S0 / z0 add phi(q_t)^T S0 to the numerator and
+ * phi(q_t)^T z0 to the denominator, which is what the recurrence gives when it
+ * starts from S0, z0. */
+static void quadratic_head(void* p, int64_t h) {
+  const la_args* a = (const la_args*)p;
+  const int N = a->N, dk = a->dk, dv = a->dv;
+  const double* S0 = a->S0 ? a->S0 + h * (int64_t)dk * dv : NULL;
+  const double* z0 = a->z0 ? a->z0 + h * (int64_t)dk : NULL;
+  double* fq = (double*)malloc(sizeof(double) * dk);
+  double* fk = (double*)malloc(sizeof(double) * dk);
+  double* num = (double*)malloc(sizeof(double) * dv);
+  for (int t = 0; t < N; ++t) {
+    const double* qt = a->q + (h * (int64_t)N + t) * dk;
+    for (int r = 0; r < dk; ++r) fq[r] = phi(qt[r]);
+    double den = 0.0;
+    for (int j = 0; j < dv; ++j) num[j] = 0.0;
+    if (S0)
+      for (int r = 0; r < dk; ++r)
+        for (int j = 0; j < dv; ++j) num[j] += fq[r] * S0[r * dv + j];
+    if (z0)
+      for (int r = 0; r < dk; ++r) den += fq[r] * z0[r];
+    for (int i = 0; i <= t; ++i) { /* causal mask: i <= t, diagonal kept */
+      const double* ki = a->k + (h * (int64_t)N + i) * dk;
+      const double* vi = a->v + (h * (int64_t)N + i) * dv;
+      for (int r = 0; r < dk; ++r) fk[r] = phi(ki[r]);
+      double w = 0.0;
+      for (int r = 0; r < dk; ++r) w += fq[r] * fk[r];
+      den += w;
+      for (int j = 0; j < dv; ++j) num[j] += w * vi[j];
+    }
+    den += a->eps;
+    double* ot = a->o + (h * (int64_t)N + t) * dv;
+    for (int j = 0; j < dv; ++j) ot[j] = num[j] / den;
+  }
+  free(fq);
+  free(fk);
+  free(num);
+}
+
+int orc_la_quadratic(const double* q, const double* k, const double* v, int B,
+                     int H, int N, int dk, int dv, double eps, const double* S0,
+                     const double* z0, double* o, int nthreads) {
+  if (la_check(q, k, v, B, H, N, dk, dv, eps, o)) return -1;
+  la_args a = {q, k, v, S0, z0, N, dk, dv, 0, eps, o, NULL, NULL};
+  for_each_head((int64_t)B * H, nthreads, quadratic_head, &a);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* (3) Chunkwise form.  P3 section 3 (Mamba-2 / SSD paragraph): inside a chunk
+ * a small masked phi(Q)phi(K)^T attention, across chunks a recurrence; P5
+ * "Chunked scan": chunks hand over only the final state.  For a chunk
+ * [c0, c1) with incoming state (S_prev, z_prev):
+ *   num_t = phi(q_t)^T S_prev + sum_{c0 <= i <= t} (phi(q_t).phi(k_i)) v_i
+ *   den_t = phi(q_t)^T z_prev + sum_{c0 <= i <= t}  phi(q_t).phi(k_i) + eps
+ *   o_t = num_t / den_t
+ * and afterwards S_prev += sum_{i in chunk} phi(k_i) v_i^T,
+ * z_prev += sum_{i in chunk} phi(k_i). */
+static void chunked_head(void* p, int64_t h) {
+  const la_args* a = (const la_args*)p;
+  const int N = a->N, dk = a->dk, dv = a->dv, C = a->C;
+  double* S = a->S_N + h * (int64_t)dk * dv;
+  double* z = a->z_N + h * (int64_t)dk;
+  if (a->S0) memcpy(S, a->S0 + h * (int64_t)dk * dv, sizeof(double) * dk * dv);
+  else memset(S, 0, sizeof(double) * dk * dv);
+  if (a->z0) memcpy(z, a->z0 + h * (int64_t)dk, sizeof(double) * dk);
+  else memset(z, 0, sizeof(double) * dk);
+
+  double* fq = (double*)malloc(sizeof(double) * (size_t)C * dk);
+  double* fk = (double*)malloc(sizeof(double) * (size_t)C * dk);
+  for (int c0 = 0; c0 < N; c0 += C) {
+    const int c1 = (c0 + C < N) ? c0 + C : N;
+    const int n = c1 - c0;
+    for (int t = 0; t < n; ++t)
+      for (int r = 0; r < dk; ++r) {
+        fq[t * dk + r] = phi(a->q[(h * (int64_t)N + c0 + t) * dk + r]);
+        fk[t * dk + r] = phi(a->k[(h * (int64_t)N + c0 + t) * dk + r]);
+      }
+    /* outputs of the chunk, read against the incoming state */
+    for (int t = 0; t < n; ++t) {
+      double* ot = a->o + (h * (int64_t)N + c0 + t) * dv;
+      double den = 0.0;
+      for (int r = 0; r < dk; ++r) den += fq[t * dk + r] * z[r];
+      for (int j = 0; j < dv; ++j) {
+        double s = 0.0;
+        for (int r = 0; r < dk; ++r) s += fq[t * dk + r] * S[r * dv + j];
+        ot[j] = s;
+      }
+      for (int i = 0; i <= t; ++i) {
+        const double* vi = a->v + (h * (int64_t)N + c0 + i) * dv;
+        double w = 0.0;
+        for (int r = 0; r < dk; ++r) w += fq[t * dk + r] * fk[i * dk + r];
+        den += w;
+        for (int j = 0; j < dv; ++j) ot[j] += w * vi[j];
+      }
+      den += a->eps;
+      for (int j = 0; j < dv; ++j) ot[j] /= den;
+    }
+    /* hand the chunk's contribution to the state */
+    for (int i = 0; i < n; ++i) {
+      const double* vi = a->v + (h * (int64_t)N + c0 + i) * dv;
+      for (int r = 0; r < dk; ++r) {
+        for (int j = 0; j < dv; ++j) S[r * dv + j] += fk[i * dk + r] * vi[j];
+        z[r] += fk[i * dk + r];
+      }
+    }
+  }
+  free(fq);
+  free(fk);
+}
+
+int orc_la_chunked(const double* q, const double* k, const double* v, int B,
+                   int H, int N, int dk, int dv, double eps, const double* S0,
+                   const double* z0, int C, double* o, double* S_N, double* z_N,
+                   int nthreads) {
+  if (la_check(q, k, v, B, H, N, dk, dv, eps, o) || C < 1 || !S_N || !z_N)
+    return -1;
+  la_args a = {q, k, v, S0, z0, N, dk, dv, C, eps, o, S_N, z_N};
+  for_each_head((int64_t)B * H, nthreads, chunked_head, &a);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* (4) One decode step: one iteration of the recurrence (1) on a given state,
+ * P1 section 03 (write the current token, then read it with the current
+ * query). */
+typedef struct {
+  const double *q, *k, *v;
+  int dk, dv;
+  double eps;
+  double *S, *z, *o;
+} decode_args;
+
+static void decode_head(void* p, int64_t h) {
+  const decode_args* a = (const decode_args*)p;
+  const int dk = a->dk, dv = a->dv;
+  const double* qh = a->q + h * dk;
+  const double* kh = a->k + h * dk;
+  const double* vh = a->v + h * dv;
+  double* Sh = a->S + h * (int64_t)dk * dv;
+  double* zh = a->z + h * dk;
+  double* oh = a->o + h * dv;
+  /* write */
+  for (int i = 0; i < dk; ++i) {
+    const double fk = phi(kh[i]);
+    for (int j = 0; j < dv; ++j) Sh[i * dv + j] += fk * vh[j];
+    zh[i] += fk;
+  }
+  /* read */
+  double den = 0.0;
+  for (int i = 0; i < dk; ++i) den += phi(qh[i]) * zh[i];
+  den += a->eps;
+  for (int j = 0; j < dv; ++j) {
+    double num = 0.0;
+    for (int i = 0; i < dk; ++i) num += phi(qh[i]) * Sh[i * dv + j];
+    oh[j] = num / den;
+  }
+}
+
+int orc_la_decode_step(const double* q, const double* k, const double* v,
+                       int B, int H, int dk, int dv, double eps, double* S,
+                       double* z, double* o, int nthreads) {
+  if (B < 1 || H < 1 || dk < 1 || dv < 1 || !(eps >= 0.0)) return -1;
+  if (!q || !k || !v || !S || !z || !o) return -1;
+  decode_args a = {q, k, v, dk, dv, eps, S, z, o};
+  for_each_head((int64_t)B * H, nthreads, decode_head, &a);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* (5) Delta rule.  P1 section 03 "从累加改成纠错" (one gradient step on
+ * 1/2 ||S^T k_t - v_t||^2 with step beta_t), P1 appendix delta_step with
+ * alpha = 1, and P5 "Delta-rule fast weight" (read the prediction first, then
+ * write the error):
+ *   reads_t = k_t^T S_{t-1}
+ *   S_t     = S_{t-1} + beta_t k_t (v_t - reads_t)^T
+ * There is no feature map, normalizer or eps. */
+typedef struct {
+  const double *k, *v, *beta, *S0;
+  int N, dk, dv;
+  double *reads, *S_N;
+} delta_args;
+
+static void delta_head(void* p, int64_t h) {
+  const delta_args* a = (const delta_args*)p;
+  const int N = a->N, dk = a->dk, dv = a->dv;
+  double* S = a->S_N + h * (int64_t)dk * dv;
+  if (a->S0) memcpy(S, a->S0 + h * (int64_t)dk * dv, sizeof(double) * dk * dv);
+  else memset(S, 0, sizeof(double) * dk * dv);
+  double* err = (double*)malloc(sizeof(double) * dv);
+  for (int t = 0; t < N; ++t) {
+    const double* kt = a->k + (h * (int64_t)N + t) * dk;
+    const double* vt = a->v + (h * (int64_t)N + t) * dv;
+    const double bt = a->beta[h * (int64_t)N + t];
+    double* rt = a->reads + (h * (int64_t)N + t) * dv;
+    for (int j = 0; j < dv; ++j) {
+      double r = 0.0;
+      for (int i = 0; i < dk; ++i) r += kt[i] * S[i * dv + j];
+      rt[j] = r;
+      err[j] = vt[j] - r;
+    }
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) S[i * dv + j] += bt * kt[i] * err[j];
+  }
+  free(err);
+}
+
+int orc_delta(const double* k, const double* v, const double* beta, int B,
+              int H, int N, int dk, int dv, const double* S0, double* reads,
+              double* S_N, int nthreads) {
+  if (B < 1 || H < 1 || N < 0 || dk < 1 || dv < 1 || !S_N) return -1;
+  if (N > 0 && (!k || !v || !beta || !reads)) return -1;
+  delta_args a = {k, v, beta, S0, N, dk, dv, reads, S_N};
+  for_each_head((int64_t)B * H, nthreads, delta_head, &a);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* (6) Additive outer-product memory with identity features, the write/read
+ * primitive of P3 section 1.3 (memory collision) and of the two-entry example
+ * on the associative-memory page: S = sum_m k_m v_m^T (k v^T convention), read
+ * with a query from the left, q^T S = sum_m (q . k_m) v_m^T. */
+int orc_outer_read(const double* keys, const double* values, int M, int dk,
+                   int dv, const double* queries, int P, double* reads) {
+  if (M < 0 || P < 0 || dk < 1 || dv < 1) return -1;
+  if ((M > 0 && (!keys || !values)) || (P > 0 && (!queries || !reads))) return -1;
+  double* S = (double*)calloc((size_t)dk * dv, sizeof(double));
+  for (int m = 0; m < M; ++m)
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) S[i * dv + j] += keys[m * dk + i] * values[m * dv + j];
+  for (int p = 0; p < P; ++p)
+    for (int j = 0; j < dv; ++j) {
+      double r = 0.0;
+      for (int i = 0; i < dk; ++i) r += queries[p * dk + i] * S[i * dv + j];
+      reads[p * dv + j] = r;
+    }
+  free(S);
+  return 0;
+}
