@@ -1,0 +1,528 @@
+"""Benchmark of the linear-attention hot path on one GB300 (or N replicas).
+
+Headline (the JSON line's value): prefill throughput, tokens/s = B*H*N / s, on
+the bf16 workload B=4 H=8 N=4096 dk=dv=64 (inputs N(0,1), fp32 state and
+accumulation).  One step = one la_prefill call over that batch (phi, the
+intra-chunk scores, the masked score-value product, the inter-chunk read, the
+normalisation, the state update and carry, the final state).  The same run
+measures the other workloads of the path and reports them under "extra":
+the long streaming prefill (B=1 H=16 N=65536), the decode step (B=256 H=32
+dk=dv=128, 100 consecutive steps as one CUDA graph, HBM GB/s), the delta-rule
+memory (B=8 H=16 N=8192 dk=dv=128) and the small fp32 case (B=1 H=1 N=256).
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and torch.cuda.synchronize(), timed with CUDA events on the launching stream;
+the step inputs rotate over four buffer sets (about 340 MB, more than the
+129 MB L2) so that no step finds its inputs in L2.  Per-launch durations of
+the prefill kernel come from events recorded around every launch in the timed
+region.  Clocks are sampled with nvidia-smi while the GPU measurements run.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload per step), printing the same JSON line
+with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("linear-attn prefill tokens/s (B*H*N/s) at dk=dv=64/128; "
+          "decode-step HBM GB/s")
+PREFILL_BYTES_PER_TOKEN = 640  # q,k,v bf16 at d=64 (384 B) + o fp32 (256 B)
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-extra", action="store_true",
+                   help="headline workload only (no long/decode/delta/e2e/cpu)")
+    p.add_argument("--only", default="",
+                   help="comma list of extra workloads to run (long,decode,delta,pr1)")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas, no collective on the
+# data path -- only the barrier and the max over ranks of the timed region)
+
+def _dist_init(n):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons (read only)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if bus_id:
+            cmd += ["-i", bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                     util=float(parts[4]), hw=parts[6], hwt=parts[7],
+                                     swt=parts[8], swp=parts[9]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        load = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "samples_under_load": len([r for r in rows if r["util"] >= 50])}
+
+
+# --------------------------------------------------------------------------
+# measured peaks and committed ncu counters
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fixed_state_recurrent_gb300", "csrc")
+    for name in ("prefill_tc.cu", "tc_primitives.cuh"):
+        p = os.path.join(csrc, name)
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def _committed_traffic(tokens):
+    """dram bytes per launch of the prefill kernel from the committed ncu
+    summary, scaled to `tokens`, or None when the kernel source changed since
+    the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "prefill_tc_ncu.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_token:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_b or m_hash.group(1) != _kernel_source_hash():
+        return None
+    return float(m_b.group(1)) * tokens
+
+
+# --------------------------------------------------------------------------
+# workloads
+
+def _device_inputs(w, seed, device):
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype, seed, w.scale)
+    return q.to(device), k.to(device), v.to(device)
+
+
+def _timed(fn, steps, stream, world, per_launch=True):
+    """Run fn(i) for i in range(steps) on `stream`; returns (total_ms, list of
+    per-step ms) with events on that stream, max over ranks for the total."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    _barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(steps):
+            fn(i)
+            if per_launch or i == steps - 1:
+                evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    total = evs[0].elapsed_time(evs[steps])
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)] if per_launch else []
+    return _max_over_ranks(total, world), per
+
+
+def bench_prefill(api, w, steps, warmup, rank, world, sets=4):
+    import torch
+    dev = torch.device("cuda")
+    bufs = []
+    for r in range(sets):
+        q, k, v = _device_inputs(w, w.seed + 1000 * rank + r, dev)
+        o = torch.empty((w.B, w.H, w.N, w.dv), device=dev)
+        S = torch.empty((w.B, w.H, w.dk, w.dv), device=dev)
+        z = torch.empty((w.B, w.H, w.dk), device=dev)
+        bufs.append((q, k, v, o, S, z))
+    ws = api.workspace(w.B, w.H, w.N, w.dk, w.dv, w.dtype, 0, dev)
+    stream = torch.cuda.Stream()
+
+    def step(i):
+        q, k, v, o, S, z = bufs[i % sets]
+        api.prefill(q, k, v, o=o, S_N=S, z_N=z, ws=ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    total, per = _timed(step, steps, stream, world)
+    status = api.read_device_status(ws, stream)
+    if status != 0:
+        raise RuntimeError(f"prefill kernel reported device status {status}")
+    return total, per
+
+
+def bench_decode(api, rank, world, reps=3):
+    """100 consecutive decode steps captured in one CUDA graph; the state comes
+    from a 1024-token prefix run through la_prefill."""
+    import torch
+    from fixed_state_recurrent_gb300 import inputs
+    w = inputs.WORKLOADS["decode"]
+    dev = torch.device("cuda")
+    B, H, d, P, T = w.B, w.H, w.dk, w.N, w.steps
+    S = torch.empty((B, H, d, d), device=dev)
+    z = torch.empty((B, H, d), device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 1000 * rank)
+    step = 32
+    for b0 in range(0, B, step):  # prefix prefilled 32 sequences at a time
+        pq = inputs.gaussian((step, H, P, d), g, torch.bfloat16, device=dev)
+        pk = inputs.gaussian((step, H, P, d), g, torch.bfloat16, device=dev)
+        pv = inputs.gaussian((step, H, P, d), g, torch.bfloat16, device=dev)
+        api.prefill(pq, pk, pv, S_N=S[b0:b0 + step], z_N=z[b0:b0 + step])
+        del pq, pk, pv
+    qs, ks, vs = inputs.decode_step_inputs(B, H, d, d, T, torch.bfloat16,
+                                           w.seed + 1000 * rank, device=dev)
+    o = torch.empty((T, B, H, d), device=dev)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        api.decode_step(qs[0], ks[0], vs[0], S, z, o=o[0])  # warm (caches attributes)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for t in range(T):
+                api.decode_step(qs[t], ks[t], vs[t], S, z, o=o[t])
+        graph.replay()
+        graph.replay()
+    times = []
+    for _ in range(reps):
+        ms, _ = _timed(lambda i: graph.replay(), 1, stream, world, per_launch=False)
+        times.append(ms)
+    ms = min(times)
+    bytes_per_head = 2 * d * d * 4 + 2 * d * 4 + 3 * d * 2 + d * 4
+    bytes_step = bytes_per_head * B * H
+    us_step = ms * 1e3 / T
+    return {"workload": "decode: B=256 H=32 dk=dv=128, 100 steps in one CUDA graph, "
+                        "state from a 1024-token bf16 prefix",
+            "us_per_step": us_step, "hbm_gbs": bytes_step / (us_step * 1e-6) / 1e9,
+            "bytes_per_step": bytes_step, "reps": reps, "launches_per_rep": T}
+
+
+def bench_delta(api, rank, world, reps=3):
+    import torch
+    from fixed_state_recurrent_gb300 import inputs
+    w = inputs.WORKLOADS["delta"]
+    dev = torch.device("cuda")
+    k, v, beta = inputs.delta_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype,
+                                     w.seed + 1000 * rank, device=dev)
+    reads = torch.empty((w.B, w.H, w.N, w.dv), device=dev)
+    S = torch.empty((w.B, w.H, w.dk, w.dv), device=dev)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    fn = lambda i: api.delta_prefill(k, v, beta, reads=reads, S_N=S)
+    with torch.cuda.stream(stream):
+        fn(0)
+    ms, per = _timed(fn, reps, stream, world)
+    ms_call = min(per)
+    tokens = w.B * w.H * w.N
+    flops = 4.0 * w.dk * w.dv * tokens
+    return {"workload": "delta: B=8 H=16 N=8192 dk=dv=128, unit bf16 keys, bf16 values, "
+                        "sigmoid beta", "ms_per_call": ms_call,
+            "tokens_per_s": tokens / (ms_call * 1e-3),
+            "fp32_tflops": flops / (ms_call * 1e-3) / 1e12}
+
+
+def bench_simple_prefill(api, wname, rank, world, reps=5):
+    import torch
+    from fixed_state_recurrent_gb300 import inputs
+    w = inputs.WORKLOADS[wname]
+    dev = torch.device("cuda")
+    q, k, v = _device_inputs(w, w.seed + 1000 * rank, dev)
+    o = torch.empty((w.B, w.H, w.N, w.dv), device=dev)
+    S = torch.empty((w.B, w.H, w.dk, w.dv), device=dev)
+    z = torch.empty((w.B, w.H, w.dk), device=dev)
+    ws = api.workspace(w.B, w.H, w.N, w.dk, w.dv, w.dtype, 0, dev)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    fn = lambda i: api.prefill(q, k, v, o=o, S_N=S, z_N=z, ws=ws)
+    with torch.cuda.stream(stream):
+        fn(0)
+    _, per = _timed(fn, reps, stream, world)
+    ms = statistics.median(per)
+    res = {"workload": f"{wname}: B={w.B} H={w.H} N={w.N} dk={w.dk} dv={w.dv} "
+                       f"{'bf16' if w.dtype == torch.bfloat16 else 'fp32'}",
+           "ms_per_call": ms, "tokens_per_s": w.tokens / (ms * 1e-3)}
+    if w.dtype == torch.bfloat16:
+        b = PREFILL_BYTES_PER_TOKEN * w.tokens + w.B * w.H * (w.dk * w.dv + w.dk) * 4
+        res["hbm_gbs"] = b / (ms * 1e-3) / 1e9
+    return res
+
+
+def bench_e2e(api, w, steps, warmup, rank, world):
+    """Same metric through the public API from pinned HOST buffers: each step
+    copies q, k, v host->device, runs la_prefill and copies o, S, z back."""
+    import torch
+    from fixed_state_recurrent_gb300 import inputs
+    dev = torch.device("cuda")
+    q, k, v = inputs.la_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype, w.seed + 1000 * rank)
+    hq, hk, hv = (x.pin_memory() for x in (q, k, v))
+    ho = torch.empty((w.B, w.H, w.N, w.dv)).pin_memory()
+    hS = torch.empty((w.B, w.H, w.dk, w.dv)).pin_memory()
+    hz = torch.empty((w.B, w.H, w.dk)).pin_memory()
+    dq, dk_, dv_ = (torch.empty_like(x, device=dev) for x in (q, k, v))
+    ws = api.workspace(w.B, w.H, w.N, w.dk, w.dv, w.dtype, 0, dev)
+    stream = torch.cuda.Stream()
+
+    def step(i):
+        dq.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        o, S, z = api.prefill(dq, dk_, dv_, ws=ws)
+        ho.copy_(o, non_blocking=True)
+        hS.copy_(S, non_blocking=True)
+        hz.copy_(z, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    total, _ = _timed(step, steps, stream, world, per_launch=False)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hS, hz))
+    return total, h2d, d2h
+
+
+def cpu_baseline(w, target_s=10.0):
+    """The fp64 oracle, as it stands, on the host cores: token recurrence over
+    the whole prefill workload, repeated until about target_s of CPU time."""
+    import torch
+    import oracle
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype, w.seed, w.scale)
+    f = lambda t: t.to(torch.float64).numpy()
+    q, k, v = f(q), f(k), f(v)
+    cores = oracle.default_threads()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.la_recurrent(q, k, v, threads=cores)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or done >= 20:
+            break
+    return {"value": done * w.tokens / el, "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"fp64 C oracle token recurrence over the whole prefill workload "
+                      f"(B={w.B} H={w.H} N={w.N} d={w.dk}, {w.tokens} tokens) x {done}, "
+                      f"{el:.1f} s, threads over heads"}
+
+
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores, one bounded
+    sample of the prefill workload (8 of its 32 heads) per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    from fixed_state_recurrent_gb300 import inputs
+    oracle.build()
+    w = inputs.WORKLOADS["prefill"]
+    q, k, v = inputs.la_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype, w.seed, w.scale)
+    heads = 8
+    f = lambda t: t.reshape(w.B * w.H, 1, w.N, -1)[:heads].to(torch.float64).numpy()
+    q, k, v = f(q), f(k), f(v)
+    cores = oracle.default_threads()
+    for _ in range(args.warmup):
+        oracle.la_recurrent(q, k, v, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.la_recurrent(q, k, v, threads=cores)
+    el = time.perf_counter() - t0
+    tokens = heads * w.N * args.steps
+    value = tokens / el
+    sample = (f"fp64 C oracle token recurrence, {heads} of the {w.B * w.H} heads "
+              f"x {w.N} tokens of the prefill workload per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill: B=4 H=8 N=4096 dk=dv=64 bf16 N(0,1) "
+                                   f"(sample: {heads} heads per step)",
+                       "B": w.B, "H": w.H, "N": w.N, "dk": w.dk, "dv": w.dv},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    from fixed_state_recurrent_gb300 import build, api, inputs
+    rank, world = _dist_init(args.gpus)
+    if rank == 0 or world == 1:
+        build.build()
+    _barrier(world)
+    api.load()
+    dev = torch.device("cuda")
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    bus_id = None
+    if isinstance(bus, int) and hasattr(props, "pci_domain_id"):
+        bus_id = f"{props.pci_domain_id:08X}:{bus:02X}:{props.pci_device_id:02X}.0"
+    sampler = ClockSampler(bus_id)
+    time.sleep(0.3)
+
+    w = inputs.WORKLOADS["prefill"]
+    total_ms, per = bench_prefill(api, w, args.steps, args.warmup, rank, world)
+    ms_step = total_ms / args.steps
+    value = w.tokens * world / (total_ms * 1e-3 / args.steps)
+
+    extra = {}
+    e2e = None
+    wanted = set(x for x in args.only.split(",") if x) or {"long", "decode", "delta", "pr1"}
+    if not args.no_extra:
+        if "long" in wanted:
+            extra["long"] = bench_simple_prefill(api, "long", rank, world)
+        if "decode" in wanted:
+            extra["decode"] = bench_decode(api, rank, world)
+        if "delta" in wanted:
+            extra["delta"] = bench_delta(api, rank, world)
+        if "pr1" in wanted:
+            extra["pr1"] = bench_simple_prefill(api, "pr1", rank, world)
+        e_ms, h2d, d2h = bench_e2e(api, w, max(args.steps // 4, 5), 3, rank, world)
+        e_steps = max(args.steps // 4, 5)
+        e2e = {"value": w.tokens * world / (e_ms * 1e-3 / e_steps), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e_steps}
+    clocks = sampler.stop()
+
+    hbm_peak, _, peak_kind = _peaks()
+    algo_bytes = PREFILL_BYTES_PER_TOKEN * w.tokens + w.B * w.H * (w.dk * w.dv + w.dk) * 4
+    launch_ms = statistics.mean(per)
+    achieved = algo_bytes / (launch_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": _committed_traffic(w.tokens),
+                "peak_kind": f"of {peak_kind}",
+                "algorithmic_bytes_per_launch": algo_bytes,
+                "launch_ms_mean": launch_ms, "launch_ms_min": min(per)}
+    if "decode" in extra:
+        extra["decode"]["hbm_frac"] = extra["decode"]["hbm_gbs"] / hbm_peak
+    if "long" in extra and "hbm_gbs" in extra["long"]:
+        extra["long"]["hbm_frac"] = extra["long"]["hbm_gbs"] / hbm_peak
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_extra:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "prefill: B=4 H=8 N=4096 dk=dv=64, bf16 q,k,v ~ N(0,1), "
+                                       "fp32 state/accumulate, zero initial state",
+                           "B": w.B, "H": w.H, "N": w.N, "dk": w.dk, "dv": w.dv,
+                           "chunk": 128, "parallelism": f"replicas x{world}",
+                           "l2": "4 rotating input/output buffer sets (~340 MB > 129 MB L2)"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps, "clocks": clocks, "extra": extra}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

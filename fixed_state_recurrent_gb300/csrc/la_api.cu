@@ -1,0 +1,230 @@
+// la_api.cu -- the C ABI of libla.so (declared in include/la.h): argument
+// validation, path choice and launches on the caller's stream.  No entry point
+// allocates memory; every tensor belongs to the caller.
+#include "la.h"
+#include "la_internal.h"
+
+#include <math.h>
+#include <stdint.h>
+
+namespace {
+
+using la::PrefillArgs;
+
+constexpr int kMaxDim = 128;
+constexpr int kMaxDevices = 64;
+
+// 0 = unknown, 1 = sm_103 device, 2 = other device.
+int g_device_kind[kMaxDevices];
+
+la_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return LA_ERR_UNSUPPORTED;
+  if (g_device_kind[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return LA_ERR_CUDA;
+    g_device_kind[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return g_device_kind[dev] == 1 ? LA_OK : LA_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+Span span(const void* p, size_t bytes) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + bytes};
+}
+
+bool overlap(Span a, Span b) {
+  if (a.lo == a.hi || b.lo == b.hi || a.lo == 0 || b.lo == 0) return false;
+  return a.lo < b.hi && b.lo < a.hi;
+}
+
+bool dims_ok(int B, int H, int N, int dk, int dv) {
+  if (B < 1 || H < 1 || N < 0 || dk < 1 || dv < 1) return false;
+  if (dk > kMaxDim || dv > kMaxDim) return false;
+  const double elems = (double)B * H * (double)(N > 0 ? N : 1) * (dk > dv ? dk : dv);
+  return elems < 1099511627776.0;  // 2^40
+}
+
+size_t elem_bytes(la_dtype t) { return t == LA_BF16 ? 2 : 4; }
+
+bool dtype_ok(la_dtype t) { return t == LA_F32 || t == LA_BF16; }
+
+la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+// Copy (or zero) an initial state into a final state for N == 0.
+cudaError_t copy_state(const float* src, float* dst, size_t bytes, cudaStream_t s) {
+  if (src == dst) return cudaSuccess;
+  if (src) return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+  return cudaMemsetAsync(dst, 0, bytes, s);
+}
+
+bool use_tensor_path(la_dtype t, int dk, int dv) {
+  return t == LA_BF16 && dk == dv && (dk == 64 || dk == 128);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t la_state_bytes(int dk, int dv) {
+  if (dk < 1 || dv < 1) return 0;
+  return ((size_t)dk * dv + dk) * sizeof(float);
+}
+
+const char* la_status_string(la_status s) {
+  switch (s) {
+    case LA_OK: return "LA_OK";
+    case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG: invalid argument";
+    case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: not supported on this device or build";
+    case LA_ERR_CUDA: return "LA_ERR_CUDA: a CUDA call failed";
+    case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded inter-block wait gave up";
+  }
+  return "LA_ERR_UNKNOWN";
+}
+
+size_t la_prefill_workspace_bytes(int B, int H, int N, int dk, int dv,
+                                  la_dtype in_dtype, int chunk) {
+  if (!dims_ok(B, H, N, dk, dv) || !dtype_ok(in_dtype)) return 0;
+  if (chunk != 0 && chunk != 128) return 0;
+  size_t bytes = sizeof(la::WsHeader);
+  if (use_tensor_path(in_dtype, dk, dv))
+    bytes += la::prefill_tc_workspace_bytes(B, H, N, dk, chunk);
+  return bytes;
+}
+
+la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                     int B, int H, int N, int dk, int dv, float eps,
+                     const float* S0, const float* z0, float* o, float* S_N,
+                     float* z_N, int chunk, void* workspace, size_t ws_bytes,
+                     cudaStream_t stream) {
+  if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return LA_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  if (chunk != 0 && chunk != 128) return LA_ERR_INVALID_ARG;
+  if (!S_N || !z_N || !workspace) return LA_ERR_INVALID_ARG;
+  if (N > 0 && (!q || !k || !v || !o)) return LA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, S0, z0, o, S_N, z_N, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
+  const size_t need = la_prefill_workspace_bytes(B, H, N, dk, dv, in_dtype, chunk);
+  if (need == 0 || ws_bytes < need) return LA_ERR_INVALID_ARG;
+
+  const size_t heads = (size_t)B * H;
+  const size_t eb = elem_bytes(in_dtype);
+  const Span sq = span(q, heads * N * dk * eb), sk = span(k, heads * N * dk * eb);
+  const Span sv = span(v, heads * N * dv * eb), so = span(o, heads * N * dv * 4);
+  const Span sS0 = span(S0, heads * dk * dv * 4), sz0 = span(z0, heads * dk * 4);
+  const Span sSN = span(S_N, heads * dk * dv * 4), szN = span(z_N, heads * dk * 4);
+  const Span sws = span(workspace, ws_bytes);
+  // outputs against every input and each other; S_N may equal S0 exactly
+  const Span outs[] = {so, sSN, szN};
+  const Span ins[] = {sq, sk, sv, sws};
+  for (const Span& a : outs)
+    for (const Span& b : ins)
+      if (overlap(a, b)) return LA_ERR_INVALID_ARG;
+  if (overlap(so, sSN) || overlap(so, szN) || overlap(sSN, szN)) return LA_ERR_INVALID_ARG;
+  if (overlap(so, sS0) || overlap(so, sz0) || overlap(szN, sS0) || overlap(sSN, sz0))
+    return LA_ERR_INVALID_ARG;
+  if (overlap(sSN, sS0) && S_N != S0) return LA_ERR_INVALID_ARG;
+  if (overlap(szN, sz0) && z_N != z0) return LA_ERR_INVALID_ARG;
+
+  const la_status dev = check_device();
+  if (dev != LA_OK) return dev;
+
+  if (N == 0) {
+    cudaError_t e = copy_state(S0, S_N, heads * dk * dv * 4, stream);
+    if (e == cudaSuccess) e = copy_state(z0, z_N, heads * dk * 4, stream);
+    return from_cuda(e);
+  }
+
+  PrefillArgs a;
+  a.q = q; a.k = k; a.v = v;
+  a.bf16 = in_dtype == LA_BF16;
+  a.B = B; a.H = H; a.N = N; a.dk = dk; a.dv = dv;
+  a.eps = eps;
+  a.S0 = S0; a.z0 = z0;
+  a.o = o; a.S_N = S_N; a.z_N = z_N;
+  a.chunk = chunk == 0 ? 128 : chunk;
+  a.workspace = workspace;
+  a.ws_bytes = ws_bytes;
+  if (use_tensor_path(in_dtype, dk, dv) && la::prefill_tc_supported(a))
+    return from_cuda(la::launch_prefill_tc(a, stream));
+  return from_cuda(la::launch_prefill_simt(a, stream));
+}
+
+la_status la_decode_step(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                         int B, int H, int dk, int dv, float eps, float* S,
+                         float* z, float* o, cudaStream_t stream) {
+  if (!dtype_ok(in_dtype) || !dims_ok(B, H, 1, dk, dv)) return LA_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !S || !z || !o) return LA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, S, z, o};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LA_ERR_INVALID_ARG;
+  const size_t heads = (size_t)B * H;
+  const size_t eb = elem_bytes(in_dtype);
+  const Span sq = span(q, heads * dk * eb), sk = span(k, heads * dk * eb);
+  const Span sv = span(v, heads * dv * eb), so = span(o, heads * dv * 4);
+  const Span sS = span(S, heads * dk * dv * 4), sz = span(z, heads * dk * 4);
+  const Span outs[] = {so, sS, sz};
+  const Span ins[] = {sq, sk, sv};
+  for (const Span& a : outs)
+    for (const Span& b : ins)
+      if (overlap(a, b)) return LA_ERR_INVALID_ARG;
+  if (overlap(so, sS) || overlap(so, sz) || overlap(sS, sz)) return LA_ERR_INVALID_ARG;
+  const la_status dev = check_device();
+  if (dev != LA_OK) return dev;
+  return from_cuda(la::launch_decode_step(q, k, v, in_dtype == LA_BF16, B, H, dk,
+                                          dv, eps, S, z, o, stream));
+}
+
+la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const float* beta,
+                        int B, int H, int N, int dk, int dv, const float* S0,
+                        float* reads, float* S_N, cudaStream_t stream) {
+  if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return LA_ERR_INVALID_ARG;
+  if (!S_N) return LA_ERR_INVALID_ARG;
+  if (N > 0 && (!k || !v || !beta || !reads)) return LA_ERR_INVALID_ARG;
+  const void* ptrs[] = {k, v, beta, S0, reads, S_N};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
+  const size_t heads = (size_t)B * H;
+  const size_t eb = elem_bytes(in_dtype);
+  const Span sk = span(k, heads * N * dk * eb), sv = span(v, heads * N * dv * eb);
+  const Span sb = span(beta, heads * N * 4), sr = span(reads, heads * N * dv * 4);
+  const Span sS0 = span(S0, heads * dk * dv * 4), sSN = span(S_N, heads * dk * dv * 4);
+  const Span outs[] = {sr, sSN};
+  const Span ins[] = {sk, sv, sb};
+  for (const Span& a : outs)
+    for (const Span& b : ins)
+      if (overlap(a, b)) return LA_ERR_INVALID_ARG;
+  if (overlap(sr, sSN) || overlap(sr, sS0)) return LA_ERR_INVALID_ARG;
+  if (overlap(sSN, sS0) && S_N != S0) return LA_ERR_INVALID_ARG;
+  const la_status dev = check_device();
+  if (dev != LA_OK) return dev;
+  if (N == 0) return from_cuda(copy_state(S0, S_N, heads * dk * dv * 4, stream));
+  return from_cuda(la::launch_delta_prefill(k, v, in_dtype == LA_BF16, beta, B, H,
+                                            N, dk, dv, S0, reads, S_N, stream));
+}
+
+la_status la_read_device_status(const void* workspace, cudaStream_t stream) {
+  if (!workspace) return LA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return LA_ERR_CUDA;
+  const la::WsHeader* h = reinterpret_cast<const la::WsHeader*>(workspace);
+  unsigned status = 0;
+  if (cudaMemcpy(&status, &h->status, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LA_ERR_CUDA;
+  if (status != 0) {
+    if (cudaMemset((void*)&h->status, 0, sizeof(status)) != cudaSuccess) return LA_ERR_CUDA;
+  }
+  return (status & la::kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
+}
+
+}  // extern "C"

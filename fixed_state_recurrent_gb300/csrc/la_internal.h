@@ -1,0 +1,76 @@
+// la_internal.h -- declarations shared by the translation units of libla.so.
+// Not part of the public ABI (that is include/la.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace la {
+
+// Workspace header: the first 256 bytes of every prefill workspace.
+//   status  sticky error bits set by kernels (kStatusTimeout)
+//   epoch   generation counter of the tensor-core prefill's inter-block flags
+//   done    blocks of the running tensor-core launch that have finished
+struct WsHeader {
+  unsigned status;
+  unsigned epoch;
+  unsigned done;
+  unsigned reserved[61];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+constexpr unsigned kStatusTimeout = 1u;
+
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  bool bf16;
+  int B, H, N, dk, dv;
+  float eps;
+  const float* S0;
+  const float* z0;
+  float* o;
+  float* S_N;
+  float* z_N;
+  int chunk;
+  void* workspace;
+  size_t ws_bytes;
+};
+
+// CUDA-core prefill (any dk, dv <= 128; fp32 or bf16 inputs).
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
+
+// Tensor-core chunked prefill (bf16, dk = dv in {64, 128}).
+bool prefill_tc_supported(const PrefillArgs& a);
+size_t prefill_tc_workspace_bytes(int B, int H, int N, int d, int chunk);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+
+cudaError_t launch_decode_step(const void* q, const void* k, const void* v,
+                               bool bf16, int B, int H, int dk, int dv,
+                               float eps, float* S, float* z, float* o,
+                               cudaStream_t stream);
+
+cudaError_t launch_delta_prefill(const void* k, const void* v, bool bf16,
+                                 const float* beta, int B, int H, int N,
+                                 int dk, int dv, const float* S0, float* reads,
+                                 float* S_N, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Device helpers shared by the CUDA-core kernels.
+
+// ELU+1 feature map, full-precision expf.  Page "AIGC 基本功|线性、循环与记忆
+// 架构-LinearMem", section 03: phi(u) = u + 1 for u > 0, exp(u) otherwise.
+__device__ __forceinline__ float phi_f32(float u) {
+  return u > 0.f ? u + 1.f : expf(u);
+}
+
+// Element e of an input tensor stored as fp32 or bf16, widened to fp32.
+__device__ __forceinline__ float load_in(const void* p, size_t e, bool bf16) {
+  if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[e]);
+  return reinterpret_cast<const float*>(p)[e];
+}
+
+}  // namespace la

@@ -1,0 +1,131 @@
+/*
+ * la.h -- C ABI of libla.so: normalized causal linear attention with the
+ * ELU+1 feature map, and the delta-rule fast-weight memory, on one GB300
+ * (sm_103a).
+ *
+ * Definitions (page "AIGC 基本功|线性、循环与记忆架构-LinearMem", section 03):
+ *   phi(u) = u + 1 (u > 0), exp(u) (u <= 0), applied elementwise
+ *   S_t = S_{t-1} + phi(k_t) v_t^T          (dk x dv, the "k v^T" layout)
+ *   z_t = z_{t-1} + phi(k_t)                (dk)
+ *   o_t^T = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps)      write, then read
+ * Delta rule (same page, "从累加改成纠错"; page "sequence-models" practice
+ * notes, "Delta-rule fast weight"):
+ *   read_t = k_t^T S_{t-1};   S_t = S_{t-1} + beta_t k_t (v_t - read_t)^T
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layouts: row-major, contiguous, innermost dimension fastest.
+ *   q, k        [B][H][N][dk]  (decode: [B][H][dk])   dtype in_dtype
+ *   v           [B][H][N][dv]  (decode: [B][H][dv])   dtype in_dtype
+ *   o, reads    [B][H][N][dv]  (decode: [B][H][dv])   float32
+ *   S, S0, S_N  [B][H][dk][dv]                        float32, S[i][j] = sum phi(k)_i v_j
+ *   z, z0, z_N  [B][H][dk]                            float32
+ *   beta        [B][H][N]                             float32
+ * Ownership: every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *   library allocates no device memory and keeps no per-call state; the only
+ *   process-wide state is cached device attributes and kernel settings.
+ * Alignment: every tensor pointer must be 16-byte aligned.
+ * Sizes: B, H, dk, dv >= 1; dk, dv <= 128; N >= 0; B*H*N*max(dk,dv) < 2^40.
+ *   N = 0 is valid: the final state is a copy of the initial state.
+ * eps: finite and >= 0 (1e-6 in the pages' experiments).
+ * Execution: every call is asynchronous on `stream` (NULL = legacy default
+ *   stream).  The return value reports argument errors (LA_ERR_INVALID_ARG,
+ *   LA_ERR_UNSUPPORTED, nothing launched) and launch errors (LA_ERR_CUDA).
+ *   Errors a kernel detects while running (a bounded wait that gave up) are
+ *   recorded in the workspace and read back with la_read_device_status.
+ * Aliasing: outputs must not overlap inputs, except the state pairs named
+ *   below (S_N may be S0, z_N may be z0).
+ * Path choice: LA_BF16 inputs with dk = dv in {64, 128} run the tensor-core
+ *   chunked kernel (tcgen05 MMA, TMEM accumulators, TMA loads); every other
+ *   valid shape and LA_F32 inputs run the CUDA-core kernel.  Both run on the
+ *   GPU; there is no CPU fallback.
+ */
+#ifndef LA_H
+#define LA_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LA_OK = 0,
+  LA_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment, aliasing or eps */
+  LA_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no sm_103a device) */
+  LA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  LA_ERR_TIMEOUT = 4       /* a kernel's bounded inter-block wait gave up */
+} la_status;
+
+typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+/*
+ * la_prefill -- causal prefill of N tokens per (batch, head).
+ * Computes o_t for t = 1..N from the recurrence above, starting from S0, z0
+ * (NULL = zero state, P1 section 05: state is reset per request), and writes
+ * the final state S_N, z_N (P1 appendix: recurrent_linear returns out, S, z).
+ *   q, k, v     inputs, in_dtype (LA_F32 or LA_BF16)
+ *   S0, z0      initial state or NULL; S_N may alias S0, z_N may alias z0
+ *   o, S_N, z_N outputs, float32
+ *   chunk       chunk length of the tensor-core path; 0 = automatic (128).
+ *               The CUDA-core path ignores it.
+ *   workspace   device scratch of at least la_prefill_workspace_bytes(...)
+ *               bytes, ZERO-FILLED before its first use; the kernels leave it
+ *               ready for the next call.  Calls that share a workspace must be
+ *               ordered on one stream.  It also holds the device status word.
+ */
+la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                     int B, int H, int N, int dk, int dv, float eps,
+                     const float* S0, const float* z0,
+                     float* o, float* S_N, float* z_N,
+                     int chunk, void* workspace, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/* Bytes of workspace la_prefill needs for these arguments (always >= 256).
+ * Returns 0 for arguments la_prefill would reject. */
+size_t la_prefill_workspace_bytes(int B, int H, int N, int dk, int dv,
+                                  la_dtype in_dtype, int chunk);
+
+/*
+ * la_decode_step -- one token per (batch, head) on a resident state, in place:
+ *   S += phi(k) v^T;  z += phi(k);  o = phi(q)^T S / (phi(q)^T z + eps)
+ * (update, then read: P1 section 03).  S and z are read once and written once.
+ *   q, k [B][H][dk], v [B][H][dv] in in_dtype;  o [B][H][dv] float32.
+ */
+la_status la_decode_step(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                         int B, int H, int dk, int dv, float eps,
+                         float* S, float* z, float* o, cudaStream_t stream);
+
+/*
+ * delta_prefill -- the delta-rule memory over N tokens per (batch, head):
+ *   reads[t] = k_t^T S_{t-1};  S_t = S_{t-1} + beta_t k_t (v_t - reads[t])^T
+ * (prediction first, then the error write: "sequence-models" practice notes,
+ * delta_memory).  No feature map, no normalizer, no eps.
+ *   k [B][H][N][dk], v [B][H][N][dv] in in_dtype;  beta [B][H][N] float32
+ *   S0 initial memory or NULL (zero); S_N may alias S0
+ *   reads [B][H][N][dv], S_N [B][H][dk][dv] float32
+ */
+la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const float* beta,
+                        int B, int H, int N, int dk, int dv,
+                        const float* S0, float* reads, float* S_N,
+                        cudaStream_t stream);
+
+/* Bytes of one head's recurrent state, (dk*dv + dk) * 4: 16640 at 64 x 64
+ * (P1 section 01).  0 for dk or dv < 1. */
+size_t la_state_bytes(int dk, int dv);
+
+/* Static, human-readable name of a status code. */
+const char* la_status_string(la_status s);
+
+/* Synchronizes `stream`, then returns and clears the status word that kernels
+ * record in `workspace` (LA_ERR_TIMEOUT if a bounded wait gave up since the
+ * last read, otherwise LA_OK).  LA_ERR_INVALID_ARG for a NULL workspace,
+ * LA_ERR_CUDA if the synchronization or copy fails. */
+la_status la_read_device_status(const void* workspace, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H */

@@ -1,0 +1,118 @@
+"""The C ABI: libla.so builds, loads, exports every symbol include/la.h
+declares, and its host-side logic (sizes, status strings, argument
+validation) behaves as documented.  No call here reaches a GPU: every
+validation case is rejected before the library touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fixed_state_recurrent_gb300 import build, api
+    build.build()
+    return api.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "la.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
+              "delta_prefill", "la_state_bytes", "la_status_string",
+              "la_read_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), f"libla.so does not export {n}"
+
+
+def test_state_bytes(lib):
+    assert lib.la_state_bytes(64, 64) == 16640   # 64x64 fp32 S plus 64 fp32 z
+    assert lib.la_state_bytes(128, 128) == (128 * 128 + 128) * 4
+    assert lib.la_state_bytes(0, 64) == 0
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert lib.la_status_string(s).startswith(b"LA_")
+    assert b"TIMEOUT" in lib.la_status_string(4)
+
+
+def test_workspace_bytes(lib):
+    assert lib.la_prefill_workspace_bytes(1, 1, 256, 64, 64, 0, 0) >= 256
+    assert lib.la_prefill_workspace_bytes(4, 8, 4096, 64, 64, 1, 0) >= 256
+    assert lib.la_prefill_workspace_bytes(0, 1, 256, 64, 64, 0, 0) == 0
+    assert lib.la_prefill_workspace_bytes(1, 1, 256, 129, 64, 0, 0) == 0
+    assert lib.la_prefill_workspace_bytes(1, 1, 256, 64, 64, 7, 0) == 0
+    assert lib.la_prefill_workspace_bytes(1, 1, 256, 64, 64, 1, 96) == 0
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+BASE = 1 << 40  # fake device addresses: never dereferenced, rejected first
+
+
+def _prefill(lib, **kw):
+    a = dict(q=BASE, k=BASE + (1 << 30), v=BASE + (2 << 30), dt=1, B=1, H=1, N=16,
+             dk=64, dv=64, eps=1e-6, S0=None, z0=None, o=BASE + (3 << 30),
+             SN=BASE + (4 << 30), zN=BASE + (5 << 30), chunk=0,
+             ws=BASE + (6 << 30), wsb=1 << 20)
+    a.update(kw)
+    p = lambda x: None if x is None else _fake(x)
+    return lib.la_prefill(p(a["q"]), p(a["k"]), p(a["v"]), a["dt"], a["B"], a["H"],
+                          a["N"], a["dk"], a["dv"], a["eps"], p(a["S0"]), p(a["z0"]),
+                          p(a["o"]), p(a["SN"]), p(a["zN"]), a["chunk"], p(a["ws"]),
+                          a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=0), dict(H=-1), dict(N=-1), dict(dk=0), dict(dv=129), dict(dk=200),
+    dict(eps=-1.0), dict(eps=float("nan")), dict(eps=float("inf")), dict(dt=2),
+    dict(q=None), dict(o=None), dict(SN=None), dict(zN=None), dict(ws=None),
+    dict(wsb=16), dict(chunk=64),
+    dict(q=BASE + 8), dict(o=BASE + (3 << 30) + 4), dict(ws=BASE + (6 << 30) + 2),
+    dict(o=BASE + 64),                       # o overlaps q
+    dict(SN=BASE + (3 << 30) + 1024),       # S_N overlaps o
+    dict(S0=BASE + (7 << 30), SN=BASE + (7 << 30) + 16),  # partial S0/S_N overlap
+    dict(zN=BASE + (4 << 30)),              # z_N overlaps S_N
+])
+def test_prefill_rejects_invalid_arguments(lib, kw):
+    assert _prefill(lib, **kw) == 1  # LA_ERR_INVALID_ARG
+
+
+def test_decode_and_delta_reject_invalid_arguments(lib):
+    p = _fake
+    # decode: null state, misaligned o, o overlapping S
+    assert lib.la_decode_step(p(BASE), p(BASE + 4096), p(BASE + 8192), 1, 1, 1, 64, 64,
+                              1e-6, None, p(BASE + (1 << 20)), p(BASE + (2 << 20)), None) == 1
+    assert lib.la_decode_step(p(BASE), p(BASE + 4096), p(BASE + 8192), 1, 1, 1, 64, 64,
+                              1e-6, p(BASE + (1 << 24)), p(BASE + (1 << 20)),
+                              p(BASE + (2 << 20) + 4), None) == 1
+    assert lib.la_decode_step(p(BASE), p(BASE + 4096), p(BASE + 8192), 1, 1, 1, 64, 64,
+                              1e-6, p(BASE + (1 << 24)), p(BASE + (1 << 20)),
+                              p(BASE + (1 << 24) + 256), None) == 1
+    assert lib.la_decode_step(p(BASE), p(BASE + 4096), p(BASE + 8192), 1, 1, 1, 0, 64,
+                              1e-6, p(BASE + (1 << 24)), p(BASE + (1 << 20)),
+                              p(BASE + (2 << 20)), None) == 1
+    # delta: bad dims, null beta, reads overlapping k
+    assert lib.delta_prefill(p(BASE), p(BASE + (1 << 24)), 1, p(BASE + (2 << 24)), 1, 1, 8,
+                             130, 64, None, p(BASE + (3 << 24)), p(BASE + (4 << 24)), None) == 1
+    assert lib.delta_prefill(p(BASE), p(BASE + (1 << 24)), 1, None, 1, 1, 8,
+                             64, 64, None, p(BASE + (3 << 24)), p(BASE + (4 << 24)), None) == 1
+    assert lib.delta_prefill(p(BASE), p(BASE + (1 << 24)), 1, p(BASE + (2 << 24)), 1, 1, 8,
+                             64, 64, None, p(BASE + 16), p(BASE + (4 << 24)), None) == 1
+    assert lib.la_read_device_status(None, None) == 1

@@ -1,0 +1,136 @@
+"""GPU parity of delta_prefill against the fp64 oracle, through the C ABI,
+including the pages' hand-worked delta-memory examples."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import golden
+from helpers import f64, relmax, tol_for, TOL_BF16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def la():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fixed_state_recurrent_gb300 import build, api
+    build.build()
+    api.load()
+    return api
+
+
+def _t(x, dtype=torch.float32):
+    return torch.tensor(np.asarray(x), dtype=dtype).cuda()
+
+
+def test_p3_memory_collision_on_gpu(la):
+    g = golden("p3_memory_collision.json")
+    k = _t(g["keys"])[None, None]
+    v = _t(g["values"])[None, None]
+    beta = torch.ones((1, 1, 4), device="cuda")
+    reads, S = la.delta_prefill(k, v, beta)
+    np.testing.assert_allclose(f64(reads)[0, 0], g["delta_reads_before_write"], atol=1e-6)
+    np.testing.assert_allclose(f64(S)[0, 0], np.array(g["delta_S_page_vkT"][3]).T, atol=1e-6)
+
+
+def test_two_entry_memory_on_gpu(la):
+    # S0 = W^T (k v^T layout), beta = 0: the reads are the page's (1,0.6), (0.6,1)
+    g = golden("two_entry_memory.json")
+    k = _t(g["keys"])[None, None]
+    v = torch.zeros((1, 1, 2, 2), device="cuda")
+    S0 = _t(np.array(g["W_vkT"]).T)[None, None].contiguous()
+    reads, S = la.delta_prefill(k, v, torch.zeros((1, 1, 2), device="cuda"), S0=S0)
+    np.testing.assert_allclose(f64(reads)[0, 0], [g["read_A"], g["read_B"]], atol=1e-6)
+    assert torch.equal(S, S0)
+
+
+def test_p1_delta_memory_on_gpu(la):
+    g = golden("p1_delta_memory.json")
+    key = np.array(g["key"])
+    vals = np.concatenate([np.array(g["values"]), np.zeros((1, 2))])
+    for beta, want in ((1.0, g["delta_beta1_read"]), (0.5, g["delta_beta_half_read"])):
+        k = _t(np.stack([key] * 3))[None, None]
+        reads, _ = la.delta_prefill(k, _t(vals)[None, None], torch.full((1, 1, 3), beta, device="cuda"))
+        np.testing.assert_allclose(f64(reads)[0, 0, 2], want, atol=1e-6)
+    for item in g["crosstalk"]:
+        rho = item["rho"]
+        k2 = np.array([rho, np.sqrt(1 - rho ** 2)])
+        k = _t(np.stack([key, k2, key]))[None, None]
+        reads, _ = la.delta_prefill(k, _t(vals)[None, None], torch.ones((1, 1, 3), device="cuda"))
+        np.testing.assert_allclose(f64(reads)[0, 0, 2], item["old_key_read"], atol=1e-6)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_exact_recall_basis_keys(la, dtype):
+    # basis keys are exact in bf16: beta = 1 writes, then re-reads return the
+    # stored values exactly (to fp32 rounding of v - read)
+    d, dv = 128, 128
+    keys = torch.eye(d, dtype=dtype)
+    g = torch.Generator().manual_seed(41)
+    vals = torch.randn((d, dv), generator=g).to(dtype)
+    k = torch.cat([keys, keys])[None, None].cuda()
+    v = torch.cat([vals, torch.zeros_like(vals)])[None, None].cuda()
+    beta = torch.cat([torch.ones(d), torch.zeros(d)])[None, None].cuda()
+    reads, S = la.delta_prefill(k, v, beta)
+    assert torch.equal(reads[0, 0, d:].cpu(), vals.float())
+    assert torch.equal(S[0, 0].cpu(), vals.float())
+    # over an arbitrary old memory the overwrite is exact up to the fp32
+    # rounding of old + (new - old)
+    S0 = (torch.randn((1, 1, d, dv), generator=g) * 5).cuda()
+    reads, S = la.delta_prefill(k, v, beta, S0=S0)
+    assert relmax(f64(reads[0, 0, d:]), f64(vals)) < 1e-6
+    assert relmax(f64(S[0, 0]), f64(vals)) < 1e-6
+
+
+SMALL = [(1, 1, 1, 1, 1), (2, 3, 37, 5, 3), (1, 2, 100, 64, 64), (2, 1, 300, 128, 128),
+         (1, 1, 77, 33, 128), (1, 2, 50, 128, 7), (1, 1, 65, 100, 100)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("shape", SMALL, ids=[str(s) for s in SMALL])
+@pytest.mark.parametrize("with_state", [False, True], ids=["zero", "state"])
+def test_delta_small(la, orc, dtype, shape, with_state):
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N, dk, dv = shape
+    k, v, beta = inputs.delta_inputs(B, H, N, dk, dv, dtype, seed=40 + N)
+    S0 = None
+    if with_state:
+        g = torch.Generator().manual_seed(42)
+        S0 = torch.randn((B, H, dk, dv), generator=g)
+    reads, S = la.delta_prefill(k.cuda(), v.cuda(), beta.cuda(),
+                                S0=None if S0 is None else S0.cuda())
+    rr, rS = orc.delta(f64(k), f64(v), f64(beta), S0=None if S0 is None else f64(S0))
+    tol = tol_for(dtype)
+    assert relmax(f64(reads), rr) <= tol
+    assert relmax(f64(S), rS) <= tol
+
+
+def test_delta_in_place_alias_and_zero_length(la, orc):
+    from fixed_state_recurrent_gb300 import inputs
+    k, v, beta = inputs.delta_inputs(1, 2, 60, 64, 64, torch.bfloat16, seed=43)
+    g = torch.Generator().manual_seed(44)
+    S0 = torch.randn((1, 2, 64, 64), generator=g)
+    Sd = S0.clone().cuda()
+    reads, S = la.delta_prefill(k.cuda(), v.cuda(), beta.cuda(), S0=Sd, S_N=Sd)
+    rr, rS = orc.delta(f64(k), f64(v), f64(beta), S0=f64(S0))
+    assert relmax(f64(Sd), rS) <= TOL_BF16 and relmax(f64(reads), rr) <= TOL_BF16
+    e = torch.empty((1, 2, 0, 64), dtype=torch.bfloat16, device="cuda")
+    reads, S = la.delta_prefill(e, e, torch.empty((1, 2, 0), device="cuda"), S0=S0.cuda())
+    assert torch.equal(S.cpu(), S0)
+
+
+def test_delta_config_sampled_heads(la, orc):
+    # B=8 H=16 N=8192 dk=dv=128: the GPU runs all heads; the oracle recomputes
+    # six of them in full.
+    from fixed_state_recurrent_gb300 import inputs
+    w = inputs.WORKLOADS["delta"]
+    k, v, beta = inputs.workload_inputs(w)
+    reads, S = la.delta_prefill(k.cuda(), v.cuda(), beta.cuda())
+    torch.cuda.synchronize()
+    reads, S = f64(reads), f64(S)
+    for (b, h) in [(0, 0), (3, 7), (7, 15), (5, 2), (1, 11), (6, 9)]:
+        rr, rS = orc.delta(f64(k[b:b + 1, h:h + 1]), f64(v[b:b + 1, h:h + 1]),
+                           f64(beta[b:b + 1, h:h + 1]))
+        assert relmax(reads[b:b + 1, h:h + 1], rr) <= TOL_BF16
+        assert relmax(S[b:b + 1, h:h + 1], rS) <= TOL_BF16
