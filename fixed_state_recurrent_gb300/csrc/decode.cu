@@ -18,7 +18,7 @@
 namespace la {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kMaxD = 128;
 
 template <int VEC>
@@ -32,7 +32,7 @@ struct DecodeShape {
 };
 
 template <int VEC, int MAXR>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 decode_step_kernel(const void* __restrict__ q, const void* __restrict__ k,
                    const void* __restrict__ v, bool bf16, int dk, int dv,
                    float eps, float* __restrict__ S, float* __restrict__ z,
@@ -132,8 +132,8 @@ cudaError_t launch_decode_step(const void* q, const void* k, const void* v,
                                cudaStream_t stream) {
   const unsigned blocks = (unsigned)((size_t)B * H);
   if (dv % 4 == 0) {
-    // rows per thread: dk / R with R = 256 / (dv / 4) >= 8, so <= 16
-    decode_step_kernel<4, 16><<<blocks, kThreads, 0, stream>>>(
+    // rows per thread: dk / R with R = 512 / (dv / 4) >= 16, so <= 8
+    decode_step_kernel<4, 8><<<blocks, kThreads, 0, stream>>>(
         q, k, v, bf16, dk, dv, eps, S, z, o);
   } else {
     decode_step_kernel<1, 1><<<blocks, kThreads, 0, stream>>>(
