@@ -216,3 +216,34 @@ def read_device_status(ws, stream=None) -> int:
     """Synchronize and return/clear the device status word of a workspace."""
     s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(ws.device)
     return int(load().la_read_device_status(_ptr(ws), s))
+
+
+def prefill_noalloc(q, k, v, eps=1e-6, S0=None, z0=None, *, o=None, S_N=None, z_N=None,
+                    chunk=0):
+    """la_prefill_noalloc: the same computation as prefill() for callers that
+    cannot allocate device memory; the library uses its own fixed 16 MiB
+    device scratch instead of a workspace (see include/la.h)."""
+    lib = load()
+    fn = lib.la_prefill_noalloc
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp, vp, vp, i, vp]
+    fn.restype = i
+    B, H, N, dk = q.shape
+    dv = v.shape[3]
+    dev = q.device
+    dt = q.dtype
+    code = _dtype_code(q)
+    _need(k, "k", (B, H, N, dk), dt, dev)
+    _need(v, "v", (B, H, N, dv), dt, dev)
+    _need(S0, "S0", (B, H, dk, dv), torch.float32, dev)
+    _need(z0, "z0", (B, H, dk), torch.float32, dev)
+    if o is None:
+        o = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
+    if S_N is None:
+        S_N = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    if z_N is None:
+        z_N = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
+    st = fn(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, dk, dv, float(eps), _ptr(S0),
+            _ptr(z0), _ptr(o), _ptr(S_N), _ptr(z_N), int(chunk), _stream(dev))
+    _check("la_prefill_noalloc", st)
+    return o, S_N, z_N

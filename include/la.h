@@ -63,8 +63,9 @@ typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
 /*
  * la_prefill -- causal prefill of N tokens per (batch, head).
  * Computes o_t for t = 1..N from the recurrence above, starting from S0, z0
- * (NULL = zero state, P1 section 05: state is reset per request), and writes
- * the final state S_N, z_N (P1 appendix: recurrent_linear returns out, S, z).
+ * (NULL = zero state: the LinearMem page, section 05, resets the state per
+ * request), and writes the final state S_N, z_N (the same page's appendix
+ * script returns the outputs together with S and z).
  *   q, k, v     inputs, in_dtype (LA_F32 or LA_BF16)
  *   S0, z0      initial state or NULL; S_N may alias S0, z_N may alias z0
  *   o, S_N, z_N outputs, float32
@@ -90,7 +91,8 @@ size_t la_prefill_workspace_bytes(int B, int H, int N, int dk, int dv,
 /*
  * la_decode_step -- one token per (batch, head) on a resident state, in place:
  *   S += phi(k) v^T;  z += phi(k);  o = phi(q)^T S / (phi(q)^T z + eps)
- * (update, then read: P1 section 03).  S and z are read once and written once.
+ * (update, then read: LinearMem page, section 03).  S and z are read once
+ * and written once.
  *   q, k [B][H][dk], v [B][H][dv] in in_dtype;  o [B][H][dv] float32.
  */
 la_status la_decode_step(const void* q, const void* k, const void* v, la_dtype in_dtype,
@@ -112,7 +114,7 @@ la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const f
                         cudaStream_t stream);
 
 /* Bytes of one head's recurrent state, (dk*dv + dk) * 4: 16640 at 64 x 64
- * (P1 section 01).  0 for dk or dv < 1. */
+ * (LinearMem page, section 01).  0 for dk or dv < 1. */
 size_t la_state_bytes(int dk, int dv);
 
 /* Static, human-readable name of a status code. */
@@ -123,6 +125,35 @@ const char* la_status_string(la_status s);
  * last read, otherwise LA_OK).  LA_ERR_INVALID_ARG for a NULL workspace,
  * LA_ERR_CUDA if the synchronization or copy fails. */
 la_status la_read_device_status(const void* workspace, cudaStream_t stream);
+
+/*
+ * la_prefill_noalloc -- la_prefill without a caller-provided workspace.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory -- code that runs while a CUDA graph is being
+ * captured, plugins whose host framework only hands out input and output
+ * buffers, or processes whose device memory belongs to another allocator.
+ * It computes exactly what la_prefill computes, with the same arguments
+ * minus the workspace, and allocates nothing: its scratch is one fixed 16 MiB
+ * array inside this library's device image, which every GPU that loads the
+ * library holds until the process exits.
+ *   Limit: requests whose la_prefill_workspace_bytes(...) exceeds 16 MiB
+ *   (16777216 bytes) are rejected with LA_ERR_INVALID_ARG, as are arguments
+ *   la_prefill rejects.  At dk = dv = 64 that is 504 items of 512 tokens
+ *   (B*H*ceil(N/512) <= 504); at dk = dv = 128, 127 items.
+ *   Set-up: the first call on each device (with that device current) looks up
+ *   the array's device address and zero-fills it synchronously; make that
+ *   first call before any stream capture.
+ *   Sharing: every call on a device uses the same array and the kernels leave
+ *   it ready for the next call; calls whose executions overlap on the GPU
+ *   (different streams, no ordering) race on it and must not be issued.
+ *   Status: bounded-wait timeouts are recorded in that shared array and cannot
+ *   be read back through la_read_device_status.
+ */
+la_status la_prefill_noalloc(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                             int B, int H, int N, int dk, int dv, float eps,
+                             const float* S0, const float* z0,
+                             float* o, float* S_N, float* z_N,
+                             int chunk, cudaStream_t stream);
 
 #ifdef __cplusplus
 }
