@@ -36,23 +36,19 @@
 // Roles: warp 0 lane 0 issues TMA loads and MMAs; warps 1..8 (two per TMEM
 // lane quadrant) apply phi, build the masked P tile, run the normalisation
 // epilogue (TMA stores of o), the state snapshots and the look-back.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <cstdlib>
-
-#include "la_internal.h"
-#include "tc_primitives.cuh"
+#include "prefill_tc_common.cuh"
 
 namespace la {
+
+cudaError_t launch_prefill_tc64(const PrefillArgs& a, cudaStream_t stream);  // prefill_tc64.cu
+
 namespace {
 
 using namespace tc;
+using namespace tcp;
 
-constexpr int C = 128;                 // chunk length = MMA M = tile rows
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (1 + kEpiWarps);
-constexpr int kItemTokens = 512;       // tokens per work item (multiple of C)
 constexpr uint32_t kTmemCols = 512;
 
 template <int D>
@@ -89,46 +85,6 @@ struct Cfg {
   static constexpr uint32_t ID_SU = idesc_bf16_f32(128, D, 1, 1);
   static constexpr uint32_t ID_ZU = idesc_bf16_f32(128, 16, 1, 0);
 };
-
-struct TcParams {
-  int BH, N, items_per_head, total_items;
-  float eps;
-  const float* S0;
-  const float* z0;
-  float* S_N;
-  float* z_N;
-  WsHeader* hdr;
-  unsigned* flags;   // total_items + 1 (the last is never written)
-  float* agg;
-  float* inc;
-  unsigned long long wait_ns;
-  int force_wait;
-};
-
-struct Item {
-  int h, w, tok0, tok1, nch;
-};
-
-__device__ __forceinline__ Item item_of(const TcParams& p, int g) {
-  Item it;
-  it.h = g % p.BH;
-  it.w = g / p.BH;
-  it.tok0 = it.w * kItemTokens;
-  it.tok1 = min(it.tok0 + kItemTokens, p.N);
-  it.nch = (it.tok1 - it.tok0 + C - 1) / C;
-  return it;
-}
-
-// phi(u) = exp(min(u,0)) + max(u,0): u + 1 for u > 0, exp(u) for u <= 0.
-__device__ __forceinline__ float phi_fast(float u) {
-  return __expf(fminf(u, 0.f)) + fmaxf(u, 0.f);
-}
-
-__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
-  const float lo = __uint_as_float(x << 16);
-  const float hi = __uint_as_float(x & 0xFFFF0000u);
-  return pack_bf16x2(phi_fast(lo), phi_fast(hi));
-}
 
 struct Sync {
   uint64_t* ld;
@@ -412,41 +368,7 @@ __device__ void epi_loop(const TcParams& p, const CUtensorMap* tm_o, uint8_t* sm
     if (et == 0) st_release_gpu(&p.flags[g], (epoch << 2) | 1u);
 
     // ---- look-back: nearest earlier item of this head with an inclusive prefix
-    if (et == 0) {
-      int start = -1;
-      bool timed_out = false;
-      const uint64_t deadline = globaltimer_ns() + p.wait_ns;
-      if (p.force_wait && it.w == 0) {  // test hook: a flag that nothing sets
-        while (!timed_out) {
-          const unsigned v = ld_acquire_gpu(&p.flags[p.total_items]);
-          if ((v >> 2) == epoch && (v & 3u)) break;
-          if (globaltimer_ns() > deadline) timed_out = true;
-          __nanosleep(256);
-        }
-      }
-      for (int ww = it.w - 1; ww >= 0 && !timed_out; --ww) {
-        const unsigned* f = &p.flags[ww * p.BH + it.h];
-        while (true) {
-          const unsigned v = ld_acquire_gpu(f);
-          if ((v >> 2) == epoch && (v & 3u) == 2u) {  // inclusive prefix published
-            start = ww;
-            break;
-          }
-          if ((v >> 2) == epoch && (v & 3u) == 1u && ww > 0) break;  // aggregate: keep walking
-          if (globaltimer_ns() > deadline) {
-            timed_out = true;
-            break;
-          }
-          __nanosleep(64);
-        }
-        if (start >= 0) break;
-      }
-      if (timed_out) {
-        atomicOr(&p.hdr->status, kStatusTimeout);
-        if (start < 0 && it.w > 0) start = it.w - 1;  // finish with unspecified values
-      }
-      *lb_start = start;
-    }
+    if (et == 0) *lb_start = lookback_start(p, it, epoch);
     named_bar_sync(1, 32 * kEpiWarps);
     const int start = *reinterpret_cast<volatile int*>(lb_start);
 
@@ -704,41 +626,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // ---------------------------------------------------------------------------
 // host side
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 3-D map over a [BH][N][d] tensor, innermost dimension first, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int d, int N,
-              int BH, int box0, int box1) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * esize, (cuuint64_t)N * d * esize};
-  cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int items_per_head(int N) { return (N + kItemTokens - 1) / kItemTokens; }
-
-unsigned long long env_ull(const char* name, unsigned long long dflt) {
-  const char* s = getenv(name);
-  if (!s || !*s) return dflt;
-  return strtoull(s, nullptr, 10);
-}
-
 template <int D>
 cudaError_t launch_d(const PrefillArgs& a, cudaStream_t stream) {
   using Cf = Cfg<D>;
@@ -763,24 +650,7 @@ cudaError_t launch_d(const PrefillArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
 
-  TcParams p;
-  p.BH = BH;
-  p.N = a.N;
-  p.items_per_head = items_per_head(a.N);
-  p.total_items = BH * p.items_per_head;
-  p.eps = a.eps;
-  p.S0 = a.S0;
-  p.z0 = a.z0;
-  p.S_N = a.S_N;
-  p.z_N = a.z_N;
-  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  p.hdr = reinterpret_cast<WsHeader*>(ws);
-  const size_t flag_bytes = ((size_t)(p.total_items + 1) * 4 + 255) & ~(size_t)255;
-  p.flags = reinterpret_cast<unsigned*>(ws + sizeof(WsHeader));
-  p.agg = reinterpret_cast<float*>(ws + sizeof(WsHeader) + flag_bytes);
-  p.inc = p.agg + (size_t)p.total_items * Cf::SZ;
-  p.wait_ns = env_ull("LA_WAIT_TIMEOUT_NS", 1000000000ull);
-  p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+  TcParams p = make_params(a, D);
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
 
   const int grid = p.total_items < sms ? p.total_items : sms;
@@ -805,14 +675,11 @@ bool prefill_tc_supported(const PrefillArgs& a) {
 }
 
 size_t prefill_tc_workspace_bytes(int B, int H, int N, int d, int /*chunk*/) {
-  const size_t T = (size_t)B * H * items_per_head(N);
-  const size_t flag_bytes = ((T + 1) * 4 + 255) & ~(size_t)255;
-  const size_t sz = (size_t)d * d + d;
-  return flag_bytes + 2 * T * sz * sizeof(float);
+  return workspace_bytes(B, H, N, d);
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
-  if (a.dk == 64) return launch_d<64>(a, stream);
+  if (a.dk == 64) return launch_prefill_tc64(a, stream);
   return launch_d<128>(a, stream);
 }
 
