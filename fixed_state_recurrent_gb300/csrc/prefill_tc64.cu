@@ -9,34 +9,39 @@
 //
 // Work items are 512-token windows of one head (window-major, one persistent
 // block per SM, cooperative launch), each processed in two phases:
-//   A. for every chunk c of the item: dS_c = phi(K_c)^T V_c, dz_c = phi(K_c)^T 1
-//      (tensor cores, fresh accumulator per chunk).  The epilogue warps add the
-//      dS_c up in fp32 registers and, after chunk c, snapshot the running sum
-//      R_{c+1} = dS_0 + ... + dS_c to bf16 (R_0 = 0): the state each chunk of
-//      the item starts from, relative to the item start.  The total R is the
-//      item's aggregate, published for the look-back.
+//   A. for every chunk c of the item the tensor cores accumulate the
+//      transposed state in one M = 128 product per 16 tokens,
+//      R += [V_c | 1]^T phi(K_c), into a TMEM accumulator: lanes 0..63 hold
+//      R^T (lane j = column j of R = sum phi(K)^T V), lane 64 holds the z part
+//      (sum phi(K)^T 1).  After chunk c the epilogue warps snapshot the running
+//      R_{c+1} to bf16 (R_0 = 0): the state each chunk of the item starts from,
+//      relative to the item start.  The final R is the item's aggregate,
+//      published for the look-back (workspace states are stored transposed,
+//      one contiguous row per thread).
 //   L. decoupled look-back (bounded waits) for the item's exclusive prefix E
 //      (S0 and all earlier items of the head, always the same left fold so that
 //      results are bit-identical from run to run); E is snapshotted to bf16.
 //   B. for every chunk: scores A = phi(Q_c) phi(K_c)^T (tensor cores); the P
 //      warps mask them causally (key <= query, diagonal kept), round to bf16
 //      and write P back into the same TMEM columns; then
-//        num = P V_c + phi(Q_c) E + phi(Q_c) R_c
-//        den = P 1  + phi(Q_c) z_E + phi(Q_c) z_R_c        (z split hi + lo)
-//      as tensor-core products with P read from TMEM, and o = num / (den + eps)
-//      is stored through TMA.
+//        [num | den] = P [V_c | 1] + phi(Q_c) [E | z_E] + phi(Q_c) [R_c | z_R_c]
+//      as three N = 80 tensor-core products (P read from TMEM; the state
+//      snapshots are K-major B operands whose rows 0..63 are S^T and rows
+//      64, 65 the bf16 hi / lo split of z), and o = num / (den + eps) is stored
+//      through TMA.  Every denominator term rides in the numerator's products.
 // Phase B has no serial dependence between chunks, and the look-back of an
 // item overlaps with the scores and P of its first chunks.
 //
-// Warp roles (448 threads):
+// Warp roles (576 threads):
 //   warp 0      TMA producer (3-stage ring of Q | K | V tiles, 48 KB each)
 //   warp 1      TMEM owner; lane 0 issues every tcgen05.mma
-//   warps 2-5   apply phi in shared memory (K in phase A, Q and K in phase B)
-//   warps 6-9   build P from the scores (one warp per TMEM lane quadrant)
-//   warps 10-13 state epilogue (phase A), look-back, output epilogue (phase B)
+//   warps 2-9   apply phi in shared memory (K in phase A, Q and K in phase B);
+//               two threads per tile row, all loads issued before any math
+//   warps 10-13 build P from the scores (one warp per TMEM lane quadrant)
+//   warps 14-17 state epilogue (phase A), look-back, output epilogue (phase B)
 // TMEM (512 columns): A[b] = cols 128b..128b+127 (scores, then P packed in
-// place; dS_c | dz_c in phase A), b = 0, 1; O[ob] = cols 256 + 80 ob: 64
-// numerator columns, then 16 denominator columns.
+// place), b = 0, 1; O[ob] = cols 256 + 80 ob: 64 numerator columns, then the
+// denominator in columns 64 (+ 65); R = cols 416..479 (phase-A running state).
 #include "prefill_tc_common.cuh"
 
 namespace la {
@@ -47,38 +52,38 @@ using namespace tcp;
 
 constexpr int D = 64;
 constexpr int NS = 3;                       // stages in the TMA ring
-constexpr int kWarps = 14;
+constexpr int kWarps = 18;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxChunks = kItemTokens / C;  // 4
 constexpr uint32_t BLK = 16384;             // [128 rows x 128 B] swizzled tile
 constexpr uint32_t STAGE = 3 * BLK;         // Q | K | V
-constexpr uint32_t SNAP = 8192;             // [64 dk rows x 64 dv] bf16, MN-major B operand
+constexpr uint32_t SNAP = 80 * 128;        // K-major [80 rows x 64 dk] bf16: S^T, z hi, z lo, 0
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_ESNAP = NS * STAGE;                       // bf16(E)
-constexpr uint32_t OFF_RSNAP = OFF_ESNAP + SNAP;                 // bf16(R_c), c = 1..3
-constexpr uint32_t OFF_BZ = OFF_RSNAP + (kMaxChunks - 1) * SNAP; // z hi/lo: E, R_1..R_3
-constexpr uint32_t OFF_B1 = OFF_BZ + kMaxChunks * 2048;          // ones in row 0 (2 blocks)
-constexpr uint32_t OFF_BAR = OFF_B1 + 4096;
+constexpr uint32_t OFF_ONES = NS * STAGE;                        // [128 x 64] MN-major, column 0 = 1
+constexpr uint32_t OFF_ESNAP = OFF_ONES + BLK;                   // snapshot of E
+constexpr uint32_t OFF_RSNAP = OFF_ESNAP + SNAP;                 // snapshots of R_c, c = 1..3
+constexpr uint32_t OFF_BAR = OFF_RSNAP + (kMaxChunks - 1) * SNAP;
 constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;                  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TA = 0;
 constexpr uint32_t TO = 256;
+constexpr uint32_t TR = 416;
 constexpr int SZ = D * D + D;
 
-constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);  // phi(Q) phi(K)^T
-constexpr uint32_t ID_PV = idesc_bf16_f32(128, D, 0, 1);   // x [*, dv] MN-major B
-constexpr uint32_t ID_N16 = idesc_bf16_f32(128, 16, 0, 0); // x [16, *] K-major B
-constexpr uint32_t ID_SU = idesc_bf16_f32(128, D, 1, 1);   // phi(K)^T V
-constexpr uint32_t ID_ZU = idesc_bf16_f32(128, 16, 1, 0);  // phi(K)^T 1
+constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);   // phi(Q) phi(K)^T
+constexpr uint32_t ID_PV = idesc_bf16_f32(128, D + 16, 0, 1); // P [V | 1]
+constexpr uint32_t ID_QS = idesc_bf16_f32(128, D + 16, 0, 0); // phi(Q) [S | z]
+constexpr uint32_t ID_DS = idesc_bf16_f32(128, D, 1, 1);    // [V | 1]^T phi(K)
 
 struct Bars {
   uint64_t full[NS];    // TMA bytes landed              (producer -> phi warps)
-  uint64_t xf[NS];      // phi applied                   (phi warps -> MMA)
+  uint64_t xf[NS];      // phi applied (8 warps)         (phi warps -> MMA)
   uint64_t empty[NS];   // stage free                    (MMA / epilogue -> producer)
-  uint64_t accA[2];     // dS_c ready in A[b]            (MMA -> state epilogue)
+  uint64_t accA;        // R updated by a chunk          (MMA -> state epilogue)
+  uint64_t rfree;       // R read: the MMA may update it (state epilogue -> MMA)
   uint64_t accB[2];     // scores ready in A[b]          (MMA -> P warps)
   uint64_t pready[2];   // P written into A[b]           (P warps -> MMA)
-  uint64_t freeb[2];    // A[b] may be overwritten       (epilogue / MMA -> MMA)
+  uint64_t freeb[2];    // A[b] may be overwritten       (MMA -> MMA)
   uint64_t oready[2];   // num, den ready in O[ob]       (MMA -> epilogue)
   uint64_t ofree[2];    // O[ob] read                    (epilogue -> MMA)
   uint64_t eready;      // E and R_c snapshots written   (epilogue -> MMA)
@@ -144,24 +149,53 @@ __device__ void producer(const Ctx& x, const CUtensorMap* tq, const CUtensorMap*
 // ---------------------------------------------------------------------------
 // warps 2-5: phi in place on the swizzled tiles
 
-__device__ __forceinline__ void phi_tile(uint8_t* tile, int r, int valid) {
-#pragma unroll
-  for (int cc = 0; cc < 8; ++cc) {
-    uint4* ptr = reinterpret_cast<uint4*>(tile + sw128_offset(r, cc));
-    uint4 v = *ptr;
-    if (r < valid) {
-      v.x = phi_bf16x2(v.x);
-      v.y = phi_bf16x2(v.y);
-      v.z = phi_bf16x2(v.z);
-      v.w = phi_bf16x2(v.w);
-    } else {
-      v = make_uint4(0, 0, 0, 0);
-    }
-    *ptr = v;
-  }
+// phi on two bf16: exp(min(u,0)) + max(u,0) with the min, max and the final
+// add done on the pair (bf16 arithmetic rounds once, so the result equals
+// rounding u + 1, resp. exp(u), to bf16) and the exponentials in fp32.
+__device__ __forceinline__ uint32_t phi_bf16x2_packed(uint32_t x) {
+  const __nv_bfloat162 u = *reinterpret_cast<const __nv_bfloat162*>(&x);
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const __nv_bfloat162 m = __hmin2(u, zero);
+  const __nv_bfloat162 M = __hmax2(u, zero);
+  const uint32_t mb = *reinterpret_cast<const uint32_t*>(&m);
+  const uint32_t e = pack_bf16x2(__expf(__uint_as_float(mb << 16)),
+                                 __expf(__uint_as_float(mb & 0xFFFF0000u)));
+  const __nv_bfloat162 r = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&e), M);
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-__device__ void transformer(const Ctx& x, int r, int lane) {
+// phi on chunks [4 part, 4 part + 4) of row r of one tile, or of both the Q
+// and K tiles; all shared-memory loads are issued before any arithmetic.
+template <int NT>
+__device__ __forceinline__ void phi_rows(uint8_t* const (&tiles)[NT], int r, int part,
+                                         int valid) {
+  uint4 v[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      v[t][i] = *reinterpret_cast<const uint4*>(tiles[t] + sw128_offset(r, 4 * part + i));
+  const bool keep = r < valid;
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 u = v[t][i];
+      u.x = keep ? phi_bf16x2_packed(u.x) : 0u;
+      u.y = keep ? phi_bf16x2_packed(u.y) : 0u;
+      u.z = keep ? phi_bf16x2_packed(u.z) : 0u;
+      u.w = keep ? phi_bf16x2_packed(u.w) : 0u;
+      v[t][i] = u;
+    }
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<uint4*>(tiles[t] + sw128_offset(r, 4 * part + i)) = v[t][i];
+}
+
+__device__ void transformer(const Ctx& x, int et, int lane) {
+  const int r = et % C, part = et / C;  // 256 threads: row r, half `part` of it
   const TcParams& p = *x.p;
   uint32_t sj = 0;
   for (int g = blockIdx.x; g < p.total_items; g += gridDim.x) {
@@ -172,8 +206,13 @@ __device__ void transformer(const Ctx& x, int r, int lane) {
         wait_bar(x, &x.bars->full[s], (sj / NS) & 1);
         uint8_t* st = stage_ptr(x, s);
         const int valid = it.tok1 - (it.tok0 + c * C);
-        if (phase == 1) phi_tile(st, r, valid);
-        phi_tile(st + BLK, r, valid);
+        if (phase == 1) {
+          uint8_t* const t2[2] = {st, st + BLK};
+          phi_rows<2>(t2, r, part, valid);
+        } else {
+          uint8_t* const t1[1] = {st + BLK};
+          phi_rows<1>(t1, r, part, valid);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&x.bars->xf[s]);
@@ -189,12 +228,12 @@ __device__ void mma_issuer(const Ctx& x) {
   const TcParams& p = *x.p;
   Bars* B = x.bars;
   const uint32_t tm = x.tmem;
-  const uint32_t aB1 = smem_u32(x.smem + OFF_B1);
+  const uint32_t aOnes = smem_u32(x.smem + OFF_ONES);
   const uint32_t aE = smem_u32(x.smem + OFF_ESNAP);
   const uint32_t aR = smem_u32(x.smem + OFF_RSNAP);
-  const uint32_t aBz = smem_u32(x.smem + OFF_BZ);
   uint32_t sj = 0, aj = 0, oj = 0, itn = 0;
   uint32_t npr[2] = {0, 0};  // uses of pready[b]
+  uint32_t nrf = 0;          // R updates issued (each but the very first waits for rfree)
 
   // wait for the stage of job `j` to be transformed and for A[b] of job `a` to be free
   auto acquire = [&](uint32_t j, uint32_t a) {
@@ -213,22 +252,23 @@ __device__ void mma_issuer(const Ctx& x) {
 
   for (int g = blockIdx.x; g < p.total_items; g += gridDim.x) {
     const Item it = item_of(p, g);
-    // ---- phase A: dS_c, dz_c per chunk, each into a fresh accumulator
-    for (int c = 0; c < it.nch; ++c, ++sj, ++aj) {
-      acquire(sj, aj);
+    // ---- phase A: R (+)= [V_c | 1]^T phi(K_c), chunk by chunk
+    for (int c = 0; c < it.nch; ++c, ++sj) {
+      wait_bar(x, &B->xf[sj % NS], (sj / NS) & 1);
+      if (nrf > 0) wait_bar(x, &B->rfree, (nrf - 1) & 1);  // previous R read / item done
+      ++nrf;
+      tc_fence_after();
       const uint32_t st = smem_u32(stage_ptr(x, sj % NS));
-      const uint32_t d = tm + TA + 128 * (aj % 2);
+      const uint32_t vt = st + 2 * BLK;
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks) {
-        // A = phi(K)^T, MN-major; its second 64-row block (rows 64..127 of the
-        // M = 128 product) reads the V tile and is ignored.
-        const uint64_t a = sdesc_sw128(st + BLK + ks * 2048, BLK, 1024);
-        mma_bf16_ss(d, a, sdesc_sw128(st + 2 * BLK + ks * 2048, BLK, 1024), ID_SU,
-                    ks > 0 ? 1u : 0u);
-        mma_bf16_ss(d + D, a, sdesc_sw128(aB1 + (ks / 4) * 2048 + (ks % 4) * 32, 16, 1024),
-                    ID_ZU, ks > 0 ? 1u : 0u);
+        // A = [V | 1]^T, MN-major: M rows 0..63 from the V tile, rows 64..127
+        // from the ones tile (row 64 all ones); B = phi(K), MN-major (N = dk).
+        const uint64_t a = sdesc_sw128(vt + ks * 2048, aOnes - vt, 1024);
+        const uint64_t b = sdesc_sw128(st + BLK + ks * 2048, BLK, 1024);
+        mma_bf16_ss(tm + TR, a, b, ID_DS, (c > 0 || ks > 0) ? 1u : 0u);
       }
-      mma_commit(&B->accA[aj % 2]);
+      mma_commit(&B->accA);
       mma_commit(&B->empty[sj % NS]);
     }
     // ---- phase B
@@ -249,24 +289,19 @@ __device__ void mma_issuer(const Ctx& x) {
       if (oj >= 2) wait_bar(x, &B->ofree[ob], ((oj / 2) - 1) & 1);
       tc_fence_after();
       const uint32_t st = smem_u32(stage_ptr(x, j % NS));
-      const uint32_t dO = tm + TO + 80 * ob, dD = dO + D;
+      const uint32_t dO = tm + TO + 80 * ob;
       const uint32_t aP = tm + TA + 128 * b;
+      const uint32_t vt = st + 2 * BLK;
 #pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) {  // P V and P 1, P from TMEM (8 columns per 16 keys)
-        mma_bf16_ts(dO, aP + 8 * ks, sdesc_sw128(st + 2 * BLK + ks * 2048, BLK, 1024), ID_PV,
+      for (int ks = 0; ks < C / 16; ++ks)  // P [V | 1], P from TMEM (8 columns per 16 keys)
+        mma_bf16_ts(dO, aP + 8 * ks, sdesc_sw128(vt + ks * 2048, aOnes - vt, 1024), ID_PV,
                     ks > 0 ? 1u : 0u);
-        mma_bf16_ts(dD, aP + 8 * ks, sdesc_sw128(aB1 + (ks / 4) * 2048 + (ks % 4) * 32, 16, 1024),
-                    ID_N16, ks > 0 ? 1u : 0u);
-      }
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {  // phi(Q) (E + R_c), phi(Q) (z_E + z_R_c)
+      for (int ks = 0; ks < D / 16; ++ks) {  // phi(Q) [E | z_E] + phi(Q) [R_c | z_R_c]
         const uint64_t aq = sdesc_sw128(st + ks * 32, 16, 1024);
-        mma_bf16_ss(dO, aq, sdesc_sw128(aE + ks * 2048, SNAP, 1024), ID_PV, 1u);
-        mma_bf16_ss(dD, aq, sdesc_sw128(aBz + ks * 32, 16, 1024), ID_N16, 1u);
-        if (c > 0) {
-          mma_bf16_ss(dO, aq, sdesc_sw128(aR + (c - 1) * SNAP + ks * 2048, SNAP, 1024), ID_PV, 1u);
-          mma_bf16_ss(dD, aq, sdesc_sw128(aBz + c * 2048 + ks * 32, 16, 1024), ID_N16, 1u);
-        }
+        mma_bf16_ss(dO, aq, sdesc_sw128(aE + ks * 32, 16, 1024), ID_QS, 1u);
+        if (c > 0)
+          mma_bf16_ss(dO, aq, sdesc_sw128(aR + (c - 1) * SNAP + ks * 32, 16, 1024), ID_QS, 1u);
       }
       mma_commit(&B->oready[ob]);
       mma_commit(&B->freeb[b]);
@@ -295,27 +330,40 @@ __device__ void p_builder(const Ctx& x, int quad, int lane) {
   uint32_t nb[2] = {0, 0};  // uses of accB[b]
   for (int g = blockIdx.x; g < p.total_items; g += gridDim.x) {
     const Item it = item_of(p, g);
-    aj += it.nch;  // phase-A jobs use the A buffers without the P warps
     for (int c = 0; c < it.nch; ++c, ++aj) {
       const int b = aj % 2;
       wait_bar(x, &x.bars->accB[b], nb[b] & 1);
       ++nb[b];
       tc_fence_after();
       const uint32_t base = tl + TA + 128 * b;
+      // Keys in blocks of 32: this warp's rows are 32 quad .. 32 quad + 31, so
+      // blocks before `quad` are fully visible, block `quad` holds the
+      // diagonal, later blocks are fully masked (written as zeros, not read).
+      // Packed keys 32 q4 .. +31 go to columns 16 q4 .. +15; in increasing q4
+      // order those columns have always been read already.
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {  // keys 32 q4 .. 32 q4 + 31
-        uint32_t r[32];
-        tmem_ld32(base + 32 * q4, r);
-        tmem_ld_wait();
+      for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t w[16];
+        if (q4 > quad) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j0 = 32 * q4 + 2 * i;
-          const float lo = (j0 <= row) ? __uint_as_float(r[2 * i]) : 0.f;
-          const float hi = (j0 + 1 <= row) ? __uint_as_float(r[2 * i + 1]) : 0.f;
-          w[i] = pack_bf16x2(lo, hi);
+          for (int i = 0; i < 16; ++i) w[i] = 0u;
+        } else {
+          uint32_t r[32];
+          tmem_ld32(base + 32 * q4, r);
+          tmem_ld_wait();
+          if (q4 < quad) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j0 = 2 * i;  // key index within the block; the row's is `lane`
+              w[i] = pack_bf16x2(j0 <= lane ? __uint_as_float(r[2 * i]) : 0.f,
+                                 j0 + 1 <= lane ? __uint_as_float(r[2 * i + 1]) : 0.f);
+            }
+          }
         }
-        // packed keys 32 q4 .. +31 go to columns 16 q4 .. +15, already read
         tmem_st16(base + 16 * q4, w);
       }
       tmem_st_wait();
@@ -329,7 +377,8 @@ __device__ void p_builder(const Ctx& x, int quad, int lane) {
 // ---------------------------------------------------------------------------
 // warps 10-13: state epilogue, look-back, output epilogue
 
-__device__ __forceinline__ void store_snap_row(uint8_t* snap, int row, const float* v /*64*/) {
+// Row `n` of a K-major snapshot from 64 fp32 values (eight values per 16-byte chunk).
+__device__ __forceinline__ void store_snap_row(uint8_t* snap, int n, const float* v /*64*/) {
 #pragma unroll
   for (int cc = 0; cc < 8; ++cc) {
     uint4 u;
@@ -337,144 +386,213 @@ __device__ __forceinline__ void store_snap_row(uint8_t* snap, int row, const flo
     u.y = pack_bf16x2(v[8 * cc + 2], v[8 * cc + 3]);
     u.z = pack_bf16x2(v[8 * cc + 4], v[8 * cc + 5]);
     u.w = pack_bf16x2(v[8 * cc + 6], v[8 * cc + 7]);
-    *reinterpret_cast<uint4*>(snap + sw128_offset(row, cc)) = u;
+    *reinterpret_cast<uint4*>(snap + sw128_offset(n, cc)) = u;
   }
 }
 
-// Bz operand (K-major [16 rows][dk]): row 0 = bf16(z), row 1 = bf16(z - row 0).
-__device__ __forceinline__ void store_bz(uint8_t* bz, int i, float z) {
-  const __nv_bfloat16 hi = __float2bfloat16_rn(z);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(z - __bfloat162float(hi));
-  const int c8 = i / 8, e = i % 8;
-  *reinterpret_cast<__nv_bfloat16*>(bz + sw128_offset(0, c8) + 2 * e) = hi;
-  *reinterpret_cast<__nv_bfloat16*>(bz + sw128_offset(1, c8) + 2 * e) = lo;
+// Rows 64 (hi) and 65 (lo) of a snapshot from the 64 fp32 values of z:
+// hi = bf16(z), lo = bf16(z - hi), so hi + lo carries about 16 bits of z.
+__device__ __forceinline__ void store_snap_z(uint8_t* snap, const float* z /*64*/) {
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    float hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      hi[i] = __bfloat162float(__float2bfloat16_rn(z[8 * cc + i]));
+      lo[i] = z[8 * cc + i] - hi[i];
+    }
+    uint4 h, l;
+    h.x = pack_bf16x2(hi[0], hi[1]); h.y = pack_bf16x2(hi[2], hi[3]);
+    h.z = pack_bf16x2(hi[4], hi[5]); h.w = pack_bf16x2(hi[6], hi[7]);
+    l.x = pack_bf16x2(lo[0], lo[1]); l.y = pack_bf16x2(lo[2], lo[3]);
+    l.z = pack_bf16x2(lo[4], lo[5]); l.w = pack_bf16x2(lo[6], lo[7]);
+    *reinterpret_cast<uint4*>(snap + sw128_offset(64, cc)) = h;
+    *reinterpret_cast<uint4*>(snap + sw128_offset(65, cc)) = l;
+  }
+}
+
+// The state threads are TMEM lanes 0..64 of the running state R: lane j < 64
+// holds row j of R^T (column j of S), lane 64 holds z.  Workspace states use
+// that transposed layout -- thread `row` owns floats [64 row, 64 row + 64) of
+// a slot, z last -- so every thread moves one contiguous 256-byte row.  S0 and
+// S_N keep the API layout [dk][dv]: there lane j < 64 touches S[i][j], i.e.
+// element i * 64 + j (coalesced across the warp), and lane 64 touches z[i].
+__device__ __forceinline__ const float* api_elem(const float* S, const float* z, int row, int i) {
+  return row < D ? S + i * D + row : z + i;
+}
+__device__ __forceinline__ float* api_elem(float* S, float* z, int row, int i) {
+  return row < D ? S + i * D + row : z + i;
+}
+
+// 32 fp32 columns [32 half, 32 half + 32) of this lane's row of R from TMEM.
+__device__ __forceinline__ void load_r_half(uint32_t tl, int half, float* out /*32*/) {
+  uint32_t r[32];
+  tmem_ld32(tl + TR + 32 * half, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(r[i]);
+}
+
+// 32 values of a row into chunks [4 half, 4 half + 4) of snapshot row n.
+__device__ __forceinline__ void store_snap_half(uint8_t* snap, int n, int half, const float* v) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * cc + 0], v[8 * cc + 1]);
+    u.y = pack_bf16x2(v[8 * cc + 2], v[8 * cc + 3]);
+    u.z = pack_bf16x2(v[8 * cc + 4], v[8 * cc + 5]);
+    u.w = pack_bf16x2(v[8 * cc + 6], v[8 * cc + 7]);
+    *reinterpret_cast<uint4*>(snap + sw128_offset(n, 4 * half + cc)) = u;
+  }
+}
+
+// A state lane's 32 values into a snapshot: S^T row `row`, or for the z lane
+// rows 64 (hi = bf16(z)) and 65 (lo = bf16(z - hi)), about 16 bits of z.
+__device__ __forceinline__ void snap_half(uint8_t* snap, int row, int half, const float* v) {
+  if (row < D) {
+    store_snap_half(snap, row, half, v);
+  } else {
+    float hi[32], lo[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      hi[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+      lo[i] = v[i] - hi[i];
+    }
+    store_snap_half(snap, 64, half, hi);
+    store_snap_half(snap, 65, half, lo);
+  }
 }
 
 __device__ void epilogue(const Ctx& x, int quad, int lane, int et, const CUtensorMap* to) {
   const TcParams& p = *x.p;
   Bars* B = x.bars;
   const int row = 32 * quad + lane;
-  const bool state_row = row < D;  // S / z rows live in TMEM lanes 0..63
+  const bool state_warp = quad <= 2;        // TMEM lanes 0..95 (loads are warp-wide)
+  const bool state_row = row <= D;          // lanes 0..64 carry R^T and z
   const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
   uint8_t* sE = x.smem + OFF_ESNAP;
   uint8_t* sR = x.smem + OFF_RSNAP;
-  uint8_t* sBz = x.smem + OFF_BZ;
-  uint32_t aj = 0, oj = 0, sj = 0, itn = 0;
-  uint32_t na[2] = {0, 0};  // uses of accA[b]
+  uint32_t oj = 0, sj = 0, itn = 0, nacc = 0;
 
   for (int g = blockIdx.x; g < p.total_items; g += gridDim.x) {
     const Item it = item_of(p, g);
     // the previous item's last MMA has read every snapshot we are about to overwrite
     if (itn > 0) wait_bar(x, &B->snapfree, (itn - 1) & 1);
 
-    // ---- phase A: running sum R of dS_c, dz_c; snapshots R_1..R_{n-1}
-    float R[D];
-    float Rz = 0.f;
+    // ---- phase A: snapshots R_1..R_{n-1} of the running state
+    for (int c = 0; c < it.nch; ++c, ++sj) {
+      wait_bar(x, &B->accA, nacc & 1);
+      ++nacc;
+      if (c + 1 < it.nch) {
+        tc_fence_after();
+        if (state_warp) {
 #pragma unroll
-    for (int i = 0; i < D; ++i) R[i] = 0.f;
-    for (int c = 0; c < it.nch; ++c, ++aj, ++sj) {
-      const int b = aj % 2;
-      wait_bar(x, &B->accA[b], na[b] & 1);
-      ++na[b];
-      tc_fence_after();
-      if (state_row) {
-        const uint32_t base = tl + TA + 128 * b;
-        uint32_t r[32];
-        tmem_ld32(base, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) R[i] += __uint_as_float(r[i]);
-        tmem_ld32(base + 32, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) R[32 + i] += __uint_as_float(r[i]);
-        uint32_t z2[2];
-        tmem_ld2(base + D, z2);
-        tmem_ld_wait();
-        Rz += __uint_as_float(z2[0]);
-      }
-      tc_fence_before();
-      named_bar_sync(1, 128);
-      if (et == 0) mbar_arrive(&B->freeb[b]);
-      if (c + 1 < it.nch && state_row) {
-        store_snap_row(sR + c * SNAP, row, R);
-        store_bz(sBz + (c + 1) * 2048, row, Rz);
+          for (int half = 0; half < 2; ++half) {
+            float v[32];
+            load_r_half(tl, half, v);
+            if (state_row) snap_half(sR + c * SNAP, row, half, v);
+          }
+        }
+        tc_fence_before();
+        named_bar_sync(1, 128);
+        if (et == 0) mbar_arrive(&B->rfree);
       }
     }
+    tc_fence_after();
 
-    // ---- publish the aggregate, look back, publish the inclusive prefix
-    float* my_agg = p.agg + (size_t)g * SZ;
-    if (state_row) {
+    // ---- publish the aggregate, look back, publish the inclusive prefix.
+    // Publication: every thread stores, the named barrier orders the stores
+    // before thread 0's release store of the flag (thread 0 issues no bulk
+    // copies).  Window 0 has no earlier item: it publishes S0 + R directly.
+    float* my_agg = p.agg + (size_t)g * SZ + row * D;
+    float* my_inc = p.inc + (size_t)g * SZ + row * D;
+    const bool last = it.w == p.items_per_head - 1;
+    if (it.w > 0) {
+      if (state_warp) {
 #pragma unroll
-      for (int i = 0; i < D; i += 4)
-        __stcg(reinterpret_cast<float4*>(my_agg + row * D + i),
-               make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]));
-      __stcg(my_agg + D * D + row, Rz);
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          load_r_half(tl, half, v);
+          if (state_row) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              __stcg(reinterpret_cast<float4*>(my_agg + 32 * half) + i,
+                     make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          }
+        }
+      }
+      named_bar_sync(1, 128);
+      if (et == 0) st_release_gpu(&p.flags[g], (x.epoch << 2) | kFlagAggregate);
     }
-    __threadfence();
-    named_bar_sync(1, 128);
-    if (et == 0) {
-      st_release_gpu(&p.flags[g], (x.epoch << 2) | kFlagAggregate);
-      B->lb_start = lookback_start(p, it, x.epoch);
-    }
+    if (et == 0) B->lb_start = lookback_start(p, it, x.epoch);  // -1 for window 0
     named_bar_sync(1, 128);
     const int start = *reinterpret_cast<volatile int*>(&B->lb_start);
-    if (state_row) {
-      // E = left fold S0 + agg_0 + ... + agg_{w-1}, eight columns at a time;
-      // inclusive = E + R is published, E goes to the bf16 snapshot
-      const float* base_src = start >= 0 ? p.inc + (size_t)(start * p.BH + it.h) * SZ
-                                         : (p.S0 ? p.S0 + (size_t)it.h * D * D : nullptr);
-      float* my_inc = p.inc + (size_t)g * SZ;
-      const bool last = it.w == p.items_per_head - 1;
+    if (state_warp) {
+      // E = left fold S0 + agg_0 + ... + agg_{w-1}, starting from the nearest
+      // published inclusive prefix; inclusive = E + R is published, E goes to
+      // the bf16 snapshot.  Every load of a step is issued before its sums.
+      const float* S0h = p.S0 ? p.S0 + (size_t)it.h * D * D : nullptr;
+      const float* z0h = p.z0 ? p.z0 + (size_t)it.h * D : nullptr;
+      const bool base_api = start < 0;
+      const bool has_base = !base_api || (row < D ? S0h != nullptr : z0h != nullptr);
+      const float* base_slot = p.inc + (size_t)(start < 0 ? 0 : start * p.BH + it.h) * SZ + row * D;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        float e[8];
-        if (base_src) {
-          const float4 u0 = __ldcg(reinterpret_cast<const float4*>(base_src + row * D + 8 * cc));
-          const float4 u1 = __ldcg(reinterpret_cast<const float4*>(base_src + row * D + 8 * cc + 4));
-          e[0] = u0.x; e[1] = u0.y; e[2] = u0.z; e[3] = u0.w;
-          e[4] = u1.x; e[5] = u1.y; e[6] = u1.z; e[7] = u1.w;
+      for (int half = 0; half < 2; ++half) {
+        float e[32];
+        if (!state_row || !has_base) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) e[i] = 0.f;
+        } else if (base_api) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) e[i] = __ldcg(api_elem(S0h, z0h, row, 32 * half + i));
         } else {
+          float4 u[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) e[i] = 0.f;
+          for (int i = 0; i < 8; ++i) u[i] = __ldcg(reinterpret_cast<const float4*>(base_slot + 32 * half) + i);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            e[4 * i] = u[i].x; e[4 * i + 1] = u[i].y; e[4 * i + 2] = u[i].z; e[4 * i + 3] = u[i].w;
+          }
         }
-        for (int ww = start + 1; ww < it.w; ++ww) {
-          const float* src = p.agg + (size_t)(ww * p.BH + it.h) * SZ + row * D + 8 * cc;
-          const float4 u0 = __ldcg(reinterpret_cast<const float4*>(src));
-          const float4 u1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-          e[0] += u0.x; e[1] += u0.y; e[2] += u0.z; e[3] += u0.w;
-          e[4] += u1.x; e[5] += u1.y; e[6] += u1.z; e[7] += u1.w;
+        if (state_row) {
+          for (int ww = start + 1; ww < it.w; ++ww) {
+            const float* src = p.agg + (size_t)(ww * p.BH + it.h) * SZ + row * D + 32 * half;
+            float4 u[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) u[i] = __ldcg(reinterpret_cast<const float4*>(src) + i);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              e[4 * i] += u[i].x; e[4 * i + 1] += u[i].y; e[4 * i + 2] += u[i].z; e[4 * i + 3] += u[i].w;
+            }
+          }
         }
-        const float4 i0 = make_float4(e[0] + R[8 * cc + 0], e[1] + R[8 * cc + 1],
-                                      e[2] + R[8 * cc + 2], e[3] + R[8 * cc + 3]);
-        const float4 i1 = make_float4(e[4] + R[8 * cc + 4], e[5] + R[8 * cc + 5],
-                                      e[6] + R[8 * cc + 6], e[7] + R[8 * cc + 7]);
-        __stcg(reinterpret_cast<float4*>(my_inc + row * D + 8 * cc), i0);
-        __stcg(reinterpret_cast<float4*>(my_inc + row * D + 8 * cc + 4), i1);
-        if (last) {
-          float* sn = p.S_N + (size_t)it.h * D * D + row * D + 8 * cc;
-          *reinterpret_cast<float4*>(sn) = i0;
-          *reinterpret_cast<float4*>(sn + 4) = i1;
+        float r[32];
+        load_r_half(tl, half, r);
+        if (state_row) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = make_float4(e[4 * i] + r[4 * i], e[4 * i + 1] + r[4 * i + 1],
+                                         e[4 * i + 2] + r[4 * i + 2], e[4 * i + 3] + r[4 * i + 3]);
+            __stcg(reinterpret_cast<float4*>(my_inc + 32 * half) + i, v);
+            if (last) {
+              float* SN = p.S_N + (size_t)it.h * D * D;
+              float* zN = p.z_N + (size_t)it.h * D;
+              *api_elem(SN, zN, row, 32 * half + 4 * i) = v.x;
+              *api_elem(SN, zN, row, 32 * half + 4 * i + 1) = v.y;
+              *api_elem(SN, zN, row, 32 * half + 4 * i + 2) = v.z;
+              *api_elem(SN, zN, row, 32 * half + 4 * i + 3) = v.w;
+            }
+          }
+          snap_half(sE, row, half, e);
         }
-        uint4 u;
-        u.x = pack_bf16x2(e[0], e[1]);
-        u.y = pack_bf16x2(e[2], e[3]);
-        u.z = pack_bf16x2(e[4], e[5]);
-        u.w = pack_bf16x2(e[6], e[7]);
-        *reinterpret_cast<uint4*>(sE + sw128_offset(row, cc)) = u;
       }
-      float ez = 0.f;
-      if (start >= 0) ez = __ldcg(p.inc + (size_t)(start * p.BH + it.h) * SZ + D * D + row);
-      else if (p.z0) ez = __ldcg(p.z0 + (size_t)it.h * D + row);
-      for (int ww = start + 1; ww < it.w; ++ww)
-        ez += __ldcg(p.agg + (size_t)(ww * p.BH + it.h) * SZ + D * D + row);
-      __stcg(my_inc + D * D + row, ez + Rz);
-      if (last) p.z_N[(size_t)it.h * D + row] = ez + Rz;
-      store_bz(sBz, row, ez);
     }
-    __threadfence();
+    tc_fence_before();
     named_bar_sync(1, 128);
-    if (et == 0) st_release_gpu(&p.flags[g], (x.epoch << 2) | kFlagInclusive);
+    if (et == 0) {
+      st_release_gpu(&p.flags[g], (x.epoch << 2) | kFlagInclusive);
+      mbar_arrive(&B->rfree);  // R may be overwritten by the next item
+    }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&B->eready);
@@ -507,7 +625,7 @@ __device__ void epilogue(const Ctx& x, int quad, int lane, int et, const CUtenso
                         __uint_as_float(n1[4 * cc + 2]) * inv, __uint_as_float(n1[4 * cc + 3]) * inv);
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
-      if (et == 0) {
+      if (et == 32) {  // the bulk-store thread (never publishes flags)
         const int tok = it.tok0 + c * C;
         tma_store_3d(to, st, 0, tok, it.h);
         tma_store_3d(to, st + BLK, 32, tok, it.h);
@@ -518,7 +636,7 @@ __device__ void epilogue(const Ctx& x, int quad, int lane, int et, const CUtenso
     }
     ++itn;
   }
-  if (et == 0) bulk_wait_all();
+  if (et == 32) bulk_wait_all();
 }
 
 // ---------------------------------------------------------------------------
@@ -537,17 +655,18 @@ prefill_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->xf[s], 4);
+      mbar_init(&bars->xf[s], 8);
       mbar_init(&bars->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->accA[b], 1);
       mbar_init(&bars->accB[b], 1);
       mbar_init(&bars->pready[b], 4);
       mbar_init(&bars->freeb[b], 1);
       mbar_init(&bars->oready[b], 1);
       mbar_init(&bars->ofree[b], 4);
     }
+    mbar_init(&bars->accA, 1);
+    mbar_init(&bars->rfree, 1);
     mbar_init(&bars->eready, 4);
     mbar_init(&bars->snapfree, 1);
     mbar_init(&bars->drain, 1);
@@ -558,14 +677,16 @@ prefill_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
   }
-  // constant B operands: B1 (row 0 ones, 2 blocks), Bz rows 2..15 zero
-  for (int i = threadIdx.x; i < (kMaxChunks * 2048 + 4096) / 16; i += kThreads)
-    reinterpret_cast<uint4*>(smem + OFF_BZ)[i] = make_uint4(0, 0, 0, 0);
+  // constant operand data: the ones tile (column 0 = 1 in every token row,
+  // MN-major 128-byte swizzle) and the snapshots' zero rows 66..79
+  for (int i = threadIdx.x; i < (int)(BLK / 16); i += kThreads)
+    reinterpret_cast<uint4*>(smem + OFF_ONES)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = threadIdx.x; i < (int)(kMaxChunks * SNAP / 16); i += kThreads)
+    reinterpret_cast<uint4*>(smem + OFF_ESNAP)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  if (threadIdx.x < 16) {
-    const uint32_t one2 = 0x3F803F80u;  // two bf16 1.0
-    reinterpret_cast<uint4*>(smem + OFF_B1 + (threadIdx.x / 8) * 2048)[threadIdx.x % 8] =
-        make_uint4(one2, one2, one2, one2);
+  if (threadIdx.x < C) {  // token row t: logical chunk 0 sits at physical chunk t % 8
+    const int t = threadIdx.x;
+    *reinterpret_cast<uint16_t*>(smem + OFF_ONES + sw128_offset(t, 0)) = 0x3F80u;  // bf16 1.0
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_slot, kTmemCols);
@@ -583,12 +704,12 @@ prefill_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(x);
     __syncwarp();
-  } else if (warp < 6) {
-    transformer(x, threadIdx.x - 64, lane);
   } else if (warp < 10) {
+    transformer(x, threadIdx.x - 64, lane);
+  } else if (warp < 14) {
     p_builder(x, warp % 4, lane);
   } else {
-    epilogue(x, warp % 4, lane, threadIdx.x - 320, &tm_o);
+    epilogue(x, warp % 4, lane, threadIdx.x - 448, &tm_o);
   }
 
   tc_fence_before();
