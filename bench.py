@@ -89,9 +89,17 @@ def _max_over_ranks(x, world):
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, world, max_ms, steps):
+    """Whole-job throughput: the units every rank processed in `steps` steps,
+    over the slowest rank's time (weak scaling: each rank runs its own
+    replica of the workload)."""
+    return units_per_rank * world * steps / (max_ms * 1e-3)
 
 
 # --------------------------------------------------------------------------
@@ -482,7 +490,7 @@ def main():
     w = inputs.WORKLOADS["prefill"]
     total_ms, per = bench_prefill(api, w, args.steps, args.warmup, rank, world)
     ms_step = total_ms / args.steps
-    value = w.tokens * world / (total_ms * 1e-3 / args.steps)
+    value = job_throughput(w.tokens, world, total_ms, args.steps)
 
     extra = {}
     e2e = None
