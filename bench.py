@@ -179,7 +179,7 @@ def _peaks():
 def _kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fixed_state_recurrent_gb300", "csrc")
-    for name in ("prefill_tc64.cu", "prefill_tc_common.cuh", "tc_primitives.cuh"):
+    for name in ("prefill_chunked64.cu", "prefill_tc_common.cuh", "tc_primitives.cuh"):
         p = os.path.join(csrc, name)
         if os.path.exists(p):
             with open(p, "rb") as f:

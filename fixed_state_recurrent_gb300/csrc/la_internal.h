@@ -43,6 +43,12 @@ struct PrefillArgs {
 // CUDA-core prefill (any dk, dv <= 128; fp32 or bf16 inputs).
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 
+// Tensor-core chunked prefill for dk = dv = 64: aggregate, scan and output
+// launches (prefill_chunked64.cu).  The workspace size depends on the SM count
+// of the current device.
+size_t prefill_chunked64_workspace_bytes(int B, int H, int N);
+cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream);
+
 // Tensor-core chunked prefill (bf16, dk = dv in {64, 128}).
 bool prefill_tc_supported(const PrefillArgs& a);
 size_t prefill_tc_workspace_bytes(int B, int H, int N, int d, int chunk);

@@ -1,0 +1,976 @@
+// prefill_chunked64.cu -- chunked causal prefill for dk = dv = 64 on the
+// sm_103a tensor cores, as three launches with no waiting between blocks.
+//
+// Operator (page "AIGC 基本功|线性、循环与记忆架构-LinearMem", section 03):
+//   o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps),  S_t = S_{t-1} + phi(k_t) v_t^T,
+//   z_t = z_{t-1} + phi(k_t),  phi = ELU + 1,  write before read.
+// Chunkwise evaluation (page "线性注意力与SSM", section 3: a small masked
+// phi(Q) phi(K)^T attention inside each chunk, and across chunks a recurrence
+// that hands over only the state), chunk C = 128 tokens.
+//
+// Work split: the B*H heads' chunks form one head-major sequence; block j of G
+// takes the contiguous run [j TC / G, (j+1) TC / G) of it (TC = total chunks,
+// so every block gets the same number of chunks to within one), cut at head
+// boundaries into "pieces".  Piece slots are numbered (head, index of the
+// block within the head's blocks).
+//   K1 (aggregate): each piece's state increment, accumulated on the tensor
+//      cores as the transposed product R = sum [V_c | 1]^T phi(K_c) (TMEM lanes
+//      0..63 = R^T, lane 64 = z), stored transposed to the workspace; phi(K)
+//      itself (bf16, the layout of K) is stored to the workspace for K3.
+//   K2 (scan): per head, the exclusive prefix of every piece as the left fold
+//      S0 + R_0 + R_1 + ... in fp32 (the same order every run), and the final
+//      state S_N, z_N.
+//   K3 (output): each piece replays its chunks from its prefix E (reading Q,
+//      phi(K) and V; phi is applied to Q only): the running
+//      state lives in TMEM (initialised to E, advanced by [V_c | 1]^T phi(K_c)
+//      after each chunk) and is snapshotted to bf16 for the next chunk; per
+//      chunk, scores phi(Q) phi(K)^T, P = causal mask of the scores (bf16,
+//      written back into TMEM), [num | den] = P [V | 1] + phi(Q) [S | z] as two
+//      N = 80 products, o = num / (den + eps) stored through TMA.
+// V and phi(K) are read again by K3 (from L2 when the workload fits in it).
+#include "prefill_tc_common.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+using namespace tcp;
+
+constexpr int D = 64;
+constexpr int SZ = D * D + D;                // floats per state slot (R^T rows, then z)
+constexpr uint32_t BLK = 16384;              // [128 rows x 128 B] swizzled bf16 tile
+constexpr uint32_t SNAP = 80 * 128;          // K-major [80 x 64]: S^T rows, z hi, z lo, zeros
+
+constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);     // phi(Q) phi(K)^T
+constexpr uint32_t ID_PV = idesc_bf16_f32(128, D + 16, 0, 1); // P [V | 1]
+constexpr uint32_t ID_QS = idesc_bf16_f32(128, D + 16, 0, 0); // phi(Q) [S | z]
+constexpr uint32_t ID_DS = idesc_bf16_f32(128, D, 1, 1);      // [V | 1]^T phi(K)
+
+// ---------------------------------------------------------------------------
+// work split (identical in the three kernels and on the host)
+
+struct Split {
+  int BH, N, NC;  // heads, tokens per head, chunks per head
+  int G;          // blocks of K1 and K3
+  int MPH;        // piece slots per head
+  __host__ __device__ long long TC() const { return (long long)BH * NC; }
+  __host__ __device__ long long start(int j) const { return (long long)j * TC() / G; }
+  // the block whose run contains global chunk x
+  __host__ __device__ int owner(long long x) const {
+    return (int)(((x + 1) * G - 1) / TC());
+  }
+};
+
+struct Piece {
+  int h, slot;
+  int tok0, tok1, nch;
+};
+
+// Block j's run of chunks [a, b) and the pieces it is cut into.  The 64-bit
+// divisions happen once, here; walking the pieces needs none.
+struct Run {
+  long long a, b;
+  int h0;    // head of the first piece
+  int idx0;  // position of block j among the blocks that meet head h0
+  __host__ __device__ Run(const Split& s, int j) {
+    a = s.start(j);
+    b = s.start(j + 1);
+    h0 = (int)(a / s.NC);
+    idx0 = j - s.owner((long long)h0 * s.NC);
+  }
+  // The i-th piece (pieces are ordered by position); false when there are
+  // fewer.  Every piece after the first starts its head, so its slot index
+  // within the head is 0.
+  __host__ __device__ bool piece(const Split& s, int i, Piece* pc) const {
+    if (a >= b) return false;
+    const int h = h0 + i;
+    const long long hs = (long long)h * s.NC;
+    if (hs >= b || h >= s.BH) return false;
+    const long long c0 = a > hs ? a : hs;
+    const long long c1 = b < hs + s.NC ? b : hs + s.NC;
+    pc->h = h;
+    pc->slot = h * s.MPH + (i == 0 ? idx0 : 0);
+    pc->tok0 = (int)(c0 - hs) * C;
+    pc->tok1 = (int)(c1 - hs) * C;
+    if (pc->tok1 > s.N) pc->tok1 = s.N;
+    pc->nch = (int)(c1 - c0);
+    return true;
+  }
+};
+
+struct Params3 {
+  Split sp;
+  float eps;
+  const float* S0;
+  const float* z0;
+  float* S_N;
+  float* z_N;
+  WsHeader* hdr;
+  float* agg;  // [BH * MPH][SZ], transposed slots
+  float* E;    // [BH * MPH][SZ], exclusive prefixes, transposed slots
+  __nv_bfloat16* phik;  // [BH][N][D], phi(K) written by K1
+  int force_wait;       // test hook: K3 waits once on a barrier that nothing completes
+};
+
+struct Ctx3 {
+  const Params3* p;
+  uint8_t* smem;
+  uint64_t* bars;
+  volatile int* abort;
+  uint32_t tmem;
+  unsigned long long mbar_ns;
+};
+
+// Bounded wait.  false once the block has given up (this wait ran out of time
+// and recorded a timeout in the status word, or another role's did).  After
+// that no role starts new asynchronous work (TMA, MMA, stores), every role
+// still runs its loops, with each wait returning at once, so that the named
+// barriers of a warp group stay matched, and the issuers drain what they
+// started before the tensor memory is freed.
+__device__ __forceinline__ bool wait3(const Ctx3& x, uint64_t* bar, uint32_t parity) {
+  if (*x.abort) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity, globaltimer_ns() + x.mbar_ns, x.abort)) return true;
+  *x.abort = 1;
+  atomicOr(&x.p->hdr->status, kStatusTimeout);
+  return false;
+}
+
+// The same decision for a whole warp (all lanes wait on the same barrier).
+__device__ __forceinline__ bool wait3_warp(const Ctx3& x, uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xFFFFFFFFu, wait3(x, bar, parity));
+}
+
+// Producer drain: the last loads that were issued (at most NS) land before the
+// block leaves.
+template <int NS_>
+__device__ __forceinline__ void drain_loads(uint64_t* full, uint32_t issued, unsigned long long ns) {
+  int never = 0;
+  const uint64_t dl = globaltimer_ns() + ns;
+  for (uint32_t q = (issued > NS_ ? issued - NS_ : 0); q < issued; ++q)
+    mbar_wait(&full[q % NS_], (q / NS_) & 1, dl, &never);
+}
+
+// phi on two bf16: phi(u) = exp(min(u, 0)) + max(u, 0), which is u + 1 for
+// u > 0 and exp(u) otherwise.  min and max are taken on the bf16 pair; the two
+// exponentials are one paired half-precision 2^x (ex2.approx.f16x2, relative
+// error about 2^-9.9) of min(u, 0) log2(e), the argument formed in fp32 and
+// rounded to f16 (absolute error |x| 2^-11, below 0.003 for |u| < 4); the sum
+// is rounded to bf16 (relative error 2^-9), the precision of the tensor-core
+// operand it feeds.
+__device__ __forceinline__ uint32_t phi2(uint32_t x) {
+  const __nv_bfloat162 u = *reinterpret_cast<const __nv_bfloat162*>(&x);
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const __nv_bfloat162 m = __hmin2(u, zero);
+  const __nv_bfloat162 M = __hmax2(u, zero);
+  const uint32_t mb = *reinterpret_cast<const uint32_t*>(&m);
+  const float xa = __uint_as_float(mb << 16) * 1.4426950408889634f;
+  const float xb = __uint_as_float(mb & 0xFFFF0000u) * 1.4426950408889634f;
+  uint32_t h, e;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(xb), "f"(xa));
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
+  float ea, eb;
+  asm("{.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;}"
+      : "=f"(ea), "=f"(eb)
+      : "r"(e));
+  const uint32_t eb2 = pack_bf16x2(ea, eb);
+  const __nv_bfloat162 r = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&eb2), M);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// phi on `nchunk` 16-byte chunks of row r of a tile starting at chunk `c0`;
+// rows at or past `valid` become zero.  Loads first, then math, then stores.
+// The row mask is applied with an AND after an unconditional phi: a
+// conditional around phi2 lets the compiler branch around every pair, which
+// serialises the 4 NCH independent exponential chains of a thread.
+template <int NCH>
+__device__ __forceinline__ void phi_row(uint8_t* tile, int r, int c0, int valid) {
+  uint4 v[NCH];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) v[i] = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, c0 + i));
+  const uint32_t keep = r < valid ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    v[i].x = phi2(v[i].x) & keep;
+    v[i].y = phi2(v[i].y) & keep;
+    v[i].z = phi2(v[i].z) & keep;
+    v[i].w = phi2(v[i].w) & keep;
+  }
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0 + i)) = v[i];
+}
+
+// The all-ones operand block: [128 token rows x 64] MN-major, column 0 = 1.
+__device__ __forceinline__ void init_ones(uint8_t* ones, int tid, int nthreads) {
+  for (int i = tid; i < (int)(BLK / 16); i += nthreads)
+    reinterpret_cast<uint4*>(ones)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  if (tid < C) *reinterpret_cast<uint16_t*>(ones + sw128_offset(tid, 0)) = 0x3F80u;  // bf16 1.0
+}
+
+// The running-state / snapshot helpers.  State lane `row` (0..64) of the
+// transposed state owns slot floats [64 row, 64 row + 64): row j < 64 is
+// column j of S (row j of S^T), row 64 is z.
+__device__ __forceinline__ void store_snap_half(uint8_t* snap, int n, int half, const float* v) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * cc + 0], v[8 * cc + 1]);
+    u.y = pack_bf16x2(v[8 * cc + 2], v[8 * cc + 3]);
+    u.z = pack_bf16x2(v[8 * cc + 4], v[8 * cc + 5]);
+    u.w = pack_bf16x2(v[8 * cc + 6], v[8 * cc + 7]);
+    *reinterpret_cast<uint4*>(snap + sw128_offset(n, 4 * half + cc)) = u;
+  }
+}
+
+// Snapshot rows of one state lane: S^T row `row`, or for lane 64 rows 64
+// (hi = bf16(z)) and 65 (lo = bf16(z - hi)): about 16 bits of z.  Works on
+// eight values at a time, so that no second copy of the half row is live.
+__device__ __forceinline__ void snap_half(uint8_t* snap, int row, int half, const float* v) {
+  if (row < D) {
+    store_snap_half(snap, row, half, v);
+  } else {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float hi[8], lo[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        hi[i] = __bfloat162float(__float2bfloat16_rn(v[8 * cc + i]));
+        lo[i] = v[8 * cc + i] - hi[i];
+      }
+      uint4 uh, ul;
+      uh.x = pack_bf16x2(hi[0], hi[1]); uh.y = pack_bf16x2(hi[2], hi[3]);
+      uh.z = pack_bf16x2(hi[4], hi[5]); uh.w = pack_bf16x2(hi[6], hi[7]);
+      ul.x = pack_bf16x2(lo[0], lo[1]); ul.y = pack_bf16x2(lo[2], lo[3]);
+      ul.z = pack_bf16x2(lo[4], lo[5]); ul.w = pack_bf16x2(lo[6], lo[7]);
+      *reinterpret_cast<uint4*>(snap + sw128_offset(64, 4 * half + cc)) = uh;
+      *reinterpret_cast<uint4*>(snap + sw128_offset(65, 4 * half + cc)) = ul;
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_ld_half(uint32_t taddr, float* out /*32*/) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void drain_and_free(const Ctx3& x, int warp, uint32_t ncols) {
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(x.tmem, ncols);
+  }
+}
+
+// ===========================================================================
+// K1: piece aggregates
+
+namespace k1 {
+
+constexpr int NS = 4;
+constexpr uint32_t STAGE = 2 * BLK;  // K | V
+constexpr uint32_t OFF_ONES = NS * STAGE;
+constexpr uint32_t OFF_BAR = OFF_ONES + BLK;
+constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+constexpr int kWarps = 10;  // 0 TMA, 1 MMA, 2-5 phi, 6-9 epilogue (thread 192 also stores phi(K))
+constexpr uint32_t kCols = 128;
+
+struct Bars {
+  uint64_t full[NS], xf[NS];
+  uint64_t empty[NS];  // the stage's MMA done and its phi(K) store read (2 arrivals)
+  uint64_t racc[2];   // a piece's R complete in R[b]   (MMA -> epilogue)
+  uint64_t rfree[2];  // R[b] stored                    (epilogue -> MMA)
+  uint64_t drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+__global__ void __launch_bounds__(32 * kWarps, 1)
+aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+       const __grid_constant__ CUtensorMap tm_phik, const Params3 p, const unsigned long long mbar_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&B->full[s], 1);
+      mbar_init(&B->xf[s], 4);
+      mbar_init(&B->empty[s], 2);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&B->racc[b], 1);
+      mbar_init(&B->rfree[b], 1);
+    }
+    mbar_init(&B->drain, 1);
+    B->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_phik);
+  }
+  init_ones(smem + OFF_ONES, threadIdx.x, 32 * kWarps);
+  if (warp == 1) {
+    tmem_alloc(&B->tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const Ctx3 x{&p, smem, reinterpret_cast<uint64_t*>(B), &B->abort,
+               *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
+  const Run run(p.sp, blockIdx.x);
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer: K, V chunk tiles
+      uint32_t sj = 0, issued = 0;
+      Piece pc;
+      for (int i = 0; run.piece(p.sp, i, &pc); ++i)
+        for (int c = 0; c < pc.nch; ++c, ++sj) {
+          const int s = sj % NS;
+          if (sj >= NS && !wait3(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
+          uint8_t* st = smem + s * STAGE;
+          const int tok = pc.tok0 + c * C;
+          mbar_arrive_expect_tx(&B->full[s], 2 * BLK);
+          tma_load_3d(st, &tm_k, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d(st + BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
+          ++issued;
+        }
+      if (*x.abort) drain_loads<NS>(B->full, issued, mbar_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA: R[b] = sum over the piece's chunks of [V | 1]^T phi(K)
+      const uint32_t aOnes = smem_u32(smem + OFF_ONES);
+      uint32_t sj = 0;
+      Piece pc;
+      for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+        const int b = i % 2;
+        if (i >= 2 && !wait3(x, &B->rfree[b], ((i / 2) - 1) & 1)) break;
+        for (int c = 0; c < pc.nch; ++c, ++sj) {
+          const int s = sj % NS;
+          if (!wait3(x, &B->xf[s], (sj / NS) & 1)) break;
+          tc_fence_after();
+          const uint32_t kt = smem_u32(smem + s * STAGE), vt = kt + BLK;
+#pragma unroll
+          for (int ks = 0; ks < C / 16; ++ks) {
+            const uint64_t a = sdesc_sw128(vt + ks * 2048, aOnes - vt, 1024);
+            const uint64_t bd = sdesc_sw128(kt + ks * 2048, BLK, 1024);
+            mma_bf16_ss(x.tmem + 64 * b, a, bd, ID_DS, (c > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(&B->empty[s]);
+        }
+        if (*x.abort) break;
+        mma_commit(&B->racc[b]);
+      }
+      if (*x.abort) {
+        int never = 0;
+        mma_commit(&B->drain);
+        mbar_wait(&B->drain, 0, globaltimer_ns() + mbar_ns, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {  // ---- phi on K (one tile row per thread)
+    const int r = threadIdx.x - 64;
+    uint32_t sj = 0;
+    Piece pc;
+    for (int i = 0; run.piece(p.sp, i, &pc); ++i)
+      for (int c = 0; c < pc.nch; ++c, ++sj) {
+        const int s = sj % NS;
+        if (!wait3_warp(x, &B->full[s], (sj / NS) & 1)) continue;
+        phi_row<8>(smem + s * STAGE, r, 0, pc.tok1 - (pc.tok0 + c * C));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B->xf[s]);
+      }
+  } else {  // ---- epilogue: R[b] -> workspace slot (transposed rows)
+    const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 192;
+    const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
+    uint32_t sj = 0;
+    Piece pc;
+    for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+      if (et == 0) {  // phi(K) of the piece's chunks -> workspace; a stage is
+                      // released once the store of the chunk after it was issued
+                      // and its own store has read shared memory
+        for (int c = 0; c < pc.nch; ++c, ++sj) {
+          const int s = sj % NS;
+          if (!wait3(x, &B->xf[s], (sj / NS) & 1)) continue;
+          tma_store_3d(&tm_phik, smem + s * STAGE, 0, pc.tok0 + c * C, pc.h);
+          bulk_commit();
+          if (sj > 0) {
+            bulk_wait_read_but_one();
+            mbar_arrive(&B->empty[(sj - 1) % NS]);
+          }
+        }
+      }
+      const int b = i % 2;
+      wait3(x, &B->racc[b], (i / 2) & 1);  // on a timeout the rest runs on, storing garbage
+      tc_fence_after();
+      if (quad <= 2) {
+        float* dst = p.agg + (size_t)pc.slot * SZ + row * D;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          tmem_ld_half(tl + 64 * b + 32 * half, v);
+          if (row <= D) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              __stcg(reinterpret_cast<float4*>(dst + 32 * half) + q,
+                     make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(1, 128);
+      if (et == 0) mbar_arrive(&B->rfree[b]);
+    }
+    if (et == 0) {
+      bulk_wait_all();
+      if (sj > 0 && !*x.abort) mbar_arrive(&B->empty[(sj - 1) % NS]);
+    }
+  }
+  drain_and_free(x, warp, kCols);
+}
+
+}  // namespace k1
+
+// ===========================================================================
+// K2: exclusive prefix of every piece (left fold from S0), final state
+
+namespace k2 {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) scan_kernel(const Params3 p) {
+  const int e = blockIdx.x * kThreads + threadIdx.x;  // slot element: row * 64 + i
+  const int h = blockIdx.y;
+  if (e >= SZ) return;
+  const Split& s = p.sp;
+  const int row = e / D, i = e % D;  // row < 64: S[i][row]; row 64: z[i]
+  float acc = 0.f;
+  if (row < D) {
+    if (p.S0) acc = p.S0[(size_t)h * D * D + i * D + row];
+  } else if (p.z0) {
+    acc = p.z0[(size_t)h * D + i];
+  }
+  const int first = s.owner((long long)h * s.NC);
+  const int npieces = s.owner((long long)(h + 1) * s.NC - 1) - first + 1;
+  const size_t base = (size_t)h * s.MPH * SZ + e;
+  constexpr int U = 8;
+  for (int w0 = 0; w0 < npieces; w0 += U) {
+    float a[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      a[u] = (w0 + u < npieces) ? __ldcg(p.agg + base + (size_t)(w0 + u) * SZ) : 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (w0 + u < npieces) {
+        __stcg(p.E + base + (size_t)(w0 + u) * SZ, acc);
+        acc += a[u];
+      }
+    }
+  }
+  if (row < D) p.S_N[(size_t)h * D * D + i * D + row] = acc;
+  else p.z_N[(size_t)h * D + i] = acc;
+}
+
+}  // namespace k2
+
+// ===========================================================================
+// K3: outputs
+
+namespace k3 {
+
+constexpr int NS = 3;
+constexpr uint32_t STAGE = 3 * BLK;                // Q | phi(K) | V
+constexpr uint32_t OFF_ONES = NS * STAGE;
+constexpr uint32_t OFF_SNAP = OFF_ONES + BLK;      // two snapshots
+constexpr uint32_t OFF_OUT = OFF_SNAP + 2 * SNAP;  // output staging: two [128 x 32] fp32 boxes
+constexpr uint32_t OFF_BAR = OFF_OUT + 2 * BLK;
+constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
+static_assert(SMEM <= 227 * 1024, "shared memory per block");
+static_assert(OFF_OUT % 1024 == 0, "swizzled staging alignment");
+// 0 TMA, 1 MMA, 2-5 phi(Q), 6-9 P, 10-13 state/output epilogue: at most four
+// warps per SM sub-partition, so 128 registers per thread
+constexpr int kWarps = 14;
+constexpr uint32_t kCols = 512;
+constexpr uint32_t TA = 0;    // A[b]: scores, then P (packed bf16) -- cols 128 b
+constexpr uint32_t TO = 256;  // O[ob]: 64 numerator + 16 denominator cols -- 256 + 80 ob
+constexpr uint32_t TS = 416;  // running state S^T (lanes 0..63) and z (lane 64), 64 cols
+
+struct Bars {
+  uint64_t full[NS], xf[NS];
+  uint64_t empty[NS];  // the stage's products done: 2 arrivals  (both MMA issuers -> TMA)
+  uint64_t accB[2];    // scores in A[b]                       (MMA -> P warps)
+  uint64_t pready[2];  // P in A[b]                            (P warps -> MMA)
+  uint64_t freeb[2];   // A[b] reusable                        (MMA -> MMA)
+  uint64_t oready[2];  // num, den in O[ob]                    (MMA -> epilogue)
+  uint64_t ofree[2];   // O[ob] read                           (epilogue -> MMA)
+  uint64_t sacc;       // running state advanced               (state MMA -> epilogue)
+  uint64_t sready[2];  // chunk j's snapshot written, in [j % 2] (epilogue -> MMA): two,
+                       // as the snapshots may run one chunk ahead of the MMA warp
+  uint64_t tsread;     // the running state read out of TMEM   (state warps -> state MMA)
+  uint64_t drain, drain2;
+  uint64_t never;      // completed by nothing (the forced-timeout test hook)
+  uint32_t tmem_slot;
+  int abort;
+  float4 zbuf[16];     // z, handed from its TMEM lane to the whole warp
+};
+static_assert(sizeof(Bars) <= 512, "barrier area");
+
+__device__ __forceinline__ uint8_t* stage_ptr(uint8_t* smem, uint32_t s) { return smem + s * STAGE; }
+
+// Two threads issue MMAs.  The MMA warp issues, per chunk a, the scores of
+// chunk a + 1 and then P [V | 1] and phi(Q) [S | z] of chunk a, so that P of
+// chunk a + 1 is built while the products of chunk a run.  The state chain is
+// issued by one thread of the snapshot warps: the advance S += [V | 1]^T
+// phi(K) of chunk a goes out as soon as the snapshot of the state before chunk
+// a has been read out of TMEM, and does not queue behind the output products.
+// A stage is released by both issuers (a commit each, or an arrival where no
+// state advance reads it).
+__global__ void __launch_bounds__(32 * kWarps, 1)
+output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+       const Params3 p, const unsigned long long mbar_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&B->full[s], 1);
+      mbar_init(&B->xf[s], 4);
+      mbar_init(&B->empty[s], 2);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&B->accB[b], 1);
+      mbar_init(&B->pready[b], 4);
+      mbar_init(&B->freeb[b], 1);
+      mbar_init(&B->oready[b], 1);
+      mbar_init(&B->ofree[b], 4);
+    }
+    mbar_init(&B->sacc, 1);
+    mbar_init(&B->sready[0], 1);
+    mbar_init(&B->sready[1], 1);
+    mbar_init(&B->drain, 1);
+    mbar_init(&B->drain2, 1);
+    mbar_init(&B->tsread, 3);
+    mbar_init(&B->never, 1);
+    B->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+  }
+  init_ones(smem + OFF_ONES, threadIdx.x, 32 * kWarps);
+  for (int i = threadIdx.x; i < (int)(2 * SNAP / 16); i += 32 * kWarps)  // snapshot rows 66..79 stay 0
+    reinterpret_cast<uint4*>(smem + OFF_SNAP)[i] = make_uint4(0, 0, 0, 0);
+  if (warp == 1) {
+    tmem_alloc(&B->tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const Ctx3 x{&p, smem, reinterpret_cast<uint64_t*>(B), &B->abort,
+               *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
+  const Run run(p.sp, blockIdx.x);
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer: Q, phi(K), V chunk tiles
+      uint32_t sj = 0, issued = 0;
+      Piece pc;
+      for (int i = 0; run.piece(p.sp, i, &pc); ++i)
+        for (int c = 0; c < pc.nch; ++c, ++sj) {
+          const int s = sj % NS;
+          if (sj >= NS && !wait3(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
+          uint8_t* st = stage_ptr(smem, s);
+          const int tok = pc.tok0 + c * C;
+          mbar_arrive_expect_tx(&B->full[s], 3 * BLK);
+          tma_load_3d(st, &tm_q, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
+          ++issued;
+        }
+      if (*x.abort) drain_loads<NS>(B->full, issued, mbar_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issue
+      const uint32_t tm = x.tmem;
+      const uint32_t aOnes = smem_u32(smem + OFF_ONES);
+      const uint32_t aSnap = smem_u32(smem + OFF_SNAP);
+      uint32_t aj = 0, oj = 0;
+      auto acquire = [&](uint32_t a) {  // job a: its stage transformed, A[a % 2] free
+        if (!wait3(x, &B->xf[a % NS], (a / NS) & 1)) return false;
+        if (a >= 2 && !wait3(x, &B->freeb[a % 2], ((a / 2) - 1) & 1)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto scores = [&](uint32_t a) {
+        const uint32_t st = smem_u32(stage_ptr(smem, a % NS));
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16_ss(tm + TA + 128 * (a % 2), sdesc_sw128(st + ks * 32, 16, 1024),
+                      sdesc_sw128(st + BLK + ks * 32, 16, 1024), ID_S, ks > 0 ? 1u : 0u);
+        mma_commit(&B->accB[a % 2]);
+      };
+      bool ok = !p.force_wait || wait3(x, &B->never, 0);
+      Piece pc;
+      for (int i = 0; ok && run.piece(p.sp, i, &pc); ++i) {
+        const uint32_t a0 = aj;
+        if (!acquire(a0)) break;
+        scores(a0);
+        for (int c = 0; ok && c < pc.nch; ++c) {
+          const uint32_t a = a0 + c;
+          const bool more = c + 1 < pc.nch;
+          if (more) {
+            if (!(ok = acquire(a + 1))) break;
+            scores(a + 1);
+          }
+          const uint32_t st = smem_u32(stage_ptr(smem, a % NS)), vt = st + 2 * BLK;
+          const int b = a % 2, ob = oj % 2;
+          ok = wait3(x, &B->sready[a % 2], (a / 2) & 1) &&  // this chunk's state snapshot
+               wait3(x, &B->pready[b], (a / 2) & 1) &&
+               (oj < 2 || wait3(x, &B->ofree[ob], ((oj / 2) - 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t dO = tm + TO + 80 * ob, aP = tm + TA + 128 * b;
+          const uint32_t sn = aSnap + (c % 2) * SNAP;
+#pragma unroll
+          for (int ks = 0; ks < C / 16; ++ks)  // P [V | 1], P from TMEM
+            mma_bf16_ts(dO, aP + 8 * ks, sdesc_sw128(vt + ks * 2048, aOnes - vt, 1024), ID_PV,
+                        ks > 0 ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)  // phi(Q) [S | z]
+            mma_bf16_ss(dO, sdesc_sw128(st + ks * 32, 16, 1024), sdesc_sw128(sn + ks * 32, 16, 1024),
+                        ID_QS, 1u);
+          mma_commit(&B->oready[ob]);
+          mma_commit(&B->freeb[b]);
+          mma_commit(&B->empty[a % NS]);
+          ++oj;
+        }
+        aj = a0 + pc.nch;
+      }
+      if (*x.abort) {
+        int never = 0;
+        mma_commit(&B->drain);
+        mbar_wait(&B->drain, 0, globaltimer_ns() + mbar_ns, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {  // ---- phi on Q (one tile row per thread); phi(K) comes from K1
+    const int r = threadIdx.x - 64;
+    uint32_t sj = 0;
+    Piece pc;
+    for (int i = 0; run.piece(p.sp, i, &pc); ++i)
+      for (int c = 0; c < pc.nch; ++c, ++sj) {
+        const int s = sj % NS;
+        if (!wait3_warp(x, &B->full[s], (sj / NS) & 1)) continue;
+        uint8_t* st = stage_ptr(smem, s);
+        const int valid = pc.tok1 - (pc.tok0 + c * C);
+        phi_row<8>(st, r, 0, valid);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B->xf[s]);
+      }
+  } else if (warp < 10) {  // ---- P = causal mask of the scores, bf16, in place in TMEM
+    const int quad = warp % 4;
+    const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
+    uint32_t aj = 0;
+    Piece pc;
+    for (int i = 0; run.piece(p.sp, i, &pc); ++i)
+      for (int c = 0; c < pc.nch; ++c, ++aj) {
+        const int b = aj % 2;
+        if (!wait3_warp(x, &B->accB[b], (aj / 2) & 1)) continue;
+        tc_fence_after();
+        const uint32_t base = tl + TA + 128 * b;
+        // this warp's query rows are 32 quad .. +31: key blocks before `quad` are
+        // fully visible, block `quad` holds the diagonal, later blocks are zero;
+        // packed keys 32 q4.. go to columns 16 q4..  Blocks are loaded two at a
+        // time, and a pair is read completely before its packed columns (which
+        // lie in the pair's own or an earlier block) are written.
+#pragma unroll
+        for (int q2 = 0; q2 < 4; q2 += 2) {
+          uint32_t r0[32], r1[32];
+          if (q2 <= quad) tmem_ld32(base + 32 * q2, r0);
+          if (q2 + 1 <= quad) tmem_ld32(base + 32 * (q2 + 1), r1);
+          if (q2 <= quad) tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int q4 = q2 + h;
+            const uint32_t* r = h ? r1 : r0;
+            uint32_t w[16];
+            if (q4 > quad) {
+#pragma unroll
+              for (int t = 0; t < 16; ++t) w[t] = 0u;
+            } else if (q4 < quad) {
+#pragma unroll
+              for (int t = 0; t < 16; ++t)
+                w[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
+            } else {
+#pragma unroll
+              for (int t = 0; t < 16; ++t)
+                w[t] = pack_bf16x2(2 * t <= lane ? __uint_as_float(r[2 * t]) : 0.f,
+                                   2 * t + 1 <= lane ? __uint_as_float(r[2 * t + 1]) : 0.f);
+            }
+            tmem_st16(base + 16 * q4, w);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B->pready[b]);
+      }
+  } else {  // ---- state snapshots and output epilogue
+    const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 320;
+    const bool state_warp = quad <= 2, state_row = row <= D;
+    const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
+    uint8_t* snap = smem + OFF_SNAP;
+    uint8_t* out = smem + OFF_OUT;
+    uint32_t oj = 0, nsa = 0, sj = 0, ntr = 0;
+    const uint32_t aOnes = smem_u32(smem + OFF_ONES);
+    // Thread et == 32 (in the warp that holds no state rows): the state advance
+    // of global chunk j, S += [V | 1]^T phi(K) (its stage loaded; the running
+    // state read), or, for a piece's last chunk, which has none, just its share
+    // of the stage's release.
+    auto advance = [&](uint32_t j, bool any) {
+      const int s = j % NS;
+      // Chunk j is loaded, so its stage's previous use has been released and
+      // the release below counts for chunk j (an earlier arrival would count
+      // for the previous use, and the stage could be refilled while read).
+      if (!wait3(x, &B->full[s], (j / NS) & 1)) return;
+      if (!any) {
+        mbar_arrive(&B->empty[s]);
+        return;
+      }
+      tc_fence_after();
+      const uint32_t st = smem_u32(stage_ptr(smem, s)), vt = st + 2 * BLK;
+#pragma unroll
+      for (int ks = 0; ks < C / 16; ++ks)
+        mma_bf16_ss(x.tmem + TS, sdesc_sw128(vt + ks * 2048, aOnes - vt, 1024),
+                    sdesc_sw128(st + BLK + ks * 2048, BLK, 1024), ID_DS, 1u);
+      mma_commit(&B->sacc);
+      mma_commit(&B->empty[s]);
+    };
+    Piece pc;
+    for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+      // The piece's entry state E: into TMEM (running state) and snapshot 0.
+      // The previous piece's products have all completed: its last output was
+      // read below, and every state advance was waited for.
+      if (state_warp) {
+        const float* src = p.E + (size_t)pc.slot * SZ + (state_row ? row : 0) * D;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float e[32];
+          if (state_row) {
+            float4 u[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) u[q] = __ldcg(reinterpret_cast<const float4*>(src + 32 * half) + q);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              e[4 * q] = u[q].x; e[4 * q + 1] = u[q].y; e[4 * q + 2] = u[q].z; e[4 * q + 3] = u[q].w;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) e[q] = 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t w[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) w[t] = __float_as_uint(e[16 * q + t]);
+            tmem_st16(tl + TS + 32 * half + 16 * q, w);
+          }
+          if (state_row) snap_half(snap, row, half, e);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (et == 0) mbar_arrive(&B->sready[sj % 2]);
+      if (et == 32) advance(sj, pc.nch > 1);  // chunk 0's state advance reads E in TMEM
+
+      for (int c = 0; c < pc.nch; ++c, ++oj, ++sj) {
+        if (c + 1 < pc.nch) {  // snapshot of the state after chunk c, for chunk c + 1
+          wait3(x, &B->sacc, nsa & 1);
+          ++nsa;
+          tc_fence_after();
+          if (state_warp) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tl + TS, r0);
+            tmem_ld32(tl + TS + 32, r1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B->tsread);  // the running state may advance again
+            uint8_t* sn = snap + ((c + 1) % 2) * SNAP;
+            if (quad < 2) {  // S^T rows
+              store_snap_half(sn, row, 0, reinterpret_cast<const float*>(r0));
+              store_snap_half(sn, row, 1, reinterpret_cast<const float*>(r1));
+            } else {  // z (lane 64 only) -> rows 64 (hi) and 65 (lo), split by the whole warp
+              if (lane == 0) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  B->zbuf[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
+                                           __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
+                  B->zbuf[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
+                                               __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
+                }
+              }
+              __syncwarp();
+              const float2 zz = reinterpret_cast<const float2*>(B->zbuf)[lane];  // z[2 lane], z[2 lane + 1]
+              const uint32_t hi = pack_bf16x2(zz.x, zz.y);
+              const uint32_t lo = pack_bf16x2(zz.x - __uint_as_float(hi << 16), zz.y - __uint_as_float(hi & 0xFFFF0000u));
+              *reinterpret_cast<uint32_t*>(sn + sw128_offset(64, lane / 4) + (lane % 4) * 4) = hi;
+              *reinterpret_cast<uint32_t*>(sn + sw128_offset(65, lane / 4) + (lane % 4) * 4) = lo;
+              __syncwarp();  // zbuf is rewritten by the next snapshot
+            }
+          } else if (et == 32) {
+            if (wait3(x, &B->tsread, ntr & 1)) advance(sj + 1, c + 2 < pc.nch);
+          }
+          ++ntr;
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (et == 0) mbar_arrive(&B->sready[(sj + 1) % 2]);
+        }
+        // o = num / (den + eps), staged in shared memory, stored by TMA
+        const int ob = oj % 2;
+        wait3(x, &B->oready[ob], (oj / 2) & 1);
+        tc_fence_after();
+        const uint32_t base = tl + TO + 80 * ob;
+        uint32_t n0[32], n1[32], d2[2];
+        tmem_ld32(base, n0);
+        tmem_ld32(base + 32, n1);
+        tmem_ld2(base + D, d2);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B->ofree[ob]);
+        const float inv = 1.f / (__uint_as_float(d2[0]) + __uint_as_float(d2[1]) + p.eps);
+        if (et == 32) bulk_wait_read_all();  // the previous chunk's store has read the staging
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<float4*>(out + sw128_offset(row, cc)) =
+              make_float4(__uint_as_float(n0[4 * cc]) * inv, __uint_as_float(n0[4 * cc + 1]) * inv,
+                          __uint_as_float(n0[4 * cc + 2]) * inv, __uint_as_float(n0[4 * cc + 3]) * inv);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<float4*>(out + BLK + sw128_offset(row, cc)) =
+              make_float4(__uint_as_float(n1[4 * cc]) * inv, __uint_as_float(n1[4 * cc + 1]) * inv,
+                          __uint_as_float(n1[4 * cc + 2]) * inv, __uint_as_float(n1[4 * cc + 3]) * inv);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (et == 32 && !*x.abort) {
+          const int tok = pc.tok0 + c * C;
+          tma_store_3d(&tm_o, out, 0, tok, pc.h);
+          tma_store_3d(&tm_o, out + BLK, 32, tok, pc.h);
+          bulk_commit();
+        }
+      }
+    }
+    if (et == 32) bulk_wait_all();
+    if (et == 32 && *x.abort) {  // the state advances in flight end before TMEM is freed
+      int never = 0;
+      mma_commit(&B->drain2);
+      mbar_wait(&B->drain2, 0, globaltimer_ns() + mbar_ns, &never);
+    }
+  }
+  drain_and_free(x, warp, kCols);
+}
+
+}  // namespace k3
+
+Split make_split(int BH, int N, int sms) {
+  Split s;
+  s.BH = BH;
+  s.N = N;
+  s.NC = (N + C - 1) / C;
+  const long long tc = (long long)BH * s.NC;
+  s.G = (int)(tc < sms ? tc : sms);
+  // Runs are L = floor(TC / G) or L + 1 chunks long; a head's NC chunks meet at
+  // most ceil(NC / L) + 1 of them (every run but the first and last lies inside).
+  const long long L = tc / s.G;
+  s.MPH = (int)((s.NC + L - 1) / L) + 1;
+  return s;
+}
+
+// SMs of the current device (152 on a GB300 when no device is visible, so
+// that host-only queries of the workspace size still answer).
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return sms;
+}
+
+}  // namespace
+
+// agg and E slots, then phi(K)
+size_t prefill_chunked64_workspace_bytes(int B, int H, int N) {
+  const Split s = make_split(B * H, N, sm_count());
+  return 2 * (size_t)s.BH * s.MPH * SZ * sizeof(float) + (size_t)s.BH * N * D * sizeof(__nv_bfloat16);
+}
+
+cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mo, a.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C))
+    return cudaErrorInvalidValue;
+  Params3 p;
+  p.sp = make_split(BH, a.N, sms);
+  p.eps = a.eps;
+  p.S0 = a.S0;
+  p.z0 = a.z0;
+  p.S_N = a.S_N;
+  p.z_N = a.z_N;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  const size_t slots = (size_t)BH * p.sp.MPH;
+  if (sizeof(WsHeader) + prefill_chunked64_workspace_bytes(a.B, a.H, a.N) > a.ws_bytes)
+    return cudaErrorInvalidValue;
+  p.agg = reinterpret_cast<float*>(ws + sizeof(WsHeader));
+  p.E = p.agg + slots * SZ;
+  p.phik = reinterpret_cast<__nv_bfloat16*>(p.E + slots * SZ);
+  CUtensorMap mphik;
+  if (!make_map(&mphik, p.phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C))
+    return cudaErrorInvalidValue;
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+
+  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)k1::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k3::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)k3::SMEM);
+  if (e != cudaSuccess) return e;
+  k1::aggregate_kernel<<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mphik, p, mbar_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k2::scan_kernel<<<dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH), k2::kThreads, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k3::output_kernel<<<p.sp.G, 32 * k3::kWarps, k3::SMEM, stream>>>(mq, mphik, mv, mo, p, mbar_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace la

@@ -40,7 +40,6 @@
 
 namespace la {
 
-cudaError_t launch_prefill_tc64(const PrefillArgs& a, cudaStream_t stream);  // prefill_tc64.cu
 
 namespace {
 
@@ -675,11 +674,12 @@ bool prefill_tc_supported(const PrefillArgs& a) {
 }
 
 size_t prefill_tc_workspace_bytes(int B, int H, int N, int d, int /*chunk*/) {
+  if (d == 64) return prefill_chunked64_workspace_bytes(B, H, N);
   return workspace_bytes(B, H, N, d);
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
-  if (a.dk == 64) return launch_prefill_tc64(a, stream);
+  if (a.dk == 64) return launch_prefill_chunked64(a, stream);
   return launch_d<128>(a, stream);
 }
 

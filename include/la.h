@@ -138,8 +138,11 @@ la_status la_read_device_status(const void* workspace, cudaStream_t stream);
  * library holds until the process exits.
  *   Limit: requests whose la_prefill_workspace_bytes(...) exceeds 16 MiB
  *   (16777216 bytes) are rejected with LA_ERR_INVALID_ARG, as are arguments
- *   la_prefill rejects.  At dk = dv = 64 that is 504 items of 512 tokens
- *   (B*H*ceil(N/512) <= 504); at dk = dv = 128, 127 items.
+ *   la_prefill rejects.  At dk = dv = 64 the workspace is a bf16 copy of
+ *   phi(K) (128 bytes per token) plus two 16.6 KB state slots per pair of
+ *   head and block that meet: 8 heads of 4096 tokens fit (13 MB on a 152-SM
+ *   GPU), 32 heads of 4096 do not; at dk = dv = 128, 127 items of 512 tokens
+ *   (B*H*ceil(N/512) <= 127).  la_prefill_workspace_bytes gives the figure.
  *   Set-up: the first call on each device (with that device current) looks up
  *   the array's device address and zero-fills it synchronously; make that
  *   first call before any stream capture.

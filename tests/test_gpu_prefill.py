@@ -225,20 +225,24 @@ def test_device_status_clean_after_calls(la):
     assert la.read_device_status(ws) == 0  # LA_OK
 
 
-def test_bounded_wait_reports_timeout(la, orc, monkeypatch):
-    # A test hook makes every head's first item wait on a flag that nothing
-    # sets, with a 2 ms limit: the wait gives up, the kernel finishes, the
-    # status word says LA_ERR_TIMEOUT, and the context stays usable.
-    q, k, v = _gen(1, 2, 1024, 64, 64, torch.bfloat16, seed=25)
-    ws = torch.zeros(la.prefill_workspace_bytes(1, 2, 1024, 64, 64), dtype=torch.uint8,
+@pytest.mark.parametrize("d,limit_env", [(64, "LA_MBAR_TIMEOUT_NS"), (128, "LA_WAIT_TIMEOUT_NS")],
+                         ids=["chunked_d64", "lookback_d128"])
+def test_bounded_wait_reports_timeout(la, orc, monkeypatch, d, limit_env):
+    # A test hook makes one wait of the kernel wait on something that nothing
+    # completes (d = 64: an mbarrier of the output kernel; d = 128: an
+    # inter-block flag of the look-back), with a 2 ms limit: the wait gives up,
+    # the kernel drains what it started and finishes, the status word says
+    # LA_ERR_TIMEOUT, and the context stays usable.
+    q, k, v = _gen(1, 2, 1024, d, d, torch.bfloat16, seed=25)
+    ws = torch.zeros(la.prefill_workspace_bytes(1, 2, 1024, d, d), dtype=torch.uint8,
                      device="cuda")
     monkeypatch.setenv("LA_TEST_FORCE_WAIT", "1")
-    monkeypatch.setenv("LA_WAIT_TIMEOUT_NS", "2000000")
+    monkeypatch.setenv(limit_env, "2000000")
     la.prefill(q.cuda(), k.cuda(), v.cuda(), ws=ws)
     assert la.read_device_status(ws) == 4  # LA_ERR_TIMEOUT
     assert la.read_device_status(ws) == 0  # reading clears it
     monkeypatch.delenv("LA_TEST_FORCE_WAIT")
-    monkeypatch.delenv("LA_WAIT_TIMEOUT_NS")
+    monkeypatch.delenv(limit_env)
     o, S, z = la.prefill(q.cuda(), k.cuda(), v.cuda(), ws=ws)
     assert la.read_device_status(ws) == 0
     ro, rS, rz = orc.la_recurrent(f64(q), f64(k), f64(v))
