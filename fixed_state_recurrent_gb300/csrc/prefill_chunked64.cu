@@ -151,30 +151,28 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, uint32_t issued, uns
     mbar_wait(&full[q % NS_], (q / NS_) & 1, dl, &never);
 }
 
+// 2^x by the single-precision hardware approximation, subnormal results
+// flushed to zero (exp(u) < 2^-126 is far below what bf16 sums of phi keep).
+__device__ __forceinline__ float exp2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // phi on two bf16: phi(u) = exp(min(u, 0)) + max(u, 0), which is u + 1 for
-// u > 0 and exp(u) otherwise.  min and max are taken on the bf16 pair; the two
-// exponentials are one paired half-precision 2^x (ex2.approx.f16x2, relative
-// error about 2^-9.9) of min(u, 0) log2(e), the argument formed in fp32 and
-// rounded to f16 (absolute error |x| 2^-11, below 0.003 for |u| < 4); the sum
-// is rounded to bf16 (relative error 2^-9), the precision of the tensor-core
-// operand it feeds.
+// u > 0 and exp(u) otherwise.  min and max are taken on the bf16 pair, the
+// exponentials as 2^(min(u, 0) log2 e) in fp32, and the sum is rounded to
+// bf16, the precision of the tensor-core operand it feeds: the result is
+// within one bf16 rounding of phi(u).
 __device__ __forceinline__ uint32_t phi2(uint32_t x) {
   const __nv_bfloat162 u = *reinterpret_cast<const __nv_bfloat162*>(&x);
   const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
   const __nv_bfloat162 m = __hmin2(u, zero);
   const __nv_bfloat162 M = __hmax2(u, zero);
   const uint32_t mb = *reinterpret_cast<const uint32_t*>(&m);
-  const float xa = __uint_as_float(mb << 16) * 1.4426950408889634f;
-  const float xb = __uint_as_float(mb & 0xFFFF0000u) * 1.4426950408889634f;
-  uint32_t h, e;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(xb), "f"(xa));
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
-  float ea, eb;
-  asm("{.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;}"
-      : "=f"(ea), "=f"(eb)
-      : "r"(e));
-  const uint32_t eb2 = pack_bf16x2(ea, eb);
-  const __nv_bfloat162 r = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&eb2), M);
+  const uint32_t e = pack_bf16x2(exp2_ftz(__uint_as_float(mb << 16) * 1.4426950408889634f),
+                                 exp2_ftz(__uint_as_float(mb & 0xFFFF0000u) * 1.4426950408889634f));
+  const __nv_bfloat162 r = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&e), M);
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
@@ -271,7 +269,7 @@ __device__ __forceinline__ void drain_and_free(const Ctx3& x, int warp, uint32_t
 
 namespace k1 {
 
-constexpr int NS = 4;
+constexpr int NS = 6;  // K, V stages: enough to cover a load from HBM, phi and the MMA
 constexpr uint32_t STAGE = 2 * BLK;  // K | V
 constexpr uint32_t OFF_ONES = NS * STAGE;
 constexpr uint32_t OFF_BAR = OFF_ONES + BLK;
@@ -326,6 +324,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   const Ctx3 x{&p, smem, reinterpret_cast<uint64_t*>(B), &B->abort,
                *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
   const Run run(p.sp, blockIdx.x);
+  pdl_launch_dependents();  // the scan may be scheduled now; it waits for this grid's results
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer: K, V chunk tiles
@@ -448,6 +447,8 @@ namespace k2 {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) scan_kernel(const Params3 p) {
+  pdl_launch_dependents();  // the output kernel may be scheduled now
+  pdl_wait();               // the aggregates of the aggregate kernel are complete
   const int e = blockIdx.x * kThreads + threadIdx.x;  // slot element: row * 64 + i
   const int h = blockIdx.y;
   if (e >= SZ) return;
@@ -496,9 +497,10 @@ constexpr uint32_t OFF_BAR = OFF_OUT + 2 * BLK;
 constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 static_assert(OFF_OUT % 1024 == 0, "swizzled staging alignment");
-// 0 TMA, 1 MMA, 2-5 phi(Q), 6-9 P, 10-13 state/output epilogue: at most four
-// warps per SM sub-partition, so 128 registers per thread
-constexpr int kWarps = 14;
+// 0 TMA, 1 MMA, 2-5 phi(Q), 6-9 P, 10-13 output epilogue (10, 12, 13 also
+// write the state snapshots), 14 state chain: at most four warps per SM
+// sub-partition, so 128 registers per thread
+constexpr int kWarps = 15;
 constexpr uint32_t kCols = 512;
 constexpr uint32_t TA = 0;    // A[b]: scores, then P (packed bf16) -- cols 128 b
 constexpr uint32_t TO = 256;  // O[ob]: 64 numerator + 16 denominator cols -- 256 + 80 ob
@@ -516,10 +518,13 @@ struct Bars {
   uint64_t sready[2];  // chunk j's snapshot written, in [j % 2] (epilogue -> MMA): two,
                        // as the snapshots may run one chunk ahead of the MMA warp
   uint64_t tsread;     // the running state read out of TMEM   (state warps -> state MMA)
+
   uint64_t drain, drain2;
   uint64_t never;      // completed by nothing (the forced-timeout test hook)
   uint32_t tmem_slot;
   int abort;
+  unsigned epieces;    // entry states stored in TMEM so far, times 3 (state warps -> state MMA):
+                       // a counter, as the state warps may run pieces ahead of the state MMA
   float4 zbuf[16];     // z, handed from its TMEM lane to the whole warp
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
@@ -528,12 +533,13 @@ __device__ __forceinline__ uint8_t* stage_ptr(uint8_t* smem, uint32_t s) { retur
 
 // Two threads issue MMAs.  The MMA warp issues, per chunk a, the scores of
 // chunk a + 1 and then P [V | 1] and phi(Q) [S | z] of chunk a, so that P of
-// chunk a + 1 is built while the products of chunk a run.  The state chain is
-// issued by one thread of the snapshot warps: the advance S += [V | 1]^T
-// phi(K) of chunk a goes out as soon as the snapshot of the state before chunk
-// a has been read out of TMEM, and does not queue behind the output products.
-// A stage is released by both issuers (a commit each, or an arrival where no
-// state advance reads it).
+// chunk a + 1 is built while the products of chunk a run.  The state chain has
+// a warp of its own: the advance S += [V | 1]^T phi(K) of chunk a goes out as
+// soon as the snapshot of the state before chunk a has been read out of TMEM.
+// The three warps that hold state lanes publish each snapshot through
+// mbarriers (three arrivals), never waiting for the issuers.  A stage is
+// released by both issuers (a commit each, or an arrival where no state
+// advance reads it).
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -557,8 +563,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(&B->ofree[b], 4);
     }
     mbar_init(&B->sacc, 1);
-    mbar_init(&B->sready[0], 1);
-    mbar_init(&B->sready[1], 1);
+    mbar_init(&B->sready[0], 3);
+    mbar_init(&B->sready[1], 3);
+    B->epieces = 0;
     mbar_init(&B->drain, 1);
     mbar_init(&B->drain2, 1);
     mbar_init(&B->tsread, 3);
@@ -597,8 +604,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const int tok = pc.tok0 + c * C;
           mbar_arrive_expect_tx(&B->full[s], 3 * BLK);
           tma_load_3d(st, &tm_q, 0, tok, pc.h, &B->full[s]);
-          tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
           tma_load_3d(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
+          if (sj == 0) pdl_wait();  // phi(K) is the aggregate kernel's output
+          tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
           ++issued;
         }
       if (*x.abort) drain_loads<NS>(B->full, issued, mbar_ns);
@@ -731,37 +739,14 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         __syncwarp();
         if (lane == 0) mbar_arrive(&B->pready[b]);
       }
-  } else {  // ---- state snapshots and output epilogue
+  } else if (warp < 14) {  // ---- state snapshots (state lanes only) and output epilogue
     const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 320;
     const bool state_warp = quad <= 2, state_row = row <= D;
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
     uint8_t* snap = smem + OFF_SNAP;
     uint8_t* out = smem + OFF_OUT;
-    uint32_t oj = 0, nsa = 0, sj = 0, ntr = 0;
-    const uint32_t aOnes = smem_u32(smem + OFF_ONES);
-    // Thread et == 32 (in the warp that holds no state rows): the state advance
-    // of global chunk j, S += [V | 1]^T phi(K) (its stage loaded; the running
-    // state read), or, for a piece's last chunk, which has none, just its share
-    // of the stage's release.
-    auto advance = [&](uint32_t j, bool any) {
-      const int s = j % NS;
-      // Chunk j is loaded, so its stage's previous use has been released and
-      // the release below counts for chunk j (an earlier arrival would count
-      // for the previous use, and the stage could be refilled while read).
-      if (!wait3(x, &B->full[s], (j / NS) & 1)) return;
-      if (!any) {
-        mbar_arrive(&B->empty[s]);
-        return;
-      }
-      tc_fence_after();
-      const uint32_t st = smem_u32(stage_ptr(smem, s)), vt = st + 2 * BLK;
-#pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks)
-        mma_bf16_ss(x.tmem + TS, sdesc_sw128(vt + ks * 2048, aOnes - vt, 1024),
-                    sdesc_sw128(st + BLK + ks * 2048, BLK, 1024), ID_DS, 1u);
-      mma_commit(&B->sacc);
-      mma_commit(&B->empty[s]);
-    };
+    uint32_t oj = 0, nsa = 0, sj = 0;
+    pdl_wait();  // the entry states E are the scan kernel's output
     Piece pc;
     for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
       // The piece's entry state E: into TMEM (running state) and snapshot 0.
@@ -794,55 +779,51 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (state_row) snap_half(snap, row, half, e);
         }
         tmem_st_wait();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          red_add_release_cta(&B->epieces, 1u);
+          mbar_arrive(&B->sready[sj % 2]);
+        }
       }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (et == 0) mbar_arrive(&B->sready[sj % 2]);
-      if (et == 32) advance(sj, pc.nch > 1);  // chunk 0's state advance reads E in TMEM
 
       for (int c = 0; c < pc.nch; ++c, ++oj, ++sj) {
-        if (c + 1 < pc.nch) {  // snapshot of the state after chunk c, for chunk c + 1
+        if (c + 1 < pc.nch && state_warp) {  // snapshot of the state after chunk c, for chunk c + 1
           wait3(x, &B->sacc, nsa & 1);
           ++nsa;
           tc_fence_after();
-          if (state_warp) {
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tl + TS, r0);
-            tmem_ld32(tl + TS + 32, r1);
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B->tsread);  // the running state may advance again
-            uint8_t* sn = snap + ((c + 1) % 2) * SNAP;
-            if (quad < 2) {  // S^T rows
-              store_snap_half(sn, row, 0, reinterpret_cast<const float*>(r0));
-              store_snap_half(sn, row, 1, reinterpret_cast<const float*>(r1));
-            } else {  // z (lane 64 only) -> rows 64 (hi) and 65 (lo), split by the whole warp
-              if (lane == 0) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tl + TS, r0);
+          tmem_ld32(tl + TS + 32, r1);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B->tsread);  // the running state may advance again
+          uint8_t* sn = snap + ((c + 1) % 2) * SNAP;
+          if (quad < 2) {  // S^T rows
+            store_snap_half(sn, row, 0, reinterpret_cast<const float*>(r0));
+            store_snap_half(sn, row, 1, reinterpret_cast<const float*>(r1));
+          } else {  // z (lane 64 only) -> rows 64 (hi) and 65 (lo), split by the whole warp
+            if (lane == 0) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  B->zbuf[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
-                                           __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
-                  B->zbuf[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
-                                               __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
-                }
+              for (int q = 0; q < 8; ++q) {
+                B->zbuf[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
+                                         __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
+                B->zbuf[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
+                                             __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
               }
-              __syncwarp();
-              const float2 zz = reinterpret_cast<const float2*>(B->zbuf)[lane];  // z[2 lane], z[2 lane + 1]
-              const uint32_t hi = pack_bf16x2(zz.x, zz.y);
-              const uint32_t lo = pack_bf16x2(zz.x - __uint_as_float(hi << 16), zz.y - __uint_as_float(hi & 0xFFFF0000u));
-              *reinterpret_cast<uint32_t*>(sn + sw128_offset(64, lane / 4) + (lane % 4) * 4) = hi;
-              *reinterpret_cast<uint32_t*>(sn + sw128_offset(65, lane / 4) + (lane % 4) * 4) = lo;
-              __syncwarp();  // zbuf is rewritten by the next snapshot
             }
-          } else if (et == 32) {
-            if (wait3(x, &B->tsread, ntr & 1)) advance(sj + 1, c + 2 < pc.nch);
+            __syncwarp();
+            const float2 zz = reinterpret_cast<const float2*>(B->zbuf)[lane];  // z[2 lane], z[2 lane + 1]
+            const uint32_t hi = pack_bf16x2(zz.x, zz.y);
+            const uint32_t lo = pack_bf16x2(zz.x - __uint_as_float(hi << 16), zz.y - __uint_as_float(hi & 0xFFFF0000u));
+            *reinterpret_cast<uint32_t*>(sn + sw128_offset(64, lane / 4) + (lane % 4) * 4) = hi;
+            *reinterpret_cast<uint32_t*>(sn + sw128_offset(65, lane / 4) + (lane % 4) * 4) = lo;
           }
-          ++ntr;
           fence_proxy_async_smem();
-          named_bar_sync(1, 128);
-          if (et == 0) mbar_arrive(&B->sready[(sj + 1) % 2]);
+          __syncwarp();  // (also: zbuf is rewritten only by the next snapshot)
+          if (lane == 0) mbar_arrive(&B->sready[(sj + 1) % 2]);
         }
         // o = num / (den + eps), staged in shared memory, stored by TMA
         const int ob = oj % 2;
@@ -881,11 +862,64 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
     }
     if (et == 32) bulk_wait_all();
-    if (et == 32 && *x.abort) {  // the state advances in flight end before TMEM is freed
-      int never = 0;
-      mma_commit(&B->drain2);
-      mbar_wait(&B->drain2, 0, globaltimer_ns() + mbar_ns, &never);
+  } else {  // ---- the state chain: S += [V | 1]^T phi(K), chunk by chunk (one thread)
+    if (lane == 0) {
+      const uint32_t aOnes = smem_u32(smem + OFF_ONES);
+      // The advance of global chunk j (its stage loaded; the running state
+      // read), or, for a piece's last chunk, which has none, just this
+      // issuer's share of the stage's release.  Chunk j is loaded, so its
+      // stage's previous use has been released and the release counts for
+      // chunk j (an earlier arrival would count for the previous use, and the
+      // stage could be refilled while read).
+      auto advance = [&](uint32_t j, bool any) {
+        const int s = j % NS;
+        if (!wait3(x, &B->full[s], (j / NS) & 1)) return false;
+        if (!any) {
+          mbar_arrive(&B->empty[s]);
+          return true;
+        }
+        tc_fence_after();
+        const uint32_t st = smem_u32(stage_ptr(smem, s)), vt = st + 2 * BLK;
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks)
+          mma_bf16_ss(x.tmem + TS, sdesc_sw128(vt + ks * 2048, aOnes - vt, 1024),
+                      sdesc_sw128(st + BLK + ks * 2048, BLK, 1024), ID_DS, 1u);
+        mma_commit(&B->sacc);
+        mma_commit(&B->empty[s]);
+        return true;
+      };
+      // piece i's entry state is in TMEM once the three state warps have
+      // counted it (bounded wait, like the mbarrier waits)
+      auto entry_stored = [&](int i) {
+        if (*x.abort) return false;
+        const uint64_t dl = globaltimer_ns() + mbar_ns;
+        while (ld_acquire_cta(&B->epieces) < 3u * (unsigned)(i + 1)) {
+          if (*x.abort) return false;
+          if (globaltimer_ns() > dl) {
+            *x.abort = 1;
+            atomicOr(&p.hdr->status, kStatusTimeout);
+            return false;
+          }
+        }
+        tc_fence_after();
+        return true;
+      };
+      uint32_t sj = 0, ntr = 0;
+      bool ok = true;
+      Piece pc;
+      for (int i = 0; ok && run.piece(p.sp, i, &pc); ++i) {
+        ok = entry_stored(i) && advance(sj, pc.nch > 1);  // chunk 0 reads E in TMEM
+        for (int c = 0; ok && c + 1 < pc.nch; ++c, ++ntr)
+          ok = wait3(x, &B->tsread, ntr & 1) && advance(sj + c + 1, c + 2 < pc.nch);
+        sj += pc.nch;
+      }
+      if (*x.abort) {  // the state advances in flight end before TMEM is freed
+        int never = 0;
+        mma_commit(&B->drain2);
+        mbar_wait(&B->drain2, 0, globaltimer_ns() + mbar_ns, &never);
+      }
     }
+    __syncwarp();
   }
   drain_and_free(x, warp, kCols);
 }
@@ -966,11 +1000,25 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   k1::aggregate_kernel<<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mphik, p, mbar_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k2::scan_kernel<<<dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH), k2::kThreads, 0, stream>>>(p);
-  e = cudaGetLastError();
+  // The scan and the output kernel are launched as programmatic dependents:
+  // their blocks may start while the kernel before them runs, and wait for
+  // its results (griddepcontrol.wait) only where they read them.
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
+  cfg.blockDim = dim3(k2::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, k2::scan_kernel, p);
   if (e != cudaSuccess) return e;
-  k3::output_kernel<<<p.sp.G, 32 * k3::kWarps, k3::SMEM, stream>>>(mq, mphik, mv, mo, p, mbar_ns);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * k3::kWarps);
+  cfg.dynamicSmemBytes = k3::SMEM;
+  return cudaLaunchKernelEx(&cfg, k3::output_kernel, mq, mphik, mv, mo, p, mbar_ns);
 }
 
 }  // namespace la

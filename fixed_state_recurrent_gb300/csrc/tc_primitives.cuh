@@ -104,6 +104,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0,
       : "memory");
 }
 
+// 3-D tiled prefetch of a box into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // 3-D tiled store from shared memory (bulk-group completion).  Coordinates
 // outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int c0, int c1,
@@ -291,6 +299,30 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 
 __device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Block-scope release add and acquire load on a shared-memory counter.
+__device__ __forceinline__ void red_add_release_cta(unsigned* p, unsigned v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_cta(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+// Programmatic dependent launch.  launch_dependents: this block no longer
+// holds back the launch of the next kernel in the stream (when every block of
+// this grid has said so or exited, the dependent grid may start).  wait: this
+// thread blocks until the grids it depends on have completed and their
+// memory operations are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32) with id `id` > 0.
