@@ -57,6 +57,9 @@ def _args():
                    help="headline workload only (no long/decode/delta/e2e/cpu)")
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run (long,decode,delta,pr1)")
+    p.add_argument("--profile", type=int, default=0, metavar="CALLS",
+                   help="run CALLS plain (non-graph) prefill calls of the headline workload on "
+                        "the same rotating buffer sets and exit: the command profilers run")
     return p.parse_args()
 
 
@@ -187,11 +190,16 @@ def _kernel_source_hash():
     return h.hexdigest()
 
 
+# Kernel launches per la_prefill call on the headline workload: the d = 64
+# tensor-core path runs the aggregate, scan and output kernels.
+PREFILL_LAUNCHES_PER_CALL = 3
+
+
 def _committed_traffic(tokens):
-    """dram bytes per launch of the prefill kernel from the committed ncu
-    summary, scaled to `tokens`, or None when the kernel source changed since
-    the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "prefill_tc_ncu.md")
+    """dram bytes of one la_prefill call (its three kernels) from the committed
+    ncu summary, scaled to `tokens`, or None when the kernel source changed
+    since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "prefill_d64_bf16_ncu.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
@@ -268,6 +276,27 @@ def bench_prefill(api, w, steps, warmup, rank, world, sets=4):
     if status != 0:
         raise RuntimeError(f"prefill kernel reported device status {status}")
     return total, [total / steps] * steps
+
+
+def profile_calls(api, w, calls, sets=4):
+    """`calls` plain la_prefill calls over the rotating buffer sets of
+    bench_prefill, launched one by one (no graph), for profilers."""
+    import torch
+    dev = torch.device("cuda")
+    bufs = []
+    for r in range(sets):
+        q, k, v = _device_inputs(w, w.seed + r, dev)
+        bufs.append((q, k, v, torch.empty((w.B, w.H, w.N, w.dv), device=dev),
+                     torch.empty((w.B, w.H, w.dk, w.dv), device=dev),
+                     torch.empty((w.B, w.H, w.dk), device=dev)))
+    ws = api.workspace(w.B, w.H, w.N, w.dk, w.dv, w.dtype, 0, dev)
+    for i in range(calls):
+        q, k, v, o, S, z = bufs[i % sets]
+        api.prefill(q, k, v, o=o, S_N=S, z_N=z, ws=ws)
+    torch.cuda.synchronize()
+    if api.read_device_status(ws) != 0:
+        raise RuntimeError("prefill kernel reported a nonzero device status")
+    print(f"profiled {calls} prefill calls", flush=True)
 
 
 def bench_decode(api, rank, world, reps=3):
@@ -488,6 +517,10 @@ def main():
     time.sleep(0.3)
 
     w = inputs.WORKLOADS["prefill"]
+    if args.profile:
+        profile_calls(api, w, args.profile)
+        sampler.stop()
+        return
     total_ms, per = bench_prefill(api, w, args.steps, args.warmup, rank, world)
     ms_step = total_ms / args.steps
     value = job_throughput(w.tokens, world, total_ms, args.steps)
@@ -540,7 +573,8 @@ def main():
                            "chunk": 128, "parallelism": f"replicas x{world}",
                            "l2": "4 rotating input/output buffer sets (~340 MB > 129 MB L2)"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps, "clocks": clocks, "extra": extra}
+                "gpu_launches": args.steps * PREFILL_LAUNCHES_PER_CALL, "clocks": clocks,
+                "extra": extra}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
