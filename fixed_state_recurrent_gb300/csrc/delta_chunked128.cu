@@ -1,0 +1,483 @@
+// delta_chunked128.cu -- the delta-rule memory on the sm_103a tensor cores,
+// chunkwise, for bf16 keys and values with dk = dv = 128.
+//
+// Recurrence (page "AIGC 基本功|线性、循环与记忆架构-LinearMem", section 03
+// "从累加改成纠错", and page "sequence-models" practice notes, "Delta-rule fast
+// weight"): read_t = S_{t-1}^T k_t, then S_t = S_{t-1} + beta_t k_t (v_t - read_t)^T.
+//
+// Chunkwise form (the LinearMem page names a chunked delta rule as the way to
+// train it fast; the steps below follow from the recurrence).  For a chunk of
+// C tokens with keys K [C x dk], values V [C x dv], beta, and the state S at
+// the chunk's start, let u_t = beta_t (v_t - read_t) and L = strictly lower
+// part of K K^T (L[t][s] = k_t . k_s for s < t).  Then
+//   read_t = S^T k_t + sum_{s<t} L[t][s] u_s,  i.e.  R = K S + L U,
+//   (I + diag(beta) L) U = diag(beta) (V - K S),  i.e.  U = T diag(beta) (V - K S)
+//   with T = (I + diag(beta) L)^-1 (unit lower triangular), and
+//   S_new = S + K^T U.
+// In exact arithmetic this equals the token recurrence; only the order of the
+// sums and the operand roundings differ.
+//
+// One block per head, chunks of C = 64 tokens taken in pairs (128 tokens per
+// TMA stage, so that the Gram matrix of a pair is one M = 128 product).  The
+// state and every product live transposed, TMEM lanes = value columns j:
+//   ST  S^T (fp32)                         SB  S^T as packed bf16 (A operand)
+//   KR  (K S)^T, then R^T = (K S + L U)^T  UU  U^T (fp32)
+//   XB  (V - K S)^T, packed bf16 (A operand)
+//   UB  U^T, packed bf16 (A operand)       LL  K2 K2^T of the pair (lanes = tokens)
+// Products per chunk (tcgen05, bf16 operands, fp32 accumulation):
+//   KR = SB  x K_c^T    (M 128, N 64, K 128)   UU = XB x (T_c B_c)^T (M 128, N 64, K 64)
+//   KR += UB x L_c^T    (M 128, N 64, K 64)    ST += UB x K_c        (M 128, N 128, K 64)
+// with B_c = diag(beta) folded into the T operand.  T is solved per chunk in
+// fp32 on CUDA cores from the Gram matrix: thread c of the chunk's 64 solves
+// column c of (I + diag(beta) L) t = e_c by forward substitution in axpy
+// order (all 64 threads read the same L column: shared-memory broadcasts).
+//
+// Schedule: the chunks form one dependent chain (SB -> KR -> XB -> UU -> UB ->
+// ST -> SB).  Off that chain run the TMA loads (one pair ahead), the Gram
+// product and T of the NEXT pair (its Gram is issued right after the current
+// pair's first K S product; T and L operand tiles are double-buffered by pair
+// parity), and the global stores of each chunk's reads (held in registers
+// while the next snapshot is packed).
+#include "prefill_tc_common.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+using namespace tcp;
+
+namespace dc {
+
+constexpr int D = 128;    // dk = dv
+constexpr int CH = 64;    // tokens per chunk
+constexpr int PT = 128;   // tokens per pair
+constexpr int NS = 2;     // pair stages
+constexpr uint32_t HALF = PT * 128;          // one 64-element column block of a pair tile: 16 KB
+constexpr uint32_t TILE = 2 * HALF;          // K or V of a pair: 32 KB
+constexpr uint32_t STAGE = 2 * TILE;         // K | V
+constexpr uint32_t CT = CH * 128;            // a [64 x 64] bf16 operand tile: 8 KB
+constexpr uint32_t OFF_T = NS * STAGE;       // (T B)_c tiles, [pair parity][chunk]
+constexpr uint32_t OFF_L = OFF_T + 4 * CT;   // L_c tiles, [pair parity][chunk]
+constexpr uint32_t OFF_LC = OFF_L + 4 * CT;  // fp32 L of both chunks, column-major (2 x 16 KB)
+constexpr uint32_t OFF_BETA = OFF_LC + 2 * CH * CH * 4;  // beta of the pair being solved
+constexpr uint32_t OFF_BAR = OFF_BETA + PT * 4;
+constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+static_assert(SMEM <= 227 * 1024, "shared memory per block");
+
+constexpr int kWarps = 10;  // 0 TMA, 1 MMA, 2-5 T builders, 6-9 state epilogue
+constexpr uint32_t kCols = 512;
+constexpr uint32_t ST = 0, LL = 128, KR = 256, UU = 320, SB = 384, XB = 448, UB = 480;
+
+constexpr uint32_t ID_LL = idesc_bf16_f32(128, 128, 0, 0);  // K2 K2^T
+constexpr uint32_t ID_KS = idesc_bf16_f32(128, CH, 0, 0);   // SB x K_c^T (B K-major)
+constexpr uint32_t ID_U = idesc_bf16_f32(128, CH, 0, 0);    // XB x (T B)_c^T (B K-major)
+constexpr uint32_t ID_R = idesc_bf16_f32(128, CH, 0, 0);    // UB x L_c^T (B K-major)
+constexpr uint32_t ID_S = idesc_bf16_f32(128, D, 0, 1);     // UB x K_c   (B MN-major)
+
+struct Params {
+  int BH, N;
+  const float* beta;
+  const float* S0;
+  float* reads;
+  float* S_N;
+  unsigned* status;
+};
+
+struct Bars {
+  uint64_t full[NS], empty[NS];
+  uint64_t lready;   // Gram product of a pair in LL        (MMA -> T)
+  uint64_t tready;   // T and L tiles of a pair              (T -> MMA)
+  uint64_t sbready;  // S^T packed into SB                  (epilogue -> MMA)
+  uint64_t krready;  // (K S)^T in KR                       (MMA -> epilogue)
+  uint64_t xready;   // X^T packed into XB                  (epilogue -> MMA)
+  uint64_t uready;   // U^T in UU                           (MMA -> epilogue)
+  uint64_t ubready;  // U^T packed into UB                  (epilogue -> MMA)
+  uint64_t rsready;  // R^T in KR, S^T advanced             (MMA -> epilogue)
+  uint64_t drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+struct Ctx {
+  const Params* p;
+  volatile int* abort;
+  unsigned long long ns;
+};
+
+__device__ __forceinline__ bool waitd(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  if (*x.abort) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity, globaltimer_ns() + x.ns, x.abort)) return true;
+  *x.abort = 1;
+  atomicOr(x.p->status, kStatusTimeout);
+  return false;
+}
+
+__device__ __forceinline__ bool waitd_warp(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xFFFFFFFFu, waitd(x, bar, parity));
+}
+
+// Element (row, col) of a 128-byte-swizzled bf16 tile with 64 elements per row.
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  return row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2;
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float f) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return *reinterpret_cast<const uint16_t*>(&b);
+}
+
+// Column c of T = (I + diag(beta) L)^-1 for one chunk: x_r = [r == c] -
+// beta_r sum_{k<r} L[r][k] x_k, accumulated in axpy order (y_r collects the
+// sum; x_k is final once every k' < k has been added).  lc is L column-major
+// (lc[k * 64 + r] = L[r][k], zero for r <= k), bs the chunk's beta.
+__device__ __forceinline__ void solve_column(const float* lc, const float* bs, int c, float (&y)[CH]) {
+#pragma unroll
+  for (int r = 0; r < CH; ++r) y[r] = 0.f;
+#pragma unroll
+  for (int k = 0; k < CH; ++k) {
+    const float xk = (k == c ? 1.f : 0.f) - bs[k] * y[k];
+    y[k] = xk;
+    // rows r > k; the 4-aligned group holding k + 1 starts at or below k,
+    // where L is zero, so whole float4 groups are safe
+#pragma unroll
+    for (int g = (k + 1) / 4; g < CH / 4; ++g) {
+      const float4 l4 = *reinterpret_cast<const float4*>(lc + k * CH + 4 * g);
+      y[4 * g + 0] = fmaf(l4.x, xk, y[4 * g + 0]);
+      y[4 * g + 1] = fmaf(l4.y, xk, y[4 * g + 1]);
+      y[4 * g + 2] = fmaf(l4.z, xk, y[4 * g + 2]);
+      y[4 * g + 3] = fmaf(l4.w, xk, y[4 * g + 3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(32 * kWarps, 1)
+delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const Params p, const unsigned long long mbar_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int head = blockIdx.x;
+  const int npairs = (p.N + PT - 1) / PT;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&B->full[s], 1);
+      mbar_init(&B->empty[s], 1);
+    }
+    mbar_init(&B->lready, 1);
+    mbar_init(&B->tready, 4);
+    mbar_init(&B->sbready, 4);
+    mbar_init(&B->krready, 1);
+    mbar_init(&B->xready, 4);
+    mbar_init(&B->uready, 1);
+    mbar_init(&B->ubready, 4);
+    mbar_init(&B->rsready, 1);
+    mbar_init(&B->drain, 1);
+    B->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&B->tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot);
+  const Ctx x{&p, &B->abort, mbar_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer: K and V of each pair (two 64-column halves each)
+      uint32_t issued = 0;
+      for (int pr = 0; pr < npairs; ++pr) {
+        const int s = pr % NS;
+        if (pr >= NS && !waitd(x, &B->empty[s], ((pr / NS) - 1) & 1)) break;
+        uint8_t* st = smem + s * STAGE;
+        mbar_arrive_expect_tx(&B->full[s], STAGE);
+        for (int h = 0; h < 2; ++h) {
+          tma_load_3d(st + h * HALF, &tm_k, 64 * h, pr * PT, head, &B->full[s]);
+          tma_load_3d(st + TILE + h * HALF, &tm_v, 64 * h, pr * PT, head, &B->full[s]);
+        }
+        ++issued;
+      }
+      if (*x.abort) {
+        int never = 0;
+        const uint64_t dl = globaltimer_ns() + mbar_ns;
+        for (uint32_t q = (issued > NS ? issued - NS : 0); q < issued; ++q)
+          mbar_wait(&B->full[q % NS], (q / NS) & 1, dl, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issue
+      // Gram product of pair pr: LL = K2 K2^T (A and B both the K tile, K-major).
+      auto gram = [&](int pr) -> bool {
+        const int s = pr % NS;
+        if (!waitd(x, &B->full[s], (pr / NS) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(smem + s * STAGE);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t a = kb + (ks / 4) * HALF + (ks % 4) * 32;
+          mma_bf16_ss(tmem + LL, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024), ID_LL, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&B->lready);
+        return true;
+      };
+      uint32_t nch = 0;  // chunks done
+      bool ok = npairs == 0 || gram(0);
+      for (int pr = 0; ok && pr < npairs; ++pr) {
+        const int s = pr % NS;
+        const uint32_t kb = smem_u32(smem + s * STAGE);
+        const uint32_t aT = smem_u32(smem + OFF_T + (pr & 1) * 2 * CT);
+        const uint32_t aL = smem_u32(smem + OFF_L + (pr & 1) * 2 * CT);
+        if (!(ok = waitd(x, &B->tready, pr & 1))) break;
+        for (int c = 0; ok && c < 2; ++c, ++nch) {
+          const uint32_t kc = kb + c * CT;  // the chunk's 64 rows inside each half
+          const uint32_t tc_ = aT + c * CT, lc = aL + c * CT;
+          if (!(ok = waitd(x, &B->sbready, nch & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)  // KR = SB x K_c^T
+            mma_bf16_ts(tmem + KR, tmem + SB + 8 * ks,
+                        sdesc_sw128(kc + (ks / 4) * HALF + (ks % 4) * 32, 16, 1024), ID_KS, ks > 0 ? 1u : 0u);
+          mma_commit(&B->krready);
+          // the next pair's Gram product runs while the epilogue builds X
+          if (c == 0 && pr + 1 < npairs && !(ok = gram(pr + 1))) break;
+          if (!(ok = waitd(x, &B->xready, nch & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < CH / 16; ++ks)  // UU = XB x (T B)_c^T
+            mma_bf16_ts(tmem + UU, tmem + XB + 8 * ks, sdesc_sw128(tc_ + ks * 32, 16, 1024), ID_U,
+                        ks > 0 ? 1u : 0u);
+          mma_commit(&B->uready);
+          if (!(ok = waitd(x, &B->ubready, nch & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < CH / 16; ++ks)  // KR += UB x L_c^T
+            mma_bf16_ts(tmem + KR, tmem + UB + 8 * ks, sdesc_sw128(lc + ks * 32, 16, 1024), ID_R, 1u);
+#pragma unroll
+          for (int ks = 0; ks < CH / 16; ++ks)  // ST += UB x K_c (K rows = tokens, B MN-major)
+            mma_bf16_ts(tmem + ST, tmem + UB + 8 * ks, sdesc_sw128(kc + ks * 2048, HALF, 1024), ID_S, 1u);
+          mma_commit(&B->rsready);
+        }
+        if (ok) mma_commit(&B->empty[s]);
+      }
+      if (*x.abort) {
+        int never = 0;
+        mma_commit(&B->drain);
+        mbar_wait(&B->drain, 0, globaltimer_ns() + mbar_ns, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {  // ---- T builders: L and (T B) operand tiles of each pair
+    // TMEM lane quadrant = warp % 4: warps 4, 5 hold pair tokens 0..63 (chunk 0),
+    // warps 2, 3 pair tokens 64..127 (chunk 1).  Thread ct of a chunk is Gram
+    // row ct while copying and T column ct while solving.
+    const int quad = warp % 4, c = quad >> 1, ct = 32 * (quad & 1) + lane;
+    const int bar_id = 2 + c;  // named barrier of the chunk's 64 threads
+    const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
+    float* lcol = reinterpret_cast<float*>(smem + OFF_LC) + c * CH * CH;
+    float* bs = reinterpret_cast<float*>(smem + OFF_BETA) + c * CH;
+    for (int pr = 0; pr < npairs; ++pr) {
+      // lready(pr) also covers the completion of every product of pair pr - 2,
+      // the last readers of this pair parity's T and L tiles.
+      const bool got = waitd(x, &B->lready, pr & 1);
+      // the chunk's threads agree (barriers follow); this also keeps the copy
+      // below from overwriting lcol and bs before every thread has solved
+      if (!named_bar_and(bar_id, 64, got)) continue;
+      tc_fence_after();
+      const int tok = pr * PT + c * CH + ct;
+      bs[ct] = tok < p.N ? p.beta[(size_t)head * p.N + tok] : 0.f;
+      uint8_t* ltile = smem + OFF_L + ((pr & 1) * 2 + c) * CT;
+      uint8_t* ttile = smem + OFF_T + ((pr & 1) * 2 + c) * CT;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t g[32];
+        tmem_ld32(tl + LL + 64 * c + 32 * h, g);
+        tmem_ld_wait();
+        float l[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          l[q] = (32 * h + q < ct) ? __uint_as_float(g[q]) : 0.f;
+          lcol[(32 * h + q) * CH + ct] = l[q];
+        }
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          uint4 w;
+          w.x = pack_bf16x2(l[8 * g8 + 0], l[8 * g8 + 1]);
+          w.y = pack_bf16x2(l[8 * g8 + 2], l[8 * g8 + 3]);
+          w.z = pack_bf16x2(l[8 * g8 + 4], l[8 * g8 + 5]);
+          w.w = pack_bf16x2(l[8 * g8 + 6], l[8 * g8 + 7]);
+          *reinterpret_cast<uint4*>(ltile + swz(ct, 32 * h + 8 * g8)) = w;
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(bar_id, 64);
+      float y[CH];
+      solve_column(lcol, bs, ct, y);
+      const float bc = bs[ct];
+#pragma unroll
+      for (int r = 0; r < CH; ++r)
+        *reinterpret_cast<uint16_t*>(ttile + swz(r, ct)) = bf16_bits(y[r] * bc);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B->tready);
+    }
+  } else {  // ---- state epilogue: lane j of S^T, one TMEM quadrant per warp
+    const int quad = warp % 4, j = 32 * quad + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
+    // S^T = S0^T
+    for (int h = 0; h < 8; ++h) {
+      uint32_t w[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        w[q] = __float_as_uint(p.S0 ? p.S0[((size_t)head * D + 16 * h + q) * D + j] : 0.f);
+      tmem_st16(tl + ST + 16 * h, w);
+    }
+    tmem_st_wait();
+    const uint32_t nchunks = 2u * (uint32_t)npairs;
+    float* reads_j = p.reads + (size_t)head * p.N * D + j;
+    for (uint32_t ch = 0; ch < nchunks; ++ch) {
+      const int pr = ch / 2, c = ch % 2;
+      const uint8_t* vt = smem + (pr % NS) * STAGE + TILE;
+      // reads of the previous chunk (R^T in KR) into registers, then the new
+      // snapshot SB = bf16(S^T); the reads go out while the chain moves on
+      uint32_t r[64];
+      if (ch > 0) {
+        waitd_warp(x, &B->rsready, (ch - 1) & 1);
+        tc_fence_after();
+        tmem_ld32(tl + KR, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(tl + KR + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+      }
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t f[32], w[16];
+        tmem_ld32(tl + ST + 32 * h, f);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) w[q] = pack_bf16x2(__uint_as_float(f[2 * q]), __uint_as_float(f[2 * q + 1]));
+        tmem_st16(tl + SB + 16 * h, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B->sbready);
+      if (ch > 0) {
+        const int t0 = (int)(ch - 1) * CH;
+#pragma unroll
+        for (int q = 0; q < 64; ++q)
+          if (t0 + q < p.N) reads_j[(size_t)(t0 + q) * D] = __uint_as_float(r[q]);
+      }
+      // X^T = V^T - (K S)^T, packed over token pairs
+      waitd_warp(x, &B->krready, ch & 1);
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t f[32], w[16];
+        tmem_ld32(tl + KR + 32 * h, f);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int t = 64 * c + 32 * h + 2 * q;  // pair token
+          const float v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+              vt + (j / 64) * HALF + swz(t, j % 64)));
+          const float v1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+              vt + (j / 64) * HALF + swz(t + 1, j % 64)));
+          w[q] = pack_bf16x2(v0 - __uint_as_float(f[2 * q]), v1 - __uint_as_float(f[2 * q + 1]));
+        }
+        tmem_st16(tl + XB + 16 * h, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B->xready);
+      // UB = bf16(U^T)
+      waitd_warp(x, &B->uready, ch & 1);
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t f[32], w[16];
+        tmem_ld32(tl + UU + 32 * h, f);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 16; ++q) w[q] = pack_bf16x2(__uint_as_float(f[2 * q]), __uint_as_float(f[2 * q + 1]));
+        tmem_st16(tl + UB + 16 * h, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B->ubready);
+    }
+    // the last chunk's reads and S_N = S^T transposed back
+    if (nchunks > 0) {
+      waitd_warp(x, &B->rsready, (nchunks - 1) & 1);
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t f[32];
+        tmem_ld32(tl + KR + 32 * h, f);
+        tmem_ld_wait();
+        const int t0 = (int)(nchunks - 1) * CH + 32 * h;
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          if (t0 + q < p.N) reads_j[(size_t)(t0 + q) * D] = __uint_as_float(f[q]);
+      }
+    }
+    for (int h = 0; h < 4; ++h) {
+      uint32_t f[32];
+      tmem_ld32(tl + ST + 32 * h, f);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 32; ++q) p.S_N[((size_t)head * D + 32 * h + q) * D + j] = __uint_as_float(f[q]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+// Bounded-wait timeouts of this kernel (delta_prefill has no workspace).
+__device__ unsigned g_delta_status;
+
+}  // namespace dc
+}  // namespace
+
+bool delta_chunked_supported(bool bf16, int dk, int dv) { return bf16 && dk == 128 && dv == 128; }
+
+cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, int B, int H,
+                                 int N, const float* S0, float* reads, float* S_N,
+                                 cudaStream_t stream) {
+  using namespace dc;
+  unsigned* status = nullptr;
+  cudaError_t se = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_delta_status);
+  if (se != cudaSuccess) return se;
+  const int BH = B * H;
+  CUtensorMap mk, mv;
+  if (!make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, PT) ||
+      !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, PT))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.BH = BH;
+  p.N = N;
+  p.beta = beta;
+  p.S0 = S0;
+  p.reads = reads;
+  p.S_N = S_N;
+  p.status = status;
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  cudaError_t e = cudaFuncSetAttribute(delta_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM);
+  if (e != cudaSuccess) return e;
+  delta_chunked_kernel<<<BH, 32 * kWarps, SMEM, stream>>>(mk, mv, p, mbar_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace la

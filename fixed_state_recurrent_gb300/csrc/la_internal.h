@@ -59,6 +59,12 @@ cudaError_t launch_decode_step(const void* q, const void* k, const void* v,
                                float eps, float* S, float* z, float* o,
                                cudaStream_t stream);
 
+// Tensor-core chunked delta rule (bf16, dk = dv = 128; delta_chunked128.cu).
+bool delta_chunked_supported(bool bf16, int dk, int dv);
+cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, int B, int H,
+                                 int N, const float* S0, float* reads, float* S_N,
+                                 cudaStream_t stream);
+
 cudaError_t launch_delta_prefill(const void* k, const void* v, bool bf16,
                                  const float* beta, int B, int H, int N,
                                  int dk, int dv, const float* S0, float* reads,

@@ -75,12 +75,22 @@ def test_exact_recall_basis_keys(la, dtype):
     reads, S = la.delta_prefill(k, v, beta)
     assert torch.equal(reads[0, 0, d:].cpu(), vals.float())
     assert torch.equal(S[0, 0].cpu(), vals.float())
-    # over an arbitrary old memory the overwrite is exact up to the fp32
-    # rounding of old + (new - old)
+    # over an arbitrary old memory the fp32 path overwrites exactly up to the
+    # fp32 rounding of old + (new - old)
     S0 = (torch.randn((1, 1, d, dv), generator=g) * 5).cuda()
     reads, S = la.delta_prefill(k, v, beta, S0=S0)
-    assert relmax(f64(reads[0, 0, d:]), f64(vals)) < 1e-6
-    assert relmax(f64(S[0, 0]), f64(vals)) < 1e-6
+    if dtype == torch.float32:
+        assert relmax(f64(reads[0, 0, d:]), f64(vals)) < 1e-6
+        assert relmax(f64(S[0, 0]), f64(vals)) < 1e-6
+        return
+    # the bf16 path gives the tensor cores a bf16 copy of the state: the write
+    # is S0 + bf16(v - bf16(S0)), off from v by at most 2^-9 (|S0| + |v - S0|),
+    # and the read rounds that state to bf16 once more, so the error is
+    # bounded by 2^-8 (max|S0| + max|v|) -- here the old memory is five times
+    # the values, so that bound exceeds 2% of the values' range
+    bound = 2.0 ** -8 * (S0.abs().max().item() + vals.float().abs().max().item())
+    assert np.abs(f64(reads[0, 0, d:]) - f64(vals)).max() <= bound
+    assert np.abs(f64(S[0, 0]) - f64(vals)).max() <= bound
 
 
 SMALL = [(1, 1, 1, 1, 1), (2, 3, 37, 5, 3), (1, 2, 100, 64, 64), (2, 1, 300, 128, 128),
@@ -104,6 +114,24 @@ def test_delta_small(la, orc, dtype, shape, with_state):
     tol = tol_for(dtype)
     assert relmax(f64(reads), rr) <= tol
     assert relmax(f64(S), rS) <= tol
+
+
+CHUNKED_N = [1, 63, 64, 65, 127, 128, 129, 200, 256, 385, 1000]
+
+
+@pytest.mark.parametrize("N", CHUNKED_N)
+def test_delta_chunked_ragged(la, orc, N):
+    # bf16 at dk = dv = 128 runs chunkwise (64-token chunks, processed in
+    # pairs): lengths that end inside a chunk, on a chunk edge and inside the
+    # second chunk of a pair, with a nonzero initial state
+    from fixed_state_recurrent_gb300 import inputs
+    k, v, beta = inputs.delta_inputs(1, 3, N, 128, 128, torch.bfloat16, seed=500 + N)
+    g = torch.Generator().manual_seed(N)
+    S0 = torch.randn((1, 3, 128, 128), generator=g) * 0.5
+    reads, S = la.delta_prefill(k.cuda(), v.cuda(), beta.cuda(), S0=S0.cuda())
+    rr, rS = orc.delta(f64(k), f64(v), f64(beta), S0=f64(S0))
+    assert relmax(f64(reads), rr) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
 
 
 def test_delta_in_place_alias_and_zero_length(la, orc):
