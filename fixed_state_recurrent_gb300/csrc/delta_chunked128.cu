@@ -27,10 +27,16 @@
 // Products per chunk (tcgen05, bf16 operands, fp32 accumulation):
 //   KR = SB  x K_c^T    (M 128, N 64, K 128)   UU = XB x (T_c B_c)^T (M 128, N 64, K 64)
 //   KR += UB x L_c^T    (M 128, N 64, K 64)    ST += UB x K_c        (M 128, N 128, K 64)
-// with B_c = diag(beta) folded into the T operand.  T is solved per chunk in
-// fp32 on CUDA cores from the Gram matrix: thread c of the chunk's 64 solves
-// column c of (I + diag(beta) L) t = e_c by forward substitution in axpy
-// order (all 64 threads read the same L column: shared-memory broadcasts).
+// with B_c = diag(beta) folded into the T operand.  T is computed per chunk
+// by 64 threads from A = diag(beta) L (fp32, in shared memory) by block
+// recursion: the four 16 x 16 diagonal blocks of (I + A)^-1 by forward
+// substitution on CUDA cores, then the off-diagonal blocks from
+//   T_ij = -T_ii A_ij T_jj      (lower block row i over block column j)
+// first at 16 x 16 and then at 32 x 32 granularity, as small products on the
+// warp-level tensor-core instruction (tf32 operands, fp32 accumulation).  A
+// column-per-thread substitution over all 64 rows would have every thread
+// load the whole of A from shared memory; the products take their operands
+// from registers instead.
 //
 // Schedule: the chunks form one dependent chain (SB -> KR -> XB -> UU -> UB ->
 // ST -> SB).  Off that chain run the TMA loads (one pair ahead), the Gram
@@ -58,8 +64,8 @@ constexpr uint32_t STAGE = 2 * TILE;         // K | V
 constexpr uint32_t CT = CH * 128;            // a [64 x 64] bf16 operand tile: 8 KB
 constexpr uint32_t OFF_T = NS * STAGE;       // (T B)_c tiles, [pair parity][chunk]
 constexpr uint32_t OFF_L = OFF_T + 4 * CT;   // L_c tiles, [pair parity][chunk]
-constexpr uint32_t OFF_LC = OFF_L + 4 * CT;  // fp32 L of both chunks, column-major (2 x 16 KB)
-constexpr uint32_t OFF_BETA = OFF_LC + 2 * CH * CH * 4;  // beta of the pair being solved
+constexpr uint32_t OFF_LC = OFF_L + 4 * CT;  // fp32 A, then T, of both chunks (2 x 16 KB)
+constexpr uint32_t OFF_BETA = OFF_LC + 2 * CH * CH * 4;  // beta of the chunks being solved
 constexpr uint32_t OFF_BAR = OFF_BETA + PT * 4;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
@@ -127,27 +133,181 @@ __device__ __forceinline__ uint16_t bf16_bits(float f) {
   return *reinterpret_cast<const uint16_t*>(&b);
 }
 
-// Column c of T = (I + diag(beta) L)^-1 for one chunk: x_r = [r == c] -
-// beta_r sum_{k<r} L[r][k] x_k, accumulated in axpy order (y_r collects the
-// sum; x_k is final once every k' < k has been added).  lc is L column-major
-// (lc[k * 64 + r] = L[r][k], zero for r <= k), bs the chunk's beta.
-__device__ __forceinline__ void solve_column(const float* lc, const float* bs, int c, float (&y)[CH]) {
+// ---- T = (I + A)^-1 of one chunk, A strictly lower 64 x 64 ----------------
+// Scratch layout: fp32 row-major, 64 floats per row, 4-float groups permuted
+// per row (column c of row r sits at c ^ sw(r)) so that row-wise 16-byte
+// stores, column-wise loads and the mma fragment loads below all spread over
+// the 32 banks.
+__device__ __forceinline__ int sw(int r) { return ((r & 3) << 3) | (((r >> 2) & 1) << 2); }
+__device__ __forceinline__ int sidx(int r, int c) { return r * CH + (c ^ sw(r)); }
+
+__device__ __forceinline__ uint32_t to_tf32(float f) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+  return r;
+}
+
+// d += a b for one 16 x 8 x 8 tile (warp-level; tf32 operands, fp32 accumulate)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Fragment of the 16 x 8 left operand whose (m, k) is scratch[r0 + m][k0 + k]:
+// lane (g = lane / 4, t = lane % 4) holds (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4).
+__device__ __forceinline__ void frag_a(const float* s, int r0, int k0, int lane, uint32_t (&a)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+  a[0] = to_tf32(s[sidx(r0 + g, k0 + t)]);
+  a[1] = to_tf32(s[sidx(r0 + g + 8, k0 + t)]);
+  a[2] = to_tf32(s[sidx(r0 + g, k0 + t + 4)]);
+  a[3] = to_tf32(s[sidx(r0 + g + 8, k0 + t + 4)]);
+}
+
+// Fragment of the 8 x 8 right operand whose (k, n) is scratch[k0 + k][n0 + n]:
+// lane holds (t, g) and (t + 4, g).
+__device__ __forceinline__ void frag_b(const float* s, int k0, int n0, int lane, uint32_t (&b)[2]) {
+  const int g = lane >> 2, t = lane & 3;
+  b[0] = to_tf32(s[sidx(k0 + t, n0 + g)]);
+  b[1] = to_tf32(s[sidx(k0 + t + 4, n0 + g)]);
+}
+
+// scratch[r0 + m][n0 + n] = scale * d(m, n); lane holds (g, 2t), (g, 2t + 1),
+// (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ void store_d(float* s, int r0, int n0, int lane, const float (&d)[4], float scale) {
+  const int g = lane >> 2, t = lane & 3;
+  *reinterpret_cast<float2*>(s + sidx(r0 + g, n0 + 2 * t)) = make_float2(scale * d[0], scale * d[1]);
+  *reinterpret_cast<float2*>(s + sidx(r0 + g + 8, n0 + 2 * t)) = make_float2(scale * d[2], scale * d[3]);
+}
+
+// (T diag(beta))[r][c0], [r][c0 + 1] as one packed bf16 pair of the operand tile
+__device__ __forceinline__ void store_tb_pair(uint8_t* ttile, int r, int c0, float v0, float v1) {
+  *reinterpret_cast<uint32_t*>(ttile + swz(r, c0)) = pack_bf16x2(v0, v1);
+}
+
+// Fragment tile (16 x 8 at rows r0, cols n0) of T, scaled by -1, into the bf16
+// (T diag(beta)) operand tile; bs = beta of the chunk's tokens.
+__device__ __forceinline__ void store_tb_tile(uint8_t* ttile, const float* bs, int r0, int n0, int lane,
+                                              const float (&d)[4]) {
+  const int g = lane >> 2, t = lane & 3, c = n0 + 2 * t;
+  const float b0 = bs[c], b1 = bs[c + 1];
+  store_tb_pair(ttile, r0 + g, c, -d[0] * b0, -d[1] * b1);
+  store_tb_pair(ttile, r0 + g + 8, c, -d[2] * b0, -d[3] * b1);
+}
+
+// T = (I + A)^-1 for one chunk, and the bf16 operand tile T diag(beta).  The
+// scratch holds A (strictly lower, zero elsewhere) on entry; the blocks of T
+// that later steps read replace the blocks of A they no longer need, and the
+// strict-upper blocks take the intermediate products.  64 threads (two
+// warps) of one chunk, tid in [0, 64).  The strictly upper 16 x 16 blocks of
+// the bf16 tile are not written (they are zero from the start).  Within each
+// step every load comes before every store: the scratch is read and written
+// through the same array, so the compiler keeps their program order.
+__device__ __forceinline__ void solve_t(float* S, const float* bs, uint8_t* ttile, int tid, int bar_id) {
+  const int lane = tid & 31, w = tid >> 5;
+  {  // (1) T_qq = (I + A_qq)^-1, q = tid / 16, column tid % 16, axpy order
+    const int q = tid >> 4, cc = tid & 15, o = 16 * q;
+    float y[16];
 #pragma unroll
-  for (int r = 0; r < CH; ++r) y[r] = 0.f;
+    for (int r = 0; r < 16; ++r) y[r] = 0.f;
 #pragma unroll
-  for (int k = 0; k < CH; ++k) {
-    const float xk = (k == c ? 1.f : 0.f) - bs[k] * y[k];
-    y[k] = xk;
-    // rows r > k; the 4-aligned group holding k + 1 starts at or below k,
-    // where L is zero, so whole float4 groups are safe
+    for (int k = 0; k < 16; ++k) {
+      const float xk = (k == cc ? 1.f : 0.f) - y[k];
+      y[k] = xk;
 #pragma unroll
-    for (int g = (k + 1) / 4; g < CH / 4; ++g) {
-      const float4 l4 = *reinterpret_cast<const float4*>(lc + k * CH + 4 * g);
-      y[4 * g + 0] = fmaf(l4.x, xk, y[4 * g + 0]);
-      y[4 * g + 1] = fmaf(l4.y, xk, y[4 * g + 1]);
-      y[4 * g + 2] = fmaf(l4.z, xk, y[4 * g + 2]);
-      y[4 * g + 3] = fmaf(l4.w, xk, y[4 * g + 3]);
+      for (int r = k + 1; r < 16; ++r) y[r] = fmaf(S[sidx(o + r, o + k)], xk, y[r]);
     }
+    __syncwarp();  // the blocks of a warp's threads are read by that warp only
+    const float bc = bs[o + cc];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      S[sidx(o + r, o + cc)] = y[r];
+      *reinterpret_cast<uint16_t*>(ttile + swz(o + r, o + cc)) = bf16_bits(y[r] * bc);
+    }
+    __syncwarp();
+  }
+  {  // (2) warp w, 32-block at O = 32 w: T_10 = -T_11 (A_10 T_00); P = A_10 T_00
+     //     goes to the free strict-upper block (rows O.., cols O + 16..)
+    const int O = 32 * w;
+    uint32_t a0[4], a1[4], b[4][2];
+    frag_a(S, O + 16, O, lane, a0);
+    frag_a(S, O + 16, O + 8, lane, a1);
+    frag_b(S, O, O, lane, b[0]);
+    frag_b(S, O + 8, O, lane, b[1]);
+    frag_b(S, O, O + 8, lane, b[2]);
+    frag_b(S, O + 8, O + 8, lane, b[3]);
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_tf32(d0, a0, b[0]);
+    mma_tf32(d0, a1, b[1]);
+    mma_tf32(d1, a0, b[2]);
+    mma_tf32(d1, a1, b[3]);
+    store_d(S, O, O + 16, lane, d0, 1.f);
+    store_d(S, O, O + 24, lane, d1, 1.f);
+    __syncwarp();
+    frag_a(S, O + 16, O + 16, lane, a0);  // T_11
+    frag_a(S, O + 16, O + 24, lane, a1);
+    frag_b(S, O, O + 16, lane, b[0]);     // P
+    frag_b(S, O + 8, O + 16, lane, b[1]);
+    frag_b(S, O, O + 24, lane, b[2]);
+    frag_b(S, O + 8, O + 24, lane, b[3]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d0[i] = d1[i] = 0.f;
+    mma_tf32(d0, a0, b[0]);
+    mma_tf32(d0, a1, b[1]);
+    mma_tf32(d1, a0, b[2]);
+    mma_tf32(d1, a1, b[3]);
+    store_d(S, O + 16, O, lane, d0, -1.f);  // over A_10, read above by this warp only
+    store_d(S, O + 16, O + 8, lane, d1, -1.f);
+    store_tb_tile(ttile, bs, O + 16, O, lane, d0);
+    store_tb_tile(ttile, bs, O + 16, O + 8, lane, d1);
+  }
+  named_bar_sync(bar_id, 64);
+  {  // (3) lower-left 32 x 32: T_(23,01) = -T_(23,23) (A_(23,01) T_(01,01)); warp w
+     //     on rows r0 = 32 + 16 w; P2 goes to the free block rows 0..31, cols 32..63
+    const int r0 = 32 + 16 * w;
+    uint32_t a[4][4];
+    float d[4][4];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) frag_a(S, r0, 8 * ks, lane, a[ks]);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[nt][i] = 0.f;
+      // T_(01,01) is lower: columns 16.. have rows 16.. only (rows 0..15 of
+      // those columns hold the warp-0 temporary)
+#pragma unroll
+      for (int ks = (nt < 2 ? 0 : 2); ks < 4; ++ks) {
+        uint32_t bb[2];
+        frag_b(S, 8 * ks, 8 * nt, lane, bb);
+        mma_tf32(d[nt], a[ks], bb);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) store_d(S, 16 * w, 32 + 8 * nt, lane, d[nt], 1.f);
+    named_bar_sync(bar_id, 64);
+    // T_(23,23) rows r0..: columns 32..47 for w = 0 (48.. hold the warp-1
+    // temporary), 32..63 for w = 1
+    const int nks = w == 0 ? 2 : 4;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      if (ks < nks) frag_a(S, r0, 32 + 8 * ks, lane, a[ks]);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[nt][i] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        if (ks < nks) {
+          uint32_t bb[2];
+          frag_b(S, 8 * ks, 32 + 8 * nt, lane, bb);
+          mma_tf32(d[nt], a[ks], bb);
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) store_tb_tile(ttile, bs, r0, 8 * nt, lane, d[nt]);
   }
 }
 
@@ -155,8 +315,9 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
 delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const Params p, const unsigned long long mbar_ns) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, derived from the shared array by pointer
+  // arithmetic so that accesses through it stay shared-space accesses
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int head = blockIdx.x;
@@ -281,33 +442,46 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const int quad = warp % 4, c = quad >> 1, ct = 32 * (quad & 1) + lane;
     const int bar_id = 2 + c;  // named barrier of the chunk's 64 threads
     const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
-    float* lcol = reinterpret_cast<float*>(smem + OFF_LC) + c * CH * CH;
+    float* sa = reinterpret_cast<float*>(smem + OFF_LC) + c * CH * CH;
     float* bs = reinterpret_cast<float*>(smem + OFF_BETA) + c * CH;
+    // The strictly upper 16 x 16 blocks of the (T B) tiles are never written
+    // by the solve: zero both pair-parity tiles of this chunk once (the first
+    // chunk barrier below orders this before any solve writes).
+    for (int e = ct; e < 2 * (int)CT / 16; e += 64) {
+      const int par = e / (CT / 16), off = e % (CT / 16);
+      *reinterpret_cast<uint4*>(smem + OFF_T + (par * 2 + c) * CT + off * 16) = make_uint4(0, 0, 0, 0);
+    }
+    const float* beta_h = p.beta + (size_t)head * p.N;
+    // beta of this thread's token, loaded one pair ahead
+    float bnext = (c * CH + ct < p.N) ? beta_h[c * CH + ct] : 0.f;
     for (int pr = 0; pr < npairs; ++pr) {
       // lready(pr) also covers the completion of every product of pair pr - 2,
       // the last readers of this pair parity's T and L tiles.
       const bool got = waitd(x, &B->lready, pr & 1);
       // the chunk's threads agree (barriers follow); this also keeps the copy
-      // below from overwriting lcol and bs before every thread has solved
+      // below from overwriting sa before every thread is done with it
       if (!named_bar_and(bar_id, 64, got)) continue;
       tc_fence_after();
-      const int tok = pr * PT + c * CH + ct;
-      bs[ct] = tok < p.N ? p.beta[(size_t)head * p.N + tok] : 0.f;
+      const float brow = bnext;  // beta of token ct: Gram row ct, T column ct
+      bs[ct] = brow;
+      const int tok_next = (pr + 1) * PT + c * CH + ct;
+      bnext = tok_next < p.N ? beta_h[tok_next] : 0.f;
       uint8_t* ltile = smem + OFF_L + ((pr & 1) * 2 + c) * CT;
       uint8_t* ttile = smem + OFF_T + ((pr & 1) * 2 + c) * CT;
-#pragma unroll
+#pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         uint32_t g[32];
         tmem_ld32(tl + LL + 64 * c + 32 * h, g);
         tmem_ld_wait();
         float l[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          l[q] = (32 * h + q < ct) ? __uint_as_float(g[q]) : 0.f;
-          lcol[(32 * h + q) * CH + ct] = l[q];
-        }
+        for (int q = 0; q < 32; ++q) l[q] = (32 * h + q < ct) ? __uint_as_float(g[q]) : 0.f;
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
+        for (int g4 = 0; g4 < 8; ++g4)  // A row ct = beta_ct L row ct, fp32
+          *reinterpret_cast<float4*>(sa + sidx(ct, 32 * h + 4 * g4)) =
+              make_float4(brow * l[4 * g4], brow * l[4 * g4 + 1], brow * l[4 * g4 + 2], brow * l[4 * g4 + 3]);
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {  // L row ct, bf16 operand tile
           uint4 w;
           w.x = pack_bf16x2(l[8 * g8 + 0], l[8 * g8 + 1]);
           w.y = pack_bf16x2(l[8 * g8 + 2], l[8 * g8 + 3]);
@@ -318,12 +492,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       }
       tc_fence_before();
       named_bar_sync(bar_id, 64);
-      float y[CH];
-      solve_column(lcol, bs, ct, y);
-      const float bc = bs[ct];
-#pragma unroll
-      for (int r = 0; r < CH; ++r)
-        *reinterpret_cast<uint16_t*>(ttile + swz(r, ct)) = bf16_bits(y[r] * bc);
+      solve_t(sa, bs, ttile, ct, bar_id);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B->tready);
@@ -354,7 +523,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         tmem_ld32(tl + KR, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
         tmem_ld32(tl + KR + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
       }
-#pragma unroll
+#pragma unroll 1
       for (int h = 0; h < 4; ++h) {
         uint32_t f[32], w[16];
         tmem_ld32(tl + ST + 32 * h, f);
@@ -376,7 +545,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       // X^T = V^T - (K S)^T, packed over token pairs
       waitd_warp(x, &B->krready, ch & 1);
       tc_fence_after();
-#pragma unroll
+#pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         uint32_t f[32], w[16];
         tmem_ld32(tl + KR + 32 * h, f);
@@ -399,7 +568,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       // UB = bf16(U^T)
       waitd_warp(x, &B->uready, ch & 1);
       tc_fence_after();
-#pragma unroll
+#pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         uint32_t f[32], w[16];
         tmem_ld32(tl + UU + 32 * h, f);
