@@ -291,8 +291,9 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
 aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
        const __grid_constant__ CUtensorMap tm_phik, const Params3 p, const unsigned long long mbar_ns) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, derived from the shared array by pointer
+  // arithmetic so that accesses through it stay shared-space accesses
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -545,8 +546,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
        const Params3 p, const unsigned long long mbar_ns) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, derived from the shared array by pointer
+  // arithmetic so that accesses through it stay shared-space accesses
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
