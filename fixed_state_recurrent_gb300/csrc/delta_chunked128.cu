@@ -22,11 +22,13 @@
 // state and every product live transposed, TMEM lanes = value columns j:
 //   ST  S^T (fp32)                         SB  S^T as packed bf16 (A operand)
 //   KR  (K S)^T, then R^T = (K S + L U)^T  UU  U^T (fp32)
+//       (KR and UU swap their two 64-column regions from chunk to chunk, so
+//       a chunk's reads can leave TMEM while the next chunk runs)
 //   XB  (V - K S)^T, packed bf16 (A operand)
 //   UB  U^T, packed bf16 (A operand)       LL  K2 K2^T of the pair (lanes = tokens)
 // Products per chunk (tcgen05, bf16 operands, fp32 accumulation):
 //   KR = SB  x K_c^T    (M 128, N 64, K 128)   UU = XB x (T_c B_c)^T (M 128, N 64, K 64)
-//   KR += UB x L_c^T    (M 128, N 64, K 64)    ST += UB x K_c        (M 128, N 128, K 64)
+//   ST += UB x K_c      (M 128, N 128, K 64)   KR += UB x L_c^T      (M 128, N 64, K 64)
 // with B_c = diag(beta) folded into the T operand.  T is computed per chunk
 // by 64 threads from A = diag(beta) L (fp32, in shared memory) by block
 // recursion: the four 16 x 16 diagonal blocks of (I + A)^-1 by forward
@@ -39,11 +41,13 @@
 // from registers instead.
 //
 // Schedule: the chunks form one dependent chain (SB -> KR -> XB -> UU -> UB ->
-// ST -> SB).  Off that chain run the TMA loads (one pair ahead), the Gram
-// product and T of the NEXT pair (its Gram is issued right after the current
-// pair's first K S product; T and L operand tiles are double-buffered by pair
-// parity), and the global stores of each chunk's reads (held in registers
-// while the next snapshot is packed).
+// ST -> SB; the reads' product KR += UB L^T comes after ST's, off the chain).  Off that chain run the TMA loads (K in a ring of three pair
+// stages, V in a ring of two chunk slots), the Gram product and T of the NEXT
+// pair (its Gram is issued after the current pair's first K S product, once
+// the T builders have copied the previous Gram out of TMEM: issuing tensor
+// instructions stalls while the tensor queue is full, so it goes where the
+// chain waits on the epilogue anyway; T and L operand tiles are double-
+// buffered by pair parity), and the global stores of each chunk's reads.
 #include "prefill_tc_common.cuh"
 
 namespace la {
@@ -57,12 +61,15 @@ namespace dc {
 constexpr int D = 128;    // dk = dv
 constexpr int CH = 64;    // tokens per chunk
 constexpr int PT = 128;   // tokens per pair
-constexpr int NS = 2;     // pair stages
-constexpr uint32_t HALF = PT * 128;          // one 64-element column block of a pair tile: 16 KB
-constexpr uint32_t TILE = 2 * HALF;          // K or V of a pair: 32 KB
-constexpr uint32_t STAGE = 2 * TILE;         // K | V
+constexpr int NK = 3;     // K stages (pairs)
+constexpr int NV = 2;     // V slots (chunks)
+constexpr uint32_t HALF = PT * 128;          // one 64-element column block of a pair's K: 16 KB
+constexpr uint32_t KSTAGE = 2 * HALF;        // K of a pair: 32 KB
+constexpr uint32_t VHALF = CH * 128;         // one 64-element column block of a chunk's V: 8 KB
+constexpr uint32_t VSLOT = 2 * VHALF;        // V of a chunk: 16 KB
 constexpr uint32_t CT = CH * 128;            // a [64 x 64] bf16 operand tile: 8 KB
-constexpr uint32_t OFF_T = NS * STAGE;       // (T B)_c tiles, [pair parity][chunk]
+constexpr uint32_t OFF_V = NK * KSTAGE;      // V slots
+constexpr uint32_t OFF_T = OFF_V + NV * VSLOT;  // (T B)_c tiles, [pair parity][chunk]
 constexpr uint32_t OFF_L = OFF_T + 4 * CT;   // L_c tiles, [pair parity][chunk]
 constexpr uint32_t OFF_LC = OFF_L + 4 * CT;  // fp32 A, then T, of both chunks (2 x 16 KB)
 constexpr uint32_t OFF_BETA = OFF_LC + 2 * CH * CH * 4;  // beta of the chunks being solved
@@ -70,9 +77,12 @@ constexpr uint32_t OFF_BAR = OFF_BETA + PT * 4;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 
-constexpr int kWarps = 10;  // 0 TMA, 1 MMA, 2-5 T builders, 6-9 state epilogue
+constexpr int kWarps = 11;  // 0 TMA of K, 1 MMA, 2-5 T builders, 6-9 state epilogue, 10 TMA of V
 constexpr uint32_t kCols = 512;
-constexpr uint32_t ST = 0, LL = 128, KR = 256, UU = 320, SB = 384, XB = 448, UB = 480;
+constexpr uint32_t ST = 0, LL = 128, KRUU = 256, SB = 384, XB = 448, UB = 480;
+// (K S)^T / R^T of chunk ch in KRUU + 64 (ch & 1), U^T in the other region
+__device__ __forceinline__ uint32_t kr_cols(uint32_t ch) { return KRUU + 64 * (ch & 1); }
+__device__ __forceinline__ uint32_t uu_cols(uint32_t ch) { return KRUU + 64 * ((ch + 1) & 1); }
 
 constexpr uint32_t ID_LL = idesc_bf16_f32(128, 128, 0, 0);  // K2 K2^T
 constexpr uint32_t ID_KS = idesc_bf16_f32(128, CH, 0, 0);   // SB x K_c^T (B K-major)
@@ -90,19 +100,24 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t full[NS], empty[NS];
+  uint64_t kfull[NK], kempty[NK];  // K ring                 (TMA <-> MMA)
+  uint64_t vfull[NV], vfree[NV];   // V ring                 (TMA <-> epilogue)
   uint64_t lready;   // Gram product of a pair in LL        (MMA -> T)
-  uint64_t tready;   // T and L tiles of a pair              (T -> MMA)
+  uint64_t llfree;   // LL copied out by the T builders     (T -> MMA)
+  uint64_t tready[2];  // T and L tiles, by pair parity    (T -> MMA)
   uint64_t sbready;  // S^T packed into SB                  (epilogue -> MMA)
   uint64_t krready;  // (K S)^T in KR                       (MMA -> epilogue)
   uint64_t xready;   // X^T packed into XB                  (epilogue -> MMA)
   uint64_t uready;   // U^T in UU                           (MMA -> epilogue)
   uint64_t ubready;  // U^T packed into UB                  (epilogue -> MMA)
-  uint64_t rsready;  // R^T in KR, S^T advanced             (MMA -> epilogue)
-  uint64_t drain;
+  uint64_t sready;   // S^T advanced past the chunk         (MMA -> epilogue)
+  uint64_t rready;   // R^T of the chunk in its KR region   (MMA -> epilogue)
+  uint64_t drain, drain2;  // completion of the MMA and Gram threads' products on abort
   uint32_t tmem_slot;
   int abort;
 };
+
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct Ctx {
   const Params* p;
@@ -287,27 +302,32 @@ __device__ __forceinline__ void solve_t(float* S, const float* bs, uint8_t* ttil
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) store_d(S, 16 * w, 32 + 8 * nt, lane, d[nt], 1.f);
     named_bar_sync(bar_id, 64);
-    // T_(23,23) rows r0..: columns 32..47 for w = 0 (48.. hold the warp-1
-    // temporary), 32..63 for w = 1
-    const int nks = w == 0 ? 2 : 4;
+    // -T_(23,23) P2, warp w on columns 16 w .. 16 w + 15 of both row tiles
+    // (12 products each).  T_(23,23) rows 32..47 use columns 32..47 only
+    // (48.. hold the warp-1 temporary); rows 48..63 use 32..63.
+    uint32_t ta[6][4];
+    frag_a(S, 32, 32, lane, ta[0]);
+    frag_a(S, 32, 40, lane, ta[1]);
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      if (ks < nks) frag_a(S, r0, 32 + 8 * ks, lane, a[ks]);
+    for (int ks = 0; ks < 4; ++ks) frag_a(S, 48, 32 + 8 * ks, lane, ta[2 + ks]);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
+      const int n0 = 16 * w + 8 * nt;
+      uint32_t bb[4][2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d[nt][i] = 0.f;
+      for (int ks = 0; ks < 4; ++ks) frag_b(S, 8 * ks, 32 + n0, lane, bb[ks]);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        if (ks < nks) {
-          uint32_t bb[2];
-          frag_b(S, 8 * ks, 32 + 8 * nt, lane, bb);
-          mma_tf32(d[nt], a[ks], bb);
-        }
-      }
+      for (int i = 0; i < 4; ++i) d[nt][i] = d[2 + nt][i] = 0.f;
+      mma_tf32(d[nt], ta[0], bb[0]);
+      mma_tf32(d[nt], ta[1], bb[1]);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) mma_tf32(d[2 + nt], ta[2 + ks], bb[ks]);
     }
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) store_tb_tile(ttile, bs, r0, 8 * nt, lane, d[nt]);
+    for (int nt = 0; nt < 2; ++nt) {
+      store_tb_tile(ttile, bs, 32, 16 * w + 8 * nt, lane, d[nt]);
+      store_tb_tile(ttile, bs, 48, 16 * w + 8 * nt, lane, d[2 + nt]);
+    }
   }
 }
 
@@ -323,19 +343,27 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
   const int head = blockIdx.x;
   const int npairs = (p.N + PT - 1) / PT;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&B->full[s], 1);
-      mbar_init(&B->empty[s], 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&B->kfull[s], 1);
+      mbar_init(&B->kempty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&B->vfull[s], 1);
+      mbar_init(&B->vfree[s], 4);
     }
     mbar_init(&B->lready, 1);
-    mbar_init(&B->tready, 4);
+    mbar_init(&B->llfree, 4);
+    mbar_init(&B->tready[0], 4);
+    mbar_init(&B->tready[1], 4);
     mbar_init(&B->sbready, 4);
     mbar_init(&B->krready, 1);
     mbar_init(&B->xready, 4);
     mbar_init(&B->uready, 1);
     mbar_init(&B->ubready, 4);
-    mbar_init(&B->rsready, 1);
+    mbar_init(&B->sready, 1);
+    mbar_init(&B->rready, 1);
     mbar_init(&B->drain, 1);
+    mbar_init(&B->drain2, 1);
     B->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_k);
@@ -352,86 +380,88 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
   const Ctx x{&p, &B->abort, mbar_ns};
 
   if (warp == 0) {
-    if (lane == 0) {  // ---- TMA producer: K and V of each pair (two 64-column halves each)
+    if (lane == 0) {  // ---- TMA producer of K, one pair (two 64-column halves) per stage
       uint32_t issued = 0;
       for (int pr = 0; pr < npairs; ++pr) {
-        const int s = pr % NS;
-        if (pr >= NS && !waitd(x, &B->empty[s], ((pr / NS) - 1) & 1)) break;
-        uint8_t* st = smem + s * STAGE;
-        mbar_arrive_expect_tx(&B->full[s], STAGE);
-        for (int h = 0; h < 2; ++h) {
-          tma_load_3d(st + h * HALF, &tm_k, 64 * h, pr * PT, head, &B->full[s]);
-          tma_load_3d(st + TILE + h * HALF, &tm_v, 64 * h, pr * PT, head, &B->full[s]);
-        }
+        const int s = pr % NK;
+        if (pr >= NK && !waitd(x, &B->kempty[s], ((pr / NK) - 1) & 1)) break;
+        uint8_t* st = smem + s * KSTAGE;
+        mbar_arrive_expect_tx(&B->kfull[s], KSTAGE);
+        for (int h = 0; h < 2; ++h) tma_load_3d(st + h * HALF, &tm_k, 64 * h, pr * PT, head, &B->kfull[s]);
         ++issued;
       }
       if (*x.abort) {
         int never = 0;
         const uint64_t dl = globaltimer_ns() + mbar_ns;
-        for (uint32_t q = (issued > NS ? issued - NS : 0); q < issued; ++q)
-          mbar_wait(&B->full[q % NS], (q / NS) & 1, dl, &never);
+        for (uint32_t q = (issued > NK ? issued - NK : 0); q < issued; ++q)
+          mbar_wait(&B->kfull[q % NK], (q / NK) & 1, dl, &never);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {  // ---- MMA issue
-      // Gram product of pair pr: LL = K2 K2^T (A and B both the K tile, K-major).
-      auto gram = [&](int pr) -> bool {
-        const int s = pr % NS;
-        if (!waitd(x, &B->full[s], (pr / NS) & 1)) return false;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(smem + s * STAGE);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t a = kb + (ks / 4) * HALF + (ks % 4) * 32;
-          mma_bf16_ss(tmem + LL, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024), ID_LL, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(&B->lready);
-        return true;
-      };
       uint32_t nch = 0;  // chunks done
-      bool ok = npairs == 0 || gram(0);
+      bool ok = true;
       for (int pr = 0; ok && pr < npairs; ++pr) {
-        const int s = pr % NS;
-        const uint32_t kb = smem_u32(smem + s * STAGE);
+        const int s = pr % NK;
+        const uint32_t kb = smem_u32(smem + s * KSTAGE);
         const uint32_t aT = smem_u32(smem + OFF_T + (pr & 1) * 2 * CT);
         const uint32_t aL = smem_u32(smem + OFF_L + (pr & 1) * 2 * CT);
-        if (!(ok = waitd(x, &B->tready, pr & 1))) break;
+        if (!(ok = waitd(x, &B->tready[pr & 1], (pr >> 1) & 1))) break;
         for (int c = 0; ok && c < 2; ++c, ++nch) {
           const uint32_t kc = kb + c * CT;  // the chunk's 64 rows inside each half
           const uint32_t tc_ = aT + c * CT, lc = aL + c * CT;
+          const uint32_t kr = kr_cols(nch), uu = uu_cols(nch);
           if (!(ok = waitd(x, &B->sbready, nch & 1))) break;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)  // KR = SB x K_c^T
-            mma_bf16_ts(tmem + KR, tmem + SB + 8 * ks,
+            mma_bf16_ts(tmem + kr, tmem + SB + 8 * ks,
                         sdesc_sw128(kc + (ks / 4) * HALF + (ks % 4) * 32, 16, 1024), ID_KS, ks > 0 ? 1u : 0u);
           mma_commit(&B->krready);
-          // the next pair's Gram product runs while the epilogue builds X
-          if (c == 0 && pr + 1 < npairs && !(ok = gram(pr + 1))) break;
           if (!(ok = waitd(x, &B->xready, nch & 1))) break;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < CH / 16; ++ks)  // UU = XB x (T B)_c^T
-            mma_bf16_ts(tmem + UU, tmem + XB + 8 * ks, sdesc_sw128(tc_ + ks * 32, 16, 1024), ID_U,
+            mma_bf16_ts(tmem + uu, tmem + XB + 8 * ks, sdesc_sw128(tc_ + ks * 32, 16, 1024), ID_U,
                         ks > 0 ? 1u : 0u);
           mma_commit(&B->uready);
           if (!(ok = waitd(x, &B->ubready, nch & 1))) break;
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < CH / 16; ++ks)  // KR += UB x L_c^T
-            mma_bf16_ts(tmem + KR, tmem + UB + 8 * ks, sdesc_sw128(lc + ks * 32, 16, 1024), ID_R, 1u);
-#pragma unroll
           for (int ks = 0; ks < CH / 16; ++ks)  // ST += UB x K_c (K rows = tokens, B MN-major)
             mma_bf16_ts(tmem + ST, tmem + UB + 8 * ks, sdesc_sw128(kc + ks * 2048, HALF, 1024), ID_S, 1u);
-          mma_commit(&B->rsready);
+          mma_commit(&B->sready);
+#pragma unroll
+          for (int ks = 0; ks < CH / 16; ++ks)  // KR += UB x L_c^T: the chunk's reads
+            mma_bf16_ts(tmem + kr, tmem + UB + 8 * ks, sdesc_sw128(lc + ks * 32, 16, 1024), ID_R, 1u);
+          mma_commit(&B->rready);
         }
-        if (ok) mma_commit(&B->empty[s]);
+        if (ok) mma_commit(&B->kempty[s]);
       }
       if (*x.abort) {
         int never = 0;
         mma_commit(&B->drain);
         mbar_wait(&B->drain, 0, globaltimer_ns() + mbar_ns, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    if (lane == 0) {  // ---- TMA producer of V, one chunk per slot
+      uint32_t issued = 0;
+      for (int ch = 0; ch < 2 * npairs; ++ch) {
+        const int s = ch % NV;
+        if (ch >= NV && !waitd(x, &B->vfree[s], ((ch / NV) - 1) & 1)) break;
+        uint8_t* st = smem + OFF_V + s * VSLOT;
+        mbar_arrive_expect_tx(&B->vfull[s], VSLOT);
+        for (int h = 0; h < 2; ++h) tma_load_3d(st + h * VHALF, &tm_v, 64 * h, ch * CH, head, &B->vfull[s]);
+        ++issued;
+      }
+      if (*x.abort) {
+        int never = 0;
+        const uint64_t dl = globaltimer_ns() + mbar_ns;
+        for (uint32_t q = (issued > NV ? issued - NV : 0); q < issued; ++q)
+          mbar_wait(&B->vfull[q % NV], (q / NV) & 1, dl, &never);
       }
     }
     __syncwarp();
@@ -454,13 +484,36 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const float* beta_h = p.beta + (size_t)head * p.N;
     // beta of this thread's token, loaded one pair ahead
     float bnext = (c * CH + ct < p.N) ? beta_h[c * CH + ct] : 0.f;
+    // Gram product of pair q, LL = K2 K2^T (A and B both the pair's K tile,
+    // K-major), issued by one T-builder thread: for pair 0 here, for pair
+    // q + 1 as soon as T of pair q is done, so that the Gram products run
+    // ahead of the state chain instead of on its issue thread.
+    const bool gram_thread = warp == 2 && lane == 0;
+    auto gram = [&](int q) -> bool {
+      const int s = q % NK;
+      if (!waitd(x, &B->kfull[s], (q / NK) & 1)) return false;
+      tc_fence_after();
+      const uint32_t kb = smem_u32(smem + s * KSTAGE);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t a = kb + (ks / 4) * HALF + (ks % 4) * 32;
+        mma_bf16_ss(tmem + LL, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024), ID_LL, ks > 0 ? 1u : 0u);
+      }
+      mma_commit(&B->lready);
+      return true;
+    };
+    bool gram_ok = !gram_thread || npairs == 0 || gram(0);
+    __syncwarp();
     for (int pr = 0; pr < npairs; ++pr) {
-      // lready(pr) also covers the completion of every product of pair pr - 2,
-      // the last readers of this pair parity's T and L tiles.
-      const bool got = waitd(x, &B->lready, pr & 1);
+      // The T and L tiles of this pair parity were last read by the products
+      // of pair pr - 2: wait for their completion (the commit of that pair's
+      // K stage) before overwriting them.
+      bool got = gram_ok && waitd(x, &B->lready, pr & 1);
+      if (pr >= 2) got = got && waitd(x, &B->kempty[(pr - 2) % NK], ((pr - 2) / NK) & 1);
       // the chunk's threads agree (barriers follow); this also keeps the copy
       // below from overwriting sa before every thread is done with it
       if (!named_bar_and(bar_id, 64, got)) continue;
+      __syncwarp();  // (re)converged for the warp-wide TMEM loads and mma below
       tc_fence_after();
       const float brow = bnext;  // beta of token ct: Gram row ct, T column ct
       bs[ct] = brow;
@@ -491,11 +544,23 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         }
       }
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B->llfree);  // LL may take the next Gram product
       named_bar_sync(bar_id, 64);
       solve_t(sa, bs, ttile, ct, bar_id);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&B->tready);
+      if (lane == 0) mbar_arrive(&B->tready[pr & 1]);
+      // the next Gram product, once every T builder has copied this pair's
+      // out of LL
+      if (gram_thread && pr + 1 < npairs)
+        gram_ok = waitd(x, &B->llfree, pr & 1) && gram(pr + 1);
+      __syncwarp();
+    }
+    if (gram_thread && *x.abort) {  // Gram products still in flight finish before TMEM is freed
+      int never = 0;
+      mma_commit(&B->drain2);
+      mbar_wait(&B->drain2, 0, globaltimer_ns() + mbar_ns, &never);
     }
   } else {  // ---- state epilogue: lane j of S^T, one TMEM quadrant per warp
     const int quad = warp % 4, j = 32 * quad + lane;
@@ -512,17 +577,10 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const uint32_t nchunks = 2u * (uint32_t)npairs;
     float* reads_j = p.reads + (size_t)head * p.N * D + j;
     for (uint32_t ch = 0; ch < nchunks; ++ch) {
-      const int pr = ch / 2, c = ch % 2;
-      const uint8_t* vt = smem + (pr % NS) * STAGE + TILE;
-      // reads of the previous chunk (R^T in KR) into registers, then the new
-      // snapshot SB = bf16(S^T); the reads go out while the chain moves on
-      uint32_t r[64];
-      if (ch > 0) {
-        waitd_warp(x, &B->rsready, (ch - 1) & 1);
-        tc_fence_after();
-        tmem_ld32(tl + KR, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld32(tl + KR + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-      }
+      const uint8_t* vt = smem + OFF_V + (ch % NV) * VSLOT;
+      // SB = bf16(S^T) once S has advanced past chunk ch - 1
+      if (ch > 0) waitd_warp(x, &B->sready, (ch - 1) & 1);
+      tc_fence_after();
 #pragma unroll 1
       for (int h = 0; h < 4; ++h) {
         uint32_t f[32], w[16];
@@ -536,42 +594,67 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B->sbready);
+      // reads of chunk ch - 1 (R^T in its KR region, which this chunk's U^T
+      // overwrites only after xready below)
       if (ch > 0) {
+        waitd_warp(x, &B->rready, (ch - 1) & 1);
+        tc_fence_after();
         const int t0 = (int)(ch - 1) * CH;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t f[32];
+          tmem_ld32(tl + kr_cols(ch - 1) + 32 * h, f);
+          tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 64; ++q)
-          if (t0 + q < p.N) reads_j[(size_t)(t0 + q) * D] = __uint_as_float(r[q]);
+          for (int q = 0; q < 32; ++q)
+            if (t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * D] = __uint_as_float(f[q]);
+        }
+      }
+      // V of the chunk, column j, into registers (token pairs packed)
+      waitd_warp(x, &B->vfull[ch % NV], (ch / NV) & 1);
+      uint32_t vv[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const uint32_t lo = *reinterpret_cast<const uint16_t*>(vt + (j / 64) * VHALF + swz(2 * q, j % 64));
+        const uint32_t hi = *reinterpret_cast<const uint16_t*>(vt + (j / 64) * VHALF + swz(2 * q + 1, j % 64));
+        vv[q] = lo | (hi << 16);
       }
       // X^T = V^T - (K S)^T, packed over token pairs
       waitd_warp(x, &B->krready, ch & 1);
       tc_fence_after();
-#pragma unroll 1
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t f[32], w[16];
-        tmem_ld32(tl + KR + 32 * h, f);
+        tmem_ld32(tl + kr_cols(ch) + 32 * h, f);
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          const int t = 64 * c + 32 * h + 2 * q;  // pair token
-          const float v0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-              vt + (j / 64) * HALF + swz(t, j % 64)));
-          const float v1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-              vt + (j / 64) * HALF + swz(t + 1, j % 64)));
-          w[q] = pack_bf16x2(v0 - __uint_as_float(f[2 * q]), v1 - __uint_as_float(f[2 * q + 1]));
+          const uint32_t v2 = vv[16 * h + q];
+          w[q] = pack_bf16x2(__uint_as_float(v2 << 16) - __uint_as_float(f[2 * q]),
+                             __uint_as_float(v2 & 0xFFFF0000u) - __uint_as_float(f[2 * q + 1]));
         }
         tmem_st16(tl + XB + 16 * h, w);
       }
       tmem_st_wait();
       tc_fence_before();
+      // The V slot goes back to the TMA producer only now that its values
+      // have been consumed, and after a proxy fence: these generic-proxy reads
+      // must be ordered before the async-proxy (TMA) write that refills the
+      // slot.  (Releasing it right after the loads let the refill overtake
+      // some of them.)
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&B->xready);
+      if (lane == 0) {
+        mbar_arrive(&B->xready);
+        mbar_arrive(&B->vfree[ch % NV]);
+      }
       // UB = bf16(U^T)
       waitd_warp(x, &B->uready, ch & 1);
       tc_fence_after();
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         uint32_t f[32], w[16];
-        tmem_ld32(tl + UU + 32 * h, f);
+        tmem_ld32(tl + uu_cols(ch) + 32 * h, f);
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 16; ++q) w[q] = pack_bf16x2(__uint_as_float(f[2 * q]), __uint_as_float(f[2 * q + 1]));
@@ -584,18 +667,19 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
     // the last chunk's reads and S_N = S^T transposed back
     if (nchunks > 0) {
-      waitd_warp(x, &B->rsready, (nchunks - 1) & 1);
+      waitd_warp(x, &B->rready, (nchunks - 1) & 1);
       tc_fence_after();
-#pragma unroll
+      const int t0 = (int)(nchunks - 1) * CH;
       for (int h = 0; h < 2; ++h) {
         uint32_t f[32];
-        tmem_ld32(tl + KR + 32 * h, f);
+        tmem_ld32(tl + kr_cols(nchunks - 1) + 32 * h, f);
         tmem_ld_wait();
-        const int t0 = (int)(nchunks - 1) * CH + 32 * h;
 #pragma unroll
         for (int q = 0; q < 32; ++q)
-          if (t0 + q < p.N) reads_j[(size_t)(t0 + q) * D] = __uint_as_float(f[q]);
+          if (t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * D] = __uint_as_float(f[q]);
       }
+      waitd_warp(x, &B->sready, (nchunks - 1) & 1);
+      tc_fence_after();
     }
     for (int h = 0; h < 4; ++h) {
       uint32_t f[32];
@@ -631,7 +715,7 @@ cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta
   const int BH = B * H;
   CUtensorMap mk, mv;
   if (!make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, PT) ||
-      !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, PT))
+      !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, CH))
     return cudaErrorInvalidValue;
   Params p;
   p.BH = BH;

@@ -134,6 +134,26 @@ def test_delta_chunked_ragged(la, orc, N):
     assert relmax(f64(S), rS) <= TOL_BF16
 
 
+def test_delta_chunked_repeatable(la, orc):
+    # A few blocks (three heads) leave the SMs lightly loaded, which is where
+    # an ordering hole between the kernel's roles shows up; the kernel has no
+    # atomics on its data path, so every run must be bitwise identical, and
+    # match the oracle.
+    from fixed_state_recurrent_gb300 import inputs
+    N = 1000
+    k, v, beta = inputs.delta_inputs(1, 3, N, 128, 128, torch.bfloat16, seed=77)
+    g = torch.Generator().manual_seed(78)
+    S0 = torch.randn((1, 3, 128, 128), generator=g) * 0.5
+    kd, vd, bd, Sd = k.cuda(), v.cuda(), beta.cuda(), S0.cuda()
+    first = la.delta_prefill(kd, vd, bd, S0=Sd)
+    for _ in range(24):
+        again = la.delta_prefill(kd, vd, bd, S0=Sd)
+        assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
+    rr, rS = orc.delta(f64(k), f64(v), f64(beta), S0=f64(S0))
+    assert relmax(f64(first[0]), rr) <= TOL_BF16
+    assert relmax(f64(first[1]), rS) <= TOL_BF16
+
+
 def test_delta_in_place_alias_and_zero_length(la, orc):
     from fixed_state_recurrent_gb300 import inputs
     k, v, beta = inputs.delta_inputs(1, 2, 60, 64, 64, torch.bfloat16, seed=43)
