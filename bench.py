@@ -57,6 +57,9 @@ def _args():
                    help="headline workload only (no long/decode/delta/e2e/cpu)")
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run (long,decode,delta,pr1)")
+    p.add_argument("--profile-delta", type=int, default=0, metavar="CALLS",
+                   help="run CALLS plain delta_prefill calls of the delta workload and exit "
+                        "(for profilers)")
     p.add_argument("--profile", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain (non-graph) prefill calls of the headline workload on "
                         "the same rotating buffer sets and exit: the command profilers run")
@@ -299,6 +302,21 @@ def profile_calls(api, w, calls, sets=4):
     print(f"profiled {calls} prefill calls", flush=True)
 
 
+def profile_delta_calls(api, calls):
+    """`calls` plain delta_prefill calls of the delta workload, for profilers."""
+    import torch
+    from fixed_state_recurrent_gb300 import inputs
+    w = inputs.WORKLOADS["delta"]
+    dev = torch.device("cuda")
+    k, v, beta = inputs.delta_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype, w.seed, device=dev)
+    reads = torch.empty((w.B, w.H, w.N, w.dv), device=dev)
+    S = torch.empty((w.B, w.H, w.dk, w.dv), device=dev)
+    for _ in range(calls):
+        api.delta_prefill(k, v, beta, reads=reads, S_N=S)
+    torch.cuda.synchronize()
+    print(f"profiled {calls} delta calls", flush=True)
+
+
 def bench_decode(api, rank, world, reps=3):
     """100 consecutive decode steps captured in one CUDA graph; the state comes
     from a 1024-token prefix run through la_prefill."""
@@ -364,10 +382,14 @@ def bench_delta(api, rank, world, reps=3):
     ms_call = min(per)
     tokens = w.B * w.H * w.N
     flops = 4.0 * w.dk * w.dv * tokens
+    # algorithmic HBM bytes: k, v (bf16) and beta (fp32) in, reads (fp32) out,
+    # per token; the final state (fp32) per head
+    nbytes = tokens * (2 * w.dk + 2 * w.dv + 4 + 4 * w.dv) + w.B * w.H * w.dk * w.dv * 4
     return {"workload": "delta: B=8 H=16 N=8192 dk=dv=128, unit bf16 keys, bf16 values, "
                         "sigmoid beta", "ms_per_call": ms_call,
             "tokens_per_s": tokens / (ms_call * 1e-3),
-            "fp32_tflops": flops / (ms_call * 1e-3) / 1e12}
+            "fp32_tflops": flops / (ms_call * 1e-3) / 1e12,
+            "bytes_per_call": nbytes, "hbm_gbs": nbytes / (ms_call * 1e-3) / 1e9}
 
 
 def bench_simple_prefill(api, wname, rank, world, reps=5):
@@ -517,6 +539,10 @@ def main():
     time.sleep(0.3)
 
     w = inputs.WORKLOADS["prefill"]
+    if args.profile_delta:
+        profile_delta_calls(api, args.profile_delta)
+        sampler.stop()
+        return
     if args.profile:
         profile_calls(api, w, args.profile)
         sampler.stop()
@@ -557,6 +583,8 @@ def main():
         extra["decode"]["hbm_frac"] = extra["decode"]["hbm_gbs"] / hbm_peak
     if "long" in extra and "hbm_gbs" in extra["long"]:
         extra["long"]["hbm_frac"] = extra["long"]["hbm_gbs"] / hbm_peak
+    if "delta" in extra:
+        extra["delta"]["hbm_frac"] = extra["delta"]["hbm_gbs"] / hbm_peak
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_extra:
