@@ -22,7 +22,7 @@ LA_F32, LA_BF16 = 0, 1
 
 SYMBOLS = ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
            "delta_prefill", "la_state_bytes", "la_status_string",
-           "la_read_device_status")
+           "la_read_device_status", "delta_read_device_status")
 
 
 class LAError(RuntimeError):
@@ -65,6 +65,8 @@ def load(path: str | None = None):
         lib.la_status_string.restype = ctypes.c_char_p
         lib.la_read_device_status.argtypes = [vp, vp]
         lib.la_read_device_status.restype = i
+        lib.delta_read_device_status.argtypes = [vp]
+        lib.delta_read_device_status.restype = i
         _lib = lib
         return lib
 
@@ -216,6 +218,15 @@ def read_device_status(ws, stream=None) -> int:
     """Synchronize and return/clear the device status word of a workspace."""
     s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(ws.device)
     return int(load().la_read_device_status(_ptr(ws), s))
+
+
+def delta_read_device_status(stream=None) -> int:
+    """Synchronize and return/clear the tensor-core delta kernel's status word
+    (current device)."""
+    import torch
+    s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else \
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return int(load().delta_read_device_status(s))
 
 
 def prefill_noalloc(q, k, v, eps=1e-6, S0=None, z0=None, *, o=None, S_N=None, z_N=None,

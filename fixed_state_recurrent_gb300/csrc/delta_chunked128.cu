@@ -97,6 +97,7 @@ struct Params {
   float* reads;
   float* S_N;
   unsigned* status;
+  int force_wait;  // test hook: the MMA thread waits once on a barrier nothing completes
 };
 
 struct Bars {
@@ -113,6 +114,7 @@ struct Bars {
   uint64_t sready;   // S^T advanced past the chunk         (MMA -> epilogue)
   uint64_t rready;   // R^T of the chunk in its KR region   (MMA -> epilogue)
   uint64_t drain, drain2;  // completion of the MMA and Gram threads' products on abort
+  uint64_t never;          // completed by nothing (the forced-timeout test hook)
   uint32_t tmem_slot;
   int abort;
 };
@@ -364,6 +366,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     mbar_init(&B->rready, 1);
     mbar_init(&B->drain, 1);
     mbar_init(&B->drain2, 1);
+    mbar_init(&B->never, 1);
     B->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_k);
@@ -401,7 +404,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
   } else if (warp == 1) {
     if (lane == 0) {  // ---- MMA issue
       uint32_t nch = 0;  // chunks done
-      bool ok = true;
+      bool ok = !p.force_wait || waitd(x, &B->never, 0);
       for (int pr = 0; ok && pr < npairs; ++pr) {
         const int s = pr % NK;
         const uint32_t kb = smem_u32(smem + s * KSTAGE);
@@ -725,12 +728,27 @@ cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta
   p.reads = reads;
   p.S_N = S_N;
   p.status = status;
+  p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
   cudaError_t e = cudaFuncSetAttribute(delta_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM);
   if (e != cudaSuccess) return e;
   delta_chunked_kernel<<<BH, 32 * kWarps, SMEM, stream>>>(mk, mv, p, mbar_ns);
   return cudaGetLastError();
+}
+
+cudaError_t delta_status_take(unsigned* out) {
+  using namespace dc;
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_delta_status, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_delta_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *out = v;
+  return cudaSuccess;
 }
 
 }  // namespace la

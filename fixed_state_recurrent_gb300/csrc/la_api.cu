@@ -227,4 +227,11 @@ la_status la_read_device_status(const void* workspace, cudaStream_t stream) {
   return (status & la::kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
 }
 
+la_status delta_read_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return LA_ERR_CUDA;
+  unsigned status = 0;
+  if (la::delta_status_take(&status) != cudaSuccess) return LA_ERR_CUDA;
+  return (status & la::kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
+}
+
 }  // extern "C"

@@ -64,6 +64,8 @@ bool delta_chunked_supported(bool bf16, int dk, int dv);
 cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, int B, int H,
                                  int N, const float* S0, float* reads, float* S_N,
                                  cudaStream_t stream);
+// Returns and clears the chunked delta kernel's status word (current device).
+cudaError_t delta_status_take(unsigned* out);
 
 cudaError_t launch_delta_prefill(const void* k, const void* v, bool bf16,
                                  const float* beta, int B, int H, int N,

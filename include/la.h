@@ -107,6 +107,10 @@ la_status la_decode_step(const void* q, const void* k, const void* v, la_dtype i
  *   k [B][H][N][dk], v [B][H][N][dv] in in_dtype;  beta [B][H][N] float32
  *   S0 initial memory or NULL (zero); S_N may alias S0
  *   reads [B][H][N][dv], S_N [B][H][dk][dv] float32
+ * bf16 inputs at dk = dv = 128 run chunkwise on the tensor cores (64-token
+ * chunks; the state enters the products as a bf16 copy of the fp32 state);
+ * other inputs run token by token in fp32.  A bounded wait of the chunkwise
+ * kernel that gives up is reported by delta_read_device_status.
  */
 la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const float* beta,
                         int B, int H, int N, int dk, int dv,
@@ -125,6 +129,15 @@ const char* la_status_string(la_status s);
  * last read, otherwise LA_OK).  LA_ERR_INVALID_ARG for a NULL workspace,
  * LA_ERR_CUDA if the synchronization or copy fails. */
 la_status la_read_device_status(const void* workspace, cudaStream_t stream);
+
+/* Synchronizes `stream`, then returns and clears the status word of the
+ * tensor-core delta kernel (delta_prefill with bf16 inputs at dk = dv = 128):
+ * LA_ERR_TIMEOUT if one of its bounded waits gave up since the last read,
+ * otherwise LA_OK; LA_ERR_CUDA if the synchronization or copy fails.  The
+ * word belongs to the current device and is shared by every delta_prefill
+ * call on it (delta_prefill takes no workspace); the token-by-token delta
+ * kernel has no waits and never sets it. */
+la_status delta_read_device_status(cudaStream_t stream);
 
 /*
  * la_prefill_noalloc -- la_prefill without a caller-provided workspace.

@@ -29,7 +29,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
               "delta_prefill", "la_state_bytes", "la_status_string",
-              "la_read_device_status"):
+              "la_read_device_status", "delta_read_device_status"):
         assert n in names
 
 

@@ -152,6 +152,30 @@ def test_delta_chunked_repeatable(la, orc):
     rr, rS = orc.delta(f64(k), f64(v), f64(beta), S0=f64(S0))
     assert relmax(f64(first[0]), rr) <= TOL_BF16
     assert relmax(f64(first[1]), rS) <= TOL_BF16
+    assert la.delta_read_device_status() == 0  # LA_OK: no wait gave up
+
+
+def test_delta_bounded_wait_reports_timeout(la, orc, monkeypatch):
+    # A test hook makes the chunked kernel's MMA thread wait on an mbarrier
+    # that nothing completes, with a 2 ms limit: the wait gives up, every role
+    # drains what it started and the launch finishes, the status word says
+    # LA_ERR_TIMEOUT (reading clears it), and the context stays usable.
+    from fixed_state_recurrent_gb300 import inputs
+    k, v, beta = inputs.delta_inputs(1, 2, 700, 128, 128, torch.bfloat16, seed=26)
+    kd, vd, bd = k.cuda(), v.cuda(), beta.cuda()
+    la.delta_read_device_status()
+    monkeypatch.setenv("LA_TEST_FORCE_WAIT", "1")
+    monkeypatch.setenv("LA_MBAR_TIMEOUT_NS", "2000000")
+    la.delta_prefill(kd, vd, bd)
+    assert la.delta_read_device_status() == 4  # LA_ERR_TIMEOUT
+    assert la.delta_read_device_status() == 0  # reading clears it
+    monkeypatch.delenv("LA_TEST_FORCE_WAIT")
+    monkeypatch.delenv("LA_MBAR_TIMEOUT_NS")
+    reads, S = la.delta_prefill(kd, vd, bd)
+    assert la.delta_read_device_status() == 0
+    rr, rS = orc.delta(f64(k), f64(v), f64(beta))
+    assert relmax(f64(reads), rr) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
 
 
 def test_delta_in_place_alias_and_zero_length(la, orc):
