@@ -21,6 +21,12 @@ page "线性注意力与SSM", sections 1.3 and 3):
 * ``la_chunked``: the same outputs chunk by chunk, carrying only (S, z)
 * ``la_decode_step``: one step of the recurrence on a given state
 * ``delta``: reads_t = k_t^T S_{t-1}; S_t = S_{t-1} + beta_t k_t (v_t - reads_t)^T
+* ``gated_delta``: D = alpha_t S_{t-1}; reads_t = k_t^T D;
+  S_t = D + beta_t k_t (v_t - reads_t)^T   (forget, then correct)
+* ``la_variant``: the recurrence with a scalar decay alpha_t of the old (S, z)
+  (mode 0, write then read), read-then-write (mode 1, strictly past), or
+  non-causal (mode 2: the state over all tokens, then every query reads it)
+* ``la_variant_quadratic``: the same outputs from explicit weights
 * ``outer_read``: additive identity-feature memory S = sum k v^T, read q^T S
 """
 from __future__ import annotations
@@ -73,9 +79,13 @@ def _load():
         lib.orc_la_decode_step.argtypes = [p, p, p, i, i, i, i, d, p, p, p, i]
         lib.orc_delta.argtypes = [p, p, p, i, i, i, i, i, p, p, p, i]
         lib.orc_outer_read.argtypes = [p, p, i, i, i, p, i, p]
+        lib.orc_gated_delta.argtypes = [p, p, p, p, i, i, i, i, i, p, p, p, i]
+        lib.orc_la_variant.argtypes = [p, p, p, p, i, i, i, i, i, d, i, p, p, p, p, p, i]
+        lib.orc_la_variant_quadratic.argtypes = [p, p, p, p, i, i, i, i, i, d, i, p, p, p, i]
         for name in ("orc_phi", "orc_la_recurrent", "orc_la_quadratic",
                      "orc_la_chunked", "orc_la_decode_step", "orc_delta",
-                     "orc_outer_read", "orc_default_threads"):
+                     "orc_outer_read", "orc_default_threads", "orc_gated_delta",
+                     "orc_la_variant", "orc_la_variant_quadratic"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -180,6 +190,51 @@ def delta(k, v, beta, S0=None, threads=0):
     _check(_load().orc_delta(_ptr(k), _ptr(v), _ptr(beta), B, H, N, dk, dv,
                              _ptr(S0), _ptr(reads), _ptr(S), threads), "delta")
     return reads, S
+
+
+def gated_delta(k, v, beta, alpha=None, S0=None, threads=0):
+    """Returns (reads, S_N) of the gated delta rule (alpha None = 1)."""
+    k, v, beta, alpha, S0 = map(_f64, (k, v, beta, alpha, S0))
+    B, H, N, dk, dv = _shape4(k, v)
+    if beta.shape != (B, H, N) or (alpha is not None and alpha.shape != (B, H, N)):
+        raise ValueError("beta and alpha must be [B, H, N]")
+    reads = np.empty((B, H, N, dv))
+    S = np.empty((B, H, dk, dv))
+    _check(_load().orc_gated_delta(_ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), B, H, N,
+                                   dk, dv, _ptr(S0), _ptr(reads), _ptr(S), threads),
+           "gated_delta")
+    return reads, S
+
+
+MODE_CAUSAL, MODE_READ_BEFORE_WRITE, MODE_NONCAUSAL = 0, 1, 2
+
+
+def la_variant(q, k, v, alpha=None, mode=MODE_CAUSAL, eps=1e-6, S0=None, z0=None,
+               threads=0):
+    """Returns (o, S_N, z_N) of a variant of the recurrence (see la_oracle.h)."""
+    q, k, v, alpha, S0, z0 = map(_f64, (q, k, v, alpha, S0, z0))
+    B, H, N, dk, dv = _shape4(q, v)
+    if alpha is not None and alpha.shape != (B, H, N):
+        raise ValueError("alpha must be [B, H, N]")
+    o = np.empty((B, H, N, dv))
+    S = np.empty((B, H, dk, dv))
+    z = np.empty((B, H, dk))
+    _check(_load().orc_la_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H, N, dk,
+                                  dv, eps, int(mode), _ptr(S0), _ptr(z0), _ptr(o),
+                                  _ptr(S), _ptr(z), threads), "la_variant")
+    return o, S, z
+
+
+def la_variant_quadratic(q, k, v, alpha=None, mode=MODE_CAUSAL, eps=1e-6, S0=None,
+                         z0=None, threads=0):
+    """Returns o of a variant from its explicit weights (small N only)."""
+    q, k, v, alpha, S0, z0 = map(_f64, (q, k, v, alpha, S0, z0))
+    B, H, N, dk, dv = _shape4(q, v)
+    o = np.empty((B, H, N, dv))
+    _check(_load().orc_la_variant_quadratic(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), B, H,
+                                            N, dk, dv, eps, int(mode), _ptr(S0), _ptr(z0),
+                                            _ptr(o), threads), "la_variant_quadratic")
+    return o
 
 
 def outer_read(keys, values, queries):

@@ -11,6 +11,7 @@
  *
  * Citations (page title, section):
  *   P1 = "AIGC 基本功|线性、循环与记忆架构-LinearMem" (jefxiong.cn)
+ *   P2 = linear-attention explainer (aiqz.cc), section 线性化核心 and its listing
  *   P3 = "线性注意力与SSM" (ggaaooppeenngg.github.io)
  *   P5 = "sequence-models" practice notes (wineandchord.com)
  */
@@ -375,6 +376,223 @@ int orc_delta(const double* k, const double* v, const double* beta, int B,
   if (N > 0 && (!k || !v || !beta || !reads)) return -1;
   delta_args a = {k, v, beta, S0, N, dk, dv, reads, S_N};
   for_each_head((int64_t)B * H, nthreads, delta_head, &a);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* (7) Gated delta rule, P1 section 03 ("再引入遗忘系数 alpha_t"), the same
+ * page's appendix delta_step(S, k, v, beta, alpha): first decay the old state,
+ * then correct against the decayed prediction:
+ *   D = alpha_t S_{t-1};  reads[t] = k_t^T D;  S_t = D + beta_t k_t (v_t - reads[t])^T.
+ * alpha = NULL means alpha_t = 1 (the plain delta rule of (5)).  The reported
+ * read is the prediction the correction uses, k_t^T D. */
+typedef struct {
+  const double *k, *v, *beta, *alpha, *S0;
+  int N, dk, dv;
+  double *reads, *S_N;
+} gdelta_args;
+
+static void gated_delta_head(void* p, int64_t h) {
+  const gdelta_args* a = (const gdelta_args*)p;
+  const int N = a->N, dk = a->dk, dv = a->dv;
+  double* S = a->S_N + h * (int64_t)dk * dv;
+  if (a->S0) memcpy(S, a->S0 + h * (int64_t)dk * dv, sizeof(double) * dk * dv);
+  else memset(S, 0, sizeof(double) * dk * dv);
+  double* corr = (double*)malloc(sizeof(double) * dv);
+  for (int t = 0; t < N; ++t) {
+    const double* key = a->k + (h * (int64_t)N + t) * dk;
+    const double* val = a->v + (h * (int64_t)N + t) * dv;
+    const double write_rate = a->beta[h * (int64_t)N + t];
+    const double forget = a->alpha ? a->alpha[h * (int64_t)N + t] : 1.0;
+    double* pred = a->reads + (h * (int64_t)N + t) * dv;
+    /* decay: D = alpha_t S */
+    for (int e = 0; e < dk * dv; ++e) S[e] *= forget;
+    /* prediction from the decayed state, and the correction v - k^T D */
+    for (int j = 0; j < dv; ++j) {
+      double kd = 0.0;
+      for (int i = 0; i < dk; ++i) kd += key[i] * S[i * dv + j];
+      pred[j] = kd;
+      corr[j] = val[j] - kd;
+    }
+    /* write: S = D + beta k corr^T */
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) S[i * dv + j] += write_rate * key[i] * corr[j];
+  }
+  free(corr);
+}
+
+int orc_gated_delta(const double* k, const double* v, const double* beta,
+                    const double* alpha, int B, int H, int N, int dk, int dv,
+                    const double* S0, double* reads, double* S_N, int nthreads) {
+  if (B < 1 || H < 1 || N < 0 || dk < 1 || dv < 1 || !S_N) return -1;
+  if (N > 0 && (!k || !v || !beta || !reads)) return -1;
+  gdelta_args a = {k, v, beta, alpha, S0, N, dk, dv, reads, S_N};
+  for_each_head((int64_t)B * H, nthreads, gated_delta_head, &a);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* (8) Variants of the recurrence of (1).
+ *   mode 0 (write, then read; P1 section 03) with a scalar decay of the old
+ *     state, P3 sections 3-4 (Mamba-2: S_t = alpha_t S_{t-1} + v_t k_t^T, the
+ *     linear-attention recurrence with one scalar on the old state).  The
+ *     normalizer is part of the state and decays with it:
+ *       S_t = alpha_t S_{t-1} + phi(k_t) v_t^T,  z_t = alpha_t z_{t-1} + phi(k_t),
+ *       o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps).
+ *   mode 1 (read, then write: strictly past; P1 section 03 and section 09,
+ *     first change): o_t = phi(q_t)^T S_{t-1} / (phi(q_t)^T z_{t-1} + eps),
+ *     then the write of mode 0 (decay included).  From a zero state the first
+ *     read is 0.
+ *   mode 2 (non-causal; P2 section 线性化核心 and its linear_attention): the state is
+ *     formed once over all N tokens, S = S0 + sum_t phi(k_t) v_t^T,
+ *     z = z0 + sum_t phi(k_t), and every query reads it.  No decay (alpha must
+ *     be NULL).
+ * alpha = NULL means alpha_t = 1. */
+typedef struct {
+  const double *q, *k, *v, *alpha, *S0, *z0;
+  int N, dk, dv, mode;
+  double eps;
+  double *o, *S_N, *z_N;
+} var_args;
+
+static void var_read(const double* fq, const double* S, const double* z, int dk,
+                     int dv, double eps, double* ot) {
+  double den = 0.0;
+  for (int i = 0; i < dk; ++i) den += fq[i] * z[i];
+  den += eps;
+  for (int j = 0; j < dv; ++j) {
+    double num = 0.0;
+    for (int i = 0; i < dk; ++i) num += fq[i] * S[i * dv + j];
+    ot[j] = num / den;
+  }
+}
+
+static void var_write(const double* fk, const double* vt, double at, double* S,
+                      double* z, int dk, int dv) {
+  for (int i = 0; i < dk; ++i) {
+    for (int j = 0; j < dv; ++j) S[i * dv + j] = at * S[i * dv + j] + fk[i] * vt[j];
+    z[i] = at * z[i] + fk[i];
+  }
+}
+
+static void variant_head(void* p, int64_t h) {
+  const var_args* a = (const var_args*)p;
+  const int N = a->N, dk = a->dk, dv = a->dv;
+  double* S = a->S_N + h * (int64_t)dk * dv;
+  double* z = a->z_N + h * (int64_t)dk;
+  if (a->S0) memcpy(S, a->S0 + h * (int64_t)dk * dv, sizeof(double) * dk * dv);
+  else memset(S, 0, sizeof(double) * dk * dv);
+  if (a->z0) memcpy(z, a->z0 + h * (int64_t)dk, sizeof(double) * dk);
+  else memset(z, 0, sizeof(double) * dk);
+  double* fk = (double*)malloc(sizeof(double) * dk);
+  double* fq = (double*)malloc(sizeof(double) * dk);
+  if (a->mode == 2) {
+    /* the state over all tokens first */
+    for (int t = 0; t < N; ++t) {
+      const double* kt = a->k + (h * (int64_t)N + t) * dk;
+      const double* vt = a->v + (h * (int64_t)N + t) * dv;
+      for (int i = 0; i < dk; ++i) fk[i] = phi(kt[i]);
+      var_write(fk, vt, 1.0, S, z, dk, dv);
+    }
+    /* then every query reads it */
+    for (int t = 0; t < N; ++t) {
+      const double* qt = a->q + (h * (int64_t)N + t) * dk;
+      for (int i = 0; i < dk; ++i) fq[i] = phi(qt[i]);
+      var_read(fq, S, z, dk, dv, a->eps, a->o + (h * (int64_t)N + t) * dv);
+    }
+  } else {
+    for (int t = 0; t < N; ++t) {
+      const double* qt = a->q + (h * (int64_t)N + t) * dk;
+      const double* kt = a->k + (h * (int64_t)N + t) * dk;
+      const double* vt = a->v + (h * (int64_t)N + t) * dv;
+      double* ot = a->o + (h * (int64_t)N + t) * dv;
+      const double at = a->alpha ? a->alpha[h * (int64_t)N + t] : 1.0;
+      for (int i = 0; i < dk; ++i) fk[i] = phi(kt[i]);
+      for (int i = 0; i < dk; ++i) fq[i] = phi(qt[i]);
+      if (a->mode == 1) var_read(fq, S, z, dk, dv, a->eps, ot);
+      var_write(fk, vt, at, S, z, dk, dv);
+      if (a->mode == 0) var_read(fq, S, z, dk, dv, a->eps, ot);
+    }
+  }
+  free(fk);
+  free(fq);
+}
+
+int orc_la_variant(const double* q, const double* k, const double* v,
+                   const double* alpha, int B, int H, int N, int dk, int dv,
+                   double eps, int mode, const double* S0, const double* z0,
+                   double* o, double* S_N, double* z_N, int nthreads) {
+  if (la_check(q, k, v, B, H, N, dk, dv, eps, o) || !S_N || !z_N) return -1;
+  if (mode < 0 || mode > 2 || (mode == 2 && alpha)) return -1;
+  var_args a = {q, k, v, alpha, S0, z0, N, dk, dv, mode, eps, o, S_N, z_N};
+  for_each_head((int64_t)B * H, nthreads, variant_head, &a);
+  return 0;
+}
+
+/* (9) The outputs of (8) from explicit weights, the pages' quadratic form
+ * (P1 appendix explicit_linear) with the recurrence unrolled: the read at t
+ * sees token s with weight phi(q_t).phi(k_s) times the decay applied to it
+ * afterwards, and the initial state with the decay applied since the start:
+ *   mode 0: tokens s <= t, decay prod_{s < r <= t} alpha_r; S0, z0 with
+ *           prod_{r <= t} alpha_r
+ *   mode 1: tokens s < t, decay prod_{s < r < t} alpha_r; S0, z0 with
+ *           prod_{r < t} alpha_r
+ *   mode 2: every token, no decay; S0, z0 as they are. */
+static void variant_quadratic_head(void* p, int64_t h) {
+  const var_args* a = (const var_args*)p;
+  const int N = a->N, dk = a->dk, dv = a->dv, mode = a->mode;
+  const double* S0 = a->S0 ? a->S0 + h * (int64_t)dk * dv : NULL;
+  const double* z0 = a->z0 ? a->z0 + h * (int64_t)dk : NULL;
+  const double* al = a->alpha ? a->alpha + h * (int64_t)N : NULL;
+  double* fq = (double*)malloc(sizeof(double) * dk);
+  double* fk = (double*)malloc(sizeof(double) * dk);
+  double* num = (double*)malloc(sizeof(double) * dv);
+  for (int t = 0; t < N; ++t) {
+    const double* qt = a->q + (h * (int64_t)N + t) * dk;
+    for (int r = 0; r < dk; ++r) fq[r] = phi(qt[r]);
+    /* decay of the initial state up to the read */
+    const int last = mode == 0 ? t : t - 1; /* alpha_r applied for r <= last */
+    double g0 = 1.0;
+    if (al && mode != 2)
+      for (int r = 0; r <= last; ++r) g0 *= al[r];
+    double den = 0.0;
+    for (int j = 0; j < dv; ++j) num[j] = 0.0;
+    if (S0)
+      for (int r = 0; r < dk; ++r)
+        for (int j = 0; j < dv; ++j) num[j] += g0 * fq[r] * S0[r * dv + j];
+    if (z0)
+      for (int r = 0; r < dk; ++r) den += g0 * fq[r] * z0[r];
+    const int send = mode == 0 ? t : (mode == 1 ? t - 1 : N - 1);
+    for (int s = 0; s <= send; ++s) {
+      const double* ks = a->k + (h * (int64_t)N + s) * dk;
+      const double* vs = a->v + (h * (int64_t)N + s) * dv;
+      for (int r = 0; r < dk; ++r) fk[r] = phi(ks[r]);
+      double g = 1.0;
+      if (al && mode != 2)
+        for (int r = s + 1; r <= last; ++r) g *= al[r];
+      double w = 0.0;
+      for (int r = 0; r < dk; ++r) w += fq[r] * fk[r];
+      w *= g;
+      den += w;
+      for (int j = 0; j < dv; ++j) num[j] += w * vs[j];
+    }
+    den += a->eps;
+    double* ot = a->o + (h * (int64_t)N + t) * dv;
+    for (int j = 0; j < dv; ++j) ot[j] = num[j] / den;
+  }
+  free(fq);
+  free(fk);
+  free(num);
+}
+
+int orc_la_variant_quadratic(const double* q, const double* k, const double* v,
+                             const double* alpha, int B, int H, int N, int dk,
+                             int dv, double eps, int mode, const double* S0,
+                             const double* z0, double* o, int nthreads) {
+  if (la_check(q, k, v, B, H, N, dk, dv, eps, o)) return -1;
+  if (mode < 0 || mode > 2 || (mode == 2 && alpha)) return -1;
+  var_args a = {q, k, v, alpha, S0, z0, N, dk, dv, mode, eps, o, NULL, NULL};
+  for_each_head((int64_t)B * H, nthreads, variant_quadratic_head, &a);
   return 0;
 }
 

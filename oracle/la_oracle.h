@@ -77,6 +77,27 @@ int orc_delta(const double* k, const double* v, const double* beta,
               int B, int H, int N, int dk, int dv, const double* S0,
               double* reads, double* S_N, int nthreads);
 
+/* Gated delta rule: D = alpha_t S_{t-1}; reads[t] = k_t^T D;
+ * S_t = D + beta_t k_t (v_t - reads[t])^T.  alpha [B][H][N] or NULL (= 1). */
+int orc_gated_delta(const double* k, const double* v, const double* beta,
+                    const double* alpha, int B, int H, int N, int dk, int dv,
+                    const double* S0, double* reads, double* S_N, int nthreads);
+
+/* Variants of the recurrence: mode 0 write-then-read with a scalar decay of
+ * the old (S, z) by alpha_t; mode 1 read-then-write (strictly past), same
+ * decay; mode 2 non-causal (state over all tokens, then every query reads;
+ * alpha must be NULL).  alpha [B][H][N] or NULL (= 1). */
+int orc_la_variant(const double* q, const double* k, const double* v,
+                   const double* alpha, int B, int H, int N, int dk, int dv,
+                   double eps, int mode, const double* S0, const double* z0,
+                   double* o, double* S_N, double* z_N, int nthreads);
+
+/* The outputs of orc_la_variant from explicit (quadratic) weights. */
+int orc_la_variant_quadratic(const double* q, const double* k, const double* v,
+                             const double* alpha, int B, int H, int N, int dk,
+                             int dv, double eps, int mode, const double* S0,
+                             const double* z0, double* o, int nthreads);
+
 /* Additive associative memory with the identity feature map (test-only
  * primitive): S = sum_m keys[m] values[m]^T, reads[p] = queries[p]^T S.
  * keys [M][dk], values [M][dv], queries [P][dk], reads [P][dv]. */

@@ -50,6 +50,24 @@ MUTANTS = [
     ("delta_read_after_write",
      "      rt[j] = r;\n      err[j] = vt[j] - r;\n    }\n    for (int i = 0; i < dk; ++i)\n      for (int j = 0; j < dv; ++j) S[i * dv + j] += bt * kt[i] * err[j];",
      "      err[j] = vt[j] - r;\n    }\n    for (int i = 0; i < dk; ++i)\n      for (int j = 0; j < dv; ++j) S[i * dv + j] += bt * kt[i] * err[j];\n    for (int j = 0; j < dv; ++j) {\n      double r = 0.0;\n      for (int i = 0; i < dk; ++i) r += kt[i] * S[i * dv + j];\n      rt[j] = r;\n    }"),
+    ("gated_delta_decays_after_read",
+     "    for (int e = 0; e < dk * dv; ++e) S[e] *= forget;\n    /* prediction from the decayed state, and the correction v - k^T D */\n    for (int j = 0; j < dv; ++j) {\n      double kd = 0.0;\n      for (int i = 0; i < dk; ++i) kd += key[i] * S[i * dv + j];\n      pred[j] = kd;\n      corr[j] = val[j] - kd;\n    }",
+     "    for (int j = 0; j < dv; ++j) {\n      double kd = 0.0;\n      for (int i = 0; i < dk; ++i) kd += key[i] * S[i * dv + j];\n      pred[j] = kd;\n      corr[j] = val[j] - kd;\n    }\n    for (int e = 0; e < dk * dv; ++e) S[e] *= forget;"),
+    ("gated_delta_ignores_alpha", "S[e] *= forget;", "S[e] *= 1.0;"),
+    ("gated_delta_drops_beta", "S[i * dv + j] += write_rate * key[i] * corr[j];",
+     "S[i * dv + j] += key[i] * corr[j];"),
+    ("variant_decay_skips_z", "    z[i] = at * z[i] + fk[i];", "    z[i] = z[i] + fk[i];"),
+    ("variant_decay_on_new_term", "S[i * dv + j] = at * S[i * dv + j] + fk[i] * vt[j];",
+     "S[i * dv + j] = at * (S[i * dv + j] + fk[i] * vt[j]);"),
+    ("variant_rbw_reads_after_write", "      if (a->mode == 1) var_read(fq, S, z, dk, dv, a->eps, ot);",
+     "      if (a->mode == 1) {}"),
+    ("variant_noncausal_reads_prefix",
+     "    /* then every query reads it */\n    for (int t = 0; t < N; ++t) {",
+     "    /* then every query reads it */\n    for (int t = 0; t < N && 0; ++t) {"),
+    ("variant_quadratic_strict_mask_for_causal", "const int send = mode == 0 ? t : (mode == 1 ? t - 1 : N - 1);",
+     "const int send = mode == 0 ? t - 1 : (mode == 1 ? t - 1 : N - 1);"),
+    ("variant_quadratic_decay_off_by_one", "for (int r = s + 1; r <= last; ++r) g *= al[r];",
+     "for (int r = s; r <= last; ++r) g *= al[r];"),
     ("outer_read_transposed", "S[i * dv + j] += keys[m * dk + i] * values[m * dv + j];",
      "S[i * dv + j] += keys[m * dk + j % dk] * values[m * dv + i % dv];"),
 ]
@@ -67,6 +85,8 @@ def _pin_functions():
             out.append(lambda orc, f=fn: [f(orc, a, b) for a, b in ((1, 1), (3, 5), (8, 2))])
         elif name == "test_chunk_size_independence":
             out.append(lambda orc, f=fn: [f(orc, c) for c in (1, 3, 16, 101)])
+        elif name == "test_variant_recurrence_equals_explicit_weights":
+            out.append(lambda orc, f=fn: [f(orc, m) for m in (0, 1, 2)])
     return out
 
 

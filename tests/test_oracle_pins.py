@@ -365,3 +365,151 @@ def test_state_accounting(orc):
     assert state == g["state_bytes"]
     assert round(state / 2 ** 20, 6) == g["state_mib_rounded"]
     assert round(history / state, 2) == g["ratio_rounded"]
+
+
+# --------------------------------------------------------------------------
+# gated delta rule (forgetting alpha, then correction)
+
+def test_p1_gated_delta_unrelated_key(orc):
+    # the pages' experiment: identity state, write the first key with alpha
+    # then read the orthogonal key (a second token with beta = 0 reads it)
+    g = golden("p1_gated_delta.json")
+    S0 = np.array(g["state"])[None, None]
+    k = np.array([g["key"], g["orthogonal_key"]])[None, None]
+    v = np.array([g["value"], [0.0, 0.0]])[None, None]
+    beta = np.array([[[g["beta"], 0.0]]])
+    for alpha_t, want in ((g["gated_alpha"], g["gated_unrelated_key_read"]),
+                          (1.0, g["no_forgetting_unrelated_key_read"])):
+        alpha = np.array([[[alpha_t, 1.0]]])
+        reads, S = orc.gated_delta(k, v, beta, alpha, S0=S0)
+        np.testing.assert_allclose(reads[0, 0, 1], want, rtol=0, atol=1e-15)
+        # the written key reads the written value exactly (beta = 1, unit key)
+        np.testing.assert_allclose(np.array(g["key"]) @ S[0, 0], g["value"], atol=1e-15)
+
+
+def test_gated_delta_alpha_one_is_the_delta_rule(orc):
+    r = _rng(60)
+    k = r.normal(size=(2, 2, 30, 5))
+    v = r.normal(size=(2, 2, 30, 3))
+    beta = r.uniform(size=(2, 2, 30))
+    S0 = r.normal(size=(2, 2, 5, 3))
+    rg, Sg = orc.gated_delta(k, v, beta, np.ones((2, 2, 30)), S0=S0)
+    rd, Sd = orc.delta(k, v, beta, S0=S0)
+    np.testing.assert_allclose(rg, rd, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(Sg, Sd, rtol=0, atol=1e-13)
+
+
+def test_gated_delta_pure_forgetting_closed_form(orc):
+    # beta = 0: nothing is written; the state decays geometrically and every
+    # read is the decayed prediction alpha^(t+1) k_t^T S0
+    r = _rng(61)
+    N, a = 12, 0.9
+    k = r.normal(size=(1, 1, N, 4))
+    v = r.normal(size=(1, 1, N, 2))
+    S0 = r.normal(size=(1, 1, 4, 2))
+    reads, S = orc.gated_delta(k, v, np.zeros((1, 1, N)), np.full((1, 1, N), a), S0=S0)
+    for t in range(N):
+        np.testing.assert_allclose(reads[0, 0, t], a ** (t + 1) * k[0, 0, t] @ S0[0, 0],
+                                   rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(S, a ** N * S0, rtol=1e-13)
+
+
+def test_gated_delta_forgets_before_correcting(orc):
+    # alpha = 0 erases the old memory before the correction: one token with a
+    # unit key and beta = 1 leaves exactly k v^T, whatever S0 was
+    r = _rng(62)
+    k = np.array([0.6, 0.8, 0.0])[None, None, None]
+    v = r.normal(size=(1, 1, 1, 2))
+    S0 = r.normal(size=(1, 1, 3, 2))
+    reads, S = orc.gated_delta(k, v, np.ones((1, 1, 1)), np.zeros((1, 1, 1)), S0=S0)
+    np.testing.assert_allclose(reads[0, 0, 0], 0.0, atol=1e-15)
+    np.testing.assert_allclose(S[0, 0], np.outer(k[0, 0, 0], v[0, 0, 0]), atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# variants: scalar decay, read before write, non-causal
+
+def test_variant_causal_without_decay_is_the_recurrence(orc):
+    q, k, v = _rand_la(63, 2, 2, 20, 4, 3)
+    r = _rng(64)
+    S0 = r.uniform(size=(2, 2, 4, 3))
+    z0 = r.uniform(size=(2, 2, 4))
+    o1, S1, z1 = orc.la_variant(q, k, v, None, orc.MODE_CAUSAL, S0=S0, z0=z0)
+    o2, S2, z2 = orc.la_recurrent(q, k, v, S0=S0, z0=z0)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(S1, S2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(z1, z2, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_variant_recurrence_equals_explicit_weights(orc, mode):
+    # an independent evaluation order: the unrolled weights (decay products
+    # and masks written out per pair of tokens) against the token loop
+    q, k, v = _rand_la(65 + mode, 2, 3, 17, 5, 4)
+    r = _rng(70 + mode)
+    alpha = None if mode == 2 else r.uniform(0.3, 1.0, size=(2, 3, 17))
+    S0 = r.uniform(size=(2, 3, 5, 4))
+    z0 = r.uniform(size=(2, 3, 5))
+    o_rec, _, _ = orc.la_variant(q, k, v, alpha, mode, S0=S0, z0=z0)
+    o_quad = orc.la_variant_quadratic(q, k, v, alpha, mode, S0=S0, z0=z0)
+    assert _relmax(o_rec, o_quad) < 1e-12
+
+
+def test_read_before_write_first_read_is_zero_and_strictly_past(orc):
+    # P1 section 09, first change: the first read is zero, later reads see
+    # only strictly earlier tokens
+    q, k, v = _rand_la(75, 1, 1, 9, 3, 2)
+    o, _, _ = orc.la_variant(q, k, v, None, orc.MODE_READ_BEFORE_WRITE)
+    np.testing.assert_array_equal(o[0, 0, 0], 0.0)
+    # token t's value never reaches o_t: changing the last value changes nothing
+    v2 = v.copy()
+    v2[0, 0, -1] += 100.0
+    o2, _, _ = orc.la_variant(q, k, v2, None, orc.MODE_READ_BEFORE_WRITE)
+    np.testing.assert_array_equal(o, o2)
+    # and o_t (read before write) is the write-then-read output one token late
+    # when the query is held fixed: compare against the causal recurrence on
+    # the shifted sequence
+    oc, _, _ = orc.la_recurrent(q[:, :, 1:], k[:, :, :-1], v[:, :, :-1])
+    np.testing.assert_allclose(o[:, :, 1:], oc, rtol=1e-13, atol=1e-15)
+
+
+def test_decay_zero_attends_to_the_current_token_only(orc):
+    q, k, v = _rand_la(76, 1, 2, 7, 4, 3)
+    eps = 1e-6
+    o, S, z = orc.la_variant(q, k, v, np.zeros((1, 2, 7)), orc.MODE_CAUSAL, eps=eps)
+    fq, fk = orc.phi(q), orc.phi(k)
+    w = np.sum(fq * fk, axis=-1, keepdims=True)
+    np.testing.assert_allclose(o, w * v / (w + eps), rtol=1e-13)
+    np.testing.assert_allclose(S[0, 1], np.outer(fk[0, 1, -1], v[0, 1, -1]), rtol=1e-13)
+
+
+def test_noncausal_reads_the_whole_sequence(orc):
+    # P2 linear_attention: S = phi(K)^T V and z = sum phi(K) once, every query
+    # reads the same state (with eps = 0, the page's form exactly)
+    q, k, v = _rand_la(77, 1, 1, 11, 4, 3)
+    o, S, z = orc.la_variant(q, k, v, None, orc.MODE_NONCAUSAL, eps=0.0)
+    fq, fk = orc.phi(q[0, 0]), orc.phi(k[0, 0])
+    Sx = fk.T @ v[0, 0]
+    zx = fk.sum(axis=0)
+    np.testing.assert_allclose(o[0, 0], (fq @ Sx) / (fq @ zx)[:, None], rtol=1e-13)
+    np.testing.assert_allclose(S[0, 0], Sx, rtol=1e-13)
+    # not causal: a change to the last value moves the first output
+    v2 = v.copy()
+    v2[0, 0, -1] += 1.0
+    o2, _, _ = orc.la_variant(q, k, v2, None, orc.MODE_NONCAUSAL, eps=0.0)
+    assert np.max(np.abs(o2[0, 0, 0] - o[0, 0, 0])) > 1e-6
+
+
+def test_decayed_state_closed_form(orc):
+    # constant decay a: S_N = a^N S0 + sum_t a^(N-1-t) phi(k_t) v_t^T
+    q, k, v = _rand_la(78, 1, 1, 10, 3, 2)
+    a = 0.7
+    r = _rng(79)
+    S0 = r.uniform(size=(1, 1, 3, 2))
+    z0 = r.uniform(size=(1, 1, 3))
+    _, S, z = orc.la_variant(q, k, v, np.full((1, 1, 10), a), orc.MODE_CAUSAL, S0=S0, z0=z0)
+    fk = orc.phi(k[0, 0])
+    Sx = a ** 10 * S0[0, 0] + sum(a ** (9 - t) * np.outer(fk[t], v[0, 0, t]) for t in range(10))
+    zx = a ** 10 * z0[0, 0] + sum(a ** (9 - t) * fk[t] for t in range(10))
+    np.testing.assert_allclose(S[0, 0], Sx, rtol=1e-13)
+    np.testing.assert_allclose(z[0, 0], zx, rtol=1e-13)
