@@ -56,7 +56,8 @@ def _args():
     p.add_argument("--no-extra", action="store_true",
                    help="headline workload only (no long/decode/delta/e2e/cpu)")
     p.add_argument("--only", default="",
-                   help="comma list of extra workloads to run (long,decode,delta,pr1)")
+                   help="comma list of extra workloads to run "
+                        "(long,decode,delta,pr1,gated,decay)")
     p.add_argument("--profile-delta", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain delta_prefill calls of the delta workload and exit "
                         "(for profilers)")
@@ -392,6 +393,58 @@ def bench_delta(api, rank, world, reps=3):
             "bytes_per_call": nbytes, "hbm_gbs": nbytes / (ms_call * 1e-3) / 1e9}
 
 
+def bench_gated_delta(api, rank, world, reps=3):
+    """gated_delta_prefill on the delta workload with alpha ~ U(0.9, 1):
+    token by token on the FP32 pipe (4 dk dv flop per token)."""
+    import torch
+    from fixed_state_recurrent_gb300 import inputs
+    w = inputs.WORKLOADS["delta"]
+    dev = torch.device("cuda")
+    k, v, beta = inputs.delta_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype,
+                                     w.seed + 1000 * rank, device=dev)
+    g = torch.Generator(device=dev).manual_seed(5 + rank)
+    alpha = 0.9 + 0.1 * torch.rand((w.B, w.H, w.N), generator=g, device=dev)
+    reads = torch.empty((w.B, w.H, w.N, w.dv), device=dev)
+    S = torch.empty((w.B, w.H, w.dk, w.dv), device=dev)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    fn = lambda i: api.gated_delta_prefill(k, v, beta, alpha, reads=reads, S_N=S)
+    with torch.cuda.stream(stream):
+        fn(0)
+    _, per = _timed(fn, reps, stream, world)
+    ms = min(per)
+    tokens = w.B * w.H * w.N
+    return {"workload": "gated delta: B=8 H=16 N=8192 dk=dv=128, bf16 keys and values, "
+                        "alpha ~ U(0.9, 1), sigmoid beta", "ms_per_call": ms,
+            "tokens_per_s": tokens / (ms * 1e-3),
+            "fp32_tflops": 4.0 * w.dk * w.dv * tokens / (ms * 1e-3) / 1e12}
+
+
+def bench_decay_prefill(api, rank, world, reps=3):
+    """la_prefill_variant, write-then-read with a per-token decay, on the
+    headline prefill shape: CUDA cores, one block per head."""
+    import torch
+    from fixed_state_recurrent_gb300 import inputs
+    w = inputs.WORKLOADS["prefill"]
+    dev = torch.device("cuda")
+    q, k, v = _device_inputs(w, w.seed + 1000 * rank, dev)
+    g = torch.Generator(device=dev).manual_seed(6 + rank)
+    alpha = 0.9 + 0.1 * torch.rand((w.B, w.H, w.N), generator=g, device=dev)
+    o = torch.empty((w.B, w.H, w.N, w.dv), device=dev)
+    S = torch.empty((w.B, w.H, w.dk, w.dv), device=dev)
+    z = torch.empty((w.B, w.H, w.dk), device=dev)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    fn = lambda i: api.prefill_variant(q, k, v, alpha, 0, o=o, S_N=S, z_N=z)
+    with torch.cuda.stream(stream):
+        fn(0)
+    _, per = _timed(fn, reps, stream, world)
+    ms = min(per)
+    return {"workload": "decayed prefill: B=4 H=8 N=4096 dk=dv=64 bf16, alpha ~ U(0.9, 1), "
+                        "write then read", "ms_per_call": ms,
+            "tokens_per_s": w.tokens / (ms * 1e-3)}
+
+
 def bench_simple_prefill(api, wname, rank, world, reps=5):
     import torch
     from fixed_state_recurrent_gb300 import inputs
@@ -553,7 +606,8 @@ def main():
 
     extra = {}
     e2e = None
-    wanted = set(x for x in args.only.split(",") if x) or {"long", "decode", "delta", "pr1"}
+    wanted = set(x for x in args.only.split(",") if x) or {"long", "decode", "delta", "pr1",
+                                                             "gated", "decay"}
     if not args.no_extra:
         if "long" in wanted:
             extra["long"] = bench_simple_prefill(api, "long", rank, world)
@@ -563,6 +617,10 @@ def main():
             extra["delta"] = bench_delta(api, rank, world)
         if "pr1" in wanted:
             extra["pr1"] = bench_simple_prefill(api, "pr1", rank, world)
+        if "gated" in wanted:
+            extra["gated_delta"] = bench_gated_delta(api, rank, world)
+        if "decay" in wanted:
+            extra["decay_prefill"] = bench_decay_prefill(api, rank, world)
         e_ms, h2d, d2h = bench_e2e(api, w, max(args.steps // 4, 5), 3, rank, world)
         e_steps = max(args.steps // 4, 5)
         e2e = {"value": w.tokens * world / (e_ms * 1e-3 / e_steps), "unit": "tokens/s",

@@ -19,10 +19,12 @@ LIB_PATH = os.path.join(_HERE, "_build", "libla.so")
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
 LA_F32, LA_BF16 = 0, 1
+LA_MODE_CAUSAL, LA_MODE_READ_BEFORE_WRITE, LA_MODE_NONCAUSAL = 0, 1, 2
 
 SYMBOLS = ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
            "delta_prefill", "la_state_bytes", "la_status_string",
-           "la_read_device_status", "delta_read_device_status")
+           "la_read_device_status", "delta_read_device_status",
+           "la_prefill_variant", "gated_delta_prefill")
 
 
 class LAError(RuntimeError):
@@ -67,6 +69,11 @@ def load(path: str | None = None):
         lib.la_read_device_status.restype = i
         lib.delta_read_device_status.argtypes = [vp]
         lib.delta_read_device_status.restype = i
+        lib.la_prefill_variant.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, vp, i, vp, vp,
+                                           vp, vp, vp, vp]
+        lib.la_prefill_variant.restype = i
+        lib.gated_delta_prefill.argtypes = [vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
+        lib.gated_delta_prefill.restype = i
         _lib = lib
         return lib
 
@@ -212,6 +219,57 @@ def delta_prefill(k, v, beta, S0=None, *, reads=None, S_N=None):
                               _ptr(S0), _ptr(reads), _ptr(S_N), _stream(dev))
     _check("delta_prefill", st)
     return reads, S_N
+
+
+def gated_delta_prefill(k, v, beta, alpha=None, S0=None, *, reads=None, S_N=None):
+    """Gated delta rule: returns (reads, S_N).  See gated_delta_prefill in la.h."""
+    B, H, N, dk = k.shape
+    dv = v.shape[3]
+    dev = k.device
+    code = _dtype_code(k)
+    _need(v, "v", (B, H, N, dv), k.dtype, dev)
+    _need(beta, "beta", (B, H, N), torch.float32, dev)
+    _need(alpha, "alpha", (B, H, N), torch.float32, dev)
+    _need(S0, "S0", (B, H, dk, dv), torch.float32, dev)
+    if reads is None:
+        reads = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
+    if S_N is None:
+        S_N = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    _need(reads, "reads", (B, H, N, dv), torch.float32, dev)
+    _need(S_N, "S_N", (B, H, dk, dv), torch.float32, dev)
+    st = load().gated_delta_prefill(_ptr(k), _ptr(v), code, _ptr(beta), _ptr(alpha), B, H,
+                                    N, dk, dv, _ptr(S0), _ptr(reads), _ptr(S_N), _stream(dev))
+    _check("gated_delta_prefill", st)
+    return reads, S_N
+
+
+def prefill_variant(q, k, v, alpha=None, mode=LA_MODE_CAUSAL, eps=1e-6, S0=None, z0=None, *,
+                    o=None, S_N=None, z_N=None):
+    """la_prefill_variant: decayed state and/or another read order; returns
+    (o, S_N, z_N).  See la_prefill_variant in la.h."""
+    B, H, N, dk = q.shape
+    dv = v.shape[3]
+    dev = q.device
+    code = _dtype_code(q)
+    _need(k, "k", (B, H, N, dk), q.dtype, dev)
+    _need(v, "v", (B, H, N, dv), q.dtype, dev)
+    _need(alpha, "alpha", (B, H, N), torch.float32, dev)
+    _need(S0, "S0", (B, H, dk, dv), torch.float32, dev)
+    _need(z0, "z0", (B, H, dk), torch.float32, dev)
+    if o is None:
+        o = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
+    if S_N is None:
+        S_N = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    if z_N is None:
+        z_N = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
+    _need(o, "o", (B, H, N, dv), torch.float32, dev)
+    _need(S_N, "S_N", (B, H, dk, dv), torch.float32, dev)
+    _need(z_N, "z_N", (B, H, dk), torch.float32, dev)
+    st = load().la_prefill_variant(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, dk, dv,
+                                   ctypes.c_float(eps), _ptr(alpha), int(mode), _ptr(S0),
+                                   _ptr(z0), _ptr(o), _ptr(S_N), _ptr(z_N), _stream(dev))
+    _check("la_prefill_variant", st)
+    return o, S_N, z_N
 
 
 def read_device_status(ws, stream=None) -> int:

@@ -16,6 +16,12 @@
 // stage's global loads are issued before the current stage is consumed.  The
 // work is 4 dk dv flops per token of fp32 FMA: this path is bound by the FP32
 // pipe, not by HBM.
+//
+// Gated form (same page, section 03, "再引入遗忘系数 alpha_t", and its appendix
+// delta_step): the old state decays first, D = alpha_t S_{t-1}; the read is
+// the prediction from D, k_t^T D = alpha_t (k_t^T S_{t-1}); the correction is
+// written on top of D: S_t = D + beta_t k_t (v_t - k_t^T D)^T.  alpha = NULL
+// is the plain rule above.
 #include "la_internal.h"
 
 namespace la {
@@ -27,15 +33,16 @@ constexpr int kPad = 36;     // words per lane slice (32 rows + 4 words of bank 
 constexpr int kRP = 32;      // max rows per lane
 constexpr int kThreads = 512;  // dv * P <= 512; lanes past dv * P only stage
 
-template <int P>
+template <int P, bool GATED>
 __global__ void __launch_bounds__(kThreads)
 delta_kernel(const void* __restrict__ kin, const void* __restrict__ vin,
-             bool bf16, const float* __restrict__ beta, int N, int dk, int dv,
-             const float* __restrict__ S0, float* __restrict__ reads,
+             bool bf16, const float* __restrict__ beta, const float* __restrict__ alpha,
+             int N, int dk, int dv, const float* __restrict__ S0, float* __restrict__ reads,
              float* __restrict__ S_N) {
   __shared__ __align__(16) float ks[kTB][4 * kPad];
   __shared__ float vs[kTB][kMaxD];
   __shared__ float bs[kTB];
+  __shared__ float as[kTB];
 
   const int tid = threadIdx.x;
   const int j = tid / P;      // column
@@ -68,10 +75,11 @@ delta_kernel(const void* __restrict__ kin, const void* __restrict__ vin,
       vreg[u] = (tok < N && i < dv) ? load_in(vin, (head * N + tok) * dv + i, bf16) : 0.f;
     }
   };
-  float breg = 0.f;
+  float breg = 0.f, areg = 1.f;
   if (N > 0) {
     fetch(0);
     if (tid < kTB) breg = tid < N ? beta[head * N + tid] : 0.f;
+    if (GATED && tid < kTB) areg = tid < N ? alpha[head * N + tid] : 1.f;
   }
   // words of the key slices that no feature maps to stay zero
   for (int e = tid; e < kTB * 4 * kPad; e += kThreads) {
@@ -91,11 +99,13 @@ delta_kernel(const void* __restrict__ kin, const void* __restrict__ vin,
       if (i < dk) ks[t][(i / rows) * kPad + (i % rows)] = kreg[u];
     }
     if (tid < kTB) bs[tid] = breg;
+    if (GATED && tid < kTB) as[tid] = areg;
     __syncthreads();
     // prefetch the next stage while this one is consumed
     if (t0 + kTB < N) {
       fetch(t0 + kTB);
       if (tid < kTB) breg = (t0 + kTB + tid < N) ? beta[head * N + t0 + kTB + tid] : 0.f;
+      if (GATED && tid < kTB) areg = (t0 + kTB + tid < N) ? alpha[head * N + t0 + kTB + tid] : 1.f;
     }
 
     const int nt = min(kTB, N - t0);
@@ -121,10 +131,19 @@ delta_kernel(const void* __restrict__ kin, const void* __restrict__ vin,
       for (int off = 1; off < P; off <<= 1)
         part += __shfl_xor_sync(0xffffffffu, part, off);
       if (active) {
-        if (p == 0) reads[(head * N + t0 + t) * dv + j] = part;
-        const float e = bs[t] * (vs[t][j] - part);
+        if (GATED) {
+          const float at = as[t];
+          part *= at;  // the prediction from the decayed state
+          if (p == 0) reads[(head * N + t0 + t) * dv + j] = part;
+          const float e = bs[t] * (vs[t][j] - part);
 #pragma unroll
-        for (int r = 0; r < kRP; ++r) S[r] += kr[r] * e;
+          for (int r = 0; r < kRP; ++r) S[r] = fmaf(at, S[r], kr[r] * e);
+        } else {
+          if (p == 0) reads[(head * N + t0 + t) * dv + j] = part;
+          const float e = bs[t] * (vs[t][j] - part);
+#pragma unroll
+          for (int r = 0; r < kRP; ++r) S[r] += kr[r] * e;
+        }
       }
     }
   }
@@ -139,12 +158,13 @@ delta_kernel(const void* __restrict__ kin, const void* __restrict__ vin,
 }  // namespace
 
 cudaError_t launch_delta_prefill(const void* k, const void* v, bool bf16,
-                                 const float* beta, int B, int H, int N,
+                                 const float* beta, const float* alpha, int B, int H, int N,
                                  int dk, int dv, const float* S0, float* reads,
                                  float* S_N, cudaStream_t stream) {
-  // bf16 keys and values at dk = dv = 128: the chunkwise tensor-core form
-  // (delta_chunked128.cu); fp32 inputs and other sizes run token by token here.
-  if (delta_chunked_supported(bf16, dk, dv))
+  // bf16 keys and values at dk = dv = 128 without gating: the chunkwise
+  // tensor-core form (delta_chunked128.cu); everything else runs token by
+  // token here.
+  if (!alpha && delta_chunked_supported(bf16, dk, dv))
     return launch_delta_chunked(k, v, beta, B, H, N, S0, reads, S_N, stream);
   const unsigned blocks = (unsigned)((size_t)B * H);
   // P lanes per column (a power of two, at most 4): enough that a lane holds
@@ -153,11 +173,23 @@ cudaError_t launch_delta_prefill(const void* k, const void* v, bool bf16,
   int P = 1;
   while (P * 32 < dk) P <<= 1;
   const int threads = kThreads;
-  switch (P) {
-    case 1: delta_kernel<1><<<blocks, threads, 0, stream>>>(k, v, bf16, beta, N, dk, dv, S0, reads, S_N); break;
-    case 2: delta_kernel<2><<<blocks, threads, 0, stream>>>(k, v, bf16, beta, N, dk, dv, S0, reads, S_N); break;
-    default: delta_kernel<4><<<blocks, threads, 0, stream>>>(k, v, bf16, beta, N, dk, dv, S0, reads, S_N); break;
+#define LA_DELTA_LAUNCH(PP, G)                                                              \
+  delta_kernel<PP, G><<<blocks, threads, 0, stream>>>(k, v, bf16, beta, alpha, N, dk, dv, S0, \
+                                                     reads, S_N)
+  if (alpha) {
+    switch (P) {
+      case 1: LA_DELTA_LAUNCH(1, true); break;
+      case 2: LA_DELTA_LAUNCH(2, true); break;
+      default: LA_DELTA_LAUNCH(4, true); break;
+    }
+  } else {
+    switch (P) {
+      case 1: LA_DELTA_LAUNCH(1, false); break;
+      case 2: LA_DELTA_LAUNCH(2, false); break;
+      default: LA_DELTA_LAUNCH(4, false); break;
+    }
   }
+#undef LA_DELTA_LAUNCH
   return cudaGetLastError();
 }
 

@@ -186,32 +186,101 @@ la_status la_decode_step(const void* q, const void* k, const void* v, la_dtype i
                                           dv, eps, S, z, o, stream));
 }
 
-la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const float* beta,
-                        int B, int H, int N, int dk, int dv, const float* S0,
-                        float* reads, float* S_N, cudaStream_t stream) {
+la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                             int B, int H, int N, int dk, int dv, float eps,
+                             const float* alpha, la_mode mode,
+                             const float* S0, const float* z0, float* o, float* S_N,
+                             float* z_N, cudaStream_t stream) {
+  if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return LA_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  if (mode != LA_MODE_CAUSAL && mode != LA_MODE_READ_BEFORE_WRITE && mode != LA_MODE_NONCAUSAL)
+    return LA_ERR_INVALID_ARG;
+  if (mode == LA_MODE_NONCAUSAL && alpha) return LA_ERR_INVALID_ARG;
+  if (!S_N || !z_N) return LA_ERR_INVALID_ARG;
+  if (N > 0 && (!q || !k || !v || !o)) return LA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, alpha, S0, z0, o, S_N, z_N};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
+
+  const size_t heads = (size_t)B * H;
+  const size_t eb = elem_bytes(in_dtype);
+  const Span sq = span(q, heads * N * dk * eb), sk = span(k, heads * N * dk * eb);
+  const Span sv = span(v, heads * N * dv * eb), so = span(o, heads * N * dv * 4);
+  const Span sa = span(alpha, heads * N * 4);
+  const Span sS0 = span(S0, heads * dk * dv * 4), sz0 = span(z0, heads * dk * 4);
+  const Span sSN = span(S_N, heads * dk * dv * 4), szN = span(z_N, heads * dk * 4);
+  const Span outs[] = {so, sSN, szN};
+  const Span ins[] = {sq, sk, sv, sa};
+  for (const Span& x : outs)
+    for (const Span& y : ins)
+      if (overlap(x, y)) return LA_ERR_INVALID_ARG;
+  if (overlap(so, sSN) || overlap(so, szN) || overlap(sSN, szN)) return LA_ERR_INVALID_ARG;
+  if (overlap(so, sS0) || overlap(so, sz0) || overlap(szN, sS0) || overlap(sSN, sz0))
+    return LA_ERR_INVALID_ARG;
+  if (overlap(sSN, sS0) && S_N != S0) return LA_ERR_INVALID_ARG;
+  if (overlap(szN, sz0) && z_N != z0) return LA_ERR_INVALID_ARG;
+
+  const la_status dev = check_device();
+  if (dev != LA_OK) return dev;
+  if (N == 0) {
+    cudaError_t e = copy_state(S0, S_N, heads * dk * dv * 4, stream);
+    if (e == cudaSuccess) e = copy_state(z0, z_N, heads * dk * 4, stream);
+    return from_cuda(e);
+  }
+  PrefillArgs a;
+  a.q = q; a.k = k; a.v = v;
+  a.bf16 = in_dtype == LA_BF16;
+  a.B = B; a.H = H; a.N = N; a.dk = dk; a.dv = dv;
+  a.eps = eps;
+  a.S0 = S0; a.z0 = z0;
+  a.o = o; a.S_N = S_N; a.z_N = z_N;
+  a.chunk = 0;
+  a.workspace = nullptr;
+  a.ws_bytes = 0;
+  return from_cuda(la::launch_prefill_variant_simt(a, alpha, (int)mode, stream));
+}
+
+static la_status delta_common(const void* k, const void* v, la_dtype in_dtype,
+                              const float* beta, const float* alpha, int B, int H, int N,
+                              int dk, int dv, const float* S0, float* reads, float* S_N,
+                              cudaStream_t stream) {
   if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return LA_ERR_INVALID_ARG;
   if (!S_N) return LA_ERR_INVALID_ARG;
   if (N > 0 && (!k || !v || !beta || !reads)) return LA_ERR_INVALID_ARG;
-  const void* ptrs[] = {k, v, beta, S0, reads, S_N};
+  const void* ptrs[] = {k, v, beta, alpha, S0, reads, S_N};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
   const size_t heads = (size_t)B * H;
   const size_t eb = elem_bytes(in_dtype);
   const Span sk = span(k, heads * N * dk * eb), sv = span(v, heads * N * dv * eb);
-  const Span sb = span(beta, heads * N * 4), sr = span(reads, heads * N * dv * 4);
+  const Span sb = span(beta, heads * N * 4), sa = span(alpha, heads * N * 4);
+  const Span sr = span(reads, heads * N * dv * 4);
   const Span sS0 = span(S0, heads * dk * dv * 4), sSN = span(S_N, heads * dk * dv * 4);
   const Span outs[] = {sr, sSN};
-  const Span ins[] = {sk, sv, sb};
-  for (const Span& a : outs)
-    for (const Span& b : ins)
-      if (overlap(a, b)) return LA_ERR_INVALID_ARG;
+  const Span ins[] = {sk, sv, sb, sa};
+  for (const Span& x : outs)
+    for (const Span& y : ins)
+      if (overlap(x, y)) return LA_ERR_INVALID_ARG;
   if (overlap(sr, sSN) || overlap(sr, sS0)) return LA_ERR_INVALID_ARG;
   if (overlap(sSN, sS0) && S_N != S0) return LA_ERR_INVALID_ARG;
   const la_status dev = check_device();
   if (dev != LA_OK) return dev;
   if (N == 0) return from_cuda(copy_state(S0, S_N, heads * dk * dv * 4, stream));
-  return from_cuda(la::launch_delta_prefill(k, v, in_dtype == LA_BF16, beta, B, H,
+  return from_cuda(la::launch_delta_prefill(k, v, in_dtype == LA_BF16, beta, alpha, B, H,
                                             N, dk, dv, S0, reads, S_N, stream));
+}
+
+la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const float* beta,
+                        int B, int H, int N, int dk, int dv, const float* S0,
+                        float* reads, float* S_N, cudaStream_t stream) {
+  return delta_common(k, v, in_dtype, beta, nullptr, B, H, N, dk, dv, S0, reads, S_N, stream);
+}
+
+la_status gated_delta_prefill(const void* k, const void* v, la_dtype in_dtype,
+                              const float* beta, const float* alpha, int B, int H, int N,
+                              int dk, int dv, const float* S0, float* reads, float* S_N,
+                              cudaStream_t stream) {
+  return delta_common(k, v, in_dtype, beta, alpha, B, H, N, dk, dv, S0, reads, S_N, stream);
 }
 
 la_status la_read_device_status(const void* workspace, cudaStream_t stream) {

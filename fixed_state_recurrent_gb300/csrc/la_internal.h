@@ -42,6 +42,11 @@ struct PrefillArgs {
 
 // CUDA-core prefill (any dk, dv <= 128; fp32 or bf16 inputs).
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
+// The CUDA-core kernel's variants: alpha = per-token decay of (S, z) or NULL;
+// mode 0 write-then-read, 1 read-then-write (strictly past), 2 non-causal
+// (alpha must be NULL).
+cudaError_t launch_prefill_variant_simt(const PrefillArgs& a, const float* alpha, int mode,
+                                        cudaStream_t stream);
 
 // Tensor-core chunked prefill for dk = dv = 64: aggregate, scan and output
 // launches (prefill_chunked64.cu).  The workspace size depends on the SM count
@@ -67,8 +72,9 @@ cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta
 // Returns and clears the chunked delta kernel's status word (current device).
 cudaError_t delta_status_take(unsigned* out);
 
+// alpha: per-token forgetting of the gated delta rule, or NULL (plain rule).
 cudaError_t launch_delta_prefill(const void* k, const void* v, bool bf16,
-                                 const float* beta, int B, int H, int N,
+                                 const float* beta, const float* alpha, int B, int H, int N,
                                  int dk, int dv, const float* S0, float* reads,
                                  float* S_N, cudaStream_t stream);
 

@@ -12,6 +12,15 @@
 // per token each thread writes its partial numerators (over its rows) and, for
 // column group 0, its partial denominators; one reduction per TB tokens then
 // forms o.  Three block barriers per TB tokens.
+//
+// Variants (la_prefill_variant), same state machinery:
+//   decay: S_t = alpha_t S_{t-1} + phi(k_t) v_t^T, z_t = alpha_t z_{t-1} + phi(k_t)
+//     (the linear-attention recurrence with one scalar on the old state: page
+//     "线性注意力与SSM", sections 3-4; the normalizer decays with the state);
+//   read before write: o_t from S_{t-1}, z_{t-1} (LinearMem sections 03 and 09:
+//     strictly past, the first read is 0);
+//   non-causal: the state over all N tokens first, then every query reads it
+//     (the linear-attention explainer, section 线性化核心).
 #include "la_internal.h"
 
 namespace la {
@@ -37,10 +46,12 @@ __host__ __device__ inline SimtShape simt_shape(int dk, int dv) {
   return s;
 }
 
+// MODE: 0 write then read, 1 read then write, 2 non-causal.  DECAY: alpha != NULL.
+template <int MODE, bool DECAY>
 __global__ void __launch_bounds__(kThreads)
 prefill_simt_kernel(const void* __restrict__ q, const void* __restrict__ k,
                     const void* __restrict__ v, bool bf16, int N, int dk, int dv,
-                    float eps, const float* __restrict__ S0,
+                    float eps, const float* __restrict__ alpha, const float* __restrict__ S0,
                     const float* __restrict__ z0, float* __restrict__ o,
                     float* __restrict__ S_N, float* __restrict__ z_N) {
   extern __shared__ float smem[];
@@ -50,6 +61,7 @@ prefill_simt_kernel(const void* __restrict__ q, const void* __restrict__ k,
   float* fv = fk + kTB * kMaxD;            // [kTB][kMaxD]
   float* part = fv + kTB * kMaxD;          // [kTB][R][dvp]
   float* dpart = part + kTB * sh.R * sh.dvp;  // [kTB][R]
+  float* fa = dpart + kTB * sh.R;          // [kTB] decay of each staged token
 
   const int tid = threadIdx.x;
   const int g = tid % sh.G;        // column group
@@ -82,8 +94,41 @@ prefill_simt_kernel(const void* __restrict__ q, const void* __restrict__ k,
     }
   }
 
+  if (MODE == 2) {
+    // ---- non-causal: the state over all tokens first
+    for (int t0 = 0; t0 < N; t0 += kTB) {
+      for (int e = tid; e < kTB * kMaxD; e += kThreads) {
+        const int t = e / kMaxD, i = e % kMaxD;
+        const int tok = t0 + t;
+        const bool in = tok < N;
+        fk[e] = (in && i < dk) ? phi_f32(load_in(k, (head * N + tok) * dk + i, bf16)) : 0.f;
+        fv[e] = (in && i < dv) ? load_in(v, (head * N + tok) * dv + i, bf16) : 0.f;
+      }
+      __syncthreads();
+      if (active) {
+        for (int t = 0; t < kTB; ++t) {
+          const float4 vv = *reinterpret_cast<const float4*>(&fv[t * kMaxD + col0]);
+#pragma unroll
+          for (int r = 0; r < kMaxRows; ++r) {
+            const int i = rg + r * sh.R;
+            if (i < dk) {
+              const float a = fk[t * kMaxD + i];
+              S[r][0] += a * vv.x;
+              S[r][1] += a * vv.y;
+              S[r][2] += a * vv.z;
+              S[r][3] += a * vv.w;
+              z[r] += a;
+            }
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+
   for (int t0 = 0; t0 < N; t0 += kTB) {
     // ---- stage kTB tokens, phi applied; rows past N are zero (no effect)
+    if (DECAY && tid < kTB) fa[tid] = (t0 + tid < N) ? alpha[head * N + t0 + tid] : 1.f;
     for (int e = tid; e < kTB * kMaxD; e += kThreads) {
       const int t = e / kMaxD, i = e % kMaxD;
       const int tok = t0 + t;
@@ -94,10 +139,12 @@ prefill_simt_kernel(const void* __restrict__ q, const void* __restrict__ k,
     }
     __syncthreads();
 
-    // ---- per thread: write, then read, token by token
+    // ---- per thread: write, then read, token by token (or read, then
+    // write; or, non-causal, read the full state)
     if (active) {
       for (int t = 0; t < kTB; ++t) {
         const float4 vv = *reinterpret_cast<const float4*>(&fv[t * kMaxD + col0]);
+        const float at = DECAY ? fa[t] : 1.f;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         float dacc = 0.f;
 #pragma unroll
@@ -106,16 +153,35 @@ prefill_simt_kernel(const void* __restrict__ q, const void* __restrict__ k,
           if (i < dk) {
             const float a = fk[t * kMaxD + i];
             const float b = fq[t * kMaxD + i];
-            S[r][0] += a * vv.x;
-            S[r][1] += a * vv.y;
-            S[r][2] += a * vv.z;
-            S[r][3] += a * vv.w;
-            acc[0] += b * S[r][0];
-            acc[1] += b * S[r][1];
-            acc[2] += b * S[r][2];
-            acc[3] += b * S[r][3];
-            z[r] += a;
-            dacc += b * z[r];
+            if (MODE == 1 || MODE == 2) {
+              acc[0] += b * S[r][0];
+              acc[1] += b * S[r][1];
+              acc[2] += b * S[r][2];
+              acc[3] += b * S[r][3];
+              dacc += b * z[r];
+            }
+            if (MODE != 2) {
+              if (DECAY) {
+                S[r][0] = fmaf(at, S[r][0], a * vv.x);
+                S[r][1] = fmaf(at, S[r][1], a * vv.y);
+                S[r][2] = fmaf(at, S[r][2], a * vv.z);
+                S[r][3] = fmaf(at, S[r][3], a * vv.w);
+                z[r] = fmaf(at, z[r], a);
+              } else {
+                S[r][0] += a * vv.x;
+                S[r][1] += a * vv.y;
+                S[r][2] += a * vv.z;
+                S[r][3] += a * vv.w;
+                z[r] += a;
+              }
+            }
+            if (MODE == 0) {
+              acc[0] += b * S[r][0];
+              acc[1] += b * S[r][1];
+              acc[2] += b * S[r][2];
+              acc[3] += b * S[r][3];
+              dacc += b * z[r];
+            }
           }
         }
         float* pp = &part[(t * sh.R + rg) * sh.dvp + col0];
@@ -162,21 +228,30 @@ prefill_simt_kernel(const void* __restrict__ q, const void* __restrict__ k,
 }  // namespace
 
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream) {
+  return launch_prefill_variant_simt(a, nullptr, 0, stream);
+}
+
+cudaError_t launch_prefill_variant_simt(const PrefillArgs& a, const float* alpha, int mode,
+                                        cudaStream_t stream) {
   const SimtShape sh = simt_shape(a.dk, a.dv);
   // Every thread must own at most kMaxRows rows.
   if ((a.dk + sh.R - 1) / sh.R > kMaxRows) return cudaErrorInvalidValue;
+  if (mode < 0 || mode > 2 || (mode == 2 && alpha)) return cudaErrorInvalidValue;
   const size_t smem =
-      sizeof(float) * (3 * kTB * kMaxD + kTB * sh.R * sh.dvp + kTB * sh.R);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(
-        prefill_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+      sizeof(float) * (3 * kTB * kMaxD + kTB * sh.R * sh.dvp + kTB * sh.R + kTB);
   const unsigned blocks = (unsigned)((size_t)a.B * a.H);
-  prefill_simt_kernel<<<blocks, kThreads, smem, stream>>>(
-      a.q, a.k, a.v, a.bf16, a.N, a.dk, a.dv, a.eps, a.S0, a.z0, a.o, a.S_N,
-      a.z_N);
-  return cudaGetLastError();
+  auto go = [&](auto kern) -> cudaError_t {
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    kern<<<blocks, kThreads, smem, stream>>>(a.q, a.k, a.v, a.bf16, a.N, a.dk, a.dv, a.eps, alpha,
+                                             a.S0, a.z0, a.o, a.S_N, a.z_N);
+    return cudaGetLastError();
+  };
+  if (mode == 2) return go(prefill_simt_kernel<2, false>);
+  if (mode == 1) return alpha ? go(prefill_simt_kernel<1, true>) : go(prefill_simt_kernel<1, false>);
+  return alpha ? go(prefill_simt_kernel<0, true>) : go(prefill_simt_kernel<0, false>);
 }
 
 }  // namespace la

@@ -60,6 +60,13 @@ typedef enum {
 
 typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
 
+/* Read order of la_prefill_variant. */
+typedef enum {
+  LA_MODE_CAUSAL = 0,             /* write, then read (la_prefill's order) */
+  LA_MODE_READ_BEFORE_WRITE = 1,  /* read, then write: strictly past */
+  LA_MODE_NONCAUSAL = 2           /* the state over all N tokens, then every read */
+} la_mode;
+
 /*
  * la_prefill -- causal prefill of N tokens per (batch, head).
  * Computes o_t for t = 1..N from the recurrence above, starting from S0, z0
@@ -82,6 +89,31 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
                      float* o, float* S_N, float* z_N,
                      int chunk, void* workspace, size_t ws_bytes,
                      cudaStream_t stream);
+
+/*
+ * la_prefill_variant -- la_prefill's recurrence with a per-token decay of the
+ * old state and a choice of read order (no workspace):
+ *   S_t = alpha_t S_{t-1} + phi(k_t) v_t^T,   z_t = alpha_t z_{t-1} + phi(k_t)
+ * (the linear-attention recurrence with one scalar on the old state: page
+ * "线性注意力与SSM", sections 3-4, Mamba-2; the normalizer decays with S), and
+ *   LA_MODE_CAUSAL:            o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps)
+ *   LA_MODE_READ_BEFORE_WRITE: o_t = phi(q_t)^T S_{t-1} / (phi(q_t)^T z_{t-1} + eps)
+ *       (LinearMem sections 03 and 09: strictly past; from a zero state the
+ *       first read is 0)
+ *   LA_MODE_NONCAUSAL:         o_t = phi(q_t)^T S_N / (phi(q_t)^T z_N + eps), with
+ *       S_N = S0 + sum_t phi(k_t) v_t^T (the linear-attention explainer,
+ *       section 线性化核心; eps = 0 gives its form exactly).
+ *   alpha   [B][H][N] float32, or NULL for no decay (then LA_MODE_CAUSAL is
+ *           la_prefill exactly).  Must be NULL for LA_MODE_NONCAUSAL.
+ * Other arguments, layouts, aliasing and errors as la_prefill.  Runs on the
+ * CUDA cores in fp32 (one block per head), for LA_F32 and LA_BF16 inputs and
+ * any dk, dv <= 128.
+ */
+la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                             int B, int H, int N, int dk, int dv, float eps,
+                             const float* alpha, la_mode mode,
+                             const float* S0, const float* z0,
+                             float* o, float* S_N, float* z_N, cudaStream_t stream);
 
 /* Bytes of workspace la_prefill needs for these arguments (always >= 256).
  * Returns 0 for arguments la_prefill would reject. */
@@ -116,6 +148,21 @@ la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const f
                         int B, int H, int N, int dk, int dv,
                         const float* S0, float* reads, float* S_N,
                         cudaStream_t stream);
+
+/*
+ * gated_delta_prefill -- the delta rule with forgetting (LinearMem section 03,
+ * "再引入遗忘系数 alpha_t", and the appendix delta_step): per token the old
+ * memory decays first, then the correction uses the decayed prediction:
+ *   D = alpha_t S_{t-1};  reads[t] = k_t^T D;  S_t = D + beta_t k_t (v_t - reads[t])^T
+ *   alpha [B][H][N] float32, or NULL (alpha_t = 1: exactly delta_prefill).
+ * Other arguments as delta_prefill.  With alpha != NULL it runs token by
+ * token in fp32 on the CUDA cores.
+ */
+la_status gated_delta_prefill(const void* k, const void* v, la_dtype in_dtype,
+                              const float* beta, const float* alpha,
+                              int B, int H, int N, int dk, int dv,
+                              const float* S0, float* reads, float* S_N,
+                              cudaStream_t stream);
 
 /* Bytes of one head's recurrent state, (dk*dv + dk) * 4: 16640 at 64 x 64
  * (LinearMem page, section 01).  0 for dk or dv < 1. */

@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
               "delta_prefill", "la_state_bytes", "la_status_string",
-              "la_read_device_status", "delta_read_device_status"):
+              "la_read_device_status", "delta_read_device_status",
+              "la_prefill_variant", "gated_delta_prefill"):
         assert n in names
 
 
@@ -116,3 +117,40 @@ def test_decode_and_delta_reject_invalid_arguments(lib):
     assert lib.delta_prefill(p(BASE), p(BASE + (1 << 24)), 1, p(BASE + (2 << 24)), 1, 1, 8,
                              64, 64, None, p(BASE + 16), p(BASE + (4 << 24)), None) == 1
     assert lib.la_read_device_status(None, None) == 1
+
+
+def _variant(lib, **kw):
+    a = dict(q=BASE, k=BASE + (1 << 30), v=BASE + (2 << 30), dt=1, B=1, H=1, N=16,
+             dk=64, dv=64, eps=1e-6, alpha=BASE + (8 << 30), mode=0, S0=None, z0=None,
+             o=BASE + (3 << 30), SN=BASE + (4 << 30), zN=BASE + (5 << 30))
+    a.update(kw)
+    p = lambda x: None if x is None else _fake(x)
+    return lib.la_prefill_variant(p(a["q"]), p(a["k"]), p(a["v"]), a["dt"], a["B"], a["H"],
+                                  a["N"], a["dk"], a["dv"], ctypes.c_float(a["eps"]),
+                                  p(a["alpha"]), a["mode"], p(a["S0"]), p(a["z0"]), p(a["o"]),
+                                  p(a["SN"]), p(a["zN"]), None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(mode=3), dict(mode=-1),
+    dict(mode=2),                           # non-causal takes no decay
+    dict(alpha=BASE + (8 << 30) + 4),       # misaligned alpha
+    dict(o=BASE + (8 << 30)),               # o overlaps alpha
+    dict(eps=-1.0), dict(dk=129), dict(zN=None), dict(q=None),
+])
+def test_prefill_variant_rejects_invalid_arguments(lib, kw):
+    assert _variant(lib, **kw) == 1  # LA_ERR_INVALID_ARG
+
+
+def test_gated_delta_rejects_invalid_arguments(lib):
+    p = _fake
+    # reads overlapping alpha; misaligned alpha; bad dims
+    assert lib.gated_delta_prefill(p(BASE), p(BASE + (1 << 24)), 1, p(BASE + (2 << 24)),
+                                   p(BASE + (5 << 24)), 1, 1, 8, 64, 64, None,
+                                   p(BASE + (5 << 24)), p(BASE + (4 << 24)), None) == 1
+    assert lib.gated_delta_prefill(p(BASE), p(BASE + (1 << 24)), 1, p(BASE + (2 << 24)),
+                                   p(BASE + (5 << 24) + 8), 1, 1, 8, 64, 64, None,
+                                   p(BASE + (3 << 24)), p(BASE + (4 << 24)), None) == 1
+    assert lib.gated_delta_prefill(p(BASE), p(BASE + (1 << 24)), 1, p(BASE + (2 << 24)),
+                                   p(BASE + (5 << 24)), 1, 1, 8, 0, 64, None,
+                                   p(BASE + (3 << 24)), p(BASE + (4 << 24)), None) == 1

@@ -1,0 +1,121 @@
+"""GPU parity of gated_delta_prefill and la_prefill_variant against the fp64
+oracle, through the C ABI: the pages' gated-memory values, every read order
+with and without decay, both input dtypes, ragged and odd sizes."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import golden
+from helpers import f64, relmax, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def la():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fixed_state_recurrent_gb300 import build, api
+    build.build()
+    api.load()
+    return api
+
+
+# --------------------------------------------------------------------------
+# gated delta
+
+def test_p1_gated_delta_on_gpu(la):
+    g = golden("p1_gated_delta.json")
+    S0 = torch.tensor(g["state"], dtype=torch.float32)[None, None].cuda()
+    k = torch.tensor([g["key"], g["orthogonal_key"]], dtype=torch.float32)[None, None].cuda()
+    v = torch.tensor([g["value"], [0.0, 0.0]], dtype=torch.float32)[None, None].cuda()
+    beta = torch.tensor([[[g["beta"], 0.0]]], dtype=torch.float32).cuda()
+    for a, want in ((g["gated_alpha"], g["gated_unrelated_key_read"]),
+                    (1.0, g["no_forgetting_unrelated_key_read"])):
+        alpha = torch.tensor([[[a, 1.0]]], dtype=torch.float32).cuda()
+        reads, S = la.gated_delta_prefill(k, v, beta, alpha, S0=S0)
+        np.testing.assert_allclose(f64(reads)[0, 0, 1], want, atol=1e-7)
+
+
+GD_SHAPES = [(1, 1, 1, 4, 3), (2, 3, 37, 5, 3), (1, 2, 100, 64, 64), (2, 1, 300, 128, 128),
+             (1, 1, 77, 33, 128), (1, 2, 65, 100, 100)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("shape", GD_SHAPES, ids=[str(s) for s in GD_SHAPES])
+def test_gated_delta_matches_oracle(la, orc, dtype, shape):
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N, dk, dv = shape
+    k, v, beta = inputs.delta_inputs(B, H, N, dk, dv, dtype, seed=90 + N)
+    g = torch.Generator().manual_seed(91 + N)
+    alpha = 0.5 + 0.5 * torch.rand((B, H, N), generator=g)
+    S0 = torch.randn((B, H, dk, dv), generator=g)
+    reads, S = la.gated_delta_prefill(k.cuda(), v.cuda(), beta.cuda(), alpha.cuda(), S0=S0.cuda())
+    rr, rS = orc.gated_delta(f64(k), f64(v), f64(beta), f64(alpha), S0=f64(S0))
+    assert relmax(f64(reads), rr) <= tol_for(dtype)
+    assert relmax(f64(S), rS) <= tol_for(dtype)
+
+
+def test_gated_delta_without_alpha_is_delta_prefill(la):
+    from fixed_state_recurrent_gb300 import inputs
+    for dtype, d in ((torch.float32, 64), (torch.bfloat16, 128)):
+        k, v, beta = inputs.delta_inputs(1, 2, 200, d, d, dtype, seed=93)
+        a = la.gated_delta_prefill(k.cuda(), v.cuda(), beta.cuda())
+        b = la.delta_prefill(k.cuda(), v.cuda(), beta.cuda())
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# --------------------------------------------------------------------------
+# decayed / read-before-write / non-causal prefill
+
+VAR_SHAPES = [(1, 1, 1, 4, 3), (2, 3, 37, 5, 3), (1, 2, 100, 64, 64), (1, 2, 129, 128, 128),
+              (1, 1, 77, 33, 7)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("mode,decay", [(0, True), (1, False), (1, True), (2, False)],
+                         ids=["causal_decay", "rbw", "rbw_decay", "noncausal"])
+@pytest.mark.parametrize("shape", VAR_SHAPES, ids=[str(s) for s in VAR_SHAPES])
+def test_prefill_variant_matches_oracle(la, orc, dtype, mode, decay, shape):
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N, dk, dv = shape
+    q, k, v = inputs.la_inputs(B, H, N, dk, dv, dtype, seed=100 + N)
+    g = torch.Generator().manual_seed(101 + N)
+    alpha = (0.8 + 0.2 * torch.rand((B, H, N), generator=g)) if decay else None
+    S0 = torch.rand((B, H, dk, dv), generator=g)
+    z0 = torch.rand((B, H, dk), generator=g) + 0.5
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(),
+                                 None if alpha is None else alpha.cuda(), mode,
+                                 S0=S0.cuda(), z0=z0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), None if alpha is None else f64(alpha),
+                                mode, S0=f64(S0), z0=f64(z0))
+    tol = tol_for(dtype)
+    assert relmax(f64(o), ro) <= tol
+    assert relmax(f64(S), rS) <= tol
+    assert relmax(f64(z), rz) <= tol
+
+
+def test_prefill_variant_causal_without_decay_is_la_prefill(la):
+    # the fp32 path of la_prefill and the variant run the same arithmetic
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(2, 2, 90, 64, 32, torch.float32, seed=110)
+    a = la.prefill_variant(q.cuda(), k.cuda(), v.cuda())
+    ws = la.workspace(2, 2, 90, 64, 32, torch.float32, 0, torch.device("cuda"))
+    b = la.prefill(q.cuda(), k.cuda(), v.cuda(), ws=ws)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_read_before_write_first_read_is_zero_on_gpu(la):
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 3, 20, 16, 8, torch.float32, seed=111)
+    o, _, _ = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), None, la.LA_MODE_READ_BEFORE_WRITE)
+    assert torch.count_nonzero(o[:, :, 0]) == 0
+
+
+def test_prefill_variant_zero_length_copies_state(la):
+    e = torch.empty((1, 2, 0, 8), device="cuda")
+    S0 = torch.rand((1, 2, 8, 8), device="cuda")
+    z0 = torch.rand((1, 2, 8), device="cuda")
+    o, S, z = la.prefill_variant(e, e, e, torch.empty((1, 2, 0), device="cuda"), 0, S0=S0, z0=z0)
+    assert torch.equal(S, S0) and torch.equal(z, z0)
