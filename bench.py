@@ -394,8 +394,8 @@ def bench_delta(api, rank, world, reps=3):
 
 
 def bench_gated_delta(api, rank, world, reps=3):
-    """gated_delta_prefill on the delta workload with alpha ~ U(0.9, 1):
-    token by token on the FP32 pipe (4 dk dv flop per token)."""
+    """gated_delta_prefill on the delta workload with alpha ~ U(0.9, 1): the
+    chunked tensor-core kernel with decay factors (bf16, dk = dv = 128)."""
     import torch
     from fixed_state_recurrent_gb300 import inputs
     w = inputs.WORKLOADS["delta"]

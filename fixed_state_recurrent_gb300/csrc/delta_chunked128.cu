@@ -17,6 +17,18 @@
 // In exact arithmetic this equals the token recurrence; only the order of the
 // sums and the operand roundings differ.
 //
+// Gated form (the LinearMem page, section 03: D = alpha_t S_{t-1}, then the
+// correction against D).  With g_t = sum_{r <= t} log2 alpha_r inside the
+// chunk, gamma_t = 2^g_t and L~[t][s] = 2^(g_t - g_s) k_t . k_s (s < t), the
+// recurrence unrolls to
+//   R = diag(gamma) K S + L~ U,   U = T~ diag(beta) (V - diag(gamma) K S),
+//   T~ = (I + diag(beta) L~)^-1,  S_new = gamma_C S + K^T diag(gamma_C / gamma) U,
+// so the same products run with L~ in place of L; the state warps scale K S by
+// gamma_t (in X and, written back, in the reads), keep a second bf16 copy of
+// U scaled by gamma_C / gamma_t for the state product, and scale S by gamma_C
+// once per chunk.  The decay ratios are taken as 2^(g_t - g_s) <= 1 (a zero
+// alpha is clamped to 1e-30), never as quotients.
+//
 // One block per head, chunks of C = 64 tokens taken in pairs (128 tokens per
 // TMA stage, so that the Gram matrix of a pair is one M = 128 product).  The
 // state and every product live transposed, TMEM lanes = value columns j:
@@ -73,8 +85,11 @@ constexpr uint32_t OFF_T = OFF_V + NV * VSLOT;  // (T B)_c tiles, [pair parity][
 constexpr uint32_t OFF_L = OFF_T + 4 * CT;   // L_c tiles, [pair parity][chunk]
 constexpr uint32_t OFF_LC = OFF_L + 4 * CT;  // fp32 A, then T, of both chunks (2 x 16 KB)
 constexpr uint32_t OFF_BETA = OFF_LC + 2 * CH * CH * 4;  // beta of the chunks being solved
-constexpr uint32_t OFF_BAR = OFF_BETA + PT * 4;
-constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+constexpr uint32_t OFF_GAM = OFF_BETA + PT * 4;  // gated: [pair parity][chunk] gamma[64], ratio[64]
+constexpr uint32_t OFF_BAR = OFF_GAM + 2 * 2 * 2 * CH * 4;
+// The dynamic shared window starts 1024-byte aligned (the kernel checks it
+// and does no work, with kStatusLayout, otherwise), so no slack is reserved.
+constexpr uint32_t SMEM = OFF_BAR + 256;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 
 constexpr int kWarps = 11;  // 0 TMA of K, 1 MMA, 2-5 T builders, 6-9 state epilogue, 10 TMA of V
@@ -93,6 +108,7 @@ constexpr uint32_t ID_S = idesc_bf16_f32(128, D, 0, 1);     // UB x K_c   (B MN-
 struct Params {
   int BH, N;
   const float* beta;
+  const float* alpha;  // gated form: per-token forgetting (kernel instantiated with GATED)
   const float* S0;
   float* reads;
   float* S_N;
@@ -333,17 +349,25 @@ __device__ __forceinline__ void solve_t(float* S, const float* bs, uint8_t* ttil
   }
 }
 
+template <bool GATED>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const Params p, const unsigned long long mbar_ns) {
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte aligned base, derived from the shared array by pointer
-  // arithmetic so that accesses through it stay shared-space accesses
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  // The base is offset by a zero the compiler cannot see through: with the
+  // base a known constant the kernel measured ~15 % slower.  The swizzled
+  // tiles need it 1024-byte aligned, which the dynamic window is; if it were
+  // not, the launch does no work and reports kStatusLayout (the layout is
+  // never shifted: no slack is reserved).
+  uint32_t zero;
+  asm volatile("mov.u32 %0, 0;" : "=r"(zero));
+  uint8_t* smem = smem_raw + zero;
+  const bool aligned = (smem_u32(smem_raw) & 1023u) == 0;
+  if (!aligned && threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int head = blockIdx.x;
-  const int npairs = (p.N + PT - 1) / PT;
+  const int npairs = aligned ? (p.N + PT - 1) / PT : 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NK; ++s) {
       mbar_init(&B->kfull[s], 1);
@@ -432,8 +456,10 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
           if (!(ok = waitd(x, &B->ubready, nch & 1))) break;
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < CH / 16; ++ks)  // ST += UB x K_c (K rows = tokens, B MN-major)
-            mma_bf16_ts(tmem + ST, tmem + UB + 8 * ks, sdesc_sw128(kc + ks * 2048, HALF, 1024), ID_S, 1u);
+          for (int ks = 0; ks < CH / 16; ++ks)  // ST += UB x K_c (K rows = tokens, B MN-major);
+                                                // gated: the gamma_C / gamma_t scaled copy (in XB)
+            mma_bf16_ts(tmem + ST, tmem + (GATED ? XB : UB) + 8 * ks, sdesc_sw128(kc + ks * 2048, HALF, 1024),
+                        ID_S, 1u);
           mma_commit(&B->sready);
 #pragma unroll
           for (int ks = 0; ks < CH / 16; ++ks)  // KR += UB x L_c^T: the chunk's reads
@@ -485,8 +511,11 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       *reinterpret_cast<uint4*>(smem + OFF_T + (par * 2 + c) * CT + off * 16) = make_uint4(0, 0, 0, 0);
     }
     const float* beta_h = p.beta + (size_t)head * p.N;
-    // beta of this thread's token, loaded one pair ahead
+    // beta (and, gated, alpha) of this thread's token, loaded one pair ahead
     float bnext = (c * CH + ct < p.N) ? beta_h[c * CH + ct] : 0.f;
+    const float* alpha_h = GATED ? p.alpha + (size_t)head * p.N : nullptr;
+    float anext = 1.f;
+    if (GATED) anext = (c * CH + ct < p.N) ? alpha_h[c * CH + ct] : 1.f;
     // Gram product of pair q, LL = K2 K2^T (A and B both the pair's K tile,
     // K-major), issued by one T-builder thread: for pair 0 here, for pair
     // q + 1 as soon as T of pair q is done, so that the Gram products run
@@ -522,6 +551,28 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       bs[ct] = brow;
       const int tok_next = (pr + 1) * PT + c * CH + ct;
       bnext = tok_next < p.N ? beta_h[tok_next] : 0.f;
+      // gated: g_ct = sum_{r <= ct} log2 alpha_r over the chunk (inclusive scan
+      // over the chunk's 64 threads), kept in this pair parity's gamma array
+      float* gam = reinterpret_cast<float*>(smem + OFF_GAM) + ((pr & 1) * 2 + c) * 2 * CH;
+      float grow = 0.f, g63 = 0.f;
+      if (GATED) {
+        const float arow = anext;
+        anext = tok_next < p.N ? alpha_h[tok_next] : 1.f;
+        grow = log2f(fmaxf(arow, 1e-30f));
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float o = __shfl_up_sync(0xFFFFFFFFu, grow, off);
+          if (lane >= off) grow += o;
+        }
+        gam[ct] = grow;
+        named_bar_sync(bar_id, 64);
+        if (ct >= 32) {
+          grow += gam[31];
+          gam[ct] = grow;
+        }
+        named_bar_sync(bar_id, 64);
+        g63 = gam[CH - 1];
+      }
       uint8_t* ltile = smem + OFF_L + ((pr & 1) * 2 + c) * CT;
       uint8_t* ttile = smem + OFF_T + ((pr & 1) * 2 + c) * CT;
 #pragma unroll 1
@@ -532,6 +583,10 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         float l[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) l[q] = (32 * h + q < ct) ? __uint_as_float(g[q]) : 0.f;
+        if (GATED) {  // L~[ct][s] = 2^(g_ct - g_s) k_ct . k_s
+#pragma unroll
+          for (int q = 0; q < 32; ++q) l[q] *= exp2f(fminf(grow - gam[32 * h + q], 0.f));
+        }
 #pragma unroll
         for (int g4 = 0; g4 < 8; ++g4)  // A row ct = beta_ct L row ct, fp32
           *reinterpret_cast<float4*>(sa + sidx(ct, 32 * h + 4 * g4)) =
@@ -550,6 +605,10 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(&B->llfree);  // LL may take the next Gram product
       named_bar_sync(bar_id, 64);
+      if (GATED) {  // per-token factors for the state warps: gamma_t and gamma_C / gamma_t
+        gam[ct] = exp2f(grow);
+        gam[CH + ct] = exp2f(fminf(g63 - grow, 0.f));
+      }
       solve_t(sa, bs, ttile, ct, bar_id);
       fence_proxy_async_smem();
       __syncwarp();
@@ -581,6 +640,9 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     float* reads_j = p.reads + (size_t)head * p.N * D + j;
     for (uint32_t ch = 0; ch < nchunks; ++ch) {
       const uint8_t* vt = smem + OFF_V + (ch % NV) * VSLOT;
+      // gated: the pair's gamma factors are published with its T (tready)
+      const float* gam = reinterpret_cast<const float*>(smem + OFF_GAM) + (((ch / 2) & 1) * 2 + (ch & 1)) * 2 * CH;
+      if (GATED && (ch & 1) == 0) waitd_warp(x, &B->tready[(ch / 2) & 1], ((ch / 2) >> 1) & 1);
       // SB = bf16(S^T) once S has advanced past chunk ch - 1
       if (ch > 0) waitd_warp(x, &B->sready, (ch - 1) & 1);
       tc_fence_after();
@@ -597,6 +659,23 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B->sbready);
+      if (GATED) {  // S <- gamma_C S before this chunk's state product (after ubready)
+        const float gc = gam[CH - 1];
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+          uint32_t f[32], w0[16], w1[16];
+          tmem_ld32(tl + ST + 32 * h, f);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            w0[q] = __float_as_uint(gc * __uint_as_float(f[q]));
+            w1[q] = __float_as_uint(gc * __uint_as_float(f[16 + q]));
+          }
+          tmem_st16(tl + ST + 32 * h, w0);
+          tmem_st16(tl + ST + 32 * h + 16, w1);
+        }
+        tmem_st_wait();
+      }
       // reads of chunk ch - 1 (R^T in its KR region, which this chunk's U^T
       // overwrites only after xready below)
       if (ch > 0) {
@@ -630,6 +709,18 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         uint32_t f[32], w[16];
         tmem_ld32(tl + kr_cols(ch) + 32 * h, f);
         tmem_ld_wait();
+        if (GATED) {  // (K S)^T -> diag(gamma) (K S)^T, kept for the reads
+          uint32_t y0[16], y1[16];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) f[q] = __float_as_uint(gam[32 * h + q] * __uint_as_float(f[q]));
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            y0[q] = f[q];
+            y1[q] = f[16 + q];
+          }
+          tmem_st16(tl + kr_cols(ch) + 32 * h, y0);
+          tmem_st16(tl + kr_cols(ch) + 32 * h + 16, y1);
+        }
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           const uint32_t v2 = vv[16 * h + q];
@@ -662,6 +753,14 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 #pragma unroll
         for (int q = 0; q < 16; ++q) w[q] = pack_bf16x2(__uint_as_float(f[2 * q]), __uint_as_float(f[2 * q + 1]));
         tmem_st16(tl + UB + 16 * h, w);
+        if (GATED) {  // the copy scaled by gamma_C / gamma_t for the state product (XB is free)
+          const float* ratio = gam + CH + 32 * h;
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            w[q] = pack_bf16x2(ratio[2 * q] * __uint_as_float(f[2 * q]),
+                               ratio[2 * q + 1] * __uint_as_float(f[2 * q + 1]));
+          tmem_st16(tl + XB + 16 * h, w);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -708,8 +807,8 @@ __device__ unsigned g_delta_status;
 
 bool delta_chunked_supported(bool bf16, int dk, int dv) { return bf16 && dk == 128 && dv == 128; }
 
-cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, int B, int H,
-                                 int N, const float* S0, float* reads, float* S_N,
+cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, const float* alpha,
+                                 int B, int H, int N, const float* S0, float* reads, float* S_N,
                                  cudaStream_t stream) {
   using namespace dc;
   unsigned* status = nullptr;
@@ -724,17 +823,20 @@ cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta
   p.BH = BH;
   p.N = N;
   p.beta = beta;
+  p.alpha = alpha;
   p.S0 = S0;
   p.reads = reads;
   p.S_N = S_N;
   p.status = status;
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
-  cudaError_t e = cudaFuncSetAttribute(delta_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM);
-  if (e != cudaSuccess) return e;
-  delta_chunked_kernel<<<BH, 32 * kWarps, SMEM, stream>>>(mk, mv, p, mbar_ns);
-  return cudaGetLastError();
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<BH, 32 * kWarps, SMEM, stream>>>(mk, mv, p, mbar_ns);
+    return cudaGetLastError();
+  };
+  return alpha ? go(delta_chunked_kernel<true>) : go(delta_chunked_kernel<false>);
 }
 
 cudaError_t delta_status_take(unsigned* out) {

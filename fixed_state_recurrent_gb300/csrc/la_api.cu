@@ -300,6 +300,7 @@ la_status delta_read_device_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return LA_ERR_CUDA;
   unsigned status = 0;
   if (la::delta_status_take(&status) != cudaSuccess) return LA_ERR_CUDA;
+  if (status & la::kStatusLayout) return LA_ERR_UNSUPPORTED;
   return (status & la::kStatusTimeout) ? LA_ERR_TIMEOUT : LA_OK;
 }
 

@@ -22,6 +22,7 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusLayout = 2u;  // a kernel found its shared window misaligned and stopped
 
 struct PrefillArgs {
   const void* q;
@@ -66,8 +67,9 @@ cudaError_t launch_decode_step(const void* q, const void* k, const void* v,
 
 // Tensor-core chunked delta rule (bf16, dk = dv = 128; delta_chunked128.cu).
 bool delta_chunked_supported(bool bf16, int dk, int dv);
-cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, int B, int H,
-                                 int N, const float* S0, float* reads, float* S_N,
+// alpha: per-token forgetting of the gated form, or NULL.
+cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, const float* alpha,
+                                 int B, int H, int N, const float* S0, float* reads, float* S_N,
                                  cudaStream_t stream);
 // Returns and clears the chunked delta kernel's status word (current device).
 cudaError_t delta_status_take(unsigned* out);

@@ -155,7 +155,9 @@ la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const f
  * memory decays first, then the correction uses the decayed prediction:
  *   D = alpha_t S_{t-1};  reads[t] = k_t^T D;  S_t = D + beta_t k_t (v_t - reads[t])^T
  *   alpha [B][H][N] float32, or NULL (alpha_t = 1: exactly delta_prefill).
- * Other arguments as delta_prefill.  With alpha != NULL it runs token by
+ * Other arguments as delta_prefill.  bf16 inputs at dk = dv = 128 run
+ * chunkwise on the tensor cores (decay factors inside each 64-token chunk,
+ * status through delta_read_device_status); everything else runs token by
  * token in fp32 on the CUDA cores.
  */
 la_status gated_delta_prefill(const void* k, const void* v, la_dtype in_dtype,
@@ -183,7 +185,8 @@ la_status la_read_device_status(const void* workspace, cudaStream_t stream);
  * otherwise LA_OK; LA_ERR_CUDA if the synchronization or copy fails.  The
  * word belongs to the current device and is shared by every delta_prefill
  * call on it (delta_prefill takes no workspace); the token-by-token delta
- * kernel has no waits and never sets it. */
+ * kernel has no waits and never sets it.  LA_ERR_UNSUPPORTED if a launch
+ * found its shared-memory window misaligned and did no work. */
 la_status delta_read_device_status(cudaStream_t stream);
 
 /*

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from conftest import golden
-from helpers import f64, relmax, tol_for
+from helpers import f64, relmax, tol_for, TOL_BF16
 
 pytestmark = pytest.mark.gpu
 
@@ -119,3 +119,60 @@ def test_prefill_variant_zero_length_copies_state(la):
     z0 = torch.rand((1, 2, 8), device="cuda")
     o, S, z = la.prefill_variant(e, e, e, torch.empty((1, 2, 0), device="cuda"), 0, S0=S0, z0=z0)
     assert torch.equal(S, S0) and torch.equal(z, z0)
+
+
+# gated delta on the tensor cores (bf16, dk = dv = 128): chunkwise with decay factors
+GATED_N = [1, 64, 65, 129, 300, 1000]
+
+
+@pytest.mark.parametrize("N", GATED_N)
+@pytest.mark.parametrize("arange", [(0.9, 1.0), (0.3, 1.0), (0.02, 0.5)], ids=["mild", "strong", "severe"])
+def test_gated_delta_chunked_matches_oracle(la, orc, N, arange):
+    from fixed_state_recurrent_gb300 import inputs
+    k, v, beta = inputs.delta_inputs(1, 3, N, 128, 128, torch.bfloat16, seed=120 + N)
+    g = torch.Generator().manual_seed(121 + N)
+    lo, hi = arange
+    alpha = lo + (hi - lo) * torch.rand((1, 3, N), generator=g)
+    S0 = torch.randn((1, 3, 128, 128), generator=g) * 0.5
+    reads, S = la.gated_delta_prefill(k.cuda(), v.cuda(), beta.cuda(), alpha.cuda(), S0=S0.cuda())
+    rr, rS = orc.gated_delta(f64(k), f64(v), f64(beta), f64(alpha), S0=f64(S0))
+    assert relmax(f64(reads), rr) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
+
+
+def test_gated_delta_chunked_zero_alpha_erases(la, orc):
+    # alpha = 0 at some tokens (clamped to 1e-30 inside the chunk factors):
+    # the memory before them is forgotten
+    from fixed_state_recurrent_gb300 import inputs
+    N = 400
+    k, v, beta = inputs.delta_inputs(1, 2, N, 128, 128, torch.bfloat16, seed=130)
+    alpha = torch.full((1, 2, N), 0.97)
+    alpha[:, :, [5, 64, 100, 255, 256, 399]] = 0.0
+    S0 = torch.randn((1, 2, 128, 128), generator=torch.Generator().manual_seed(131))
+    reads, S = la.gated_delta_prefill(k.cuda(), v.cuda(), beta.cuda(), alpha.cuda(), S0=S0.cuda())
+    rr, rS = orc.gated_delta(f64(k), f64(v), f64(beta), f64(alpha), S0=f64(S0))
+    assert relmax(f64(reads), rr) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+
+
+def test_gated_delta_chunked_alpha_one_is_delta(la):
+    # the gated kernel with alpha = 1 against the plain chunked kernel: the same
+    # products, the factors all exactly 1
+    from fixed_state_recurrent_gb300 import inputs
+    k, v, beta = inputs.delta_inputs(1, 2, 333, 128, 128, torch.bfloat16, seed=132)
+    kd, vd, bd = k.cuda(), v.cuda(), beta.cuda()
+    a = la.gated_delta_prefill(kd, vd, bd, torch.ones((1, 2, 333), device="cuda"))
+    b = la.delta_prefill(kd, vd, bd)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_gated_delta_chunked_repeatable(la):
+    from fixed_state_recurrent_gb300 import inputs
+    k, v, beta = inputs.delta_inputs(1, 3, 777, 128, 128, torch.bfloat16, seed=133)
+    alpha = 0.5 + 0.5 * torch.rand((1, 3, 777), generator=torch.Generator().manual_seed(134))
+    kd, vd, bd, ad = k.cuda(), v.cuda(), beta.cuda(), alpha.cuda()
+    first = la.gated_delta_prefill(kd, vd, bd, ad)
+    for _ in range(12):
+        again = la.gated_delta_prefill(kd, vd, bd, ad)
+        assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
