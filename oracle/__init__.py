@@ -27,6 +27,7 @@ page "线性注意力与SSM", sections 1.3 and 3):
   (mode 0, write then read), read-then-write (mode 1, strictly past), or
   non-causal (mode 2: the state over all tokens, then every query reads it)
 * ``la_variant_quadratic``: the same outputs from explicit weights
+* ``la_backward``: the exact gradient of ``la_recurrent`` (states recomputed)
 * ``outer_read``: additive identity-feature memory S = sum k v^T, read q^T S
 """
 from __future__ import annotations
@@ -82,10 +83,11 @@ def _load():
         lib.orc_gated_delta.argtypes = [p, p, p, p, i, i, i, i, i, p, p, p, i]
         lib.orc_la_variant.argtypes = [p, p, p, p, i, i, i, i, i, d, i, p, p, p, p, p, i]
         lib.orc_la_variant_quadratic.argtypes = [p, p, p, p, i, i, i, i, i, d, i, p, p, p, i]
+        lib.orc_la_backward.argtypes = [p, p, p, i, i, i, i, i, d, p, p, p, p, p, p, p, p, p, p, i]
         for name in ("orc_phi", "orc_la_recurrent", "orc_la_quadratic",
                      "orc_la_chunked", "orc_la_decode_step", "orc_delta",
                      "orc_outer_read", "orc_default_threads", "orc_gated_delta",
-                     "orc_la_variant", "orc_la_variant_quadratic"):
+                     "orc_la_variant", "orc_la_variant_quadratic", "orc_la_backward"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -235,6 +237,23 @@ def la_variant_quadratic(q, k, v, alpha=None, mode=MODE_CAUSAL, eps=1e-6, S0=Non
                                             N, dk, dv, eps, int(mode), _ptr(S0), _ptr(z0),
                                             _ptr(o), threads), "la_variant_quadratic")
     return o
+
+
+def la_backward(q, k, v, dO, eps=1e-6, S0=None, z0=None, dS_N=None, dz_N=None, threads=0):
+    """Returns (dq, dk, dv, dS0, dz0): the gradient of la_recurrent's
+    (o, S_N, z_N) against dO, dS_N, dz_N (None = zero)."""
+    q, k, v, dO, S0, z0, dS_N, dz_N = map(_f64, (q, k, v, dO, S0, z0, dS_N, dz_N))
+    B, H, N, dk, dv = _shape4(q, v)
+    dq = np.empty((B, H, N, dk))
+    dk_ = np.empty((B, H, N, dk))
+    dv_ = np.empty((B, H, N, dv))
+    dS0 = np.empty((B, H, dk, dv))
+    dz0 = np.empty((B, H, dk))
+    _check(_load().orc_la_backward(_ptr(q), _ptr(k), _ptr(v), B, H, N, dk, dv, eps, _ptr(S0),
+                                   _ptr(z0), _ptr(dO), _ptr(dS_N), _ptr(dz_N), _ptr(dq),
+                                   _ptr(dk_), _ptr(dv_), _ptr(dS0), _ptr(dz0), threads),
+           "la_backward")
+    return dq, dk_, dv_, dS0, dz0
 
 
 def outer_read(keys, values, queries):

@@ -597,6 +597,119 @@ int orc_la_variant_quadratic(const double* q, const double* k, const double* v,
 }
 
 /* ------------------------------------------------------------------------ */
+/* (10) Gradient of (1).  The pages give no backward pass: P1 section 03 only
+ * notes that training must not keep every state, and that prefix sums,
+ * chunking and recomputation handle it.  This is the exact derivative of the
+ * map (q, k, v, S0, z0) -> (o, S_N, z_N) of (1), with the states recomputed:
+ * given dO (upstream gradient of o) and dS_N, dz_N (of the final state, NULL =
+ * zero), with num_t = S_t^T phi(q_t), den_t = phi(q_t).z_t + eps, o_t = num_t / den_t:
+ *   dnum_t = dO_t / den_t,   dden_t = -(dO_t . o_t) / den_t
+ *   dphi(q_t) = S_t dnum_t + dden_t z_t                      (forward sweep)
+ *   G_t = dS_N + sum_{tau >= t} phi(q_tau) dnum_tau^T,  g_t = dz_N + sum_{tau >= t} dden_tau phi(q_tau)
+ *   dphi(k_t) = G_t v_t + g_t,   dv_t = G_t^T phi(k_t)      (reverse sweep)
+ *   dS0 = G_0, dz0 = g_0;  dq = dphi(q) phi'(q), dk = dphi(k) phi'(k)
+ * with phi'(u) = 1 for u > 0 and exp(u) for u <= 0. */
+static double dphi(double u) { return u > 0.0 ? 1.0 : exp(u); }
+
+typedef struct {
+  const double *q, *k, *v, *S0, *z0, *dO, *dS_N, *dz_N;
+  int N, dk, dv;
+  double eps;
+  double *dq, *dk_out, *dv_out, *dS0, *dz0;
+} bwd_args;
+
+static void backward_head(void* p, int64_t h) {
+  const bwd_args* a = (const bwd_args*)p;
+  const int N = a->N, dk = a->dk, dv = a->dv;
+  double* S = (double*)malloc(sizeof(double) * dk * dv);
+  double* z = (double*)malloc(sizeof(double) * dk);
+  double* fq = (double*)malloc(sizeof(double) * dk);
+  double* fk = (double*)malloc(sizeof(double) * dk);
+  double* num = (double*)malloc(sizeof(double) * dv);
+  double* dnum = (double*)malloc(sizeof(double) * (N > 0 ? N : 1) * dv);
+  double* dden = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
+  if (a->S0) memcpy(S, a->S0 + h * (int64_t)dk * dv, sizeof(double) * dk * dv);
+  else memset(S, 0, sizeof(double) * dk * dv);
+  if (a->z0) memcpy(z, a->z0 + h * (int64_t)dk, sizeof(double) * dk);
+  else memset(z, 0, sizeof(double) * dk);
+  /* forward sweep: the states again, the output's local gradients, dq */
+  for (int t = 0; t < N; ++t) {
+    const double* qt = a->q + (h * (int64_t)N + t) * dk;
+    const double* kt = a->k + (h * (int64_t)N + t) * dk;
+    const double* vt = a->v + (h * (int64_t)N + t) * dv;
+    const double* gt = a->dO + (h * (int64_t)N + t) * dv;
+    for (int i = 0; i < dk; ++i) fk[i] = phi(kt[i]);
+    for (int i = 0; i < dk; ++i) fq[i] = phi(qt[i]);
+    for (int i = 0; i < dk; ++i) {
+      for (int j = 0; j < dv; ++j) S[i * dv + j] += fk[i] * vt[j];
+      z[i] += fk[i];
+    }
+    double den = a->eps;
+    for (int i = 0; i < dk; ++i) den += fq[i] * z[i];
+    double go = 0.0;
+    for (int j = 0; j < dv; ++j) {
+      double nj = 0.0;
+      for (int i = 0; i < dk; ++i) nj += fq[i] * S[i * dv + j];
+      num[j] = nj;
+      go += gt[j] * (nj / den);
+    }
+    for (int j = 0; j < dv; ++j) dnum[(int64_t)t * dv + j] = gt[j] / den;
+    dden[t] = -go / den;
+    double* dqt = a->dq + (h * (int64_t)N + t) * dk;
+    for (int i = 0; i < dk; ++i) {
+      double d = dden[t] * z[i];
+      for (int j = 0; j < dv; ++j) d += S[i * dv + j] * dnum[(int64_t)t * dv + j];
+      dqt[i] = d * dphi(qt[i]);
+    }
+  }
+  /* reverse sweep: the gradient of every later state, dk, dv */
+  double* G = S; /* reuse */
+  double* g = z;
+  if (a->dS_N) memcpy(G, a->dS_N + h * (int64_t)dk * dv, sizeof(double) * dk * dv);
+  else memset(G, 0, sizeof(double) * dk * dv);
+  if (a->dz_N) memcpy(g, a->dz_N + h * (int64_t)dk, sizeof(double) * dk);
+  else memset(g, 0, sizeof(double) * dk);
+  for (int t = N - 1; t >= 0; --t) {
+    const double* qt = a->q + (h * (int64_t)N + t) * dk;
+    const double* kt = a->k + (h * (int64_t)N + t) * dk;
+    const double* vt = a->v + (h * (int64_t)N + t) * dv;
+    for (int i = 0; i < dk; ++i) fq[i] = phi(qt[i]);
+    for (int i = 0; i < dk; ++i) fk[i] = phi(kt[i]);
+    for (int i = 0; i < dk; ++i) {
+      for (int j = 0; j < dv; ++j) G[i * dv + j] += fq[i] * dnum[(int64_t)t * dv + j];
+      g[i] += dden[t] * fq[i];
+    }
+    double* dkt = a->dk_out + (h * (int64_t)N + t) * dk;
+    double* dvt = a->dv_out + (h * (int64_t)N + t) * dv;
+    for (int i = 0; i < dk; ++i) {
+      double d = g[i];
+      for (int j = 0; j < dv; ++j) d += G[i * dv + j] * vt[j];
+      dkt[i] = d * dphi(kt[i]);
+    }
+    for (int j = 0; j < dv; ++j) {
+      double d = 0.0;
+      for (int i = 0; i < dk; ++i) d += G[i * dv + j] * fk[i];
+      dvt[j] = d;
+    }
+  }
+  if (a->dS0) memcpy(a->dS0 + h * (int64_t)dk * dv, G, sizeof(double) * dk * dv);
+  if (a->dz0) memcpy(a->dz0 + h * (int64_t)dk, g, sizeof(double) * dk);
+  free(S); free(z); free(fq); free(fk); free(num); free(dnum); free(dden);
+}
+
+int orc_la_backward(const double* q, const double* k, const double* v, int B, int H,
+                    int N, int dk, int dv, double eps, const double* S0,
+                    const double* z0, const double* dO, const double* dS_N,
+                    const double* dz_N, double* dq, double* dk_out, double* dv_out,
+                    double* dS0, double* dz0, int nthreads) {
+  if (la_check(q, k, v, B, H, N, dk, dv, eps, dO)) return -1;
+  if (N > 0 && (!dq || !dk_out || !dv_out)) return -1;
+  bwd_args a = {q, k, v, S0, z0, dO, dS_N, dz_N, N, dk, dv, eps, dq, dk_out, dv_out, dS0, dz0};
+  for_each_head((int64_t)B * H, nthreads, backward_head, &a);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* (6) Additive outer-product memory with identity features, the write/read
  * primitive of P3 section 1.3 (memory collision) and of the two-entry example
  * on the associative-memory page: S = sum_m k_m v_m^T (k v^T convention), read

@@ -98,6 +98,15 @@ int orc_la_variant_quadratic(const double* q, const double* k, const double* v,
                              int dv, double eps, int mode, const double* S0,
                              const double* z0, double* o, int nthreads);
 
+/* Gradient of orc_la_recurrent with respect to q, k, v, S0, z0, given dO and
+ * (optionally, NULL = 0) dS_N, dz_N; the states are recomputed.  dS0, dz0 may
+ * be NULL. */
+int orc_la_backward(const double* q, const double* k, const double* v, int B, int H,
+                    int N, int dk, int dv, double eps, const double* S0,
+                    const double* z0, const double* dO, const double* dS_N,
+                    const double* dz_N, double* dq, double* dk_out, double* dv_out,
+                    double* dS0, double* dz0, int nthreads);
+
 /* Additive associative memory with the identity feature map (test-only
  * primitive): S = sum_m keys[m] values[m]^T, reads[p] = queries[p]^T S.
  * keys [M][dk], values [M][dv], queries [P][dk], reads [P][dv]. */

@@ -68,6 +68,15 @@ MUTANTS = [
      "const int send = mode == 0 ? t - 1 : (mode == 1 ? t - 1 : N - 1);"),
     ("variant_quadratic_decay_off_by_one", "for (int r = s + 1; r <= last; ++r) g *= al[r];",
      "for (int r = s; r <= last; ++r) g *= al[r];"),
+    ("backward_drops_den_term", "    dden[t] = -go / den;", "    dden[t] = 0.0 * go;"),
+    ("backward_den_sign", "    dden[t] = -go / den;", "    dden[t] = go / den;"),
+    ("backward_phi_prime_one", "static double dphi(double u) { return u > 0.0 ? 1.0 : exp(u); }",
+     "static double dphi(double u) { return u > 0.0 ? 1.0 : 1.0; }"),
+    ("backward_excludes_current_token",
+     "      for (int j = 0; j < dv; ++j) G[i * dv + j] += fq[i] * dnum[(int64_t)t * dv + j];\n      g[i] += dden[t] * fq[i];\n    }\n    double* dkt",
+     "    }\n    double* dkt"),
+    ("backward_dk_forgets_g", "      double d = g[i];\n      for (int j = 0; j < dv; ++j) d += G[i * dv + j] * vt[j];",
+     "      double d = 0.0;\n      for (int j = 0; j < dv; ++j) d += G[i * dv + j] * vt[j];"),
     ("outer_read_transposed", "S[i * dv + j] += keys[m * dk + i] * values[m * dv + j];",
      "S[i * dv + j] += keys[m * dk + j % dk] * values[m * dv + i % dv];"),
 ]
@@ -87,6 +96,8 @@ def _pin_functions():
             out.append(lambda orc, f=fn: [f(orc, c) for c in (1, 3, 16, 101)])
         elif name == "test_variant_recurrence_equals_explicit_weights":
             out.append(lambda orc, f=fn: [f(orc, m) for m in (0, 1, 2)])
+        elif name == "test_backward_matches_finite_differences":
+            out.append(lambda orc, f=fn: [f(orc, w) for w in (False, True)])
     return out
 
 

@@ -513,3 +513,67 @@ def test_decayed_state_closed_form(orc):
     zx = a ** 10 * z0[0, 0] + sum(a ** (9 - t) * fk[t] for t in range(10))
     np.testing.assert_allclose(S[0, 0], Sx, rtol=1e-13)
     np.testing.assert_allclose(z[0, 0], zx, rtol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# gradient (the pages name recomputation; the derivative itself is fixed by
+# the forward map): checked against central finite differences of la_recurrent
+
+def _fd_loss(orc, q, k, v, S0, z0, w_o, w_S, w_z, eps):
+    o, S, z = orc.la_recurrent(q, k, v, eps=eps, S0=S0, z0=z0)
+    return float(np.sum(w_o * o) + np.sum(w_S * S) + np.sum(w_z * z))
+
+
+@pytest.mark.parametrize("with_state", [False, True], ids=["zero", "state"])
+def test_backward_matches_finite_differences(orc, with_state):
+    r = _rng(140 + int(with_state))
+    B, H, N, dk, dv, eps = 1, 2, 6, 3, 2, 1e-6
+    q, k, v = _rand_la(141, B, H, N, dk, dv)
+    S0 = r.uniform(size=(B, H, dk, dv)) if with_state else None
+    z0 = r.uniform(size=(B, H, dk)) if with_state else None
+    w_o = r.normal(size=(B, H, N, dv))        # dO
+    w_S = r.normal(size=(B, H, dk, dv))       # dS_N
+    w_z = r.normal(size=(B, H, dk))           # dz_N
+    dq, dk_, dv_, dS0, dz0 = orc.la_backward(q, k, v, w_o, eps=eps, S0=S0, z0=z0,
+                                             dS_N=w_S, dz_N=w_z)
+    h = 1e-6
+    args = {"q": q, "k": k, "v": v, "S0": S0, "z0": z0}
+    grads = {"q": dq, "k": dk_, "v": dv_, "S0": dS0, "z0": dz0}
+    for name in (["q", "k", "v"] + (["S0", "z0"] if with_state else [])):
+        x = args[name]
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            a_p = dict(args); a_p[name] = xp
+            a_m = dict(args); a_m[name] = xm
+            num[idx] = (_fd_loss(orc, a_p["q"], a_p["k"], a_p["v"], a_p["S0"], a_p["z0"], w_o, w_S, w_z, eps)
+                        - _fd_loss(orc, a_m["q"], a_m["k"], a_m["v"], a_m["S0"], a_m["z0"], w_o, w_S, w_z, eps)) / (2 * h)
+        np.testing.assert_allclose(grads[name], num, rtol=1e-6, atol=1e-7, err_msg=name)
+
+
+def test_backward_state_only_passes_through(orc):
+    # with dO = 0 only the final state's gradient flows: S_N = S0 + sum phi(k) v^T,
+    # so dS0 = dS_N, dz0 = dz_N, dv_t = dS_N^T phi(k_t), dq = 0
+    r = _rng(150)
+    q, k, v = _rand_la(151, 1, 1, 5, 3, 2)
+    dS = r.normal(size=(1, 1, 3, 2))
+    dz = r.normal(size=(1, 1, 3))
+    dq, dk_, dv_, dS0, dz0 = orc.la_backward(q, k, v, np.zeros((1, 1, 5, 2)), dS_N=dS, dz_N=dz)
+    np.testing.assert_array_equal(dq, 0.0)
+    np.testing.assert_allclose(dS0, dS, rtol=0, atol=0)
+    np.testing.assert_allclose(dz0, dz, rtol=0, atol=0)
+    fk = orc.phi(k)
+    for t in range(5):
+        np.testing.assert_allclose(dv_[0, 0, t], dS[0, 0].T @ fk[0, 0, t], rtol=1e-13, atol=1e-15)
+
+
+def test_backward_single_token_closed_form(orc):
+    # N = 1 from a zero state: o = v w / (w + eps) with w = phi(q).phi(k), so
+    # do/dv = w / (w + eps) times dO exactly
+    q, k, v = _rand_la(152, 1, 1, 1, 4, 3)
+    dO = _rng(153).normal(size=(1, 1, 1, 3))
+    eps = 0.25
+    _, _, dv_, _, _ = orc.la_backward(q, k, v, dO, eps=eps)
+    w = float(np.sum(orc.phi(q) * orc.phi(k)))
+    np.testing.assert_allclose(dv_[0, 0, 0], dO[0, 0, 0] * w / (w + eps), rtol=1e-14)
