@@ -57,7 +57,7 @@ def _args():
                    help="headline workload only (no long/decode/delta/e2e/cpu)")
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run "
-                        "(long,decode,delta,pr1,gated,decay)")
+                        "(long,decode,delta,pr1,gated,decay,backward)")
     p.add_argument("--profile-delta", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain delta_prefill calls of the delta workload and exit "
                         "(for profilers)")
@@ -445,6 +445,32 @@ def bench_decay_prefill(api, rank, world, reps=3):
             "tokens_per_s": w.tokens / (ms * 1e-3)}
 
 
+def bench_backward(api, rank, world, reps=3):
+    """la_prefill_backward on the headline prefill shape (dO ~ N(0,1)): CUDA
+    cores, one block per head, token by token."""
+    import torch
+    w = inputs_mod().WORKLOADS["prefill"]
+    dev = torch.device("cuda")
+    q, k, v = _device_inputs(w, w.seed + 1000 * rank, dev)
+    g = torch.Generator(device=dev).manual_seed(7 + rank)
+    dO = torch.randn((w.B, w.H, w.N, w.dv), generator=g, device=dev)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    fn = lambda i: api.prefill_backward(q, k, v, dO)
+    with torch.cuda.stream(stream):
+        fn(0)
+    _, per = _timed(fn, reps, stream, world)
+    ms = min(per)
+    return {"workload": "backward: B=4 H=8 N=4096 dk=dv=64 bf16 inputs, dO ~ N(0,1), "
+                        "gradients of q, k, v, S0, z0", "ms_per_call": ms,
+            "tokens_per_s": w.tokens / (ms * 1e-3)}
+
+
+def inputs_mod():
+    from fixed_state_recurrent_gb300 import inputs
+    return inputs
+
+
 def bench_simple_prefill(api, wname, rank, world, reps=5):
     import torch
     from fixed_state_recurrent_gb300 import inputs
@@ -607,7 +633,7 @@ def main():
     extra = {}
     e2e = None
     wanted = set(x for x in args.only.split(",") if x) or {"long", "decode", "delta", "pr1",
-                                                             "gated", "decay"}
+                                                             "gated", "decay", "backward"}
     if not args.no_extra:
         if "long" in wanted:
             extra["long"] = bench_simple_prefill(api, "long", rank, world)
@@ -621,6 +647,8 @@ def main():
             extra["gated_delta"] = bench_gated_delta(api, rank, world)
         if "decay" in wanted:
             extra["decay_prefill"] = bench_decay_prefill(api, rank, world)
+        if "backward" in wanted:
+            extra["backward"] = bench_backward(api, rank, world)
         e_ms, h2d, d2h = bench_e2e(api, w, max(args.steps // 4, 5), 3, rank, world)
         e_steps = max(args.steps // 4, 5)
         e2e = {"value": w.tokens * world / (e_ms * 1e-3 / e_steps), "unit": "tokens/s",

@@ -24,7 +24,7 @@ LA_MODE_CAUSAL, LA_MODE_READ_BEFORE_WRITE, LA_MODE_NONCAUSAL = 0, 1, 2
 SYMBOLS = ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
            "delta_prefill", "la_state_bytes", "la_status_string",
            "la_read_device_status", "delta_read_device_status",
-           "la_prefill_variant", "gated_delta_prefill")
+           "la_prefill_variant", "gated_delta_prefill", "la_prefill_backward")
 
 
 class LAError(RuntimeError):
@@ -74,6 +74,9 @@ def load(path: str | None = None):
         lib.la_prefill_variant.restype = i
         lib.gated_delta_prefill.argtypes = [vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
         lib.gated_delta_prefill.restype = i
+        lib.la_prefill_backward.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp, vp, vp,
+                                            vp, vp, vp, vp, vp, vp]
+        lib.la_prefill_backward.restype = i
         _lib = lib
         return lib
 
@@ -270,6 +273,34 @@ def prefill_variant(q, k, v, alpha=None, mode=LA_MODE_CAUSAL, eps=1e-6, S0=None,
                                    _ptr(z0), _ptr(o), _ptr(S_N), _ptr(z_N), _stream(dev))
     _check("la_prefill_variant", st)
     return o, S_N, z_N
+
+
+def prefill_backward(q, k, v, dO, eps=1e-6, S0=None, z0=None, dS_N=None, dz_N=None, *,
+                     want_state_grads=True):
+    """la_prefill_backward: returns (dq, dk, dv, dS0, dz0) (the last two None
+    unless want_state_grads).  See la_prefill_backward in la.h."""
+    B, H, N, dk = q.shape
+    dv = v.shape[3]
+    dev = q.device
+    code = _dtype_code(q)
+    _need(k, "k", (B, H, N, dk), q.dtype, dev)
+    _need(v, "v", (B, H, N, dv), q.dtype, dev)
+    _need(dO, "dO", (B, H, N, dv), torch.float32, dev)
+    _need(S0, "S0", (B, H, dk, dv), torch.float32, dev)
+    _need(z0, "z0", (B, H, dk), torch.float32, dev)
+    _need(dS_N, "dS_N", (B, H, dk, dv), torch.float32, dev)
+    _need(dz_N, "dz_N", (B, H, dk), torch.float32, dev)
+    dq = torch.empty((B, H, N, dk), dtype=torch.float32, device=dev)
+    dk_ = torch.empty((B, H, N, dk), dtype=torch.float32, device=dev)
+    dv_ = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
+    dS0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev) if want_state_grads else None
+    dz0 = torch.empty((B, H, dk), dtype=torch.float32, device=dev) if want_state_grads else None
+    st = load().la_prefill_backward(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, dk, dv,
+                                    ctypes.c_float(eps), _ptr(S0), _ptr(z0), _ptr(dO),
+                                    _ptr(dS_N), _ptr(dz_N), _ptr(dq), _ptr(dk_), _ptr(dv_),
+                                    _ptr(dS0), _ptr(dz0), _stream(dev))
+    _check("la_prefill_backward", st)
+    return dq, dk_, dv_, dS0, dz0
 
 
 def read_device_status(ws, stream=None) -> int:

@@ -240,6 +240,54 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   return from_cuda(la::launch_prefill_variant_simt(a, alpha, (int)mode, stream));
 }
 
+la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                              int B, int H, int N, int dk, int dv, float eps,
+                              const float* S0, const float* z0, const float* dO,
+                              const float* dS_N, const float* dz_N, float* dq, float* dk_out,
+                              float* dv_out, float* dS0, float* dz0, cudaStream_t stream) {
+  if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return LA_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  if (N > 0 && (!q || !k || !v || !dO || !dq || !dk_out || !dv_out)) return LA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, S0, z0, dO, dS_N, dz_N, dq, dk_out, dv_out, dS0, dz0};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
+  const size_t heads = (size_t)B * H;
+  const size_t eb = elem_bytes(in_dtype);
+  const Span ins[] = {span(q, heads * N * dk * eb), span(k, heads * N * dk * eb),
+                      span(v, heads * N * dv * eb), span(S0, heads * dk * dv * 4),
+                      span(z0, heads * dk * 4), span(dO, heads * N * dv * 4),
+                      span(dS_N, heads * dk * dv * 4), span(dz_N, heads * dk * 4)};
+  const Span outs[] = {span(dq, heads * N * dk * 4), span(dk_out, heads * N * dk * 4),
+                       span(dv_out, heads * N * dv * 4), span(dS0, heads * dk * dv * 4),
+                       span(dz0, heads * dk * 4)};
+  for (const Span& x : outs) {
+    for (const Span& y : ins)
+      if (overlap(x, y)) return LA_ERR_INVALID_ARG;
+    for (const Span& y : outs)
+      if (&x != &y && overlap(x, y)) return LA_ERR_INVALID_ARG;
+  }
+  const la_status dev = check_device();
+  if (dev != LA_OK) return dev;
+  if (N == 0) {
+    cudaError_t e = cudaSuccess;
+    if (dS0) e = copy_state(dS_N, dS0, heads * dk * dv * 4, stream);
+    if (e == cudaSuccess && dz0) e = copy_state(dz_N, dz0, heads * dk * 4, stream);
+    return from_cuda(e);
+  }
+  PrefillArgs a;
+  a.q = q; a.k = k; a.v = v;
+  a.bf16 = in_dtype == LA_BF16;
+  a.B = B; a.H = H; a.N = N; a.dk = dk; a.dv = dv;
+  a.eps = eps;
+  a.S0 = S0; a.z0 = z0;
+  a.o = nullptr; a.S_N = nullptr; a.z_N = nullptr;
+  a.chunk = 0;
+  a.workspace = nullptr;
+  a.ws_bytes = 0;
+  return from_cuda(la::launch_prefill_backward(a, dO, dS_N, dz_N, dq, dk_out, dv_out, dS0, dz0,
+                                               stream));
+}
+
 static la_status delta_common(const void* k, const void* v, la_dtype in_dtype,
                               const float* beta, const float* alpha, int B, int H, int N,
                               int dk, int dv, const float* S0, float* reads, float* S_N,

@@ -49,6 +49,12 @@ cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_variant_simt(const PrefillArgs& a, const float* alpha, int mode,
                                         cudaStream_t stream);
 
+// Gradient of the causal prefill (backward_simt.cu): dq, dk, dv (and dS0, dz0
+// if not NULL) given dO and dS_N, dz_N (NULL = zero).
+cudaError_t launch_prefill_backward(const PrefillArgs& p, const float* dO, const float* dS_N,
+                                    const float* dz_N, float* dq, float* dk, float* dv,
+                                    float* dS0, float* dz0, cudaStream_t stream);
+
 // Tensor-core chunked prefill for dk = dv = 64: aggregate, scan and output
 // launches (prefill_chunked64.cu).  The workspace size depends on the SM count
 // of the current device.

@@ -115,6 +115,32 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
                              const float* S0, const float* z0,
                              float* o, float* S_N, float* z_N, cudaStream_t stream);
 
+/*
+ * la_prefill_backward -- the gradient of la_prefill's map
+ *   (q, k, v, S0, z0) -> (o, S_N, z_N)
+ * given dO [B][H][N][dv] and dS_N [B][H][dk][dv], dz_N [B][H][dk] (NULL = zero).
+ * The pages give no backward pass; the LinearMem page (section 03) notes only
+ * that training must not keep every state and that recomputation handles it.
+ * This recomputes the states: a forward sweep gives
+ *   dnum_t = dO_t / den_t,  dden_t = -(dO_t . o_t) / den_t,  dq via
+ *   dphi(q_t) = S_t dnum_t + dden_t z_t,
+ * and a reverse sweep accumulates G_t = dS_N + sum_{tau >= t} phi(q_tau) dnum_tau^T
+ * and g_t = dz_N + sum_{tau >= t} dden_tau phi(q_tau) for
+ *   dphi(k_t) = G_t v_t + g_t,  dv_t = G_t^T phi(k_t),  dS0 = G_0,  dz0 = g_0,
+ * with dq = dphi(q) phi'(q), dk = dphi(k) phi'(k), phi'(u) = 1 (u > 0), exp(u) (u <= 0).
+ *   dq, dk_out [B][H][N][dk], dv_out [B][H][N][dv]: float32 outputs (the
+ *               gradients with respect to q, k and v)
+ *   dS0 [B][H][dk][dv], dz0 [B][H][dk]: float32 outputs, or NULL if not wanted
+ * Outputs must not overlap any input or each other.  Runs on the CUDA cores in
+ * fp32, one block per head, token by token (no workspace); any dk, dv <= 128.
+ */
+la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                              int B, int H, int N, int dk, int dv, float eps,
+                              const float* S0, const float* z0, const float* dO,
+                              const float* dS_N, const float* dz_N,
+                              float* dq, float* dk_out, float* dv_out, float* dS0, float* dz0,
+                              cudaStream_t stream);
+
 /* Bytes of workspace la_prefill needs for these arguments (always >= 256).
  * Returns 0 for arguments la_prefill would reject. */
 size_t la_prefill_workspace_bytes(int B, int H, int N, int dk, int dv,

@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     for n in ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
               "delta_prefill", "la_state_bytes", "la_status_string",
               "la_read_device_status", "delta_read_device_status",
-              "la_prefill_variant", "gated_delta_prefill"):
+              "la_prefill_variant", "gated_delta_prefill", "la_prefill_backward"):
         assert n in names
 
 
@@ -154,3 +154,26 @@ def test_gated_delta_rejects_invalid_arguments(lib):
     assert lib.gated_delta_prefill(p(BASE), p(BASE + (1 << 24)), 1, p(BASE + (2 << 24)),
                                    p(BASE + (5 << 24)), 1, 1, 8, 0, 64, None,
                                    p(BASE + (3 << 24)), p(BASE + (4 << 24)), None) == 1
+
+
+def test_backward_rejects_invalid_arguments(lib):
+    p = _fake
+    MB = 1 << 24
+    def call(**kw):
+        a = dict(q=BASE, k=BASE + MB, v=BASE + 2 * MB, dt=1, B=1, H=1, N=16, dk=64, dv=64,
+                 eps=1e-6, S0=None, z0=None, dO=BASE + 3 * MB, dSN=None, dzN=None,
+                 dq=BASE + 4 * MB, dk_=BASE + 5 * MB, dv_=BASE + 6 * MB, dS0=None, dz0=None)
+        a.update(kw)
+        f = lambda x: None if x is None else p(x)
+        return lib.la_prefill_backward(f(a["q"]), f(a["k"]), f(a["v"]), a["dt"], a["B"], a["H"],
+                                       a["N"], a["dk"], a["dv"], ctypes.c_float(a["eps"]),
+                                       f(a["S0"]), f(a["z0"]), f(a["dO"]), f(a["dSN"]), f(a["dzN"]),
+                                       f(a["dq"]), f(a["dk_"]), f(a["dv_"]), f(a["dS0"]),
+                                       f(a["dz0"]), None)
+    assert call(dO=None) == 1                    # dO required
+    assert call(dq=BASE + 3 * MB) == 1           # dq overlaps dO
+    assert call(dk_=BASE + 4 * MB + 64) == 1     # dk overlaps dq
+    assert call(dv_=BASE + 6 * MB + 4) == 1      # misaligned
+    assert call(dS0=BASE + 2 * MB) == 1          # dS0 overlaps v
+    assert call(dk=129) == 1
+    assert call(eps=-1.0) == 1
