@@ -799,7 +799,8 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
   }
 }
 
-// Bounded-wait timeouts of this kernel (delta_prefill has no workspace).
+// Bounded-wait timeouts of the kernels whose calls take no workspace (this
+// kernel, and the decayed tensor-core prefill of la_prefill_variant).
 __device__ unsigned g_delta_status;
 
 }  // namespace dc
@@ -837,6 +838,10 @@ cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta
     return cudaGetLastError();
   };
   return alpha ? go(delta_chunked_kernel<true>) : go(delta_chunked_kernel<false>);
+}
+
+cudaError_t library_status_word(unsigned** out) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(out), dc::g_delta_status);
 }
 
 cudaError_t delta_status_take(unsigned* out) {

@@ -237,6 +237,9 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   a.chunk = 0;
   a.workspace = nullptr;
   a.ws_bytes = 0;
+  // bf16 at dk = dv = 64, write then read with a decay: tensor cores
+  if (alpha && mode == LA_MODE_CAUSAL && la::prefill_decay64_supported(a))
+    return from_cuda(la::launch_prefill_decay64(a, alpha, stream));
   return from_cuda(la::launch_prefill_variant_simt(a, alpha, (int)mode, stream));
 }
 

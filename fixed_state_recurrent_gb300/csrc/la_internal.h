@@ -60,6 +60,10 @@ cudaError_t launch_prefill_backward(const PrefillArgs& p, const float* dO, const
 // of the current device.
 size_t prefill_chunked64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream);
+// The decayed write-then-read form of the same products (bf16, dk = dv = 64),
+// one block per head; alpha: [B][H][N] per-token decay.  Needs no workspace.
+bool prefill_decay64_supported(const PrefillArgs& a);
+cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream);
 
 // Tensor-core chunked prefill (bf16, dk = dv in {64, 128}).
 bool prefill_tc_supported(const PrefillArgs& a);
@@ -77,7 +81,10 @@ bool delta_chunked_supported(bool bf16, int dk, int dv);
 cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, const float* alpha,
                                  int B, int H, int N, const float* S0, float* reads, float* S_N,
                                  cudaStream_t stream);
-// Returns and clears the chunked delta kernel's status word (current device).
+// The status word of the kernels whose calls take no workspace (the chunked
+// delta kernels, the decayed tensor-core prefill): its device address, and
+// reading it (returns and clears it; current device).
+cudaError_t library_status_word(unsigned** out);
 cudaError_t delta_status_take(unsigned* out);
 
 // alpha: per-token forgetting of the gated delta rule, or NULL (plain rule).

@@ -105,7 +105,8 @@ struct Params3 {
   const float* z0;
   float* S_N;
   float* z_N;
-  WsHeader* hdr;
+  unsigned* status;  // sticky error bits (the workspace header's, or the library's)
+  const float* alpha;  // [BH][N] per-token decay of the state, or NULL
   float* agg;  // [BH * MPH][SZ], transposed slots
   float* E;    // [BH * MPH][SZ], exclusive prefixes, transposed slots
   __nv_bfloat16* phik;  // [BH][N][D], phi(K) written by K1
@@ -132,13 +133,28 @@ __device__ __forceinline__ bool wait3(const Ctx3& x, uint64_t* bar, uint32_t par
   if (mbar_try_wait(bar, parity)) return true;
   if (mbar_wait(bar, parity, globaltimer_ns() + x.mbar_ns, x.abort)) return true;
   *x.abort = 1;
-  atomicOr(&x.p->hdr->status, kStatusTimeout);
+  atomicOr(x.p->status, kStatusTimeout);
   return false;
 }
 
 // The same decision for a whole warp (all lanes wait on the same barrier).
 __device__ __forceinline__ bool wait3_warp(const Ctx3& x, uint64_t* bar, uint32_t parity) {
   return __all_sync(0xFFFFFFFFu, wait3(x, bar, parity));
+}
+
+// Bounded wait until a CTA-scope counter reaches `target` (acquire).
+__device__ __forceinline__ bool count_reached(const Ctx3& x, const unsigned* c, unsigned target) {
+  if (*x.abort) return false;
+  const uint64_t dl = globaltimer_ns() + x.mbar_ns;
+  while (ld_acquire_cta(c) < target) {
+    if (*x.abort) return false;
+    if (globaltimer_ns() > dl) {
+      *x.abort = 1;
+      atomicOr(x.p->status, kStatusTimeout);
+      return false;
+    }
+  }
+  return true;
 }
 
 // Producer drain: the last loads that were issued (at most NS) land before the
@@ -495,9 +511,14 @@ constexpr uint32_t OFF_ONES = NS * STAGE;
 constexpr uint32_t OFF_SNAP = OFF_ONES + BLK;      // two snapshots
 constexpr uint32_t OFF_OUT = OFF_SNAP + 2 * SNAP;  // output staging: two [128 x 32] fp32 boxes
 constexpr uint32_t OFF_BAR = OFF_OUT + 2 * BLK;
-constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
+// decayed form only: per stage, the inclusive sums g_t of log2 alpha over the
+// chunk (128 floats), then the four warps' totals of the scan
+constexpr uint32_t OFF_G = OFF_BAR + 512;
+constexpr int GSTRIDE = C + 4;
+constexpr uint32_t SMEM = OFF_G + NS * GSTRIDE * 4 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 static_assert(OFF_OUT % 1024 == 0, "swizzled staging alignment");
+constexpr float kAlphaMin = 1e-30f;  // a zero decay is taken as this (its log2 stays finite)
 // 0 TMA, 1 MMA, 2-5 phi(Q), 6-9 P, 10-13 output epilogue (10, 12, 13 also
 // write the state snapshots), 14 state chain: at most four warps per SM
 // sub-partition, so 128 registers per thread
@@ -526,9 +547,32 @@ struct Bars {
   int abort;
   unsigned epieces;    // entry states stored in TMEM so far, times 3 (state warps -> state MMA):
                        // a counter, as the state warps may run pieces ahead of the state MMA
+  unsigned pdone[4];   // decayed form: chunks whose phi(K) rows P warp q has rescaled
+                       // (P warps -> state MMA); counters, as the P warps may run two chunks
+                       // ahead of the state MMA and apart from each other
   float4 zbuf[16];     // z, handed from its TMEM lane to the whole warp
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
+
+// Row r of a bf16 [128 x 64] swizzled tile, times f, rounded to bf16 again.
+__device__ __forceinline__ void scale_row(uint8_t* tile, int r, float f) {
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, i));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      w[j] = pack_bf16x2(__uint_as_float(w[j] << 16) * f, __uint_as_float(w[j] & 0xFFFF0000u) * f);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(tile + sw128_offset(r, i)) = v[i];
+}
+
+__device__ __forceinline__ const float* gsums(uint8_t* smem, uint32_t s) {
+  return reinterpret_cast<const float*>(smem + OFF_G) + s * GSTRIDE;
+}
 
 __device__ __forceinline__ uint8_t* stage_ptr(uint8_t* smem, uint32_t s) { return smem + s * STAGE; }
 
@@ -541,6 +585,20 @@ __device__ __forceinline__ uint8_t* stage_ptr(uint8_t* smem, uint32_t s) { retur
 // mbarriers (three arrivals), never waiting for the issuers.  A stage is
 // released by both issuers (a commit each, or an arrival where no state
 // advance reads it).
+//
+// DECAY (one block per head, entry state S0, no aggregate kernel):
+// S_t = alpha_t S_{t-1} + phi(k_t) v_t^T, z likewise.  With g_t the inclusive
+// sum of log2 alpha over the chunk up to t and gamma_t = 2^g_t, a chunk's
+// state enters token t as gamma_t S and its own tokens s <= t with weight
+// 2^(g_t - g_s); after the chunk, S <- gamma_C S + sum_s 2^(g_C - g_s) phi(k_s)
+// [v_s | 1]^T (gamma_C = gamma of the chunk's last token).  The phi warps load
+// K (phi is applied here) and scan log2 alpha; the P warps weight each kept
+// score by 2^(g_t - g_s) and, once the scores have read them, rescale the
+// phi(Q) rows by gamma_t and the phi(K) rows by 2^(g_C - g_t) in place for the
+// two later products; the state warps scale the running state by gamma_C of
+// the next chunk before its advance, and after the last advance store S_N,
+// z_N.  All factors are at most 1 for alpha <= 1.
+template <bool DECAY>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -568,6 +626,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(&B->sready[0], 3);
     mbar_init(&B->sready[1], 3);
     B->epieces = 0;
+    for (int q = 0; q < 4; ++q) B->pdone[q] = 0;
     mbar_init(&B->drain, 1);
     mbar_init(&B->drain2, 1);
     mbar_init(&B->tsread, 3);
@@ -607,7 +666,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           mbar_arrive_expect_tx(&B->full[s], 3 * BLK);
           tma_load_3d(st, &tm_q, 0, tok, pc.h, &B->full[s]);
           tma_load_3d(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
-          if (sj == 0) pdl_wait();  // phi(K) is the aggregate kernel's output
+          if (!DECAY && sj == 0) pdl_wait();  // phi(K) is the aggregate kernel's output
           tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
           ++issued;
         }
@@ -685,10 +744,32 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int i = 0; run.piece(p.sp, i, &pc); ++i)
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const int s = sj % NS;
-        if (!wait3_warp(x, &B->full[s], (sj / NS) & 1)) continue;
+        const bool got = wait3_warp(x, &B->full[s], (sj / NS) & 1);
+        if (!DECAY && !got) continue;
         uint8_t* st = stage_ptr(smem, s);
         const int valid = pc.tok1 - (pc.tok0 + c * C);
-        phi_row<8>(st, r, 0, valid);
+        if (got) phi_row<8>(st, r, 0, valid);
+        if (DECAY) {
+          if (got) phi_row<8>(st + BLK, r, 0, valid);
+          // g_t: inclusive sums of log2 alpha over the chunk (alpha = 1 past the
+          // end); a warp scan, then the totals of the warps before.  The named
+          // barrier runs whether or not the wait succeeded, so that all four
+          // warps always meet it.
+          float la = 0.f;
+          if (got && r < valid)
+            la = __log2f(fmaxf(__ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + c * C + r), kAlphaMin));
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xFFFFFFFFu, la, off);
+            if (lane >= off) la += y;
+          }
+          float* g = reinterpret_cast<float*>(smem + OFF_G) + s * GSTRIDE;
+          if (lane == 31) g[C + r / 32] = la;
+          named_bar_sync(2, 128);
+          for (int w = 0; w < r / 32; ++w) la += g[C + w];
+          g[r] = la;
+          if (!got) continue;
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&B->xf[s]);
@@ -704,6 +785,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!wait3_warp(x, &B->accB[b], (aj / 2) & 1)) continue;
         tc_fence_after();
         const uint32_t base = tl + TA + 128 * b;
+        const int row = 32 * quad + lane;
+        const float* g = gsums(smem, aj % NS);
+        const float gt = DECAY ? g[row] : 0.f;
         // this warp's query rows are 32 quad .. +31: key blocks before `quad` are
         // fully visible, block `quad` holds the diagonal, later blocks are zero;
         // packed keys 32 q4.. go to columns 16 q4..  Blocks are loaded two at a
@@ -723,23 +807,41 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (q4 > quad) {
 #pragma unroll
               for (int t = 0; t < 16; ++t) w[t] = 0u;
-            } else if (q4 < quad) {
+            } else if (!DECAY && q4 < quad) {
 #pragma unroll
               for (int t = 0; t < 16; ++t)
                 w[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
-            } else {
+            } else if (!DECAY) {
 #pragma unroll
               for (int t = 0; t < 16; ++t)
                 w[t] = pack_bf16x2(2 * t <= lane ? __uint_as_float(r[2 * t]) : 0.f,
                                    2 * t + 1 <= lane ? __uint_as_float(r[2 * t + 1]) : 0.f);
+            } else {  // kept scores weighted by 2^(g_t - g_s)
+              const float* gk = g + 32 * q4;
+#pragma unroll
+              for (int t = 0; t < 16; ++t) {
+                const bool k0 = q4 < quad || 2 * t <= lane, k1 = q4 < quad || 2 * t + 1 <= lane;
+                const float f0 = exp2_ftz(gt - gk[2 * t]), f1 = exp2_ftz(gt - gk[2 * t + 1]);
+                w[t] = pack_bf16x2(k0 ? __uint_as_float(r[2 * t]) * f0 : 0.f,
+                                   k1 ? __uint_as_float(r[2 * t + 1]) * f1 : 0.f);
+              }
             }
             tmem_st16(base + 16 * q4, w);
           }
         }
         tmem_st_wait();
+        if (DECAY) {  // the scores have read phi(Q), phi(K): rescale them for the later products
+          uint8_t* st = stage_ptr(smem, aj % NS);
+          scale_row(st, row, exp2_ftz(gt));                 // phi(Q) [S | z]: gamma_t
+          scale_row(st + BLK, row, exp2_ftz(g[C - 1] - gt));  // the advance: 2^(g_C - g_t)
+          fence_proxy_async_smem();
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&B->pready[b]);
+        if (lane == 0) {
+          mbar_arrive(&B->pready[b]);
+          if (DECAY) red_add_release_cta(&B->pdone[quad], 1u);
+        }
       }
   } else if (warp < 14) {  // ---- state snapshots (state lanes only) and output epilogue
     const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 320;
@@ -748,18 +850,32 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     uint8_t* snap = smem + OFF_SNAP;
     uint8_t* out = smem + OFF_OUT;
     uint32_t oj = 0, nsa = 0, sj = 0;
-    pdl_wait();  // the entry states E are the scan kernel's output
+    if (!DECAY) pdl_wait();  // the entry states E are the scan kernel's output
     Piece pc;
     for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
       // The piece's entry state E: into TMEM (running state) and snapshot 0.
       // The previous piece's products have all completed: its last output was
       // read below, and every state advance was waited for.
       if (state_warp) {
+        // decayed form: the state enters the first advance as gamma_C E
+        float gC = 1.f;
+        if (DECAY) {
+          wait3_warp(x, &B->xf[sj % NS], (sj / NS) & 1);  // the chunk's decay sums
+          gC = exp2_ftz(gsums(smem, sj % NS)[C - 1]);
+        }
         const float* src = p.E + (size_t)pc.slot * SZ + (state_row ? row : 0) * D;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float e[32];
-          if (state_row) {
+          if (DECAY) {  // S0 and z0 themselves (the whole head is the piece)
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const int i = 32 * half + q;
+              e[q] = !state_row ? 0.f
+                     : row < D ? (p.S0 ? __ldg(p.S0 + ((size_t)pc.h * D + i) * D + row) : 0.f)
+                               : (p.z0 ? __ldg(p.z0 + (size_t)pc.h * D + i) : 0.f);
+            }
+          } else if (state_row) {
             float4 u[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) u[q] = __ldcg(reinterpret_cast<const float4*>(src + 32 * half) + q);
@@ -775,7 +891,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           for (int q = 0; q < 2; ++q) {
             uint32_t w[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) w[t] = __float_as_uint(e[16 * q + t]);
+            for (int t = 0; t < 16; ++t) w[t] = __float_as_uint(e[16 * q + t] * gC);
             tmem_st16(tl + TS + 32 * half + 16 * q, w);
           }
           if (state_row) snap_half(snap, row, half, e);
@@ -799,6 +915,20 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           tmem_ld32(tl + TS, r0);
           tmem_ld32(tl + TS + 32, r1);
           tmem_ld_wait();
+          if (DECAY) {  // the next advance adds onto gamma_C S, gamma_C of the next chunk
+            const uint32_t sn1 = sj + 1;
+            wait3_warp(x, &B->xf[sn1 % NS], (sn1 / NS) & 1);
+            const float gC = exp2_ftz(gsums(smem, sn1 % NS)[C - 1]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t* rr = q < 2 ? r0 + 16 * q : r1 + 16 * (q - 2);
+              uint32_t w[16];
+#pragma unroll
+              for (int t = 0; t < 16; ++t) w[t] = __float_as_uint(__uint_as_float(rr[t]) * gC);
+              tmem_st16(tl + TS + 16 * q, w);
+            }
+            tmem_st_wait();
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B->tsread);  // the running state may advance again
@@ -862,6 +992,24 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           bulk_commit();
         }
       }
+      if (DECAY && state_warp) {  // the state after the last advance: S_N, z_N
+        wait3(x, &B->sacc, nsa & 1);
+        ++nsa;
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tl + TS, r0);
+        tmem_ld32(tl + TS + 32, r1);
+        tmem_ld_wait();
+        tc_fence_before();
+        if (state_row && pc.tok1 == p.sp.N && !*x.abort) {
+#pragma unroll
+          for (int i = 0; i < D; ++i) {
+            const float f = __uint_as_float(i < 32 ? r0[i] : r1[i - 32]);
+            if (row < D) p.S_N[((size_t)pc.h * D + i) * D + row] = f;
+            else p.z_N[(size_t)pc.h * D + i] = f;
+          }
+        }
+      }
     }
     if (et == 32) bulk_wait_all();
   } else {  // ---- the state chain: S += [V | 1]^T phi(K), chunk by chunk (one thread)
@@ -879,6 +1027,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!any) {
           mbar_arrive(&B->empty[s]);
           return true;
+        }
+        if (DECAY) {  // phi(K) of chunk j rescaled by all four P warps
+          for (int q = 0; q < 4; ++q)
+            if (!count_reached(x, &B->pdone[q], j + 1)) return false;
         }
         tc_fence_after();
         const uint32_t st = smem_u32(stage_ptr(smem, s)), vt = st + 2 * BLK;
@@ -899,7 +1051,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (*x.abort) return false;
           if (globaltimer_ns() > dl) {
             *x.abort = 1;
-            atomicOr(&p.hdr->status, kStatusTimeout);
+            atomicOr(p.status, kStatusTimeout);
             return false;
           }
         }
@@ -910,9 +1062,11 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       bool ok = true;
       Piece pc;
       for (int i = 0; ok && run.piece(p.sp, i, &pc); ++i) {
-        ok = entry_stored(i) && advance(sj, pc.nch > 1);  // chunk 0 reads E in TMEM
+        // a piece's last chunk advances only in the decayed form (whose final
+        // state comes from the running state)
+        ok = entry_stored(i) && advance(sj, DECAY || pc.nch > 1);  // chunk 0 reads E in TMEM
         for (int c = 0; ok && c + 1 < pc.nch; ++c, ++ntr)
-          ok = wait3(x, &B->tsread, ntr & 1) && advance(sj + c + 1, c + 2 < pc.nch);
+          ok = wait3(x, &B->tsread, ntr & 1) && advance(sj + c + 1, DECAY || c + 2 < pc.nch);
         sj += pc.nch;
       }
       if (*x.abort) {  // the state advances in flight end before TMEM is freed
@@ -980,7 +1134,8 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   p.S_N = a.S_N;
   p.z_N = a.z_N;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.status = &reinterpret_cast<WsHeader*>(ws)->status;
+  p.alpha = nullptr;
   const size_t slots = (size_t)BH * p.sp.MPH;
   if (sizeof(WsHeader) + prefill_chunked64_workspace_bytes(a.B, a.H, a.N) > a.ws_bytes)
     return cudaErrorInvalidValue;
@@ -996,7 +1151,7 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)k1::SMEM);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k3::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k3::output_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)k3::SMEM);
   if (e != cudaSuccess) return e;
   k1::aggregate_kernel<<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mphik, p, mbar_ns);
@@ -1020,7 +1175,41 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k3::kWarps);
   cfg.dynamicSmemBytes = k3::SMEM;
-  return cudaLaunchKernelEx(&cfg, k3::output_kernel, mq, mphik, mv, mo, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, k3::output_kernel<false>, mq, mphik, mv, mo, p, mbar_ns);
+}
+
+bool prefill_decay64_supported(const PrefillArgs& a) {
+  return a.bf16 && a.dk == 64 && a.dv == 64 && a.N > 0 && get_encode() != nullptr;
+}
+
+// The decayed write-then-read prefill: the output kernel alone, one block per
+// head (whole heads are the pieces, the entry state is S0), phi applied to K in
+// the kernel.  Bounded-wait failures go to the library status word.
+cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mo, a.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C))
+    return cudaErrorInvalidValue;
+  Params3 p = {};
+  p.sp = make_split(BH, a.N, BH);  // G = BH: block j runs head j
+  p.eps = a.eps;
+  p.S0 = a.S0;
+  p.z0 = a.z0;
+  p.S_N = a.S_N;
+  p.z_N = a.z_N;
+  p.alpha = alpha;
+  cudaError_t e = library_status_word(&p.status);
+  if (e != cudaSuccess) return e;
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+  e = cudaFuncSetAttribute(k3::output_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)k3::SMEM);
+  if (e != cudaSuccess) return e;
+  k3::output_kernel<true><<<p.sp.G, 32 * k3::kWarps, k3::SMEM, stream>>>(mq, mk, mv, mo, p, mbar_ns);
+  return cudaGetLastError();
 }
 
 }  // namespace la

@@ -105,9 +105,14 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  *       section 线性化核心; eps = 0 gives its form exactly).
  *   alpha   [B][H][N] float32, or NULL for no decay (then LA_MODE_CAUSAL is
  *           la_prefill exactly).  Must be NULL for LA_MODE_NONCAUSAL.
- * Other arguments, layouts, aliasing and errors as la_prefill.  Runs on the
- * CUDA cores in fp32 (one block per head), for LA_F32 and LA_BF16 inputs and
- * any dk, dv <= 128.
+ * Other arguments, layouts, aliasing and errors as la_prefill.  LA_BF16 at
+ * dk = dv = 64 with a decay in LA_MODE_CAUSAL runs on the tensor cores, one
+ * block per head, 128-token chunks with the decay factors inside each chunk
+ * (the state enters the products as a bf16 copy of the fp32 state; a zero
+ * alpha_t is taken as 1e-30); a bounded wait of that kernel that gives up is
+ * reported by delta_read_device_status.  Everything else runs on the CUDA
+ * cores in fp32 (one block per head), for LA_F32 and LA_BF16 inputs and any
+ * dk, dv <= 128.
  */
 la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dtype in_dtype,
                              int B, int H, int N, int dk, int dv, float eps,
@@ -206,13 +211,14 @@ const char* la_status_string(la_status s);
 la_status la_read_device_status(const void* workspace, cudaStream_t stream);
 
 /* Synchronizes `stream`, then returns and clears the status word of the
- * tensor-core delta kernel (delta_prefill with bf16 inputs at dk = dv = 128):
- * LA_ERR_TIMEOUT if one of its bounded waits gave up since the last read,
- * otherwise LA_OK; LA_ERR_CUDA if the synchronization or copy fails.  The
- * word belongs to the current device and is shared by every delta_prefill
- * call on it (delta_prefill takes no workspace); the token-by-token delta
- * kernel has no waits and never sets it.  LA_ERR_UNSUPPORTED if a launch
- * found its shared-memory window misaligned and did no work. */
+ * tensor-core kernels whose calls take no workspace: delta_prefill and
+ * gated_delta_prefill with bf16 inputs at dk = dv = 128, and la_prefill_variant
+ * with a decay on bf16 inputs at dk = dv = 64.  LA_ERR_TIMEOUT if one of their
+ * bounded waits gave up since the last read, otherwise LA_OK; LA_ERR_CUDA if
+ * the synchronization or copy fails.  The word belongs to the current device
+ * and is shared by every such call on it; the token-by-token kernels have no
+ * waits and never set it.  LA_ERR_UNSUPPORTED if a launch found its
+ * shared-memory window misaligned and did no work. */
 la_status delta_read_device_status(cudaStream_t stream);
 
 /*

@@ -176,3 +176,98 @@ def test_gated_delta_chunked_repeatable(la):
     for _ in range(12):
         again = la.gated_delta_prefill(kd, vd, bd, ad)
         assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
+
+
+# decayed write-then-read prefill on the tensor cores (bf16, dk = dv = 64):
+# one block per head, 128-token chunks with decay factors inside each chunk
+DECAY_N = [1, 127, 128, 129, 300, 1000]
+
+
+@pytest.mark.parametrize("N", DECAY_N)
+@pytest.mark.parametrize("arange", [(0.9, 1.0), (0.3, 1.0), (0.02, 0.5)], ids=["mild", "strong", "severe"])
+def test_decay_prefill_tc_matches_oracle(la, orc, N, arange):
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 3, N, 64, 64, torch.bfloat16, seed=140 + N)
+    g = torch.Generator().manual_seed(141 + N)
+    lo, hi = arange
+    alpha = lo + (hi - lo) * torch.rand((1, 3, N), generator=g)
+    S0 = torch.randn((1, 3, 64, 64), generator=g) * 0.5
+    z0 = torch.rand((1, 3, 64), generator=g) * 4 + 0.5
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), alpha.cuda(), 0,
+                                 S0=S0.cuda(), z0=z0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha), 0, S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
+
+
+def test_decay_prefill_tc_zero_alpha_forgets(la, orc):
+    # alpha = 0 at some tokens (taken as 1e-30 in the chunk factors): the state
+    # before them is forgotten, including right at chunk edges
+    from fixed_state_recurrent_gb300 import inputs
+    N = 520
+    q, k, v = inputs.la_inputs(2, 2, N, 64, 64, torch.bfloat16, seed=150)
+    alpha = torch.full((2, 2, N), 0.97)
+    alpha[:, :, [0, 5, 127, 128, 255, 300, 519]] = 0.0
+    S0 = torch.randn((2, 2, 64, 64), generator=torch.Generator().manual_seed(151))
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), alpha.cuda(), 0, S0=S0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha), 0, S0=f64(S0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+
+
+def test_decay_prefill_tc_alpha_one_is_prefill(la):
+    # alpha = 1: the decayed kernel computes la_prefill's recurrence (through
+    # other kernels, so within the bf16 tolerance rather than bit for bit)
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 4, 700, 64, 64, torch.bfloat16, seed=152)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    a = la.prefill_variant(qd, kd, vd, torch.ones((1, 4, 700), device="cuda"), 0)
+    ws = la.workspace(1, 4, 700, 64, 64, torch.bfloat16, 0, torch.device("cuda"))
+    b = la.prefill(qd, kd, vd, ws=ws)
+    for x, y in zip(a, b):
+        assert relmax(f64(x), f64(y)) <= TOL_BF16
+
+
+def test_decay_prefill_tc_state_in_place_and_repeatable(la, orc):
+    # S_N over S0 and z_N over z0 (the allowed aliasing); runs are bitwise equal
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 3, 777, 64, 64, torch.bfloat16, seed=153)
+    g = torch.Generator().manual_seed(154)
+    alpha = 0.6 + 0.4 * torch.rand((1, 3, 777), generator=g)
+    S0 = torch.randn((1, 3, 64, 64), generator=g)
+    z0 = torch.rand((1, 3, 64), generator=g) + 1.0
+    qd, kd, vd, ad = q.cuda(), k.cuda(), v.cuda(), alpha.cuda()
+    first = la.prefill_variant(qd, kd, vd, ad, 0, S0=S0.cuda(), z0=z0.cuda())
+    for _ in range(8):
+        again = la.prefill_variant(qd, kd, vd, ad, 0, S0=S0.cuda(), z0=z0.cuda())
+        assert all(torch.equal(x, y) for x, y in zip(first, again))
+    Sd, zd = S0.clone().cuda(), z0.clone().cuda()
+    o, S, z = la.prefill_variant(qd, kd, vd, ad, 0, S0=Sd, z0=zd, S_N=Sd, z_N=zd)
+    assert torch.equal(o, first[0]) and torch.equal(Sd, first[1]) and torch.equal(zd, first[2])
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha), 0, S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(first[0]), ro) <= TOL_BF16 and relmax(f64(Sd), rS) <= TOL_BF16
+
+
+def test_decay_prefill_tc_bounded_wait_reports_timeout(la, orc, monkeypatch):
+    # the test hook makes the kernel's MMA thread wait on an mbarrier that
+    # nothing completes (2 ms limit): the launch finishes, the library status
+    # word says LA_ERR_TIMEOUT, reading clears it, and the next call is right
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 2, 600, 64, 64, torch.bfloat16, seed=155)
+    alpha = torch.full((1, 2, 600), 0.99, device="cuda")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    la.delta_read_device_status()
+    monkeypatch.setenv("LA_TEST_FORCE_WAIT", "1")
+    monkeypatch.setenv("LA_MBAR_TIMEOUT_NS", "2000000")
+    la.prefill_variant(qd, kd, vd, alpha, 0)
+    assert la.delta_read_device_status() == 4  # LA_ERR_TIMEOUT
+    assert la.delta_read_device_status() == 0
+    monkeypatch.delenv("LA_TEST_FORCE_WAIT")
+    monkeypatch.delenv("LA_MBAR_TIMEOUT_NS")
+    o, S, z = la.prefill_variant(qd, kd, vd, alpha, 0)
+    assert la.delta_read_device_status() == 0
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha.cpu()), 0)
+    assert relmax(f64(o), ro) <= TOL_BF16
