@@ -58,6 +58,8 @@ def _args():
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run "
                         "(long,decode,delta,pr1,gated,decay,backward)")
+    p.add_argument("--profile-decay", type=int, default=0, metavar="CALLS",
+                   help="run CALLS plain decayed-prefill calls and exit (for ncu)")
     p.add_argument("--profile-delta", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain delta_prefill calls of the delta workload and exit "
                         "(for profilers)")
@@ -316,6 +318,24 @@ def profile_delta_calls(api, calls):
         api.delta_prefill(k, v, beta, reads=reads, S_N=S)
     torch.cuda.synchronize()
     print(f"profiled {calls} delta calls", flush=True)
+
+
+def profile_decay_calls(api, calls, sets=4):
+    """`calls` plain decayed-prefill calls (la_prefill_variant, alpha ~ U(0.9, 1))
+    on the headline prefill shape over rotating input sets, for profilers."""
+    import torch
+    w = inputs_mod().WORKLOADS["prefill"]
+    dev = torch.device("cuda")
+    bufs = []
+    for r in range(sets):
+        q, k, v = _device_inputs(w, w.seed + r, dev)
+        g = torch.Generator(device=dev).manual_seed(6 + 17 * r)
+        bufs.append((q, k, v, 0.9 + 0.1 * torch.rand((w.B, w.H, w.N), generator=g, device=dev)))
+    for i in range(calls):
+        q, k, v, alpha = bufs[i % sets]
+        api.prefill_variant(q, k, v, alpha, 0)
+    torch.cuda.synchronize()
+    print(f"profiled {calls} decayed prefill calls", flush=True)
 
 
 def bench_decode(api, rank, world, reps=3):
@@ -659,6 +679,10 @@ def main():
     time.sleep(0.3)
 
     w = inputs.WORKLOADS["prefill"]
+    if args.profile_decay:
+        profile_decay_calls(api, args.profile_decay)
+        sampler.stop()
+        return
     if args.profile_delta:
         profile_delta_calls(api, args.profile_delta)
         sampler.stop()
