@@ -329,6 +329,19 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_phik);
   }
+  const Run run(p.sp, blockIdx.x);
+  uint32_t pre = 0;  // loads issued during the set-up (thread 0)
+  if (threadIdx.x == 0) {  // the first stages' loads go out before the rest of the set-up
+    Piece pc;
+    for (int i = 0; pre < NS && run.piece(p.sp, i, &pc); ++i)
+      for (int c = 0; pre < NS && c < pc.nch; ++c, ++pre) {
+        uint8_t* st = smem + pre * STAGE;
+        const int tok = pc.tok0 + c * C;
+        mbar_arrive_expect_tx(&B->full[pre], 2 * BLK);
+        tma_load_3d(st, &tm_k, 0, tok, pc.h, &B->full[pre]);
+        tma_load_3d(st + BLK, &tm_v, 0, tok, pc.h, &B->full[pre]);
+      }
+  }
   init_ones(smem + OFF_ONES, threadIdx.x, 32 * kWarps);
   if (warp == 1) {
     tmem_alloc(&B->tmem_slot, kCols);
@@ -340,16 +353,16 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   tc_fence_after();
   const Ctx3 x{&p, smem, reinterpret_cast<uint64_t*>(B), &B->abort,
                *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
-  const Run run(p.sp, blockIdx.x);
   pdl_launch_dependents();  // the scan may be scheduled now; it waits for this grid's results
 
   if (warp == 0) {
-    if (lane == 0) {  // ---- TMA producer: K, V chunk tiles
-      uint32_t sj = 0, issued = 0;
+    if (lane == 0) {  // ---- TMA producer: K, V chunk tiles (the first `pre` went out above)
+      uint32_t sj = 0, issued = pre;
       Piece pc;
       for (int i = 0; run.piece(p.sp, i, &pc); ++i)
         for (int c = 0; c < pc.nch; ++c, ++sj) {
           const int s = sj % NS;
+          if (sj < pre) continue;
           if (sj >= NS && !wait3(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           uint8_t* st = smem + s * STAGE;
           const int tok = pc.tok0 + c * C;
@@ -638,6 +651,24 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
   }
+  const Run run(p.sp, blockIdx.x);
+  // The first stages' Q and V tiles (and K in the decayed form, which depends
+  // on no other kernel) go out before the rest of the set-up; each stage's
+  // barrier expects all three tiles, so phi(K) of the aggregate kernel joins
+  // it later without another arrival.
+  uint32_t pre = 0;
+  if (threadIdx.x == 0) {
+    Piece pc;
+    for (int i = 0; pre < NS && run.piece(p.sp, i, &pc); ++i)
+      for (int c = 0; pre < NS && c < pc.nch; ++c, ++pre) {
+        uint8_t* st = stage_ptr(smem, pre);
+        const int tok = pc.tok0 + c * C;
+        mbar_arrive_expect_tx(&B->full[pre], 3 * BLK);
+        tma_load_3d(st, &tm_q, 0, tok, pc.h, &B->full[pre]);
+        tma_load_3d(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[pre]);
+        if (DECAY) tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[pre]);
+      }
+  }
   init_ones(smem + OFF_ONES, threadIdx.x, 32 * kWarps);
   for (int i = threadIdx.x; i < (int)(2 * SNAP / 16); i += 32 * kWarps)  // snapshot rows 66..79 stay 0
     reinterpret_cast<uint4*>(smem + OFF_SNAP)[i] = make_uint4(0, 0, 0, 0);
@@ -651,22 +682,27 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   tc_fence_after();
   const Ctx3 x{&p, smem, reinterpret_cast<uint64_t*>(B), &B->abort,
                *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
-  const Run run(p.sp, blockIdx.x);
 
   if (warp == 0) {
-    if (lane == 0) {  // ---- TMA producer: Q, phi(K), V chunk tiles
-      uint32_t sj = 0, issued = 0;
+    if (lane == 0) {  // ---- TMA producer: Q, phi(K), V chunk tiles (see the set-up for the first)
+      uint32_t sj = 0, issued = pre;
       Piece pc;
       for (int i = 0; run.piece(p.sp, i, &pc); ++i)
         for (int c = 0; c < pc.nch; ++c, ++sj) {
           const int s = sj % NS;
-          if (sj >= NS && !wait3(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           uint8_t* st = stage_ptr(smem, s);
           const int tok = pc.tok0 + c * C;
+          if (sj < pre) {  // Q and V are on their way; phi(K) follows the aggregate kernel
+            if (!DECAY) {
+              if (sj == 0) pdl_wait();  // phi(K) is the aggregate kernel's output
+              tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
+            }
+            continue;
+          }
+          if (!wait3(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           mbar_arrive_expect_tx(&B->full[s], 3 * BLK);
           tma_load_3d(st, &tm_q, 0, tok, pc.h, &B->full[s]);
           tma_load_3d(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
-          if (!DECAY && sj == 0) pdl_wait();  // phi(K) is the aggregate kernel's output
           tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
           ++issued;
         }
