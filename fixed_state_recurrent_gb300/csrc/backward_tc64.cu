@@ -1,0 +1,622 @@
+// backward_tc64.cu -- the gradient of the causal prefill (la_prefill_backward)
+// on the sm_103a tensor cores, for bf16 inputs at dk = dv = 64.
+//
+// Forward map (page "AIGC 基本功|线性、循环与记忆架构-LinearMem", section 03):
+//   o_t = num_t / den_t,  num_t = phi(q_t)^T S_t,  den_t = phi(q_t)^T z_t + eps,
+//   S_t = S0 + sum_{s<=t} phi(k_s) v_s^T,  z_t = z0 + sum_{s<=t} phi(k_s).
+// The pages give no backward pass (the LinearMem page notes only that training
+// recomputes states instead of keeping them).  With dnum_t = dO_t / den_t and
+// dden_t = -(dO_t . o_t) / den_t, write W = phi(Q), U = phi(K), the C x 65
+// blocks D = [dnum | dden] and V~ = [V | 1] of one chunk, S_c, z_c the state
+// entering it and G_c, g_c the gradient state leaving it
+// (G = dS_N + sum over later tokens of phi(q) dnum^T, g likewise with dden):
+//   dW = mask(D V~^T) U + D [S_c | z_c]^T          (mask: s <= t)
+//   dU = mask^T(V~ D^T) W + V~ [G_c | g_c]^T       (mask^T: tau >= t)
+//   dV = mask^T(U W^T) dnum + U G_c
+//   G before the chunk = G_c + W^T dnum,  g likewise with dden;
+//   dS0 = G, dz0 = g before the first chunk; dq = dW phi'(q), dk = dU phi'(k).
+// These are the token formulas of the CUDA-core backward gathered chunkwise.
+//
+// One block per head, two sweeps over its 128-token chunks:
+//   forward:  recompute num and den (the prefill's products with the running
+//             state in TMEM), form D, then dW = mask(D V~^T) U + D [S_c | z_c]^T
+//             and dq; D (bf16) is parked in the head's rows of dv_out, which
+//             the reverse sweep reads back before overwriting them with dv;
+//   reverse:  from G = dS_N, g = dz_N, per chunk (last to first) dU and dV,
+//             then G += W^T D on the tensor cores; finally dS0, dz0.
+// The block's four warps own the TMEM lane quadrants (thread t: token row t
+// of the chunk, or state lane t); one thread issues the TMA copies and the
+// MMAs, and the steps of a chunk are separated by block barriers.  Every wait
+// is bounded; a wait that gives up records LA_ERR_TIMEOUT in the library
+// status word and the kernel finishes with unspecified outputs.
+#include "prefill_tc_common.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+using namespace tcp;
+
+namespace bw {
+
+constexpr int D = 64;
+constexpr uint32_t BLK = 16384;      // [128 rows x 128 B] swizzled tile
+constexpr uint32_t SNAP = 80 * 128;  // [80 x 64] bf16: row j = column j of the state, 64/65 = z or g
+// stage: Q | K | V | X, X = dO (fp32, two [128 x 32] boxes) in the forward
+// sweep, the parked D (bf16, two [128 x 64] blocks) in the reverse sweep
+constexpr uint32_t STAGE = 5 * BLK;
+constexpr uint32_t OFF_DT = 2 * STAGE;        // forward: D being formed (two blocks)
+constexpr uint32_t OFF_ONES = OFF_DT + 2 * BLK;
+constexpr uint32_t OFF_SNAP = OFF_ONES + BLK;
+constexpr uint32_t OFF_BAR = OFF_SNAP + SNAP;
+constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+static_assert(SMEM <= 227 * 1024, "shared memory per block");
+static_assert(OFF_SNAP % 1024 == 0, "swizzled tile alignment");
+constexpr int kThreads = 128;
+constexpr uint32_t kCols = 512;
+// TMEM columns.  Forward: A scores / P, O [num | den parts], dW, S (running
+// state, lanes j).  Reverse: A2 (V~ D^T, then its mask), dU, A3 (U W^T, then
+// its mask), dV, G (running gradient state, lanes j).
+// Every N = 128 accumulator starts at a multiple of 128 columns, the others at
+// multiples of 64.
+constexpr uint32_t T_A = 0, T_O = 128, T_DW = 256, T_S = 384;
+constexpr uint32_t T_A2 = 0, T_A3 = 128, T_DU = 256, T_DV = 320, T_G = 384;
+
+constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);   // K-major x K-major, N = 128
+constexpr uint32_t ID_QS = idesc_bf16_f32(128, 80, 0, 0);   // phi(Q) [S | z]
+constexpr uint32_t ID_PV = idesc_bf16_f32(128, 80, 0, 1);   // P [V | 1]
+constexpr uint32_t ID_N64_MN = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major, N = 64
+constexpr uint32_t ID_N64_K = idesc_bf16_f32(128, 64, 0, 0);   // both K-major, N = 64
+constexpr uint32_t ID_ADV = idesc_bf16_f32(128, 64, 1, 1);     // both MN-major (state advances)
+
+struct Params {
+  int BH, N, NC;
+  float eps;
+  const float* S0;
+  const float* z0;
+  const float* dS_N;
+  const float* dz_N;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dS0;
+  float* dz0;
+  unsigned* status;
+  int force_wait;
+};
+
+struct Bars {
+  uint64_t full[2];  // stage loads
+  uint64_t mma;      // the last MMA group complete
+  uint64_t never;    // completed by nothing (the forced-timeout test hook)
+  uint64_t drain;    // after a timeout: the MMAs in flight have ended
+  uint32_t tmem_slot;
+  int abort;
+};
+
+struct Ctx {
+  const Params* p;
+  Bars* B;
+  unsigned long long ns;
+};
+
+// Bounded wait of one thread; false once the block has given up.
+__device__ __forceinline__ bool waitb(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  if (*reinterpret_cast<volatile int*>(&x.B->abort)) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity, globaltimer_ns() + x.ns, reinterpret_cast<volatile int*>(&x.B->abort)))
+    return true;
+  x.B->abort = 1;
+  atomicOr(x.p->status, kStatusTimeout);
+  return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Row r of a [128 x 64] bf16 tile, unpacked: out[i] = element i.
+__device__ __forceinline__ void load_row_bf16(const uint8_t* tile, int r, float* out) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, c));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      out[8 * c + 2 * j] = __uint_as_float(w[j] << 16);
+      out[8 * c + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
+
+// Row r of a [128 x 64] bf16 tile from 64 floats (rounded to nearest even).
+__device__ __forceinline__ void store_row_bf16(uint8_t* tile, int r, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+    u.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+    u.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+    u.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+    *reinterpret_cast<uint4*>(tile + sw128_offset(r, c)) = u;
+  }
+}
+
+// 64 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_row64(uint32_t taddr, float* out) {
+  uint32_t a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    out[i] = __uint_as_float(a[i]);
+    out[32 + i] = __uint_as_float(b[i]);
+  }
+}
+
+// 64 floats into this thread's lane, columns [taddr, taddr + 64).
+__device__ __forceinline__ void tmem_put64(uint32_t taddr, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[16 * q + i]);
+    tmem_st16(taddr + 16 * q, w);
+  }
+}
+
+// The causal mask of a [128 x 128] fp32 score tile in TMEM (this thread's
+// row t = 32 quad + lane), packed to bf16 in place over the tile's first 64
+// columns: keep s <= t (lower), or s >= t (upper).  Column blocks are read two
+// at a time and a pair is read completely before its packed columns (which lie
+// in the pair's own or an earlier block) are written.
+template <bool UPPER>
+__device__ __forceinline__ void mask_pack(uint32_t base, int quad, int lane) {
+#pragma unroll
+  for (int q2 = 0; q2 < 4; q2 += 2) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(base + 32 * q2, r0);
+    tmem_ld32(base + 32 * (q2 + 1), r1);
+    tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q4 = q2 + h;
+      const uint32_t* r = h ? r1 : r0;
+      uint32_t w[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const int s0 = 2 * t, s1 = 2 * t + 1;  // keys 32 q4 + s within the block
+        bool k0, k1;
+        if (UPPER) {
+          k0 = q4 > quad || (q4 == quad && s0 >= lane);
+          k1 = q4 > quad || (q4 == quad && s1 >= lane);
+        } else {
+          k0 = q4 < quad || (q4 == quad && s0 <= lane);
+          k1 = q4 < quad || (q4 == quad && s1 <= lane);
+        }
+        w[t] = pack_bf16x2(k0 ? __uint_as_float(r[s0]) : 0.f, k1 ? __uint_as_float(r[s1]) : 0.f);
+      }
+      tmem_st16(base + 16 * q4, w);
+    }
+  }
+  tmem_st_wait();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_park, const Params p,
+                const unsigned long long mbar_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base, derived from the shared array by pointer
+  // arithmetic so that accesses through it stay shared-space accesses
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+  const int h = blockIdx.x;
+  const int NC = p.NC;
+  uint8_t* dt = smem + OFF_DT;
+  uint8_t* snap = smem + OFF_SNAP;
+  if (t == 0) {
+    mbar_init(&B->full[0], 1);
+    mbar_init(&B->full[1], 1);
+    mbar_init(&B->mma, 1);
+    mbar_init(&B->never, 1);
+    mbar_init(&B->drain, 1);
+    B->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_park);
+  }
+  init_ones(smem + OFF_ONES, t, kThreads);  // (contains a block barrier)
+  for (int i = t; i < (int)(2 * BLK / 16); i += kThreads)  // the D blocks
+    reinterpret_cast<uint4*>(dt)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = t; i < (int)(SNAP / 16); i += kThreads)  // the snapshot (rows 66..79 stay 0)
+    reinterpret_cast<uint4*>(snap)[i] = make_uint4(0, 0, 0, 0);
+  if (warp == 0) {
+    tmem_alloc(&B->tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot);
+  const uint32_t tl = tm + ((uint32_t)(32 * warp) << 16);  // this thread's TMEM lane (t)
+  const Ctx x{&p, B, mbar_ns};
+  const uint32_t aOnes = smem_u32(smem + OFF_ONES), aSnap = smem_u32(snap), aDt = smem_u32(dt);
+  uint32_t nload = 0, nmma = 0;  // loads issued so far (stage nload % 2), MMA groups waited
+
+  // thread 0: the loads of chunk c into stage `nload % 2`
+  auto load = [&](int c, bool forward) {
+    const int s = nload % 2;
+    uint8_t* st = smem + s * STAGE;
+    const int tok = c * C;
+    mbar_arrive_expect_tx(&B->full[s], 5 * BLK);
+    tma_load_3d(st, &tm_q, 0, tok, h, &B->full[s]);
+    tma_load_3d(st + BLK, &tm_k, 0, tok, h, &B->full[s]);
+    tma_load_3d(st + 2 * BLK, &tm_v, 0, tok, h, &B->full[s]);
+    if (forward) {
+      tma_load_3d(st + 3 * BLK, &tm_do, 0, tok, h, &B->full[s]);
+      tma_load_3d(st + 4 * BLK, &tm_do, 32, tok, h, &B->full[s]);
+    } else {
+      tma_load_3d(st + 3 * BLK, &tm_park, 0, tok, h, &B->full[s]);
+      tma_load_3d(st + 4 * BLK, &tm_park, 64, tok, h, &B->full[s]);
+    }
+    ++nload;
+  };
+  // every thread: the MMA group thread 0 committed has completed
+  auto mma_done = [&]() {
+    waitb(x, &B->mma, nmma & 1);
+    ++nmma;
+    tc_fence_after();
+  };
+  // thread 0, before issuing MMAs
+  auto issuing = [&]() {
+    tc_fence_after();
+    return !*reinterpret_cast<volatile int*>(&B->abort);
+  };
+  // the end of a CUDA-core step whose TMEM and shared-memory writes MMAs read
+  auto step_done = [&]() {
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+  };
+
+  // =================== forward sweep ===================
+  // S0, z0 -> the running state (lane j: column j of S, lane 64: z) and its
+  // snapshot (row j; rows 64, 65: z in two bf16 parts)
+  {
+    float e[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      e[i] = t < D ? (p.S0 ? __ldg(p.S0 + ((size_t)h * D + i) * D + t) : 0.f)
+                   : (t == D && p.z0 ? __ldg(p.z0 + (size_t)h * D + i) : 0.f);
+    tmem_put64(tl + T_S, e);
+    tmem_st_wait();
+    if (t < D) {
+      store_row_bf16(snap, t, e);
+    } else if (t == D) {
+      float lo[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) lo[i] = e[i] - __bfloat162float(__float2bfloat16_rn(e[i]));
+      store_row_bf16(snap, D, e);
+      store_row_bf16(snap, D + 1, lo);
+    }
+  }
+  if (t == 0 && NC > 0) load(0, true);
+  step_done();
+
+  for (int c = 0; c < NC; ++c) {
+    const int s = c % 2;
+    uint8_t* st = smem + s * STAGE;
+    const uint32_t aq = smem_u32(st), ak = aq + BLK, av = aq + 2 * BLK;
+    const int valid = min(C, p.N - c * C);
+    if (t == 0 && c + 1 < NC) load(c + 1, true);
+    waitb(x, &B->full[s], (c / 2) & 1);
+    phi_row<8>(st, t, 0, valid);
+    phi_row<8>(st + BLK, t, 0, valid);
+    step_done();
+
+    // scores, and phi(Q) [S | z] into O
+    if (t == 0 && (!p.force_wait || waitb(x, &B->never, 0)) && issuing()) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_bf16_ss(tm + T_A, sdesc_sw128(aq + ks * 32, 16, 1024), sdesc_sw128(ak + ks * 32, 16, 1024),
+                    ID_S, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_bf16_ss(tm + T_O, sdesc_sw128(aq + ks * 32, 16, 1024), sdesc_sw128(aSnap + ks * 32, 16, 1024),
+                    ID_QS, ks > 0);
+    }
+    if (t == 0) mma_commit(&B->mma);
+    mma_done();
+    mask_pack<false>(tl + T_A, warp, lane);
+    step_done();
+
+    // O += P [V | 1]
+    if (t == 0 && issuing()) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < C / 16; ++ks)
+        mma_bf16_ts(tm + T_O, tm + T_A + 8 * ks, sdesc_sw128(av + ks * 2048, aOnes - av, 1024), ID_PV, 1u);
+    }
+    if (t == 0) mma_commit(&B->mma);
+    mma_done();
+    {  // den, o, then D = [dnum | dden] of row t
+      float num[64];
+      tmem_row64(tl + T_O, num);
+      uint32_t d2[2];
+      tmem_ld2(tl + T_O + D, d2);
+      tmem_ld_wait();
+      const float den = __uint_as_float(d2[0]) + __uint_as_float(d2[1]) + p.eps;
+      const float inv = 1.f / den;
+      float dot = 0.f;
+      const uint8_t* x0 = st + 3 * BLK;
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {
+        const float4 g4 = *reinterpret_cast<const float4*>(x0 + (cc / 8) * BLK + sw128_offset(t, cc % 8));
+        const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          dot += gv[j] * (num[4 * cc + j] * inv);
+          num[4 * cc + j] = gv[j] * inv;  // now dnum
+        }
+      }
+      const float dden = -dot * inv;
+      store_row_bf16(dt, t, num);
+      *reinterpret_cast<uint4*>(dt + BLK + sw128_offset(t, 0)) =
+          make_uint4(pack_bf16x2(dden, dden), 0u, 0u, 0u);
+      // parked in dv's row (256 bytes): 64 bf16 dnum, then dden twice and zeros,
+      // the row-major form the reverse sweep's tile loads read back
+      if (t < valid) {
+        uint4* row = reinterpret_cast<uint4*>(p.dv + ((size_t)h * p.N + c * C + t) * D);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          row[q] = make_uint4(pack_bf16x2(num[8 * q], num[8 * q + 1]), pack_bf16x2(num[8 * q + 2], num[8 * q + 3]),
+                              pack_bf16x2(num[8 * q + 4], num[8 * q + 5]), pack_bf16x2(num[8 * q + 6], num[8 * q + 7]));
+        row[8] = make_uint4(pack_bf16x2(dden, dden), 0u, 0u, 0u);
+#pragma unroll
+        for (int q = 9; q < 16; ++q) row[q] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    step_done();
+
+    // A = D V~^T, dW = D [S | z]^T; D goes to dv_out to wait for the reverse sweep
+    if (t == 0 && issuing()) {
+#pragma unroll
+      for (int ks = 0; ks < 5; ++ks) {
+        const uint32_t a = ks < 4 ? aDt + ks * 32 : aDt + BLK;
+        const uint32_t b = ks < 4 ? av + ks * 32 : aOnes;
+        mma_bf16_ss(tm + T_A, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024), ID_S, ks > 0);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 5; ++ks) {
+        const uint32_t a = ks < 4 ? aDt + ks * 32 : aDt + BLK;
+        mma_bf16_ss(tm + T_DW, sdesc_sw128(a, 16, 1024), sdesc_sw128(aSnap + ks * 2048, 16, 1024),
+                    ID_N64_MN, ks > 0);
+      }
+    }
+    if (t == 0) mma_commit(&B->mma);
+    mma_done();
+    mask_pack<false>(tl + T_A, warp, lane);
+    step_done();
+
+    // dW += mask(A) U;  S += [V | 1]^T U
+    if (t == 0 && issuing()) {
+#pragma unroll
+      for (int ks = 0; ks < C / 16; ++ks)
+        mma_bf16_ts(tm + T_DW, tm + T_A + 8 * ks, sdesc_sw128(ak + ks * 2048, BLK, 1024), ID_N64_MN, 1u);
+#pragma unroll
+      for (int ks = 0; ks < C / 16; ++ks)
+        mma_bf16_ss(tm + T_S, sdesc_sw128(av + ks * 2048, aOnes - av, 1024),
+                    sdesc_sw128(ak + ks * 2048, BLK, 1024), ID_ADV, 1u);
+    }
+    if (t == 0) mma_commit(&B->mma);
+    mma_done();
+    {  // dq = dW phi'(q), phi'(u) = min(phi(u), 1); the state snapshot for the next chunk
+      float g[64], f[64];
+      tmem_row64(tl + T_DW, g);
+      load_row_bf16(st, t, f);
+      if (t < valid && !*reinterpret_cast<volatile int*>(&B->abort)) {
+        float4* dst = reinterpret_cast<float4*>(p.dq + ((size_t)h * p.N + c * C + t) * D);
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          dst[q] = make_float4(g[4 * q] * fminf(f[4 * q], 1.f), g[4 * q + 1] * fminf(f[4 * q + 1], 1.f),
+                               g[4 * q + 2] * fminf(f[4 * q + 2], 1.f), g[4 * q + 3] * fminf(f[4 * q + 3], 1.f));
+      }
+      if (c + 1 < NC && warp <= 2) {  // whole warps: tcgen05.ld is warp-collective
+        float e[64];
+        tmem_row64(tl + T_S, e);
+        if (t < D) store_row_bf16(snap, t, e);
+        if (t == D) {
+          store_row_bf16(snap, D, e);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) e[i] -= __bfloat162float(__float2bfloat16_rn(e[i]));
+          store_row_bf16(snap, D + 1, e);
+        }
+      }
+    }
+    step_done();
+  }
+  // every thread's parked rows are written before the tile loads read them
+  __threadfence();
+  fence_proxy_async_global();
+
+  // =================== reverse sweep ===================
+  // G = dS_N, g = dz_N -> the running gradient state (lane j: column j of G,
+  // lane 64: g) and its snapshot (row j; row 64: g; row 65 stays 0)
+  {
+    float e[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      e[i] = t < D ? (p.dS_N ? __ldg(p.dS_N + ((size_t)h * D + i) * D + t) : 0.f)
+                   : (t == D && p.dz_N ? __ldg(p.dz_N + (size_t)h * D + i) : 0.f);
+    tmem_put64(tl + T_G, e);
+    tmem_st_wait();
+    if (t <= D) store_row_bf16(snap, t, e);
+    if (t == D + 1) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) e[i] = 0.f;
+      store_row_bf16(snap, D + 1, e);
+    }
+  }
+  step_done();  // (also: every thread's parked rows are fenced before the first tile load)
+  if (t == 0 && NC > 0) load(NC - 1, false);
+
+  for (int r = 0; r < NC; ++r) {
+    const int c = NC - 1 - r;
+    const uint32_t li = (uint32_t)NC + r;  // this chunk's load
+    const int s = li % 2;
+    uint8_t* st = smem + s * STAGE;
+    const uint32_t aq = smem_u32(st), ak = aq + BLK, av = aq + 2 * BLK, ax = aq + 3 * BLK;
+    const int valid = min(C, p.N - c * C);
+    if (t == 0 && c > 0) load(c - 1, false);
+    waitb(x, &B->full[s], (li / 2) & 1);
+    phi_row<8>(st, t, 0, valid);
+    phi_row<8>(st + BLK, t, 0, valid);
+    step_done();
+
+    // A2 = V~ D^T, dU = V~ [G | g]^T, A3 = U W^T, dV = U G
+    if (t == 0 && issuing()) {
+#pragma unroll
+      for (int ks = 0; ks < 5; ++ks) {
+        const uint32_t a = ks < 4 ? av + ks * 32 : aOnes;
+        const uint32_t b = ks < 4 ? ax + ks * 32 : ax + BLK;
+        mma_bf16_ss(tm + T_A2, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024), ID_S, ks > 0);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 5; ++ks) {
+        const uint32_t a = ks < 4 ? av + ks * 32 : aOnes;
+        mma_bf16_ss(tm + T_DU, sdesc_sw128(a, 16, 1024), sdesc_sw128(aSnap + ks * 2048, 16, 1024),
+                    ID_N64_MN, ks > 0);
+      }
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_bf16_ss(tm + T_A3, sdesc_sw128(ak + ks * 32, 16, 1024), sdesc_sw128(aq + ks * 32, 16, 1024),
+                    ID_S, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_bf16_ss(tm + T_DV, sdesc_sw128(ak + ks * 32, 16, 1024), sdesc_sw128(aSnap + ks * 32, 16, 1024),
+                    ID_N64_K, ks > 0);
+    }
+    if (t == 0) mma_commit(&B->mma);
+    mma_done();
+    mask_pack<true>(tl + T_A2, warp, lane);
+    mask_pack<true>(tl + T_A3, warp, lane);
+    step_done();
+
+    // dU += mask^T(A2) W, dV += mask^T(A3) dnum, G += W^T D
+    if (t == 0 && issuing()) {
+#pragma unroll
+      for (int ks = 0; ks < C / 16; ++ks)
+        mma_bf16_ts(tm + T_DU, tm + T_A2 + 8 * ks, sdesc_sw128(aq + ks * 2048, BLK, 1024), ID_N64_MN, 1u);
+#pragma unroll
+      for (int ks = 0; ks < C / 16; ++ks)
+        mma_bf16_ts(tm + T_DV, tm + T_A3 + 8 * ks, sdesc_sw128(ax + ks * 2048, BLK, 1024), ID_N64_MN, 1u);
+#pragma unroll
+      for (int ks = 0; ks < C / 16; ++ks)
+        mma_bf16_ss(tm + T_G, sdesc_sw128(ax + ks * 2048, BLK, 1024), sdesc_sw128(aq + ks * 2048, BLK, 1024),
+                    ID_ADV, 1u);
+    }
+    if (t == 0) mma_commit(&B->mma);
+    mma_done();
+    {  // dk = dU phi'(k), dv; the gradient-state snapshot for the chunk before
+      float g[64], f[64];
+      tmem_row64(tl + T_DU, g);
+      load_row_bf16(st + BLK, t, f);
+      const bool out = t < valid && !*reinterpret_cast<volatile int*>(&B->abort);
+      if (out) {
+        float4* dst = reinterpret_cast<float4*>(p.dk + ((size_t)h * p.N + c * C + t) * D);
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          dst[q] = make_float4(g[4 * q] * fminf(f[4 * q], 1.f), g[4 * q + 1] * fminf(f[4 * q + 1], 1.f),
+                               g[4 * q + 2] * fminf(f[4 * q + 2], 1.f), g[4 * q + 3] * fminf(f[4 * q + 3], 1.f));
+      }
+      tmem_row64(tl + T_DV, g);
+      if (out) {
+        float4* dst = reinterpret_cast<float4*>(p.dv + ((size_t)h * p.N + c * C + t) * D);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) dst[q] = make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+      }
+      if (warp <= 2) {  // whole warps: tcgen05.ld is warp-collective; lanes 0..64 are kept
+        float e[64];
+        tmem_row64(tl + T_G, e);
+        if (c > 0 && t <= D) store_row_bf16(snap, t, e);
+        if (c == 0 && t <= D && !*reinterpret_cast<volatile int*>(&B->abort)) {  // dS0, dz0
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            if (t < D) {
+              if (p.dS0) p.dS0[((size_t)h * D + i) * D + t] = e[i];
+            } else if (p.dz0) {
+              p.dz0[(size_t)h * D + i] = e[i];
+            }
+          }
+        }
+      }
+    }
+    step_done();
+  }
+
+  if (t == 0 && *reinterpret_cast<volatile int*>(&B->abort)) {  // MMAs in flight end first
+    int never = 0;
+    mma_commit(&B->drain);
+    mbar_wait(&B->drain, 0, globaltimer_ns() + mbar_ns, &never);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tm, kCols);
+  }
+}
+
+}  // namespace bw
+}  // namespace
+
+bool backward_tc64_supported(const PrefillArgs& a) {
+  return a.bf16 && a.dk == 64 && a.dv == 64 && a.N > 0 && get_encode() != nullptr;
+}
+
+cudaError_t launch_backward_tc64(const PrefillArgs& a, const float* dO, const float* dS_N,
+                                 const float* dz_N, float* dq, float* dk, float* dv, float* dS0,
+                                 float* dz0, cudaStream_t stream) {
+  using namespace bw;
+  const int BH = a.B * a.H;
+  CUtensorMap mq, mk, mv, mdo, mpark;
+  if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
+      // dv's rows seen as 128 bf16 each: two [128 x 64] blocks of D per chunk
+      !make_map(&mpark, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2 * D, a.N, BH, 64, C))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.BH = BH;
+  p.N = a.N;
+  p.NC = (a.N + C - 1) / C;
+  p.eps = a.eps;
+  p.S0 = a.S0;
+  p.z0 = a.z0;
+  p.dS_N = dS_N;
+  p.dz_N = dz_N;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.dS0 = dS0;
+  p.dz0 = dz0;
+  cudaError_t e = library_status_word(&p.status);
+  if (e != cudaSuccess) return e;
+  p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  e = cudaFuncSetAttribute(backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  if (e != cudaSuccess) return e;
+  backward_kernel<<<BH, kThreads, SMEM, stream>>>(mq, mk, mv, mdo, mpark, p, mbar_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace la

@@ -287,6 +287,8 @@ la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dt
   a.chunk = 0;
   a.workspace = nullptr;
   a.ws_bytes = 0;
+  if (la::backward_tc64_supported(a))
+    return from_cuda(la::launch_backward_tc64(a, dO, dS_N, dz_N, dq, dk_out, dv_out, dS0, dz0, stream));
   return from_cuda(la::launch_prefill_backward(a, dO, dS_N, dz_N, dq, dk_out, dv_out, dS0, dz0,
                                                stream));
 }

@@ -54,6 +54,15 @@ cudaError_t launch_prefill_variant_simt(const PrefillArgs& a, const float* alpha
 cudaError_t launch_prefill_backward(const PrefillArgs& p, const float* dO, const float* dS_N,
                                     const float* dz_N, float* dq, float* dk, float* dv,
                                     float* dS0, float* dz0, cudaStream_t stream);
+// The same gradient on the tensor cores for bf16 inputs at dk = dv = 64
+// (backward_tc64.cu): one block per head, a forward and a reverse sweep over
+// 128-token chunks.  Needs no workspace (it parks bf16 data in dv until the
+// reverse sweep overwrites it); bounded-wait failures go to the library status
+// word.
+bool backward_tc64_supported(const PrefillArgs& a);
+cudaError_t launch_backward_tc64(const PrefillArgs& a, const float* dO, const float* dS_N,
+                                 const float* dz_N, float* dq, float* dk, float* dv, float* dS0,
+                                 float* dz0, cudaStream_t stream);
 
 // Tensor-core chunked prefill for dk = dv = 64: aggregate, scan and output
 // launches (prefill_chunked64.cu).  The workspace size depends on the SM count

@@ -62,6 +62,63 @@ __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
   return tc::pack_bf16x2(phi_fast(lo), phi_fast(hi));
 }
 
+// 2^x by the single-precision hardware approximation, subnormal results
+// flushed to zero (exp(u) < 2^-126 is far below what bf16 sums of phi keep).
+__device__ __forceinline__ float exp2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// phi on two bf16: phi(u) = exp(min(u, 0)) + max(u, 0), which is u + 1 for
+// u > 0 and exp(u) otherwise.  min and max are taken on the bf16 pair, the
+// exponentials as 2^(min(u, 0) log2 e) in fp32, and the sum is rounded to
+// bf16, the precision of the tensor-core operand it feeds: the result is
+// within one bf16 rounding of phi(u).
+__device__ __forceinline__ uint32_t phi2(uint32_t x) {
+  const __nv_bfloat162 u = *reinterpret_cast<const __nv_bfloat162*>(&x);
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const __nv_bfloat162 m = __hmin2(u, zero);
+  const __nv_bfloat162 M = __hmax2(u, zero);
+  const uint32_t mb = *reinterpret_cast<const uint32_t*>(&m);
+  const uint32_t e = tc::pack_bf16x2(exp2_ftz(__uint_as_float(mb << 16) * 1.4426950408889634f),
+                                 exp2_ftz(__uint_as_float(mb & 0xFFFF0000u) * 1.4426950408889634f));
+  const __nv_bfloat162 r = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&e), M);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// phi on `nchunk` 16-byte chunks of row r of a tile starting at chunk `c0`;
+// rows at or past `valid` become zero.  Loads first, then math, then stores.
+// The row mask is applied with an AND after an unconditional phi: a
+// conditional around phi2 lets the compiler branch around every pair, which
+// serialises the 4 NCH independent exponential chains of a thread.
+template <int NCH>
+__device__ __forceinline__ void phi_row(uint8_t* tile, int r, int c0, int valid) {
+  uint4 v[NCH];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) v[i] = *reinterpret_cast<const uint4*>(tile + tc::sw128_offset(r, c0 + i));
+  const uint32_t keep = r < valid ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    v[i].x = phi2(v[i].x) & keep;
+    v[i].y = phi2(v[i].y) & keep;
+    v[i].z = phi2(v[i].z) & keep;
+    v[i].w = phi2(v[i].w) & keep;
+  }
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) *reinterpret_cast<uint4*>(tile + tc::sw128_offset(r, c0 + i)) = v[i];
+}
+
+// The all-ones operand block: a [128 token rows x 64] bf16 swizzled tile whose
+// column 0 is 1 (as the second atom of [V | 1], read MN-major or K-major).
+// Contains a block-wide barrier.
+__device__ __forceinline__ void init_ones(uint8_t* ones, int tid, int nthreads) {
+  for (int i = tid; i < (int)(16384 / 16); i += nthreads)
+    reinterpret_cast<uint4*>(ones)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  if (tid < C) *reinterpret_cast<uint16_t*>(ones + tc::sw128_offset(tid, 0)) = 0x3F80u;  // bf16 1.0
+}
+
 // Flag word of an item: (generation << 2) | state.
 constexpr unsigned kFlagAggregate = 1u;  // agg[g] is published
 constexpr unsigned kFlagInclusive = 2u;  // inc[g] is published

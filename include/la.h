@@ -136,8 +136,13 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
  *   dq, dk_out [B][H][N][dk], dv_out [B][H][N][dv]: float32 outputs (the
  *               gradients with respect to q, k and v)
  *   dS0 [B][H][dk][dv], dz0 [B][H][dk]: float32 outputs, or NULL if not wanted
- * Outputs must not overlap any input or each other.  Runs on the CUDA cores in
- * fp32, one block per head, token by token (no workspace); any dk, dv <= 128.
+ * Outputs must not overlap any input or each other.  LA_BF16 at dk = dv = 64
+ * runs on the tensor cores: one block per head, a forward and a reverse sweep
+ * over 128-token chunks (bf16 operands, fp32 accumulation; dv_out holds bf16
+ * intermediate rows between the sweeps); a bounded wait of that kernel that
+ * gives up is reported by delta_read_device_status.  Everything else runs on
+ * the CUDA cores in fp32, one block per head, token by token; any dk, dv <= 128.
+ * Neither takes a workspace.
  */
 la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dtype in_dtype,
                               int B, int H, int N, int dk, int dv, float eps,
@@ -212,8 +217,8 @@ la_status la_read_device_status(const void* workspace, cudaStream_t stream);
 
 /* Synchronizes `stream`, then returns and clears the status word of the
  * tensor-core kernels whose calls take no workspace: delta_prefill and
- * gated_delta_prefill with bf16 inputs at dk = dv = 128, and la_prefill_variant
- * with a decay on bf16 inputs at dk = dv = 64.  LA_ERR_TIMEOUT if one of their
+ * gated_delta_prefill with bf16 inputs at dk = dv = 128, la_prefill_variant
+ * with a decay and la_prefill_backward on bf16 inputs at dk = dv = 64.  LA_ERR_TIMEOUT if one of their
  * bounded waits gave up since the last read, otherwise LA_OK; LA_ERR_CUDA if
  * the synchronization or copy fails.  The word belongs to the current device
  * and is shared by every such call on it; the token-by-token kernels have no

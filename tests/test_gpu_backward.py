@@ -62,3 +62,81 @@ def test_backward_zero_length_passes_state_gradient(la):
     dq, dk, dv, dS0, dz0 = la.prefill_backward(e, e, e, e, dS_N=dS)
     assert torch.equal(dS0, dS)
     assert torch.count_nonzero(dz0) == 0
+
+
+# the tensor-core backward (bf16, dk = dv = 64): one block per head, a forward
+# and a reverse sweep over 128-token chunks
+TC_N = [1, 2, 127, 128, 129, 300, 1000]
+
+
+@pytest.mark.parametrize("N", TC_N)
+@pytest.mark.parametrize("with_state", [False, True], ids=["zero", "state"])
+def test_backward_tc_matches_oracle(la, orc, N, with_state):
+    from fixed_state_recurrent_gb300 import inputs
+    B, H = 1, 3
+    q, k, v = inputs.la_inputs(B, H, N, 64, 64, torch.bfloat16, seed=170 + N)
+    g = torch.Generator().manual_seed(171 + N)
+    dO = torch.randn((B, H, N, 64), generator=g)
+    S0 = z0 = dS = dz = None
+    if with_state:
+        S0 = torch.randn((B, H, 64, 64), generator=g) * 0.5
+        z0 = torch.rand((B, H, 64), generator=g) * 4 + 0.5
+        dS = torch.randn((B, H, 64, 64), generator=g)
+        dz = torch.randn((B, H, 64), generator=g)
+    cu = lambda t: None if t is None else t.cuda()
+    got = la.prefill_backward(q.cuda(), k.cuda(), v.cuda(), dO.cuda(), S0=cu(S0), z0=cu(z0),
+                              dS_N=cu(dS), dz_N=cu(dz))
+    f = lambda t: None if t is None else f64(t)
+    want = orc.la_backward(f64(q), f64(k), f64(v), f64(dO), S0=f(S0), z0=f(z0), dS_N=f(dS),
+                           dz_N=f(dz))
+    for name, a, b in zip(("dq", "dk", "dv", "dS0", "dz0"), got, want):
+        if N == 1 and not with_state and name in ("dq", "dk"):
+            # one token from a zero state: the exact gradient is O(eps) (see
+            # test_backward_matches_oracle), the difference of two terms of
+            # size T = max|phi(k)| |v.dO| / den (dq; phi(q) for dk) that the
+            # tensor cores form from bf16 operands, each term within about
+            # 3 * 2^-9 of itself: checked against 2^-6 T
+            phi = lambda u: np.where(u > 0, u + 1.0, np.exp(np.minimum(u, 0.0)))
+            fq, fk = phi(f64(q)[0, :, 0]), phi(f64(k)[0, :, 0])   # [H, 64]
+            vd = np.abs(np.sum(f64(v)[0, :, 0] * f64(dO)[0, :, 0], axis=-1))
+            den = np.sum(fq * fk, axis=-1) + 1e-6
+            other = fk if name == "dq" else fq
+            T = np.max(np.abs(other).max(axis=-1) * vd / den)
+            assert np.max(np.abs(f64(a) - b)) <= 2.0 ** -6 * T, name
+            continue
+        assert relmax(f64(a), b) <= tol_for(torch.bfloat16), name
+    assert la.delta_read_device_status() == 0
+
+
+def test_backward_tc_repeatable(la):
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(2, 2, 555, 64, 64, torch.bfloat16, seed=180)
+    dO = torch.randn((2, 2, 555, 64), generator=torch.Generator().manual_seed(181)).cuda()
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    first = la.prefill_backward(qd, kd, vd, dO)
+    for _ in range(6):
+        again = la.prefill_backward(qd, kd, vd, dO)
+        assert all(torch.equal(a, b) for a, b in zip(first, again))
+
+
+def test_backward_tc_bounded_wait_reports_timeout(la, orc, monkeypatch):
+    # the test hook makes the kernel's MMA issuer wait on an mbarrier that
+    # nothing completes (2 ms limit): the launch finishes, the library status
+    # word says LA_ERR_TIMEOUT, reading clears it, and the next call is right
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 2, 400, 64, 64, torch.bfloat16, seed=182)
+    dO = torch.randn((1, 2, 400, 64), generator=torch.Generator().manual_seed(183))
+    qd, kd, vd, dd = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    la.delta_read_device_status()
+    monkeypatch.setenv("LA_TEST_FORCE_WAIT", "1")
+    monkeypatch.setenv("LA_MBAR_TIMEOUT_NS", "2000000")
+    la.prefill_backward(qd, kd, vd, dd)
+    assert la.delta_read_device_status() == 4  # LA_ERR_TIMEOUT
+    assert la.delta_read_device_status() == 0
+    monkeypatch.delenv("LA_TEST_FORCE_WAIT")
+    monkeypatch.delenv("LA_MBAR_TIMEOUT_NS")
+    got = la.prefill_backward(qd, kd, vd, dd)
+    assert la.delta_read_device_status() == 0
+    want = orc.la_backward(f64(q), f64(k), f64(v), f64(dO))
+    for a, b in zip(got[:3], want[:3]):
+        assert relmax(f64(a), b) <= tol_for(torch.bfloat16)
