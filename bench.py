@@ -58,6 +58,8 @@ def _args():
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run "
                         "(long,decode,delta,pr1,gated,decay,backward)")
+    p.add_argument("--profile-backward", type=int, default=0, metavar="CALLS",
+                   help="run CALLS plain la_prefill_backward calls and exit (for ncu)")
     p.add_argument("--profile-decay", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain decayed-prefill calls and exit (for ncu)")
     p.add_argument("--profile-delta", type=int, default=0, metavar="CALLS",
@@ -338,6 +340,21 @@ def profile_decay_calls(api, calls, sets=4):
     print(f"profiled {calls} decayed prefill calls", flush=True)
 
 
+def profile_backward_calls(api, calls):
+    """`calls` plain la_prefill_backward calls on the headline prefill shape
+    (bf16 inputs, dO ~ N(0,1)), for profilers."""
+    import torch
+    w = inputs_mod().WORKLOADS["prefill"]
+    dev = torch.device("cuda")
+    q, k, v = _device_inputs(w, w.seed, dev)
+    g = torch.Generator(device=dev).manual_seed(9)
+    dO = torch.randn((w.B, w.H, w.N, w.dv), generator=g, device=dev)
+    for _ in range(calls):
+        api.prefill_backward(q, k, v, dO)
+    torch.cuda.synchronize()
+    print(f"profiled {calls} backward calls", flush=True)
+
+
 def bench_decode(api, rank, world, reps=3):
     """100 consecutive decode steps captured in one CUDA graph; the state comes
     from a 1024-token prefix run through la_prefill."""
@@ -477,9 +494,9 @@ def bench_decay_prefill(api, rank, world, reps=12, sets=4):
             "l2": f"{sets} rotating input/output sets"}
 
 
-def bench_backward(api, rank, world, reps=3):
-    """la_prefill_backward on the headline prefill shape (dO ~ N(0,1)): CUDA
-    cores, one block per head, token by token."""
+def bench_backward(api, rank, world, reps=5):
+    """la_prefill_backward on the headline prefill shape (dO ~ N(0,1)): tensor
+    cores, one block per head, a forward and a reverse sweep."""
     import torch
     w = inputs_mod().WORKLOADS["prefill"]
     dev = torch.device("cuda")
@@ -492,10 +509,14 @@ def bench_backward(api, rank, world, reps=3):
     with torch.cuda.stream(stream):
         fn(0)
     _, per = _timed(fn, reps, stream, world)
-    ms = min(per)
+    ms = statistics.median(per)
+    # algorithmic bytes: q, k, v (bf16) and dO (fp32) in, dq, dk, dv (fp32) out
+    b = (3 * 2 * w.dk + 4 * w.dv + 4 * (2 * w.dk + w.dv)) * w.tokens
+    hbm_peak, _, kind = _peaks()
     return {"workload": "backward: B=4 H=8 N=4096 dk=dv=64 bf16 inputs, dO ~ N(0,1), "
                         "gradients of q, k, v, S0, z0", "ms_per_call": ms,
-            "tokens_per_s": w.tokens / (ms * 1e-3)}
+            "tokens_per_s": w.tokens / (ms * 1e-3), "hbm_gbs": b / (ms * 1e-3) / 1e9,
+            "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": f"of {kind}"}
 
 
 def inputs_mod():
@@ -679,6 +700,10 @@ def main():
     time.sleep(0.3)
 
     w = inputs.WORKLOADS["prefill"]
+    if args.profile_backward:
+        profile_backward_calls(api, args.profile_backward)
+        sampler.stop()
+        return
     if args.profile_decay:
         profile_decay_calls(api, args.profile_decay)
         sampler.stop()
