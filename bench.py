@@ -459,8 +459,8 @@ def bench_gated_delta(api, rank, world, reps=3):
 
 def bench_decay_prefill(api, rank, world, reps=12, sets=4):
     """la_prefill_variant, write-then-read with a per-token decay, on the
-    headline prefill shape (tensor cores, one block per head), over `sets`
-    rotating input/output sets (~350 MB > L2)."""
+    headline prefill shape (tensor cores, the heads split over the SMs with a
+    workspace), over `sets` rotating input/output sets (~350 MB > L2)."""
     import torch
     w = inputs_mod().WORKLOADS["prefill"]
     dev = torch.device("cuda")
@@ -524,29 +524,23 @@ def inputs_mod():
     return inputs
 
 
-def bench_simple_prefill(api, wname, rank, world, reps=5):
+def bench_simple_prefill(api, wname, rank, world, steps=20):
+    """la_prefill on another workload, timed like the headline: `steps` calls
+    over rotating buffer sets captured as one CUDA graph and replayed, so the
+    figure is device time per call (the host's call path is not in it)."""
     import torch
     from fixed_state_recurrent_gb300 import inputs
     w = inputs.WORKLOADS[wname]
-    dev = torch.device("cuda")
-    q, k, v = _device_inputs(w, w.seed + 1000 * rank, dev)
-    o = torch.empty((w.B, w.H, w.N, w.dv), device=dev)
-    S = torch.empty((w.B, w.H, w.dk, w.dv), device=dev)
-    z = torch.empty((w.B, w.H, w.dk), device=dev)
-    ws = api.workspace(w.B, w.H, w.N, w.dk, w.dv, w.dtype, 0, dev)
-    stream = torch.cuda.Stream()
-    stream.wait_stream(torch.cuda.current_stream())
-    fn = lambda i: api.prefill(q, k, v, o=o, S_N=S, z_N=z, ws=ws)
-    with torch.cuda.stream(stream):
-        fn(0)
-    _, per = _timed(fn, reps, stream, world)
-    ms = statistics.median(per)
+    total, _ = bench_prefill(api, w, steps, 3, rank, world)
+    ms = total / steps
     res = {"workload": f"{wname}: B={w.B} H={w.H} N={w.N} dk={w.dk} dv={w.dv} "
                        f"{'bf16' if w.dtype == torch.bfloat16 else 'fp32'}",
-           "ms_per_call": ms, "tokens_per_s": w.tokens / (ms * 1e-3)}
+           "ms_per_call": ms, "tokens_per_s": w.tokens / (ms * 1e-3),
+           "timing": f"{steps} calls in one CUDA graph, rotating buffer sets"}
     if w.dtype == torch.bfloat16:
         b = PREFILL_BYTES_PER_TOKEN * w.tokens + w.B * w.H * (w.dk * w.dv + w.dk) * 4
         res["hbm_gbs"] = b / (ms * 1e-3) / 1e9
+        res["hbm_frac"] = b / (ms * 1e-3) / 1e9 / _peaks()[0]
     return res
 
 

@@ -24,7 +24,8 @@ LA_MODE_CAUSAL, LA_MODE_READ_BEFORE_WRITE, LA_MODE_NONCAUSAL = 0, 1, 2
 SYMBOLS = ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
            "delta_prefill", "la_state_bytes", "la_status_string",
            "la_read_device_status", "delta_read_device_status",
-           "la_prefill_variant", "gated_delta_prefill", "la_prefill_backward")
+           "la_prefill_variant", "la_prefill_variant_workspace_bytes", "gated_delta_prefill",
+           "la_prefill_backward")
 
 
 class LAError(RuntimeError):
@@ -70,8 +71,10 @@ def load(path: str | None = None):
         lib.delta_read_device_status.argtypes = [vp]
         lib.delta_read_device_status.restype = i
         lib.la_prefill_variant.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, vp, i, vp, vp,
-                                           vp, vp, vp, vp]
+                                           vp, vp, vp, vp, sz, vp]
         lib.la_prefill_variant.restype = i
+        lib.la_prefill_variant_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.la_prefill_variant_workspace_bytes.restype = sz
         lib.gated_delta_prefill.argtypes = [vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
         lib.gated_delta_prefill.restype = i
         lib.la_prefill_backward.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp, vp, vp,
@@ -246,10 +249,23 @@ def gated_delta_prefill(k, v, beta, alpha=None, S0=None, *, reads=None, S_N=None
     return reads, S_N
 
 
+_vws_cache: dict = {}
+
+
+def variant_workspace_bytes(B, H, N, dk, dv, dtype=torch.bfloat16, mode=LA_MODE_CAUSAL,
+                            decay=True) -> int:
+    """la_prefill_variant_workspace_bytes (0: the call uses no workspace)."""
+    code = LA_BF16 if dtype == torch.bfloat16 else LA_F32
+    return int(load().la_prefill_variant_workspace_bytes(B, H, N, dk, dv, code, int(mode),
+                                                         int(bool(decay))))
+
+
 def prefill_variant(q, k, v, alpha=None, mode=LA_MODE_CAUSAL, eps=1e-6, S0=None, z0=None, *,
-                    o=None, S_N=None, z_N=None):
+                    o=None, S_N=None, z_N=None, ws=None):
     """la_prefill_variant: decayed state and/or another read order; returns
-    (o, S_N, z_N).  See la_prefill_variant in la.h."""
+    (o, S_N, z_N).  See la_prefill_variant in la.h.  ws: a device uint8
+    tensor for the workspace; None uses a scratch cached per device, grown on
+    demand; False passes none (the one-block-per-head form)."""
     B, H, N, dk = q.shape
     dv = v.shape[3]
     dev = q.device
@@ -268,9 +284,22 @@ def prefill_variant(q, k, v, alpha=None, mode=LA_MODE_CAUSAL, eps=1e-6, S0=None,
     _need(o, "o", (B, H, N, dv), torch.float32, dev)
     _need(S_N, "S_N", (B, H, dk, dv), torch.float32, dev)
     _need(z_N, "z_N", (B, H, dk), torch.float32, dev)
+    if ws is None:
+        need = variant_workspace_bytes(B, H, N, dk, dv, q.dtype, mode, alpha is not None)
+        if need > 0:
+            key = dev if dev.index is not None else torch.device("cuda", torch.cuda.current_device())
+            ws = _vws_cache.get(key)
+            if ws is None or ws.numel() < need:
+                ws = torch.empty(need, dtype=torch.uint8, device=dev)
+                _vws_cache[key] = ws
+    if ws is False or ws is None:
+        ws_ptr, ws_bytes = None, 0
+    else:
+        ws_ptr, ws_bytes = _ptr(ws), ws.numel() * ws.element_size()
     st = load().la_prefill_variant(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, dk, dv,
                                    ctypes.c_float(eps), _ptr(alpha), int(mode), _ptr(S0),
-                                   _ptr(z0), _ptr(o), _ptr(S_N), _ptr(z_N), _stream(dev))
+                                   _ptr(z0), _ptr(o), _ptr(S_N), _ptr(z_N), ws_ptr, ws_bytes,
+                                   _stream(dev))
     _check("la_prefill_variant", st)
     return o, S_N, z_N
 

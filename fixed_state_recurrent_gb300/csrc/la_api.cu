@@ -186,11 +186,21 @@ la_status la_decode_step(const void* q, const void* k, const void* v, la_dtype i
                                           dv, eps, S, z, o, stream));
 }
 
+size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv, la_dtype in_dtype,
+                                          la_mode mode, int decay) {
+  if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return 0;
+  if (mode != LA_MODE_CAUSAL && mode != LA_MODE_READ_BEFORE_WRITE && mode != LA_MODE_NONCAUSAL)
+    return 0;
+  if (decay && mode == LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 64 && dv == 64 && N > 0)
+    return la::prefill_decay64_workspace_bytes(B, H, N);
+  return 0;
+}
+
 la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dtype in_dtype,
                              int B, int H, int N, int dk, int dv, float eps,
                              const float* alpha, la_mode mode,
                              const float* S0, const float* z0, float* o, float* S_N,
-                             float* z_N, cudaStream_t stream) {
+                             float* z_N, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return LA_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
   if (mode != LA_MODE_CAUSAL && mode != LA_MODE_READ_BEFORE_WRITE && mode != LA_MODE_NONCAUSAL)
@@ -198,15 +208,19 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   if (mode == LA_MODE_NONCAUSAL && alpha) return LA_ERR_INVALID_ARG;
   if (!S_N || !z_N) return LA_ERR_INVALID_ARG;
   if (N > 0 && (!q || !k || !v || !o)) return LA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, alpha, S0, z0, o, S_N, z_N};
+  const void* ptrs[] = {q, k, v, alpha, S0, z0, o, S_N, z_N, workspace};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
+  if (workspace &&
+      ws_bytes < la_prefill_variant_workspace_bytes(B, H, N, dk, dv, in_dtype, mode, alpha != nullptr))
+    return LA_ERR_INVALID_ARG;
 
   const size_t heads = (size_t)B * H;
   const size_t eb = elem_bytes(in_dtype);
   const Span sq = span(q, heads * N * dk * eb), sk = span(k, heads * N * dk * eb);
   const Span sv = span(v, heads * N * dv * eb), so = span(o, heads * N * dv * 4);
   const Span sa = span(alpha, heads * N * 4);
+  const Span sw = span(workspace, ws_bytes);
   const Span sS0 = span(S0, heads * dk * dv * 4), sz0 = span(z0, heads * dk * 4);
   const Span sSN = span(S_N, heads * dk * dv * 4), szN = span(z_N, heads * dk * 4);
   const Span outs[] = {so, sSN, szN};
@@ -214,6 +228,9 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   for (const Span& x : outs)
     for (const Span& y : ins)
       if (overlap(x, y)) return LA_ERR_INVALID_ARG;
+  const Span all[] = {sq, sk, sv, sa, so, sSN, szN, sS0, sz0};
+  for (const Span& x : all)
+    if (overlap(sw, x)) return LA_ERR_INVALID_ARG;
   if (overlap(so, sSN) || overlap(so, szN) || overlap(sSN, szN)) return LA_ERR_INVALID_ARG;
   if (overlap(so, sS0) || overlap(so, sz0) || overlap(szN, sS0) || overlap(sSN, sz0))
     return LA_ERR_INVALID_ARG;
@@ -235,8 +252,8 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   a.S0 = S0; a.z0 = z0;
   a.o = o; a.S_N = S_N; a.z_N = z_N;
   a.chunk = 0;
-  a.workspace = nullptr;
-  a.ws_bytes = 0;
+  a.workspace = workspace;
+  a.ws_bytes = workspace ? ws_bytes : 0;
   // bf16 at dk = dv = 64, write then read with a decay: tensor cores
   if (alpha && mode == LA_MODE_CAUSAL && la::prefill_decay64_supported(a))
     return from_cuda(la::launch_prefill_decay64(a, alpha, stream));

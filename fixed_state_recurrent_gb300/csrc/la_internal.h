@@ -71,7 +71,10 @@ size_t prefill_chunked64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream);
 // The decayed write-then-read form of the same products (bf16, dk = dv = 64),
 // one block per head; alpha: [B][H][N] per-token decay.  Needs no workspace.
+// With a.workspace of at least prefill_decay64_workspace_bytes the heads are
+// split over every SM (aggregate, scan, output), otherwise one block per head.
 bool prefill_decay64_supported(const PrefillArgs& a);
+size_t prefill_decay64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream);
 
 // Tensor-core chunked prefill (bf16, dk = dv in {64, 128}).

@@ -38,6 +38,7 @@ using namespace tcp;
 
 constexpr int D = 64;
 constexpr int SZ = D * D + D;                // floats per state slot (R^T rows, then z)
+constexpr float kAlphaMin = 1e-30f;          // a zero decay is taken as this (its log2 stays finite)
 constexpr uint32_t BLK = 16384;              // [128 rows x 128 B] swizzled bf16 tile
 constexpr uint32_t SNAP = 80 * 128;          // K-major [80 x 64]: S^T rows, z hi, z lo, zeros
 
@@ -109,6 +110,7 @@ struct Params3 {
   const float* alpha;  // [BH][N] per-token decay of the state, or NULL
   float* agg;  // [BH * MPH][SZ], transposed slots
   float* E;    // [BH * MPH][SZ], exclusive prefixes, transposed slots
+  float* gam;  // decayed form: [BH * MPH] the decay over each piece (product of its alphas)
   __nv_bfloat16* phik;  // [BH][N][D], phi(K) written by K1
   int force_wait;       // test hook: K3 waits once on a barrier that nothing completes
 };
@@ -225,6 +227,22 @@ __device__ __forceinline__ void drain_and_free(const Ctx3& x, int warp, uint32_t
   }
 }
 
+// Row r of a bf16 [128 x 64] swizzled tile, times f, rounded to bf16 again.
+__device__ __forceinline__ void scale_row(uint8_t* tile, int r, float f) {
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, i));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      w[j] = pack_bf16x2(__uint_as_float(w[j] << 16) * f, __uint_as_float(w[j] & 0xFFFF0000u) * f);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(tile + sw128_offset(r, i)) = v[i];
+}
+
 // ===========================================================================
 // K1: piece aggregates
 
@@ -240,14 +258,24 @@ constexpr uint32_t kCols = 128;
 
 struct Bars {
   uint64_t full[NS], xf[NS];
-  uint64_t empty[NS];  // the stage's MMA done and its phi(K) store read (2 arrivals)
+  uint64_t empty[NS];  // the stage's MMA done and (plain form) its phi(K) store read: 2 arrivals
   uint64_t racc[2];   // a piece's R complete in R[b]   (MMA -> epilogue)
   uint64_t rfree[2];  // R[b] stored                    (epilogue -> MMA)
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
+  float part[4];      // decayed form: the phi warps' partial sums of log2 alpha
 };
+static_assert(sizeof(Bars) <= 256, "barrier area");
 
+// DECAY: the piece total with each token weighted by the decay from it to the
+// piece's end, R = sum_t 2^(G_end - G_t) [v_t | 1]^T phi(k_t) (G: running sum of
+// log2 alpha over the piece), so that the scan can chain pieces as
+// E' = Gamma E + R with Gamma = 2^G_end.  The phi warps first sum log2 alpha
+// over the piece, then scale each phi(K) row by that weight (at most 1) before
+// the MMA reads it; phi(K) is not stored (the decayed output kernel applies phi
+// to K itself).
+template <bool DECAY>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
        const __grid_constant__ CUtensorMap tm_phik, const Params3 p, const unsigned long long mbar_ns) {
@@ -261,7 +289,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     for (int s = 0; s < NS; ++s) {
       mbar_init(&B->full[s], 1);
       mbar_init(&B->xf[s], 4);
-      mbar_init(&B->empty[s], 2);
+      mbar_init(&B->empty[s], DECAY ? 1 : 2);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&B->racc[b], 1);
@@ -351,27 +379,79 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
     __syncwarp();
   } else if (warp < 6) {  // ---- phi on K (one tile row per thread)
-    const int r = threadIdx.x - 64;
+    const int r = threadIdx.x - 64, w = r / 32;
     uint32_t sj = 0;
     Piece pc;
-    for (int i = 0; run.piece(p.sp, i, &pc); ++i)
+    // decayed form: the four warps' sum of v over their lanes (block-wide
+    // total of the phi warps); both named barriers run on every call
+    auto sum4 = [&](float v) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+      if (lane == 0) B->part[w] = v;
+      named_bar_sync(2, 128);
+      const float tot = (B->part[0] + B->part[1]) + (B->part[2] + B->part[3]);
+      named_bar_sync(2, 128);
+      return tot;
+    };
+    for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+      float rem = 0.f;  // decayed form: log2 of the decay from the chunk's start to the piece's end
+      if (DECAY) {
+        const float* al = p.alpha + (size_t)pc.h * p.sp.N;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        int t = pc.tok0 + r;
+        for (; t + 7 * C < pc.tok1; t += 8 * C) {  // eight loads in flight
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] += __log2f(fmaxf(__ldg(al + t + u * C), kAlphaMin));
+        }
+        for (; t < pc.tok1; t += C) acc[0] += __log2f(fmaxf(__ldg(al + t), kAlphaMin));
+        rem = sum4(((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
+        if (r == 0) p.gam[pc.slot] = exp2_ftz(rem);
+      }
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const int s = sj % NS;
-        if (!wait3_warp(x, &B->full[s], (sj / NS) & 1)) continue;
-        phi_row<8>(smem + s * STAGE, r, 0, pc.tok1 - (pc.tok0 + c * C));
+        const bool got = wait3_warp(x, &B->full[s], (sj / NS) & 1);
+        if (!DECAY && !got) continue;
+        const int valid = pc.tok1 - (pc.tok0 + c * C);
+        if (got) phi_row<8>(smem + s * STAGE, r, 0, valid);
+        if (DECAY) {
+          // g_r: inclusive sum of log2 alpha over the chunk up to row r; the
+          // row's weight is 2^(rem - g_r), the decay over the piece's later tokens
+          float la = 0.f;
+          if (got && r < valid)
+            la = __log2f(fmaxf(__ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + c * C + r), kAlphaMin));
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xFFFFFFFFu, la, off);
+            if (lane >= off) la += y;
+          }
+          if (lane == 31) B->part[w] = la;
+          named_bar_sync(2, 128);
+          float g = la, tot = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float pq = B->part[q];
+            if (q < w) g += pq;
+            tot += pq;
+          }
+          named_bar_sync(2, 128);
+          if (got) scale_row(smem + s * STAGE, r, exp2_ftz(rem - g));
+          rem -= tot;
+          if (!got) continue;
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&B->xf[s]);
       }
+    }
   } else {  // ---- epilogue: R[b] -> workspace slot (transposed rows)
     const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 192;
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
     uint32_t sj = 0;
     Piece pc;
     for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
-      if (et == 0) {  // phi(K) of the piece's chunks -> workspace; a stage is
-                      // released once the store of the chunk after it was issued
-                      // and its own store has read shared memory
+      if (!DECAY && et == 0) {  // phi(K) of the piece's chunks -> workspace; a stage is
+                                // released once the store of the chunk after it was
+                                // issued and its own store has read shared memory
         for (int c = 0; c < pc.nch; ++c, ++sj) {
           const int s = sj % NS;
           if (!wait3(x, &B->xf[s], (sj / NS) & 1)) continue;
@@ -404,7 +484,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       named_bar_sync(1, 128);
       if (et == 0) mbar_arrive(&B->rfree[b]);
     }
-    if (et == 0) {
+    if (!DECAY && et == 0) {
       bulk_wait_all();
       if (sj > 0 && !*x.abort) mbar_arrive(&B->empty[(sj - 1) % NS]);
     }
@@ -421,6 +501,8 @@ namespace k2 {
 
 constexpr int kThreads = 256;
 
+// DECAY: each piece first decays what came before it, E' = Gamma E + R.
+template <bool DECAY>
 __global__ void __launch_bounds__(kThreads) scan_kernel(const Params3 p) {
   pdl_launch_dependents();  // the output kernel may be scheduled now
   pdl_wait();               // the aggregates of the aggregate kernel are complete
@@ -440,15 +522,17 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const Params3 p) {
   const size_t base = (size_t)h * s.MPH * SZ + e;
   constexpr int U = 8;
   for (int w0 = 0; w0 < npieces; w0 += U) {
-    float a[U];
+    float a[U], gm[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u) {
       a[u] = (w0 + u < npieces) ? __ldcg(p.agg + base + (size_t)(w0 + u) * SZ) : 0.f;
+      gm[u] = (DECAY && w0 + u < npieces) ? __ldcg(p.gam + (size_t)h * s.MPH + w0 + u) : 1.f;
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (w0 + u < npieces) {
         __stcg(p.E + base + (size_t)(w0 + u) * SZ, acc);
-        acc += a[u];
+        acc = DECAY ? fmaf(gm[u], acc, a[u]) : acc + a[u];
       }
     }
   }
@@ -476,7 +560,6 @@ constexpr int GSTRIDE = C + 4;
 constexpr uint32_t SMEM = OFF_G + NS * GSTRIDE * 4 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 static_assert(OFF_OUT % 1024 == 0, "swizzled staging alignment");
-constexpr float kAlphaMin = 1e-30f;  // a zero decay is taken as this (its log2 stays finite)
 // 0 TMA, 1 MMA, 2-5 phi(Q), 6-9 P, 10-13 output epilogue (10, 12, 13 also
 // write the state snapshots), 14 state chain: at most four warps per SM
 // sub-partition, so 128 registers per thread
@@ -511,22 +594,6 @@ struct Bars {
   float4 zbuf[16];     // z, handed from its TMEM lane to the whole warp
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
-
-// Row r of a bf16 [128 x 64] swizzled tile, times f, rounded to bf16 again.
-__device__ __forceinline__ void scale_row(uint8_t* tile, int r, float f) {
-  uint4 v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, i));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t* w = reinterpret_cast<uint32_t*>(&v[i]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      w[j] = pack_bf16x2(__uint_as_float(w[j] << 16) * f, __uint_as_float(w[j] & 0xFFFF0000u) * f);
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(tile + sw128_offset(r, i)) = v[i];
-}
 
 __device__ __forceinline__ const float* gsums(uint8_t* smem, uint32_t s) {
   return reinterpret_cast<const float*>(smem + OFF_G) + s * GSTRIDE;
@@ -597,6 +664,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     tma_prefetch_desc(&tm_o);
   }
   const Run run(p.sp, blockIdx.x);
+  const bool whole = DECAY && !p.E;  // decayed form without a workspace: one block per head
   // The first stages' Q and V tiles (and K in the decayed form, which depends
   // on no other kernel) go out before the rest of the set-up; each stage's
   // barrier expects all three tiles, so phi(K) of the aggregate kernel joins
@@ -831,7 +899,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     uint8_t* snap = smem + OFF_SNAP;
     uint8_t* out = smem + OFF_OUT;
     uint32_t oj = 0, nsa = 0, sj = 0;
-    if (!DECAY) pdl_wait();  // the entry states E are the scan kernel's output
+    if (!whole) pdl_wait();  // the entry states E are the scan kernel's output
     Piece pc;
     for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
       // The piece's entry state E: into TMEM (running state) and snapshot 0.
@@ -848,7 +916,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float e[32];
-          if (DECAY) {  // S0 and z0 themselves (the whole head is the piece)
+          if (whole) {  // S0 and z0 themselves (the whole head is the piece)
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
               const int i = 32 * half + q;
@@ -973,7 +1041,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           bulk_commit();
         }
       }
-      if (DECAY && state_warp) {  // the state after the last advance: S_N, z_N
+      if (whole && state_warp) {  // the state after the last advance: S_N, z_N
         wait3(x, &B->sacc, nsa & 1);
         ++nsa;
         tc_fence_after();
@@ -1045,9 +1113,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int i = 0; ok && run.piece(p.sp, i, &pc); ++i) {
         // a piece's last chunk advances only in the decayed form (whose final
         // state comes from the running state)
-        ok = entry_stored(i) && advance(sj, DECAY || pc.nch > 1);  // chunk 0 reads E in TMEM
+        ok = entry_stored(i) && advance(sj, whole || pc.nch > 1);  // chunk 0 reads E in TMEM
         for (int c = 0; ok && c + 1 < pc.nch; ++c, ++ntr)
-          ok = wait3(x, &B->tsread, ntr & 1) && advance(sj + c + 1, DECAY || c + 2 < pc.nch);
+          ok = wait3(x, &B->tsread, ntr & 1) && advance(sj + c + 1, whole || c + 2 < pc.nch);
         sj += pc.nch;
       }
       if (*x.abort) {  // the state advances in flight end before TMEM is freed
@@ -1117,6 +1185,7 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.status = &reinterpret_cast<WsHeader*>(ws)->status;
   p.alpha = nullptr;
+  p.gam = nullptr;
   const size_t slots = (size_t)BH * p.sp.MPH;
   if (sizeof(WsHeader) + prefill_chunked64_workspace_bytes(a.B, a.H, a.N) > a.ws_bytes)
     return cudaErrorInvalidValue;
@@ -1129,13 +1198,13 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
 
-  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)k1::SMEM);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k3::output_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)k3::SMEM);
   if (e != cudaSuccess) return e;
-  k1::aggregate_kernel<<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mphik, p, mbar_ns);
+  k1::aggregate_kernel<false><<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mphik, p, mbar_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // The scan and the output kernel are launched as programmatic dependents:
@@ -1151,7 +1220,7 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
   cfg.blockDim = dim3(k2::kThreads);
   cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, k2::scan_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, k2::scan_kernel<false>, p);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k3::kWarps);
@@ -1159,13 +1228,24 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   return cudaLaunchKernelEx(&cfg, k3::output_kernel<false>, mq, mphik, mv, mo, p, mbar_ns);
 }
 
+// the decayed form's slots: agg and E, then one decay factor per piece slot
+size_t prefill_decay64_workspace_bytes(int B, int H, int N) {
+  const Split s = make_split(B * H, N, sm_count());
+  const size_t slots = (size_t)s.BH * s.MPH;
+  return (2 * slots * SZ + slots) * sizeof(float);
+}
+
 bool prefill_decay64_supported(const PrefillArgs& a) {
   return a.bf16 && a.dk == 64 && a.dv == 64 && a.N > 0 && get_encode() != nullptr;
 }
 
-// The decayed write-then-read prefill: the output kernel alone, one block per
-// head (whole heads are the pieces, the entry state is S0), phi applied to K in
-// the kernel.  Bounded-wait failures go to the library status word.
+// The decayed write-then-read prefill.  With a workspace of at least
+// prefill_decay64_workspace_bytes: the three launches of the plain form in
+// their decayed instantiations (decayed piece totals, the chain
+// E' = Gamma E + R, the outputs).  Without one: the output kernel alone, one
+// block per head (the whole head is the piece and S0 its entry state).  phi is
+// applied to K inside the output kernel either way.  Bounded-wait failures go
+// to the library status word.
 cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream) {
   const int BH = a.B * a.H;
   CUtensorMap mq, mk, mv, mo;
@@ -1174,14 +1254,23 @@ cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cud
       !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mo, a.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C))
     return cudaErrorInvalidValue;
+  const bool pieces = a.workspace && a.ws_bytes >= prefill_decay64_workspace_bytes(a.B, a.H, a.N);
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
   Params3 p = {};
-  p.sp = make_split(BH, a.N, BH);  // G = BH: block j runs head j
+  p.sp = make_split(BH, a.N, pieces ? sms : BH);  // without a workspace, block j runs head j
   p.eps = a.eps;
   p.S0 = a.S0;
   p.z0 = a.z0;
   p.S_N = a.S_N;
   p.z_N = a.z_N;
   p.alpha = alpha;
+  if (pieces) {
+    const size_t slots = (size_t)BH * p.sp.MPH;
+    p.agg = static_cast<float*>(a.workspace);
+    p.E = p.agg + slots * SZ;
+    p.gam = p.E + slots * SZ;
+  }
   cudaError_t e = library_status_word(&p.status);
   if (e != cudaSuccess) return e;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
@@ -1189,8 +1278,33 @@ cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cud
   e = cudaFuncSetAttribute(k3::output_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)k3::SMEM);
   if (e != cudaSuccess) return e;
-  k3::output_kernel<true><<<p.sp.G, 32 * k3::kWarps, k3::SMEM, stream>>>(mq, mk, mv, mo, p, mbar_ns);
-  return cudaGetLastError();
+  if (!pieces) {
+    k3::output_kernel<true><<<p.sp.G, 32 * k3::kWarps, k3::SMEM, stream>>>(mq, mk, mv, mo, p, mbar_ns);
+    return cudaGetLastError();
+  }
+  e = cudaFuncSetAttribute(k1::aggregate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)k1::SMEM);
+  if (e != cudaSuccess) return e;
+  // (the decayed aggregate kernel stores no phi(K): its third map is unused)
+  k1::aggregate_kernel<true><<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mk, p, mbar_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
+  cfg.blockDim = dim3(k2::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, k2::scan_kernel<true>, p);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * k3::kWarps);
+  cfg.dynamicSmemBytes = k3::SMEM;
+  return cudaLaunchKernelEx(&cfg, k3::output_kernel<true>, mq, mk, mv, mo, p, mbar_ns);
 }
 
 }  // namespace la

@@ -105,20 +105,34 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  *       section 线性化核心; eps = 0 gives its form exactly).
  *   alpha   [B][H][N] float32, or NULL for no decay (then LA_MODE_CAUSAL is
  *           la_prefill exactly).  Must be NULL for LA_MODE_NONCAUSAL.
- * Other arguments, layouts, aliasing and errors as la_prefill.  LA_BF16 at
- * dk = dv = 64 with a decay in LA_MODE_CAUSAL runs on the tensor cores, one
- * block per head, 128-token chunks with the decay factors inside each chunk
- * (the state enters the products as a bf16 copy of the fp32 state; a zero
- * alpha_t is taken as 1e-30); a bounded wait of that kernel that gives up is
- * reported by delta_read_device_status.  Everything else runs on the CUDA
- * cores in fp32 (one block per head), for LA_F32 and LA_BF16 inputs and any
- * dk, dv <= 128.
+ *   workspace  device scratch of at least la_prefill_variant_workspace_bytes(...)
+ *              bytes, or NULL; its contents need not be initialised.  Calls
+ *              that share a workspace must be ordered on one stream.
+ * Other arguments, layouts, aliasing and errors as la_prefill (a workspace
+ * smaller than asked for, or overlapping another argument, is
+ * LA_ERR_INVALID_ARG).  LA_BF16 at dk = dv = 64 with a decay in
+ * LA_MODE_CAUSAL runs on the tensor cores with 128-token chunks and the decay
+ * factors inside each chunk (the state enters the products as a bf16 copy of
+ * the fp32 state; a zero alpha_t is taken as 1e-30): with a workspace, the
+ * heads are split over every SM (decayed piece totals, then the chained
+ * scan E' = Gamma E + R, then the outputs); with NULL, one block per head.  A
+ * bounded wait of those kernels that gives up is reported by
+ * delta_read_device_status.  Everything else runs on the CUDA cores in fp32
+ * (one block per head, no workspace needed), for LA_F32 and LA_BF16 inputs
+ * and any dk, dv <= 128.
  */
 la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dtype in_dtype,
                              int B, int H, int N, int dk, int dv, float eps,
                              const float* alpha, la_mode mode,
                              const float* S0, const float* z0,
-                             float* o, float* S_N, float* z_N, cudaStream_t stream);
+                             float* o, float* S_N, float* z_N,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Bytes of workspace la_prefill_variant uses for these arguments (decay:
+ * nonzero when alpha is given); 0 when it uses none, or for invalid
+ * arguments.  The figure depends on the SM count of the current device. */
+size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv,
+                                          la_dtype in_dtype, la_mode mode, int decay);
 
 /*
  * la_prefill_backward -- the gradient of la_prefill's map

@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     for n in ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
               "delta_prefill", "la_state_bytes", "la_status_string",
               "la_read_device_status", "delta_read_device_status",
-              "la_prefill_variant", "gated_delta_prefill", "la_prefill_backward"):
+              "la_prefill_variant", "la_prefill_variant_workspace_bytes",
+              "gated_delta_prefill", "la_prefill_backward"):
         assert n in names
 
 
@@ -122,13 +123,13 @@ def test_decode_and_delta_reject_invalid_arguments(lib):
 def _variant(lib, **kw):
     a = dict(q=BASE, k=BASE + (1 << 30), v=BASE + (2 << 30), dt=1, B=1, H=1, N=16,
              dk=64, dv=64, eps=1e-6, alpha=BASE + (8 << 30), mode=0, S0=None, z0=None,
-             o=BASE + (3 << 30), SN=BASE + (4 << 30), zN=BASE + (5 << 30))
+             o=BASE + (3 << 30), SN=BASE + (4 << 30), zN=BASE + (5 << 30), ws=None, wsb=0)
     a.update(kw)
     p = lambda x: None if x is None else _fake(x)
     return lib.la_prefill_variant(p(a["q"]), p(a["k"]), p(a["v"]), a["dt"], a["B"], a["H"],
                                   a["N"], a["dk"], a["dv"], ctypes.c_float(a["eps"]),
                                   p(a["alpha"]), a["mode"], p(a["S0"]), p(a["z0"]), p(a["o"]),
-                                  p(a["SN"]), p(a["zN"]), None)
+                                  p(a["SN"]), p(a["zN"]), p(a["ws"]), a["wsb"], None)
 
 
 @pytest.mark.parametrize("kw", [
@@ -137,9 +138,23 @@ def _variant(lib, **kw):
     dict(alpha=BASE + (8 << 30) + 4),       # misaligned alpha
     dict(o=BASE + (8 << 30)),               # o overlaps alpha
     dict(eps=-1.0), dict(dk=129), dict(zN=None), dict(q=None),
+    dict(ws=BASE + (9 << 30), wsb=16),          # workspace smaller than asked for
+    dict(ws=BASE + (9 << 30) + 8, wsb=1 << 26),  # misaligned workspace
+    dict(ws=BASE + (3 << 30), wsb=1 << 26),      # workspace overlaps o
 ])
 def test_prefill_variant_rejects_invalid_arguments(lib, kw):
     assert _variant(lib, **kw) == 1  # LA_ERR_INVALID_ARG
+
+
+def test_prefill_variant_workspace_bytes(lib):
+    # bf16 at d = 64 with a decay, write then read: the split over the SMs needs
+    # slots; every other form needs none
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 0, 1) > 0
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 0, 0) == 0
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 0, 0, 1) == 0
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 1, 1) == 0
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 128, 128, 1, 0, 1) == 0
+    assert lib.la_prefill_variant_workspace_bytes(0, 8, 4096, 64, 64, 1, 0, 1) == 0
 
 
 def test_gated_delta_rejects_invalid_arguments(lib):

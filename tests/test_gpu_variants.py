@@ -271,3 +271,28 @@ def test_decay_prefill_tc_bounded_wait_reports_timeout(la, orc, monkeypatch):
     assert la.delta_read_device_status() == 0
     ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha.cpu()), 0)
     assert relmax(f64(o), ro) <= TOL_BF16
+
+
+@pytest.mark.parametrize("shape", [(1, 3, 700), (2, 8, 2000), (1, 5, 4096)],
+                         ids=["3x700", "16x2000", "5x4096"])
+def test_decay_prefill_tc_split_and_per_head_agree(la, orc, shape):
+    # with a workspace the heads are cut into pieces over every SM (pieces
+    # start and end inside heads, and one piece spans two heads), chained by
+    # the scan E' = Gamma E + R; without one, one block per head.  Both match
+    # the oracle, on heads that carry an entry state.
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N = shape
+    q, k, v = inputs.la_inputs(B, H, N, 64, 64, torch.bfloat16, seed=190 + N)
+    g = torch.Generator().manual_seed(191 + N)
+    alpha = 0.85 + 0.15 * torch.rand((B, H, N), generator=g)
+    S0 = torch.randn((B, H, 64, 64), generator=g) * 0.5
+    z0 = torch.rand((B, H, 64), generator=g) + 0.5
+    args = (q.cuda(), k.cuda(), v.cuda(), alpha.cuda(), 0)
+    split = la.prefill_variant(*args, S0=S0.cuda(), z0=z0.cuda())
+    whole = la.prefill_variant(*args, S0=S0.cuda(), z0=z0.cuda(), ws=False)
+    assert la.delta_read_device_status() == 0
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha), 0, S0=f64(S0), z0=f64(z0))
+    for got in (split, whole):
+        assert relmax(f64(got[0]), ro) <= TOL_BF16
+        assert relmax(f64(got[1]), rS) <= TOL_BF16
+        assert relmax(f64(got[2]), rz) <= TOL_BF16
