@@ -496,7 +496,8 @@ def bench_decay_prefill(api, rank, world, reps=12, sets=4):
 
 def bench_backward(api, rank, world, reps=5):
     """la_prefill_backward on the headline prefill shape (dO ~ N(0,1)): tensor
-    cores, one block per head, a forward and a reverse sweep."""
+    cores, a forward and a reverse sweep, the heads split over every SM (the
+    default, with a workspace); the one-block-per-head form beside it."""
     import torch
     w = inputs_mod().WORKLOADS["prefill"]
     dev = torch.device("cuda")
@@ -506,15 +507,20 @@ def bench_backward(api, rank, world, reps=5):
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     fn = lambda i: api.prefill_backward(q, k, v, dO)
+    fh = lambda i: api.prefill_backward(q, k, v, dO, ws=False)
     with torch.cuda.stream(stream):
         fn(0)
+        fh(0)
     _, per = _timed(fn, reps, stream, world)
     ms = statistics.median(per)
+    _, per = _timed(fh, reps, stream, world)
+    ms_head = statistics.median(per)
     # algorithmic bytes: q, k, v (bf16) and dO (fp32) in, dq, dk, dv (fp32) out
     b = (3 * 2 * w.dk + 4 * w.dv + 4 * (2 * w.dk + w.dv)) * w.tokens
     hbm_peak, _, kind = _peaks()
     return {"workload": "backward: B=4 H=8 N=4096 dk=dv=64 bf16 inputs, dO ~ N(0,1), "
                         "gradients of q, k, v, S0, z0", "ms_per_call": ms,
+            "ms_per_call_one_block_per_head": ms_head,
             "tokens_per_s": w.tokens / (ms * 1e-3), "hbm_gbs": b / (ms * 1e-3) / 1e9,
             "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": f"of {kind}"}
 

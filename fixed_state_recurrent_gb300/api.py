@@ -25,7 +25,7 @@ SYMBOLS = ("la_prefill", "la_prefill_workspace_bytes", "la_decode_step",
            "delta_prefill", "la_state_bytes", "la_status_string",
            "la_read_device_status", "delta_read_device_status",
            "la_prefill_variant", "la_prefill_variant_workspace_bytes", "gated_delta_prefill",
-           "la_prefill_backward")
+           "la_prefill_backward", "la_prefill_backward_workspace_bytes")
 
 
 class LAError(RuntimeError):
@@ -78,8 +78,10 @@ def load(path: str | None = None):
         lib.gated_delta_prefill.argtypes = [vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
         lib.gated_delta_prefill.restype = i
         lib.la_prefill_backward.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp, vp, vp,
-                                            vp, vp, vp, vp, vp, vp]
+                                            vp, vp, vp, vp, vp, vp, sz, vp]
         lib.la_prefill_backward.restype = i
+        lib.la_prefill_backward_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.la_prefill_backward_workspace_bytes.restype = sz
         _lib = lib
         return lib
 
@@ -252,6 +254,26 @@ def gated_delta_prefill(k, v, beta, alpha=None, S0=None, *, reads=None, S_N=None
 _vws_cache: dict = {}
 
 
+def _cached_scratch(dev, need):
+    """A device uint8 scratch of at least `need` bytes, cached per device and
+    grown on demand (shared by the optional-workspace calls; they run in
+    stream order on the current stream).  None when need is 0."""
+    if need <= 0:
+        return None
+    key = dev if dev.index is not None else torch.device("cuda", torch.cuda.current_device())
+    ws = _vws_cache.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        _vws_cache[key] = ws
+    return ws
+
+
+def _ws_args(ws):
+    if ws is False or ws is None:
+        return None, 0
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
 def variant_workspace_bytes(B, H, N, dk, dv, dtype=torch.bfloat16, mode=LA_MODE_CAUSAL,
                             decay=True) -> int:
     """la_prefill_variant_workspace_bytes (0: the call uses no workspace)."""
@@ -285,17 +307,9 @@ def prefill_variant(q, k, v, alpha=None, mode=LA_MODE_CAUSAL, eps=1e-6, S0=None,
     _need(S_N, "S_N", (B, H, dk, dv), torch.float32, dev)
     _need(z_N, "z_N", (B, H, dk), torch.float32, dev)
     if ws is None:
-        need = variant_workspace_bytes(B, H, N, dk, dv, q.dtype, mode, alpha is not None)
-        if need > 0:
-            key = dev if dev.index is not None else torch.device("cuda", torch.cuda.current_device())
-            ws = _vws_cache.get(key)
-            if ws is None or ws.numel() < need:
-                ws = torch.empty(need, dtype=torch.uint8, device=dev)
-                _vws_cache[key] = ws
-    if ws is False or ws is None:
-        ws_ptr, ws_bytes = None, 0
-    else:
-        ws_ptr, ws_bytes = _ptr(ws), ws.numel() * ws.element_size()
+        ws = _cached_scratch(dev, variant_workspace_bytes(B, H, N, dk, dv, q.dtype, mode,
+                                                          alpha is not None))
+    ws_ptr, ws_bytes = _ws_args(ws)
     st = load().la_prefill_variant(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, dk, dv,
                                    ctypes.c_float(eps), _ptr(alpha), int(mode), _ptr(S0),
                                    _ptr(z0), _ptr(o), _ptr(S_N), _ptr(z_N), ws_ptr, ws_bytes,
@@ -304,10 +318,18 @@ def prefill_variant(q, k, v, alpha=None, mode=LA_MODE_CAUSAL, eps=1e-6, S0=None,
     return o, S_N, z_N
 
 
+def backward_workspace_bytes(B, H, N, dk, dv, dtype=torch.bfloat16) -> int:
+    """la_prefill_backward_workspace_bytes (0: the call uses no workspace)."""
+    code = LA_BF16 if dtype == torch.bfloat16 else LA_F32
+    return int(load().la_prefill_backward_workspace_bytes(B, H, N, dk, dv, code))
+
+
 def prefill_backward(q, k, v, dO, eps=1e-6, S0=None, z0=None, dS_N=None, dz_N=None, *,
-                     want_state_grads=True):
+                     want_state_grads=True, ws=None):
     """la_prefill_backward: returns (dq, dk, dv, dS0, dz0) (the last two None
-    unless want_state_grads).  See la_prefill_backward in la.h."""
+    unless want_state_grads).  See la_prefill_backward in la.h.  ws as for
+    prefill_variant: None uses the cached per-device scratch, False none (one
+    block per head), else a device uint8 tensor."""
     B, H, N, dk = q.shape
     dv = v.shape[3]
     dev = q.device
@@ -324,10 +346,13 @@ def prefill_backward(q, k, v, dO, eps=1e-6, S0=None, z0=None, dS_N=None, dz_N=No
     dv_ = torch.empty((B, H, N, dv), dtype=torch.float32, device=dev)
     dS0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev) if want_state_grads else None
     dz0 = torch.empty((B, H, dk), dtype=torch.float32, device=dev) if want_state_grads else None
+    if ws is None:
+        ws = _cached_scratch(dev, backward_workspace_bytes(B, H, N, dk, dv, q.dtype))
+    ws_ptr, ws_bytes = _ws_args(ws)
     st = load().la_prefill_backward(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, dk, dv,
                                     ctypes.c_float(eps), _ptr(S0), _ptr(z0), _ptr(dO),
                                     _ptr(dS_N), _ptr(dz_N), _ptr(dq), _ptr(dk_), _ptr(dv_),
-                                    _ptr(dS0), _ptr(dz0), _stream(dev))
+                                    _ptr(dS0), _ptr(dz0), ws_ptr, ws_bytes, _stream(dev))
     _check("la_prefill_backward", st)
     return dq, dk_, dv_, dS0, dz0
 

@@ -59,7 +59,7 @@ constexpr uint32_t kCols = 512;
 // its mask), dV, G (running gradient state, lanes j).
 // Every N = 128 accumulator starts at a multiple of 128 columns, the others at
 // multiples of 64.
-constexpr uint32_t T_A = 0, T_O = 128, T_DW = 256, T_S = 384;
+constexpr uint32_t T_A = 0, T_O = 128, T_DW = 256, T_S = 384, T_DG = 448;
 constexpr uint32_t T_A2 = 0, T_A3 = 128, T_DU = 256, T_DV = 320, T_G = 384;
 
 constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);   // K-major x K-major, N = 128
@@ -69,8 +69,11 @@ constexpr uint32_t ID_N64_MN = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B M
 constexpr uint32_t ID_N64_K = idesc_bf16_f32(128, 64, 0, 0);   // both K-major, N = 64
 constexpr uint32_t ID_ADV = idesc_bf16_f32(128, 64, 1, 1);     // both MN-major (state advances)
 
+constexpr int SZ = D * D + D;  // floats of a state slot: rows j = column j of the state, row 64 = z
+
 struct Params {
-  int BH, N, NC;
+  Split sp;  // pieces: whole heads (one block per head), or the split over the SMs
+  int N;
   float eps;
   const float* S0;
   const float* z0;
@@ -83,6 +86,11 @@ struct Params {
   float* dz0;
   unsigned* status;
   int force_wait;
+  // split form: per piece slot, the entry state (from the prefill's scan), the
+  // piece's gradient-state increment W^T D, and the gradient state after it
+  const float* E;
+  float* dG;
+  const float* Gaft;
 };
 
 struct Bars {
@@ -203,6 +211,11 @@ __device__ __forceinline__ void mask_pack(uint32_t base, int quad, int lane) {
   tmem_st_wait();
 }
 
+// MODE 0: one block per head, both sweeps (no workspace).  MODE 1: the
+// forward sweep of every piece of the block's run, from the piece's entry
+// state, also summing the piece's W^T D into dG.  MODE 2: the reverse sweep
+// of every piece, from the gradient state after the piece.
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -214,8 +227,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
-  const int h = blockIdx.x;
-  const int NC = p.NC;
+  if (MODE != 0) pdl_launch_dependents();  // the next launch may be scheduled now
   uint8_t* dt = smem + OFF_DT;
   uint8_t* snap = smem + OFF_SNAP;
   if (t == 0) {
@@ -249,10 +261,12 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t tl = tm + ((uint32_t)(32 * warp) << 16);  // this thread's TMEM lane (t)
   const Ctx x{&p, B, mbar_ns};
   const uint32_t aOnes = smem_u32(smem + OFF_ONES), aSnap = smem_u32(snap), aDt = smem_u32(dt);
-  uint32_t nload = 0, nmma = 0;  // loads issued so far (stage nload % 2), MMA groups waited
+  // loads issued (thread 0) and loads consumed (every thread), in the same
+  // order: load i goes to stage i % 2; MMA groups waited
+  uint32_t nload = 0, nuse = 0, nmma = 0;
 
-  // thread 0: the loads of chunk c into stage `nload % 2`
-  auto load = [&](int c, bool forward) {
+  // thread 0: the loads of chunk c (of head h) into stage `nload % 2`
+  auto load = [&](int h, int c, bool forward) {
     const int s = nload % 2;
     uint8_t* st = smem + s * STAGE;
     const int tok = c * C;
@@ -287,15 +301,24 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
   };
 
-  // =================== forward sweep ===================
-  // S0, z0 -> the running state (lane j: column j of S, lane 64: z) and its
-  // snapshot (row j; rows 64, 65: z in two bf16 parts)
+  // =================== forward sweep of one piece ===================
+  auto fwd_piece = [&](const Piece& pc) {
+  const int h = pc.h, c0 = pc.tok0 / C, NC = pc.nch;
+  // the entry state (S0, z0 for a whole head; the scan's E otherwise) -> the
+  // running state (lane j: column j of S, lane 64: z) and its snapshot (row j;
+  // rows 64, 65: z in two bf16 parts)
   {
     float e[64];
+    if (MODE == 0) {
 #pragma unroll
-    for (int i = 0; i < 64; ++i)
-      e[i] = t < D ? (p.S0 ? __ldg(p.S0 + ((size_t)h * D + i) * D + t) : 0.f)
-                   : (t == D && p.z0 ? __ldg(p.z0 + (size_t)h * D + i) : 0.f);
+      for (int i = 0; i < 64; ++i)
+        e[i] = t < D ? (p.S0 ? __ldg(p.S0 + ((size_t)h * D + i) * D + t) : 0.f)
+                     : (t == D && p.z0 ? __ldg(p.z0 + (size_t)h * D + i) : 0.f);
+    } else {
+      const float* src = p.E + (size_t)pc.slot * SZ + (t <= D ? t : 0) * D;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) e[i] = t <= D ? __ldcg(src + i) : 0.f;
+    }
     tmem_put64(tl + T_S, e);
     tmem_st_wait();
     if (t < D) {
@@ -308,16 +331,17 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       store_row_bf16(snap, D + 1, lo);
     }
   }
-  if (t == 0 && NC > 0) load(0, true);
+  if (t == 0) load(h, c0, true);
   step_done();
 
-  for (int c = 0; c < NC; ++c) {
-    const int s = c % 2;
+  for (int c = 0; c < NC; ++c, ++nuse) {
+    const int s = nuse % 2;
     uint8_t* st = smem + s * STAGE;
     const uint32_t aq = smem_u32(st), ak = aq + BLK, av = aq + 2 * BLK;
-    const int valid = min(C, p.N - c * C);
-    if (t == 0 && c + 1 < NC) load(c + 1, true);
-    waitb(x, &B->full[s], (c / 2) & 1);
+    const int tok = (c0 + c) * C;
+    const int valid = min(C, p.N - tok);
+    if (t == 0 && c + 1 < NC) load(h, c0 + c + 1, true);
+    waitb(x, &B->full[s], (nuse / 2) & 1);
     phi_row<8>(st, t, 0, valid);
     phi_row<8>(st + BLK, t, 0, valid);
     step_done();
@@ -374,7 +398,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // parked in dv's row (256 bytes): 64 bf16 dnum, then dden twice and zeros,
       // the row-major form the reverse sweep's tile loads read back
       if (t < valid) {
-        uint4* row = reinterpret_cast<uint4*>(p.dv + ((size_t)h * p.N + c * C + t) * D);
+        uint4* row = reinterpret_cast<uint4*>(p.dv + ((size_t)h * p.N + tok + t) * D);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           row[q] = make_uint4(pack_bf16x2(num[8 * q], num[8 * q + 1]), pack_bf16x2(num[8 * q + 2], num[8 * q + 3]),
@@ -415,6 +439,12 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int ks = 0; ks < C / 16; ++ks)
         mma_bf16_ss(tm + T_S, sdesc_sw128(av + ks * 2048, aOnes - av, 1024),
                     sdesc_sw128(ak + ks * 2048, BLK, 1024), ID_ADV, 1u);
+      if (MODE == 1) {  // the piece's gradient-state increment W^T D (lanes j)
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks)
+          mma_bf16_ss(tm + T_DG, sdesc_sw128(aDt + ks * 2048, BLK, 1024), sdesc_sw128(aq + ks * 2048, BLK, 1024),
+                      ID_ADV, (c > 0 || ks > 0) ? 1u : 0u);
+      }
     }
     if (t == 0) mma_commit(&B->mma);
     mma_done();
@@ -423,7 +453,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_row64(tl + T_DW, g);
       load_row_bf16(st, t, f);
       if (t < valid && !*reinterpret_cast<volatile int*>(&B->abort)) {
-        float4* dst = reinterpret_cast<float4*>(p.dq + ((size_t)h * p.N + c * C + t) * D);
+        float4* dst = reinterpret_cast<float4*>(p.dq + ((size_t)h * p.N + tok + t) * D);
 #pragma unroll
         for (int q = 0; q < 16; ++q)
           dst[q] = make_float4(g[4 * q] * fminf(f[4 * q], 1.f), g[4 * q + 1] * fminf(f[4 * q + 1], 1.f),
@@ -443,19 +473,36 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     step_done();
   }
-  // every thread's parked rows are written before the tile loads read them
-  __threadfence();
-  fence_proxy_async_global();
+  if (MODE == 1 && warp <= 2) {  // whole warps: tcgen05.ld is warp-collective
+    float e[64];
+    tmem_row64(tl + T_DG, e);
+    if (t <= D && !*reinterpret_cast<volatile int*>(&B->abort)) {
+      float4* dst = reinterpret_cast<float4*>(p.dG + (size_t)pc.slot * SZ + t * D);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) __stcg(dst + q, make_float4(e[4 * q], e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]));
+    }
+  }
+  step_done();
+  };
 
-  // =================== reverse sweep ===================
-  // G = dS_N, g = dz_N -> the running gradient state (lane j: column j of G,
-  // lane 64: g) and its snapshot (row j; row 64: g; row 65 stays 0)
+  // =================== reverse sweep of one piece ===================
+  auto rev_piece = [&](const Piece& pc) {
+  const int h = pc.h, c0 = pc.tok0 / C, NC = pc.nch;
+  // the gradient state after the piece (dS_N, dz_N for a whole head; the
+  // reverse scan's otherwise) -> the running gradient state (lane j: column j
+  // of G, lane 64: g) and its snapshot (row j; row 64: g; row 65 stays 0)
   {
     float e[64];
+    if (MODE == 0) {
 #pragma unroll
-    for (int i = 0; i < 64; ++i)
-      e[i] = t < D ? (p.dS_N ? __ldg(p.dS_N + ((size_t)h * D + i) * D + t) : 0.f)
-                   : (t == D && p.dz_N ? __ldg(p.dz_N + (size_t)h * D + i) : 0.f);
+      for (int i = 0; i < 64; ++i)
+        e[i] = t < D ? (p.dS_N ? __ldg(p.dS_N + ((size_t)h * D + i) * D + t) : 0.f)
+                     : (t == D && p.dz_N ? __ldg(p.dz_N + (size_t)h * D + i) : 0.f);
+    } else {
+      const float* src = p.Gaft + (size_t)pc.slot * SZ + (t <= D ? t : 0) * D;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) e[i] = t <= D ? __ldcg(src + i) : 0.f;
+    }
     tmem_put64(tl + T_G, e);
     tmem_st_wait();
     if (t <= D) store_row_bf16(snap, t, e);
@@ -466,17 +513,17 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   }
   step_done();  // (also: every thread's parked rows are fenced before the first tile load)
-  if (t == 0 && NC > 0) load(NC - 1, false);
+  if (t == 0) load(h, c0 + NC - 1, false);
 
-  for (int r = 0; r < NC; ++r) {
+  for (int r = 0; r < NC; ++r, ++nuse) {
     const int c = NC - 1 - r;
-    const uint32_t li = (uint32_t)NC + r;  // this chunk's load
-    const int s = li % 2;
+    const int s = nuse % 2;
     uint8_t* st = smem + s * STAGE;
     const uint32_t aq = smem_u32(st), ak = aq + BLK, av = aq + 2 * BLK, ax = aq + 3 * BLK;
-    const int valid = min(C, p.N - c * C);
-    if (t == 0 && c > 0) load(c - 1, false);
-    waitb(x, &B->full[s], (li / 2) & 1);
+    const int tok = (c0 + c) * C;
+    const int valid = min(C, p.N - tok);
+    if (t == 0 && c > 0) load(h, c0 + c - 1, false);
+    waitb(x, &B->full[s], (nuse / 2) & 1);
     phi_row<8>(st, t, 0, valid);
     phi_row<8>(st + BLK, t, 0, valid);
     step_done();
@@ -531,7 +578,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       load_row_bf16(st + BLK, t, f);
       const bool out = t < valid && !*reinterpret_cast<volatile int*>(&B->abort);
       if (out) {
-        float4* dst = reinterpret_cast<float4*>(p.dk + ((size_t)h * p.N + c * C + t) * D);
+        float4* dst = reinterpret_cast<float4*>(p.dk + ((size_t)h * p.N + tok + t) * D);
 #pragma unroll
         for (int q = 0; q < 16; ++q)
           dst[q] = make_float4(g[4 * q] * fminf(f[4 * q], 1.f), g[4 * q + 1] * fminf(f[4 * q + 1], 1.f),
@@ -539,7 +586,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       tmem_row64(tl + T_DV, g);
       if (out) {
-        float4* dst = reinterpret_cast<float4*>(p.dv + ((size_t)h * p.N + c * C + t) * D);
+        float4* dst = reinterpret_cast<float4*>(p.dv + ((size_t)h * p.N + tok + t) * D);
 #pragma unroll
         for (int q = 0; q < 16; ++q) dst[q] = make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
       }
@@ -547,7 +594,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         float e[64];
         tmem_row64(tl + T_G, e);
         if (c > 0 && t <= D) store_row_bf16(snap, t, e);
-        if (c == 0 && t <= D && !*reinterpret_cast<volatile int*>(&B->abort)) {  // dS0, dz0
+        if (MODE == 0 && c == 0 && t <= D && !*reinterpret_cast<volatile int*>(&B->abort)) {  // dS0, dz0
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             if (t < D) {
@@ -560,6 +607,25 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     }
     step_done();
+  }
+  };
+
+  const Run run(p.sp, blockIdx.x);
+  Piece pc;
+  if (MODE == 0) {  // the block's head: forward sweep, then reverse sweep
+    if (run.piece(p.sp, 0, &pc)) {
+      fwd_piece(pc);
+      // every thread's parked rows are written before the tile loads read them
+      __threadfence();
+      fence_proxy_async_global();
+      rev_piece(pc);
+    }
+  } else {
+    pdl_wait();  // the entry (gradient) states come from the launches before
+    for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+      if (MODE == 1) fwd_piece(pc);
+      else rev_piece(pc);
+    }
   }
 
   if (t == 0 && *reinterpret_cast<volatile int*>(&B->abort)) {  // MMAs in flight end first
@@ -575,11 +641,62 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
+// The gradient state after every piece of a head, from the last piece back:
+// G_after(last) = dS_N (z: dz_N), G_after(p) = G_after(p + 1) + dG(p + 1); what
+// remains after the first piece is dS0, dz0.  One thread per slot element.
+constexpr int kScanThreads = 256;
+
+__global__ void __launch_bounds__(kScanThreads) gscan_kernel(const Params p, float* Gaft) {
+  pdl_launch_dependents();  // the reverse sweep may be scheduled now
+  pdl_wait();               // dG of every piece is complete
+  const int e = blockIdx.x * kScanThreads + threadIdx.x;  // slot element: row * 64 + i
+  const int h = blockIdx.y;
+  if (e >= SZ) return;
+  const Split& s = p.sp;
+  const int row = e / D, i = e % D;  // row < 64: G[i][row]; row 64: g[i]
+  float acc = 0.f;
+  if (row < D) {
+    if (p.dS_N) acc = p.dS_N[((size_t)h * D + i) * D + row];
+  } else if (p.dz_N) {
+    acc = p.dz_N[(size_t)h * D + i];
+  }
+  const int first = s.owner((long long)h * s.NC);
+  const int npieces = s.owner((long long)(h + 1) * s.NC - 1) - first + 1;
+  const size_t base = (size_t)h * s.MPH * SZ + e;
+  constexpr int U = 8;
+  for (int w1 = npieces; w1 > 0; w1 -= U) {  // pieces w1 - 1, w1 - 2, ... (eight at a time)
+    float a[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) a[u] = (w1 - 1 - u >= 0) ? __ldcg(p.dG + base + (size_t)(w1 - 1 - u) * SZ) : 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (w1 - 1 - u >= 0) {
+        __stcg(Gaft + base + (size_t)(w1 - 1 - u) * SZ, acc);
+        acc += a[u];
+      }
+    }
+  }
+  if (row < D) {
+    if (p.dS0) p.dS0[((size_t)h * D + i) * D + row] = acc;
+  } else if (p.dz0) {
+    p.dz0[(size_t)h * D + i] = acc;
+  }
+}
+
 }  // namespace bw
 }  // namespace
 
 bool backward_tc64_supported(const PrefillArgs& a) {
   return a.bf16 && a.dk == 64 && a.dv == 64 && a.N > 0 && get_encode() != nullptr;
+}
+
+// The split form's workspace: agg, E, dG and G-after slots, S_N and z_N
+// scratch for the prefill's scan, phi(K) scratch for its aggregate kernel.
+size_t backward_tc64_workspace_bytes(int B, int H, int N) {
+  using namespace bw;
+  const Split s = make_split(B * H, N, sm_count());
+  const size_t slots = (size_t)s.BH * s.MPH;
+  return (4 * slots + s.BH) * SZ * sizeof(float) + (size_t)s.BH * N * D * sizeof(__nv_bfloat16);
 }
 
 cudaError_t launch_backward_tc64(const PrefillArgs& a, const float* dO, const float* dS_N,
@@ -595,10 +712,12 @@ cudaError_t launch_backward_tc64(const PrefillArgs& a, const float* dO, const fl
       // dv's rows seen as 128 bf16 each: two [128 x 64] blocks of D per chunk
       !make_map(&mpark, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2 * D, a.N, BH, 64, C))
     return cudaErrorInvalidValue;
-  Params p;
-  p.BH = BH;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const bool split = a.workspace && a.ws_bytes >= backward_tc64_workspace_bytes(a.B, a.H, a.N);
+  Params p = {};
+  p.sp = make_split(BH, a.N, split ? sms : BH);  // without a workspace, block j runs head j
   p.N = a.N;
-  p.NC = (a.N + C - 1) / C;
   p.eps = a.eps;
   p.S0 = a.S0;
   p.z0 = a.z0;
@@ -613,10 +732,52 @@ cudaError_t launch_backward_tc64(const PrefillArgs& a, const float* dO, const fl
   if (e != cudaSuccess) return e;
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
-  e = cudaFuncSetAttribute(backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  if (!split) {
+    e = cudaFuncSetAttribute(backward_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+    if (e != cudaSuccess) return e;
+    backward_kernel<0><<<p.sp.G, kThreads, SMEM, stream>>>(mq, mk, mv, mdo, mpark, p, mbar_ns);
+    return cudaGetLastError();
+  }
+  const size_t slots = (size_t)BH * p.sp.MPH;
+  float* agg = static_cast<float*>(a.workspace);
+  float* E = agg + slots * SZ;
+  float* dG = E + slots * SZ;
+  float* Gaft = dG + slots * SZ;
+  float* SNz = Gaft + slots * SZ;  // S_N (BH x 64 x 64), then z_N (BH x 64)
+  __nv_bfloat16* phik = reinterpret_cast<__nv_bfloat16*>(SNz + (size_t)BH * SZ);
+  p.E = E;
+  p.dG = dG;
+  p.Gaft = Gaft;
+  // the prefill's aggregate and scan: every piece's entry state
+  e = launch_prefill_entry_states64(a, agg, E, phik, SNz, SNz + (size_t)BH * D * D, p.status, stream);
   if (e != cudaSuccess) return e;
-  backward_kernel<<<BH, kThreads, SMEM, stream>>>(mq, mk, mv, mdo, mpark, p, mbar_ns);
-  return cudaGetLastError();
+  e = cudaFuncSetAttribute(backward_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(backward_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+  if (e != cudaSuccess) return e;
+  // forward sweeps, the reverse scan of the gradient state, reverse sweeps:
+  // programmatic dependents, each waiting for the launch before it
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SMEM;
+  e = cudaLaunchKernelEx(&cfg, backward_kernel<1>, mq, mk, mv, mdo, mpark, p, mbar_ns);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((SZ + kScanThreads - 1) / kScanThreads, BH);
+  cfg.blockDim = dim3(kScanThreads);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, gscan_kernel, p, Gaft);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SMEM;
+  return cudaLaunchKernelEx(&cfg, backward_kernel<2>, mq, mk, mv, mdo, mpark, p, mbar_ns);
 }
 
 }  // namespace la

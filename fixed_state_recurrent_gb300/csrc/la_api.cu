@@ -260,17 +260,27 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   return from_cuda(la::launch_prefill_variant_simt(a, alpha, (int)mode, stream));
 }
 
+size_t la_prefill_backward_workspace_bytes(int B, int H, int N, int dk, int dv, la_dtype in_dtype) {
+  if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return 0;
+  if (in_dtype == LA_BF16 && dk == 64 && dv == 64 && N > 0)
+    return la::backward_tc64_workspace_bytes(B, H, N);
+  return 0;
+}
+
 la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dtype in_dtype,
                               int B, int H, int N, int dk, int dv, float eps,
                               const float* S0, const float* z0, const float* dO,
                               const float* dS_N, const float* dz_N, float* dq, float* dk_out,
-                              float* dv_out, float* dS0, float* dz0, cudaStream_t stream) {
+                              float* dv_out, float* dS0, float* dz0, void* workspace,
+                              size_t ws_bytes, cudaStream_t stream) {
   if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return LA_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
   if (N > 0 && (!q || !k || !v || !dO || !dq || !dk_out || !dv_out)) return LA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, S0, z0, dO, dS_N, dz_N, dq, dk_out, dv_out, dS0, dz0};
+  const void* ptrs[] = {q, k, v, S0, z0, dO, dS_N, dz_N, dq, dk_out, dv_out, dS0, dz0, workspace};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return LA_ERR_INVALID_ARG;
+  if (workspace && ws_bytes < la_prefill_backward_workspace_bytes(B, H, N, dk, dv, in_dtype))
+    return LA_ERR_INVALID_ARG;
   const size_t heads = (size_t)B * H;
   const size_t eb = elem_bytes(in_dtype);
   const Span ins[] = {span(q, heads * N * dk * eb), span(k, heads * N * dk * eb),
@@ -286,6 +296,11 @@ la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dt
     for (const Span& y : outs)
       if (&x != &y && overlap(x, y)) return LA_ERR_INVALID_ARG;
   }
+  const Span sw = span(workspace, ws_bytes);
+  for (const Span& x : ins)
+    if (overlap(sw, x)) return LA_ERR_INVALID_ARG;
+  for (const Span& x : outs)
+    if (overlap(sw, x)) return LA_ERR_INVALID_ARG;
   const la_status dev = check_device();
   if (dev != LA_OK) return dev;
   if (N == 0) {
@@ -302,8 +317,8 @@ la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dt
   a.S0 = S0; a.z0 = z0;
   a.o = nullptr; a.S_N = nullptr; a.z_N = nullptr;
   a.chunk = 0;
-  a.workspace = nullptr;
-  a.ws_bytes = 0;
+  a.workspace = workspace;
+  a.ws_bytes = workspace ? ws_bytes : 0;
   if (la::backward_tc64_supported(a))
     return from_cuda(la::launch_backward_tc64(a, dO, dS_N, dz_N, dq, dk_out, dv_out, dS0, dz0, stream));
   return from_cuda(la::launch_prefill_backward(a, dO, dS_N, dz_N, dq, dk_out, dv_out, dS0, dz0,

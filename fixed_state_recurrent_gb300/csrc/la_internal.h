@@ -55,11 +55,15 @@ cudaError_t launch_prefill_backward(const PrefillArgs& p, const float* dO, const
                                     const float* dz_N, float* dq, float* dk, float* dv,
                                     float* dS0, float* dz0, cudaStream_t stream);
 // The same gradient on the tensor cores for bf16 inputs at dk = dv = 64
-// (backward_tc64.cu): one block per head, a forward and a reverse sweep over
-// 128-token chunks.  Needs no workspace (it parks bf16 data in dv until the
-// reverse sweep overwrites it); bounded-wait failures go to the library status
-// word.
+// (backward_tc64.cu): a forward and a reverse sweep over 128-token chunks (it
+// parks bf16 data in dv until the reverse sweep overwrites it); bounded-wait
+// failures go to the library status word.
+// With a.workspace of at least backward_tc64_workspace_bytes the pieces of the
+// d = 64 split run over every SM (the prefill's aggregate and scan for the
+// entry states, forward sweeps, a reverse scan of the gradient state, reverse
+// sweeps); without one, one block per head.
 bool backward_tc64_supported(const PrefillArgs& a);
+size_t backward_tc64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_backward_tc64(const PrefillArgs& a, const float* dO, const float* dS_N,
                                  const float* dz_N, float* dq, float* dk, float* dv, float* dS0,
                                  float* dz0, cudaStream_t stream);
@@ -74,6 +78,13 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream);
 // With a.workspace of at least prefill_decay64_workspace_bytes the heads are
 // split over every SM (aggregate, scan, output), otherwise one block per head.
 bool prefill_decay64_supported(const PrefillArgs& a);
+// The entry state of every piece of the d = 64 split (the split of
+// prefill_tc_common.cuh's make_split over the current device's SMs) into E,
+// slot layout [BH * MPH][64 * 64 + 64]; agg (the same size), phik (BH * N * 64
+// bf16), S_N and z_N (B * H states) are scratch.
+cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, float* E,
+                                          __nv_bfloat16* phik, float* S_N, float* z_N,
+                                          unsigned* status, cudaStream_t stream);
 size_t prefill_decay64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream);
 

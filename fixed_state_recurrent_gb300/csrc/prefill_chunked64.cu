@@ -47,58 +47,6 @@ constexpr uint32_t ID_PV = idesc_bf16_f32(128, D + 16, 0, 1); // P [V | 1]
 constexpr uint32_t ID_QS = idesc_bf16_f32(128, D + 16, 0, 0); // phi(Q) [S | z]
 constexpr uint32_t ID_DS = idesc_bf16_f32(128, D, 1, 1);      // [V | 1]^T phi(K)
 
-// ---------------------------------------------------------------------------
-// work split (identical in the three kernels and on the host)
-
-struct Split {
-  int BH, N, NC;  // heads, tokens per head, chunks per head
-  int G;          // blocks of K1 and K3
-  int MPH;        // piece slots per head
-  __host__ __device__ long long TC() const { return (long long)BH * NC; }
-  __host__ __device__ long long start(int j) const { return (long long)j * TC() / G; }
-  // the block whose run contains global chunk x
-  __host__ __device__ int owner(long long x) const {
-    return (int)(((x + 1) * G - 1) / TC());
-  }
-};
-
-struct Piece {
-  int h, slot;
-  int tok0, tok1, nch;
-};
-
-// Block j's run of chunks [a, b) and the pieces it is cut into.  The 64-bit
-// divisions happen once, here; walking the pieces needs none.
-struct Run {
-  long long a, b;
-  int h0;    // head of the first piece
-  int idx0;  // position of block j among the blocks that meet head h0
-  __host__ __device__ Run(const Split& s, int j) {
-    a = s.start(j);
-    b = s.start(j + 1);
-    h0 = (int)(a / s.NC);
-    idx0 = j - s.owner((long long)h0 * s.NC);
-  }
-  // The i-th piece (pieces are ordered by position); false when there are
-  // fewer.  Every piece after the first starts its head, so its slot index
-  // within the head is 0.
-  __host__ __device__ bool piece(const Split& s, int i, Piece* pc) const {
-    if (a >= b) return false;
-    const int h = h0 + i;
-    const long long hs = (long long)h * s.NC;
-    if (hs >= b || h >= s.BH) return false;
-    const long long c0 = a > hs ? a : hs;
-    const long long c1 = b < hs + s.NC ? b : hs + s.NC;
-    pc->h = h;
-    pc->slot = h * s.MPH + (i == 0 ? idx0 : 0);
-    pc->tok0 = (int)(c0 - hs) * C;
-    pc->tok1 = (int)(c1 - hs) * C;
-    if (pc->tok1 > s.N) pc->tok1 = s.N;
-    pc->nch = (int)(c1 - c0);
-    return true;
-  }
-};
-
 struct Params3 {
   Split sp;
   float eps;
@@ -1131,32 +1079,6 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
 }  // namespace k3
 
-Split make_split(int BH, int N, int sms) {
-  Split s;
-  s.BH = BH;
-  s.N = N;
-  s.NC = (N + C - 1) / C;
-  const long long tc = (long long)BH * s.NC;
-  s.G = (int)(tc < sms ? tc : sms);
-  // Runs are L = floor(TC / G) or L + 1 chunks long; a head's NC chunks meet at
-  // most ceil(NC / L) + 1 of them (every run but the first and last lies inside).
-  const long long L = tc / s.G;
-  s.MPH = (int)((s.NC + L - 1) / L) + 1;
-  return s;
-}
-
-// SMs of the current device (152 on a GB300 when no device is visible, so
-// that host-only queries of the workspace size still answer).
-int sm_count() {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
-    cudaGetLastError();
-    return 152;
-  }
-  return sms;
-}
-
 }  // namespace
 
 // agg and E slots, then phi(K)
@@ -1233,6 +1155,52 @@ size_t prefill_decay64_workspace_bytes(int B, int H, int N) {
   const Split s = make_split(B * H, N, sm_count());
   const size_t slots = (size_t)s.BH * s.MPH;
   return (2 * slots * SZ + slots) * sizeof(float);
+}
+
+// The entry state of every piece of the d = 64 split, for other kernels that
+// walk the same pieces (the gradient): the aggregate and scan launches of the
+// plain form into agg and E (slot layout), with phik, S_N and z_N as scratch
+// the two kernels fill; bounded-wait failures go to `status`.  The scan is a
+// programmatic dependent, and so may be the launch that follows.
+cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, float* E,
+                                          __nv_bfloat16* phik, float* S_N, float* z_N,
+                                          unsigned* status, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  CUtensorMap mk, mv, mphik;
+  if (!make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mphik, phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C))
+    return cudaErrorInvalidValue;
+  Params3 p = {};
+  p.sp = make_split(BH, a.N, sms);
+  p.S0 = a.S0;
+  p.z0 = a.z0;
+  p.S_N = S_N;
+  p.z_N = z_N;
+  p.status = status;
+  p.agg = agg;
+  p.E = E;
+  p.phik = phik;
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k1::SMEM);
+  if (e != cudaSuccess) return e;
+  k1::aggregate_kernel<false><<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mphik, p, mbar_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
+  cfg.blockDim = dim3(k2::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, k2::scan_kernel<false>, p);
 }
 
 bool prefill_decay64_supported(const PrefillArgs& a) {

@@ -119,6 +119,84 @@ __device__ __forceinline__ void init_ones(uint8_t* ones, int tid, int nthreads) 
   if (tid < C) *reinterpret_cast<uint16_t*>(ones + tc::sw128_offset(tid, 0)) = 0x3F80u;  // bf16 1.0
 }
 
+// ---------------------------------------------------------------------------
+// work split (the kernels and the host share it)
+
+struct Split {
+  int BH, N, NC;  // heads, tokens per head, chunks per head
+  int G;          // blocks of K1 and K3
+  int MPH;        // piece slots per head
+  __host__ __device__ long long TC() const { return (long long)BH * NC; }
+  __host__ __device__ long long start(int j) const { return (long long)j * TC() / G; }
+  // the block whose run contains global chunk x
+  __host__ __device__ int owner(long long x) const {
+    return (int)(((x + 1) * G - 1) / TC());
+  }
+};
+
+struct Piece {
+  int h, slot;
+  int tok0, tok1, nch;
+};
+
+// Block j's run of chunks [a, b) and the pieces it is cut into.  The 64-bit
+// divisions happen once, here; walking the pieces needs none.
+struct Run {
+  long long a, b;
+  int h0;    // head of the first piece
+  int idx0;  // position of block j among the blocks that meet head h0
+  __host__ __device__ Run(const Split& s, int j) {
+    a = s.start(j);
+    b = s.start(j + 1);
+    h0 = (int)(a / s.NC);
+    idx0 = j - s.owner((long long)h0 * s.NC);
+  }
+  // The i-th piece (pieces are ordered by position); false when there are
+  // fewer.  Every piece after the first starts its head, so its slot index
+  // within the head is 0.
+  __host__ __device__ bool piece(const Split& s, int i, Piece* pc) const {
+    if (a >= b) return false;
+    const int h = h0 + i;
+    const long long hs = (long long)h * s.NC;
+    if (hs >= b || h >= s.BH) return false;
+    const long long c0 = a > hs ? a : hs;
+    const long long c1 = b < hs + s.NC ? b : hs + s.NC;
+    pc->h = h;
+    pc->slot = h * s.MPH + (i == 0 ? idx0 : 0);
+    pc->tok0 = (int)(c0 - hs) * C;
+    pc->tok1 = (int)(c1 - hs) * C;
+    if (pc->tok1 > s.N) pc->tok1 = s.N;
+    pc->nch = (int)(c1 - c0);
+    return true;
+  }
+};
+
+inline Split make_split(int BH, int N, int sms) {
+  Split s;
+  s.BH = BH;
+  s.N = N;
+  s.NC = (N + C - 1) / C;
+  const long long tc = (long long)BH * s.NC;
+  s.G = (int)(tc < sms ? tc : sms);
+  // Runs are L = floor(TC / G) or L + 1 chunks long; a head's NC chunks meet at
+  // most ceil(NC / L) + 1 of them (every run but the first and last lies inside).
+  const long long L = tc / s.G;
+  s.MPH = (int)((s.NC + L - 1) / L) + 1;
+  return s;
+}
+
+// SMs of the current device (152 on a GB300 when no device is visible, so
+// that host-only queries of the workspace size still answer).
+inline int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return sms;
+}
+
 // Flag word of an item: (generation << 2) | state.
 constexpr unsigned kFlagAggregate = 1u;  // agg[g] is published
 constexpr unsigned kFlagInclusive = 2u;  // inc[g] is published

@@ -150,20 +150,31 @@ size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv,
  *   dq, dk_out [B][H][N][dk], dv_out [B][H][N][dv]: float32 outputs (the
  *               gradients with respect to q, k and v)
  *   dS0 [B][H][dk][dv], dz0 [B][H][dk]: float32 outputs, or NULL if not wanted
- * Outputs must not overlap any input or each other.  LA_BF16 at dk = dv = 64
- * runs on the tensor cores: one block per head, a forward and a reverse sweep
- * over 128-token chunks (bf16 operands, fp32 accumulation; dv_out holds bf16
- * intermediate rows between the sweeps); a bounded wait of that kernel that
- * gives up is reported by delta_read_device_status.  Everything else runs on
- * the CUDA cores in fp32, one block per head, token by token; any dk, dv <= 128.
- * Neither takes a workspace.
+ *   workspace  device scratch of at least la_prefill_backward_workspace_bytes(...)
+ *              bytes, or NULL; its contents need not be initialised.  Calls
+ *              that share a workspace must be ordered on one stream.
+ * Outputs must not overlap any input, each other or the workspace (a
+ * workspace smaller than asked for is LA_ERR_INVALID_ARG).  LA_BF16 at
+ * dk = dv = 64 runs on the tensor cores: a forward and a reverse sweep over
+ * 128-token chunks (bf16 operands, fp32 accumulation; dv_out holds bf16
+ * intermediate rows between the sweeps).  With a workspace the heads are cut
+ * into pieces over every SM (the prefill's own aggregate and scan give each
+ * piece its entry state, a reverse scan its gradient state); with NULL, one
+ * block per head.  A bounded wait of those kernels that gives up is reported
+ * by delta_read_device_status.  Everything else runs on the CUDA cores in
+ * fp32, one block per head, token by token, with no workspace; any dk, dv <= 128.
  */
 la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dtype in_dtype,
                               int B, int H, int N, int dk, int dv, float eps,
                               const float* S0, const float* z0, const float* dO,
                               const float* dS_N, const float* dz_N,
                               float* dq, float* dk_out, float* dv_out, float* dS0, float* dz0,
-                              cudaStream_t stream);
+                              void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Bytes of workspace la_prefill_backward uses for these arguments; 0 when it
+ * uses none, or for invalid arguments.  The figure depends on the SM count of
+ * the current device. */
+size_t la_prefill_backward_workspace_bytes(int B, int H, int N, int dk, int dv, la_dtype in_dtype);
 
 /* Bytes of workspace la_prefill needs for these arguments (always >= 256).
  * Returns 0 for arguments la_prefill would reject. */
@@ -232,7 +243,8 @@ la_status la_read_device_status(const void* workspace, cudaStream_t stream);
 /* Synchronizes `stream`, then returns and clears the status word of the
  * tensor-core kernels whose calls take no workspace: delta_prefill and
  * gated_delta_prefill with bf16 inputs at dk = dv = 128, la_prefill_variant
- * with a decay and la_prefill_backward on bf16 inputs at dk = dv = 64.  LA_ERR_TIMEOUT if one of their
+ * with a decay and la_prefill_backward on bf16 inputs at dk = dv = 64 (also
+ * when they are given a workspace).  LA_ERR_TIMEOUT if one of their
  * bounded waits gave up since the last read, otherwise LA_OK; LA_ERR_CUDA if
  * the synchronization or copy fails.  The word belongs to the current device
  * and is shared by every such call on it; the token-by-token kernels have no

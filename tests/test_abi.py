@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
               "delta_prefill", "la_state_bytes", "la_status_string",
               "la_read_device_status", "delta_read_device_status",
               "la_prefill_variant", "la_prefill_variant_workspace_bytes",
-              "gated_delta_prefill", "la_prefill_backward"):
+              "gated_delta_prefill", "la_prefill_backward",
+              "la_prefill_backward_workspace_bytes"):
         assert n in names
 
 
@@ -155,6 +156,16 @@ def test_prefill_variant_workspace_bytes(lib):
     assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 1, 1) == 0
     assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 128, 128, 1, 0, 1) == 0
     assert lib.la_prefill_variant_workspace_bytes(0, 8, 4096, 64, 64, 1, 0, 1) == 0
+    # the backward splits its heads over the SMs only on the tensor-core form
+    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 1) > 0
+    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 0) == 0
+    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 128, 128, 1) == 0
+    assert lib.la_prefill_backward_workspace_bytes(4, 8, 0, 64, 64, 1) == 0
+    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 129, 64, 1) == 0
+    # it grows with the tokens (the parked phi(K) rows) and covers at least them
+    small = lib.la_prefill_backward_workspace_bytes(1, 1, 256, 64, 64, 1)
+    big = lib.la_prefill_backward_workspace_bytes(1, 1, 8192, 64, 64, 1)
+    assert big > small and big >= 8192 * 64 * 2
 
 
 def test_gated_delta_rejects_invalid_arguments(lib):
@@ -177,14 +188,15 @@ def test_backward_rejects_invalid_arguments(lib):
     def call(**kw):
         a = dict(q=BASE, k=BASE + MB, v=BASE + 2 * MB, dt=1, B=1, H=1, N=16, dk=64, dv=64,
                  eps=1e-6, S0=None, z0=None, dO=BASE + 3 * MB, dSN=None, dzN=None,
-                 dq=BASE + 4 * MB, dk_=BASE + 5 * MB, dv_=BASE + 6 * MB, dS0=None, dz0=None)
+                 dq=BASE + 4 * MB, dk_=BASE + 5 * MB, dv_=BASE + 6 * MB, dS0=None, dz0=None,
+                 ws=None, wsb=0)
         a.update(kw)
         f = lambda x: None if x is None else p(x)
         return lib.la_prefill_backward(f(a["q"]), f(a["k"]), f(a["v"]), a["dt"], a["B"], a["H"],
                                        a["N"], a["dk"], a["dv"], ctypes.c_float(a["eps"]),
                                        f(a["S0"]), f(a["z0"]), f(a["dO"]), f(a["dSN"]), f(a["dzN"]),
                                        f(a["dq"]), f(a["dk_"]), f(a["dv_"]), f(a["dS0"]),
-                                       f(a["dz0"]), None)
+                                       f(a["dz0"]), f(a["ws"]), a["wsb"], None)
     assert call(dO=None) == 1                    # dO required
     assert call(dq=BASE + 3 * MB) == 1           # dq overlaps dO
     assert call(dk_=BASE + 4 * MB + 64) == 1     # dk overlaps dq
@@ -192,3 +204,9 @@ def test_backward_rejects_invalid_arguments(lib):
     assert call(dS0=BASE + 2 * MB) == 1          # dS0 overlaps v
     assert call(dk=129) == 1
     assert call(eps=-1.0) == 1
+    need = lib.la_prefill_backward_workspace_bytes(1, 1, 16, 64, 64, 1)
+    assert need > 0
+    assert call(ws=BASE + 8 * MB, wsb=need - 1) == 1       # workspace too small
+    assert call(ws=BASE + 8 * MB + 8, wsb=need) == 1       # misaligned workspace
+    assert call(ws=BASE + 6 * MB, wsb=need) == 1           # workspace overlaps dv
+    assert call(ws=BASE + 2 * MB - 16, wsb=need) == 1      # workspace overlaps v

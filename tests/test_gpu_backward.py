@@ -64,18 +64,18 @@ def test_backward_zero_length_passes_state_gradient(la):
     assert torch.count_nonzero(dz0) == 0
 
 
-# the tensor-core backward (bf16, dk = dv = 64): one block per head, a forward
-# and a reverse sweep over 128-token chunks
+# the tensor-core backward (bf16, dk = dv = 64): a forward and a reverse sweep
+# over 128-token chunks, split over every SM when given a workspace (the
+# default), one block per head without one (ws=False)
 TC_N = [1, 2, 127, 128, 129, 300, 1000]
+WS = [None, False]
+WS_IDS = ["split", "per_head"]
 
 
-@pytest.mark.parametrize("N", TC_N)
-@pytest.mark.parametrize("with_state", [False, True], ids=["zero", "state"])
-def test_backward_tc_matches_oracle(la, orc, N, with_state):
+def _tc_case(la, orc, B, H, N, with_state, ws, seed):
     from fixed_state_recurrent_gb300 import inputs
-    B, H = 1, 3
-    q, k, v = inputs.la_inputs(B, H, N, 64, 64, torch.bfloat16, seed=170 + N)
-    g = torch.Generator().manual_seed(171 + N)
+    q, k, v = inputs.la_inputs(B, H, N, 64, 64, torch.bfloat16, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
     dO = torch.randn((B, H, N, 64), generator=g)
     S0 = z0 = dS = dz = None
     if with_state:
@@ -85,7 +85,7 @@ def test_backward_tc_matches_oracle(la, orc, N, with_state):
         dz = torch.randn((B, H, 64), generator=g)
     cu = lambda t: None if t is None else t.cuda()
     got = la.prefill_backward(q.cuda(), k.cuda(), v.cuda(), dO.cuda(), S0=cu(S0), z0=cu(z0),
-                              dS_N=cu(dS), dz_N=cu(dz))
+                              dS_N=cu(dS), dz_N=cu(dz), ws=ws)
     f = lambda t: None if t is None else f64(t)
     want = orc.la_backward(f64(q), f64(k), f64(v), f64(dO), S0=f(S0), z0=f(z0), dS_N=f(dS),
                            dz_N=f(dz))
@@ -97,8 +97,8 @@ def test_backward_tc_matches_oracle(la, orc, N, with_state):
             # tensor cores form from bf16 operands, each term within about
             # 3 * 2^-9 of itself: checked against 2^-6 T
             phi = lambda u: np.where(u > 0, u + 1.0, np.exp(np.minimum(u, 0.0)))
-            fq, fk = phi(f64(q)[0, :, 0]), phi(f64(k)[0, :, 0])   # [H, 64]
-            vd = np.abs(np.sum(f64(v)[0, :, 0] * f64(dO)[0, :, 0], axis=-1))
+            fq, fk = phi(f64(q)[:, :, 0]), phi(f64(k)[:, :, 0])   # [B, H, 64]
+            vd = np.abs(np.sum(f64(v)[:, :, 0] * f64(dO)[:, :, 0], axis=-1))
             den = np.sum(fq * fk, axis=-1) + 1e-6
             other = fk if name == "dq" else fq
             T = np.max(np.abs(other).max(axis=-1) * vd / den)
@@ -108,18 +108,56 @@ def test_backward_tc_matches_oracle(la, orc, N, with_state):
     assert la.delta_read_device_status() == 0
 
 
-def test_backward_tc_repeatable(la):
+@pytest.mark.parametrize("ws", WS, ids=WS_IDS)
+@pytest.mark.parametrize("N", TC_N)
+@pytest.mark.parametrize("with_state", [False, True], ids=["zero", "state"])
+def test_backward_tc_matches_oracle(la, orc, N, with_state, ws):
+    _tc_case(la, orc, 1, 3, N, with_state, ws, seed=170 + N)
+
+
+# the split's pieces: several per head (long heads), runs that cross heads
+# (many short heads), a ragged last chunk in each
+SPLIT_SHAPES = [(1, 2, 20000), (2, 5, 3000), (3, 40, 333), (1, 1, 40000)]
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=[str(s) for s in SPLIT_SHAPES])
+def test_backward_tc_split_pieces_match_oracle(la, orc, shape):
+    B, H, N = shape
+    _tc_case(la, orc, B, H, N, True, None, seed=190 + N % 97)
+
+
+@pytest.mark.parametrize("ws", WS, ids=WS_IDS)
+def test_backward_tc_repeatable(la, ws):
+    # no atomics and a fixed split: the same bits every call
     from fixed_state_recurrent_gb300 import inputs
-    q, k, v = inputs.la_inputs(2, 2, 555, 64, 64, torch.bfloat16, seed=180)
-    dO = torch.randn((2, 2, 555, 64), generator=torch.Generator().manual_seed(181)).cuda()
+    q, k, v = inputs.la_inputs(2, 2, 5555, 64, 64, torch.bfloat16, seed=180)
+    dO = torch.randn((2, 2, 5555, 64), generator=torch.Generator().manual_seed(181)).cuda()
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    first = la.prefill_backward(qd, kd, vd, dO)
+    first = la.prefill_backward(qd, kd, vd, dO, ws=ws)
     for _ in range(6):
-        again = la.prefill_backward(qd, kd, vd, dO)
+        again = la.prefill_backward(qd, kd, vd, dO, ws=ws)
         assert all(torch.equal(a, b) for a, b in zip(first, again))
 
 
-def test_backward_tc_bounded_wait_reports_timeout(la, orc, monkeypatch):
+def test_backward_tc_explicit_workspace(la, orc):
+    # a caller-owned workspace of exactly the asked-for size, whose stale
+    # contents (NaN) do not reach the outputs
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N = 2, 3, 2500
+    q, k, v = inputs.la_inputs(B, H, N, 64, 64, torch.bfloat16, seed=184)
+    dO = torch.randn((B, H, N, 64), generator=torch.Generator().manual_seed(185))
+    need = la.backward_workspace_bytes(B, H, N, 64, 64)
+    assert need > 0 and need % 4 == 0
+    ws = torch.full((need // 4,), float("nan"), device="cuda").view(torch.uint8)
+    got = la.prefill_backward(q.cuda(), k.cuda(), v.cuda(), dO.cuda(), ws=ws)
+    assert la.delta_read_device_status() == 0
+    want = orc.la_backward(f64(q), f64(k), f64(v), f64(dO))
+    for name, a, b in zip(("dq", "dk", "dv", "dS0", "dz0"), got, want):
+        assert relmax(f64(a), b) <= tol_for(torch.bfloat16), name
+
+
+@pytest.mark.parametrize("ws", WS, ids=WS_IDS)
+def test_backward_tc_bounded_wait_reports_timeout(la, orc, monkeypatch, ws):
     # the test hook makes the kernel's MMA issuer wait on an mbarrier that
     # nothing completes (2 ms limit): the launch finishes, the library status
     # word says LA_ERR_TIMEOUT, reading clears it, and the next call is right
@@ -130,12 +168,12 @@ def test_backward_tc_bounded_wait_reports_timeout(la, orc, monkeypatch):
     la.delta_read_device_status()
     monkeypatch.setenv("LA_TEST_FORCE_WAIT", "1")
     monkeypatch.setenv("LA_MBAR_TIMEOUT_NS", "2000000")
-    la.prefill_backward(qd, kd, vd, dd)
+    la.prefill_backward(qd, kd, vd, dd, ws=ws)
     assert la.delta_read_device_status() == 4  # LA_ERR_TIMEOUT
     assert la.delta_read_device_status() == 0
     monkeypatch.delenv("LA_TEST_FORCE_WAIT")
     monkeypatch.delenv("LA_MBAR_TIMEOUT_NS")
-    got = la.prefill_backward(qd, kd, vd, dd)
+    got = la.prefill_backward(qd, kd, vd, dd, ws=ws)
     assert la.delta_read_device_status() == 0
     want = orc.la_backward(f64(q), f64(k), f64(v), f64(dO))
     for a, b in zip(got[:3], want[:3]):
