@@ -24,9 +24,10 @@
 //             the reverse sweep reads back before overwriting them with dv;
 //   reverse:  from G = dS_N, g = dz_N, per chunk (last to first) dU and dV,
 //             then G += W^T D on the tensor cores; finally dS0, dz0.
-// The block's four warps own the TMEM lane quadrants (thread t: token row t
-// of the chunk, or state lane t); one thread issues the TMA copies and the
-// MMAs, and the steps of a chunk are separated by block barriers.  Every wait
+// The block's eight warps own the TMEM lane quadrants two by two (threads t
+// and t + 128: token row t of the chunk, or state lane t, each one half of
+// the row's 64 columns); one thread issues the TMA copies and the MMAs, and
+// the steps of a chunk are separated by block barriers.  Every wait
 // is bounded; a wait that gives up records LA_ERR_TIMEOUT in the library
 // status word and the kernel finishes with unspecified outputs.
 #include "prefill_tc_common.cuh"
@@ -49,10 +50,11 @@ constexpr uint32_t OFF_DT = 2 * STAGE;        // forward: D being formed (two bl
 constexpr uint32_t OFF_ONES = OFF_DT + 2 * BLK;
 constexpr uint32_t OFF_SNAP = OFF_ONES + BLK;
 constexpr uint32_t OFF_BAR = OFF_SNAP + SNAP;
-constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+constexpr uint32_t OFF_RED = OFF_BAR + 256;   // per thread: its half of a row's dot product
+constexpr uint32_t SMEM = OFF_RED + 256 * 4 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 static_assert(OFF_SNAP % 1024 == 0, "swizzled tile alignment");
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // two threads per chunk row / TMEM lane
 constexpr uint32_t kCols = 512;
 // TMEM columns.  Forward: A scores / P, O [num | den parts], dW, S (running
 // state, lanes j).  Reverse: A2 (V~ D^T, then its mask), dU, A3 (U W^T, then
@@ -123,11 +125,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Row r of a [128 x 64] bf16 tile, unpacked: out[i] = element i.
-__device__ __forceinline__ void load_row_bf16(const uint8_t* tile, int r, float* out) {
+// Half `hf` (columns 32 hf .. 32 hf + 31) of row r of a [128 x 64] bf16 tile,
+// unpacked: out[i] = element 32 hf + i.
+__device__ __forceinline__ void load_half_bf16(const uint8_t* tile, int r, int hf, float* out) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 u = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, c));
+  for (int c = 0; c < 4; ++c) {
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, 4 * hf + c));
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -137,36 +140,33 @@ __device__ __forceinline__ void load_row_bf16(const uint8_t* tile, int r, float*
   }
 }
 
-// Row r of a [128 x 64] bf16 tile from 64 floats (rounded to nearest even).
-__device__ __forceinline__ void store_row_bf16(uint8_t* tile, int r, const float* v) {
+// Half `hf` of row r of a [128 x 64] bf16 tile from 32 floats (rounded to
+// nearest even).
+__device__ __forceinline__ void store_half_bf16(uint8_t* tile, int r, int hf, const float* v) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < 4; ++c) {
     uint4 u;
     u.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
     u.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
     u.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
     u.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
-    *reinterpret_cast<uint4*>(tile + sw128_offset(r, c)) = u;
+    *reinterpret_cast<uint4*>(tile + sw128_offset(r, 4 * hf + c)) = u;
   }
 }
 
-// 64 consecutive TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_row64(uint32_t taddr, float* out) {
-  uint32_t a[32], b[32];
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_row32(uint32_t taddr, float* out) {
+  uint32_t a[32];
   tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
   tmem_ld_wait();
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    out[i] = __uint_as_float(a[i]);
-    out[32 + i] = __uint_as_float(b[i]);
-  }
+  for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(a[i]);
 }
 
-// 64 floats into this thread's lane, columns [taddr, taddr + 64).
-__device__ __forceinline__ void tmem_put64(uint32_t taddr, const float* v) {
+// 32 floats into this thread's lane, columns [taddr, taddr + 32).
+__device__ __forceinline__ void tmem_put32(uint32_t taddr, const float* v) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 2; ++q) {
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[16 * q + i]);
@@ -176,39 +176,46 @@ __device__ __forceinline__ void tmem_put64(uint32_t taddr, const float* v) {
 
 // The causal mask of a [128 x 128] fp32 score tile in TMEM (this thread's
 // row t = 32 quad + lane), packed to bf16 in place over the tile's first 64
-// columns: keep s <= t (lower), or s >= t (upper).  Column blocks are read two
-// at a time and a pair is read completely before its packed columns (which lie
-// in the pair's own or an earlier block) are written.
+// columns: keep s <= t (lower), or s >= t (upper).  The two threads of a row
+// split the columns: half hf reads column blocks 2 hf, 2 hf + 1 and writes
+// packed columns [32 hf, 32 hf + 32), which half 0 reads; every thread's reads
+// finish (the block barrier) before any packed column is written.  Called by
+// every thread of the block.
 template <bool UPPER>
-__device__ __forceinline__ void mask_pack(uint32_t base, int quad, int lane) {
+__device__ __forceinline__ void mask_pack(uint32_t base, int quad, int lane, int hf) {
+  uint32_t r0[32], r1[32];
+  tmem_ld32(base + 64 * hf, r0);
+  tmem_ld32(base + 64 * hf + 32, r1);
+  tmem_ld_wait();
+  __syncthreads();
 #pragma unroll
-  for (int q2 = 0; q2 < 4; q2 += 2) {
-    uint32_t r0[32], r1[32];
-    tmem_ld32(base + 32 * q2, r0);
-    tmem_ld32(base + 32 * (q2 + 1), r1);
-    tmem_ld_wait();
+  for (int h = 0; h < 2; ++h) {
+    const int q4 = 2 * hf + h;
+    const uint32_t* r = h ? r1 : r0;
+    uint32_t w[16];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int q4 = q2 + h;
-      const uint32_t* r = h ? r1 : r0;
-      uint32_t w[16];
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const int s0 = 2 * t, s1 = 2 * t + 1;  // keys 32 q4 + s within the block
-        bool k0, k1;
-        if (UPPER) {
-          k0 = q4 > quad || (q4 == quad && s0 >= lane);
-          k1 = q4 > quad || (q4 == quad && s1 >= lane);
-        } else {
-          k0 = q4 < quad || (q4 == quad && s0 <= lane);
-          k1 = q4 < quad || (q4 == quad && s1 <= lane);
-        }
-        w[t] = pack_bf16x2(k0 ? __uint_as_float(r[s0]) : 0.f, k1 ? __uint_as_float(r[s1]) : 0.f);
+    for (int t = 0; t < 16; ++t) {
+      const int s0 = 2 * t, s1 = 2 * t + 1;  // keys 32 q4 + s within the block
+      bool k0, k1;
+      if (UPPER) {
+        k0 = q4 > quad || (q4 == quad && s0 >= lane);
+        k1 = q4 > quad || (q4 == quad && s1 >= lane);
+      } else {
+        k0 = q4 < quad || (q4 == quad && s0 <= lane);
+        k1 = q4 < quad || (q4 == quad && s1 <= lane);
       }
-      tmem_st16(base + 16 * q4, w);
+      w[t] = pack_bf16x2(k0 ? __uint_as_float(r[s0]) : 0.f, k1 ? __uint_as_float(r[s1]) : 0.f);
     }
+    tmem_st16(base + 16 * q4, w);
   }
   tmem_st_wait();
+}
+
+// Row r of a float array in global memory, 32 floats from column 32 hf.
+__device__ __forceinline__ void store_half_f32(float* rowp, int hf, const float* v) {
+  float4* dst = reinterpret_cast<float4*>(rowp + 32 * hf);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
 // MODE 0: one block per head, both sweeps (no workspace).  MODE 1: the
@@ -226,7 +233,11 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // arithmetic so that accesses through it stay shared-space accesses
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  float* red = reinterpret_cast<float*>(smem + OFF_RED);
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+  // two threads per row: row (TMEM lane) t % 128, column half t / 128; warps w
+  // and w + 4 share TMEM lane quadrant w % 4
+  const int row = t & (C - 1), hf = t >> 7, quad = warp & 3;
   if (MODE != 0) pdl_launch_dependents();  // the next launch may be scheduled now
   uint8_t* dt = smem + OFF_DT;
   uint8_t* snap = smem + OFF_SNAP;
@@ -258,7 +269,8 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot);
-  const uint32_t tl = tm + ((uint32_t)(32 * warp) << 16);  // this thread's TMEM lane (t)
+  const uint32_t tl = tm + ((uint32_t)(32 * quad) << 16);  // this thread's TMEM lane (row)
+  const uint32_t th = 32 * hf;                              // and its column half
   const Ctx x{&p, B, mbar_ns};
   const uint32_t aOnes = smem_u32(smem + OFF_ONES), aSnap = smem_u32(snap), aDt = smem_u32(dt);
   // loads issued (thread 0) and loads consumed (every thread), in the same
@@ -300,35 +312,36 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_before();
     __syncthreads();
   };
+  auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&B->abort) != 0; };
 
   // =================== forward sweep of one piece ===================
   auto fwd_piece = [&](const Piece& pc) {
   const int h = pc.h, c0 = pc.tok0 / C, NC = pc.nch;
   // the entry state (S0, z0 for a whole head; the scan's E otherwise) -> the
   // running state (lane j: column j of S, lane 64: z) and its snapshot (row j;
-  // rows 64, 65: z in two bf16 parts)
+  // rows 64, 65: z in two bf16 parts); each thread its column half
   {
-    float e[64];
+    float e[32];
     if (MODE == 0) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        e[i] = t < D ? (p.S0 ? __ldg(p.S0 + ((size_t)h * D + i) * D + t) : 0.f)
-                     : (t == D && p.z0 ? __ldg(p.z0 + (size_t)h * D + i) : 0.f);
+      for (int i = 0; i < 32; ++i)
+        e[i] = row < D ? (p.S0 ? __ldg(p.S0 + ((size_t)h * D + th + i) * D + row) : 0.f)
+                       : (row == D && p.z0 ? __ldg(p.z0 + (size_t)h * D + th + i) : 0.f);
     } else {
-      const float* src = p.E + (size_t)pc.slot * SZ + (t <= D ? t : 0) * D;
+      const float* src = p.E + (size_t)pc.slot * SZ + (row <= D ? row : 0) * D + th;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) e[i] = t <= D ? __ldcg(src + i) : 0.f;
+      for (int i = 0; i < 32; ++i) e[i] = row <= D ? __ldcg(src + i) : 0.f;
     }
-    tmem_put64(tl + T_S, e);
+    tmem_put32(tl + T_S + th, e);
     tmem_st_wait();
-    if (t < D) {
-      store_row_bf16(snap, t, e);
-    } else if (t == D) {
-      float lo[64];
+    if (row < D) {
+      store_half_bf16(snap, row, hf, e);
+    } else if (row == D) {
+      float lo[32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) lo[i] = e[i] - __bfloat162float(__float2bfloat16_rn(e[i]));
-      store_row_bf16(snap, D, e);
-      store_row_bf16(snap, D + 1, lo);
+      for (int i = 0; i < 32; ++i) lo[i] = e[i] - __bfloat162float(__float2bfloat16_rn(e[i]));
+      store_half_bf16(snap, D, hf, e);
+      store_half_bf16(snap, D + 1, hf, lo);
     }
   }
   if (t == 0) load(h, c0, true);
@@ -342,8 +355,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int valid = min(C, p.N - tok);
     if (t == 0 && c + 1 < NC) load(h, c0 + c + 1, true);
     waitb(x, &B->full[s], (nuse / 2) & 1);
-    phi_row<8>(st, t, 0, valid);
-    phi_row<8>(st + BLK, t, 0, valid);
+    phi_row<8>(st + hf * BLK, row, 0, valid);  // half 0: phi(Q), half 1: phi(K)
     step_done();
 
     // scores, and phi(Q) [S | z] into O
@@ -359,7 +371,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (t == 0) mma_commit(&B->mma);
     mma_done();
-    mask_pack<false>(tl + T_A, warp, lane);
+    mask_pack<false>(tl + T_A, quad, lane, hf);
     step_done();
 
     // O += P [V | 1]
@@ -371,41 +383,45 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (t == 0) mma_commit(&B->mma);
     mma_done();
-    {  // den, o, then D = [dnum | dden] of row t
-      float num[64];
-      tmem_row64(tl + T_O, num);
-      uint32_t d2[2];
+    {  // den, o, then D = [dnum | dden] of the row; this thread's column half of dnum
+      uint32_t nr[32], d2[2];
+      tmem_ld32(tl + T_O + th, nr);
       tmem_ld2(tl + T_O + D, d2);
       tmem_ld_wait();
       const float den = __uint_as_float(d2[0]) + __uint_as_float(d2[1]) + p.eps;
       const float inv = 1.f / den;
-      float dot = 0.f;
-      const uint8_t* x0 = st + 3 * BLK;
+      float dn[32], dot = 0.f;
+      const uint8_t* x0 = st + 3 * BLK + hf * BLK;  // dO columns 32 hf .. 32 hf + 31
 #pragma unroll
-      for (int cc = 0; cc < 16; ++cc) {
-        const float4 g4 = *reinterpret_cast<const float4*>(x0 + (cc / 8) * BLK + sw128_offset(t, cc % 8));
+      for (int cc = 0; cc < 8; ++cc) {
+        const float4 g4 = *reinterpret_cast<const float4*>(x0 + sw128_offset(row, cc));
         const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          dot += gv[j] * (num[4 * cc + j] * inv);
-          num[4 * cc + j] = gv[j] * inv;  // now dnum
+          dot += gv[j] * (__uint_as_float(nr[4 * cc + j]) * inv);
+          dn[4 * cc + j] = gv[j] * inv;
         }
       }
-      const float dden = -dot * inv;
-      store_row_bf16(dt, t, num);
-      *reinterpret_cast<uint4*>(dt + BLK + sw128_offset(t, 0)) =
-          make_uint4(pack_bf16x2(dden, dden), 0u, 0u, 0u);
+      red[t] = dot;
+      store_half_bf16(dt, row, hf, dn);
+      __syncthreads();
+      const float dden = -(red[row] + red[row + C]) * inv;
+      if (hf == 0)
+        *reinterpret_cast<uint4*>(dt + BLK + sw128_offset(row, 0)) = make_uint4(pack_bf16x2(dden, dden), 0u, 0u, 0u);
       // parked in dv's row (256 bytes): 64 bf16 dnum, then dden twice and zeros,
       // the row-major form the reverse sweep's tile loads read back
-      if (t < valid) {
-        uint4* row = reinterpret_cast<uint4*>(p.dv + ((size_t)h * p.N + tok + t) * D);
+      if (row < valid) {
+        uint4* prow = reinterpret_cast<uint4*>(p.dv + ((size_t)h * p.N + tok + row) * D);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          row[q] = make_uint4(pack_bf16x2(num[8 * q], num[8 * q + 1]), pack_bf16x2(num[8 * q + 2], num[8 * q + 3]),
-                              pack_bf16x2(num[8 * q + 4], num[8 * q + 5]), pack_bf16x2(num[8 * q + 6], num[8 * q + 7]));
-        row[8] = make_uint4(pack_bf16x2(dden, dden), 0u, 0u, 0u);
+        for (int q = 0; q < 4; ++q)
+          prow[4 * hf + q] = make_uint4(pack_bf16x2(dn[8 * q], dn[8 * q + 1]), pack_bf16x2(dn[8 * q + 2], dn[8 * q + 3]),
+                                        pack_bf16x2(dn[8 * q + 4], dn[8 * q + 5]), pack_bf16x2(dn[8 * q + 6], dn[8 * q + 7]));
+        if (hf == 0) {
+          prow[8] = make_uint4(pack_bf16x2(dden, dden), 0u, 0u, 0u);
+        } else {
 #pragma unroll
-        for (int q = 9; q < 16; ++q) row[q] = make_uint4(0u, 0u, 0u, 0u);
+          for (int q = 9; q < 16; ++q) prow[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
     step_done();
@@ -427,7 +443,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (t == 0) mma_commit(&B->mma);
     mma_done();
-    mask_pack<false>(tl + T_A, warp, lane);
+    mask_pack<false>(tl + T_A, quad, lane, hf);
     step_done();
 
     // dW += mask(A) U;  S += [V | 1]^T U
@@ -449,37 +465,35 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (t == 0) mma_commit(&B->mma);
     mma_done();
     {  // dq = dW phi'(q), phi'(u) = min(phi(u), 1); the state snapshot for the next chunk
-      float g[64], f[64];
-      tmem_row64(tl + T_DW, g);
-      load_row_bf16(st, t, f);
-      if (t < valid && !*reinterpret_cast<volatile int*>(&B->abort)) {
-        float4* dst = reinterpret_cast<float4*>(p.dq + ((size_t)h * p.N + tok + t) * D);
+      float g[32], f[32];
+      tmem_row32(tl + T_DW + th, g);
+      load_half_bf16(st, row, hf, f);
+      if (row < valid && !aborted()) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          dst[q] = make_float4(g[4 * q] * fminf(f[4 * q], 1.f), g[4 * q + 1] * fminf(f[4 * q + 1], 1.f),
-                               g[4 * q + 2] * fminf(f[4 * q + 2], 1.f), g[4 * q + 3] * fminf(f[4 * q + 3], 1.f));
+        for (int i = 0; i < 32; ++i) g[i] *= fminf(f[i], 1.f);
+        store_half_f32(p.dq + ((size_t)h * p.N + tok + row) * D, hf, g);
       }
-      if (c + 1 < NC && warp <= 2) {  // whole warps: tcgen05.ld is warp-collective
-        float e[64];
-        tmem_row64(tl + T_S, e);
-        if (t < D) store_row_bf16(snap, t, e);
-        if (t == D) {
-          store_row_bf16(snap, D, e);
+      if (c + 1 < NC && quad <= 2) {  // whole warps: tcgen05.ld is warp-collective
+        float e[32];
+        tmem_row32(tl + T_S + th, e);
+        if (row < D) store_half_bf16(snap, row, hf, e);
+        if (row == D) {
+          store_half_bf16(snap, D, hf, e);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) e[i] -= __bfloat162float(__float2bfloat16_rn(e[i]));
-          store_row_bf16(snap, D + 1, e);
+          for (int i = 0; i < 32; ++i) e[i] -= __bfloat162float(__float2bfloat16_rn(e[i]));
+          store_half_bf16(snap, D + 1, hf, e);
         }
       }
     }
     step_done();
   }
-  if (MODE == 1 && warp <= 2) {  // whole warps: tcgen05.ld is warp-collective
-    float e[64];
-    tmem_row64(tl + T_DG, e);
-    if (t <= D && !*reinterpret_cast<volatile int*>(&B->abort)) {
-      float4* dst = reinterpret_cast<float4*>(p.dG + (size_t)pc.slot * SZ + t * D);
+  if (MODE == 1 && quad <= 2) {  // whole warps: tcgen05.ld is warp-collective
+    float e[32];
+    tmem_row32(tl + T_DG + th, e);
+    if (row <= D && !aborted()) {
+      float4* dst = reinterpret_cast<float4*>(p.dG + (size_t)pc.slot * SZ + row * D + th);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) __stcg(dst + q, make_float4(e[4 * q], e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]));
+      for (int q = 0; q < 8; ++q) __stcg(dst + q, make_float4(e[4 * q], e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]));
     }
   }
   step_done();
@@ -492,24 +506,24 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // reverse scan's otherwise) -> the running gradient state (lane j: column j
   // of G, lane 64: g) and its snapshot (row j; row 64: g; row 65 stays 0)
   {
-    float e[64];
+    float e[32];
     if (MODE == 0) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        e[i] = t < D ? (p.dS_N ? __ldg(p.dS_N + ((size_t)h * D + i) * D + t) : 0.f)
-                     : (t == D && p.dz_N ? __ldg(p.dz_N + (size_t)h * D + i) : 0.f);
+      for (int i = 0; i < 32; ++i)
+        e[i] = row < D ? (p.dS_N ? __ldg(p.dS_N + ((size_t)h * D + th + i) * D + row) : 0.f)
+                       : (row == D && p.dz_N ? __ldg(p.dz_N + (size_t)h * D + th + i) : 0.f);
     } else {
-      const float* src = p.Gaft + (size_t)pc.slot * SZ + (t <= D ? t : 0) * D;
+      const float* src = p.Gaft + (size_t)pc.slot * SZ + (row <= D ? row : 0) * D + th;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) e[i] = t <= D ? __ldcg(src + i) : 0.f;
+      for (int i = 0; i < 32; ++i) e[i] = row <= D ? __ldcg(src + i) : 0.f;
     }
-    tmem_put64(tl + T_G, e);
+    tmem_put32(tl + T_G + th, e);
     tmem_st_wait();
-    if (t <= D) store_row_bf16(snap, t, e);
-    if (t == D + 1) {
+    if (row <= D) store_half_bf16(snap, row, hf, e);
+    if (row == D + 1) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) e[i] = 0.f;
-      store_row_bf16(snap, D + 1, e);
+      for (int i = 0; i < 32; ++i) e[i] = 0.f;
+      store_half_bf16(snap, D + 1, hf, e);
     }
   }
   step_done();  // (also: every thread's parked rows are fenced before the first tile load)
@@ -524,8 +538,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int valid = min(C, p.N - tok);
     if (t == 0 && c > 0) load(h, c0 + c - 1, false);
     waitb(x, &B->full[s], (nuse / 2) & 1);
-    phi_row<8>(st, t, 0, valid);
-    phi_row<8>(st + BLK, t, 0, valid);
+    phi_row<8>(st + hf * BLK, row, 0, valid);  // half 0: phi(Q), half 1: phi(K)
     step_done();
 
     // A2 = V~ D^T, dU = V~ [G | g]^T, A3 = U W^T, dV = U G
@@ -553,8 +566,8 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (t == 0) mma_commit(&B->mma);
     mma_done();
-    mask_pack<true>(tl + T_A2, warp, lane);
-    mask_pack<true>(tl + T_A3, warp, lane);
+    mask_pack<true>(tl + T_A2, quad, lane, hf);
+    mask_pack<true>(tl + T_A3, quad, lane, hf);
     step_done();
 
     // dU += mask^T(A2) W, dV += mask^T(A3) dnum, G += W^T D
@@ -573,34 +586,28 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (t == 0) mma_commit(&B->mma);
     mma_done();
     {  // dk = dU phi'(k), dv; the gradient-state snapshot for the chunk before
-      float g[64], f[64];
-      tmem_row64(tl + T_DU, g);
-      load_row_bf16(st + BLK, t, f);
-      const bool out = t < valid && !*reinterpret_cast<volatile int*>(&B->abort);
+      float g[32], f[32];
+      tmem_row32(tl + T_DU + th, g);
+      load_half_bf16(st + BLK, row, hf, f);
+      const bool out = row < valid && !aborted();
       if (out) {
-        float4* dst = reinterpret_cast<float4*>(p.dk + ((size_t)h * p.N + tok + t) * D);
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          dst[q] = make_float4(g[4 * q] * fminf(f[4 * q], 1.f), g[4 * q + 1] * fminf(f[4 * q + 1], 1.f),
-                               g[4 * q + 2] * fminf(f[4 * q + 2], 1.f), g[4 * q + 3] * fminf(f[4 * q + 3], 1.f));
+        for (int i = 0; i < 32; ++i) g[i] *= fminf(f[i], 1.f);
+        store_half_f32(p.dk + ((size_t)h * p.N + tok + row) * D, hf, g);
       }
-      tmem_row64(tl + T_DV, g);
-      if (out) {
-        float4* dst = reinterpret_cast<float4*>(p.dv + ((size_t)h * p.N + tok + t) * D);
+      tmem_row32(tl + T_DV + th, g);
+      if (out) store_half_f32(p.dv + ((size_t)h * p.N + tok + row) * D, hf, g);
+      if (quad <= 2) {  // whole warps: tcgen05.ld is warp-collective; lanes 0..64 are kept
+        float e[32];
+        tmem_row32(tl + T_G + th, e);
+        if (c > 0 && row <= D) store_half_bf16(snap, row, hf, e);
+        if (MODE == 0 && c == 0 && row <= D && !aborted()) {  // dS0, dz0
 #pragma unroll
-        for (int q = 0; q < 16; ++q) dst[q] = make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
-      }
-      if (warp <= 2) {  // whole warps: tcgen05.ld is warp-collective; lanes 0..64 are kept
-        float e[64];
-        tmem_row64(tl + T_G, e);
-        if (c > 0 && t <= D) store_row_bf16(snap, t, e);
-        if (MODE == 0 && c == 0 && t <= D && !*reinterpret_cast<volatile int*>(&B->abort)) {  // dS0, dz0
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            if (t < D) {
-              if (p.dS0) p.dS0[((size_t)h * D + i) * D + t] = e[i];
+          for (int i = 0; i < 32; ++i) {
+            if (row < D) {
+              if (p.dS0) p.dS0[((size_t)h * D + th + i) * D + row] = e[i];
             } else if (p.dz0) {
-              p.dz0[(size_t)h * D + i] = e[i];
+              p.dz0[(size_t)h * D + th + i] = e[i];
             }
           }
         }
@@ -628,7 +635,7 @@ backward_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   }
 
-  if (t == 0 && *reinterpret_cast<volatile int*>(&B->abort)) {  // MMAs in flight end first
+  if (t == 0 && aborted()) {  // MMAs in flight end first
     int never = 0;
     mma_commit(&B->drain);
     mbar_wait(&B->drain, 0, globaltimer_ns() + mbar_ns, &never);
