@@ -286,6 +286,22 @@ def bench_prefill(api, w, steps, warmup, rank, world, sets=4):
     return total, [total / steps] * steps
 
 
+def _graph_ms(step, steps, stream, world):
+    """Device ms per call of `step(i)`: `steps` calls captured as one CUDA
+    graph on `stream` (after the caller's warm-up calls), replayed once
+    untimed, then once between events; max over ranks."""
+    import torch
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(steps):
+                step(i)
+        graph.replay()
+    total, _ = _timed(lambda i: graph.replay(), 1, stream, world, per_launch=False)
+    return total / steps
+
+
 def profile_calls(api, w, calls, sets=4):
     """`calls` plain la_prefill calls over the rotating buffer sets of
     bench_prefill, launched one by one (no graph), for profilers."""
@@ -483,12 +499,16 @@ def bench_decay_prefill(api, rank, world, reps=12, sets=4):
         for i in range(sets):
             fn(i)
     _, per = _timed(fn, reps, stream, world)
-    ms = statistics.median(per)
+    ms_calls = statistics.median(per)
+    ms = _graph_ms(fn, 4 * sets, stream, world)
     # algorithmic bytes: q, k, v in, o out (640 B/token), alpha (4 B/token), final state
     b = (PREFILL_BYTES_PER_TOKEN + 4) * w.tokens + w.B * w.H * (w.dk * w.dv + w.dk) * 4
     hbm_peak, _, kind = _peaks()
     return {"workload": "decayed prefill: B=4 H=8 N=4096 dk=dv=64 bf16, alpha ~ U(0.9, 1), "
                         "write then read", "ms_per_call": ms,
+            "ms_per_python_call": ms_calls,
+            "timing": f"{4 * sets} calls in one CUDA graph, replayed (device time per call); "
+                      "ms_per_python_call: median of back-to-back calls from Python",
             "tokens_per_s": w.tokens / (ms * 1e-3), "hbm_gbs": b / (ms * 1e-3) / 1e9,
             "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": f"of {kind}",
             "l2": f"{sets} rotating input/output sets"}
@@ -509,18 +529,21 @@ def bench_backward(api, rank, world, reps=5):
     fn = lambda i: api.prefill_backward(q, k, v, dO)
     fh = lambda i: api.prefill_backward(q, k, v, dO, ws=False)
     with torch.cuda.stream(stream):
-        fn(0)
-        fh(0)
+        for i in range(3):
+            fn(i)
+            fh(i)
     _, per = _timed(fn, reps, stream, world)
-    ms = statistics.median(per)
-    _, per = _timed(fh, reps, stream, world)
-    ms_head = statistics.median(per)
+    ms_calls = statistics.median(per)
+    ms = _graph_ms(fn, reps, stream, world)
+    ms_head = _graph_ms(fh, reps, stream, world)
     # algorithmic bytes: q, k, v (bf16) and dO (fp32) in, dq, dk, dv (fp32) out
     b = (3 * 2 * w.dk + 4 * w.dv + 4 * (2 * w.dk + w.dv)) * w.tokens
     hbm_peak, _, kind = _peaks()
     return {"workload": "backward: B=4 H=8 N=4096 dk=dv=64 bf16 inputs, dO ~ N(0,1), "
                         "gradients of q, k, v, S0, z0", "ms_per_call": ms,
-            "ms_per_call_one_block_per_head": ms_head,
+            "ms_per_call_one_block_per_head": ms_head, "ms_per_python_call": ms_calls,
+            "timing": f"{reps} calls in one CUDA graph, replayed (device time per call); "
+                      "ms_per_python_call: median of back-to-back calls from Python",
             "tokens_per_s": w.tokens / (ms * 1e-3), "hbm_gbs": b / (ms * 1e-3) / 1e9,
             "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": f"of {kind}"}
 

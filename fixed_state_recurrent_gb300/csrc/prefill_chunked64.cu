@@ -502,9 +502,11 @@ constexpr uint32_t OFF_SNAP = OFF_ONES + BLK;      // two snapshots
 constexpr uint32_t OFF_OUT = OFF_SNAP + 2 * SNAP;  // output staging: two [128 x 32] fp32 boxes
 constexpr uint32_t OFF_BAR = OFF_OUT + 2 * BLK;
 // decayed form only: per stage, the inclusive sums g_t of log2 alpha over the
-// chunk (128 floats), then the four warps' totals of the scan
+// chunk (128 floats), the four warps' totals of the scan, then per key s the
+// factor 2^(g_e - g_s), g_e the sum at the last key of s's 32-key block
 constexpr uint32_t OFF_G = OFF_BAR + 512;
-constexpr int GSTRIDE = C + 4;
+constexpr int GKF = C + 4;  // offset of the key factors
+constexpr int GSTRIDE = 2 * C + 4;
 constexpr uint32_t SMEM = OFF_G + NS * GSTRIDE * 4 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 static_assert(OFF_OUT % 1024 == 0, "swizzled staging alignment");
@@ -741,26 +743,34 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int i = 0; run.piece(p.sp, i, &pc); ++i)
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const int s = sj % NS;
+        const int valid = pc.tok1 - (pc.tok0 + c * C);
+        // the decay of this row's token, loaded before the wait for the tiles
+        float av = 1.f;
+        if (DECAY && r < valid) av = __ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + c * C + r);
         const bool got = wait3_warp(x, &B->full[s], (sj / NS) & 1);
         if (!DECAY && !got) continue;
         uint8_t* st = stage_ptr(smem, s);
-        const int valid = pc.tok1 - (pc.tok0 + c * C);
-        if (got) phi_row<8>(st, r, 0, valid);
+        if (got) {
+          // Q, and in the decayed form K too: one copy of the loop body (the
+          // roles' code together must stay within the instruction caches)
+#pragma unroll 1
+          for (int m = 0; m < (DECAY ? 2 : 1); ++m) phi_row<8>(st + m * BLK, r, 0, valid);
+        }
         if (DECAY) {
-          if (got) phi_row<8>(st + BLK, r, 0, valid);
           // g_t: inclusive sums of log2 alpha over the chunk (alpha = 1 past the
           // end); a warp scan, then the totals of the warps before.  The named
           // barrier runs whether or not the wait succeeded, so that all four
           // warps always meet it.
           float la = 0.f;
-          if (got && r < valid)
-            la = __log2f(fmaxf(__ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + c * C + r), kAlphaMin));
+          if (got && r < valid) la = __log2f(fmaxf(av, kAlphaMin));
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) {
             const float y = __shfl_up_sync(0xFFFFFFFFu, la, off);
             if (lane >= off) la += y;
           }
           float* g = reinterpret_cast<float*>(smem + OFF_G) + s * GSTRIDE;
+          // the key factor from the warp's own sums (the earlier warps' totals cancel)
+          g[GKF + r] = exp2_ftz(__shfl_sync(0xFFFFFFFFu, la, 31) - la);
           if (lane == 31) g[C + r / 32] = la;
           named_bar_sync(2, 128);
           for (int w = 0; w < r / 32; ++w) la += g[C + w];
@@ -787,50 +797,83 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const float gt = DECAY ? g[row] : 0.f;
         // this warp's query rows are 32 quad .. +31: key blocks before `quad` are
         // fully visible, block `quad` holds the diagonal, later blocks are zero;
-        // packed keys 32 q4.. go to columns 16 q4..  Blocks are loaded two at a
-        // time, and a pair is read completely before its packed columns (which
-        // lie in the pair's own or an earlier block) are written.
-#pragma unroll
-        for (int q2 = 0; q2 < 4; q2 += 2) {
-          uint32_t r0[32], r1[32];
-          if (q2 <= quad) tmem_ld32(base + 32 * q2, r0);
-          if (q2 + 1 <= quad) tmem_ld32(base + 32 * (q2 + 1), r1);
-          if (q2 <= quad) tmem_ld_wait();
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int q4 = q2 + h;
-            const uint32_t* r = h ? r1 : r0;
+        // packed keys 32 q4.. go to columns 16 q4..
+        if (DECAY) {
+          // One key block at a time (one copy of the loop body): block q4 is
+          // read completely before its packed columns, which lie in block
+          // q4 / 2 <= q4, are written.  Kept scores are weighted by
+          // 2^(g_t - g_s); for a block before the diagonal that is
+          // 2^(g_t - g_e) 2^(g_e - g_s), g_e the sum at the block's last key:
+          // one exponential per block and row, the key factors from the phi
+          // warps (each factor <= 1 when alpha <= 1).
+          const float* kf = g + GKF;
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t w[16];
             if (q4 > quad) {
 #pragma unroll
               for (int t = 0; t < 16; ++t) w[t] = 0u;
-            } else if (!DECAY && q4 < quad) {
-#pragma unroll
-              for (int t = 0; t < 16; ++t)
-                w[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
-            } else if (!DECAY) {
-#pragma unroll
-              for (int t = 0; t < 16; ++t)
-                w[t] = pack_bf16x2(2 * t <= lane ? __uint_as_float(r[2 * t]) : 0.f,
-                                   2 * t + 1 <= lane ? __uint_as_float(r[2 * t + 1]) : 0.f);
-            } else {  // kept scores weighted by 2^(g_t - g_s)
+            } else {
+              uint32_t r[32];
+              tmem_ld32(base + 32 * q4, r);
+              tmem_ld_wait();
               const float* gk = g + 32 * q4;
+              if (q4 < quad) {
+                const float rf = exp2_ftz(gt - gk[31]);
+                const float* ck = kf + 32 * q4;
 #pragma unroll
-              for (int t = 0; t < 16; ++t) {
-                const bool k0 = q4 < quad || 2 * t <= lane, k1 = q4 < quad || 2 * t + 1 <= lane;
-                const float f0 = exp2_ftz(gt - gk[2 * t]), f1 = exp2_ftz(gt - gk[2 * t + 1]);
-                w[t] = pack_bf16x2(k0 ? __uint_as_float(r[2 * t]) * f0 : 0.f,
-                                   k1 ? __uint_as_float(r[2 * t + 1]) * f1 : 0.f);
+                for (int t = 0; t < 16; ++t)
+                  w[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * rf * ck[2 * t],
+                                     __uint_as_float(r[2 * t + 1]) * rf * ck[2 * t + 1]);
+              } else {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                  const float f0 = exp2_ftz(gt - gk[2 * t]), f1 = exp2_ftz(gt - gk[2 * t + 1]);
+                  w[t] = pack_bf16x2(2 * t <= lane ? __uint_as_float(r[2 * t]) * f0 : 0.f,
+                                     2 * t + 1 <= lane ? __uint_as_float(r[2 * t + 1]) * f1 : 0.f);
+                }
               }
             }
             tmem_st16(base + 16 * q4, w);
+          }
+        } else {
+          // Blocks are loaded two at a time, and a pair is read completely
+          // before its packed columns (which lie in the pair's own or an
+          // earlier block) are written.
+#pragma unroll
+          for (int q2 = 0; q2 < 4; q2 += 2) {
+            uint32_t r0[32], r1[32];
+            if (q2 <= quad) tmem_ld32(base + 32 * q2, r0);
+            if (q2 + 1 <= quad) tmem_ld32(base + 32 * (q2 + 1), r1);
+            if (q2 <= quad) tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int q4 = q2 + h;
+              const uint32_t* r = h ? r1 : r0;
+              uint32_t w[16];
+              if (q4 > quad) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) w[t] = 0u;
+              } else if (q4 < quad) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                  w[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
+              } else {
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                  w[t] = pack_bf16x2(2 * t <= lane ? __uint_as_float(r[2 * t]) : 0.f,
+                                     2 * t + 1 <= lane ? __uint_as_float(r[2 * t + 1]) : 0.f);
+              }
+              tmem_st16(base + 16 * q4, w);
+            }
           }
         }
         tmem_st_wait();
         if (DECAY) {  // the scores have read phi(Q), phi(K): rescale them for the later products
           uint8_t* st = stage_ptr(smem, aj % NS);
-          scale_row(st, row, exp2_ftz(gt));                 // phi(Q) [S | z]: gamma_t
-          scale_row(st + BLK, row, exp2_ftz(g[C - 1] - gt));  // the advance: 2^(g_C - g_t)
+          // phi(Q) [S | z]: gamma_t; the advance: phi(K) by 2^(g_C - g_t)
+#pragma unroll 1
+          for (int m = 0; m < 2; ++m) scale_row(st + m * BLK, row, exp2_ftz(m ? g[C - 1] - gt : gt));
           fence_proxy_async_smem();
         }
         tc_fence_before();
