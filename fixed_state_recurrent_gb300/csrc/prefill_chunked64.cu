@@ -754,7 +754,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           // Q, and in the decayed form K too: one copy of the loop body (the
           // roles' code together must stay within the instruction caches)
 #pragma unroll 1
-          for (int m = 0; m < (DECAY ? 2 : 1); ++m) phi_row<8>(st + m * BLK, r, 0, valid);
+          for (int m = 0; m < (DECAY ? 4 : 2); ++m) phi_row<4>(st + (m / 2) * BLK, r, 4 * (m % 2), valid);
         }
         if (DECAY) {
           // g_t: inclusive sums of log2 alpha over the chunk (alpha = 1 past the
@@ -797,76 +797,50 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const float gt = DECAY ? g[row] : 0.f;
         // this warp's query rows are 32 quad .. +31: key blocks before `quad` are
         // fully visible, block `quad` holds the diagonal, later blocks are zero;
-        // packed keys 32 q4.. go to columns 16 q4..
-        if (DECAY) {
-          // One key block at a time (one copy of the loop body): block q4 is
-          // read completely before its packed columns, which lie in block
-          // q4 / 2 <= q4, are written.  Kept scores are weighted by
-          // 2^(g_t - g_s); for a block before the diagonal that is
-          // 2^(g_t - g_e) 2^(g_e - g_s), g_e the sum at the block's last key:
-          // one exponential per block and row, the key factors from the phi
-          // warps (each factor <= 1 when alpha <= 1).
-          const float* kf = g + GKF;
+        // packed keys 32 q4.. go to columns 16 q4..  One key block at a time
+        // (one copy of the loop body: the roles' code together must stay
+        // within the instruction caches): block q4 is read completely before
+        // its packed columns, which lie in block q4 / 2 <= q4, are written.
+        // Decayed form: kept scores are weighted by 2^(g_t - g_s); for a block
+        // before the diagonal that is 2^(g_t - g_e) 2^(g_e - g_s), g_e the sum
+        // at the block's last key: one exponential per block and row, the key
+        // factors from the phi warps (each factor <= 1 when alpha <= 1).
 #pragma unroll 1
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t w[16];
-            if (q4 > quad) {
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t w[16];
+          if (q4 > quad) {
 #pragma unroll
-              for (int t = 0; t < 16; ++t) w[t] = 0u;
-            } else {
-              uint32_t r[32];
-              tmem_ld32(base + 32 * q4, r);
-              tmem_ld_wait();
-              const float* gk = g + 32 * q4;
-              if (q4 < quad) {
-                const float rf = exp2_ftz(gt - gk[31]);
-                const float* ck = kf + 32 * q4;
+            for (int t = 0; t < 16; ++t) w[t] = 0u;
+          } else {
+            uint32_t r[32];
+            tmem_ld32(base + 32 * q4, r);
+            tmem_ld_wait();
+            if (q4 < quad) {
+              float rf = 1.f;
+              const float* ck = g + GKF + 32 * q4;
+              if (DECAY) rf = exp2_ftz(gt - g[32 * q4 + 31]);
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                  w[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * rf * ck[2 * t],
-                                     __uint_as_float(r[2 * t + 1]) * rf * ck[2 * t + 1]);
-              } else {
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                  const float f0 = exp2_ftz(gt - gk[2 * t]), f1 = exp2_ftz(gt - gk[2 * t + 1]);
-                  w[t] = pack_bf16x2(2 * t <= lane ? __uint_as_float(r[2 * t]) * f0 : 0.f,
-                                     2 * t + 1 <= lane ? __uint_as_float(r[2 * t + 1]) * f1 : 0.f);
+              for (int t = 0; t < 16; ++t) {
+                float a0 = __uint_as_float(r[2 * t]), a1 = __uint_as_float(r[2 * t + 1]);
+                if (DECAY) {
+                  a0 *= rf * ck[2 * t];
+                  a1 *= rf * ck[2 * t + 1];
                 }
+                w[t] = pack_bf16x2(a0, a1);
+              }
+            } else {
+#pragma unroll
+              for (int t = 0; t < 16; ++t) {
+                float a0 = __uint_as_float(r[2 * t]), a1 = __uint_as_float(r[2 * t + 1]);
+                if (DECAY) {
+                  a0 *= exp2_ftz(gt - g[32 * q4 + 2 * t]);
+                  a1 *= exp2_ftz(gt - g[32 * q4 + 2 * t + 1]);
+                }
+                w[t] = pack_bf16x2(2 * t <= lane ? a0 : 0.f, 2 * t + 1 <= lane ? a1 : 0.f);
               }
             }
-            tmem_st16(base + 16 * q4, w);
           }
-        } else {
-          // Blocks are loaded two at a time, and a pair is read completely
-          // before its packed columns (which lie in the pair's own or an
-          // earlier block) are written.
-#pragma unroll
-          for (int q2 = 0; q2 < 4; q2 += 2) {
-            uint32_t r0[32], r1[32];
-            if (q2 <= quad) tmem_ld32(base + 32 * q2, r0);
-            if (q2 + 1 <= quad) tmem_ld32(base + 32 * (q2 + 1), r1);
-            if (q2 <= quad) tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int q4 = q2 + h;
-              const uint32_t* r = h ? r1 : r0;
-              uint32_t w[16];
-              if (q4 > quad) {
-#pragma unroll
-                for (int t = 0; t < 16; ++t) w[t] = 0u;
-              } else if (q4 < quad) {
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                  w[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
-              } else {
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                  w[t] = pack_bf16x2(2 * t <= lane ? __uint_as_float(r[2 * t]) : 0.f,
-                                     2 * t + 1 <= lane ? __uint_as_float(r[2 * t + 1]) : 0.f);
-              }
-              tmem_st16(base + 16 * q4, w);
-            }
-          }
+          tmem_st16(base + 16 * q4, w);
         }
         tmem_st_wait();
         if (DECAY) {  // the scores have read phi(Q), phi(K): rescale them for the later products
