@@ -357,16 +357,21 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       }
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const int s = sj % NS;
+        const int valid = pc.tok1 - (pc.tok0 + c * C);
+        // the decay of this row's token, loaded before the wait for the tiles
+        float av = 1.f;
+        if (DECAY && r < valid) av = __ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + c * C + r);
         const bool got = wait3_warp(x, &B->full[s], (sj / NS) & 1);
         if (!DECAY && !got) continue;
-        const int valid = pc.tok1 - (pc.tok0 + c * C);
-        if (got) phi_row<8>(smem + s * STAGE, r, 0, valid);
+        if (got) {  // half a row per iteration: one small copy of the loop body
+#pragma unroll 1
+          for (int m = 0; m < 2; ++m) phi_row<4>(smem + s * STAGE, r, 4 * m, valid);
+        }
         if (DECAY) {
           // g_r: inclusive sum of log2 alpha over the chunk up to row r; the
           // row's weight is 2^(rem - g_r), the decay over the piece's later tokens
           float la = 0.f;
-          if (got && r < valid)
-            la = __log2f(fmaxf(__ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + c * C + r), kAlphaMin));
+          if (got && r < valid) la = __log2f(fmaxf(av, kAlphaMin));
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) {
             const float y = __shfl_up_sync(0xFFFFFFFFu, la, off);
