@@ -191,6 +191,28 @@ __device__ __forceinline__ void scale_row(uint8_t* tile, int r, float f) {
   for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(tile + sw128_offset(r, i)) = v[i];
 }
 
+// phi_row followed by scale_row on `nchunk` 16-byte chunks of row r from
+// chunk c0, in one pass (the same two roundings to bf16, one shared-memory
+// round trip).
+template <int NCH>
+__device__ __forceinline__ void phi_scale_row(uint8_t* tile, int r, int c0, int valid, float f) {
+  uint4 v[NCH];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) v[i] = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, c0 + i));
+  const uint32_t keep = r < valid ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t y = phi2(w[j]) & keep;
+      w[j] = pack_bf16x2(__uint_as_float(y << 16) * f, __uint_as_float(y & 0xFFFF0000u) * f);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0 + i)) = v[i];
+}
+
 // ===========================================================================
 // K1: piece aggregates
 
@@ -361,17 +383,13 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         // the decay of this row's token, loaded before the wait for the tiles
         float av = 1.f;
         if (DECAY && r < valid) av = __ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + c * C + r);
-        const bool got = wait3_warp(x, &B->full[s], (sj / NS) & 1);
-        if (!DECAY && !got) continue;
-        if (got) {  // half a row per iteration: one small copy of the loop body
-#pragma unroll 1
-          for (int m = 0; m < 2; ++m) phi_row<4>(smem + s * STAGE, r, 4 * m, valid);
-        }
+        // decayed form: the row's weight 2^(rem - g_r), g_r the inclusive sum
+        // of log2 alpha over the chunk up to row r (rem - g_r: the decay over
+        // the piece's later tokens), found before the tiles are waited for;
+        // both named barriers run on every call
+        float wt = 1.f;
         if (DECAY) {
-          // g_r: inclusive sum of log2 alpha over the chunk up to row r; the
-          // row's weight is 2^(rem - g_r), the decay over the piece's later tokens
-          float la = 0.f;
-          if (got && r < valid) la = __log2f(fmaxf(av, kAlphaMin));
+          float la = r < valid ? __log2f(fmaxf(av, kAlphaMin)) : 0.f;
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) {
             const float y = __shfl_up_sync(0xFFFFFFFFu, la, off);
@@ -387,9 +405,16 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             tot += pq;
           }
           named_bar_sync(2, 128);
-          if (got) scale_row(smem + s * STAGE, r, exp2_ftz(rem - g));
+          wt = exp2_ftz(rem - g);
           rem -= tot;
-          if (!got) continue;
+        }
+        const bool got = wait3_warp(x, &B->full[s], (sj / NS) & 1);
+        if (!got) continue;
+        // half a row per iteration: one small copy of the loop body
+#pragma unroll 1
+        for (int m = 0; m < 2; ++m) {
+          if (DECAY) phi_scale_row<4>(smem + s * STAGE, r, 4 * m, valid, wt);
+          else phi_row<4>(smem + s * STAGE, r, 4 * m, valid);
         }
         fence_proxy_async_smem();
         __syncwarp();
