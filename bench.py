@@ -57,7 +57,7 @@ def _args():
                    help="headline workload only (no long/decode/delta/e2e/cpu)")
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run "
-                        "(long,decode,delta,pr1,gated,decay,backward)")
+                        "(long,decode,delta,pr1,gated,decay,backward,prefill128)")
     p.add_argument("--profile-backward", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain la_prefill_backward calls and exit (for ncu)")
     p.add_argument("--profile-decay", type=int, default=0, metavar="CALLS",
@@ -567,7 +567,8 @@ def bench_simple_prefill(api, wname, rank, world, steps=20):
            "ms_per_call": ms, "tokens_per_s": w.tokens / (ms * 1e-3),
            "timing": f"{steps} calls in one CUDA graph, rotating buffer sets"}
     if w.dtype == torch.bfloat16:
-        b = PREFILL_BYTES_PER_TOKEN * w.tokens + w.B * w.H * (w.dk * w.dv + w.dk) * 4
+        per_token = 2 * (w.dk + w.dk + w.dv) + 4 * w.dv  # q, k, v bf16 in, o fp32 out
+        b = per_token * w.tokens + w.B * w.H * (w.dk * w.dv + w.dk) * 4
         res["hbm_gbs"] = b / (ms * 1e-3) / 1e9
         res["hbm_frac"] = b / (ms * 1e-3) / 1e9 / _peaks()[0]
     return res
@@ -746,7 +747,8 @@ def main():
     extra = {}
     e2e = None
     wanted = set(x for x in args.only.split(",") if x) or {"long", "decode", "delta", "pr1",
-                                                             "gated", "decay", "backward"}
+                                                             "gated", "decay", "backward",
+                                                             "prefill128"}
     if not args.no_extra:
         if "long" in wanted:
             extra["long"] = bench_simple_prefill(api, "long", rank, world)
@@ -756,6 +758,8 @@ def main():
             extra["delta"] = bench_delta(api, rank, world)
         if "pr1" in wanted:
             extra["pr1"] = bench_simple_prefill(api, "pr1", rank, world)
+        if "prefill128" in wanted:
+            extra["prefill_d128"] = bench_simple_prefill(api, "prefill128", rank, world)
         if "gated" in wanted:
             extra["gated_delta"] = bench_gated_delta(api, rank, world)
         if "decay" in wanted:
@@ -780,8 +784,9 @@ def main():
                 "launch_ms_mean": launch_ms, "launch_ms_min": min(per)}
     if "decode" in extra:
         extra["decode"]["hbm_frac"] = extra["decode"]["hbm_gbs"] / hbm_peak
-    if "long" in extra and "hbm_gbs" in extra["long"]:
-        extra["long"]["hbm_frac"] = extra["long"]["hbm_gbs"] / hbm_peak
+    for name in ("long", "prefill_d128"):
+        if name in extra and "hbm_gbs" in extra[name]:
+            extra[name]["hbm_frac"] = extra[name]["hbm_gbs"] / hbm_peak
     if "delta" in extra:
         extra["delta"]["hbm_frac"] = extra["delta"]["hbm_gbs"] / hbm_peak
 

@@ -88,6 +88,10 @@ cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, floa
 size_t prefill_decay64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream);
 
+// The same three launches for dk = dv = 128 (prefill_chunked128.cu).
+size_t prefill_chunked128_workspace_bytes(int B, int H, int N);
+cudaError_t launch_prefill_chunked128(const PrefillArgs& a, cudaStream_t stream);
+
 // Tensor-core chunked prefill (bf16, dk = dv in {64, 128}).
 bool prefill_tc_supported(const PrefillArgs& a);
 size_t prefill_tc_workspace_bytes(int B, int H, int N, int d, int chunk);

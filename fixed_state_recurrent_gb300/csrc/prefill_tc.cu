@@ -676,12 +676,12 @@ bool prefill_tc_supported(const PrefillArgs& a) {
 
 size_t prefill_tc_workspace_bytes(int B, int H, int N, int d, int /*chunk*/) {
   if (d == 64) return prefill_chunked64_workspace_bytes(B, H, N);
-  return workspace_bytes(B, H, N, d);
+  return prefill_chunked128_workspace_bytes(B, H, N);
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   if (a.dk == 64) return launch_prefill_chunked64(a, stream);
-  return launch_d<128>(a, stream);
+  return launch_prefill_chunked128(a, stream);
 }
 
 }  // namespace la

@@ -47,7 +47,8 @@ class Workload:
 
 # The five workloads of the hot path.  "pr1" is the small fp32 case, "prefill"
 # and "long" the bf16 prefill cases, "decode" 100 steps after a 1024-token
-# prefix (N is the prefix length), "delta" the delta-rule memory.
+# prefix (N is the prefix length), "delta" the delta-rule memory;
+# "prefill128" is the prefill case at dk = dv = 128.
 WORKLOADS = {
     "pr1": Workload("pr1", 1, 1, 256, 64, 64, torch.float32, 7),
     "prefill": Workload("prefill", 4, 8, 4096, 64, 64, torch.bfloat16, 1),
@@ -55,6 +56,8 @@ WORKLOADS = {
     "decode": Workload("decode", 256, 32, 1024, 128, 128, torch.bfloat16, 3,
                        steps=100),
     "delta": Workload("delta", 8, 16, 8192, 128, 128, torch.bfloat16, 4),
+    # the prefill operator at the wider head size dk = dv = 128
+    "prefill128": Workload("prefill128", 4, 8, 4096, 128, 128, torch.bfloat16, 5),
 }
 
 

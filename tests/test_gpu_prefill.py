@@ -225,12 +225,11 @@ def test_device_status_clean_after_calls(la):
     assert la.read_device_status(ws) == 0  # LA_OK
 
 
-@pytest.mark.parametrize("d,limit_env", [(64, "LA_MBAR_TIMEOUT_NS"), (128, "LA_WAIT_TIMEOUT_NS")],
-                         ids=["chunked_d64", "lookback_d128"])
+@pytest.mark.parametrize("d,limit_env", [(64, "LA_MBAR_TIMEOUT_NS"), (128, "LA_MBAR_TIMEOUT_NS")],
+                         ids=["chunked_d64", "chunked_d128"])
 def test_bounded_wait_reports_timeout(la, orc, monkeypatch, d, limit_env):
     # A test hook makes one wait of the kernel wait on something that nothing
-    # completes (d = 64: an mbarrier of the output kernel; d = 128: an
-    # inter-block flag of the look-back), with a 2 ms limit: the wait gives up,
+    # completes (an mbarrier of the output kernel), with a 2 ms limit: the wait gives up,
     # the kernel drains what it started and finishes, the status word says
     # LA_ERR_TIMEOUT, and the context stays usable.
     q, k, v = _gen(1, 2, 1024, d, d, torch.bfloat16, seed=25)
