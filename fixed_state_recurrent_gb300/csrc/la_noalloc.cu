@@ -13,9 +13,9 @@
 
 namespace {
 
-// 16 MiB of scratch per device: enough for la_prefill's workspace up to about
-// 500 items of 512 tokens at dk = dv = 64 (e.g. B*H = 32 heads of 8192 tokens),
-// or about 120 at dk = dv = 128.
+// 16 MiB of scratch per device: enough for la_prefill's workspace at
+// dk = dv = 64 up to e.g. 8 heads of 4096 tokens, at dk = dv = 128 up to e.g.
+// 4 heads of 2048 tokens.
 constexpr size_t kScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_la_scratch[kScratchBytes];

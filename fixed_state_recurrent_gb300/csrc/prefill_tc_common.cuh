@@ -1,6 +1,6 @@
 // prefill_tc_common.cuh -- pieces shared by the tensor-core prefill kernels:
-// launch parameters, work items, the ELU+1 feature map on packed bf16, the
-// look-back over published item prefixes, and tensor-map creation.
+// the chunk length, the ELU+1 feature map on packed bf16, the work split over
+// the SMs, and tensor-map creation.
 #pragma once
 
 #include <cuda.h>
@@ -15,52 +15,6 @@ namespace la {
 namespace tcp {
 
 constexpr int C = 128;            // chunk length = MMA M = tile rows
-constexpr int kItemTokens = 512;  // tokens per work item (a multiple of C)
-
-// Parameters of one tensor-core prefill launch.
-struct TcParams {
-  int BH, N, items_per_head, total_items;
-  float eps;
-  const float* S0;
-  const float* z0;
-  float* S_N;
-  float* z_N;
-  WsHeader* hdr;
-  unsigned* flags;   // total_items + 1 words (the last is never written)
-  float* agg;        // per item: its own (dS, dz)
-  float* inc;        // per item: S0 + every (dS, dz) of its head up to and including it
-  unsigned long long wait_ns;
-  int force_wait;
-};
-
-// A work item: tokens [tok0, tok1) of head h, window w of that head.
-// Items are numbered window-major: g = w * BH + h.
-struct Item {
-  int h, w, tok0, tok1, nch;
-};
-
-__device__ __forceinline__ Item item_of(const TcParams& p, int g) {
-  Item it;
-  it.h = g % p.BH;
-  it.w = g / p.BH;
-  it.tok0 = it.w * kItemTokens;
-  it.tok1 = min(it.tok0 + kItemTokens, p.N);
-  it.nch = (it.tok1 - it.tok0 + C - 1) / C;
-  return it;
-}
-
-// ELU+1: phi(u) = exp(min(u,0)) + max(u,0), i.e. u + 1 for u > 0 and exp(u)
-// for u <= 0 (page "AIGC 基本功|线性、循环与记忆架构-LinearMem", section 03).
-// The result is rounded to bf16 for the tensor cores, so the fast exp suffices.
-__device__ __forceinline__ float phi_fast(float u) {
-  return __expf(fminf(u, 0.f)) + fmaxf(u, 0.f);
-}
-
-__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x) {
-  const float lo = __uint_as_float(x << 16);
-  const float hi = __uint_as_float(x & 0xFFFF0000u);
-  return tc::pack_bf16x2(phi_fast(lo), phi_fast(hi));
-}
 
 // 2^x by the single-precision hardware approximation, subnormal results
 // flushed to zero (exp(u) < 2^-126 is far below what bf16 sums of phi keep).
@@ -197,54 +151,6 @@ inline int sm_count() {
   return sms;
 }
 
-// Flag word of an item: (generation << 2) | state.
-constexpr unsigned kFlagAggregate = 1u;  // agg[g] is published
-constexpr unsigned kFlagInclusive = 2u;  // inc[g] is published
-
-// Look-back of item `it` (one thread): the window index of the nearest earlier
-// item of the same head whose inclusive prefix is published, or -1 for the
-// first window (whose prefix is S0 itself).  Walks back over windows whose
-// aggregate is published; waits (bounded) where neither is published yet.
-// Window 0 always publishes its inclusive prefix, so the walk ends there at
-// the latest.  On timeout it records LA_ERR_TIMEOUT and returns a window whose
-// published data, if any, is used unchecked (outputs become unspecified).
-__device__ __forceinline__ int lookback_start(const TcParams& p, const Item& it,
-                                              unsigned epoch) {
-  int start = -1;
-  bool timed_out = false;
-  const uint64_t deadline = tc::globaltimer_ns() + p.wait_ns;
-  if (p.force_wait && it.w == 0) {  // test hook: a flag that nothing sets
-    while (!timed_out) {
-      const unsigned v = tc::ld_acquire_gpu(&p.flags[p.total_items]);
-      if ((v >> 2) == epoch && (v & 3u)) break;
-      if (tc::globaltimer_ns() > deadline) timed_out = true;
-      __nanosleep(256);
-    }
-  }
-  for (int ww = it.w - 1; ww >= 0 && !timed_out; --ww) {
-    const unsigned* f = &p.flags[ww * p.BH + it.h];
-    while (true) {
-      const unsigned v = tc::ld_acquire_gpu(f);
-      if ((v >> 2) == epoch && (v & 3u) == kFlagInclusive) {
-        start = ww;
-        break;
-      }
-      if ((v >> 2) == epoch && (v & 3u) == kFlagAggregate && ww > 0) break;  // keep walking
-      if (tc::globaltimer_ns() > deadline) {
-        timed_out = true;
-        break;
-      }
-      __nanosleep(64);
-    }
-    if (start >= 0) break;
-  }
-  if (timed_out) {
-    atomicOr(&p.hdr->status, kStatusTimeout);
-    if (start < 0 && it.w > 0) start = it.w - 1;
-  }
-  return start;
-}
-
 // ---------------------------------------------------------------------------
 // host helpers
 
@@ -277,42 +183,10 @@ inline bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, i
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-inline int items_per_head(int N) { return (N + kItemTokens - 1) / kItemTokens; }
-
 inline unsigned long long env_ull(const char* name, unsigned long long dflt) {
   const char* s = getenv(name);
   if (!s || !*s) return dflt;
   return strtoull(s, nullptr, 10);
-}
-
-// Fills the launch parameters (workspace carving included) for head size d.
-inline TcParams make_params(const PrefillArgs& a, int d) {
-  TcParams p;
-  p.BH = a.B * a.H;
-  p.N = a.N;
-  p.items_per_head = items_per_head(a.N);
-  p.total_items = p.BH * p.items_per_head;
-  p.eps = a.eps;
-  p.S0 = a.S0;
-  p.z0 = a.z0;
-  p.S_N = a.S_N;
-  p.z_N = a.z_N;
-  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  p.hdr = reinterpret_cast<WsHeader*>(ws);
-  const size_t flag_bytes = ((size_t)(p.total_items + 1) * 4 + 255) & ~(size_t)255;
-  p.flags = reinterpret_cast<unsigned*>(ws + sizeof(WsHeader));
-  p.agg = reinterpret_cast<float*>(ws + sizeof(WsHeader) + flag_bytes);
-  p.inc = p.agg + (size_t)p.total_items * ((size_t)d * d + d);
-  p.wait_ns = env_ull("LA_WAIT_TIMEOUT_NS", 1000000000ull);
-  p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
-  return p;
-}
-
-inline size_t workspace_bytes(int B, int H, int N, int d) {
-  const size_t T = (size_t)B * H * items_per_head(N);
-  const size_t flag_bytes = ((T + 1) * 4 + 255) & ~(size_t)255;
-  const size_t sz = (size_t)d * d + d;
-  return flag_bytes + 2 * T * sz * sizeof(float);
 }
 
 }  // namespace tcp

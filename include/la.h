@@ -267,8 +267,10 @@ la_status delta_read_device_status(cudaStream_t stream);
  *   la_prefill rejects.  At dk = dv = 64 the workspace is a bf16 copy of
  *   phi(K) (128 bytes per token) plus two 16.6 KB state slots per pair of
  *   head and block that meet: 8 heads of 4096 tokens fit (13 MB on a 152-SM
- *   GPU), 32 heads of 4096 do not; at dk = dv = 128, 127 items of 512 tokens
- *   (B*H*ceil(N/512) <= 127).  la_prefill_workspace_bytes gives the figure.
+ *   GPU), 32 heads of 4096 do not; at dk = dv = 128 the copy of phi(K) takes
+ *   256 bytes per token and the slots are 66 KB: 4 heads of 2048 tokens fit
+ *   (11 MB), a problem with a chunk of 128 tokens for every SM does not.
+ *   la_prefill_workspace_bytes gives the figure.
  *   Set-up: the first call on each device (with that device current) looks up
  *   the array's device address and zero-fills it synchronously; make that
  *   first call before any stream capture.
