@@ -68,6 +68,8 @@ def _args():
     p.add_argument("--profile", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain (non-graph) prefill calls of the headline workload on "
                         "the same rotating buffer sets and exit: the command profilers run")
+    p.add_argument("--profile-workload", default="prefill", choices=["prefill", "long", "prefill128"],
+                   help="workload that --profile runs (default: the headline prefill)")
     return p.parse_args()
 
 
@@ -737,7 +739,7 @@ def main():
         sampler.stop()
         return
     if args.profile:
-        profile_calls(api, w, args.profile)
+        profile_calls(api, inputs.WORKLOADS[args.profile_workload], args.profile)
         sampler.stop()
         return
     total_ms, per = bench_prefill(api, w, args.steps, args.warmup, rank, world)

@@ -198,9 +198,10 @@ def test_first_step_closed_form(la):
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 8192, 64), (1, 1, 5000, 128), (2, 3, 1537, 64)],
-                         ids=["1head_16items", "1head_d128", "ragged_items"])
-def test_deep_lookback_chains(la, orc, shape):
-    # few heads and many 512-token items: long look-back chains across blocks
+                         ids=["1head_64pieces", "1head_d128", "ragged_pieces"])
+def test_few_heads_many_pieces(la, orc, shape):
+    # few heads over many blocks: each head is cut into many pieces whose entry
+    # states come from the scan over the earlier pieces' totals
     B, H, N, d = shape
     q, k, v = _gen(B, H, N, d, d, torch.bfloat16, seed=21)
     S0, z0 = _state(B, H, d, d, 22)
