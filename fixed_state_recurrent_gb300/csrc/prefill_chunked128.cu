@@ -51,6 +51,35 @@ constexpr uint32_t ID_QS = idesc_bf16_f32(128, 144, 0, 0);  // phi(Q) [S | z_hi 
 constexpr uint32_t ID_PV = idesc_bf16_f32(128, D, 0, 1);    // P V, P in TMEM
 constexpr uint32_t ID_P1 = idesc_bf16_f32(128, 16, 0, 0);   // P 1
 
+// L2 eviction priority for the streams that are touched once: K in the
+// aggregate kernel; Q, phi(K), V and o in the output kernel.  phi(K) and V,
+// written or read by the aggregate kernel and read again by the output
+// kernel, keep the normal priority, so they are the lines L2 holds on to.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_3d_ef(void* dst, const void* tmap, int c0, int c1, int c2,
+                                               uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+      "l"(l2_evict_first())
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d_ef(const void* tmap, const void* src, int c0, int c1,
+                                                int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "l"(l2_evict_first())
+      : "memory");
+}
+
 struct Params {
   Split sp;
   float eps;
@@ -234,8 +263,8 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   auto load_stage = [&](uint32_t s, int tok, int h) {
     uint8_t* st = smem + s * STAGE;
     mbar_arrive_expect_tx(&B->full[s], 2 * TILE);
-    tma_load_3d(st, &tm_k, 0, tok, h, &B->full[s]);
-    tma_load_3d(st + BLK, &tm_k, 64, tok, h, &B->full[s]);
+    tma_load_3d_ef(st, &tm_k, 0, tok, h, &B->full[s]);
+    tma_load_3d_ef(st + BLK, &tm_k, 64, tok, h, &B->full[s]);
     tma_load_3d(st + TILE, &tm_v, 0, tok, h, &B->full[s]);
     tma_load_3d(st + TILE + BLK, &tm_v, 64, tok, h, &B->full[s]);
   };
@@ -517,12 +546,12 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         uint8_t* st = smem + pre * STAGE;
         const int tok = pc.tok0 + c * C;
         mbar_arrive_expect_tx(&B->full[pre], 2 * TILE);
-        tma_load_3d(st + TILE, &tm_v, 0, tok, pc.h, &B->full[pre]);
-        tma_load_3d(st + TILE + BLK, &tm_v, 64, tok, pc.h, &B->full[pre]);
+        tma_load_3d_ef(st + TILE, &tm_v, 0, tok, pc.h, &B->full[pre]);
+        tma_load_3d_ef(st + TILE + BLK, &tm_v, 64, tok, pc.h, &B->full[pre]);
         if (pre == 0) {
           mbar_arrive_expect_tx(&B->qfull, TILE);
-          tma_load_3d(smem + OFF_Q, &tm_q, 0, tok, pc.h, &B->qfull);
-          tma_load_3d(smem + OFF_Q + BLK, &tm_q, 64, tok, pc.h, &B->qfull);
+          tma_load_3d_ef(smem + OFF_Q, &tm_q, 0, tok, pc.h, &B->qfull);
+          tma_load_3d_ef(smem + OFF_Q + BLK, &tm_q, 64, tok, pc.h, &B->qfull);
         }
       }
   }
@@ -554,16 +583,16 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const int tok = pc.tok0 + c * C;
           if (sj < pre) {  // phi(K) is the aggregate kernel's output
             if (sj == 0) pdl_wait();
-            tma_load_3d(st, &tm_k, 0, tok, pc.h, &B->full[s]);
-            tma_load_3d(st + BLK, &tm_k, 64, tok, pc.h, &B->full[s]);
+            tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[s]);
+            tma_load_3d_ef(st + BLK, &tm_k, 64, tok, pc.h, &B->full[s]);
             continue;
           }
           if (!wait_b(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           mbar_arrive_expect_tx(&B->full[s], 2 * TILE);
-          tma_load_3d(st, &tm_k, 0, tok, pc.h, &B->full[s]);
-          tma_load_3d(st + BLK, &tm_k, 64, tok, pc.h, &B->full[s]);
-          tma_load_3d(st + TILE, &tm_v, 0, tok, pc.h, &B->full[s]);
-          tma_load_3d(st + TILE + BLK, &tm_v, 64, tok, pc.h, &B->full[s]);
+          tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d_ef(st + BLK, &tm_k, 64, tok, pc.h, &B->full[s]);
+          tma_load_3d_ef(st + TILE, &tm_v, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d_ef(st + TILE + BLK, &tm_v, 64, tok, pc.h, &B->full[s]);
           ++issued;
         }
       if (*x.abort) drain_ring(B->full, NS, issued, NS, mbar_ns);
@@ -579,8 +608,8 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (!wait_b(x, &B->qempty, (qj - 1) & 1)) break;
           const int tok = pc.tok0 + c * C;
           mbar_arrive_expect_tx(&B->qfull, TILE);
-          tma_load_3d(smem + OFF_Q, &tm_q, 0, tok, pc.h, &B->qfull);
-          tma_load_3d(smem + OFF_Q + BLK, &tm_q, 64, tok, pc.h, &B->qfull);
+          tma_load_3d_ef(smem + OFF_Q, &tm_q, 0, tok, pc.h, &B->qfull);
+          tma_load_3d_ef(smem + OFF_Q + BLK, &tm_q, 64, tok, pc.h, &B->qfull);
           ++issued;
         }
       if (*x.abort) drain_ring(&B->qfull, 1, issued, 1, mbar_ns);
@@ -809,7 +838,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
           if (et == 0 && !*x.abort) {
-            tma_store_3d(&tm_o, out, 32 * q, tok, pc.h);
+            tma_store_3d_ef(&tm_o, out, 32 * q, tok, pc.h);
             bulk_commit();
           }
         }
