@@ -51,35 +51,6 @@ constexpr uint32_t ID_QS = idesc_bf16_f32(128, 144, 0, 0);  // phi(Q) [S | z_hi 
 constexpr uint32_t ID_PV = idesc_bf16_f32(128, D, 0, 1);    // P V, P in TMEM
 constexpr uint32_t ID_P1 = idesc_bf16_f32(128, 16, 0, 0);   // P 1
 
-// L2 eviction priority for the streams that are touched once: K in the
-// aggregate kernel; Q, phi(K), V and o in the output kernel.  phi(K) and V,
-// written or read by the aggregate kernel and read again by the output
-// kernel, keep the normal priority, so they are the lines L2 holds on to.
-__device__ __forceinline__ uint64_t l2_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-__device__ __forceinline__ void tma_load_3d_ef(void* dst, const void* tmap, int c0, int c1, int c2,
-                                               uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
-      "l"(l2_evict_first())
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_store_3d_ef(const void* tmap, const void* src, int c0, int c1,
-                                                int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
-      " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "l"(l2_evict_first())
-      : "memory");
-}
-
 struct Params {
   Split sp;
   float eps;

@@ -281,7 +281,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         uint8_t* st = smem + pre * STAGE;
         const int tok = pc.tok0 + c * C;
         mbar_arrive_expect_tx(&B->full[pre], 2 * BLK);
-        tma_load_3d(st, &tm_k, 0, tok, pc.h, &B->full[pre]);
+        tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[pre]);
         tma_load_3d(st + BLK, &tm_v, 0, tok, pc.h, &B->full[pre]);
       }
   }
@@ -310,7 +310,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           uint8_t* st = smem + s * STAGE;
           const int tok = pc.tok0 + c * C;
           mbar_arrive_expect_tx(&B->full[s], 2 * BLK);
-          tma_load_3d(st, &tm_k, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[s]);
           tma_load_3d(st + BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
           ++issued;
         }
@@ -581,6 +581,10 @@ __device__ __forceinline__ const float* gsums(uint8_t* smem, uint32_t s) {
 
 __device__ __forceinline__ uint8_t* stage_ptr(uint8_t* smem, uint32_t s) { return smem + s * STAGE; }
 
+// Q, phi(K), V and o are touched once by this kernel and go through TMA with
+// the evict-first L2 policy (the aggregate kernel loads K the same way), so
+// that V and phi(K), which both launches read, are what L2 keeps.
+//
 // Two threads issue MMAs.  The MMA warp issues, per chunk a, the scores of
 // chunk a + 1 and then P [V | 1] and phi(Q) [S | z] of chunk a, so that P of
 // chunk a + 1 is built while the products of chunk a run.  The state chain has
@@ -657,9 +661,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         uint8_t* st = stage_ptr(smem, pre);
         const int tok = pc.tok0 + c * C;
         mbar_arrive_expect_tx(&B->full[pre], 3 * BLK);
-        tma_load_3d(st, &tm_q, 0, tok, pc.h, &B->full[pre]);
-        tma_load_3d(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[pre]);
-        if (DECAY) tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[pre]);
+        tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->full[pre]);
+        tma_load_3d_ef(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[pre]);
+        if (DECAY) tma_load_3d_ef(st + BLK, &tm_k, 0, tok, pc.h, &B->full[pre]);
       }
   }
   init_ones(smem + OFF_ONES, threadIdx.x, 32 * kWarps);
@@ -688,15 +692,15 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (sj < pre) {  // Q and V are on their way; phi(K) follows the aggregate kernel
             if (!DECAY) {
               if (sj == 0) pdl_wait();  // phi(K) is the aggregate kernel's output
-              tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
+              tma_load_3d_ef(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
             }
             continue;
           }
           if (!wait3(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           mbar_arrive_expect_tx(&B->full[s], 3 * BLK);
-          tma_load_3d(st, &tm_q, 0, tok, pc.h, &B->full[s]);
-          tma_load_3d(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
-          tma_load_3d(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d_ef(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d_ef(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
           ++issued;
         }
       if (*x.abort) drain_loads<NS>(B->full, issued, mbar_ns);
@@ -1031,8 +1035,8 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         named_bar_sync(1, 128);
         if (et == 32 && !*x.abort) {
           const int tok = pc.tok0 + c * C;
-          tma_store_3d(&tm_o, out, 0, tok, pc.h);
-          tma_store_3d(&tm_o, out + BLK, 32, tok, pc.h);
+          tma_store_3d_ef(&tm_o, out, 0, tok, pc.h);
+          tma_store_3d_ef(&tm_o, out + BLK, 32, tok, pc.h);
           bulk_commit();
         }
       }
