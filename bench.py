@@ -50,7 +50,10 @@ PREFILL_BYTES_PER_TOKEN = 640  # q,k,v bf16 at d=64 (384 B) + o fp32 (256 B)
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default 10000 prefill calls, about 0.3 s of device time, "
+                        "so that the clock samples taken every 100 ms fall inside the timed "
+                        "region; 200 oracle samples for --impl reference)")
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-extra", action="store_true",
@@ -70,7 +73,10 @@ def _args():
                         "the same rotating buffer sets and exit: the command profilers run")
     p.add_argument("--profile-workload", default="prefill", choices=["prefill", "long", "prefill128"],
                    help="workload that --profile runs (default: the headline prefill)")
-    return p.parse_args()
+    args = p.parse_args()
+    if args.steps is None:
+        args.steps = 200 if args.impl == "reference" else 10000
+    return args
 
 
 # --------------------------------------------------------------------------
@@ -187,6 +193,22 @@ def _peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, 1900.0, "fallback"
+
+
+def tensor_fractions(d, chunk, tokens, ms, bf16_peak):
+    """Contraction work of the chunked prefill against the bf16 tensor peak.
+    Per token, with full C x C tiles as executed: scores 2 C d, masked P V
+    2 C d, inter-chunk read 2 d d, state update 2 d d; causal-only counts
+    half of the C x C tiles.  The path is HBM-bound at these sizes, so these
+    fractions are reported beside the HBM roofline, not as the bound."""
+    executed = (4 * chunk * d + 4 * d * d) * tokens
+    causal = (2 * chunk * d + 4 * d * d) * tokens
+    t = ms * 1e-3
+    return {"flop_per_token_executed": 4 * chunk * d + 4 * d * d,
+            "flop_per_token_causal": 2 * chunk * d + 4 * d * d,
+            "tflops_executed": executed / t / 1e12, "tflops_causal": causal / t / 1e12,
+            "frac_executed": executed / t / 1e12 / bf16_peak,
+            "frac_causal": causal / t / 1e12 / bf16_peak, "peak_tflops": bf16_peak}
 
 
 def _kernel_source_hash():
@@ -783,12 +805,16 @@ def main():
                 "frac": achieved / hbm_peak, "traffic": _committed_traffic(w.tokens),
                 "peak_kind": f"of {peak_kind}",
                 "algorithmic_bytes_per_launch": algo_bytes,
-                "launch_ms_mean": launch_ms, "launch_ms_min": min(per)}
+                "launch_ms_mean": launch_ms, "launch_ms_min": min(per),
+                "tensor": tensor_fractions(w.dk, 128, w.tokens, launch_ms, _peaks()[1])}
     if "decode" in extra:
         extra["decode"]["hbm_frac"] = extra["decode"]["hbm_gbs"] / hbm_peak
     for name in ("long", "prefill_d128"):
         if name in extra and "hbm_gbs" in extra[name]:
             extra[name]["hbm_frac"] = extra[name]["hbm_gbs"] / hbm_peak
+            ew = inputs.WORKLOADS["prefill128" if name == "prefill_d128" else name]
+            extra[name]["tensor"] = tensor_fractions(ew.dk, 128, ew.tokens,
+                                                     extra[name]["ms_per_call"], _peaks()[1])
     if "delta" in extra:
         extra["delta"]["hbm_frac"] = extra["delta"]["hbm_gbs"] / hbm_peak
 
