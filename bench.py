@@ -31,7 +31,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -65,6 +64,9 @@ def _args():
                    help="run CALLS plain la_prefill_backward calls and exit (for ncu)")
     p.add_argument("--profile-decay", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain decayed-prefill calls and exit (for ncu)")
+    p.add_argument("--profile-decode", type=int, default=0, metavar="CALLS",
+                   help="run CALLS plain decode steps of the decode workload (B=256 H=32 "
+                        "dk=dv=128, random fp32 state) and exit (for ncu)")
     p.add_argument("--profile-delta", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain delta_prefill calls of the delta workload and exit "
                         "(for profilers)")
@@ -229,18 +231,17 @@ PREFILL_LAUNCHES_PER_CALL = 3
 
 def _committed_traffic(tokens):
     """dram bytes of one la_prefill call (its three kernels) from the committed
-    ncu summary, scaled to `tokens`, or None when the kernel source changed
-    since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "prefill_d64_bf16_ncu.md")
+    ncu counters (profiles/prefill_d64_bf16_ncu.json), scaled to `tokens`, or
+    None when the kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "prefill_d64_bf16_ncu.json")
     try:
-        text = open(path, encoding="utf-8").read()
-    except OSError:
+        with open(path, encoding="utf-8") as f:
+            rec = json.load(f)
+        if rec["kernel_source_sha256"] != _kernel_source_hash():
+            return None
+        return float(rec["dram_bytes_per_token"]) * tokens
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
-    m_b = re.search(r"dram_bytes_per_token:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_b or m_hash.group(1) != _kernel_source_hash():
-        return None
-    return float(m_b.group(1)) * tokens
 
 
 # --------------------------------------------------------------------------
@@ -360,6 +361,26 @@ def profile_delta_calls(api, calls):
         api.delta_prefill(k, v, beta, reads=reads, S_N=S)
     torch.cuda.synchronize()
     print(f"profiled {calls} delta calls", flush=True)
+
+
+def profile_decode_calls(api, calls):
+    """`calls` plain decode steps on the decode workload's shapes (B=256 H=32
+    dk=dv=128, bf16 tokens); the state is random fp32 (the DRAM traffic of a
+    step does not depend on its values), for profilers."""
+    import torch
+    from fixed_state_recurrent_gb300 import inputs
+    w = inputs.WORKLOADS["decode"]
+    dev = torch.device("cuda")
+    B, H, d = w.B, w.H, w.dk
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    S = torch.randn((B, H, d, d), generator=g, device=dev)
+    z = torch.rand((B, H, d), generator=g, device=dev) * 100 + 1
+    qs, ks, vs = inputs.decode_step_inputs(B, H, d, d, calls, torch.bfloat16, w.seed, device=dev)
+    o = torch.empty((B, H, d), device=dev)
+    for t in range(calls):
+        api.decode_step(qs[t], ks[t], vs[t], S, z, o=o)
+    torch.cuda.synchronize()
+    print(f"profiled {calls} decode steps", flush=True)
 
 
 def profile_decay_calls(api, calls, sets=4):
@@ -611,18 +632,18 @@ def bench_e2e(api, w, steps, warmup, rank, world, lanes=2):
     dev = torch.device("cuda")
     q, k, v = inputs.la_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype, w.seed + 1000 * rank)
     hq, hk, hv = (x.pin_memory() for x in (q, k, v))
-    ho = torch.empty((w.B, w.H, w.N, w.dv)).pin_memory()
-    hS = torch.empty((w.B, w.H, w.dk, w.dv)).pin_memory()
-    hz = torch.empty((w.B, w.H, w.dk)).pin_memory()
     need = api.prefill_workspace_bytes(w.B, w.H, w.N, w.dk, w.dv, w.dtype)
     lane_bufs = []
-    for _ in range(lanes):
+    for _ in range(lanes):  # every lane owns its device buffers and its pinned host results
         lane_bufs.append(dict(
             q=torch.empty_like(q, device=dev), k=torch.empty_like(k, device=dev),
             v=torch.empty_like(v, device=dev),
             o=torch.empty((w.B, w.H, w.N, w.dv), device=dev),
             S=torch.empty((w.B, w.H, w.dk, w.dv), device=dev),
             z=torch.empty((w.B, w.H, w.dk), device=dev),
+            ho=torch.empty((w.B, w.H, w.N, w.dv)).pin_memory(),
+            hS=torch.empty((w.B, w.H, w.dk, w.dv)).pin_memory(),
+            hz=torch.empty((w.B, w.H, w.dk)).pin_memory(),
             ws=torch.zeros(need, dtype=torch.uint8, device=dev),
             stream=torch.cuda.Stream()))
     main = torch.cuda.current_stream()
@@ -634,9 +655,9 @@ def bench_e2e(api, w, steps, warmup, rank, world, lanes=2):
             L["k"].copy_(hk, non_blocking=True)
             L["v"].copy_(hv, non_blocking=True)
             api.prefill(L["q"], L["k"], L["v"], o=L["o"], S_N=L["S"], z_N=L["z"], ws=L["ws"])
-            ho.copy_(L["o"], non_blocking=True)
-            hS.copy_(L["S"], non_blocking=True)
-            hz.copy_(L["z"], non_blocking=True)
+            L["ho"].copy_(L["o"], non_blocking=True)
+            L["hS"].copy_(L["S"], non_blocking=True)
+            L["hz"].copy_(L["z"], non_blocking=True)
 
     for i in range(warmup):
         step(i)
@@ -656,7 +677,8 @@ def bench_e2e(api, w, steps, warmup, rank, world, lanes=2):
     _barrier(world)
     total = _max_over_ranks(t0.elapsed_time(t1), world)
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
-    d2h = sum(x.numel() * x.element_size() for x in (ho, hS, hz))
+    L = lane_bufs[0]
+    d2h = sum(x.numel() * x.element_size() for x in (L["ho"], L["hS"], L["hz"]))
     return total, h2d, d2h
 
 
@@ -687,8 +709,8 @@ def cpu_baseline(w, target_s=10.0):
 # --------------------------------------------------------------------------
 
 def run_reference(args):
-    """The reference arm: the fp64 oracle on the host cores, one bounded
-    sample of the prefill workload (8 of its 32 heads) per step."""
+    """The reference arm: the fp64 oracle on the host cores, the whole prefill
+    workload (all 32 heads, threads over the heads) per step."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
@@ -698,7 +720,7 @@ def run_reference(args):
     oracle.build()
     w = inputs.WORKLOADS["prefill"]
     q, k, v = inputs.la_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype, w.seed, w.scale)
-    heads = 8
+    heads = w.B * w.H
     f = lambda t: t.reshape(w.B * w.H, 1, w.N, -1)[:heads].to(torch.float64).numpy()
     q, k, v = f(q), f(k), f(v)
     cores = oracle.default_threads()
@@ -710,14 +732,14 @@ def run_reference(args):
     el = time.perf_counter() - t0
     tokens = heads * w.N * args.steps
     value = tokens / el
-    sample = (f"fp64 C oracle token recurrence, {heads} of the {w.B * w.H} heads "
-              f"x {w.N} tokens of the prefill workload per step")
+    sample = (f"fp64 C oracle token recurrence over the whole prefill workload per step "
+              f"({heads} heads x {w.N} tokens), threads over heads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / max(args.steps, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "prefill: B=4 H=8 N=4096 dk=dv=64 bf16 N(0,1) "
-                                   f"(sample: {heads} heads per step)",
+            "config": {"workload": "prefill: B=4 H=8 N=4096 dk=dv=64, bf16 q,k,v ~ N(0,1), "
+                                   "fp32 state/accumulate, zero initial state",
                        "B": w.B, "H": w.H, "N": w.N, "dk": w.dk, "dv": w.dv},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
@@ -756,6 +778,10 @@ def main():
         profile_decay_calls(api, args.profile_decay)
         sampler.stop()
         return
+    if args.profile_decode:
+        profile_decode_calls(api, args.profile_decode)
+        sampler.stop()
+        return
     if args.profile_delta:
         profile_delta_calls(api, args.profile_delta)
         sampler.stop()
@@ -790,8 +816,8 @@ def main():
             extra["decay_prefill"] = bench_decay_prefill(api, rank, world)
         if "backward" in wanted:
             extra["backward"] = bench_backward(api, rank, world)
-        e_ms, h2d, d2h = bench_e2e(api, w, max(args.steps // 4, 5), 3, rank, world)
-        e_steps = max(args.steps // 4, 5)
+        e_steps = min(max(args.steps // 4, 20), 200)  # at least 20 steps whatever --steps is
+        e_ms, h2d, d2h = bench_e2e(api, w, e_steps, 3, rank, world)
         e2e = {"value": w.tokens * world / (e_ms * 1e-3 / e_steps), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": e_steps}

@@ -17,8 +17,8 @@
 // work is 4 dk dv flops per token of fp32 FMA: this path is bound by the FP32
 // pipe, not by HBM.
 //
-// Gated form (same page, section 03, "再引入遗忘系数 alpha_t", and its appendix
-// delta_step): the old state decays first, D = alpha_t S_{t-1}; the read is
+// Gated form (same page, section 03, the forgetting factor alpha_t, and its
+// appendix delta_step): the old state decays first, D = alpha_t S_{t-1}; the read is
 // the prediction from D, k_t^T D = alpha_t (k_t^T S_{t-1}); the correction is
 // written on top of D: S_t = D + beta_t k_t (v_t - k_t^T D)^T.  alpha = NULL
 // is the plain rule above.

@@ -106,6 +106,19 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
                      const float* S0, const float* z0, float* o, float* S_N,
                      float* z_N, int chunk, void* workspace, size_t ws_bytes,
                      cudaStream_t stream) {
+  return la::prefill_entry(q, k, v, in_dtype, B, H, N, dk, dv, eps, S0, z0, o, S_N, z_N, chunk,
+                           workspace, ws_bytes, nullptr, stream);
+}
+
+}  // extern "C"
+
+// la_prefill's validation and launch; `status` is where the tensor-core
+// kernels record a bounded wait that gave up (NULL: the workspace header).
+la_status la::prefill_entry(const void* q, const void* k, const void* v, la_dtype in_dtype,
+                            int B, int H, int N, int dk, int dv, float eps, const float* S0,
+                            const float* z0, float* o, float* S_N, float* z_N, int chunk,
+                            void* workspace, size_t ws_bytes, unsigned* status,
+                            cudaStream_t stream) {
   if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return LA_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
   if (chunk != 0 && chunk != 128) return LA_ERR_INVALID_ARG;
@@ -145,7 +158,7 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
     return from_cuda(e);
   }
 
-  PrefillArgs a;
+  PrefillArgs a = {};
   a.q = q; a.k = k; a.v = v;
   a.bf16 = in_dtype == LA_BF16;
   a.B = B; a.H = H; a.N = N; a.dk = dk; a.dv = dv;
@@ -155,10 +168,13 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
   a.chunk = chunk == 0 ? 128 : chunk;
   a.workspace = workspace;
   a.ws_bytes = ws_bytes;
+  a.status = status;
   if (use_tensor_path(in_dtype, dk, dv) && la::prefill_tc_supported(a))
     return from_cuda(la::launch_prefill_tc(a, stream));
   return from_cuda(la::launch_prefill_simt(a, stream));
 }
+
+extern "C" {
 
 la_status la_decode_step(const void* q, const void* k, const void* v, la_dtype in_dtype,
                          int B, int H, int dk, int dv, float eps, float* S,
@@ -244,7 +260,7 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
     if (e == cudaSuccess) e = copy_state(z0, z_N, heads * dk * 4, stream);
     return from_cuda(e);
   }
-  PrefillArgs a;
+  PrefillArgs a = {};
   a.q = q; a.k = k; a.v = v;
   a.bf16 = in_dtype == LA_BF16;
   a.B = B; a.H = H; a.N = N; a.dk = dk; a.dv = dv;
@@ -309,7 +325,7 @@ la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dt
     if (e == cudaSuccess && dz0) e = copy_state(dz_N, dz0, heads * dk * 4, stream);
     return from_cuda(e);
   }
-  PrefillArgs a;
+  PrefillArgs a = {};
   a.q = q; a.k = k; a.v = v;
   a.bf16 = in_dtype == LA_BF16;
   a.B = B; a.H = H; a.N = N; a.dk = dk; a.dv = dv;

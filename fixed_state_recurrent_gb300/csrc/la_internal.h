@@ -7,17 +7,18 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include "la.h"
+
 namespace la {
 
 // Workspace header: the first 256 bytes of every prefill workspace.
-//   status  sticky error bits set by kernels (kStatusTimeout)
-//   epoch   generation counter of the tensor-core prefill's inter-block flags
-//   done    blocks of the running tensor-core launch that have finished
+//   status  sticky error bits set by kernels (kStatusTimeout); it must be zero
+//           before the workspace's first use, and la_read_device_status
+//           clears it.  Nothing else in a workspace is read before the call
+//           that uses it has written it.
 struct WsHeader {
   unsigned status;
-  unsigned epoch;
-  unsigned done;
-  unsigned reserved[61];
+  unsigned reserved[63];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -39,7 +40,16 @@ struct PrefillArgs {
   int chunk;
   void* workspace;
   size_t ws_bytes;
+  unsigned* status;  // where the tensor-core kernels record errors; NULL = the workspace header's word
 };
+
+// la_prefill's argument checks, path choice and launches, with the status
+// word of the tensor-core kernels given explicitly (NULL: the workspace
+// header's word, as la_prefill does).
+la_status prefill_entry(const void* q, const void* k, const void* v, la_dtype in_dtype, int B,
+                        int H, int N, int dk, int dv, float eps, const float* S0, const float* z0,
+                        float* o, float* S_N, float* z_N, int chunk, void* workspace,
+                        size_t ws_bytes, unsigned* status, cudaStream_t stream);
 
 // CUDA-core prefill (any dk, dv <= 128; fp32 or bf16 inputs).
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);

@@ -11,6 +11,9 @@
 #include "la.h"
 #include "la_internal.h"
 
+#include <atomic>
+#include <mutex>
+
 namespace {
 
 // 16 MiB of scratch per device: enough for la_prefill's workspace at
@@ -21,22 +24,36 @@ constexpr size_t kScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_la_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices];  // device address of g_la_scratch, per device
 
-// One-time set-up on the current device: look up the device address of the
-// scratch array (its host-side name is only a stand-in) and zero it, since
-// la_prefill expects a zero-filled workspace on first use.
-la_status scratch_for_current_device(void** out) {
+// Per device: the device address of g_la_scratch (its host-side name is only
+// a stand-in) and of the library status word, looked up once with that device
+// current.  Published with release order after both are known, so a thread
+// that sees the scratch address also sees the status address.
+std::atomic<void*> g_scratch_ptr[kMaxDevices];
+unsigned* g_status_ptr[kMaxDevices];
+std::mutex g_setup_mutex;
+
+// The scratch needs no initialisation: the kernels write every part of it
+// before reading it, and their error bits go to the library status word, not
+// into the scratch.  So the set-up issues no device work at all.
+la_status scratch_for_current_device(void** scratch, unsigned** status) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return LA_ERR_UNSUPPORTED;
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_la_scratch) != cudaSuccess || !ptr) return LA_ERR_CUDA;
-    if (cudaMemset(ptr, 0, kScratchBytes) != cudaSuccess) return LA_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
+  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      unsigned* st = nullptr;
+      if (cudaGetSymbolAddress(&p, g_la_scratch) != cudaSuccess || !p) return LA_ERR_CUDA;
+      if (la::library_status_word(&st) != cudaSuccess || !st) return LA_ERR_CUDA;
+      g_status_ptr[dev] = st;
+      g_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = g_scratch_ptr[dev];
+  *scratch = p;
+  *status = g_status_ptr[dev];
   return LA_OK;
 }
 
@@ -49,8 +66,9 @@ extern "C" la_status la_prefill_noalloc(const void* q, const void* k, const void
   const size_t need = la_prefill_workspace_bytes(B, H, N, dk, dv, in_dtype, chunk);
   if (need == 0 || need > kScratchBytes) return LA_ERR_INVALID_ARG;
   void* scratch = nullptr;
-  const la_status st = scratch_for_current_device(&scratch);
+  unsigned* status = nullptr;
+  const la_status st = scratch_for_current_device(&scratch, &status);
   if (st != LA_OK) return st;
-  return la_prefill(q, k, v, in_dtype, B, H, N, dk, dv, eps, S0, z0, o, S_N, z_N, chunk,
-                    scratch, kScratchBytes, stream);
+  return la::prefill_entry(q, k, v, in_dtype, B, H, N, dk, dv, eps, S0, z0, o, S_N, z_N, chunk,
+                           scratch, kScratchBytes, status, stream);
 }

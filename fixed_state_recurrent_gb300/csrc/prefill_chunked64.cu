@@ -1156,7 +1156,7 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   p.S_N = a.S_N;
   p.z_N = a.z_N;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  p.status = &reinterpret_cast<WsHeader*>(ws)->status;
+  p.status = a.status ? a.status : &reinterpret_cast<WsHeader*>(ws)->status;
   p.alpha = nullptr;
   p.gam = nullptr;
   const size_t slots = (size_t)BH * p.sp.MPH;

@@ -79,9 +79,12 @@ typedef enum {
  *   chunk       chunk length of the tensor-core path; 0 = automatic (128).
  *               The CUDA-core path ignores it.
  *   workspace   device scratch of at least la_prefill_workspace_bytes(...)
- *               bytes, ZERO-FILLED before its first use; the kernels leave it
- *               ready for the next call.  Calls that share a workspace must be
- *               ordered on one stream.  It also holds the device status word.
+ *               bytes.  Its first 256 bytes hold the device status word and
+ *               must be zero before the workspace's first use (one
+ *               cudaMemset after allocating it; la_read_device_status clears
+ *               the word again); the rest need not be initialised, as every
+ *               call writes what it reads.  Calls that share a workspace must
+ *               be ordered on one stream.
  */
 la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dtype,
                      int B, int H, int N, int dk, int dv, float eps,
@@ -212,7 +215,7 @@ la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const f
 
 /*
  * gated_delta_prefill -- the delta rule with forgetting (LinearMem section 03,
- * "再引入遗忘系数 alpha_t", and the appendix delta_step): per token the old
+ * the forgetting factor alpha_t, and the appendix delta_step): per token the old
  * memory decays first, then the correction uses the decayed prediction:
  *   D = alpha_t S_{t-1};  reads[t] = k_t^T D;  S_t = D + beta_t k_t (v_t - reads[t])^T
  *   alpha [B][H][N] float32, or NULL (alpha_t = 1: exactly delta_prefill).
@@ -244,7 +247,7 @@ la_status la_read_device_status(const void* workspace, cudaStream_t stream);
  * tensor-core kernels whose calls take no workspace: delta_prefill and
  * gated_delta_prefill with bf16 inputs at dk = dv = 128, la_prefill_variant
  * with a decay and la_prefill_backward on bf16 inputs at dk = dv = 64 (also
- * when they are given a workspace).  LA_ERR_TIMEOUT if one of their
+ * when they are given a workspace), and la_prefill_noalloc.  LA_ERR_TIMEOUT if one of their
  * bounded waits gave up since the last read, otherwise LA_OK; LA_ERR_CUDA if
  * the synchronization or copy fails.  The word belongs to the current device
  * and is shared by every such call on it; the token-by-token kernels have no
@@ -272,13 +275,16 @@ la_status delta_read_device_status(cudaStream_t stream);
  *   (11 MB), a problem with a chunk of 128 tokens for every SM does not.
  *   la_prefill_workspace_bytes gives the figure.
  *   Set-up: the first call on each device (with that device current) looks up
- *   the array's device address and zero-fills it synchronously; make that
- *   first call before any stream capture.
- *   Sharing: every call on a device uses the same array and the kernels leave
- *   it ready for the next call; calls whose executions overlap on the GPU
- *   (different streams, no ordering) race on it and must not be issued.
- *   Status: bounded-wait timeouts are recorded in that shared array and cannot
- *   be read back through la_read_device_status.
+ *   the device addresses of the array and of the library's status word; it
+ *   issues no device work, and concurrent first calls from several host
+ *   threads are safe.  Make that first call before any stream capture.
+ *   Contents: the array needs no initialisation; every call writes what it
+ *   reads, and it keeps the last call's contents.
+ *   Sharing: every call on a device uses the same array; calls whose
+ *   executions overlap on the GPU (different streams, no ordering) race on it
+ *   and must not be issued.
+ *   Status: a bounded wait that gave up is recorded in the library status
+ *   word, read back and cleared by delta_read_device_status.
  */
 la_status la_prefill_noalloc(const void* q, const void* k, const void* v, la_dtype in_dtype,
                              int B, int H, int N, int dk, int dv, float eps,

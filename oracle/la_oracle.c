@@ -380,7 +380,7 @@ int orc_delta(const double* k, const double* v, const double* beta, int B,
 }
 
 /* ------------------------------------------------------------------------ */
-/* (7) Gated delta rule, P1 section 03 ("再引入遗忘系数 alpha_t"), the same
+/* (7) Gated delta rule, P1 section 03 (the forgetting factor alpha_t), the same
  * page's appendix delta_step(S, k, v, beta, alpha): first decay the old state,
  * then correct against the decayed prediction:
  *   D = alpha_t S_{t-1};  reads[t] = k_t^T D;  S_t = D + beta_t k_t (v_t - reads[t])^T.
