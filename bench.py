@@ -216,7 +216,7 @@ def tensor_fractions(d, chunk, tokens, ms, bf16_peak):
 def _kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fixed_state_recurrent_gb300", "csrc")
-    for name in ("prefill_chunked64.cu", "prefill_tc_common.cuh", "tc_primitives.cuh"):
+    for name in ("prefill_prefix64.cu", "prefill_tc_common.cuh", "tc_primitives.cuh"):
         p = os.path.join(csrc, name)
         if os.path.exists(p):
             with open(p, "rb") as f:
@@ -225,12 +225,12 @@ def _kernel_source_hash():
 
 
 # Kernel launches per la_prefill call on the headline workload: the d = 64
-# tensor-core path runs the aggregate, scan and output kernels.
-PREFILL_LAUNCHES_PER_CALL = 3
+# tensor-core path runs the prefix and output kernels.
+PREFILL_LAUNCHES_PER_CALL = 2
 
 
 def _committed_traffic(tokens):
-    """dram bytes of one la_prefill call (its three kernels) from the committed
+    """dram bytes of one la_prefill call (its two kernels) from the committed
     ncu counters (profiles/prefill_d64_bf16_ncu.json), scaled to `tokens`, or
     None when the kernel sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "prefill_d64_bf16_ncu.json")

@@ -98,6 +98,14 @@ cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, floa
 size_t prefill_decay64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream);
 
+// Two-launch form for dk = dv = 64 (prefill_prefix64.cu): per-chunk prefix
+// tiles and piece totals, then the outputs.  Chosen by the tensor-core
+// dispatch for calls small enough that what the second launch reads again
+// stays in L2.
+bool prefill_prefix64_chosen(int B, int H, int N);
+size_t prefill_prefix64_workspace_bytes(int B, int H, int N);
+cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream);
+
 // The same three launches for dk = dv = 128 (prefill_chunked128.cu).
 size_t prefill_chunked128_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_chunked128(const PrefillArgs& a, cudaStream_t stream);
