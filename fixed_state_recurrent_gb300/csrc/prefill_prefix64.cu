@@ -422,16 +422,18 @@ static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0 && OFF_V % 1024 == 0 && OFF
               OFF_OUT % 1024 == 0 && OFF_ONES % 1024 == 0, "swizzled tile alignment");
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 // 0 TMA, 1 MMA, 2-9 phi(Q) and the mask, 10-13 output epilogue; 2-14 build
-// the entry state first, 10-14 then store the final states (14 then has
-// nothing left to do)
+// the entry state and store the final states first (14 then has nothing left
+// to do)
 constexpr int kWarps = 15;
 constexpr uint32_t kCols = 512;
-constexpr uint32_t TB = 256;   // buffer b at 256 b: scores then P (128 columns),
-constexpr uint32_t TOO = 128;  //   then [num | den] (80 columns) at +128,
-constexpr uint32_t TQ = 208;   //   then phi(Q) of the chunk (bf16 pairs, 32 columns) at +208
+constexpr uint32_t TB = 208;   // buffer b at 208 b: scores then P (128 columns),
+constexpr uint32_t TOO = 128;  //   then [num | den] (80 columns) at +128
+constexpr uint32_t TQ = 416;   // phi(Q) of chunk j (bf16 pairs, 32 columns) at 416 + 32 (j % 3)
 
 struct Bars {
-  uint64_t full[NS], xf[NS];
+  uint64_t qfull[NS];   // Q loaded                              (TMA -> phi warps)
+  uint64_t full[NS];    // phi(K), P, V loaded                   (TMA -> MMA)
+  uint64_t xf[NS];      // phi(Q) in TMEM: eight warps           (phi warps -> MMA)
   uint64_t empty[NS];   // the stage's products done             (MMA -> TMA)
   uint64_t accB[2];     // scores and state part in buffer b     (MMA -> mask)
   uint64_t pready[2];   // P in buffer b: eight warps            (mask -> MMA)
@@ -447,33 +449,42 @@ static_assert(sizeof(Bars) <= 512, "barrier area");
 
 // The entry state E of the block's first piece: the sum, in order, of the
 // totals of the head's earlier blocks (which already hold S0), as a bf16 tile
-// in shared memory (left zero when there are none).  Thread t of nthr, after
-// the earlier launch's results are visible; each thread keeps twelve loads in
-// flight.
-__device__ __forceinline__ void build_entry(const Params& p, const Run& run, uint8_t* et, int t,
-                                            int nthr) {
+// in shared memory (left zero when there are none).  If that piece also ends
+// its head, E plus the piece's own total is its final state, which goes to T
+// ([64][65] fp32, transposed) and z_N.  Thread t of nthr, after the earlier
+// launch's results are visible; each thread keeps up to fifteen loads in
+// flight.  Returns whether T holds a final state.
+__device__ __forceinline__ bool build_entry(const Params& p, const Run& run, uint8_t* et, float* T,
+                                            int t, int nthr) {
   Piece pc;
-  if (run.idx0 == 0 || !run.piece(p.sp, 0, &pc)) return;
+  if (!run.piece(p.sp, 0, &pc)) return false;
   const int npred = run.idx0;
+  const bool last = pc.tok1 == p.sp.N;
+  if (npred == 0 && !last) return false;
   const float4* Rh = reinterpret_cast<const float4*>(p.R + (size_t)pc.h * p.sp.MPH * SZ);
+  const int nsum = npred + (last ? 1 : 0);  // slots read: the earlier blocks, then the own total
   for (int f0 = t; f0 < SZ / 4; f0 += 3 * nthr) {  // float4 f: slot row f / 16, columns 4 (f % 16)..
-    float4 e[3];
+    float4 e[3], fin[3];
 #pragma unroll
-    for (int u = 0; u < 3; ++u) e[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < npred; k0 += 4) {
-      float4 r[3][4];
+    for (int u = 0; u < 3; ++u) e[u] = fin[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < nsum; k0 += 5) {
+      float4 r[3][5];
 #pragma unroll
       for (int u = 0; u < 3; ++u)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          r[u][kk] = (f0 + u * nthr < SZ / 4 && k0 + kk < npred)
+        for (int kk = 0; kk < 5; ++kk)
+          r[u][kk] = (f0 + u * nthr < SZ / 4 && k0 + kk < nsum)
                          ? __ldcg(Rh + (size_t)(k0 + kk) * (SZ / 4) + f0 + u * nthr)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int u = 0; u < 3; ++u)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          e[u].x += r[u][kk].x; e[u].y += r[u][kk].y; e[u].z += r[u][kk].z; e[u].w += r[u][kk].w;
+        for (int kk = 0; kk < 5; ++kk) {
+          if (k0 + kk < npred) {
+            e[u].x += r[u][kk].x; e[u].y += r[u][kk].y; e[u].z += r[u][kk].z; e[u].w += r[u][kk].w;
+          } else if (k0 + kk == npred) {  // the own total (only when the head ends here)
+            fin[u] = r[u][kk];
+          }
         }
     }
 #pragma unroll
@@ -481,61 +492,68 @@ __device__ __forceinline__ void build_entry(const Params& p, const Run& run, uin
       const int f = f0 + u * nthr;
       if (f >= SZ / 4) continue;
       const int row = f / 16, col = 4 * (f % 16);
-      uint2 hi;
-      hi.x = pack_bf16x2(e[u].x, e[u].y);
-      hi.y = pack_bf16x2(e[u].z, e[u].w);
-      if (row < D) {
-        *reinterpret_cast<uint2*>(et + sw128_offset(row, col / 8) + (col % 8) * 2) = hi;
-      } else {  // z: hi in row 64, lo in row 65
-        uint2 lo;
-        lo.x = pack_bf16x2(e[u].x - __uint_as_float(hi.x << 16), e[u].y - __uint_as_float(hi.x & 0xFFFF0000u));
-        lo.y = pack_bf16x2(e[u].z - __uint_as_float(hi.y << 16), e[u].w - __uint_as_float(hi.y & 0xFFFF0000u));
-        *reinterpret_cast<uint2*>(et + sw128_offset(64, col / 8) + (col % 8) * 2) = hi;
-        *reinterpret_cast<uint2*>(et + sw128_offset(65, col / 8) + (col % 8) * 2) = lo;
+      if (npred > 0) {
+        uint2 hi;
+        hi.x = pack_bf16x2(e[u].x, e[u].y);
+        hi.y = pack_bf16x2(e[u].z, e[u].w);
+        if (row < D) {
+          *reinterpret_cast<uint2*>(et + sw128_offset(row, col / 8) + (col % 8) * 2) = hi;
+        } else {  // z: hi in row 64, lo in row 65
+          uint2 lo;
+          lo.x = pack_bf16x2(e[u].x - __uint_as_float(hi.x << 16), e[u].y - __uint_as_float(hi.x & 0xFFFF0000u));
+          lo.y = pack_bf16x2(e[u].z - __uint_as_float(hi.y << 16), e[u].w - __uint_as_float(hi.y & 0xFFFF0000u));
+          *reinterpret_cast<uint2*>(et + sw128_offset(64, col / 8) + (col % 8) * 2) = hi;
+          *reinterpret_cast<uint2*>(et + sw128_offset(65, col / 8) + (col % 8) * 2) = lo;
+        }
+      }
+      if (last) {
+        const float4 v = make_float4(e[u].x + fin[u].x, e[u].y + fin[u].y, e[u].z + fin[u].z, e[u].w + fin[u].w);
+        if (row < D) {
+          T[(col + 0) * (D + 1) + row] = v.x;
+          T[(col + 1) * (D + 1) + row] = v.y;
+          T[(col + 2) * (D + 1) + row] = v.z;
+          T[(col + 3) * (D + 1) + row] = v.w;
+        } else {
+          reinterpret_cast<float4*>(p.z_N + (size_t)pc.h * D)[col / 4] = v;
+        }
       }
     }
   }
+  return last;
 }
 
-// The final state of every head whose last chunk is in this block: the sum of
-// all its blocks' totals (those of the earlier blocks, then the piece's own),
-// transposed through shared memory (T: [64][65] fp32) so that the stores of
-// S_N are whole rows.  Threads t of nthr (a named barrier `bar` of them).
-__device__ __forceinline__ void store_final(const Params& p, const Run& run, float* T, int t, int nthr,
-                                            int bar) {
+// S_N of head h from T (written by the same nthr threads before a barrier).
+__device__ __forceinline__ void store_S_from_T(const Params& p, int h, const float* T, int t, int nthr) {
+  for (int g = t; g < D * D / 4; g += nthr) {  // S_N[i][4 g' ..], i = g / 16
+    const int ii = g / 16, j0 = 4 * (g % 16);
+    const float* src = T + ii * (D + 1) + j0;
+    reinterpret_cast<float4*>(p.S_N + (size_t)h * D * D)[g] = make_float4(src[0], src[1], src[2], src[3]);
+  }
+}
+
+// The final states of the heads that start and end in this block (pieces
+// after the first): their own totals, through T like the first piece's.
+// Threads t of nthr, a named barrier `bar` of them.
+__device__ __forceinline__ void store_final_later(const Params& p, const Run& run, float* T, int t,
+                                                  int nthr, int bar) {
   Piece pc;
-  for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+  for (int i = 1; run.piece(p.sp, i, &pc); ++i) {
     if (pc.tok1 != p.sp.N) continue;
-    const int nslots = (i == 0 ? run.idx0 : 0) + 1;
-    const float4* Rh = reinterpret_cast<const float4*>(p.R + (size_t)pc.h * p.sp.MPH * SZ);
-    for (int f = t; f < SZ / 4; f += nthr) {  // float4 f: slot row f / 16, columns 4 (f % 16)..
-      float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k0 = 0; k0 < nslots; k0 += 4) {
-        float4 r[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          r[kk] = k0 + kk < nslots ? __ldcg(Rh + (size_t)(k0 + kk) * (SZ / 4) + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          e.x += r[kk].x; e.y += r[kk].y; e.z += r[kk].z; e.w += r[kk].w;
-        }
-      }
+    const float4* Rs = reinterpret_cast<const float4*>(p.R + (size_t)pc.slot * SZ);
+    for (int f = t; f < SZ / 4; f += nthr) {
+      const float4 v = __ldcg(Rs + f);
       const int row = f / 16, col = 4 * (f % 16);
       if (row < D) {
-        T[(col + 0) * (D + 1) + row] = e.x;
-        T[(col + 1) * (D + 1) + row] = e.y;
-        T[(col + 2) * (D + 1) + row] = e.z;
-        T[(col + 3) * (D + 1) + row] = e.w;
+        T[(col + 0) * (D + 1) + row] = v.x;
+        T[(col + 1) * (D + 1) + row] = v.y;
+        T[(col + 2) * (D + 1) + row] = v.z;
+        T[(col + 3) * (D + 1) + row] = v.w;
       } else {
-        reinterpret_cast<float4*>(p.z_N + (size_t)pc.h * D)[col / 4] = e;
+        reinterpret_cast<float4*>(p.z_N + (size_t)pc.h * D)[col / 4] = v;
       }
     }
     named_bar_sync(bar, nthr);
-    for (int g = t; g < D * D / 4; g += nthr) {  // S_N[i][4 g' ..], i = g / 16
-      const int ii = g / 16, j0 = 4 * (g % 16);
-      const float* src = T + ii * (D + 1) + j0;
-      reinterpret_cast<float4*>(p.S_N + (size_t)pc.h * D * D)[g] = make_float4(src[0], src[1], src[2], src[3]);
-    }
+    store_S_from_T(p, pc.h, T, t, nthr);
     named_bar_sync(bar, nthr);  // T is free again
   }
 }
@@ -559,6 +577,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   if (threadIdx.x == 0) LA_TRACE(2, 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
+      mbar_init(&B->qfull[s], 1);
       mbar_init(&B->full[s], 1);
       mbar_init(&B->xf[s], 8);
       mbar_init(&B->empty[s], 1);
@@ -581,8 +600,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     tma_prefetch_desc(&tm_o);
   }
   // The first stages' Q and V (inputs of the call) go out before the earlier
-  // launch has finished; each stage's barrier expects all four tiles, so
-  // phi(K) and P join it once they may be read.
+  // launch has finished, so that phi(Q) of the first chunks is ready when it
+  // is; each stage's `full` expects V, phi(K) and P, so phi(K) and P join it
+  // once they may be read.
   int pre = 0;
   if (threadIdx.x == 0) {
     Piece pc;
@@ -590,8 +610,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int c = 0; pre < NS && c < pc.nch; ++c, ++pre) {
         uint8_t* st = smem + pre * STAGE;
         const int tok = pc.tok0 + c * C;
-        mbar_arrive_expect_tx(&B->full[pre], 3 * BLK + XG);
-        tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->full[pre]);
+        mbar_arrive_expect_tx(&B->qfull[pre], BLK);
+        tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->qfull[pre]);
+        mbar_arrive_expect_tx(&B->full[pre], 2 * BLK + XG);
         tma_load_3d_ef(st + OFF_V, &tm_v, 0, tok, pc.h, &B->full[pre]);
       }
   }
@@ -614,14 +635,27 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   tc_fence_after();
   const Ctx x{p.status, &B->abort, *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
 
-  if (warp >= 2) {  // the entry-state tile, needed by the first products
-    pdl_wait();      // the piece totals of the earlier launch are complete
-    build_entry(p, run, smem + OFF_E, threadIdx.x - 64, 32 * (kWarps - 2));
+  // The entry-state tile, needed by the first products, and the final states:
+  // warps 2..14, the phi warps once the first chunks' phi(Q) is in TMEM.
+  auto entry_part = [&]() {
+    pdl_wait();  // the piece totals of the earlier launch are complete
+    const int t = threadIdx.x - 64, nthr = 32 * (kWarps - 2);
+    if (t == 0) LA_TRACE(1, 0);
+    float* T = reinterpret_cast<float*>(smem + OFF_OUT);  // the output staging, free until the epilogue
+    const bool last = build_entry(p, run, smem + OFF_E, T, t, nthr);
+    if (t == 0) LA_TRACE(1, 1);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&B->eready);
-    if (threadIdx.x == 64) LA_TRACE(1, 2);
-  }
+    if (last) {
+      Piece pc;
+      run.piece(p.sp, 0, &pc);
+      named_bar_sync(6, nthr);
+      store_S_from_T(p, pc.h, T, t, nthr);
+      named_bar_sync(6, nthr);
+    }
+    store_final_later(p, run, T, t, nthr, 6);
+  };
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer
@@ -647,14 +681,18 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (!waitb(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           uint8_t* st = smem + s * STAGE;
           const int tok = pc.tok0 + c * C;
-          mbar_arrive_expect_tx(&B->full[s], 3 * BLK + XG);
-          tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->full[s]);
+          mbar_arrive_expect_tx(&B->qfull[s], BLK);
+          tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->qfull[s]);
+          mbar_arrive_expect_tx(&B->full[s], 2 * BLK + XG);
           tma_load_3d_ef(st + OFF_K, &tm_phik, 0, tok, pc.h, &B->full[s]);
           tma_load_3d_ef(st + OFF_P, &tm_p, 0, 0, (int)(run.a + sj), &B->full[s]);
           tma_load_3d_ef(st + OFF_V, &tm_v, 0, tok, pc.h, &B->full[s]);
           ++issued;
         }
-      if (*x.abort) drain_loads<NS>(B->full, issued, mbar_ns);
+      if (*x.abort) {
+        drain_loads<NS>(B->qfull, issued, mbar_ns);
+        drain_loads<NS>(B->full, issued, mbar_ns);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -663,9 +701,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       // O += phi(Q) E^T for the chunks of a first piece that has earlier
       // blocks, then O += P [V | 1].  Jobs in whichever order they become
       // ready (the products of chunk ap first): the first products of a need
-      // phi(Q) of a (and the stage), and buffer a % 2 read by the epilogue of
-      // a - 2 (which implies that the products of a - 2, the last readers of
-      // that buffer's P, are done); the products need P of a.
+      // phi(Q) of a, the stage's other tiles, and buffer a % 2 read by the
+      // epilogue of a - 2 (which implies that the products of a - 2, the last
+      // readers of that buffer's P, are done); the products need P of a.
       const uint32_t tm = x.tmem;
       const uint32_t aOnes = smem_u32(smem + OFF_ONES);
       const uint64_t e0 = sdesc_sw128(smem_u32(smem + OFF_E), 16, 1024);
@@ -693,12 +731,13 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           ++ap;
           did = true;
         } else if (as < n && as < ap + 2 && mbar_test_wait(&B->xf[as % NS], (as / NS) & 1) &&
+                   mbar_test_wait(&B->full[as % NS], (as / NS) & 1) &&
                    (as < 2 || mbar_test_wait(&B->ofree[as % 2], ((as / 2) - 1) & 1))) {
           tc_fence_after();
           const uint32_t a = as;
           if (a < 16) LA_TRACE(3, a);
           const uint32_t st = smem_u32(smem + (a % NS) * STAGE);
-          const uint32_t dA = tm + TB * (a % 2), aQ = dA + TQ;
+          const uint32_t dA = tm + TB * (a % 2), aQ = tm + TQ + 32 * (a % 3);
           const uint64_t b0 = sdesc_sw128(st + OFF_K, 16, 1024);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)  // phi(Q) from TMEM, [phi(K) ; P] from shared memory
@@ -732,10 +771,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   } else if (warp < 10) {
     // ---- two jobs per chunk, in whichever order they become ready (a mask
     // before a phi when both are), each mask after its chunk's phi:
-    //   phi(j): phi(Q) into TMEM (buffer j % 2), the A operand of the chunk's
+    //   phi(j): phi(Q) into TMEM (buffer j % 3), the A operand of the chunk's
     //     first products: the two warps of a lane quadrant take half a row
-    //     each (after mask(j - 2), whose products were the last to read the
-    //     buffer);
+    //     each (after mask(j - 3): the first products of j - 3, the last to
+    //     read the buffer, are complete once their scores are);
     //   mask(j): the causal mask P of the scores, bf16, in place in TMEM.  The
     //     mask of a TMEM lane quadrant is split over its two warps (warp w
     //     reaches lanes 32 (w % 4)..+31): the warp of the first half builds key
@@ -747,7 +786,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
     auto prep_step = [&](uint32_t j) {
       const int s = j % NS;
-      if (!waitb_warp(x, &B->full[s], (j / NS) & 1)) return;
+      if (!waitb_warp(x, &B->qfull[s], (j / NS) & 1)) return;
       const long long gc = run.a + j;
       const int valid = p.sp.N - (int)(gc % p.sp.NC) * C;
       if (cw == 0 && lane == 0 && j < 6) LA_TRACE(2, 4 + j);
@@ -765,7 +804,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         w[4 * i + 2] = phi2(v[i].z) & keep;
         w[4 * i + 3] = phi2(v[i].w) & keep;
       }
-      tmem_st16(tl + TB * (j % 2) + TQ + 16 * half, w);
+      tmem_st16(tl + TQ + 32 * (j % 3) + 16 * half, w);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -821,6 +860,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     };
     const uint32_t n = (uint32_t)total;
     uint32_t jp = 0, jm = 0, idle = 0;
+    // phi(Q) of the first chunks (one per phi(Q) buffer) needs only Q: before
+    // the earlier launch has finished
+    for (; jp < n && jp < 3; ++jp) prep_step(jp);
+    entry_part();
     uint64_t dl = globaltimer_ns() + x.mbar_ns;
     while (jp < n || jm < n) {
       if (*x.abort) {  // given up: the remaining masks still meet their pair barriers
@@ -831,8 +874,8 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (jm < jp && __shfl_sync(0xFFFFFFFFu, (int)mbar_test_wait(&B->accB[jm % 2], (jm / 2) & 1), 0)) {
         mask_step(jm++);
         did = true;
-      } else if (jp < n && jm + 1 >= jp &&  // mask(jp - 2) done: its products read buffer jp % 2
-                 __shfl_sync(0xFFFFFFFFu, (int)mbar_test_wait(&B->full[jp % NS], (jp / NS) & 1), 0)) {
+      } else if (jp < n && jm + 2 >= jp &&  // mask(jp - 3) done: phi(Q) buffer jp % 3 is free
+                 __shfl_sync(0xFFFFFFFFu, (int)mbar_test_wait(&B->qfull[jp % NS], (jp / NS) & 1), 0)) {
         prep_step(jp++);
         did = true;
       }
@@ -848,11 +891,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
     }
   } else {
-    // ---- the final states (warps 10..14), then the output epilogue (warps
-    // 10..13), o = num / (den + eps) (den = the hi and lo columns of z plus
-    // the ones column), staged in shared memory and stored by TMA (thread 352)
-    // (the output staging is free until the first epilogue, on these warps)
-    store_final(p, run, reinterpret_cast<float*>(smem + OFF_OUT), threadIdx.x - 320, 32 * (kWarps - 10), 6);
+    entry_part();
+    // ---- the output epilogue (warps 10..13), o = num / (den + eps) (den =
+    // the hi and lo columns of z plus the ones column), staged in shared
+    // memory and stored by TMA (thread 352)
     if (warp < 14) {
       const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 320;
       const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
