@@ -120,12 +120,13 @@ def test_long_config_full(la, orc):
     _check(la, orc, q, k, v)
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_prefill_workspace_needs_only_its_status_word_zeroed(la, orc, d):
+@pytest.mark.parametrize("d,B,H,N", [(64, 2, 5, 3000), (64, 1, 4, 51200), (128, 2, 5, 3000)],
+                         ids=["prefix_d64", "three_launch_d64", "chunked_d128"])
+def test_prefill_workspace_needs_only_its_status_word_zeroed(la, orc, d, B, H, N):
     # Only the 256-byte header (the status word) of a workspace must be zero
     # before its first use; the rest may hold anything (NaN here), because
-    # every call writes what it reads.
-    B, H, N = 2, 5, 3000
+    # every call writes what it reads (both d = 64 forms: the two-launch one
+    # up to 1536 chunks, the three-launch one above).
     q, k, v = _gen(B, H, N, d, d, torch.bfloat16, seed=26)
     S0, z0 = _state(B, H, d, d, 27)
     need = la.prefill_workspace_bytes(B, H, N, d, d)
@@ -133,6 +134,20 @@ def test_prefill_workspace_needs_only_its_status_word_zeroed(la, orc, d):
     ws[:256] = 0
     o, S, z = la.prefill(q.cuda(), k.cuda(), v.cuda(), S0=S0.cuda(), z0=z0.cuda(), ws=ws)
     assert la.read_device_status(ws) == 0
+    ro, rS, rz = orc.la_recurrent(f64(q), f64(k), f64(v), S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16 and relmax(f64(z), rz) <= TOL_BF16
+
+
+@pytest.mark.parametrize("N", [16384, 16385], ids=["1536_chunks", "1548_chunks"])
+def test_d64_forms_either_side_of_the_l2_limit(la, orc, N):
+    # 12 heads of 16384 tokens are 1536 chunks, the most the two-launch form
+    # takes; one more token per head (a one-token last chunk) takes the
+    # three-launch form.  Both against the oracle, with an initial state.
+    B, H, d = 1, 12, 64
+    q, k, v = _gen(B, H, N, d, d, torch.bfloat16, seed=28)
+    S0, z0 = _state(B, H, d, d, 29)
+    o, S, z = la.prefill(q.cuda(), k.cuda(), v.cuda(), S0=S0.cuda(), z0=z0.cuda())
     ro, rS, rz = orc.la_recurrent(f64(q), f64(k), f64(v), S0=f64(S0), z0=f64(z0))
     assert relmax(f64(o), ro) <= TOL_BF16
     assert relmax(f64(S), rS) <= TOL_BF16 and relmax(f64(z), rz) <= TOL_BF16
@@ -234,23 +249,25 @@ def test_device_status_clean_after_calls(la):
     assert la.read_device_status(ws) == 0  # LA_OK
 
 
-@pytest.mark.parametrize("d,limit_env", [(64, "LA_MBAR_TIMEOUT_NS"), (128, "LA_MBAR_TIMEOUT_NS")],
-                         ids=["chunked_d64", "chunked_d128"])
-def test_bounded_wait_reports_timeout(la, orc, monkeypatch, d, limit_env):
+# d = 64 calls of up to 1536 chunks take the two-launch form (prefix tiles,
+# outputs), larger ones the three launches (aggregate, scan, outputs)
+@pytest.mark.parametrize("d,H,N", [(64, 2, 1024), (64, 4, 51200), (128, 2, 1024)],
+                         ids=["prefix_d64", "three_launch_d64", "chunked_d128"])
+def test_bounded_wait_reports_timeout(la, orc, monkeypatch, d, H, N):
     # A test hook makes one wait of the kernel wait on something that nothing
     # completes (an mbarrier of the output kernel), with a 2 ms limit: the wait gives up,
     # the kernel drains what it started and finishes, the status word says
     # LA_ERR_TIMEOUT, and the context stays usable.
-    q, k, v = _gen(1, 2, 1024, d, d, torch.bfloat16, seed=25)
-    ws = torch.zeros(la.prefill_workspace_bytes(1, 2, 1024, d, d), dtype=torch.uint8,
+    q, k, v = _gen(1, H, N, d, d, torch.bfloat16, seed=25)
+    ws = torch.zeros(la.prefill_workspace_bytes(1, H, N, d, d), dtype=torch.uint8,
                      device="cuda")
     monkeypatch.setenv("LA_TEST_FORCE_WAIT", "1")
-    monkeypatch.setenv(limit_env, "2000000")
+    monkeypatch.setenv("LA_MBAR_TIMEOUT_NS", "2000000")
     la.prefill(q.cuda(), k.cuda(), v.cuda(), ws=ws)
     assert la.read_device_status(ws) == 4  # LA_ERR_TIMEOUT
     assert la.read_device_status(ws) == 0  # reading clears it
     monkeypatch.delenv("LA_TEST_FORCE_WAIT")
-    monkeypatch.delenv(limit_env)
+    monkeypatch.delenv("LA_MBAR_TIMEOUT_NS")
     o, S, z = la.prefill(q.cuda(), k.cuda(), v.cuda(), ws=ws)
     assert la.read_device_status(ws) == 0
     ro, rS, rz = orc.la_recurrent(f64(q), f64(k), f64(v))
