@@ -98,6 +98,8 @@ size_t la_prefill_workspace_bytes(int B, int H, int N, int dk, int dv,
   size_t bytes = sizeof(la::WsHeader);
   if (use_tensor_path(in_dtype, dk, dv))
     bytes += la::prefill_tc_workspace_bytes(B, H, N, dk, chunk);
+  else
+    bytes += la::prefill_simt_workspace_bytes(B, H, N, dk, dv);
   return bytes;
 }
 
@@ -171,6 +173,9 @@ la_status la::prefill_entry(const void* q, const void* k, const void* v, la_dtyp
   a.status = status;
   if (use_tensor_path(in_dtype, dk, dv) && la::prefill_tc_supported(a))
     return from_cuda(la::launch_prefill_tc(a, stream));
+  // the CUDA-core path's chunk slots follow the workspace header
+  a.workspace = static_cast<uint8_t*>(workspace) + sizeof(la::WsHeader);
+  a.ws_bytes = ws_bytes - sizeof(la::WsHeader);
   return from_cuda(la::launch_prefill_simt(a, stream));
 }
 
@@ -209,7 +214,7 @@ size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv, l
     return 0;
   if (decay && mode == LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 64 && dv == 64 && N > 0)
     return la::prefill_decay64_workspace_bytes(B, H, N);
-  return 0;
+  return la::prefill_simt_workspace_bytes(B, H, N, dk, dv);
 }
 
 la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dtype in_dtype,

@@ -51,7 +51,11 @@ la_status prefill_entry(const void* q, const void* k, const void* v, la_dtype in
                         float* o, float* S_N, float* z_N, int chunk, void* workspace,
                         size_t ws_bytes, unsigned* status, cudaStream_t stream);
 
-// CUDA-core prefill (any dk, dv <= 128; fp32 or bf16 inputs).
+// CUDA-core prefill (any dk, dv <= 128; fp32 or bf16 inputs).  With a
+// workspace of at least prefill_simt_workspace_bytes (nonzero when the heads'
+// sequences are worth cutting into chunks) the chunks run in parallel (three
+// launches); without one, one block walks each head.
+size_t prefill_simt_workspace_bytes(int B, int H, int N, int dk, int dv);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 // The CUDA-core kernel's variants: alpha = per-token decay of (S, z) or NULL;
 // mode 0 write-then-read, 1 read-then-write (strictly past), 2 non-causal

@@ -77,7 +77,12 @@ typedef enum {
  *   S0, z0      initial state or NULL; S_N may alias S0, z_N may alias z0
  *   o, S_N, z_N outputs, float32
  *   chunk       chunk length of the tensor-core path; 0 = automatic (128).
- *               The CUDA-core path ignores it.
+ *               The CUDA-core path (LA_F32, or dk, dv outside the
+ *               tensor-core sizes) picks its own chunks: with the workspace
+ *               la_prefill_workspace_bytes asks for, each head's sequence is
+ *               cut into up to 64 chunks run in parallel (their increments,
+ *               a scan of the states between them in chunk order, their
+ *               outputs, all in fp32).
  *   workspace   device scratch of at least la_prefill_workspace_bytes(...)
  *               bytes.  Its first 256 bytes hold the device status word and
  *               must be zero before the workspace's first use (one
@@ -95,7 +100,7 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
 
 /*
  * la_prefill_variant -- la_prefill's recurrence with a per-token decay of the
- * old state and a choice of read order (no workspace):
+ * old state and a choice of read order:
  *   S_t = alpha_t S_{t-1} + phi(k_t) v_t^T,   z_t = alpha_t z_{t-1} + phi(k_t)
  * (the linear-attention recurrence with one scalar on the old state: page
  * "线性注意力与SSM", sections 3-4, Mamba-2; the normalizer decays with S), and
@@ -120,9 +125,12 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  * heads are split over every SM (decayed piece totals, then the chained
  * scan E' = Gamma E + R, then the outputs); with NULL, one block per head.  A
  * bounded wait of those kernels that gives up is reported by
- * delta_read_device_status.  Everything else runs on the CUDA cores in fp32
- * (one block per head, no workspace needed), for LA_F32 and LA_BF16 inputs
- * and any dk, dv <= 128.
+ * delta_read_device_status.  Everything else runs on the CUDA cores in fp32,
+ * for LA_F32 and LA_BF16 inputs and any dk, dv <= 128: with a workspace of
+ * la_prefill_variant_workspace_bytes, each head's sequence in up to 64
+ * chunks run in parallel (as la_prefill's CUDA-core path; the chunks' decayed
+ * increments and total decays chained as E' = gamma E + R); with NULL, one
+ * block per head, token by token.
  */
 la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dtype in_dtype,
                              int B, int H, int N, int dk, int dv, float eps,
@@ -133,7 +141,8 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
 
 /* Bytes of workspace la_prefill_variant uses for these arguments (decay:
  * nonzero when alpha is given); 0 when it uses none, or for invalid
- * arguments.  The figure depends on the SM count of the current device. */
+ * arguments.  The figure of the tensor-core decayed form depends on the SM
+ * count of the current device. */
 size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv,
                                           la_dtype in_dtype, la_mode mode, int decay);
 

@@ -148,14 +148,21 @@ def test_prefill_variant_rejects_invalid_arguments(lib, kw):
 
 
 def test_prefill_variant_workspace_bytes(lib):
-    # bf16 at d = 64 with a decay, write then read: the split over the SMs needs
-    # slots; every other form needs none
+    # bf16 at d = 64 with a decay, write then read: the tensor-core split over
+    # the SMs; every other form the CUDA-core chunk slots (dk dv + dk + 1 floats
+    # per chunk), when its heads are few enough to be worth cutting
     assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 0, 1) > 0
-    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 0, 0) == 0
-    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 0, 0, 1) == 0
-    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 1, 1) == 0
-    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 128, 128, 1, 0, 1) == 0
+    slots = 32 * 10 * (64 * 64 + 64 + 1) * 4  # 32 heads: 10 chunks each fill ~2 blocks per SM
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 0, 0) == slots
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 0, 0, 1) == slots
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 1, 1) == slots
+    assert lib.la_prefill_variant_workspace_bytes(1, 1, 256, 64, 64, 0, 2, 0) == 32 * (64 * 64 + 64 + 1) * 4
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 128, 128, 1, 0, 1) > 0
+    assert lib.la_prefill_variant_workspace_bytes(1, 1, 8, 64, 64, 0, 0, 0) == 0   # one chunk
+    assert lib.la_prefill_variant_workspace_bytes(8, 64, 4096, 64, 64, 0, 0, 0) == 0  # 512 heads
     assert lib.la_prefill_variant_workspace_bytes(0, 8, 4096, 64, 64, 1, 0, 1) == 0
+    # la_prefill's CUDA-core path: the same slots after the 256-byte header
+    assert lib.la_prefill_workspace_bytes(1, 1, 256, 64, 64, 0, 0) == 256 + 32 * (64 * 64 + 64 + 1) * 4
     # the backward splits its heads over the SMs only on the tensor-core form
     assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 1) > 0
     assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 0) == 0

@@ -76,7 +76,10 @@ VAR_SHAPES = [(1, 1, 1, 4, 3), (2, 3, 37, 5, 3), (1, 2, 100, 64, 64), (1, 2, 129
 @pytest.mark.parametrize("mode,decay", [(0, True), (1, False), (1, True), (2, False)],
                          ids=["causal_decay", "rbw", "rbw_decay", "noncausal"])
 @pytest.mark.parametrize("shape", VAR_SHAPES, ids=[str(s) for s in VAR_SHAPES])
-def test_prefill_variant_matches_oracle(la, orc, dtype, mode, decay, shape):
+@pytest.mark.parametrize("ws", [None, False], ids=["chunks", "whole_heads"])
+def test_prefill_variant_matches_oracle(la, orc, dtype, mode, decay, shape, ws):
+    # with a workspace (the binding's cached scratch) the CUDA-core path runs
+    # each head in parallel chunks; without one, one block walks each head
     from fixed_state_recurrent_gb300 import inputs
     B, H, N, dk, dv = shape
     q, k, v = inputs.la_inputs(B, H, N, dk, dv, dtype, seed=100 + N)
@@ -86,7 +89,7 @@ def test_prefill_variant_matches_oracle(la, orc, dtype, mode, decay, shape):
     z0 = torch.rand((B, H, dk), generator=g) + 0.5
     o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(),
                                  None if alpha is None else alpha.cuda(), mode,
-                                 S0=S0.cuda(), z0=z0.cuda())
+                                 S0=S0.cuda(), z0=z0.cuda(), ws=ws)
     ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), None if alpha is None else f64(alpha),
                                 mode, S0=f64(S0), z0=f64(z0))
     tol = tol_for(dtype)
