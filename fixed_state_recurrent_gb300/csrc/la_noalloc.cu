@@ -17,7 +17,7 @@
 namespace {
 
 // 16 MiB of scratch per device: enough for la_prefill's workspace at
-// dk = dv = 64 up to e.g. 8 heads of 4096 tokens, at dk = dv = 128 up to e.g.
+// dk = dv = 64 up to e.g. 16 heads of 4096 tokens, at dk = dv = 128 up to e.g.
 // 4 heads of 2048 tokens.
 constexpr size_t kScratchBytes = size_t(16) << 20;
 

@@ -277,12 +277,14 @@ la_status delta_read_device_status(cudaStream_t stream);
  *   Limit: requests whose la_prefill_workspace_bytes(...) exceeds 16 MiB
  *   (16777216 bytes) are rejected with LA_ERR_INVALID_ARG, as are arguments
  *   la_prefill rejects.  At dk = dv = 64 the workspace is a bf16 copy of
- *   phi(K) (128 bytes per token) plus two 16.6 KB state slots per pair of
- *   head and block that meet: 8 heads of 4096 tokens fit (13 MB on a 152-SM
- *   GPU), 32 heads of 4096 do not; at dk = dv = 128 the copy of phi(K) takes
- *   256 bytes per token and the slots are 66 KB: 4 heads of 2048 tokens fit
- *   (11 MB), a problem with a chunk of 128 tokens for every SM does not.
- *   la_prefill_workspace_bytes gives the figure.
+ *   phi(K) (128 bytes per token), an 8.4 KB prefix tile per 128-token chunk
+ *   and a 16.6 KB state slot per pair of head and block that meet: 8 heads of
+ *   4096 tokens fit (10.3 MiB on a 152-SM GPU), 16 heads of 4096 just fit
+ *   (15.2 MiB), 32 do not; at dk = dv = 128 the copy of phi(K) takes 256
+ *   bytes per token and the slots are 66 KB: 4 heads of 2048 tokens fit
+ *   (10.6 MiB), 8 do not.  The CUDA-core path's chunk slots take
+ *   (dk dv + dk + 1) * 4 bytes per chunk (1.2 MiB for 2 heads of 300 tokens
+ *   at d = 64).  la_prefill_workspace_bytes gives the figure.
  *   Set-up: the first call on each device (with that device current) looks up
  *   the device addresses of the array and of the library's status word; it
  *   issues no device work, and concurrent first calls from several host
