@@ -273,13 +273,27 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     tma_prefetch_desc(&tm_phik);
   }
   const Run run(p.sp, blockIdx.x);
+  // The plain form walks its run backwards (last piece and last chunk first),
+  // so that the phi(K) and V it touches last -- those of its first chunks,
+  // which the output kernel reads first -- are the ones L2 still holds when
+  // that kernel starts (on calls too large for L2 to hold them all).  The
+  // decayed form walks forwards: its weights run to each piece's end.
+  const int npieces = DECAY ? 0 : run.count(p.sp);
+  auto walk = [&](int i, Piece* pc) -> bool {
+    if (!DECAY) {
+      if (i >= npieces) return false;
+      i = npieces - 1 - i;
+    }
+    return run.piece(p.sp, i, pc);
+  };
+  auto chunk_of = [&](const Piece& pc, int c) { return DECAY ? c : pc.nch - 1 - c; };
   uint32_t pre = 0;  // loads issued during the set-up (thread 0)
   if (threadIdx.x == 0) {  // the first stages' loads go out before the rest of the set-up
     Piece pc;
-    for (int i = 0; pre < NS && run.piece(p.sp, i, &pc); ++i)
+    for (int i = 0; pre < NS && walk(i, &pc); ++i)
       for (int c = 0; pre < NS && c < pc.nch; ++c, ++pre) {
         uint8_t* st = smem + pre * STAGE;
-        const int tok = pc.tok0 + c * C;
+        const int tok = pc.tok0 + chunk_of(pc, c) * C;
         mbar_arrive_expect_tx(&B->full[pre], 2 * BLK);
         tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[pre]);
         tma_load_3d(st + BLK, &tm_v, 0, tok, pc.h, &B->full[pre]);
@@ -302,13 +316,13 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (lane == 0) {  // ---- TMA producer: K, V chunk tiles (the first `pre` went out above)
       uint32_t sj = 0, issued = pre;
       Piece pc;
-      for (int i = 0; run.piece(p.sp, i, &pc); ++i)
+      for (int i = 0; walk(i, &pc); ++i)
         for (int c = 0; c < pc.nch; ++c, ++sj) {
           const int s = sj % NS;
           if (sj < pre) continue;
           if (sj >= NS && !wait3(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           uint8_t* st = smem + s * STAGE;
-          const int tok = pc.tok0 + c * C;
+          const int tok = pc.tok0 + chunk_of(pc, c) * C;
           mbar_arrive_expect_tx(&B->full[s], 2 * BLK);
           tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[s]);
           tma_load_3d(st + BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
@@ -322,7 +336,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       const uint32_t aOnes = smem_u32(smem + OFF_ONES);
       uint32_t sj = 0;
       Piece pc;
-      for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+      for (int i = 0; walk(i, &pc); ++i) {
         const int b = i % 2;
         if (i >= 2 && !wait3(x, &B->rfree[b], ((i / 2) - 1) & 1)) break;
         for (int c = 0; c < pc.nch; ++c, ++sj) {
@@ -363,7 +377,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       named_bar_sync(2, 128);
       return tot;
     };
-    for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+    for (int i = 0; walk(i, &pc); ++i) {
       float rem = 0.f;  // decayed form: log2 of the decay from the chunk's start to the piece's end
       if (DECAY) {
         const float* al = p.alpha + (size_t)pc.h * p.sp.N;
@@ -379,10 +393,10 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       }
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const int s = sj % NS;
-        const int valid = pc.tok1 - (pc.tok0 + c * C);
+        const int valid = pc.tok1 - (pc.tok0 + chunk_of(pc, c) * C);
         // the decay of this row's token, loaded before the wait for the tiles
         float av = 1.f;
-        if (DECAY && r < valid) av = __ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + c * C + r);
+        if (DECAY && r < valid) av = __ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + chunk_of(pc, c) * C + r);
         // decayed form: the row's weight 2^(rem - g_r), g_r the inclusive sum
         // of log2 alpha over the chunk up to row r (rem - g_r: the decay over
         // the piece's later tokens), found before the tiles are waited for;
@@ -426,14 +440,14 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
     uint32_t sj = 0;
     Piece pc;
-    for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+    for (int i = 0; walk(i, &pc); ++i) {
       if (!DECAY && et == 0) {  // phi(K) of the piece's chunks -> workspace; a stage is
                                 // released once the store of the chunk after it was
                                 // issued and its own store has read shared memory
         for (int c = 0; c < pc.nch; ++c, ++sj) {
           const int s = sj % NS;
           if (!wait3(x, &B->xf[s], (sj / NS) & 1)) continue;
-          tma_store_3d(&tm_phik, smem + s * STAGE, 0, pc.tok0 + c * C, pc.h);
+          tma_store_3d(&tm_phik, smem + s * STAGE, 0, pc.tok0 + chunk_of(pc, c) * C, pc.h);
           bulk_commit();
           if (sj > 0) {
             bulk_wait_read_but_one();

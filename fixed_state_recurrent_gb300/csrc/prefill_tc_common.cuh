@@ -105,6 +105,13 @@ struct Run {
     h0 = (int)(a / s.NC);
     idx0 = j - s.owner((long long)h0 * s.NC);
   }
+  // Number of pieces.
+  __host__ __device__ int count(const Split& s) const {
+    int n = 0;
+    Piece pc;
+    while (piece(s, n, &pc)) ++n;
+    return n;
+  }
   // The i-th piece (pieces are ordered by position); false when there are
   // fewer.  Every piece after the first starts its head, so its slot index
   // within the head is 0.
