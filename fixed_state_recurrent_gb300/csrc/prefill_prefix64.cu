@@ -218,6 +218,10 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   }
   uint32_t pre = 0;  // loads issued during the set-up (thread 0)
   if (threadIdx.x == 0) {
+    // This launch is a programmatic dependent of whatever ran before it on
+    // the stream (so that its set-up overlaps that kernel's last blocks): no
+    // global memory is touched before the wait.
+    pdl_wait();
     Piece pc;
     for (int i = 0; pre < NS && run.piece(p.sp, i, &pc); ++i)
       for (int c = 0; pre < NS && c < pc.nch; ++c, ++pre) {
@@ -239,6 +243,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   tc_fence_after();
   const Ctx x{p.status, &B->abort, *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
   pdl_launch_dependents();  // the output kernel may be scheduled now; it waits for this grid's results
+  pdl_wait();               // (see thread 0's loads above)
   if (threadIdx.x == 0) LA_TRACE(0, 1);
 
   if (warp == 0) {
@@ -633,6 +638,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();  // a following launch may set up while this one runs
   const Ctx x{p.status, &B->abort, *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
 
   // The entry-state tile, needed by the first products, and the final states:
@@ -1001,12 +1007,9 @@ cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(out::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)out::SMEM);
   if (e != cudaSuccess) return e;
-  pfx::prefix_kernel<<<p.sp.G, 32 * pfx::kWarps, pfx::SMEM, stream>>>(mk, mv, mphik, mp, p, mbar_ns);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // The output kernel is a programmatic dependent: its blocks may start while
-  // the prefix kernel runs, and wait for its results (griddepcontrol.wait)
-  // only where they read them.
+  // Both launches are programmatic dependents of what precedes them on the
+  // stream: their blocks may start while the kernel before runs, and wait for
+  // it (griddepcontrol.wait) before touching what it may write.
   cudaLaunchAttribute pdl;
   pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl.val.programmaticStreamSerializationAllowed = 1;
@@ -1014,6 +1017,11 @@ cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = &pdl;
   cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * pfx::kWarps);
+  cfg.dynamicSmemBytes = pfx::SMEM;
+  e = cudaLaunchKernelEx(&cfg, pfx::prefix_kernel, mk, mv, mphik, mp, p, mbar_ns);
+  if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * out::kWarps);
   cfg.dynamicSmemBytes = out::SMEM;
