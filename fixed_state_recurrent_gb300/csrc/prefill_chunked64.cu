@@ -289,6 +289,9 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   auto chunk_of = [&](const Piece& pc, int c) { return DECAY ? c : pc.nch - 1 - c; };
   uint32_t pre = 0;  // loads issued during the set-up (thread 0)
   if (threadIdx.x == 0) {  // the first stages' loads go out before the rest of the set-up
+    // a programmatic dependent of what ran before it on the stream (its
+    // set-up overlaps that kernel's last blocks): no global memory before the wait
+    pdl_wait();
     Piece pc;
     for (int i = 0; pre < NS && walk(i, &pc); ++i)
       for (int c = 0; pre < NS && c < pc.nch; ++c, ++pre) {
@@ -311,6 +314,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   const Ctx3 x{&p, smem, reinterpret_cast<uint64_t*>(B), &B->abort,
                *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
   pdl_launch_dependents();  // the scan may be scheduled now; it waits for this grid's results
+  pdl_wait();               // (see thread 0's first loads)
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer: K, V chunk tiles (the first `pre` went out above)
@@ -691,6 +695,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();  // a following launch may set up while this one runs
   const Ctx3 x{&p, smem, reinterpret_cast<uint64_t*>(B), &B->abort,
                *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
 
@@ -1191,12 +1196,9 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
     e = cudaFuncSetAttribute(k3::output_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)k3::SMEM);
   if (e != cudaSuccess) return e;
-  k1::aggregate_kernel<false><<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mphik, p, mbar_ns);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // The scan and the output kernel are launched as programmatic dependents:
-  // their blocks may start while the kernel before them runs, and wait for
-  // its results (griddepcontrol.wait) only where they read them.
+  // All three launches are programmatic dependents of what precedes them on
+  // the stream: their blocks may start while the kernel before them runs, and
+  // wait for it (griddepcontrol.wait) before touching what it may write.
   cudaLaunchAttribute pdl;
   pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl.val.programmaticStreamSerializationAllowed = 1;
@@ -1204,6 +1206,11 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   cfg.stream = stream;
   cfg.attrs = &pdl;
   cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * k1::kWarps);
+  cfg.dynamicSmemBytes = k1::SMEM;
+  e = cudaLaunchKernelEx(&cfg, k1::aggregate_kernel<false>, mk, mv, mphik, p, mbar_ns);
+  if (e != cudaSuccess) return e;
   cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
   cfg.blockDim = dim3(k2::kThreads);
   cfg.dynamicSmemBytes = 0;
