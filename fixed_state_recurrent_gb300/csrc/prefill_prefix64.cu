@@ -728,8 +728,8 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const uint32_t dO = tm + TB * (a % 2) + TOO, aP = tm + TB * (a % 2);
           const uint64_t v0 = sdesc_sw128(vt, aOnes - vt, 1024);
 #pragma unroll
-          for (int ks = 0; ks < C / 16; ++ks)  // P [V | 1], P from TMEM
-            mma_bf16_ts(dO, aP + 8 * ks, v0 + ks * kStepMN, ID_PV, 1u);
+          for (int ks = 0; ks < C / 16; ++ks)  // P [V | 1], P from TMEM (keys 0..63, then 64..127)
+            mma_bf16_ts(dO, aP + (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4)), v0 + ks * kStepMN, ID_PV, 1u);
           if (a < 16) LA_TRACE(3, 48 + a);
           mma_commit(&B->oready[a % 2]);
           mma_commit(&B->empty[a % NS]);
@@ -784,10 +784,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     //   mask(j): the causal mask P of the scores, bf16, in place in TMEM.  The
     //     mask of a TMEM lane quadrant is split over its two warps (warp w
     //     reaches lanes 32 (w % 4)..+31): the warp of the first half builds key
-    //     blocks 0 and 1, the other blocks 2 and 3.  Key block q4 packs into
-    //     columns 16 q4..16 q4 + 15, so blocks 2 and 3 land on block 1's
-    //     scores; the two warps meet at a named barrier once both have read
-    //     their scores.
+    //     blocks 0 and 1 and packs them into columns 0..31, the other blocks 2
+    //     and 3 into columns 64..95, each over scores it has read itself, so
+    //     the two warps never wait for each other (the products read keys
+    //     0..63 from columns 0..31 and keys 64..127 from columns 64..95).
     const int cw = warp - 2, quad = warp % 4, half = cw / 4;
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
     auto prep_step = [&](uint32_t j) {
@@ -824,18 +824,11 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint32_t base = tl + TB * b;
       const int q0 = 2 * half;  // this warp's key blocks: q0, q0 + 1
       uint32_t r0[32], r1[32];
-      if (got) {
-        tc_fence_after();
-        if (q0 <= quad) tmem_ld32(base + 32 * q0, r0);
-        if (q0 + 1 <= quad) tmem_ld32(base + 32 * (q0 + 1), r1);
-        tmem_ld_wait();
-      }
-      // both warps of the quadrant have read their scores (always met, also
-      // after a timeout, so that the pair stays matched)
-      tc_fence_before();
-      named_bar_sync(1 + quad, 64);
       if (!got) return;
       tc_fence_after();
+      if (q0 <= quad) tmem_ld32(base + 32 * q0, r0);
+      if (q0 + 1 <= quad) tmem_ld32(base + 32 * (q0 + 1), r1);
+      tmem_ld_wait();
 #pragma unroll 1
       for (int k = 0; k < 2; ++k) {
         const int q4 = q0 + k;
@@ -856,7 +849,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                   2 * t2 + 1 <= lane ? __uint_as_float(r[2 * t2 + 1]) : 0.f);
           }
         }
-        tmem_st16(base + 16 * q4, w);
+        tmem_st16(base + 64 * half + 16 * k, w);  // over this warp's own block q0's scores
       }
       tmem_st_wait();
       tc_fence_before();
@@ -872,10 +865,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     entry_part();
     uint64_t dl = globaltimer_ns() + x.mbar_ns;
     while (jp < n || jm < n) {
-      if (*x.abort) {  // given up: the remaining masks still meet their pair barriers
-        while (jm < n) mask_step(jm++);
-        break;
-      }
+      if (*x.abort) break;  // given up
       bool did = false;
       if (jm < jp && __shfl_sync(0xFFFFFFFFu, (int)mbar_test_wait(&B->accB[jm % 2], (jm / 2) & 1), 0)) {
         mask_step(jm++);
