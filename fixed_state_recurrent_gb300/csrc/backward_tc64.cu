@@ -701,6 +701,7 @@ bool backward_tc64_supported(const PrefillArgs& a) {
 // scratch for the prefill's scan, phi(K) scratch for its aggregate kernel.
 size_t backward_tc64_workspace_bytes(int B, int H, int N) {
   using namespace bw;
+  if (prefill_prefix64_chosen(B, H, N)) return backward_prefix64_workspace_bytes(B, H, N);
   const Split s = make_split(B * H, N, sm_count());
   const size_t slots = (size_t)s.BH * s.MPH;
   return (4 * slots + s.BH) * SZ * sizeof(float) + (size_t)s.BH * N * D * sizeof(__nv_bfloat16);
@@ -722,6 +723,8 @@ cudaError_t launch_backward_tc64(const PrefillArgs& a, const float* dO, const fl
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const bool split = a.workspace && a.ws_bytes >= backward_tc64_workspace_bytes(a.B, a.H, a.N);
+  if (split && prefill_prefix64_chosen(a.B, a.H, a.N))  // chunk-parallel, four launches
+    return launch_backward_prefix64(a, dO, dS_N, dz_N, dq, dk, dv, dS0, dz0, stream);
   Params p = {};
   p.sp = make_split(BH, a.N, split ? sms : BH);  // without a workspace, block j runs head j
   p.N = a.N;

@@ -109,6 +109,36 @@ cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cud
 bool prefill_prefix64_chosen(int B, int H, int N);
 size_t prefill_prefix64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream);
+// The same two launches with every buffer given: R piece totals ([BH * MPH]
+// slots of 64 * 64 + 64 floats, MPH of prefill_tc_common.cuh's make_split over
+// the current device's SMs), P prefix tiles ([BH * ceil(N / 128)][66][64]
+// bf16), phik ([BH][N][64] bf16), o ([BH][N][64] fp32), den (NULL, or
+// [BH][N] fp32: den_t = phi(q_t)^T z_t + eps), S_N and z_N (B * H final
+// states), status (where bounded waits that give up are recorded);
+// force_wait: the test hook of the output kernel.  q, k, v, S0, z0, N, eps
+// come from a.
+struct Prefix64Buffers {
+  float* R;
+  uint8_t* P;
+  __nv_bfloat16* phik;
+  float* o;
+  float* den;
+  float* S_N;
+  float* z_N;
+  unsigned* status;
+  int force_wait;
+};
+cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b, cudaStream_t stream);
+
+// The gradient of the prefill for bf16 at dk = dv = 64, chunk-parallel in four
+// launches (backward_prefix64.cu): the two launches above (o and den into the
+// workspace), the gradient-state tiles, then dq, dk, dv.  For the calls that
+// prefill_prefix64_chosen takes; bounded-wait failures go to the library
+// status word.
+size_t backward_prefix64_workspace_bytes(int B, int H, int N);
+cudaError_t launch_backward_prefix64(const PrefillArgs& a, const float* dO, const float* dS_N,
+                                     const float* dz_N, float* dq, float* dk, float* dv, float* dS0,
+                                     float* dz0, cudaStream_t stream);
 
 // The same three launches for dk = dv = 128 (prefill_chunked128.cu).
 size_t prefill_chunked128_workspace_bytes(int B, int H, int N);

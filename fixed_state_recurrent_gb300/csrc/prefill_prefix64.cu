@@ -90,6 +90,7 @@ struct Params {
   unsigned* status;    // sticky error bits (the workspace header's, or the library's)
   float* R;            // [BH * MPH][SZ] piece totals (slot layout)
   uint8_t* P;          // [TC][66][64] bf16 prefix tiles
+  float* den;          // NULL, or [BH][N]: the output kernel also stores den_t = phi(q_t)^T z_t + eps
   int force_wait;      // test hook: the output kernel waits once on a barrier that nothing completes
 };
 
@@ -912,7 +913,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B->ofree[ob]);
-          const float inv = 1.f / (__uint_as_float(d2[0]) + __uint_as_float(d2[1]) + p.eps);
+          const float den = __uint_as_float(d2[0]) + __uint_as_float(d2[1]) + p.eps;
+          const float inv = 1.f / den;
+          if (p.den && row < pc.tok1 - (pc.tok0 + c * C) && !*x.abort)
+            p.den[(size_t)pc.h * p.sp.N + pc.tok0 + c * C + row] = den;
           if (et == 32) bulk_wait_read_all();  // the previous chunk's store has read the staging
           named_bar_sync(5, 128);
 #pragma unroll
@@ -929,8 +933,13 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           named_bar_sync(5, 128);
           if (et == 32 && !*x.abort) {
             const int tok = pc.tok0 + c * C;
-            tma_store_3d_ef(&tm_o, out, 0, tok, pc.h);
-            tma_store_3d_ef(&tm_o, out + BLK, 32, tok, pc.h);
+            if (p.den) {  // o is read again soon (the gradient's next launch)
+              tma_store_3d(&tm_o, out, 0, tok, pc.h);
+              tma_store_3d(&tm_o, out + BLK, 32, tok, pc.h);
+            } else {
+              tma_store_3d_ef(&tm_o, out, 0, tok, pc.h);
+              tma_store_3d_ef(&tm_o, out + BLK, 32, tok, pc.h);
+            }
             bulk_commit();
             if (oj < 6) LA_TRACE(2, 40 + oj);
           }
@@ -962,7 +971,7 @@ size_t prefill_prefix64_workspace_bytes(int B, int H, int N) {
          (size_t)B * H * N * D * sizeof(__nv_bfloat16);
 }
 
-cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
+cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b, cudaStream_t stream) {
   const int BH = a.B * a.H;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
@@ -971,25 +980,22 @@ cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
   p.eps = a.eps;
   p.S0 = a.S0;
   p.z0 = a.z0;
-  p.S_N = a.S_N;
-  p.z_N = a.z_N;
-  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  p.status = a.status ? a.status : &reinterpret_cast<WsHeader*>(ws)->status;
-  if (sizeof(WsHeader) + prefill_prefix64_workspace_bytes(a.B, a.H, a.N) > a.ws_bytes)
-    return cudaErrorInvalidValue;
-  p.R = reinterpret_cast<float*>(ws + sizeof(WsHeader));
-  p.P = reinterpret_cast<uint8_t*>(p.R + (size_t)BH * p.sp.MPH * SZ);
-  __nv_bfloat16* phik = reinterpret_cast<__nv_bfloat16*>(p.P + (size_t)p.sp.TC() * XG);
+  p.S_N = b.S_N;
+  p.z_N = b.z_N;
+  p.status = b.status;
+  p.R = b.R;
+  p.P = b.P;
+  p.den = b.den;
+  p.force_wait = b.force_wait;
   CUtensorMap mq, mk, mv, mo, mphik, mp;
   if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
-      !make_map(&mo, a.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
-      !make_map(&mphik, phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mo, b.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
+      !make_map(&mphik, b.phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mp, p.P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, (int)p.sp.TC(), 64, XROWS))
     return cudaErrorInvalidValue;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
-  p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
 
   cudaError_t e = cudaFuncSetAttribute(pfx::prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pfx::SMEM);
@@ -1016,6 +1022,27 @@ cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
   cfg.blockDim = dim3(32 * out::kWarps);
   cfg.dynamicSmemBytes = out::SMEM;
   return cudaLaunchKernelEx(&cfg, out::output_kernel, mq, mphik, mp, mv, mo, p, mbar_ns);
+}
+
+cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const Split sp = make_split(BH, a.N, sms);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  if (sizeof(WsHeader) + prefill_prefix64_workspace_bytes(a.B, a.H, a.N) > a.ws_bytes)
+    return cudaErrorInvalidValue;
+  Prefix64Buffers b = {};
+  b.R = reinterpret_cast<float*>(ws + sizeof(WsHeader));
+  b.P = reinterpret_cast<uint8_t*>(b.R + (size_t)BH * sp.MPH * SZ);
+  b.phik = reinterpret_cast<__nv_bfloat16*>(b.P + (size_t)sp.TC() * XG);
+  b.o = a.o;
+  b.den = nullptr;
+  b.S_N = a.S_N;
+  b.z_N = a.z_N;
+  b.status = a.status ? a.status : &reinterpret_cast<WsHeader*>(ws)->status;
+  b.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+  return launch_prefix64_pair(a, b, stream);
 }
 
 }  // namespace la

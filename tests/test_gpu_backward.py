@@ -116,8 +116,10 @@ def test_backward_tc_matches_oracle(la, orc, N, with_state, ws):
 
 
 # the split's pieces: several per head (long heads), runs that cross heads
-# (many short heads), a ragged last chunk in each
-SPLIT_SHAPES = [(1, 2, 20000), (2, 5, 3000), (3, 40, 333), (1, 1, 40000)]
+# (many short heads), a ragged last chunk in each; the last shape has more
+# chunks (2188) than the chunk-parallel form takes, so it runs the sweeps over
+# the pieces
+SPLIT_SHAPES = [(1, 2, 20000), (2, 5, 3000), (3, 40, 333), (1, 1, 40000), (1, 4, 70000)]
 
 
 @pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=[str(s) for s in SPLIT_SHAPES])
