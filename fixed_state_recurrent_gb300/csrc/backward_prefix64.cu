@@ -41,6 +41,24 @@
 // status word and the kernel finishes with unspecified outputs.
 #include "prefill_tc_common.cuh"
 
+#ifdef LA_TRACE
+static __device__ unsigned long long g_bw_trace[2 * 160 * 64];
+#define BW_TRACE(kern, ev)                                                              \
+  do {                                                                                 \
+    if ((ev) < 64 && blockIdx.x < 160)                                                 \
+      g_bw_trace[((kern) * 160 + blockIdx.x) * 64 + (ev)] = la::tc::globaltimer_ns();  \
+  } while (0)
+extern "C" int la_backward64_trace_read(unsigned long long* host, int n) {
+  return cudaMemcpyFromSymbol(host, g_bw_trace, (size_t)n * 8) == cudaSuccess ? 0 : -1;
+}
+extern "C" int la_backward64_trace_clear() {
+  static unsigned long long zeros[2 * 160 * 64];
+  return cudaMemcpyToSymbol(g_bw_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -1;
+}
+#else
+#define BW_TRACE(kern, ev) ((void)0)
+#endif
+
 namespace la {
 namespace {
 
@@ -96,6 +114,16 @@ __device__ __forceinline__ void put8(uint8_t* tile, int row, int chunk, const fl
                  pack_bf16x2(v[6], v[7]));
 }
 
+// Plain bulk copy global -> shared of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned), completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Element (row, col) of a [rows x 64] bf16 swizzled tile, widened.
 __device__ __forceinline__ float tile_at(const uint8_t* tile, int row, int col) {
   const uint16_t b = *reinterpret_cast<const uint16_t*>(tile + sw128_offset(row, col / 8) + (col % 8) * 2);
@@ -133,7 +161,7 @@ struct Params {
   const float* dS_N;  // [BH][64][64] or NULL
   const float* dz_N;  // [BH][64] or NULL
   const float* den;   // [BH][N]: den_t of the prefill
-  float* dden;        // [BH][N] out
+  float* dden;        // [BH * NC][128] out: dden of every chunk row (0 past the sequence)
   float* RG;          // [BH * MPH][SZ] gradient totals of the pieces (slot layout)
   unsigned* status;
 };
@@ -191,8 +219,10 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const Ctx x{p.status, &B->abort, *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
+  if (threadIdx.x == 0) BW_TRACE(1, 0);
   pdl_launch_dependents();  // the gradient kernel may be scheduled now; it waits for this grid
   pdl_wait();               // o and den of the output kernel are complete
+  if (threadIdx.x == 0) BW_TRACE(1, 1);
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer: Q, o, dO
@@ -222,6 +252,7 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int s = j % NS, b = j % NB;
         if (j >= NB && !waitb(x, &B->dsfree[b], ((j / NB) - 1) & 1)) break;
         if (!waitb(x, &B->xf[s], (j / NS) & 1)) break;
+        if (j < 16) BW_TRACE(1, 2 + j);
         tc_fence_after();
         const uint32_t qt = smem_u32(smem + s * STAGE), dn = qt + OFF_O;
         const uint64_t a0 = sdesc_sw128(dn, BLK, 1024), b0 = sdesc_sw128(qt, BLK, 1024);
@@ -281,8 +312,8 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           *reinterpret_cast<uint4*>(db + sw128_offset(r, 0)) = make_uint4(pack_bf16x2(dden, 0.f), 0u, 0u, 0u);
 #pragma unroll
           for (int q = 1; q < 8; ++q) *reinterpret_cast<uint4*>(db + sw128_offset(r, q)) = make_uint4(0u, 0u, 0u, 0u);
-        } else if (r < valid && !*x.abort) {
-          p.dden[(size_t)pc.h * N + tok + r] = dden;
+        } else if (!*x.abort) {  // rows past the sequence: 0
+          p.dden[((size_t)pc.h * p.sp.NC + pc.tok0 / C + c) * C + r] = dden;
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -346,6 +377,7 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         const int b = sj % NB;
         const bool got = waitb_warp(x, &B->dsready[b], (sj / NB) & 1);
+        if (et == 32 && sj < 16) BW_TRACE(1, 18 + sj);
         if (state_warp) {
           if (got) {
             tc_fence_after();
@@ -372,6 +404,7 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
     }
     if (et == 32) bulk_wait_all();
+    if (et == 32) BW_TRACE(1, 63);
   } else if (lane == 0) {  // ---- phi(Q), dnum -> workspace; the stage is released once read
     uint32_t sj = 0;
     Piece pc;
@@ -405,23 +438,27 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 namespace grd {
 
 // stage: phi(Q) | phi(K) | V | dnum (bf16 [128 x 64] tiles) | the state tile
-// S_c - E and the gradient-state tile G_c - EG (66 rows each)
+// S_c - E and the gradient-state tile G_c - EG (66 rows each).  OFF_OUT stages
+// dq for its TMA stores (two [128 x 32] fp32 boxes); once a chunk's products
+// are done its stage stages dv (over phi(Q) and phi(K)) and dk (over V and
+// dnum).
 constexpr uint32_t OFF_KF = BLK, OFF_V = 2 * BLK, OFF_DN = 3 * BLK;
 constexpr uint32_t OFF_ST = 4 * BLK, OFF_GT = 4 * BLK + XT;
 constexpr uint32_t STAGE = 4 * BLK + 2 * XT;
 constexpr uint32_t OFF_E = 2 * STAGE;        // E, EG: bf16 tiles (rows 0..63 used)
 constexpr uint32_t OFF_EG = OFF_E + XT;
-constexpr uint32_t OFF_VEC = OFF_EG + XT;    // floats: dd[2][128], zc[64], gc[64], zE[64], gE[64]
+constexpr uint32_t OFF_OUT = OFF_EG + XT;    // dq staging: two [128 x 32] fp32 boxes
+constexpr uint32_t OFF_VEC = OFF_OUT + 2 * BLK;  // floats: dd[2][128], zc[64], gc[64], zE[64], gE[64]
 constexpr uint32_t OFF_BAR = OFF_VEC + (2 * 128 + 4 * 64) * 4;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
-static_assert(STAGE % 1024 == 0 && OFF_GT % 1024 == 0 && OFF_E % 1024 == 0 && OFF_EG % 1024 == 0,
-              "swizzled tile alignment");
+static_assert(STAGE % 1024 == 0 && OFF_GT % 1024 == 0 && OFF_E % 1024 == 0 && OFF_EG % 1024 == 0 &&
+              OFF_OUT % 1024 == 0, "swizzled tile alignment");
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 constexpr int kThreads = 256;  // two threads per chunk row / TMEM lane
 constexpr uint32_t kCols = 512;
-// TMEM: A1 = dnum V^T (then its mask P1; later U W^T and its mask P3), A2 =
-// V dnum^T (then P2), dW, dU, dV
-constexpr uint32_t T_A1 = 0, T_A2 = 128, T_DW = 256, T_DU = 320, T_DV = 384;
+// TMEM: the scores A1 = dnum V^T, A2 = V dnum^T, A3 = U W^T (then their masks
+// P1, P2, P3, packed in place), dW, dU; dV over A1 once P1 is read
+constexpr uint32_t T_A1 = 0, T_A2 = 128, T_A3 = 256, T_DW = 384, T_DU = 448, T_DV = 0;
 
 constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);      // both K-major, N = 128
 constexpr uint32_t ID_N64_MN = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major, N = 64
@@ -431,7 +468,7 @@ struct Params {
   Split sp;
   const float* R;     // forward piece totals (slot layout; with S0)
   const float* RG;    // gradient piece totals (slot layout; with dS_N)
-  const float* dden;  // [BH][N]
+  const float* dden;  // [BH * NC][128]
   float* dq;
   float* dk;
   float* dv;
@@ -457,32 +494,51 @@ struct Bars {
 __device__ __forceinline__ void sum_slots(const float* tot, size_t base, int k0, int k1, uint8_t* tile,
                                           float* vec, const float* own, float* dS, float* dz, int t,
                                           int nthr) {
-  for (int f = t; f < SZ / 4; f += nthr) {
-    float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = k0; k < k1; ++k) {
-      const float4 r = __ldcg(reinterpret_cast<const float4*>(tot + (base + k) * SZ) + f);
-      e.x += r.x; e.y += r.y; e.z += r.z; e.w += r.w;
-    }
-    const int row = f / 16, col = 4 * (f % 16);
-    if (row < D) {
-      if (tile) {
-        uint2 hi;
-        hi.x = pack_bf16x2(e.x, e.y);
-        hi.y = pack_bf16x2(e.z, e.w);
-        *reinterpret_cast<uint2*>(tile + sw128_offset(row, col / 8) + (col % 8) * 2) = hi;
-      }
-    } else if (vec) {
-      vec[col] = e.x; vec[col + 1] = e.y; vec[col + 2] = e.z; vec[col + 3] = e.w;
-    }
-    if (own) {
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(own) + f);
-      const float v4[4] = {e.x + o.x, e.y + o.y, e.z + o.z, e.w + o.w};
-      if (row < D) {
-        if (dS)
+  constexpr int U = 4;  // slots read at once for each of two float4 of a thread
+  for (int f0 = t; f0 < SZ / 4; f0 += 2 * nthr) {
+    float4 e[2];
+    e[0] = e[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = k0; k < k1; k += U) {
+      float4 r[2][U];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) dS[(size_t)(col + u) * D + row] = v4[u];
-      } else if (dz) {
-        reinterpret_cast<float4*>(dz)[col / 4] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int kk = 0; kk < U; ++kk)
+          r[u][kk] = (f0 + u * nthr < SZ / 4 && k + kk < k1)
+                         ? __ldcg(reinterpret_cast<const float4*>(tot + (base + k + kk) * SZ) + f0 + u * nthr)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int kk = 0; kk < U; ++kk) {  // in slot order
+          e[u].x += r[u][kk].x; e[u].y += r[u][kk].y; e[u].z += r[u][kk].z; e[u].w += r[u][kk].w;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int f = f0 + u * nthr;
+      if (f >= SZ / 4) continue;
+      const int row = f / 16, col = 4 * (f % 16);
+      if (row < D) {
+        if (tile) {
+          uint2 hi;
+          hi.x = pack_bf16x2(e[u].x, e[u].y);
+          hi.y = pack_bf16x2(e[u].z, e[u].w);
+          *reinterpret_cast<uint2*>(tile + sw128_offset(row, col / 8) + (col % 8) * 2) = hi;
+        }
+      } else if (vec) {
+        vec[col] = e[u].x; vec[col + 1] = e[u].y; vec[col + 2] = e[u].z; vec[col + 3] = e[u].w;
+      }
+      if (own) {
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(own) + f);
+        const float v4[4] = {e[u].x + o.x, e[u].y + o.y, e[u].z + o.z, e[u].w + o.w};
+        if (row < D) {
+          if (dS)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) dS[(size_t)(col + w) * D + row] = v4[w];
+        } else if (dz) {
+          reinterpret_cast<float4*>(dz)[col / 4] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+        }
       }
     }
   }
@@ -510,49 +566,44 @@ __device__ __forceinline__ void tmem_row32(uint32_t taddr, float* out) {
   for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(a[i]);
 }
 
-__device__ __forceinline__ void store_half_f32(float* rowp, int hf, const float* v) {
-  float4* dst = reinterpret_cast<float4*>(rowp + 32 * hf);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-
 // A masked score tile in TMEM (this thread's row = 32 quad + lane), rounded to
 // bf16 and packed in place: the thread of column half hf reads key blocks
 // 2 hf, 2 hf + 1 and writes them packed over the first of them (columns
 // 64 hf .. 64 hf + 31), so the two threads of a row never touch each other's
 // columns; the products read keys 0..63 from columns 0..31 and keys 64..127
-// from 64..95.  UPPER keeps columns >= the row (else <=).  `rowadd` is added
-// to every kept element, `coladd[col]` too (NULL: nothing).
-template <bool UPPER>
-__device__ __forceinline__ void mask_pack(uint32_t base, int quad, int lane, int hf, float rowadd,
-                                          const float* coladd) {
+// from 64..95.  `upper` keeps columns >= the row (else <=).  `rowadd` is
+// added to every kept element, and `coladd[col]` unless it is NULL.
+__device__ __forceinline__ void mask_pack(uint32_t base, bool upper, int quad, int lane, int hf,
+                                          float rowadd, const float* coladd) {
   uint32_t r0[32], r1[32];
   const int q0 = 2 * hf;
-  const bool need0 = UPPER ? q0 >= quad : q0 <= quad;
-  const bool need1 = UPPER ? q0 + 1 >= quad : q0 + 1 <= quad;
-  if (need0) tmem_ld32(base + 32 * q0, r0);
-  if (need1) tmem_ld32(base + 32 * (q0 + 1), r1);
+  if (upper ? q0 >= quad : q0 <= quad) tmem_ld32(base + 32 * q0, r0);
+  if (upper ? q0 + 1 >= quad : q0 + 1 <= quad) tmem_ld32(base + 32 * (q0 + 1), r1);
   tmem_ld_wait();
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int q4 = q0 + k;
     const uint32_t* r = k ? r1 : r0;
-    const bool all = UPPER ? q4 > quad : q4 < quad;
-    const bool none = UPPER ? q4 < quad : q4 > quad;
     uint32_t w[16];
+    if (upper ? q4 < quad : q4 > quad) {  // nothing kept
 #pragma unroll
-    for (int t2 = 0; t2 < 16; ++t2) {
-      const int s0 = 2 * t2, s1 = 2 * t2 + 1;
-      float a0 = 0.f, a1 = 0.f;
-      if (!none) {
-        const bool k0 = all || (UPPER ? s0 >= lane : s0 <= lane);
-        const bool k1 = all || (UPPER ? s1 >= lane : s1 <= lane);
-        const float c0 = coladd ? coladd[32 * q4 + s0] : 0.f;
-        const float c1 = coladd ? coladd[32 * q4 + s1] : 0.f;
-        a0 = k0 ? __uint_as_float(r[s0]) + rowadd + c0 : 0.f;
-        a1 = k1 ? __uint_as_float(r[s1]) + rowadd + c1 : 0.f;
+      for (int t2 = 0; t2 < 16; ++t2) w[t2] = 0u;
+    } else {
+      // the diagonal block keeps keys on the kept side of the lane; the
+      // others keep all (lo..hi: the kept range of this block's columns)
+      const int lo = (q4 == quad && upper) ? lane : 0, hi = (q4 == quad && !upper) ? lane : 31;
+      const float* ca = coladd ? coladd + 32 * q4 : nullptr;
+#pragma unroll
+      for (int t2 = 0; t2 < 16; ++t2) {
+        const int s0 = 2 * t2, s1 = 2 * t2 + 1;
+        float a0 = __uint_as_float(r[s0]) + rowadd, a1 = __uint_as_float(r[s1]) + rowadd;
+        if (ca) {
+          const float2 c2 = reinterpret_cast<const float2*>(ca)[t2];  // the same address across the warp
+          a0 += c2.x;
+          a1 += c2.y;
+        }
+        w[t2] = pack_bf16x2(s0 >= lo && s0 <= hi ? a0 : 0.f, s1 >= lo && s1 <= hi ? a1 : 0.f);
       }
-      w[t2] = pack_bf16x2(a0, a1);
     }
     tmem_st16(base + 64 * hf + 16 * k, w);
   }
@@ -565,7 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__ CUtensorMap tm_phik,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dn,
             const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_gt,
-            const Params p, const unsigned long long mbar_ns) {
+            const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+            const __grid_constant__ CUtensorMap tm_dv, const Params p, const unsigned long long mbar_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
@@ -577,7 +629,7 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
   const int row = t & (C - 1), hf = t >> 7, quad = warp & 3;
   const Split& sp = p.sp;
-  const int N = sp.N, NC = sp.NC;
+  const int NC = sp.NC;
   const Run run(sp, blockIdx.x);
   const uint32_t total = (uint32_t)(run.b - run.a);
   if (t == 0) {
@@ -594,6 +646,9 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
     tma_prefetch_desc(&tm_dn);
     tma_prefetch_desc(&tm_p);
     tma_prefetch_desc(&tm_gt);
+    tma_prefetch_desc(&tm_dq);
+    tma_prefetch_desc(&tm_dk);
+    tma_prefetch_desc(&tm_dv);
   }
   if (warp == 0) {
     tmem_alloc(&B->tmem_slot, kCols);
@@ -606,17 +661,22 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
   const uint32_t tl = tm + ((uint32_t)(32 * quad) << 16);  // this thread's TMEM lane (row)
   const uint32_t th = 32 * hf;                              // and its column half
   const Ctx x{p.status, &B->abort, tm, mbar_ns};
+  if (t == 0) BW_TRACE(0, 0);
   pdl_launch_dependents();
   pdl_wait();  // every earlier launch of the gradient is complete
+  if (t == 0) BW_TRACE(0, 1);
 
   uint32_t nload = 0, nmma = 0;
-  // thread 0: the loads of the run's chunk j into stage j % 2
+  // thread 32 (kLd): the loads of the run's chunk j into stage j % 2 and its
+  // dden into dd[j % 2]; it also issues the output stores
+  constexpr int kLd = 32;
   auto load = [&](uint32_t j) {
     const int s = j % 2;
     uint8_t* st = smem + s * STAGE;
     const long long gi = run.a + j;
     const int h = (int)(gi / NC), tok = (int)(gi % NC) * C;
-    mbar_arrive_expect_tx(&B->full[s], 4 * BLK + 2 * XG);
+    mbar_arrive_expect_tx(&B->full[s], 4 * BLK + 2 * XG + C * 4);
+    bulk_load(dd + s * C, p.dden + (size_t)gi * C, C * 4, &B->full[s]);
     tma_load_3d_ef(st, &tm_phiq, 0, tok, h, &B->full[s]);
     tma_load_3d_ef(st + OFF_KF, &tm_phik, 0, tok, h, &B->full[s]);
     tma_load_3d_ef(st + OFF_V, &tm_v, 0, tok, h, &B->full[s]);
@@ -625,7 +685,7 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
     tma_load_3d_ef(st + OFF_GT, &tm_gt, 0, 0, (int)gi, &B->full[s]);
     ++nload;
   };
-  if (t == 0 && total > 0) load(0);
+  if (t == kLd && total > 0) load(0);
 
   // The first piece's entry state E (the forward totals of the head's earlier
   // blocks), the last piece's exit gradient state EG (the gradient totals of
@@ -652,6 +712,7 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
               p.dz0 ? p.dz0 + (size_t)h * D : nullptr, t, kThreads);
   }
   __syncthreads();
+  if (t == 0) BW_TRACE(0, 2);
 
   auto issuing = [&]() {
     tc_fence_after();
@@ -670,31 +731,28 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
   const uint64_t eS = sdesc_sw128(smem_u32(smem + OFF_E), 16, 1024);
   const uint64_t eG = sdesc_sw128(smem_u32(smem + OFF_EG), 16, 1024);
 
-  for (uint32_t j = 0; j < total; ++j) {
+  // thread 0: A1 = dnum V^T, A2 = V dnum^T, A3 = U W^T, dW = dnum (S_c)^T,
+  // dU = V (G_c)^T of the run's chunk j, once its tiles are in
+  auto issue_first = [&](uint32_t j) {
     const int s = j % 2;
-    uint8_t* st = smem + s * STAGE;
     const long long gi = run.a + j;
-    const int h = (int)(gi / NC), tok = (int)(gi % NC) * C;
-    const int valid = min(C, N - tok);
+    const int h = (int)(gi / NC);
     const bool useE = haveE && h == h0, useEG = lastContinues && h == hl;
-    if (t == 0 && j + 1 < total && !aborted()) load(j + 1);
-    if (t < C) dd[s * C + t] = t < valid ? __ldcg(p.dden + (size_t)h * N + tok + t) : 0.f;
-    waitb(x, &B->full[s], (j / 2) & 1);
-    if (t < D) {
-      zc[t] = tile_at(st + OFF_ST, 64, t) + tile_at(st + OFF_ST, 65, t) + (useE ? zE[t] : 0.f);
-    } else if (t < 2 * D) {
-      const int i = t - D;
-      gc[i] = tile_at(st + OFF_GT, 64, i) + tile_at(st + OFF_GT, 65, i) + (useEG ? gE[i] : 0.f);
-    }
-    step_done();
-    const uint32_t aQ = smem_u32(st), aK = aQ + OFF_KF, aV = aQ + OFF_V, aD = aQ + OFF_DN;
+    const uint32_t aQ = smem_u32(smem + s * STAGE), aK = aQ + OFF_KF, aV = aQ + OFF_V, aD = aQ + OFF_DN;
     const uint32_t aS = aQ + OFF_ST, aG = aQ + OFF_GT;
-
-    // A1 = dnum V^T, dW = dnum (S_c)^T, A2 = V dnum^T, dU = V (G_c)^T, dV = U G_c
-    if (t == 0 && (!p.force_wait || j > 0 || waitb(x, &B->never, 0)) && issuing()) {
+    if (waitb(x, &B->full[s], (j / 2) & 1) && (!p.force_wait || j > 0 || waitb(x, &B->never, 0)) &&
+        issuing()) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         mma_bf16_ss(tm + T_A1, sdesc_sw128(aD + ks * 32, 16, 1024), sdesc_sw128(aV + ks * 32, 16, 1024), ID_S,
+                    ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_bf16_ss(tm + T_A2, sdesc_sw128(aV + ks * 32, 16, 1024), sdesc_sw128(aD + ks * 32, 16, 1024), ID_S,
+                    ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_bf16_ss(tm + T_A3, sdesc_sw128(aK + ks * 32, 16, 1024), sdesc_sw128(aQ + ks * 32, 16, 1024), ID_S,
                     ks > 0);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
@@ -707,31 +765,47 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
       }
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_A2, sdesc_sw128(aV + ks * 32, 16, 1024), sdesc_sw128(aD + ks * 32, 16, 1024), ID_S,
-                    ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
         mma_bf16_ss(tm + T_DU, sdesc_sw128(aV + ks * 32, 16, 1024), sdesc_sw128(aG + ks * 2048, 16, 1024),
                     ID_N64_MN, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_DV, sdesc_sw128(aK + ks * 32, 16, 1024), sdesc_sw128(aG + ks * 32, 16, 1024),
-                    ID_N64_K, ks > 0);
       if (useEG) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           mma_bf16_ss(tm + T_DU, sdesc_sw128(aV + ks * 32, 16, 1024), eG + ks * kStepRows16, ID_N64_MN, 1u);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_bf16_ss(tm + T_DV, sdesc_sw128(aK + ks * 32, 16, 1024), eG + ks * kStepK16, ID_N64_K, 1u);
       }
     }
-    if (t == 0) mma_commit(&B->mma);
-    mma_done();
-    // P1 = mask(A1 + dden_t) (keys s <= t), P2 = mask^T(A2 + dden_t) (queries t >= s)
-    mask_pack<false>(tl + T_A1, quad, lane, hf, dd[s * C + row], nullptr);
-    mask_pack<true>(tl + T_A2, quad, lane, hf, 0.f, dd + s * C);
+    mma_commit(&B->mma);
+  };
+  if (t == 0 && total > 0) issue_first(0);
+
+  for (uint32_t j = 0; j < total; ++j) {
+    const int s = j % 2;
+    uint8_t* st = smem + s * STAGE;
+    const long long gi = run.a + j;
+    const int h = (int)(gi / NC), tok = (int)(gi % NC) * C;
+    const bool useE = haveE && h == h0, useEG = lastContinues && h == hl;
+    const uint32_t aQ = smem_u32(st), aK = aQ + OFF_KF, aD = aQ + OFF_DN, aG = aQ + OFF_GT;
+    // the stores of the chunk before have read their staging (the dq staging
+    // and the other stage); the next chunk's tiles into that stage
+    if (t == kLd && j > 0) bulk_wait_read_all();
+    if (t == kLd && j + 1 < total && !aborted()) load(j + 1);
+    waitb(x, &B->full[s], (j / 2) & 1);
+    if (t == 0 && j < 8) BW_TRACE(0, 3 + 6 * j);
+    if (t < D) {
+      zc[t] = tile_at(st + OFF_ST, 64, t) + tile_at(st + OFF_ST, 65, t) + (useE ? zE[t] : 0.f);
+    } else if (t < 2 * D) {
+      const int i = t - D;
+      gc[i] = tile_at(st + OFF_GT, 64, i) + tile_at(st + OFF_GT, 65, i) + (useEG ? gE[i] : 0.f);
+    }
+    mma_done();  // the first products of chunk j
+    if (t == 0 && j < 8) BW_TRACE(0, 4 + 6 * j);
+    // P1 = mask(A1 + dden_t) (keys s <= t), P2 = mask^T(A2 + dden_t) and
+    // P3 = mask^T(A3) (queries t >= s)
+#pragma unroll 1
+    for (int m = 0; m < 3; ++m)
+      mask_pack(tl + (m == 0 ? T_A1 : m == 1 ? T_A2 : T_A3), m > 0, quad, lane, hf,
+                m == 0 ? dd[s * C + row] : 0.f, m == 1 ? dd + s * C : nullptr);
     step_done();
+    if (t == 0 && j < 8) BW_TRACE(0, 5 + 6 * j);
 
     // dW += P1 U, dU += P2 W
     if (t == 0 && issuing()) {
@@ -744,59 +818,84 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
     }
     if (t == 0) mma_commit(&B->mma);
     mma_done();
-    // A3 = U W^T (over A1, whose P1 the products above have read)
+    if (t == 0 && j < 8) BW_TRACE(0, 6 + 6 * j);
+    // dV = U G_c + P3 dnum (over A1, whose P1 the products above have read)
     if (t == 0 && issuing()) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_A1, sdesc_sw128(aK + ks * 32, 16, 1024), sdesc_sw128(aQ + ks * 32, 16, 1024), ID_S,
-                    ks > 0);
-    }
-    if (t == 0) mma_commit(&B->mma);
-    {  // dq = (dW + dden_t z_c) phi'(q), dk = (dU + g_c) phi'(k)
-      float g[32], f[32];
-      const bool out = row < valid && !aborted();
-      tmem_row32(tl + T_DW + th, g);
-      load_half_bf16(st, row, hf, f);
-      const float dr = dd[s * C + row];
-      if (out) {
+        mma_bf16_ss(tm + T_DV, sdesc_sw128(aK + ks * 32, 16, 1024), sdesc_sw128(aG + ks * 32, 16, 1024),
+                    ID_N64_K, ks > 0);
+      if (useEG) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = (g[i] + dr * zc[th + i]) * fminf(f[i], 1.f);
-        store_half_f32(p.dq + ((size_t)h * N + tok + row) * D, hf, g);
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16_ss(tm + T_DV, sdesc_sw128(aK + ks * 32, 16, 1024), eG + ks * kStepK16, ID_N64_K, 1u);
       }
-      tmem_row32(tl + T_DU + th, g);
-      load_half_bf16(st + OFF_KF, row, hf, f);
-      if (out) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = (g[i] + gc[th + i]) * fminf(f[i], 1.f);
-        store_half_f32(p.dk + ((size_t)h * N + tok + row) * D, hf, g);
-      }
-    }
-    mma_done();
-    mask_pack<true>(tl + T_A1, quad, lane, hf, 0.f, nullptr);  // P3 = mask^T(A3)
-    step_done();
-
-    // dV += P3 dnum
-    if (t == 0 && issuing()) {
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks)
-        mma_bf16_ts(tm + T_DV, tm + T_A1 + pcol(ks), sdesc_sw128(aD + ks * 2048, BLK, 1024), ID_N64_MN, 1u);
+        mma_bf16_ts(tm + T_DV, tm + T_A3 + pcol(ks), sdesc_sw128(aD + ks * 2048, BLK, 1024), ID_N64_MN, 1u);
     }
     if (t == 0) mma_commit(&B->mma);
-    mma_done();
+    // meanwhile dq = (dW + dden_t z_c) phi'(q) into its staging, dk = (dU + g_c) phi'(k)
+    float o[32], f[32];
     {
-      float g[32];
-      tmem_row32(tl + T_DV + th, g);
-      if (row < valid && !aborted()) store_half_f32(p.dv + ((size_t)h * N + tok + row) * D, hf, g);
+      uint8_t* bq = smem + OFF_OUT + hf * BLK;
+      const float dr = dd[s * C + row];
+      tmem_row32(tl + T_DW + th, o);
+      load_half_bf16(st, row, hf, f);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        float4 v4;
+        v4.x = (o[4 * cc] + dr * zc[th + 4 * cc]) * fminf(f[4 * cc], 1.f);
+        v4.y = (o[4 * cc + 1] + dr * zc[th + 4 * cc + 1]) * fminf(f[4 * cc + 1], 1.f);
+        v4.z = (o[4 * cc + 2] + dr * zc[th + 4 * cc + 2]) * fminf(f[4 * cc + 2], 1.f);
+        v4.w = (o[4 * cc + 3] + dr * zc[th + 4 * cc + 3]) * fminf(f[4 * cc + 3], 1.f);
+        *reinterpret_cast<float4*>(bq + sw128_offset(row, cc)) = v4;
+      }
+      tmem_row32(tl + T_DU + th, o);
+      load_half_bf16(st + OFF_KF, row, hf, f);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = (o[i] + gc[th + i]) * fminf(f[i], 1.f);
     }
-    step_done();  // the stage and every TMEM region are free for the chunk after next
+    mma_done();
+    if (t == 0 && j < 8) BW_TRACE(0, 7 + 6 * j);
+    tmem_row32(tl + T_DV + th, f);
+    step_done();  // every read of this chunk's stage and TMEM is done
+    // dk over V | dnum, dv over phi(Q) | phi(K); rows past the sequence are
+    // not stored.  The next chunk's first products go out while they are.
+    {
+      uint8_t* bk = st + OFF_V + hf * BLK;
+      uint8_t* bv = st + hf * BLK;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        *reinterpret_cast<float4*>(bk + sw128_offset(row, cc)) =
+            make_float4(o[4 * cc], o[4 * cc + 1], o[4 * cc + 2], o[4 * cc + 3]);
+        *reinterpret_cast<float4*>(bv + sw128_offset(row, cc)) =
+            make_float4(f[4 * cc], f[4 * cc + 1], f[4 * cc + 2], f[4 * cc + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (t == 0 && j + 1 < total) issue_first(j + 1);
+    if (t == kLd && !aborted()) {
+      tma_store_3d_ef(&tm_dq, smem + OFF_OUT, 0, tok, h);
+      tma_store_3d_ef(&tm_dq, smem + OFF_OUT + BLK, 32, tok, h);
+      tma_store_3d_ef(&tm_dk, st + OFF_V, 0, tok, h);
+      tma_store_3d_ef(&tm_dk, st + OFF_V + BLK, 32, tok, h);
+      tma_store_3d_ef(&tm_dv, st, 0, tok, h);
+      tma_store_3d_ef(&tm_dv, st + BLK, 32, tok, h);
+      bulk_commit();
+    }
+    if (t == 0 && j < 8) BW_TRACE(0, 8 + 6 * j);
   }
+  if (t == kLd) bulk_wait_all();
+  if (t == 0) BW_TRACE(0, 63);
 
-  if (t == 0 && aborted()) {  // MMAs and loads in flight end first
+  if (t == 0 && aborted()) {  // MMAs in flight end first
     int never = 0;
     mma_commit(&B->drain);
     mbar_wait(&B->drain, 0, globaltimer_ns() + mbar_ns, &never);
-    drain_loads<2>(B->full, nload, mbar_ns);
   }
+  if (t == kLd && aborted()) drain_loads<2>(B->full, nload, mbar_ns);  // and loads
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -833,7 +932,7 @@ Layout layout(int BH, int N, const Split& s) {
   L.GT = take((size_t)s.TC() * XG);
   L.phiq = take(tok * D * 2);
   L.dn = take(tok * D * 2);
-  L.dd = take(tok * sizeof(float));
+  L.dd = take((size_t)s.TC() * C * sizeof(float));
   L.total = off;
   return L;
 }
@@ -874,7 +973,7 @@ cudaError_t launch_backward_prefix64(const PrefillArgs& a, const float* dO, cons
   e = launch_prefix64_pair(a, b, stream);
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mq, mo, mdo, mphiq, mdn, mgt, mphik, mv, mp;
+  CUtensorMap mq, mo, mdo, mphiq, mdn, mgt, mphik, mv, mp, mdq, mdk, mdv;
   uint8_t* GT = ws + L.GT;
   if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mo, b.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
@@ -884,7 +983,10 @@ cudaError_t launch_backward_prefix64(const PrefillArgs& a, const float* dO, cons
       !make_map(&mgt, GT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, (int)sp.TC(), 64, XROWS) ||
       !make_map(&mphik, b.phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
-      !make_map(&mp, b.P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, (int)sp.TC(), 64, XROWS))
+      !make_map(&mp, b.P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, (int)sp.TC(), 64, XROWS) ||
+      !make_map(&mdq, dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
+      !make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
+      !make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C))
     return cudaErrorInvalidValue;
 
   gpx::Params gp = {};
@@ -928,7 +1030,8 @@ cudaError_t launch_backward_prefix64(const PrefillArgs& a, const float* dO, cons
   if (e != cudaSuccess) return e;
   cfg.blockDim = dim3(grd::kThreads);
   cfg.dynamicSmemBytes = grd::SMEM;
-  return cudaLaunchKernelEx(&cfg, grd::grad_kernel, mphiq, mphik, mv, mdn, mp, mgt, rp, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, grd::grad_kernel, mphiq, mphik, mv, mdn, mp, mgt, mdq, mdk, mdv, rp,
+                            mbar_ns);
 }
 
 }  // namespace la
