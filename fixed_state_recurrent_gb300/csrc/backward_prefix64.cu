@@ -135,14 +135,16 @@ __device__ __forceinline__ float tile_at(const uint8_t* tile, int row, int col) 
 
 namespace gpx {
 
-constexpr int NS = 2;
-// stage: Q | o (two [128 x 32] fp32 boxes) | dO (two boxes).  The D warps
-// overwrite Q with phi(Q), o's first box with dnum (bf16 tile) and o's second
-// box with the dden block (column 0 = dden, the rest zero): the A operand
-// [dnum | dden] of the increment, M = 128 over its two 64-column blocks.
+constexpr int NS = 3;
+// stage: Q | o (bf16 tile) | dO (two [128 x 32] fp32 boxes).  The D warps
+// overwrite Q with phi(Q), o with dnum (bf16 tile) and dO's second box with
+// the dden block (column 0 = dden, the rest zero): the A operand
+// [dnum | dden] of the increment, M = 128 over its two 64-column blocks
+// (2 * BLK apart).
 constexpr uint32_t OFF_O = BLK;
-constexpr uint32_t OFF_DO = 3 * BLK;
-constexpr uint32_t STAGE = 5 * BLK;
+constexpr uint32_t OFF_DO = 2 * BLK;
+constexpr uint32_t OFF_DD = OFF_DO + BLK;
+constexpr uint32_t STAGE = 4 * BLK;
 constexpr uint32_t PST = 9 * 1024;          // staging of one state tile (66 rows)
 constexpr uint32_t OFF_PST = NS * STAGE;
 constexpr uint32_t OFF_BAR = OFF_PST + 2 * PST;
@@ -234,10 +236,9 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           if (sj >= NS && !waitb(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           uint8_t* st = smem + s * STAGE;
           const int tok = pc.tok0 + c * C;
-          mbar_arrive_expect_tx(&B->full[s], 5 * BLK);
+          mbar_arrive_expect_tx(&B->full[s], 4 * BLK);
           tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->full[s]);
           tma_load_3d_ef(st + OFF_O, &tm_o, 0, tok, pc.h, &B->full[s]);
-          tma_load_3d_ef(st + OFF_O + BLK, &tm_o, 32, tok, pc.h, &B->full[s]);
           tma_load_3d_ef(st + OFF_DO, &tm_do, 0, tok, pc.h, &B->full[s]);
           tma_load_3d_ef(st + OFF_DO + BLK, &tm_do, 32, tok, pc.h, &B->full[s]);
           ++issued;
@@ -255,7 +256,7 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (j < 16) BW_TRACE(1, 2 + j);
         tc_fence_after();
         const uint32_t qt = smem_u32(smem + s * STAGE), dn = qt + OFF_O;
-        const uint64_t a0 = sdesc_sw128(dn, BLK, 1024), b0 = sdesc_sw128(qt, BLK, 1024);
+        const uint64_t a0 = sdesc_sw128(dn, OFF_DD - OFF_O, 1024), b0 = sdesc_sw128(qt, BLK, 1024);
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks)
           mma_bf16_ss(x.tmem + 64 * b, a0 + ks * kStepRows16, b0 + ks * kStepRows16, ID_DG, ks > 0 ? 1u : 0u);
@@ -283,32 +284,37 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!waitb_warp(x, &B->full[s], (sj / NS) & 1)) continue;
         uint8_t* st = smem + s * STAGE;
         phi_row<4>(st, r, 4 * hf, valid);
-        // this thread's 32 columns of o and dO: box hf of each
-        const uint8_t* ob = st + OFF_O + hf * BLK;
+        // this thread's 32 columns of o (chunks 4 hf.. of its bf16 row) and of
+        // dO (box hf)
         const uint8_t* gb = st + OFF_DO + hf * BLK;
         float g[32], dot = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-          const float4 o4 = *reinterpret_cast<const float4*>(ob + sw128_offset(r, cc));
           const float4 g4 = *reinterpret_cast<const float4*>(gb + sw128_offset(r, cc));
           g[4 * cc] = g4.x;
           g[4 * cc + 1] = g4.y;
           g[4 * cc + 2] = g4.z;
           g[4 * cc + 3] = g4.w;
-          dot += o4.x * g4.x + o4.y * g4.y + o4.z * g4.z + o4.w * g4.w;
         }
-        // after the exchange both halves have read their o and dO: row r of
-        // o's boxes may be overwritten
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = *reinterpret_cast<const uint4*>(st + OFF_O + sw128_offset(r, 4 * hf + q));
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dot += __uint_as_float(w4[e] << 16) * g[8 * q + 2 * e] +
+                   __uint_as_float(w4[e] & 0xFFFF0000u) * g[8 * q + 2 * e + 1];
+        }
         dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 1);
         const float inv = r < valid ? 1.f / den : 0.f;
         const float dden = -dot * inv;
 #pragma unroll
         for (int e = 0; e < 32; ++e) g[e] *= inv;
-        uint8_t* dn = st + OFF_O;  // dnum: columns 32 hf .. 32 hf + 31 of row r
+        uint8_t* dn = st + OFF_O;  // dnum over the bytes of o this thread read
 #pragma unroll
         for (int q = 0; q < 4; ++q) put8(dn, r, 4 * hf + q, g + 8 * q);
-        if (hf == 1) {  // the dden block's row r
-          uint8_t* db = st + OFF_O + BLK;
+        if (hf == 1) {  // the dden block's row r, over the row of dO's box 1 this thread read
+          uint8_t* db = st + OFF_DD;
           *reinterpret_cast<uint4*>(db + sw128_offset(r, 0)) = make_uint4(pack_bf16x2(dden, 0.f), 0u, 0u, 0u);
 #pragma unroll
           for (int q = 1; q < 8; ++q) *reinterpret_cast<uint4*>(db + sw128_offset(r, q)) = make_uint4(0u, 0u, 0u, 0u);
@@ -445,11 +451,11 @@ namespace grd {
 constexpr uint32_t OFF_KF = BLK, OFF_V = 2 * BLK, OFF_DN = 3 * BLK;
 constexpr uint32_t OFF_ST = 4 * BLK, OFF_GT = 4 * BLK + XT;
 constexpr uint32_t STAGE = 4 * BLK + 2 * XT;
-constexpr uint32_t OFF_E = 2 * STAGE;        // E, EG: bf16 tiles (rows 0..63 used)
+constexpr uint32_t OFF_E = 2 * STAGE;        // E (66 rows, from the output kernel), EG (rows 0..63)
 constexpr uint32_t OFF_EG = OFF_E + XT;
 constexpr uint32_t OFF_OUT = OFF_EG + XT;    // dq staging: two [128 x 32] fp32 boxes
-constexpr uint32_t OFF_VEC = OFF_OUT + 2 * BLK;  // floats: dd[2][128], zc[64], gc[64], zE[64], gE[64]
-constexpr uint32_t OFF_BAR = OFF_VEC + (2 * 128 + 4 * 64) * 4;
+constexpr uint32_t OFF_VEC = OFF_OUT + 2 * BLK;  // floats: dd[2][128], zc[64], gc[64], gE[64]
+constexpr uint32_t OFF_BAR = OFF_VEC + (2 * 128 + 3 * 64) * 4;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
 static_assert(STAGE % 1024 == 0 && OFF_GT % 1024 == 0 && OFF_E % 1024 == 0 && OFF_EG % 1024 == 0 &&
               OFF_OUT % 1024 == 0, "swizzled tile alignment");
@@ -466,7 +472,6 @@ constexpr uint32_t ID_N64_K = idesc_bf16_f32(128, 64, 0, 0);   // both K-major, 
 
 struct Params {
   Split sp;
-  const float* R;     // forward piece totals (slot layout; with S0)
   const float* RG;    // gradient piece totals (slot layout; with dS_N)
   const float* dden;  // [BH * NC][128]
   float* dq;
@@ -617,15 +622,15 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dn,
             const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_gt,
             const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
-            const __grid_constant__ CUtensorMap tm_dv, const Params p, const unsigned long long mbar_ns) {
+            const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_e,
+            const Params p, const unsigned long long mbar_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
   float* dd = reinterpret_cast<float*>(smem + OFF_VEC);  // [2][128]
   float* zc = dd + 256;
   float* gc = zc + 64;
-  float* zE = gc + 64;
-  float* gE = zE + 64;
+  float* gE = gc + 64;
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
   const int row = t & (C - 1), hf = t >> 7, quad = warp & 3;
   const Split& sp = p.sp;
@@ -649,6 +654,7 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
     tma_prefetch_desc(&tm_dq);
     tma_prefetch_desc(&tm_dk);
     tma_prefetch_desc(&tm_dv);
+    tma_prefetch_desc(&tm_e);
   }
   if (warp == 0) {
     tmem_alloc(&B->tmem_slot, kCols);
@@ -670,12 +676,15 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
   // thread 32 (kLd): the loads of the run's chunk j into stage j % 2 and its
   // dden into dd[j % 2]; it also issues the output stores
   constexpr int kLd = 32;
+  const bool haveE = total > 0 && run.idx0 > 0;
   auto load = [&](uint32_t j) {
     const int s = j % 2;
     uint8_t* st = smem + s * STAGE;
     const long long gi = run.a + j;
     const int h = (int)(gi / NC), tok = (int)(gi % NC) * C;
-    mbar_arrive_expect_tx(&B->full[s], 4 * BLK + 2 * XG + C * 4);
+    const bool withE = j == 0 && haveE;  // the first piece's entry-state tile comes with chunk 0
+    mbar_arrive_expect_tx(&B->full[s], 4 * BLK + 2 * XG + C * 4 + (withE ? XG : 0));
+    if (withE) tma_load_3d_ef(smem + OFF_E, &tm_e, 0, 0, (int)blockIdx.x, &B->full[s]);
     bulk_load(dd + s * C, p.dden + (size_t)gi * C, C * 4, &B->full[s]);
     tma_load_3d_ef(st, &tm_phiq, 0, tok, h, &B->full[s]);
     tma_load_3d_ef(st + OFF_KF, &tm_phik, 0, tok, h, &B->full[s]);
@@ -685,19 +694,18 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
     tma_load_3d_ef(st + OFF_GT, &tm_gt, 0, 0, (int)gi, &B->full[s]);
     ++nload;
   };
+
   if (t == kLd && total > 0) load(0);
 
   // The first piece's entry state E (the forward totals of the head's earlier
   // blocks), the last piece's exit gradient state EG (the gradient totals of
   // the head's later blocks), and dS0, dz0 of every head that starts here.
   const int h0 = run.h0, hl = total > 0 ? (int)((run.b - 1) / NC) : h0;
-  const bool haveE = total > 0 && run.idx0 > 0;
   const bool lastContinues = total > 0 && (run.b - (long long)hl * NC) < NC;
   const int npieces = total > 0 ? hl - h0 + 1 : 0;
   // position of this block among the blocks meeting head hl, and their count
   const int idxl = npieces == 1 ? run.idx0 : 0;
   const int nbl = sp.owner((long long)hl * NC + NC - 1) - sp.owner((long long)hl * NC) + 1;
-  if (haveE) sum_slots(p.R, (size_t)h0 * sp.MPH, 0, run.idx0, smem + OFF_E, zE, nullptr, nullptr, nullptr, t, kThreads);
   if (lastContinues) {
     const bool starts = (long long)hl * NC >= run.a;  // head hl's first chunk is in this run
     const float* own = p.RG + ((size_t)hl * sp.MPH + idxl) * SZ;
@@ -735,42 +743,39 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
   // dU = V (G_c)^T of the run's chunk j, once its tiles are in
   auto issue_first = [&](uint32_t j) {
     const int s = j % 2;
-    const long long gi = run.a + j;
-    const int h = (int)(gi / NC);
+    const int h = (int)((run.a + j) / NC);
     const bool useE = haveE && h == h0, useEG = lastContinues && h == hl;
-    const uint32_t aQ = smem_u32(smem + s * STAGE), aK = aQ + OFF_KF, aV = aQ + OFF_V, aD = aQ + OFF_DN;
-    const uint32_t aS = aQ + OFF_ST, aG = aQ + OFF_GT;
+    const uint32_t aQ = smem_u32(smem + s * STAGE);
+    // K-major operands step 32 bytes along K, MN-major ones 16 rows
+    const uint64_t dQ = sdesc_sw128(aQ, 16, 1024), dK = sdesc_sw128(aQ + OFF_KF, 16, 1024);
+    const uint64_t dV = sdesc_sw128(aQ + OFF_V, 16, 1024), dD = sdesc_sw128(aQ + OFF_DN, 16, 1024);
+    const uint64_t dS = sdesc_sw128(aQ + OFF_ST, 16, 1024), dG = sdesc_sw128(aQ + OFF_GT, 16, 1024);
     if (waitb(x, &B->full[s], (j / 2) & 1) && (!p.force_wait || j > 0 || waitb(x, &B->never, 0)) &&
         issuing()) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_A1, sdesc_sw128(aD + ks * 32, 16, 1024), sdesc_sw128(aV + ks * 32, 16, 1024), ID_S,
-                    ks > 0);
+        mma_bf16_ss(tm + T_A1, dD + ks * kStepK16, dV + ks * kStepK16, ID_S, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_A2, sdesc_sw128(aV + ks * 32, 16, 1024), sdesc_sw128(aD + ks * 32, 16, 1024), ID_S,
-                    ks > 0);
+        mma_bf16_ss(tm + T_A2, dV + ks * kStepK16, dD + ks * kStepK16, ID_S, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_A3, sdesc_sw128(aK + ks * 32, 16, 1024), sdesc_sw128(aQ + ks * 32, 16, 1024), ID_S,
-                    ks > 0);
+        mma_bf16_ss(tm + T_A3, dK + ks * kStepK16, dQ + ks * kStepK16, ID_S, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_DW, sdesc_sw128(aD + ks * 32, 16, 1024), sdesc_sw128(aS + ks * 2048, 16, 1024),
-                    ID_N64_MN, ks > 0);
+        mma_bf16_ss(tm + T_DW, dD + ks * kStepK16, dS + ks * kStepRows16, ID_N64_MN, ks > 0);
       if (useE) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_bf16_ss(tm + T_DW, sdesc_sw128(aD + ks * 32, 16, 1024), eS + ks * kStepRows16, ID_N64_MN, 1u);
+          mma_bf16_ss(tm + T_DW, dD + ks * kStepK16, eS + ks * kStepRows16, ID_N64_MN, 1u);
       }
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_DU, sdesc_sw128(aV + ks * 32, 16, 1024), sdesc_sw128(aG + ks * 2048, 16, 1024),
-                    ID_N64_MN, ks > 0);
+        mma_bf16_ss(tm + T_DU, dV + ks * kStepK16, dG + ks * kStepRows16, ID_N64_MN, ks > 0);
       if (useEG) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_bf16_ss(tm + T_DU, sdesc_sw128(aV + ks * 32, 16, 1024), eG + ks * kStepRows16, ID_N64_MN, 1u);
+          mma_bf16_ss(tm + T_DU, dV + ks * kStepK16, eG + ks * kStepRows16, ID_N64_MN, 1u);
       }
     }
     mma_commit(&B->mma);
@@ -791,7 +796,8 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
     waitb(x, &B->full[s], (j / 2) & 1);
     if (t == 0 && j < 8) BW_TRACE(0, 3 + 6 * j);
     if (t < D) {
-      zc[t] = tile_at(st + OFF_ST, 64, t) + tile_at(st + OFF_ST, 65, t) + (useE ? zE[t] : 0.f);
+      zc[t] = tile_at(st + OFF_ST, 64, t) + tile_at(st + OFF_ST, 65, t) +
+              (useE ? tile_at(smem + OFF_E, 64, t) + tile_at(smem + OFF_E, 65, t) : 0.f);
     } else if (t < 2 * D) {
       const int i = t - D;
       gc[i] = tile_at(st + OFF_GT, 64, i) + tile_at(st + OFF_GT, 65, i) + (useEG ? gE[i] : 0.f);
@@ -908,7 +914,7 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
 
 // Workspace layout (byte offsets, each 256-byte aligned).
 struct Layout {
-  size_t R, P, phik, o, den, SN, RG, GT, phiq, dn, dd, total;
+  size_t R, P, phik, o, den, E, SN, RG, GT, phiq, dn, dd, total;
 };
 
 inline size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -925,8 +931,9 @@ Layout layout(int BH, int N, const Split& s) {
   L.R = take(slots * SZ * sizeof(float));
   L.P = take((size_t)s.TC() * XG);
   L.phik = take(tok * D * 2);
-  L.o = take(tok * D * sizeof(float));
+  L.o = take(tok * D * 2);
   L.den = take(tok * sizeof(float));
+  L.E = take((size_t)s.G * XG);
   L.SN = take((size_t)BH * SZ * sizeof(float));
   L.RG = take(slots * SZ * sizeof(float));
   L.GT = take((size_t)s.TC() * XG);
@@ -964,8 +971,9 @@ cudaError_t launch_backward_prefix64(const PrefillArgs& a, const float* dO, cons
   b.R = reinterpret_cast<float*>(ws + L.R);
   b.P = ws + L.P;
   b.phik = reinterpret_cast<__nv_bfloat16*>(ws + L.phik);
-  b.o = reinterpret_cast<float*>(ws + L.o);
+  b.o = ws + L.o;
   b.den = reinterpret_cast<float*>(ws + L.den);
+  b.E = ws + L.E;
   b.S_N = reinterpret_cast<float*>(ws + L.SN);
   b.z_N = b.S_N + (size_t)BH * D * D;
   b.status = status;
@@ -973,10 +981,11 @@ cudaError_t launch_backward_prefix64(const PrefillArgs& a, const float* dO, cons
   e = launch_prefix64_pair(a, b, stream);
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mq, mo, mdo, mphiq, mdn, mgt, mphik, mv, mp, mdq, mdk, mdv;
+  CUtensorMap mq, mo, mdo, mphiq, mdn, mgt, mphik, mv, mp, mdq, mdk, mdv, me;
   uint8_t* GT = ws + L.GT;
   if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
-      !make_map(&mo, b.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
+      !make_map(&mo, b.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&me, b.E, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, sp.G, 64, XROWS) ||
       !make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
       !make_map(&mphiq, ws + L.phiq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mdn, ws + L.dn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
@@ -1000,7 +1009,6 @@ cudaError_t launch_backward_prefix64(const PrefillArgs& a, const float* dO, cons
 
   grd::Params rp = {};
   rp.sp = sp;
-  rp.R = b.R;
   rp.RG = gp.RG;
   rp.dden = gp.dden;
   rp.dq = dq;
@@ -1030,7 +1038,7 @@ cudaError_t launch_backward_prefix64(const PrefillArgs& a, const float* dO, cons
   if (e != cudaSuccess) return e;
   cfg.blockDim = dim3(grd::kThreads);
   cfg.dynamicSmemBytes = grd::SMEM;
-  return cudaLaunchKernelEx(&cfg, grd::grad_kernel, mphiq, mphik, mv, mdn, mp, mgt, mdq, mdk, mdv, rp,
+  return cudaLaunchKernelEx(&cfg, grd::grad_kernel, mphiq, mphik, mv, mdn, mp, mgt, mdq, mdk, mdv, me, rp,
                             mbar_ns);
 }
 

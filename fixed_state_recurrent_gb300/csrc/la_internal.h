@@ -112,17 +112,20 @@ cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream);
 // The same two launches with every buffer given: R piece totals ([BH * MPH]
 // slots of 64 * 64 + 64 floats, MPH of prefill_tc_common.cuh's make_split over
 // the current device's SMs), P prefix tiles ([BH * ceil(N / 128)][66][64]
-// bf16), phik ([BH][N][64] bf16), o ([BH][N][64] fp32), den (NULL, or
-// [BH][N] fp32: den_t = phi(q_t)^T z_t + eps), S_N and z_N (B * H final
-// states), status (where bounded waits that give up are recorded);
-// force_wait: the test hook of the output kernel.  q, k, v, S0, z0, N, eps
-// come from a.
+// bf16), phik ([BH][N][64] bf16), o ([BH][N][64]: fp32, or bf16 when den is
+// given), den (NULL, or [BH][N] fp32: den_t = phi(q_t)^T z_t + eps), E (with
+// den: [G][66][64] bf16, G the split's block count: the entry-state tile of
+// each block whose first piece has one, in the prefix tiles' format), S_N and
+// z_N (B * H final states), status (where bounded waits that give up are
+// recorded); force_wait: the test hook of the output kernel.  q, k, v, S0,
+// z0, N, eps come from a.
 struct Prefix64Buffers {
   float* R;
   uint8_t* P;
   __nv_bfloat16* phik;
-  float* o;
+  void* o;
   float* den;
+  uint8_t* E;
   float* S_N;
   float* z_N;
   unsigned* status;

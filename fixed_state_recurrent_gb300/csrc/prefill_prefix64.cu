@@ -90,7 +90,7 @@ struct Params {
   unsigned* status;    // sticky error bits (the workspace header's, or the library's)
   float* R;            // [BH * MPH][SZ] piece totals (slot layout)
   uint8_t* P;          // [TC][66][64] bf16 prefix tiles
-  float* den;          // NULL, or [BH][N]: the output kernel also stores den_t = phi(q_t)^T z_t + eps
+  float* den;          // [BH][N] den_t = phi(q_t)^T z_t + eps (the output kernel's BWD form only)
   int force_wait;      // test hook: the output kernel waits once on a barrier that nothing completes
 };
 
@@ -565,12 +565,15 @@ __device__ __forceinline__ void store_final_later(const Params& p, const Run& ru
 }
 
 // Q, phi(K), P, V and o are touched once here and go through TMA with the
-// evict-first L2 policy.
+// evict-first L2 policy.  BWD (the gradient's second launch): den goes to
+// p.den, o out as bf16 (tm_o) and the entry-state tile to slot blockIdx.x of
+// tm_e.
+template <bool BWD>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_phik,
               const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_v,
-              const __grid_constant__ CUtensorMap tm_o, const Params p,
-              const unsigned long long mbar_ns) {
+              const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_e,
+              const Params p, const unsigned long long mbar_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
@@ -604,6 +607,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     tma_prefetch_desc(&tm_p);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
+    if (BWD) tma_prefetch_desc(&tm_e);
   }
   // The first stages' Q and V (inputs of the call) go out before the earlier
   // launch has finished, so that phi(Q) of the first chunks is ready when it
@@ -717,6 +721,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       uint32_t as = 0, ap = 0, idle = 0;
       const uint32_t n = (uint32_t)total;
       bool ok = (!p.force_wait || waitb(x, &B->never, 0)) && (nE == 0 || waitb(x, &B->eready, 0));
+      if (BWD && ok && nE > 0) {  // the entry-state tile, for the gradient's last launch
+        tma_store_3d(&tm_e, smem + OFF_E, 0, 0, (int)blockIdx.x);
+        bulk_commit();
+      }
       uint64_t dl = globaltimer_ns() + mbar_ns;
       while (ok && ap < n) {
         if (*x.abort) break;
@@ -773,6 +781,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mma_commit(&B->drain);
         mbar_wait(&B->drain, 0, globaltimer_ns() + mbar_ns, &never);
       }
+      if (BWD) bulk_wait_all();
     }
     __syncwarp();
   } else if (warp < 10) {
@@ -915,27 +924,43 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (lane == 0) mbar_arrive(&B->ofree[ob]);
           const float den = __uint_as_float(d2[0]) + __uint_as_float(d2[1]) + p.eps;
           const float inv = 1.f / den;
-          if (p.den && row < pc.tok1 - (pc.tok0 + c * C) && !*x.abort)
+          if (BWD && row < pc.tok1 - (pc.tok0 + c * C) && !*x.abort)
             p.den[(size_t)pc.h * p.sp.N + pc.tok0 + c * C + row] = den;
           if (et == 32) bulk_wait_read_all();  // the previous chunk's store has read the staging
           named_bar_sync(5, 128);
+          if (BWD) {  // o as bf16, one [128 x 64] tile
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-            *reinterpret_cast<float4*>(out + sw128_offset(row, cc)) =
-                make_float4(__uint_as_float(n0[4 * cc]) * inv, __uint_as_float(n0[4 * cc + 1]) * inv,
-                            __uint_as_float(n0[4 * cc + 2]) * inv, __uint_as_float(n0[4 * cc + 3]) * inv);
+            for (int cc = 0; cc < 4; ++cc)
+              *reinterpret_cast<uint4*>(out + sw128_offset(row, cc)) =
+                  make_uint4(pack_bf16x2(__uint_as_float(n0[8 * cc]) * inv, __uint_as_float(n0[8 * cc + 1]) * inv),
+                             pack_bf16x2(__uint_as_float(n0[8 * cc + 2]) * inv, __uint_as_float(n0[8 * cc + 3]) * inv),
+                             pack_bf16x2(__uint_as_float(n0[8 * cc + 4]) * inv, __uint_as_float(n0[8 * cc + 5]) * inv),
+                             pack_bf16x2(__uint_as_float(n0[8 * cc + 6]) * inv, __uint_as_float(n0[8 * cc + 7]) * inv));
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-            *reinterpret_cast<float4*>(out + BLK + sw128_offset(row, cc)) =
-                make_float4(__uint_as_float(n1[4 * cc]) * inv, __uint_as_float(n1[4 * cc + 1]) * inv,
-                            __uint_as_float(n1[4 * cc + 2]) * inv, __uint_as_float(n1[4 * cc + 3]) * inv);
+            for (int cc = 0; cc < 4; ++cc)
+              *reinterpret_cast<uint4*>(out + sw128_offset(row, 4 + cc)) =
+                  make_uint4(pack_bf16x2(__uint_as_float(n1[8 * cc]) * inv, __uint_as_float(n1[8 * cc + 1]) * inv),
+                             pack_bf16x2(__uint_as_float(n1[8 * cc + 2]) * inv, __uint_as_float(n1[8 * cc + 3]) * inv),
+                             pack_bf16x2(__uint_as_float(n1[8 * cc + 4]) * inv, __uint_as_float(n1[8 * cc + 5]) * inv),
+                             pack_bf16x2(__uint_as_float(n1[8 * cc + 6]) * inv, __uint_as_float(n1[8 * cc + 7]) * inv));
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+              *reinterpret_cast<float4*>(out + sw128_offset(row, cc)) =
+                  make_float4(__uint_as_float(n0[4 * cc]) * inv, __uint_as_float(n0[4 * cc + 1]) * inv,
+                              __uint_as_float(n0[4 * cc + 2]) * inv, __uint_as_float(n0[4 * cc + 3]) * inv);
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+              *reinterpret_cast<float4*>(out + BLK + sw128_offset(row, cc)) =
+                  make_float4(__uint_as_float(n1[4 * cc]) * inv, __uint_as_float(n1[4 * cc + 1]) * inv,
+                              __uint_as_float(n1[4 * cc + 2]) * inv, __uint_as_float(n1[4 * cc + 3]) * inv);
+          }
           fence_proxy_async_smem();
           named_bar_sync(5, 128);
           if (et == 32 && !*x.abort) {
             const int tok = pc.tok0 + c * C;
-            if (p.den) {  // o is read again soon (the gradient's next launch)
+            if (BWD) {  // read again soon (the gradient's next launch)
               tma_store_3d(&tm_o, out, 0, tok, pc.h);
-              tma_store_3d(&tm_o, out + BLK, 32, tok, pc.h);
             } else {
               tma_store_3d_ef(&tm_o, out, 0, tok, pc.h);
               tma_store_3d_ef(&tm_o, out + BLK, 32, tok, pc.h);
@@ -987,21 +1012,26 @@ cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b,
   p.P = b.P;
   p.den = b.den;
   p.force_wait = b.force_wait;
-  CUtensorMap mq, mk, mv, mo, mphik, mp;
+  CUtensorMap mq, mk, mv, mo, mphik, mp, me;
+  const bool bwd = b.den != nullptr;
+  if (bwd && !b.E) return cudaErrorInvalidValue;
   if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
-      !make_map(&mo, b.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
+      !(bwd ? make_map(&mo, b.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C)
+            : make_map(&mo, b.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C)) ||
       !make_map(&mphik, b.phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
-      !make_map(&mp, p.P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, (int)p.sp.TC(), 64, XROWS))
+      !make_map(&mp, p.P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, (int)p.sp.TC(), 64, XROWS) ||
+      !make_map(&me, bwd ? b.E : p.P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS,
+                bwd ? p.sp.G : (int)p.sp.TC(), 64, XROWS))
     return cudaErrorInvalidValue;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
 
   cudaError_t e = cudaFuncSetAttribute(pfx::prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pfx::SMEM);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(out::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)out::SMEM);
+    e = cudaFuncSetAttribute(bwd ? out::output_kernel<true> : out::output_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)out::SMEM);
   if (e != cudaSuccess) return e;
   // Both launches are programmatic dependents of what precedes them on the
   // stream: their blocks may start while the kernel before runs, and wait for
@@ -1021,7 +1051,8 @@ cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b,
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * out::kWarps);
   cfg.dynamicSmemBytes = out::SMEM;
-  return cudaLaunchKernelEx(&cfg, out::output_kernel, mq, mphik, mp, mv, mo, p, mbar_ns);
+  if (bwd) return cudaLaunchKernelEx(&cfg, out::output_kernel<true>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, out::output_kernel<false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
 }
 
 cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
@@ -1038,6 +1069,7 @@ cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
   b.phik = reinterpret_cast<__nv_bfloat16*>(b.P + (size_t)sp.TC() * XG);
   b.o = a.o;
   b.den = nullptr;
+  b.E = nullptr;
   b.S_N = a.S_N;
   b.z_N = a.z_N;
   b.status = a.status ? a.status : &reinterpret_cast<WsHeader*>(ws)->status;
