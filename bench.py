@@ -561,8 +561,8 @@ def bench_decay_prefill(api, rank, world, reps=12, sets=4):
 
 def bench_backward(api, rank, world, reps=5):
     """la_prefill_backward on the headline prefill shape (dO ~ N(0,1)): tensor
-    cores, a forward and a reverse sweep, the heads split over every SM (the
-    default, with a workspace); the one-block-per-head form beside it."""
+    cores, every chunk independent from per-chunk state tiles over every SM (the
+    default, with a workspace); the one-block-per-head sweeps beside it."""
     import torch
     w = inputs_mod().WORKLOADS["prefill"]
     dev = torch.device("cuda")

@@ -167,14 +167,18 @@ size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv,
  *              that share a workspace must be ordered on one stream.
  * Outputs must not overlap any input, each other or the workspace (a
  * workspace smaller than asked for is LA_ERR_INVALID_ARG).  LA_BF16 at
- * dk = dv = 64 runs on the tensor cores: a forward and a reverse sweep over
- * 128-token chunks (bf16 operands, fp32 accumulation; dv_out holds bf16
- * intermediate rows between the sweeps).  With a workspace the heads are cut
- * into pieces over every SM (the prefill's own aggregate and scan give each
- * piece its entry state, a reverse scan its gradient state); with NULL, one
- * block per head.  A bounded wait of those kernels that gives up is reported
- * by delta_read_device_status.  Everything else runs on the CUDA cores in
- * fp32, one block per head, token by token, with no workspace; any dk, dv <= 128.
+ * dk = dv = 64 runs on the tensor cores (bf16 operands, fp32 accumulation),
+ * the heads cut into pieces over every SM when a workspace is given: calls of
+ * at most 2048 chunks of 128 tokens (B * H * ceil(N / 128)) take every chunk
+ * independently from per-chunk state tiles (four launches: the prefill's
+ * prefix tiles and outputs, the gradient-state tiles, then dq, dk, dv), larger
+ * ones a forward and a reverse sweep over each piece (the prefill's own
+ * aggregate and scan give each piece its entry state, a reverse scan its
+ * gradient state; dv_out holds bf16 intermediate rows between the sweeps).
+ * With NULL, one block per head, both sweeps.  A bounded wait of those kernels
+ * that gives up is reported by delta_read_device_status.  Everything else runs
+ * on the CUDA cores in fp32, one block per head, token by token, with no
+ * workspace; any dk, dv <= 128.
  */
 la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dtype in_dtype,
                               int B, int H, int N, int dk, int dv, float eps,
