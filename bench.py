@@ -59,7 +59,7 @@ def _args():
                    help="headline workload only (no long/decode/delta/e2e/cpu)")
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run "
-                        "(long,decode,delta,pr1,gated,decay,backward,prefill128)")
+                        "(long,decode,delta,pr1,gated,decay,rbw,backward,prefill128)")
     p.add_argument("--profile-backward", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain la_prefill_backward calls and exit (for ncu)")
     p.add_argument("--profile-decay", type=int, default=0, metavar="CALLS",
@@ -593,6 +593,43 @@ def bench_backward(api, rank, world, reps=5):
             "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": f"of {kind}"}
 
 
+def bench_rbw_prefill(api, rank, world, reps=12, sets=4):
+    """la_prefill_variant in read-before-write order (no decay) on the headline
+    prefill shape: tensor cores, la_prefill's two launches with a strict mask,
+    over `sets` rotating input/output sets."""
+    import torch
+    w = inputs_mod().WORKLOADS["prefill"]
+    dev = torch.device("cuda")
+    bufs = []
+    for r in range(sets):
+        q, k, v = _device_inputs(w, w.seed + 1000 * rank + r, dev)
+        bufs.append((q, k, v, torch.empty((w.B, w.H, w.N, w.dv), device=dev),
+                     torch.empty((w.B, w.H, w.dk, w.dv), device=dev),
+                     torch.empty((w.B, w.H, w.dk), device=dev)))
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+
+    def fn(i):
+        q, k, v, o, S, z = bufs[i % sets]
+        api.prefill_variant(q, k, v, None, api.LA_MODE_READ_BEFORE_WRITE, o=o, S_N=S, z_N=z)
+
+    with torch.cuda.stream(stream):
+        for i in range(sets):
+            fn(i)
+    _, per = _timed(fn, reps, stream, world)
+    ms_calls = statistics.median(per)
+    ms = _graph_ms(fn, 4 * sets, stream, world)
+    b = PREFILL_BYTES_PER_TOKEN * w.tokens
+    hbm_peak, _, kind = _peaks()
+    return {"workload": "read-before-write prefill: B=4 H=8 N=4096 dk=dv=64 bf16",
+            "ms_per_call": ms, "ms_per_python_call": ms_calls,
+            "timing": f"{4 * sets} calls in one CUDA graph, replayed (device time per call); "
+                      "ms_per_python_call: median of back-to-back calls from Python",
+            "tokens_per_s": w.tokens / (ms * 1e-3), "hbm_gbs": b / (ms * 1e-3) / 1e9,
+            "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": f"of {kind}",
+            "l2": f"{sets} rotating input/output sets"}
+
+
 def inputs_mod():
     from fixed_state_recurrent_gb300 import inputs
     return inputs
@@ -797,7 +834,7 @@ def main():
     extra = {}
     e2e = None
     wanted = set(x for x in args.only.split(",") if x) or {"long", "decode", "delta", "pr1",
-                                                             "gated", "decay", "backward",
+                                                             "gated", "decay", "rbw", "backward",
                                                              "prefill128"}
     if not args.no_extra:
         if "long" in wanted:
@@ -814,6 +851,8 @@ def main():
             extra["gated_delta"] = bench_gated_delta(api, rank, world)
         if "decay" in wanted:
             extra["decay_prefill"] = bench_decay_prefill(api, rank, world)
+        if "rbw" in wanted:
+            extra["rbw_prefill"] = bench_rbw_prefill(api, rank, world)
         if "backward" in wanted:
             extra["backward"] = bench_backward(api, rank, world)
         e_steps = min(max(args.steps // 4, 20), 200)  # at least 20 steps whatever --steps is

@@ -130,8 +130,14 @@ struct Prefix64Buffers {
   float* z_N;
   unsigned* status;
   int force_wait;
+  int strict;  // read before write (keys s < t inside a chunk); not with den
 };
 cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b, cudaStream_t stream);
+// Read-before-write order (la_prefill_variant's LA_MODE_READ_BEFORE_WRITE, no
+// decay) in the same two launches, for the calls prefill_prefix64_chosen
+// takes; a.workspace of at least prefill_prefix64_workspace_bytes (no header;
+// bounded-wait failures go to the library status word).
+cudaError_t launch_prefill_rbw64(const PrefillArgs& a, cudaStream_t stream);
 
 // The gradient of the prefill for bf16 at dk = dv = 64, chunk-parallel in four
 // launches (backward_prefix64.cu): the two launches above (o and den into the

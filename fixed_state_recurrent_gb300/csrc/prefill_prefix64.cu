@@ -567,8 +567,9 @@ __device__ __forceinline__ void store_final_later(const Params& p, const Run& ru
 // Q, phi(K), P, V and o are touched once here and go through TMA with the
 // evict-first L2 policy.  BWD (the gradient's second launch): den goes to
 // p.den, o out as bf16 (tm_o) and the entry-state tile to slot blockIdx.x of
-// tm_e.
-template <bool BWD>
+// tm_e.  STRICT: read before write (token t reads the state before its own
+// write: keys s < t inside the chunk).
+template <bool BWD, bool STRICT>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_phik,
               const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_v,
@@ -855,8 +856,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           } else {
 #pragma unroll
             for (int t2 = 0; t2 < 16; ++t2)
-              w[t2] = pack_bf16x2(2 * t2 <= lane ? __uint_as_float(r[2 * t2]) : 0.f,
-                                  2 * t2 + 1 <= lane ? __uint_as_float(r[2 * t2 + 1]) : 0.f);
+              w[t2] = pack_bf16x2((STRICT ? 2 * t2 < lane : 2 * t2 <= lane) ? __uint_as_float(r[2 * t2]) : 0.f,
+                                  (STRICT ? 2 * t2 + 1 < lane : 2 * t2 + 1 <= lane)
+                                      ? __uint_as_float(r[2 * t2 + 1]) : 0.f);
           }
         }
         tmem_st16(base + 64 * half + 16 * k, w);  // over this warp's own block q0's scores
@@ -1014,7 +1016,7 @@ cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b,
   p.force_wait = b.force_wait;
   CUtensorMap mq, mk, mv, mo, mphik, mp, me;
   const bool bwd = b.den != nullptr;
-  if (bwd && !b.E) return cudaErrorInvalidValue;
+  if ((bwd && !b.E) || (bwd && b.strict)) return cudaErrorInvalidValue;
   if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
@@ -1030,7 +1032,8 @@ cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b,
   cudaError_t e = cudaFuncSetAttribute(pfx::prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pfx::SMEM);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(bwd ? out::output_kernel<true> : out::output_kernel<false>,
+    e = cudaFuncSetAttribute(bwd ? out::output_kernel<true, false>
+                             : b.strict ? out::output_kernel<false, true> : out::output_kernel<false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)out::SMEM);
   if (e != cudaSuccess) return e;
   // Both launches are programmatic dependents of what precedes them on the
@@ -1051,8 +1054,11 @@ cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b,
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * out::kWarps);
   cfg.dynamicSmemBytes = out::SMEM;
-  if (bwd) return cudaLaunchKernelEx(&cfg, out::output_kernel<true>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
-  return cudaLaunchKernelEx(&cfg, out::output_kernel<false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
+  if (bwd)
+    return cudaLaunchKernelEx(&cfg, out::output_kernel<true, false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
+  if (b.strict)
+    return cudaLaunchKernelEx(&cfg, out::output_kernel<false, true>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, out::output_kernel<false, false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
 }
 
 cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
@@ -1074,6 +1080,28 @@ cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
   b.z_N = a.z_N;
   b.status = a.status ? a.status : &reinterpret_cast<WsHeader*>(ws)->status;
   b.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+  return launch_prefix64_pair(a, b, stream);
+}
+
+cudaError_t launch_prefill_rbw64(const PrefillArgs& a, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const Split sp = make_split(BH, a.N, sms);
+  if (!a.workspace || prefill_prefix64_workspace_bytes(a.B, a.H, a.N) > a.ws_bytes)
+    return cudaErrorInvalidValue;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  Prefix64Buffers b = {};
+  b.R = reinterpret_cast<float*>(ws);
+  b.P = reinterpret_cast<uint8_t*>(b.R + (size_t)BH * sp.MPH * SZ);
+  b.phik = reinterpret_cast<__nv_bfloat16*>(b.P + (size_t)sp.TC() * XG);
+  b.o = a.o;
+  b.S_N = a.S_N;
+  b.z_N = a.z_N;
+  cudaError_t e = library_status_word(&b.status);
+  if (e != cudaSuccess) return e;
+  b.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+  b.strict = 1;
   return launch_prefix64_pair(a, b, stream);
 }
 

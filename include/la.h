@@ -123,8 +123,11 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  * factors inside each chunk (the state enters the products as a bf16 copy of
  * the fp32 state; a zero alpha_t is taken as 1e-30): with a workspace, the
  * heads are split over every SM (decayed piece totals, then the chained
- * scan E' = Gamma E + R, then the outputs); with NULL, one block per head.  A
- * bounded wait of those kernels that gives up is reported by
+ * scan E' = Gamma E + R, then the outputs); with NULL, one block per head.
+ * LA_BF16 at dk = dv = 64 in LA_MODE_READ_BEFORE_WRITE without a decay, with a
+ * workspace, for calls of at most 2048 chunks of 128 tokens, runs la_prefill's
+ * two tensor-core launches with a strict mask inside each chunk.  A bounded
+ * wait of those kernels that gives up is reported by
  * delta_read_device_status.  Everything else runs on the CUDA cores in fp32,
  * for LA_F32 and LA_BF16 inputs and any dk, dv <= 128: with a workspace of
  * la_prefill_variant_workspace_bytes, each head's sequence in up to 64

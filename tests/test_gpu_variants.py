@@ -116,6 +116,40 @@ def test_read_before_write_first_read_is_zero_on_gpu(la):
     assert torch.count_nonzero(o[:, :, 0]) == 0
 
 
+# read before write on the tensor cores (bf16, dk = dv = 64, no decay, with a
+# workspace): la_prefill's two launches with a strict mask inside each chunk;
+# chunk edges, runs that cross heads and several pieces per head
+RBW_SHAPES = [(1, 3, 1), (1, 3, 127), (1, 3, 128), (1, 3, 129), (1, 3, 300), (2, 5, 3000),
+              (3, 40, 333), (1, 2, 20000)]
+
+
+@pytest.mark.parametrize("shape", RBW_SHAPES, ids=[str(s) for s in RBW_SHAPES])
+def test_read_before_write_tc_matches_oracle(la, orc, shape):
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N = shape
+    q, k, v = inputs.la_inputs(B, H, N, 64, 64, torch.bfloat16, seed=160 + N % 89)
+    g = torch.Generator().manual_seed(161 + N)
+    S0 = torch.randn((B, H, 64, 64), generator=g) * 0.5
+    z0 = torch.rand((B, H, 64), generator=g) * 4 + 0.5
+    la.delta_read_device_status()
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), None, la.LA_MODE_READ_BEFORE_WRITE,
+                                 S0=S0.cuda(), z0=z0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), None, 1, S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
+
+
+def test_read_before_write_tc_first_read_is_zero(la):
+    # from a zero state the first token of each head reads nothing: exactly 0
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(2, 3, 300, 64, 64, torch.bfloat16, seed=162)
+    o, _, _ = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), None, la.LA_MODE_READ_BEFORE_WRITE)
+    assert torch.count_nonzero(o[:, :, 0]) == 0
+    assert torch.count_nonzero(o[:, :, 1]) > 0
+
+
 def test_prefill_variant_zero_length_copies_state(la):
     e = torch.empty((1, 2, 0, 8), device="cuda")
     S0 = torch.rand((1, 2, 8, 8), device="cuda")
