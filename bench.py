@@ -59,7 +59,7 @@ def _args():
                    help="headline workload only (no long/decode/delta/e2e/cpu)")
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run "
-                        "(long,decode,delta,pr1,gated,decay,rbw,backward,prefill128)")
+                        "(long,decode,delta,pr1,gated,decay,rbw,nc,backward,prefill128)")
     p.add_argument("--profile-backward", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain la_prefill_backward calls and exit (for ncu)")
     p.add_argument("--profile-decay", type=int, default=0, metavar="CALLS",
@@ -593,10 +593,12 @@ def bench_backward(api, rank, world, reps=5):
             "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": f"of {kind}"}
 
 
-def bench_rbw_prefill(api, rank, world, reps=12, sets=4):
-    """la_prefill_variant in read-before-write order (no decay) on the headline
-    prefill shape: tensor cores, la_prefill's two launches with a strict mask,
-    over `sets` rotating input/output sets."""
+def bench_order_prefill(api, rank, world, mode, reps=12, sets=4):
+    """la_prefill_variant in read-before-write or non-causal order (no decay)
+    on the headline prefill shape, on the tensor cores (read before write:
+    la_prefill's two launches with a strict mask; non-causal: the piece totals,
+    then one product per chunk against the head's final state), over `sets`
+    rotating input/output sets."""
     import torch
     w = inputs_mod().WORKLOADS["prefill"]
     dev = torch.device("cuda")
@@ -611,7 +613,7 @@ def bench_rbw_prefill(api, rank, world, reps=12, sets=4):
 
     def fn(i):
         q, k, v, o, S, z = bufs[i % sets]
-        api.prefill_variant(q, k, v, None, api.LA_MODE_READ_BEFORE_WRITE, o=o, S_N=S, z_N=z)
+        api.prefill_variant(q, k, v, None, mode, o=o, S_N=S, z_N=z)
 
     with torch.cuda.stream(stream):
         for i in range(sets):
@@ -621,7 +623,8 @@ def bench_rbw_prefill(api, rank, world, reps=12, sets=4):
     ms = _graph_ms(fn, 4 * sets, stream, world)
     b = PREFILL_BYTES_PER_TOKEN * w.tokens
     hbm_peak, _, kind = _peaks()
-    return {"workload": "read-before-write prefill: B=4 H=8 N=4096 dk=dv=64 bf16",
+    order = "read-before-write" if mode == api.LA_MODE_READ_BEFORE_WRITE else "non-causal"
+    return {"workload": f"{order} prefill: B=4 H=8 N=4096 dk=dv=64 bf16",
             "ms_per_call": ms, "ms_per_python_call": ms_calls,
             "timing": f"{4 * sets} calls in one CUDA graph, replayed (device time per call); "
                       "ms_per_python_call: median of back-to-back calls from Python",
@@ -834,7 +837,7 @@ def main():
     extra = {}
     e2e = None
     wanted = set(x for x in args.only.split(",") if x) or {"long", "decode", "delta", "pr1",
-                                                             "gated", "decay", "rbw", "backward",
+                                                             "gated", "decay", "rbw", "nc", "backward",
                                                              "prefill128"}
     if not args.no_extra:
         if "long" in wanted:
@@ -852,7 +855,9 @@ def main():
         if "decay" in wanted:
             extra["decay_prefill"] = bench_decay_prefill(api, rank, world)
         if "rbw" in wanted:
-            extra["rbw_prefill"] = bench_rbw_prefill(api, rank, world)
+            extra["rbw_prefill"] = bench_order_prefill(api, rank, world, api.LA_MODE_READ_BEFORE_WRITE)
+        if "nc" in wanted:
+            extra["noncausal_prefill"] = bench_order_prefill(api, rank, world, api.LA_MODE_NONCAUSAL)
         if "backward" in wanted:
             extra["backward"] = bench_backward(api, rank, world)
         e_steps = min(max(args.steps // 4, 20), 200)  # at least 20 steps whatever --steps is

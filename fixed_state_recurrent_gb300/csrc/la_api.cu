@@ -216,7 +216,7 @@ size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv, l
     return 0;
   if (decay && mode == LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 64 && dv == 64 && N > 0)
     return la::prefill_decay64_workspace_bytes(B, H, N);
-  if (!decay && mode == LA_MODE_READ_BEFORE_WRITE && in_dtype == LA_BF16 && dk == 64 && dv == 64 &&
+  if (!decay && mode != LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 64 && dv == 64 &&
       la::prefill_prefix64_chosen(B, H, N))  // the tensor-core form, or the CUDA-core one if it cannot run
     return std::max(la::prefill_prefix64_workspace_bytes(B, H, N),
                     la::prefill_simt_workspace_bytes(B, H, N, dk, dv));
@@ -284,14 +284,15 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   // bf16 at dk = dv = 64, write then read with a decay: tensor cores
   if (alpha && mode == LA_MODE_CAUSAL && la::prefill_decay64_supported(a))
     return from_cuda(la::launch_prefill_decay64(a, alpha, stream));
-  // bf16 at dk = dv = 64, read before write, no decay, with a workspace: the
-  // two tensor-core launches of the prefill with a strict mask
+  // bf16 at dk = dv = 64, no decay, with a workspace: read before write in
+  // the two tensor-core launches of the prefill with a strict mask
   PrefillArgs tc = a;
   tc.chunk = 128;  // the tensor-core chunk
-  if (!alpha && mode == LA_MODE_READ_BEFORE_WRITE && dk == 64 && la::prefill_tc_supported(tc) &&
-      la::prefill_prefix64_chosen(B, H, N) && workspace &&
-      ws_bytes >= la::prefill_prefix64_workspace_bytes(B, H, N))
-    return from_cuda(la::launch_prefill_rbw64(a, stream));
+  const bool tc64 = !alpha && dk == 64 && la::prefill_tc_supported(tc) && la::prefill_prefix64_chosen(B, H, N) &&
+                    workspace && ws_bytes >= la::prefill_prefix64_workspace_bytes(B, H, N);
+  if (tc64 && mode == LA_MODE_READ_BEFORE_WRITE) return from_cuda(la::launch_prefill_rbw64(a, stream));
+  // non-causal: the piece totals, then every query reads its head's final state
+  if (tc64 && mode == LA_MODE_NONCAUSAL) return from_cuda(la::launch_prefill_nc64(a, stream));
   return from_cuda(la::launch_prefill_variant_simt(a, alpha, (int)mode, stream));
 }
 

@@ -1061,6 +1061,41 @@ cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b,
   return cudaLaunchKernelEx(&cfg, out::output_kernel<false, false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
 }
 
+cudaError_t launch_prefix64_totals(const PrefillArgs& a, const Prefix64Buffers& b, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  Params p = {};
+  p.sp = make_split(BH, a.N, sms);
+  p.eps = a.eps;
+  p.S0 = a.S0;
+  p.z0 = a.z0;
+  p.status = b.status;
+  p.R = b.R;
+  p.P = b.P;
+  CUtensorMap mk, mv, mphik, mp;
+  if (!make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mphik, b.phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mp, p.P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, (int)p.sp.TC(), 64, XROWS))
+    return cudaErrorInvalidValue;
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  cudaError_t e = cudaFuncSetAttribute(pfx::prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pfx::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * pfx::kWarps);
+  cfg.dynamicSmemBytes = pfx::SMEM;
+  return cudaLaunchKernelEx(&cfg, pfx::prefix_kernel, mk, mv, mphik, mp, p, mbar_ns);
+}
+
 cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
   const int BH = a.B * a.H;
   const int sms = sm_count();

@@ -124,9 +124,12 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  * the fp32 state; a zero alpha_t is taken as 1e-30): with a workspace, the
  * heads are split over every SM (decayed piece totals, then the chained
  * scan E' = Gamma E + R, then the outputs); with NULL, one block per head.
- * LA_BF16 at dk = dv = 64 in LA_MODE_READ_BEFORE_WRITE without a decay, with a
- * workspace, for calls of at most 2048 chunks of 128 tokens, runs la_prefill's
- * two tensor-core launches with a strict mask inside each chunk.  A bounded
+ * LA_BF16 at dk = dv = 64 without a decay, with a workspace, for calls of at
+ * most 2048 chunks of 128 tokens, also runs on the tensor cores:
+ * LA_MODE_READ_BEFORE_WRITE as la_prefill's two launches with a strict mask
+ * inside each chunk; LA_MODE_NONCAUSAL as la_prefill's first launch (the
+ * totals of the heads' pieces), then every query reads its head's final state
+ * (one product per chunk against a bf16 copy of it, z as hi + lo).  A bounded
  * wait of those kernels that gives up is reported by
  * delta_read_device_status.  Everything else runs on the CUDA cores in fp32,
  * for LA_F32 and LA_BF16 inputs and any dk, dv <= 128: with a workspace of

@@ -150,6 +150,40 @@ def test_read_before_write_tc_first_read_is_zero(la):
     assert torch.count_nonzero(o[:, :, 1]) > 0
 
 
+# non-causal on the tensor cores (bf16, dk = dv = 64, with a workspace): the
+# piece totals, then every query reads its head's final state
+NC_SHAPES = [(1, 3, 1), (1, 3, 129), (1, 3, 1000), (2, 5, 3000), (3, 40, 333), (1, 2, 20000)]
+
+
+@pytest.mark.parametrize("shape", NC_SHAPES, ids=[str(s) for s in NC_SHAPES])
+def test_noncausal_tc_matches_oracle(la, orc, shape):
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N = shape
+    q, k, v = inputs.la_inputs(B, H, N, 64, 64, torch.bfloat16, seed=170 + N % 83)
+    g = torch.Generator().manual_seed(171 + N)
+    S0 = torch.randn((B, H, 64, 64), generator=g) * 0.5
+    z0 = torch.rand((B, H, 64), generator=g) * 4 + 0.5
+    la.delta_read_device_status()
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), None, la.LA_MODE_NONCAUSAL,
+                                 S0=S0.cuda(), z0=z0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), None, 2, S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
+
+
+def test_noncausal_tc_queries_read_one_state(la):
+    # every query of a head reads the same state: two equal queries far apart in
+    # the sequence (other chunks, other blocks) give the same output
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 2, 700, 64, 64, torch.bfloat16, seed=172)
+    q[:, :, 650] = q[:, :, 3]
+    o, _, _ = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), None, la.LA_MODE_NONCAUSAL)
+    a, b = o[:, :, 650], o[:, :, 3]
+    assert (a - b).abs().max().item() <= 1e-6 * b.abs().max().item()
+
+
 def test_prefill_variant_zero_length_copies_state(la):
     e = torch.empty((1, 2, 0, 8), device="cuda")
     S0 = torch.rand((1, 2, 8, 8), device="cuda")
