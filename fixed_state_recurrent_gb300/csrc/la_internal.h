@@ -147,6 +147,12 @@ cudaError_t launch_prefix64_totals(const PrefillArgs& a, const Prefix64Buffers& 
 // a.workspace of at least prefill_prefix64_workspace_bytes (no header);
 // bounded-wait failures go to the library status word.
 cudaError_t launch_prefill_nc64(const PrefillArgs& a, cudaStream_t stream);
+// The decayed write-then-read form (alpha: [B][H][N]) in the same two launches,
+// for the calls prefill_prefix64_chosen takes: a.workspace of at least
+// prefill_prefix64_decay_workspace_bytes (no header); bounded-wait failures go
+// to the library status word.
+size_t prefill_prefix64_decay_workspace_bytes(int B, int H, int N);
+cudaError_t launch_prefill_prefix64_decay(const PrefillArgs& a, const float* alpha, cudaStream_t stream);
 
 // The gradient of the prefill for bf16 at dk = dv = 64, chunk-parallel in four
 // launches (backward_prefix64.cu): the two launches above (o and den into the

@@ -1226,7 +1226,13 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
 size_t prefill_decay64_workspace_bytes(int B, int H, int N) {
   const Split s = make_split(B * H, N, sm_count());
   const size_t slots = (size_t)s.BH * s.MPH;
-  return (2 * slots * SZ + slots) * sizeof(float);
+  const size_t three = (2 * slots * SZ + slots) * sizeof(float);
+  // calls that the two-launch form takes need its workspace
+  if (prefill_prefix64_chosen(B, H, N)) {
+    const size_t two = prefill_prefix64_decay_workspace_bytes(B, H, N);
+    return two > three ? two : three;
+  }
+  return three;
 }
 
 // The entry state of every piece of the d = 64 split, for other kernels that
@@ -1288,6 +1294,10 @@ bool prefill_decay64_supported(const PrefillArgs& a) {
 // to the library status word.
 cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream) {
   const int BH = a.B * a.H;
+  // calls whose re-read data stays in L2: the two launches of prefill_prefix64.cu
+  if (a.workspace && prefill_prefix64_chosen(a.B, a.H, a.N) &&
+      a.ws_bytes >= prefill_prefix64_decay_workspace_bytes(a.B, a.H, a.N))
+    return launch_prefill_prefix64_decay(a, alpha, stream);
   CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||

@@ -91,6 +91,11 @@ struct Params {
   float* R;            // [BH * MPH][SZ] piece totals (slot layout)
   uint8_t* P;          // [TC][66][64] bf16 prefix tiles
   float* den;          // [BH][N] den_t = phi(q_t)^T z_t + eps (the output kernel's BWD form only)
+  // decayed form (S_t = alpha_t S_{t-1} + phi(k_t) v_t^T, z likewise):
+  const float* alpha;  // [BH][N] per-token decay
+  float* G;            // [TC][128] per chunk row: g_t, the inclusive sum of log2 alpha over the chunk
+  float* gamc;         // [TC] per chunk: the decay from its piece's start to the chunk's start
+  float* gam;          // [BH * MPH] per piece slot: the decay over the whole piece
   int force_wait;      // test hook: the output kernel waits once on a barrier that nothing completes
 };
 
@@ -148,6 +153,16 @@ __device__ __forceinline__ void free_tmem(const Ctx& x, int warp, uint32_t ncols
   }
 }
 
+// Plain bulk copy global -> shared of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned), completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Eight bf16 of one state row, K-major swizzled operand tile.
 __device__ __forceinline__ void put8(uint8_t* tile, int row, int chunk, const float* v) {
   *reinterpret_cast<uint4*>(tile + sw128_offset(row, chunk)) =
@@ -160,15 +175,21 @@ __device__ __forceinline__ void put8(uint8_t* tile, int row, int chunk, const fl
 
 namespace pfx {
 
-constexpr int NS = 4;                       // K | V stages
-constexpr uint32_t STAGE = 2 * BLK;
+constexpr int NS = 4;                       // K | V stages (decayed form: K | V | weights)
 constexpr uint32_t PST = 9 * 1024;          // staging of one prefix tile (66 rows, 1024-byte aligned)
-constexpr uint32_t OFF_PST = NS * STAGE;
-constexpr uint32_t OFF_ONES = OFF_PST + 2 * PST;
-constexpr uint32_t OFF_BAR = OFF_ONES + ONES;
-constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
-static_assert(PST >= XG && OFF_PST % 1024 == 0 && PST % 1024 == 0, "prefix staging");
-static_assert(SMEM <= 227 * 1024, "shared memory per block");
+template <bool DECAY>
+struct Layout {
+  static constexpr uint32_t STAGE = DECAY ? 3 * BLK : 2 * BLK;
+  static constexpr uint32_t OFF_PST = NS * STAGE;
+  static constexpr uint32_t OFF_ONES = OFF_PST + 2 * PST;
+  static constexpr uint32_t OFF_BAR = OFF_ONES + ONES;
+  static constexpr uint32_t OFF_DBAR = OFF_BAR + 512;  // decayed form's extra barriers
+  static constexpr uint32_t SMEM = OFF_BAR + (DECAY ? 1024 : 512) + 1024;
+  static_assert(PST >= XG && OFF_PST % 1024 == 0 && PST % 1024 == 0, "prefix staging");
+  static_assert(SMEM <= 227 * 1024, "shared memory per block");
+};
+constexpr uint32_t SMEM_PLAIN = Layout<false>::SMEM;
+constexpr uint32_t SMEM_DECAY = Layout<true>::SMEM;
 // 0 TMA, 1 MMA, 2-9 phi(K) (half a row per thread), 10-13 prefix (TMEM lanes
 // 0..64 on warps 10, 12, 13), 14 phi(K) stores
 constexpr int kWarps = 15;
@@ -186,16 +207,35 @@ struct Bars {
   float4 zbuf[16];       // z, handed from its TMEM lane to the whole warp
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
+// decayed form: each chunk's decay gamma_C (phi warps -> prefix warps, a ring
+// of eight: the phi warps run at most seven chunks ahead of the prefix warps)
+// and the phi warps' partial scan sums
+struct DBars {
+  uint64_t gready[8];
+  float gring[8];
+  float part[8];
+};
 
+// DECAY: per chunk the phi warps also take g_t (the inclusive sum of
+// log2 alpha over the chunk, a zero alpha taken as 1e-30), scale V's rows by
+// w_s = 2^(g_C - g_s) (the decay from token s to the chunk's end, <= 1) and
+// write w_s as the only column of a weights block, so that the product
+// [w V | w]^T phi(K) is the chunk's decayed increment; phi(K) itself stays
+// unscaled (the output kernel's scores).  The prefix advances as
+// P <- gamma_C P + increment.
+template <bool DECAY>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ CUtensorMap tm_phik, const __grid_constant__ CUtensorMap tm_p,
               const Params p, const unsigned long long mbar_ns) {
+  using L = Layout<DECAY>;
+  constexpr uint32_t STAGE = L::STAGE, OFF_PST = L::OFF_PST, OFF_ONES = L::OFF_ONES;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the shared array by pointer
   // arithmetic so that accesses through it stay shared-space accesses
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  Bars* B = reinterpret_cast<Bars*>(smem + L::OFF_BAR);
+  DBars* DB = reinterpret_cast<DBars*>(smem + L::OFF_DBAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const Run run(p.sp, blockIdx.x);
   if (threadIdx.x == 0) LA_TRACE(0, 0);
@@ -210,6 +250,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       mbar_init(&B->dsfree[b], 3);
     }
     mbar_init(&B->drain, 1);
+    if (DECAY)
+      for (int q = 0; q < 8; ++q) mbar_init(&DB->gready[q], 1);
     B->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_k);
@@ -217,6 +259,11 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     tma_prefetch_desc(&tm_phik);
     tma_prefetch_desc(&tm_p);
   }
+  if (DECAY)  // the weights blocks: only column 0 is ever rewritten
+    for (int i = threadIdx.x; i < (int)(NS * BLK / 16); i += 32 * kWarps) {
+      const int st = i / (BLK / 16), k = i % (BLK / 16);
+      reinterpret_cast<uint4*>(smem + st * STAGE + 2 * BLK)[k] = make_uint4(0, 0, 0, 0);
+    }
   uint32_t pre = 0;  // loads issued during the set-up (thread 0)
   if (threadIdx.x == 0) {
     // This launch is a programmatic dependent of whatever ran before it on
@@ -276,10 +323,18 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         if (!waitb(x, &B->xf[s], (j / NS) & 1)) break;
         tc_fence_after();
         const uint32_t kt = smem_u32(smem + s * STAGE), vt = kt + BLK;
-        const uint64_t a0 = sdesc_sw128(vt, aOnes - vt, 1024), b0 = sdesc_sw128(kt, BLK, 1024);
+        const uint64_t b0 = sdesc_sw128(kt, BLK, 1024);
+        if (DECAY) {  // [w V | weights block]: two 64-row atoms along M, BLK apart
+          const uint64_t a0 = sdesc_sw128(vt, BLK, 1024);
 #pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks)
-          mma_bf16_ss(x.tmem + 64 * b, a0 + ks * kStepMN, b0 + ks * kStepRows16, ID_DS, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < C / 16; ++ks)
+            mma_bf16_ss(x.tmem + 64 * b, a0 + ks * kStepRows16, b0 + ks * kStepRows16, ID_DS, ks > 0 ? 1u : 0u);
+        } else {
+          const uint64_t a0 = sdesc_sw128(vt, aOnes - vt, 1024);
+#pragma unroll
+          for (int ks = 0; ks < C / 16; ++ks)
+            mma_bf16_ss(x.tmem + 64 * b, a0 + ks * kStepMN, b0 + ks * kStepRows16, ID_DS, ks > 0 ? 1u : 0u);
+        }
         mma_commit(&B->empty[s]);
         mma_commit(&B->dsready[b]);
         if (j < 8) LA_TRACE(0, 18 + j);
@@ -292,15 +347,69 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
     __syncwarp();
   } else if (warp < 10) {  // ---- phi on K, half a tile row per thread
-    const int t = threadIdx.x - 64, r = t >> 1, c0 = 4 * (t & 1);
+    const int t = threadIdx.x - 64, r = t >> 1, c0 = 4 * (t & 1), pw = warp - 2;
     uint32_t sj = 0;
+    // decayed form: alpha of this row in the run's chunk j (1 past the sequence),
+    // loaded a chunk ahead
+    const uint32_t total = (uint32_t)(run.b - run.a);
+    auto alpha_of = [&](uint32_t j) {
+      const long long gi = run.a + j;
+      const int tok = (int)(gi % p.sp.NC) * C + r;
+      return (c0 == 0 && j < total && tok < p.sp.N)
+                 ? __ldg(p.alpha + (size_t)(gi / p.sp.NC) * p.sp.N + tok) : 1.f;
+    };
+    float anext = DECAY ? alpha_of(0) : 1.f;
     Piece pc;
     for (int i = 0; run.piece(p.sp, i, &pc); ++i)
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const int s = sj % NS;
+        const int tok = pc.tok0 + c * C, valid = pc.tok1 - tok;
+        float g = 0.f, tot = 0.f;
+        if (DECAY) {  // g of this row (every call runs both named barriers)
+          const float acur = anext;
+          anext = alpha_of(sj + 1);
+          float la = 0.f;
+          if (c0 == 0 && r < valid) la = __log2f(fmaxf(acur, 1e-30f));
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {  // rows 16 pw .. 16 pw + 15, once each (even lanes)
+            const float y = __shfl_up_sync(0xFFFFFFFFu, la, off);
+            if (lane >= off) la += y;
+          }
+          if (lane == 31) DB->part[pw] = la;
+          named_bar_sync(3, 256);
+          g = la;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float pq = DB->part[q];
+            if (q < pw) g += pq;
+            tot += pq;
+          }
+          named_bar_sync(3, 256);
+        }
         if (!waitb_warp(x, &B->full[s], (sj / NS) & 1)) continue;
         if (t == 0 && sj < 8) LA_TRACE(0, 2 + sj);
-        phi_row<4>(smem + s * STAGE, r, c0, pc.tok1 - (pc.tok0 + c * C));
+        phi_row<4>(smem + s * STAGE, r, c0, valid);
+        if (DECAY) {
+          const float w = exp2_ftz(tot - g);
+          uint8_t* vt = smem + s * STAGE + BLK;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {  // V's half row times w
+            uint4 u = *reinterpret_cast<const uint4*>(vt + sw128_offset(r, c0 + q));
+            uint32_t* e = &u.x;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              e[k] = pack_bf16x2(__uint_as_float(e[k] << 16) * w, __uint_as_float(e[k] & 0xFFFF0000u) * w);
+            *reinterpret_cast<uint4*>(vt + sw128_offset(r, c0 + q)) = u;
+          }
+          if (c0 == 0) {
+            *reinterpret_cast<uint4*>(vt + BLK + sw128_offset(r, 0)) = make_uint4(pack_bf16x2(w, 0.f), 0u, 0u, 0u);
+            if (!*x.abort) p.G[(size_t)(run.a + sj) * C + r] = g;
+          }
+          if (t == 0) {  // the chunk's decay, for the prefix warps
+            DB->gring[sj % 8] = exp2_ftz(tot);
+            mbar_arrive(&DB->gready[sj % 8]);
+          }
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (t == 0 && sj < 8) LA_TRACE(0, 10 + sj);
@@ -318,6 +427,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     uint32_t sj = 0;
     Piece pc;
     for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+      float gpiece = 1.f;  // decayed form: the decay from the piece's start to the current chunk
       // a piece that starts its head starts from S0, z0 (row `row` of S^T: column `row` of S0)
 #pragma unroll
       for (int q = 0; q < D; ++q) acc[q] = 0.f;
@@ -359,9 +469,13 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         if (et == 32 && !*x.abort) {
           tma_store_3d(&tm_p, stg, 0, 0, (int)(run.a + sj));
           bulk_commit();
+          if (DECAY) p.gamc[run.a + sj] = gpiece;
         }
         const int b = sj % NB;
         const bool got = waitb_warp(x, &B->dsready[b], (sj / NB) & 1);
+        float gC = 1.f;
+        if (DECAY && waitb_warp(x, &DB->gready[sj % 8], (sj / 8) & 1)) gC = DB->gring[sj % 8];
+        gpiece *= gC;
         if (state_warp) {
           if (got) {
             tc_fence_after();
@@ -371,8 +485,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             tmem_ld_wait();
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
-              acc[q] += __uint_as_float(r0[q]);
-              acc[32 + q] += __uint_as_float(r1[q]);
+              acc[q] = DECAY ? fmaf(gC, acc[q], __uint_as_float(r0[q])) : acc[q] + __uint_as_float(r0[q]);
+              acc[32 + q] = DECAY ? fmaf(gC, acc[32 + q], __uint_as_float(r1[q])) : acc[32 + q] + __uint_as_float(r1[q]);
             }
           }
           tc_fence_before();
@@ -387,6 +501,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (int q = 0; q < 16; ++q)
           __stcg(dst + q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
       }
+      if (DECAY && et == 32 && !*x.abort) p.gam[pc.slot] = gpiece;  // the decay over the whole piece
     }
     if (et == 32) bulk_wait_all();
   } else if (lane == 0) {  // ---- phi(K) -> workspace; the stage is released once read
@@ -418,15 +533,22 @@ constexpr int NS = 3;                              // Q | phi(K) | P | V stages
 constexpr uint32_t OFF_K = BLK;
 constexpr uint32_t OFF_P = 2 * BLK;                // P right after phi(K): one operand [phi(K) ; P]
 constexpr uint32_t OFF_V = 2 * BLK + XT;
-constexpr uint32_t STAGE = 3 * BLK + XT;
-constexpr uint32_t OFF_E = NS * STAGE;             // the first piece's entry state (bf16 tile)
-constexpr uint32_t OFF_OUT = OFF_E + XT;           // output staging: two [128 x 32] fp32 boxes
-constexpr uint32_t OFF_ONES = OFF_OUT + 2 * BLK;
-constexpr uint32_t OFF_BAR = OFF_ONES + ONES;
-constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
-static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0 && OFF_V % 1024 == 0 && OFF_E % 1024 == 0 &&
-              OFF_OUT % 1024 == 0 && OFF_ONES % 1024 == 0, "swizzled tile alignment");
-static_assert(SMEM <= 227 * 1024, "shared memory per block");
+constexpr uint32_t OFF_G = 3 * BLK + XT;           // decayed form: g_t of the chunk's rows (128
+                                                   // floats), then the key factors (128 floats)
+template <bool DECAY>
+struct Layout {
+  static constexpr uint32_t STAGE = 3 * BLK + XT + (DECAY ? 1024 : 0);
+  static constexpr uint32_t OFF_E = NS * STAGE;      // the first piece's entry state (bf16 tile)
+  static constexpr uint32_t OFF_OUT = OFF_E + XT;    // output staging: two [128 x 32] fp32 boxes
+  static constexpr uint32_t OFF_ONES = OFF_OUT + 2 * BLK;
+  static constexpr uint32_t OFF_BAR = OFF_ONES + ONES;
+  static constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
+  static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0 && OFF_V % 1024 == 0 && OFF_E % 1024 == 0 &&
+                OFF_OUT % 1024 == 0 && OFF_ONES % 1024 == 0, "swizzled tile alignment");
+  static_assert(SMEM <= 227 * 1024, "shared memory per block");
+};
+constexpr uint32_t SMEM_PLAIN = Layout<false>::SMEM;
+constexpr uint32_t SMEM_DECAY = Layout<true>::SMEM;
 // 0 TMA, 1 MMA, 2-9 phi(Q) and the mask, 10-13 output epilogue; 2-14 build
 // the entry state and store the final states first (14 then has nothing left
 // to do)
@@ -460,8 +582,12 @@ static_assert(sizeof(Bars) <= 512, "barrier area");
 // ([64][65] fp32, transposed) and z_N.  Thread t of nthr, after the earlier
 // launch's results are visible; each thread keeps up to fifteen loads in
 // flight.  Returns whether T holds a final state.
+// DECAY: `wts` holds w_k = prod_{k < k' < npred} Gamma_k' for the earlier
+// slots k and, at [npred], the first piece's own decay: E = sum_k w_k R_k, and
+// the final state is Gamma E + R.
+template <bool DECAY>
 __device__ __forceinline__ bool build_entry(const Params& p, const Run& run, uint8_t* et, float* T,
-                                            int t, int nthr) {
+                                            int t, int nthr, const float* wts) {
   Piece pc;
   if (!run.piece(p.sp, 0, &pc)) return false;
   const int npred = run.idx0;
@@ -487,7 +613,13 @@ __device__ __forceinline__ bool build_entry(const Params& p, const Run& run, uin
 #pragma unroll
         for (int kk = 0; kk < 5; ++kk) {
           if (k0 + kk < npred) {
-            e[u].x += r[u][kk].x; e[u].y += r[u][kk].y; e[u].z += r[u][kk].z; e[u].w += r[u][kk].w;
+            if (DECAY) {
+              const float wk = wts[k0 + kk];
+              e[u].x = fmaf(wk, r[u][kk].x, e[u].x); e[u].y = fmaf(wk, r[u][kk].y, e[u].y);
+              e[u].z = fmaf(wk, r[u][kk].z, e[u].z); e[u].w = fmaf(wk, r[u][kk].w, e[u].w);
+            } else {
+              e[u].x += r[u][kk].x; e[u].y += r[u][kk].y; e[u].z += r[u][kk].z; e[u].w += r[u][kk].w;
+            }
           } else if (k0 + kk == npred) {  // the own total (only when the head ends here)
             fin[u] = r[u][kk];
           }
@@ -513,7 +645,9 @@ __device__ __forceinline__ bool build_entry(const Params& p, const Run& run, uin
         }
       }
       if (last) {
-        const float4 v = make_float4(e[u].x + fin[u].x, e[u].y + fin[u].y, e[u].z + fin[u].z, e[u].w + fin[u].w);
+        const float gw = DECAY ? wts[npred] : 1.f;
+        const float4 v = make_float4(fmaf(gw, e[u].x, fin[u].x), fmaf(gw, e[u].y, fin[u].y),
+                                     fmaf(gw, e[u].z, fin[u].z), fmaf(gw, e[u].w, fin[u].w));
         if (row < D) {
           T[(col + 0) * (D + 1) + row] = v.x;
           T[(col + 1) * (D + 1) + row] = v.y;
@@ -568,16 +702,27 @@ __device__ __forceinline__ void store_final_later(const Params& p, const Run& ru
 // evict-first L2 policy.  BWD (the gradient's second launch): den goes to
 // p.den, o out as bf16 (tm_o) and the entry-state tile to slot blockIdx.x of
 // tm_e.  STRICT: read before write (token t reads the state before its own
-// write: keys s < t inside the chunk).
-template <bool BWD, bool STRICT>
+// write: keys s < t inside the chunk).  DECAY: S_t = alpha_t S_{t-1} +
+// phi(k_t) v_t^T; with g_t the inclusive sum of log2 alpha over the chunk
+// (from the prefix kernel, with each stage's tiles) the state before the chunk
+// enters token t as 2^g_t (P_c + Gamma_c E) (Gamma_c: the decay from the
+// piece's start, applied to a copy of phi(Q) in shared memory for the E
+// product) and key s <= t with weight 2^(g_t - g_s): the mask warps weight the
+// scores (a row factor 2^(g_t - g_e) times a key factor 2^(g_e - g_s) below
+// the diagonal block, g_e at the block's last key, both <= 1) and scale the
+// state part of the row by 2^g_t before P [V | 1] is added.
+template <bool BWD, bool STRICT, bool DECAY>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_phik,
               const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_e,
               const Params p, const unsigned long long mbar_ns) {
+  using OL = Layout<DECAY>;
+  constexpr uint32_t STAGE = OL::STAGE, OFF_E = OL::OFF_E, OFF_OUT = OL::OFF_OUT, OFF_ONES = OL::OFF_ONES;
+  constexpr uint32_t XB = 2 * BLK + XG + (DECAY ? C * 4 : 0);  // bytes of a stage's `full`
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  Bars* B = reinterpret_cast<Bars*>(smem + OL::OFF_BAR);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const Run run(p.sp, blockIdx.x);
   const int total = (int)(run.b - run.a);
@@ -623,7 +768,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int tok = pc.tok0 + c * C;
         mbar_arrive_expect_tx(&B->qfull[pre], BLK);
         tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->qfull[pre]);
-        mbar_arrive_expect_tx(&B->full[pre], 2 * BLK + XG);
+        mbar_arrive_expect_tx(&B->full[pre], XB);
         tma_load_3d_ef(st + OFF_V, &tm_v, 0, tok, pc.h, &B->full[pre]);
       }
   }
@@ -654,7 +799,21 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int t = threadIdx.x - 64, nthr = 32 * (kWarps - 2);
     if (t == 0) LA_TRACE(1, 0);
     float* T = reinterpret_cast<float*>(smem + OFF_OUT);  // the output staging, free until the epilogue
-    const bool last = build_entry(p, run, smem + OFF_E, T, t, nthr);
+    float* wts = T + D * (D + 1);  // decayed form: the weights of the earlier totals, after T
+    if (DECAY) {
+      if (t == 0 && have0) {
+        const int n = run.idx0;
+        const float* gm = p.gam + (size_t)pc0.h * p.sp.MPH;
+        float acc = 1.f;
+        for (int k = n - 1; k >= 0; --k) {  // w_k = prod of the decays after slot k
+          wts[k] = acc;
+          acc *= __ldcg(gm + k);
+        }
+        wts[n] = __ldcg(gm + n);  // the first piece's own decay (for its final state)
+      }
+      named_bar_sync(6, nthr);
+    }
+    const bool last = build_entry<DECAY>(p, run, smem + OFF_E, T, t, nthr, wts);
     if (t == 0) LA_TRACE(1, 1);
     fence_proxy_async_smem();
     __syncwarp();
@@ -682,6 +841,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             uint8_t* st = smem + j * STAGE;
             tma_load_3d_ef(st + OFF_K, &tm_phik, 0, pc.tok0 + c * C, pc.h, &B->full[j]);
             tma_load_3d_ef(st + OFF_P, &tm_p, 0, 0, (int)(run.a + j), &B->full[j]);
+            if (DECAY) bulk_load(st + OFF_G, p.G + (size_t)(run.a + j) * C, C * 4, &B->full[j]);
           }
       }
       uint32_t sj = 0, issued = pre;
@@ -695,10 +855,11 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const int tok = pc.tok0 + c * C;
           mbar_arrive_expect_tx(&B->qfull[s], BLK);
           tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->qfull[s]);
-          mbar_arrive_expect_tx(&B->full[s], 2 * BLK + XG);
+          mbar_arrive_expect_tx(&B->full[s], XB);
           tma_load_3d_ef(st + OFF_K, &tm_phik, 0, tok, pc.h, &B->full[s]);
           tma_load_3d_ef(st + OFF_P, &tm_p, 0, 0, (int)(run.a + sj), &B->full[s]);
           tma_load_3d_ef(st + OFF_V, &tm_v, 0, tok, pc.h, &B->full[s]);
+          if (DECAY) bulk_load(st + OFF_G, p.G + (size_t)(run.a + sj) * C, C * 4, &B->full[s]);
           ++issued;
         }
       if (*x.abort) {
@@ -759,9 +920,16 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           for (int ks = 0; ks < D / 16; ++ks)  // phi(Q) from TMEM, [phi(K) ; P] from shared memory
             mma_bf16_ts(dA, aQ + 8 * ks, b0 + ks * kStepK16, ID_SX, ks > 0 ? 1u : 0u);
           if ((int)a < nE) {
+            if (DECAY) {  // Gamma_c phi(Q), written over Q by the phi warps
+              const uint64_t q0 = sdesc_sw128(st, 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-              mma_bf16_ts(dA + TOO, aQ + 8 * ks, e0 + ks * kStepK16, ID_X, 1u);
+              for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16_ss(dA + TOO, q0 + ks * kStepK16, e0 + ks * kStepK16, ID_X, 1u);
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16_ts(dA + TOO, aQ + 8 * ks, e0 + ks * kStepK16, ID_X, 1u);
+            }
           }
           if (a < 16) LA_TRACE(3, 32 + a);
           mma_commit(&B->accB[a % 2]);
@@ -822,6 +990,32 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         w[4 * i + 3] = phi2(v[i].w) & keep;
       }
       tmem_st16(tl + TQ + 32 * (j % 3) + 16 * half, w);
+      if (DECAY) {
+        // g of the stage (with its other tiles, after the prefix kernel): the
+        // key factors 2^(g_e - g_s) of this lane's row s (e: the last key of
+        // its 32-key block), and for a chunk with an entry state Gamma_c phi(Q)
+        // over Q's half row (the A operand of the E product)
+        pdl_wait();
+        if (waitb_warp(x, &B->full[s], (j / NS) & 1)) {
+          float* gs = reinterpret_cast<float*>(smem + s * STAGE + OFF_G);
+          if (half == 0) gs[C + row] = exp2_ftz(gs[row | 31] - gs[row]);
+          if ((int)j < nE) {
+            const float gm = __ldcg(p.gamc + gc);
+            uint8_t* qw = smem + s * STAGE;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 u;
+              uint32_t* e = &u.x;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                e[k] = pack_bf16x2(__uint_as_float(w[4 * i + k] << 16) * gm,
+                                   __uint_as_float(w[4 * i + k] & 0xFFFF0000u) * gm);
+              *reinterpret_cast<uint4*>(qw + sw128_offset(row, 4 * half + i)) = u;
+            }
+            fence_proxy_async_smem();
+          }
+        }
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -837,6 +1031,14 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       uint32_t r0[32], r1[32];
       if (!got) return;
       tc_fence_after();
+      // decayed form: the stage's g and key factors, written by the phi warps
+      // before their arrivals on xf (whose phase for chunk j is still current)
+      const float* gs = reinterpret_cast<const float*>(smem + (j % NS) * STAGE + OFF_G);
+      float gt = 0.f;
+      if (DECAY) {
+        waitb_warp(x, &B->xf[j % NS], (j / NS) & 1);
+        gt = gs[32 * quad + lane];
+      }
       if (q0 <= quad) tmem_ld32(base + 32 * q0, r0);
       if (q0 + 1 <= quad) tmem_ld32(base + 32 * (q0 + 1), r1);
       tmem_ld_wait();
@@ -849,7 +1051,21 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           for (int t2 = 0; t2 < 16; ++t2) w[t2] = 0u;
         } else {
           const uint32_t* r = k ? r1 : r0;
-          if (q4 < quad) {
+          if (DECAY && q4 < quad) {  // row factor times key factor, both <= 1
+            const float rf = exp2_ftz(gt - gs[32 * q4 + 31]);
+            const float* kf = gs + C + 32 * q4;
+#pragma unroll
+            for (int t2 = 0; t2 < 16; ++t2)
+              w[t2] = pack_bf16x2(__uint_as_float(r[2 * t2]) * (rf * kf[2 * t2]),
+                                  __uint_as_float(r[2 * t2 + 1]) * (rf * kf[2 * t2 + 1]));
+          } else if (DECAY) {  // the diagonal block: 2^(g_t - g_s) for s <= t
+            const float* gk = gs + 32 * q4;
+#pragma unroll
+            for (int t2 = 0; t2 < 16; ++t2)
+              w[t2] = pack_bf16x2(2 * t2 <= lane ? __uint_as_float(r[2 * t2]) * exp2_ftz(gt - gk[2 * t2]) : 0.f,
+                                  2 * t2 + 1 <= lane ? __uint_as_float(r[2 * t2 + 1]) * exp2_ftz(gt - gk[2 * t2 + 1])
+                                                     : 0.f);
+          } else if (q4 < quad) {
 #pragma unroll
             for (int t2 = 0; t2 < 16; ++t2)
               w[t2] = pack_bf16x2(__uint_as_float(r[2 * t2]), __uint_as_float(r[2 * t2 + 1]));
@@ -862,6 +1078,28 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
         }
         tmem_st16(base + 64 * half + 16 * k, w);  // over this warp's own block q0's scores
+      }
+      if (DECAY) {  // the state part of the row, phi(Q) (P_c + Gamma_c E), times 2^g_t
+        const float ga = exp2_ftz(gt);
+        const uint32_t ob = base + TOO + 32 * half;  // columns 32 half .. +31, and 64..79 for half 0
+        uint32_t o32[32];
+        tmem_ld32(ob, o32);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t wq[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) wq[i] = __float_as_uint(__uint_as_float(o32[16 * q + i]) * ga);
+          tmem_st16(ob + 16 * q, wq);
+        }
+        if (half == 0) {
+          uint32_t o16[16];
+          tmem_ld16(base + TOO + D, o16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o16[i] = __float_as_uint(__uint_as_float(o16[i]) * ga);
+          tmem_st16(base + TOO + D, o16);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -1029,12 +1267,12 @@ cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b,
     return cudaErrorInvalidValue;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
 
-  cudaError_t e = cudaFuncSetAttribute(pfx::prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)pfx::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(pfx::prefix_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pfx::SMEM_PLAIN);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(bwd ? out::output_kernel<true, false>
-                             : b.strict ? out::output_kernel<false, true> : out::output_kernel<false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)out::SMEM);
+    e = cudaFuncSetAttribute(bwd ? out::output_kernel<true, false, false>
+                             : b.strict ? out::output_kernel<false, true, false> : out::output_kernel<false, false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)out::SMEM_PLAIN);
   if (e != cudaSuccess) return e;
   // Both launches are programmatic dependents of what precedes them on the
   // stream: their blocks may start while the kernel before runs, and wait for
@@ -1048,17 +1286,17 @@ cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b,
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * pfx::kWarps);
-  cfg.dynamicSmemBytes = pfx::SMEM;
-  e = cudaLaunchKernelEx(&cfg, pfx::prefix_kernel, mk, mv, mphik, mp, p, mbar_ns);
+  cfg.dynamicSmemBytes = pfx::SMEM_PLAIN;
+  e = cudaLaunchKernelEx(&cfg, pfx::prefix_kernel<false>, mk, mv, mphik, mp, p, mbar_ns);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * out::kWarps);
-  cfg.dynamicSmemBytes = out::SMEM;
+  cfg.dynamicSmemBytes = out::SMEM_PLAIN;
   if (bwd)
-    return cudaLaunchKernelEx(&cfg, out::output_kernel<true, false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
+    return cudaLaunchKernelEx(&cfg, out::output_kernel<true, false, false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
   if (b.strict)
-    return cudaLaunchKernelEx(&cfg, out::output_kernel<false, true>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
-  return cudaLaunchKernelEx(&cfg, out::output_kernel<false, false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
+    return cudaLaunchKernelEx(&cfg, out::output_kernel<false, true, false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, out::output_kernel<false, false, false>, mq, mphik, mp, mv, mo, me, p, mbar_ns);
 }
 
 cudaError_t launch_prefix64_totals(const PrefillArgs& a, const Prefix64Buffers& b, cudaStream_t stream) {
@@ -1080,8 +1318,8 @@ cudaError_t launch_prefix64_totals(const PrefillArgs& a, const Prefix64Buffers& 
       !make_map(&mp, p.P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, (int)p.sp.TC(), 64, XROWS))
     return cudaErrorInvalidValue;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
-  cudaError_t e = cudaFuncSetAttribute(pfx::prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)pfx::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(pfx::prefix_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pfx::SMEM_PLAIN);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute pdl;
   pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1092,8 +1330,8 @@ cudaError_t launch_prefix64_totals(const PrefillArgs& a, const Prefix64Buffers& 
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * pfx::kWarps);
-  cfg.dynamicSmemBytes = pfx::SMEM;
-  return cudaLaunchKernelEx(&cfg, pfx::prefix_kernel, mk, mv, mphik, mp, p, mbar_ns);
+  cfg.dynamicSmemBytes = pfx::SMEM_PLAIN;
+  return cudaLaunchKernelEx(&cfg, pfx::prefix_kernel<false>, mk, mv, mphik, mp, p, mbar_ns);
 }
 
 cudaError_t launch_prefill_prefix64(const PrefillArgs& a, cudaStream_t stream) {
@@ -1138,6 +1376,85 @@ cudaError_t launch_prefill_rbw64(const PrefillArgs& a, cudaStream_t stream) {
   b.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
   b.strict = 1;
   return launch_prefix64_pair(a, b, stream);
+}
+
+
+// Decayed form's workspace (no header): piece totals, prefix tiles, phi(K),
+// then per chunk row g (fp32), per chunk the decay from its piece's start,
+// per piece slot its decay.
+struct DecayLayout {
+  size_t R, P, phik, G, gamc, gam, total;
+};
+static DecayLayout decay_layout(int B, int H, int N) {
+  const Split s = make_split(B * H, N, sm_count());
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  DecayLayout L;
+  L.R = 0;
+  L.P = up(L.R + (size_t)s.BH * s.MPH * SZ * sizeof(float));
+  L.phik = up(L.P + (size_t)s.TC() * XG);
+  L.G = up(L.phik + (size_t)s.BH * N * D * 2);
+  L.gamc = up(L.G + (size_t)s.TC() * C * sizeof(float));
+  L.gam = up(L.gamc + (size_t)s.TC() * sizeof(float));
+  L.total = up(L.gam + (size_t)s.BH * s.MPH * sizeof(float));
+  return L;
+}
+
+size_t prefill_prefix64_decay_workspace_bytes(int B, int H, int N) { return decay_layout(B, H, N).total; }
+
+cudaError_t launch_prefill_prefix64_decay(const PrefillArgs& a, const float* alpha, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const DecayLayout L = decay_layout(a.B, a.H, a.N);
+  if (!a.workspace || a.ws_bytes < L.total || !alpha) return cudaErrorInvalidValue;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  Params p = {};
+  p.sp = make_split(BH, a.N, sms);
+  p.eps = a.eps;
+  p.S0 = a.S0;
+  p.z0 = a.z0;
+  p.S_N = a.S_N;
+  p.z_N = a.z_N;
+  cudaError_t e = library_status_word(&p.status);
+  if (e != cudaSuccess) return e;
+  p.R = reinterpret_cast<float*>(ws + L.R);
+  p.P = ws + L.P;
+  __nv_bfloat16* phik = reinterpret_cast<__nv_bfloat16*>(ws + L.phik);
+  p.alpha = alpha;
+  p.G = reinterpret_cast<float*>(ws + L.G);
+  p.gamc = reinterpret_cast<float*>(ws + L.gamc);
+  p.gam = reinterpret_cast<float*>(ws + L.gam);
+  p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+  CUtensorMap mq, mk, mv, mo, mphik, mp;
+  if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mo, a.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C) ||
+      !make_map(&mphik, phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mp, p.P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, XROWS, (int)p.sp.TC(), 64, XROWS))
+    return cudaErrorInvalidValue;
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  e = cudaFuncSetAttribute(pfx::prefix_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)pfx::SMEM_DECAY);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(out::output_kernel<false, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)out::SMEM_DECAY);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * pfx::kWarps);
+  cfg.dynamicSmemBytes = pfx::SMEM_DECAY;
+  e = cudaLaunchKernelEx(&cfg, pfx::prefix_kernel<true>, mk, mv, mphik, mp, p, mbar_ns);
+  if (e != cudaSuccess) return e;
+  cfg.blockDim = dim3(32 * out::kWarps);
+  cfg.dynamicSmemBytes = out::SMEM_DECAY;
+  return cudaLaunchKernelEx(&cfg, out::output_kernel<false, false, true>, mq, mphik, mp, mv, mo, mp, p, mbar_ns);
 }
 
 }  // namespace la

@@ -273,6 +273,32 @@ def test_decay_prefill_tc_matches_oracle(la, orc, N, arange):
     assert la.delta_read_device_status() == 0
 
 
+# the decayed two-launch form over pieces: runs that cross heads, heads over
+# many blocks (entry states folded from earlier totals and decays)
+DECAY_SHAPES = [(2, 5, 3000), (3, 40, 333), (1, 2, 20000)]
+
+
+@pytest.mark.parametrize("shape", DECAY_SHAPES, ids=[str(s) for s in DECAY_SHAPES])
+@pytest.mark.parametrize("arange", [(0.9, 1.0), (0.02, 0.5)], ids=["mild", "severe"])
+def test_decay_prefill_tc_pieces_match_oracle(la, orc, shape, arange):
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N = shape
+    q, k, v = inputs.la_inputs(B, H, N, 64, 64, torch.bfloat16, seed=145 + N % 61)
+    g = torch.Generator().manual_seed(146 + N)
+    lo, hi = arange
+    alpha = lo + (hi - lo) * torch.rand((B, H, N), generator=g)
+    S0 = torch.randn((B, H, 64, 64), generator=g) * 0.5
+    z0 = torch.rand((B, H, 64), generator=g) * 4 + 0.5
+    la.delta_read_device_status()
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), alpha.cuda(), 0,
+                                 S0=S0.cuda(), z0=z0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha), 0, S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
+
+
 def test_decay_prefill_tc_zero_alpha_forgets(la, orc):
     # alpha = 0 at some tokens (taken as 1e-30 in the chunk factors): the state
     # before them is forgotten, including right at chunk edges
