@@ -209,11 +209,9 @@ struct Bars {
 static_assert(sizeof(Bars) <= 512, "barrier area");
 // decayed form: each chunk's decay gamma_C (phi warps -> prefix warps, a ring
 // of eight: the phi warps run at most seven chunks ahead of the prefix warps)
-// and the phi warps' partial scan sums
 struct DBars {
   uint64_t gready[8];
   float gring[8];
-  float part[8];
 };
 
 // DECAY: per chunk the phi warps also take g_t (the inclusive sum of
@@ -347,44 +345,57 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
     __syncwarp();
   } else if (warp < 10) {  // ---- phi on K, half a tile row per thread
-    const int t = threadIdx.x - 64, r = t >> 1, c0 = 4 * (t & 1), pw = warp - 2;
+    const int t = threadIdx.x - 64, r = t >> 1, c0 = 4 * (t & 1);
     uint32_t sj = 0;
-    // decayed form: alpha of this row in the run's chunk j (1 past the sequence),
-    // loaded a chunk ahead
+    // decayed form: every phi warp scans the whole chunk itself (lane l holds
+    // tokens 4 l .. 4 l + 3; alpha 1 past the sequence), so that no barrier
+    // between the warps sits on the chain; alpha is loaded a chunk ahead
     const uint32_t total = (uint32_t)(run.b - run.a);
-    auto alpha_of = [&](uint32_t j) {
-      const long long gi = run.a + j;
-      const int tok = (int)(gi % p.sp.NC) * C + r;
-      return (c0 == 0 && j < total && tok < p.sp.N)
-                 ? __ldg(p.alpha + (size_t)(gi / p.sp.NC) * p.sp.N + tok) : 1.f;
+    auto alpha4 = [&](uint32_t j) {
+      float4 a = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (DECAY && j < total) {
+        const long long gi = run.a + j;
+        const int tok = (int)(gi % p.sp.NC) * C + 4 * lane;
+        const float* ap = p.alpha + (size_t)(gi / p.sp.NC) * p.sp.N + tok;
+        if (tok + 3 < p.sp.N && ((reinterpret_cast<uintptr_t>(ap) & 15) == 0)) {
+          a = __ldg(reinterpret_cast<const float4*>(ap));
+        } else {
+          if (tok < p.sp.N) a.x = __ldg(ap);
+          if (tok + 1 < p.sp.N) a.y = __ldg(ap + 1);
+          if (tok + 2 < p.sp.N) a.z = __ldg(ap + 2);
+          if (tok + 3 < p.sp.N) a.w = __ldg(ap + 3);
+        }
+      }
+      return a;
     };
-    float anext = DECAY ? alpha_of(0) : 1.f;
+    float4 anext = alpha4(0);
     Piece pc;
     for (int i = 0; run.piece(p.sp, i, &pc); ++i)
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const int s = sj % NS;
         const int tok = pc.tok0 + c * C, valid = pc.tok1 - tok;
         float g = 0.f, tot = 0.f;
-        if (DECAY) {  // g of this row (every call runs both named barriers)
-          const float acur = anext;
-          anext = alpha_of(sj + 1);
-          float la = 0.f;
-          if (c0 == 0 && r < valid) la = __log2f(fmaxf(acur, 1e-30f));
+        if (DECAY) {  // g of this thread's row r, and of the chunk's last token
+          const float4 acur = anext;
+          anext = alpha4(sj + 1);
+          const float l0 = __log2f(fmaxf(acur.x, 1e-30f)), l1 = __log2f(fmaxf(acur.y, 1e-30f));
+          const float l2 = __log2f(fmaxf(acur.z, 1e-30f)), l3 = __log2f(fmaxf(acur.w, 1e-30f));
+          const float p0 = l0, p1 = l0 + l1, p2 = p1 + l2, p3 = p2 + l3;
+          float sc = p3;
 #pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {  // rows 16 pw .. 16 pw + 15, once each (even lanes)
-            const float y = __shfl_up_sync(0xFFFFFFFFu, la, off);
-            if (lane >= off) la += y;
+          for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xFFFFFFFFu, sc, off);
+            if (lane >= off) sc += y;
           }
-          if (lane == 31) DB->part[pw] = la;
-          named_bar_sync(3, 256);
-          g = la;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float pq = DB->part[q];
-            if (q < pw) g += pq;
-            tot += pq;
-          }
-          named_bar_sync(3, 256);
+          const float ex = sc - p3;  // the sum over the lanes before this one
+          tot = __shfl_sync(0xFFFFFFFFu, sc, 31);
+          // row r's value from lane r / 4, element r % 4
+          const float g0 = __shfl_sync(0xFFFFFFFFu, ex + p0, r >> 2);
+          const float g1 = __shfl_sync(0xFFFFFFFFu, ex + p1, r >> 2);
+          const float g2 = __shfl_sync(0xFFFFFFFFu, ex + p2, r >> 2);
+          const float g3 = __shfl_sync(0xFFFFFFFFu, ex + p3, r >> 2);
+          const int e = r & 3;
+          g = e == 0 ? g0 : e == 1 ? g1 : e == 2 ? g2 : g3;
         }
         if (!waitb_warp(x, &B->full[s], (sj / NS) & 1)) continue;
         if (t == 0 && sj < 8) LA_TRACE(0, 2 + sj);
