@@ -544,8 +544,7 @@ constexpr int NS = 3;                              // Q | phi(K) | P | V stages
 constexpr uint32_t OFF_K = BLK;
 constexpr uint32_t OFF_P = 2 * BLK;                // P right after phi(K): one operand [phi(K) ; P]
 constexpr uint32_t OFF_V = 2 * BLK + XT;
-constexpr uint32_t OFF_G = 3 * BLK + XT;           // decayed form: g_t of the chunk's rows (128
-                                                   // floats), then the key factors (128 floats)
+constexpr uint32_t OFF_G = 3 * BLK + XT;           // decayed form: g_t of the chunk's rows (128 floats)
 template <bool DECAY>
 struct Layout {
   static constexpr uint32_t STAGE = 3 * BLK + XT + (DECAY ? 1024 : 0);
@@ -718,10 +717,9 @@ __device__ __forceinline__ void store_final_later(const Params& p, const Run& ru
 // (from the prefix kernel, with each stage's tiles) the state before the chunk
 // enters token t as 2^g_t (P_c + Gamma_c E) (Gamma_c: the decay from the
 // piece's start, applied to a copy of phi(Q) in shared memory for the E
-// product) and key s <= t with weight 2^(g_t - g_s): the mask warps weight the
-// scores (a row factor 2^(g_t - g_e) times a key factor 2^(g_e - g_s) below
-// the diagonal block, g_e at the block's last key, both <= 1) and scale the
-// state part of the row by 2^g_t before P [V | 1] is added.
+// product) and key s <= t with weight 2^(g_t - g_s) <= 1: the mask warps
+// weight the scores and scale the state part of the row by 2^g_t before
+// P [V | 1] is added.
 template <bool BWD, bool STRICT, bool DECAY>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_phik,
@@ -1001,31 +999,23 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         w[4 * i + 3] = phi2(v[i].w) & keep;
       }
       tmem_st16(tl + TQ + 32 * (j % 3) + 16 * half, w);
-      if (DECAY) {
-        // g of the stage (with its other tiles, after the prefix kernel): the
-        // key factors 2^(g_e - g_s) of this lane's row s (e: the last key of
-        // its 32-key block), and for a chunk with an entry state Gamma_c phi(Q)
-        // over Q's half row (the A operand of the E product)
+      if (DECAY && (int)j < nE) {
+        // a chunk with an entry state: Gamma_c phi(Q) over Q's half row (the
+        // A operand of the E product), Gamma_c from the prefix kernel
         pdl_wait();
-        if (waitb_warp(x, &B->full[s], (j / NS) & 1)) {
-          float* gs = reinterpret_cast<float*>(smem + s * STAGE + OFF_G);
-          if (half == 0) gs[C + row] = exp2_ftz(gs[row | 31] - gs[row]);
-          if ((int)j < nE) {
-            const float gm = __ldcg(p.gamc + gc);
-            uint8_t* qw = smem + s * STAGE;
+        const float gm = __ldcg(p.gamc + gc);
+        uint8_t* qw = smem + s * STAGE;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 u;
-              uint32_t* e = &u.x;
+        for (int i = 0; i < 4; ++i) {
+          uint4 u;
+          uint32_t* e = &u.x;
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                e[k] = pack_bf16x2(__uint_as_float(w[4 * i + k] << 16) * gm,
-                                   __uint_as_float(w[4 * i + k] & 0xFFFF0000u) * gm);
-              *reinterpret_cast<uint4*>(qw + sw128_offset(row, 4 * half + i)) = u;
-            }
-            fence_proxy_async_smem();
-          }
+          for (int k = 0; k < 4; ++k)
+            e[k] = pack_bf16x2(__uint_as_float(w[4 * i + k] << 16) * gm,
+                               __uint_as_float(w[4 * i + k] & 0xFFFF0000u) * gm);
+          *reinterpret_cast<uint4*>(qw + sw128_offset(row, 4 * half + i)) = u;
         }
+        fence_proxy_async_smem();
       }
       tmem_st_wait();
       tc_fence_before();
@@ -1042,12 +1032,12 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       uint32_t r0[32], r1[32];
       if (!got) return;
       tc_fence_after();
-      // decayed form: the stage's g and key factors, written by the phi warps
-      // before their arrivals on xf (whose phase for chunk j is still current)
+      // decayed form: the stage's g (loaded with its tiles; the phase of the
+      // stage's `full` for chunk j is still current)
       const float* gs = reinterpret_cast<const float*>(smem + (j % NS) * STAGE + OFF_G);
       float gt = 0.f;
       if (DECAY) {
-        waitb_warp(x, &B->xf[j % NS], (j / NS) & 1);
+        waitb_warp(x, &B->full[j % NS], (j / NS) & 1);
         gt = gs[32 * quad + lane];
       }
       if (q0 <= quad) tmem_ld32(base + 32 * q0, r0);
@@ -1062,13 +1052,12 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           for (int t2 = 0; t2 < 16; ++t2) w[t2] = 0u;
         } else {
           const uint32_t* r = k ? r1 : r0;
-          if (DECAY && q4 < quad) {  // row factor times key factor, both <= 1
-            const float rf = exp2_ftz(gt - gs[32 * q4 + 31]);
-            const float* kf = gs + C + 32 * q4;
+          if (DECAY && q4 < quad) {  // 2^(g_t - g_s) <= 1
+            const float* gk = gs + 32 * q4;
 #pragma unroll
             for (int t2 = 0; t2 < 16; ++t2)
-              w[t2] = pack_bf16x2(__uint_as_float(r[2 * t2]) * (rf * kf[2 * t2]),
-                                  __uint_as_float(r[2 * t2 + 1]) * (rf * kf[2 * t2 + 1]));
+              w[t2] = pack_bf16x2(__uint_as_float(r[2 * t2]) * exp2_ftz(gt - gk[2 * t2]),
+                                  __uint_as_float(r[2 * t2 + 1]) * exp2_ftz(gt - gk[2 * t2 + 1]));
           } else if (DECAY) {  // the diagonal block: 2^(g_t - g_s) for s <= t
             const float* gk = gs + 32 * q4;
 #pragma unroll
