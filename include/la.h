@@ -122,8 +122,11 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  * LA_MODE_CAUSAL runs on the tensor cores with 128-token chunks and the decay
  * factors inside each chunk (the state enters the products as a bf16 copy of
  * the fp32 state; a zero alpha_t is taken as 1e-30): with a workspace, the
- * heads are split over every SM (decayed piece totals, then the chained
- * scan E' = Gamma E + R, then the outputs); with NULL, one block per head.
+ * heads are split over every SM -- for calls of at most 2048 chunks of 128
+ * tokens two launches (decayed prefix tiles, piece totals and decays, then
+ * the outputs, each block folding its entry state from the earlier totals),
+ * for larger ones three (decayed piece totals, the chained scan
+ * E' = Gamma E + R, then the outputs); with NULL, one block per head.
  * LA_BF16 at dk = dv = 64 without a decay, with a workspace, for calls of at
  * most 2048 chunks of 128 tokens, also runs on the tensor cores:
  * LA_MODE_READ_BEFORE_WRITE as la_prefill's two launches with a strict mask
