@@ -444,31 +444,34 @@ gprefix_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 namespace grd {
 
 // stage: phi(Q) | phi(K) | V | dnum (bf16 [128 x 64] tiles) | the state tile
-// S_c - E and the gradient-state tile G_c - EG (66 rows each).  OFF_OUT stages
-// dq for its TMA stores (two [128 x 32] fp32 boxes); once a chunk's products
-// are done its stage stages dv (over phi(Q) and phi(K)) and dk (over V and
-// dnum).
+// S_c - E and the gradient-state tile G_c - EG (66 rows each).  OFF_P1 holds
+// P1 (bf16 [128 x 128], two column blocks), then stages dq for its TMA stores
+// (two [128 x 32] fp32 boxes); once a chunk's products are done its stage
+// stages dv (over phi(Q) and phi(K)) and dk (over V and dnum).
 constexpr uint32_t OFF_KF = BLK, OFF_V = 2 * BLK, OFF_DN = 3 * BLK;
 constexpr uint32_t OFF_ST = 4 * BLK, OFF_GT = 4 * BLK + XT;
 constexpr uint32_t STAGE = 4 * BLK + 2 * XT;
 constexpr uint32_t OFF_E = 2 * STAGE;        // E (66 rows, from the output kernel), EG (rows 0..63)
 constexpr uint32_t OFF_EG = OFF_E + XT;
-constexpr uint32_t OFF_OUT = OFF_EG + XT;    // dq staging: two [128 x 32] fp32 boxes
-constexpr uint32_t OFF_VEC = OFF_OUT + 2 * BLK;  // floats: dd[2][128], zc[64], gc[64], gE[64]
+constexpr uint32_t OFF_P1 = OFF_EG + XT;     // P1, then the dq staging
+constexpr uint32_t OFF_VEC = OFF_P1 + 2 * BLK;  // floats: dd[2][128], zc[64], gc[64], gE[64]
 constexpr uint32_t OFF_BAR = OFF_VEC + (2 * 128 + 3 * 64) * 4;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
 static_assert(STAGE % 1024 == 0 && OFF_GT % 1024 == 0 && OFF_E % 1024 == 0 && OFF_EG % 1024 == 0 &&
-              OFF_OUT % 1024 == 0, "swizzled tile alignment");
+              OFF_P1 % 1024 == 0, "swizzled tile alignment");
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 constexpr int kThreads = 256;  // two threads per chunk row / TMEM lane
 constexpr uint32_t kCols = 512;
-// TMEM: the scores A1 = dnum V^T, A2 = V dnum^T, A3 = U W^T (then their masks
-// P1, P2, P3, packed in place), dW, dU; dV over A1 once P1 is read
-constexpr uint32_t T_A1 = 0, T_A2 = 128, T_A3 = 256, T_DW = 384, T_DU = 448, T_DV = 0;
+// TMEM: the scores A1 = dnum V^T (masked into P1 in shared memory) and
+// A3 = U W^T (masked into P3, packed in place), dW, dU, dV.  V dnum^T, the
+// scores of dU's product, is A1^T, and its mask P2 = P1^T (the dden_t term
+// included): dU's product reads P1 from shared memory as an MN-major operand.
+constexpr uint32_t T_A1 = 0, T_A3 = 128, T_DW = 256, T_DU = 320, T_DV = 384;
 
 constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);      // both K-major, N = 128
 constexpr uint32_t ID_N64_MN = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major, N = 64
 constexpr uint32_t ID_N64_K = idesc_bf16_f32(128, 64, 0, 0);   // both K-major, N = 64
+constexpr uint32_t ID_MN_MN = idesc_bf16_f32(128, 64, 1, 1);   // both MN-major, N = 64
 
 struct Params {
   Split sp;
@@ -617,6 +620,38 @@ __device__ __forceinline__ void mask_pack(uint32_t base, bool upper, int quad, i
 
 __device__ __forceinline__ uint32_t pcol(int ks) { return ks < 4 ? 8 * ks : 64 + 8 * (ks - 4); }
 
+// P1 = the lower-triangular mask (keys s <= t) of A1 + rowadd, rounded to
+// bf16, into a [128 x 128] K-major tile in shared memory (column block hf
+// holds keys 64 hf .. 64 hf + 63): this thread's half of row `row`.  Every
+// element is written, zeros included.
+__device__ __forceinline__ void mask_to_smem(uint32_t base, uint8_t* p1, int row, int quad, int lane,
+                                             int hf, float rowadd) {
+  uint32_t r0[32], r1[32];
+  const int q0 = 2 * hf;
+  if (q0 <= quad) tmem_ld32(base + 32 * q0, r0);
+  if (q0 + 1 <= quad) tmem_ld32(base + 32 * (q0 + 1), r1);
+  tmem_ld_wait();
+  uint8_t* dst = p1 + hf * BLK;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int q4 = q0 + k;
+    const uint32_t* r = k ? r1 : r0;
+    const int hi = q4 < quad ? 31 : q4 == quad ? lane : -1;  // kept keys 0 .. hi of the block
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int s0 = 8 * c + 2 * e, s1 = s0 + 1;
+        w[e] = pack_bf16x2(s0 <= hi ? __uint_as_float(r[s0]) + rowadd : 0.f,
+                           s1 <= hi ? __uint_as_float(r[s1]) + rowadd : 0.f);
+      }
+      *reinterpret_cast<uint4*>(dst + sw128_offset(row, 4 * k + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+
 __global__ void __launch_bounds__(kThreads, 1)
 grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__ CUtensorMap tm_phik,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dn,
@@ -739,8 +774,8 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
   const uint64_t eS = sdesc_sw128(smem_u32(smem + OFF_E), 16, 1024);
   const uint64_t eG = sdesc_sw128(smem_u32(smem + OFF_EG), 16, 1024);
 
-  // thread 0: A1 = dnum V^T, A2 = V dnum^T, A3 = U W^T, dW = dnum (S_c)^T,
-  // dU = V (G_c)^T of the run's chunk j, once its tiles are in
+  // thread 0: A1 = dnum V^T, A3 = U W^T, dW = dnum (S_c)^T, dU = V (G_c)^T,
+  // dV = U G_c of the run's chunk j, once its tiles are in
   auto issue_first = [&](uint32_t j) {
     const int s = j % 2;
     const int h = (int)((run.a + j) / NC);
@@ -755,9 +790,6 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         mma_bf16_ss(tm + T_A1, dD + ks * kStepK16, dV + ks * kStepK16, ID_S, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_A2, dV + ks * kStepK16, dD + ks * kStepK16, ID_S, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         mma_bf16_ss(tm + T_A3, dK + ks * kStepK16, dQ + ks * kStepK16, ID_S, ks > 0);
@@ -777,6 +809,14 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
         for (int ks = 0; ks < D / 16; ++ks)
           mma_bf16_ss(tm + T_DU, dV + ks * kStepK16, eG + ks * kStepRows16, ID_N64_MN, 1u);
       }
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)  // dV = U G_c
+        mma_bf16_ss(tm + T_DV, dK + ks * kStepK16, dG + ks * kStepK16, ID_N64_K, ks > 0);
+      if (useEG) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16_ss(tm + T_DV, dK + ks * kStepK16, eG + ks * kStepK16, ID_N64_K, 1u);
+      }
     }
     mma_commit(&B->mma);
   };
@@ -788,9 +828,9 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
     const long long gi = run.a + j;
     const int h = (int)(gi / NC), tok = (int)(gi % NC) * C;
     const bool useE = haveE && h == h0, useEG = lastContinues && h == hl;
-    const uint32_t aQ = smem_u32(st), aK = aQ + OFF_KF, aD = aQ + OFF_DN, aG = aQ + OFF_GT;
-    // the stores of the chunk before have read their staging (the dq staging
-    // and the other stage); the next chunk's tiles into that stage
+    const uint32_t aQ = smem_u32(st), aK = aQ + OFF_KF, aD = aQ + OFF_DN;
+    // the stores of the chunk before have read their staging (P1's region and
+    // the other stage); the next chunk's tiles into that stage
     if (t == kLd && j > 0) bulk_wait_read_all();
     if (t == kLd && j + 1 < total && !aborted()) load(j + 1);
     waitb(x, &B->full[s], (j / 2) & 1);
@@ -802,49 +842,41 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
       const int i = t - D;
       gc[i] = tile_at(st + OFF_GT, 64, i) + tile_at(st + OFF_GT, 65, i) + (useEG ? gE[i] : 0.f);
     }
-    mma_done();  // the first products of chunk j
+    mma_done();       // the first products of chunk j
+    __syncthreads();  // (also: P1's region has been read by the stores of the chunk before)
     if (t == 0 && j < 8) BW_TRACE(0, 4 + 6 * j);
-    // P1 = mask(A1 + dden_t) (keys s <= t), P2 = mask^T(A2 + dden_t) and
-    // P3 = mask^T(A3) (queries t >= s)
-#pragma unroll 1
-    for (int m = 0; m < 3; ++m)
-      mask_pack(tl + (m == 0 ? T_A1 : m == 1 ? T_A2 : T_A3), m > 0, quad, lane, hf,
-                m == 0 ? dd[s * C + row] : 0.f, m == 1 ? dd + s * C : nullptr);
+    // P1 = mask(A1 + dden_t) (keys s <= t) into shared memory, P3 = mask^T(A3)
+    // (queries t >= s) in place
+    mask_to_smem(tl + T_A1, smem + OFF_P1, row, quad, lane, hf, dd[s * C + row]);
+    mask_pack(tl + T_A3, true, quad, lane, hf, 0.f, nullptr);
+    fence_proxy_async_smem();
     step_done();
     if (t == 0 && j < 8) BW_TRACE(0, 5 + 6 * j);
 
-    // dW += P1 U, dU += P2 W
+    // dW += P1 U, dU += P1^T W (P1 read MN-major: its rows t are the K index),
+    // dV += P3 dnum
     if (t == 0 && issuing()) {
+      const uint32_t aP1 = smem_u32(smem + OFF_P1);
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks)
-        mma_bf16_ts(tm + T_DW, tm + T_A1 + pcol(ks), sdesc_sw128(aK + ks * 2048, BLK, 1024), ID_N64_MN, 1u);
+        mma_bf16_ss(tm + T_DW, sdesc_sw128(aP1 + (ks < 4 ? 32 * ks : BLK + 32 * (ks - 4)), 16, 1024),
+                    sdesc_sw128(aK + ks * 2048, BLK, 1024), ID_N64_MN, 1u);
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks)
-        mma_bf16_ts(tm + T_DU, tm + T_A2 + pcol(ks), sdesc_sw128(aQ + ks * 2048, BLK, 1024), ID_N64_MN, 1u);
-    }
-    if (t == 0) mma_commit(&B->mma);
-    mma_done();
-    if (t == 0 && j < 8) BW_TRACE(0, 6 + 6 * j);
-    // dV = U G_c + P3 dnum (over A1, whose P1 the products above have read)
-    if (t == 0 && issuing()) {
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16_ss(tm + T_DV, sdesc_sw128(aK + ks * 32, 16, 1024), sdesc_sw128(aG + ks * 32, 16, 1024),
-                    ID_N64_K, ks > 0);
-      if (useEG) {
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_bf16_ss(tm + T_DV, sdesc_sw128(aK + ks * 32, 16, 1024), eG + ks * kStepK16, ID_N64_K, 1u);
-      }
+        mma_bf16_ss(tm + T_DU, sdesc_sw128(aP1 + ks * 2048, BLK, 1024), sdesc_sw128(aQ + ks * 2048, BLK, 1024),
+                    ID_MN_MN, 1u);
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks)
         mma_bf16_ts(tm + T_DV, tm + T_A3 + pcol(ks), sdesc_sw128(aD + ks * 2048, BLK, 1024), ID_N64_MN, 1u);
     }
     if (t == 0) mma_commit(&B->mma);
-    // meanwhile dq = (dW + dden_t z_c) phi'(q) into its staging, dk = (dU + g_c) phi'(k)
-    float o[32], f[32];
+    mma_done();
+    if (t == 0 && j < 8) BW_TRACE(0, 6 + 6 * j);
+    // dq = (dW + dden_t z_c) phi'(q) over P1's region, dk = (dU + g_c) phi'(k)
+    // over V | dnum, then (every read of phi(Q), phi(K) done) dv over them
     {
-      uint8_t* bq = smem + OFF_OUT + hf * BLK;
+      float o[32], f[32];
+      uint8_t* bq = smem + OFF_P1 + hf * BLK;
       const float dr = dd[s * C + row];
       tmem_row32(tl + T_DW + th, o);
       load_half_bf16(st, row, hf, f);
@@ -859,32 +891,31 @@ grad_kernel(const __grid_constant__ CUtensorMap tm_phiq, const __grid_constant__
       }
       tmem_row32(tl + T_DU + th, o);
       load_half_bf16(st + OFF_KF, row, hf, f);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = (o[i] + gc[th + i]) * fminf(f[i], 1.f);
-    }
-    mma_done();
-    if (t == 0 && j < 8) BW_TRACE(0, 7 + 6 * j);
-    tmem_row32(tl + T_DV + th, f);
-    step_done();  // every read of this chunk's stage and TMEM is done
-    // dk over V | dnum, dv over phi(Q) | phi(K); rows past the sequence are
-    // not stored.  The next chunk's first products go out while they are.
-    {
       uint8_t* bk = st + OFF_V + hf * BLK;
-      uint8_t* bv = st + hf * BLK;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
-        *reinterpret_cast<float4*>(bk + sw128_offset(row, cc)) =
-            make_float4(o[4 * cc], o[4 * cc + 1], o[4 * cc + 2], o[4 * cc + 3]);
-        *reinterpret_cast<float4*>(bv + sw128_offset(row, cc)) =
-            make_float4(f[4 * cc], f[4 * cc + 1], f[4 * cc + 2], f[4 * cc + 3]);
+        float4 v4;
+        v4.x = (o[4 * cc] + gc[th + 4 * cc]) * fminf(f[4 * cc], 1.f);
+        v4.y = (o[4 * cc + 1] + gc[th + 4 * cc + 1]) * fminf(f[4 * cc + 1], 1.f);
+        v4.z = (o[4 * cc + 2] + gc[th + 4 * cc + 2]) * fminf(f[4 * cc + 2], 1.f);
+        v4.w = (o[4 * cc + 3] + gc[th + 4 * cc + 3]) * fminf(f[4 * cc + 3], 1.f);
+        *reinterpret_cast<float4*>(bk + sw128_offset(row, cc)) = v4;
       }
+      tmem_row32(tl + T_DV + th, o);
+      if (t == 0 && j < 8) BW_TRACE(0, 7 + 6 * j);
+      step_done();  // every read of this chunk's phi tiles and TMEM is done
+      uint8_t* bv = st + hf * BLK;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<float4*>(bv + sw128_offset(row, cc)) =
+            make_float4(o[4 * cc], o[4 * cc + 1], o[4 * cc + 2], o[4 * cc + 3]);
     }
     fence_proxy_async_smem();
     __syncthreads();
-    if (t == 0 && j + 1 < total) issue_first(j + 1);
-    if (t == kLd && !aborted()) {
-      tma_store_3d_ef(&tm_dq, smem + OFF_OUT, 0, tok, h);
-      tma_store_3d_ef(&tm_dq, smem + OFF_OUT + BLK, 32, tok, h);
+    if (t == 0 && j + 1 < total) issue_first(j + 1);  // while this chunk's outputs are stored
+    if (t == kLd && !aborted()) {  // rows past the sequence are not stored
+      tma_store_3d_ef(&tm_dq, smem + OFF_P1, 0, tok, h);
+      tma_store_3d_ef(&tm_dq, smem + OFF_P1 + BLK, 32, tok, h);
       tma_store_3d_ef(&tm_dk, st + OFF_V, 0, tok, h);
       tma_store_3d_ef(&tm_dk, st + OFF_V + BLK, 32, tok, h);
       tma_store_3d_ef(&tm_dv, st, 0, tok, h);
