@@ -231,6 +231,13 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     tma_prefetch_desc(&tm_phik);
   }
   const Run run(p.sp, blockIdx.x);
+  // The run is walked backwards (last piece, last chunk first): the phi(K) and
+  // V it touches last are those of the run's first chunks, which the output
+  // kernel reads first, so they are still in L2.  A piece's total does not
+  // depend on the order.
+  const int npieces = run.count(p.sp);
+  auto walk = [&](int i, Piece* pc) { return i < npieces && run.piece(p.sp, npieces - 1 - i, pc); };
+  auto chunk_of = [&](const Piece& pc, int c) { return pc.nch - 1 - c; };
   auto load_stage = [&](uint32_t s, int tok, int h) {
     uint8_t* st = smem + s * STAGE;
     mbar_arrive_expect_tx(&B->full[s], 2 * TILE);
@@ -245,8 +252,8 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     // set-up overlaps that kernel's last blocks): no global memory before the wait
     pdl_wait();
     Piece pc;
-    for (int i = 0; pre < NS && run.piece(p.sp, i, &pc); ++i)
-      for (int c = 0; pre < NS && c < pc.nch; ++c, ++pre) load_stage(pre, pc.tok0 + c * C, pc.h);
+    for (int i = 0; pre < NS && walk(i, &pc); ++i)
+      for (int c = 0; pre < NS && c < pc.nch; ++c, ++pre) load_stage(pre, pc.tok0 + chunk_of(pc, c) * C, pc.h);
   }
   init_ones16(smem + OFF_ONES, threadIdx.x, 32 * kWarps);
   if (warp == 1) {
@@ -265,12 +272,12 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (lane == 0) {  // ---- TMA producer: K, V chunk tiles (the first `pre` went out above)
       uint32_t sj = 0, issued = pre;
       Piece pc;
-      for (int i = 0; run.piece(p.sp, i, &pc); ++i)
+      for (int i = 0; walk(i, &pc); ++i)
         for (int c = 0; c < pc.nch; ++c, ++sj) {
           const uint32_t s = sj % NS;
           if (sj < pre) continue;
           if (!wait_b(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
-          load_stage(s, pc.tok0 + c * C, pc.h);
+          load_stage(s, pc.tok0 + chunk_of(pc, c) * C, pc.h);
           ++issued;
         }
       if (*x.abort) drain_ring(B->full, NS, issued, NS, mbar_ns);
@@ -281,7 +288,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       const uint64_t ones = sdesc_sw128(smem_u32(smem + OFF_ONES), 16, 1024);
       uint32_t sj = 0;
       Piece pc;
-      for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+      for (int i = 0; walk(i, &pc); ++i) {
         const int b = i % 2;
         if (i >= 2 && !wait_b(x, &B->rfree[b], ((i / 2) - 1) & 1)) break;
         for (int c = 0; c < pc.nch; ++c, ++sj) {
@@ -312,10 +319,10 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int r = threadIdx.x - 64;
     uint32_t sj = 0;
     Piece pc;
-    for (int i = 0; run.piece(p.sp, i, &pc); ++i)
+    for (int i = 0; walk(i, &pc); ++i)
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const uint32_t s = sj % NS;
-        const int valid = pc.tok1 - (pc.tok0 + c * C);
+        const int valid = pc.tok1 - (pc.tok0 + chunk_of(pc, c) * C);
         if (!wait_w(x, &B->full[s], (sj / NS) & 1)) continue;
         uint8_t* st = smem + s * STAGE;
 #pragma unroll 1
@@ -329,7 +336,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
     uint32_t sj = 0;
     Piece pc;
-    for (int i = 0; run.piece(p.sp, i, &pc); ++i) {
+    for (int i = 0; walk(i, &pc); ++i) {
       if (et == 0) {  // phi(K) of the piece's chunks -> workspace; a stage is released
                       // once the store of the chunk after it was issued and its own
                       // store has read shared memory
@@ -337,8 +344,8 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           const uint32_t s = sj % NS;
           if (!wait_b(x, &B->xf[s], (sj / NS) & 1)) continue;
           uint8_t* st = smem + s * STAGE;
-          tma_store_3d(&tm_phik, st, 0, pc.tok0 + c * C, pc.h);
-          tma_store_3d(&tm_phik, st + BLK, 64, pc.tok0 + c * C, pc.h);
+          tma_store_3d(&tm_phik, st, 0, pc.tok0 + chunk_of(pc, c) * C, pc.h);
+          tma_store_3d(&tm_phik, st + BLK, 64, pc.tok0 + chunk_of(pc, c) * C, pc.h);
           bulk_commit();
           if (sj > 0) {
             bulk_wait_read_but_one();
