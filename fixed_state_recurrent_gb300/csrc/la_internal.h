@@ -138,8 +138,9 @@ cudaError_t launch_prefix64_pair(const PrefillArgs& a, const Prefix64Buffers& b,
 // takes; a.workspace of at least prefill_prefix64_workspace_bytes (no header;
 // bounded-wait failures go to the library status word).
 cudaError_t launch_prefill_rbw64(const PrefillArgs& a, cudaStream_t stream);
-// The first of those launches alone (the piece totals R, with S0 in a piece
-// that starts its head; P and phik are written too), from buffers as above.
+// The first of those launches alone, for its piece totals R only (with S0 in
+// a piece that starts its head; neither P nor phik is written, but their maps
+// are still made over the buffers given).
 cudaError_t launch_prefix64_totals(const PrefillArgs& a, const Prefix64Buffers& b, cudaStream_t stream);
 // Non-causal order (la_prefill_variant's LA_MODE_NONCAUSAL) at bf16,
 // dk = dv = 64, for the calls prefill_prefix64_chosen takes: the piece totals,

@@ -5,11 +5,12 @@
 // reads the state over the whole sequence,
 //   o_t = phi(q_t)^T S_N / (phi(q_t)^T z_N + eps),
 //   S_N = S0 + sum_t phi(k_t) v_t^T,  z_N = z0 + sum_t phi(k_t).
-// Two launches over the split of prefill_tc_common.cuh:
+// Two launches over splits of prefill_tc_common.cuh:
 //   1. the prefill's prefix kernel (prefill_prefix64.cu): the piece totals R
 //      (with S0 for a piece that starts its head);
-//   2. nc_kernel: per piece of the block's run, S_N of its head as the sum of
-//      the head's totals (fp32, in slot order), a bf16 operand tile (z as
+//   2. nc_kernel (two blocks per SM, over a split of twice as many runs): per
+//      piece of the block's run, S_N of its head as the sum of the head's
+//      totals from the first launch (fp32, in slot order), a bf16 operand tile (z as
 //      hi + lo rows); per chunk [num | den] = phi(Q) [S_N | z_N]^T as one
 //      N = 80 product, o = num / (den + eps) staged for TMA.  The block that
 //      holds a head's last chunk writes S_N, z_N.
@@ -40,9 +41,10 @@ static_assert(SMEM <= 227 * 1024, "shared memory per block");
 constexpr uint32_t ID_N80 = idesc_bf16_f32(128, D + 16, 0, 0);  // phi(Q) [S | z]^T, both K-major
 
 struct Params {
-  Split sp;
+  Split sp;         // this kernel's runs (two blocks per SM)
+  Split sr;         // the prefix kernel's split, whose slots hold the piece totals
   float eps;
-  const float* R;   // [BH * MPH][SZ] piece totals (slot layout)
+  const float* R;   // [BH * sr.MPH][SZ] piece totals (slot layout)
   float* S_N;
   float* z_N;
   unsigned* status;
@@ -129,9 +131,10 @@ nc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   for (int i = 0; run.piece(sp, i, &pc); ++i) {
     // S_N of the piece's head: the sum of all its slots, in slot order
     const int h = pc.h;
-    const int nb = sp.owner((long long)h * NC + NC - 1) - sp.owner((long long)h * NC) + 1;
+    const Split& sr = p.sr;
+    const int nb = sr.owner((long long)h * NC + NC - 1) - sr.owner((long long)h * NC) + 1;
     const bool last = pc.tok1 == N;  // this block holds the head's last chunk: it writes S_N, z_N
-    const float4* Rh = reinterpret_cast<const float4*>(p.R + (size_t)h * sp.MPH * SZ);
+    const float4* Rh = reinterpret_cast<const float4*>(p.R + (size_t)h * sr.MPH * SZ);
     for (int f = t; f < SZ / 4; f += kThreads) {
       constexpr int U = 4;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -268,7 +271,8 @@ cudaError_t launch_prefill_nc64(const PrefillArgs& a, cudaStream_t stream) {
       !make_map(&mo, a.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C))
     return cudaErrorInvalidValue;
   Params p = {};
-  p.sp = sp;
+  p.sp = make_split(BH, a.N, 2 * sms);  // 77 KB of shared memory: two blocks per SM
+  p.sr = sp;
   p.eps = a.eps;
   p.R = b.R;
   p.S_N = a.S_N;
@@ -285,7 +289,7 @@ cudaError_t launch_prefill_nc64(const PrefillArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = &pdl;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(sp.G);
+  cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = SMEM;
   return cudaLaunchKernelEx(&cfg, nc_kernel, mq, mo, p, mbar_ns);

@@ -91,6 +91,7 @@ struct Params {
   float* R;            // [BH * MPH][SZ] piece totals (slot layout)
   uint8_t* P;          // [TC][66][64] bf16 prefix tiles
   float* den;          // [BH][N] den_t = phi(q_t)^T z_t + eps (the output kernel's BWD form only)
+  int totals_only;     // the prefix kernel stores neither the prefix tiles nor phi(K)
   // decayed form (S_t = alpha_t S_{t-1} + phi(k_t) v_t^T, z likewise):
   const float* alpha;  // [BH][N] per-token decay
   float* G;            // [TC][128] per chunk row: g_t, the inclusive sum of log2 alpha over the chunk
@@ -477,7 +478,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
-        if (et == 32 && !*x.abort) {
+        if (et == 32 && !*x.abort && !p.totals_only) {
           tma_store_3d(&tm_p, stg, 0, 0, (int)(run.a + sj));
           bulk_commit();
           if (DECAY) p.gamc[run.a + sj] = gpiece;
@@ -522,9 +523,11 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const int s = sj % NS;
         if (!waitb(x, &B->xf[s], (sj / NS) & 1)) continue;
-        tma_store_3d(&tm_phik, smem + s * STAGE, 0, pc.tok0 + c * C, pc.h);
-        bulk_commit();
-        bulk_wait_read_all();
+        if (!p.totals_only) {
+          tma_store_3d(&tm_phik, smem + s * STAGE, 0, pc.tok0 + c * C, pc.h);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
         mbar_arrive(&B->empty[s]);
       }
     bulk_wait_all();
@@ -1311,6 +1314,7 @@ cudaError_t launch_prefix64_totals(const PrefillArgs& a, const Prefix64Buffers& 
   p.status = b.status;
   p.R = b.R;
   p.P = b.P;
+  p.totals_only = 1;
   CUtensorMap mk, mv, mphik, mp;
   if (!make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
       !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
