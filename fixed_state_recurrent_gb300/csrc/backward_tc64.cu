@@ -698,13 +698,13 @@ bool backward_tc64_supported(const PrefillArgs& a) {
 }
 
 // The split form's workspace: agg, E, dG and G-after slots, S_N and z_N
-// scratch for the prefill's scan, phi(K) scratch for its aggregate kernel.
+// scratch for the prefill's scan.
 size_t backward_tc64_workspace_bytes(int B, int H, int N) {
   using namespace bw;
   if (prefill_prefix64_chosen(B, H, N)) return backward_prefix64_workspace_bytes(B, H, N);
   const Split s = make_split(B * H, N, sm_count());
   const size_t slots = (size_t)s.BH * s.MPH;
-  return (4 * slots + s.BH) * SZ * sizeof(float) + (size_t)s.BH * N * D * sizeof(__nv_bfloat16);
+  return (4 * slots + s.BH) * SZ * sizeof(float);
 }
 
 cudaError_t launch_backward_tc64(const PrefillArgs& a, const float* dO, const float* dS_N,
@@ -754,12 +754,11 @@ cudaError_t launch_backward_tc64(const PrefillArgs& a, const float* dO, const fl
   float* dG = E + slots * SZ;
   float* Gaft = dG + slots * SZ;
   float* SNz = Gaft + slots * SZ;  // S_N (BH x 64 x 64), then z_N (BH x 64)
-  __nv_bfloat16* phik = reinterpret_cast<__nv_bfloat16*>(SNz + (size_t)BH * SZ);
   p.E = E;
   p.dG = dG;
   p.Gaft = Gaft;
   // the prefill's aggregate and scan: every piece's entry state
-  e = launch_prefill_entry_states64(a, agg, E, phik, SNz, SNz + (size_t)BH * D * D, p.status, stream);
+  e = launch_prefill_entry_states64(a, agg, E, SNz, SNz + (size_t)BH * D * D, p.status, stream);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(backward_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e == cudaSuccess)

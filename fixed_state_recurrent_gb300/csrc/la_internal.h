@@ -94,11 +94,10 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream);
 bool prefill_decay64_supported(const PrefillArgs& a);
 // The entry state of every piece of the d = 64 split (the split of
 // prefill_tc_common.cuh's make_split over the current device's SMs) into E,
-// slot layout [BH * MPH][64 * 64 + 64]; agg (the same size), phik (BH * N * 64
-// bf16), S_N and z_N (B * H states) are scratch.
-cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, float* E,
-                                          __nv_bfloat16* phik, float* S_N, float* z_N,
-                                          unsigned* status, cudaStream_t stream);
+// slot layout [BH * MPH][64 * 64 + 64]; agg (the same size), S_N and z_N
+// (B * H states) are scratch.
+cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, float* E, float* S_N,
+                                          float* z_N, unsigned* status, cudaStream_t stream);
 size_t prefill_decay64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream);
 

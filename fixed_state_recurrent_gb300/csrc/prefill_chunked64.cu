@@ -59,7 +59,6 @@ struct Params3 {
   float* agg;  // [BH * MPH][SZ], transposed slots
   float* E;    // [BH * MPH][SZ], exclusive prefixes, transposed slots
   float* gam;  // decayed form: [BH * MPH] the decay over each piece (product of its alphas)
-  __nv_bfloat16* phik;  // [BH][N][D], phi(K) written by K1
   int force_wait;       // test hook: K3 waits once on a barrier that nothing completes
 };
 
@@ -228,7 +227,7 @@ constexpr uint32_t kCols = 128;
 
 struct Bars {
   uint64_t full[NS], xf[NS];
-  uint64_t empty[NS];  // the stage's MMA done and (plain form) its phi(K) store read: 2 arrivals
+  uint64_t empty[NS];  // the stage's MMA done
   uint64_t racc[2];   // a piece's R complete in R[b]   (MMA -> epilogue)
   uint64_t rfree[2];  // R[b] stored                    (epilogue -> MMA)
   uint64_t drain;
@@ -243,12 +242,14 @@ static_assert(sizeof(Bars) <= 256, "barrier area");
 // log2 alpha over the piece), so that the scan can chain pieces as
 // E' = Gamma E + R with Gamma = 2^G_end.  The phi warps first sum log2 alpha
 // over the piece, then scale each phi(K) row by that weight (at most 1) before
-// the MMA reads it; phi(K) is not stored (the decayed output kernel applies phi
-// to K itself).
+// the MMA reads it.  In either form phi(K) is not stored: the output kernel
+// applies phi to K itself, so K is read twice (the second time largely from L2:
+// both kernels walk a run in opposite orders) but phi(K) never goes through
+// DRAM.
 template <bool DECAY>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-       const __grid_constant__ CUtensorMap tm_phik, const Params3 p, const unsigned long long mbar_ns) {
+       const Params3 p, const unsigned long long mbar_ns) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the shared array by pointer
   // arithmetic so that accesses through it stay shared-space accesses
@@ -259,7 +260,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     for (int s = 0; s < NS; ++s) {
       mbar_init(&B->full[s], 1);
       mbar_init(&B->xf[s], 4);
-      mbar_init(&B->empty[s], DECAY ? 1 : 2);
+      mbar_init(&B->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&B->racc[b], 1);
@@ -270,7 +271,6 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     fence_mbar_init();
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_phik);
   }
   const Run run(p.sp, blockIdx.x);
   // The plain form walks its run backwards (last piece and last chunk first),
@@ -298,7 +298,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         uint8_t* st = smem + pre * STAGE;
         const int tok = pc.tok0 + chunk_of(pc, c) * C;
         mbar_arrive_expect_tx(&B->full[pre], 2 * BLK);
-        tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[pre]);
+        tma_load_3d(st, &tm_k, 0, tok, pc.h, &B->full[pre]);
         tma_load_3d(st + BLK, &tm_v, 0, tok, pc.h, &B->full[pre]);
       }
   }
@@ -328,7 +328,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           uint8_t* st = smem + s * STAGE;
           const int tok = pc.tok0 + chunk_of(pc, c) * C;
           mbar_arrive_expect_tx(&B->full[s], 2 * BLK);
-          tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[s]);
+          tma_load_3d(st, &tm_k, 0, tok, pc.h, &B->full[s]);
           tma_load_3d(st + BLK, &tm_v, 0, tok, pc.h, &B->full[s]);
           ++issued;
         }
@@ -442,23 +442,8 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   } else {  // ---- epilogue: R[b] -> workspace slot (transposed rows)
     const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 192;
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
-    uint32_t sj = 0;
     Piece pc;
     for (int i = 0; walk(i, &pc); ++i) {
-      if (!DECAY && et == 0) {  // phi(K) of the piece's chunks -> workspace; a stage is
-                                // released once the store of the chunk after it was
-                                // issued and its own store has read shared memory
-        for (int c = 0; c < pc.nch; ++c, ++sj) {
-          const int s = sj % NS;
-          if (!wait3(x, &B->xf[s], (sj / NS) & 1)) continue;
-          tma_store_3d(&tm_phik, smem + s * STAGE, 0, pc.tok0 + chunk_of(pc, c) * C, pc.h);
-          bulk_commit();
-          if (sj > 0) {
-            bulk_wait_read_but_one();
-            mbar_arrive(&B->empty[(sj - 1) % NS]);
-          }
-        }
-      }
       const int b = i % 2;
       wait3(x, &B->racc[b], (i / 2) & 1);  // on a timeout the rest runs on, storing garbage
       tc_fence_after();
@@ -479,10 +464,6 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       tc_fence_before();
       named_bar_sync(1, 128);
       if (et == 0) mbar_arrive(&B->rfree[b]);
-    }
-    if (!DECAY && et == 0) {
-      bulk_wait_all();
-      if (sj > 0 && !*x.abort) mbar_arrive(&B->empty[(sj - 1) % NS]);
     }
   }
   drain_and_free(x, warp, kCols);
@@ -544,7 +525,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const Params3 p) {
 namespace k3 {
 
 constexpr int NS = 3;
-constexpr uint32_t STAGE = 3 * BLK;                // Q | phi(K) | V
+constexpr uint32_t STAGE = 3 * BLK;                // Q | K (phi applied here) | V
 constexpr uint32_t OFF_ONES = NS * STAGE;
 constexpr uint32_t OFF_SNAP = OFF_ONES + BLK;      // two snapshots
 constexpr uint32_t OFF_OUT = OFF_SNAP + 2 * SNAP;  // output staging: two [128 x 32] fp32 boxes
@@ -599,9 +580,9 @@ __device__ __forceinline__ const float* gsums(uint8_t* smem, uint32_t s) {
 
 __device__ __forceinline__ uint8_t* stage_ptr(uint8_t* smem, uint32_t s) { return smem + s * STAGE; }
 
-// Q, phi(K), V and o are touched once by this kernel and go through TMA with
-// the evict-first L2 policy (the aggregate kernel loads K the same way), so
-// that V and phi(K), which both launches read, are what L2 keeps.
+// Q, K, V and o go through TMA with the evict-first L2 policy here (the
+// aggregate kernel loads K and V with the normal one, so that what both
+// launches read is what L2 keeps).  The phi warps apply phi to Q and K.
 //
 // Two threads issue MMAs.  The MMA warp issues, per chunk a, the scores of
 // chunk a + 1 and then P [V | 1] and phi(Q) [S | z] of chunk a, so that P of
@@ -681,7 +662,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_arrive_expect_tx(&B->full[pre], 3 * BLK);
         tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->full[pre]);
         tma_load_3d_ef(st + 2 * BLK, &tm_v, 0, tok, pc.h, &B->full[pre]);
-        if (DECAY) tma_load_3d_ef(st + BLK, &tm_k, 0, tok, pc.h, &B->full[pre]);
+        tma_load_3d_ef(st + BLK, &tm_k, 0, tok, pc.h, &B->full[pre]);
       }
   }
   init_ones(smem + OFF_ONES, threadIdx.x, 32 * kWarps);
@@ -700,7 +681,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
 
   if (warp == 0) {
-    if (lane == 0) {  // ---- TMA producer: Q, phi(K), V chunk tiles (see the set-up for the first)
+    if (lane == 0) {  // ---- TMA producer: Q, K, V chunk tiles (see the set-up for the first)
       uint32_t sj = 0, issued = pre;
       Piece pc;
       for (int i = 0; run.piece(p.sp, i, &pc); ++i)
@@ -708,13 +689,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const int s = sj % NS;
           uint8_t* st = stage_ptr(smem, s);
           const int tok = pc.tok0 + c * C;
-          if (sj < pre) {  // Q and V are on their way; phi(K) follows the aggregate kernel
-            if (!DECAY) {
-              if (sj == 0) pdl_wait();  // phi(K) is the aggregate kernel's output
-              tma_load_3d_ef(st + BLK, &tm_k, 0, tok, pc.h, &B->full[s]);
-            }
-            continue;
-          }
+          if (sj < pre) continue;  // went out during the set-up
           if (!wait3(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           mbar_arrive_expect_tx(&B->full[s], 3 * BLK);
           tma_load_3d_ef(st, &tm_q, 0, tok, pc.h, &B->full[s]);
@@ -789,7 +764,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
     }
     __syncwarp();
-  } else if (warp < 6) {  // ---- phi on Q (one tile row per thread); phi(K) comes from K1
+  } else if (warp < 6) {  // ---- phi on Q and K (one tile row per thread)
     const int r = threadIdx.x - 64;
     uint32_t sj = 0;
     Piece pc;
@@ -807,7 +782,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           // Q, and in the decayed form K too: one copy of the loop body (the
           // roles' code together must stay within the instruction caches)
 #pragma unroll 1
-          for (int m = 0; m < (DECAY ? 4 : 2); ++m) phi_row<4>(st + (m / 2) * BLK, r, 4 * (m % 2), valid);
+          for (int m = 0; m < 4; ++m) phi_row<4>(st + (m / 2) * BLK, r, 4 * (m % 2), valid);
         }
         if (DECAY) {
           // g_t: inclusive sums of log2 alpha over the chunk (alpha = 1 past the
@@ -1098,6 +1073,8 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (DECAY) {  // phi(K) of chunk j rescaled by all four P warps
           for (int q = 0; q < 4; ++q)
             if (!count_reached(x, &B->pdone[q], j + 1)) return false;
+        } else if (!wait3(x, &B->xf[s], (j / NS) & 1)) {  // phi applied to K by the phi warps
+          return false;
         }
         tc_fence_after();
         const uint32_t st = smem_u32(stage_ptr(smem, s)), vt = st + 2 * BLK;
@@ -1152,9 +1129,11 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 }  // namespace
 
 // agg and E slots, then phi(K)
+// the piece totals and the entry states (phi(K) does not go through the
+// workspace: the output kernel applies phi to K itself)
 size_t prefill_chunked64_workspace_bytes(int B, int H, int N) {
   const Split s = make_split(B * H, N, sm_count());
-  return 2 * (size_t)s.BH * s.MPH * SZ * sizeof(float) + (size_t)s.BH * N * D * sizeof(__nv_bfloat16);
+  return 2 * (size_t)s.BH * s.MPH * SZ * sizeof(float);
 }
 
 cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) {
@@ -1183,10 +1162,6 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
     return cudaErrorInvalidValue;
   p.agg = reinterpret_cast<float*>(ws + sizeof(WsHeader));
   p.E = p.agg + slots * SZ;
-  p.phik = reinterpret_cast<__nv_bfloat16*>(p.E + slots * SZ);
-  CUtensorMap mphik;
-  if (!make_map(&mphik, p.phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C))
-    return cudaErrorInvalidValue;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
 
@@ -1209,7 +1184,7 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k1::kWarps);
   cfg.dynamicSmemBytes = k1::SMEM;
-  e = cudaLaunchKernelEx(&cfg, k1::aggregate_kernel<false>, mk, mv, mphik, p, mbar_ns);
+  e = cudaLaunchKernelEx(&cfg, k1::aggregate_kernel<false>, mk, mv, p, mbar_ns);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
   cfg.blockDim = dim3(k2::kThreads);
@@ -1219,7 +1194,7 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k3::kWarps);
   cfg.dynamicSmemBytes = k3::SMEM;
-  return cudaLaunchKernelEx(&cfg, k3::output_kernel<false>, mq, mphik, mv, mo, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, k3::output_kernel<false>, mq, mk, mv, mo, p, mbar_ns);
 }
 
 // the decayed form's slots: agg and E, then one decay factor per piece slot
@@ -1237,19 +1212,17 @@ size_t prefill_decay64_workspace_bytes(int B, int H, int N) {
 
 // The entry state of every piece of the d = 64 split, for other kernels that
 // walk the same pieces (the gradient): the aggregate and scan launches of the
-// plain form into agg and E (slot layout), with phik, S_N and z_N as scratch
-// the two kernels fill; bounded-wait failures go to `status`.  The scan is a
+// plain form into agg and E (slot layout), with S_N and z_N as scratch the
+// scan fills; bounded-wait failures go to `status`.  The scan is a
 // programmatic dependent, and so may be the launch that follows.
-cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, float* E,
-                                          __nv_bfloat16* phik, float* S_N, float* z_N,
+cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, float* E, float* S_N, float* z_N,
                                           unsigned* status, cudaStream_t stream) {
   const int BH = a.B * a.H;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  CUtensorMap mk, mv, mphik;
+  CUtensorMap mk, mv;
   if (!make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
-      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
-      !make_map(&mphik, phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C))
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C))
     return cudaErrorInvalidValue;
   Params3 p = {};
   p.sp = make_split(BH, a.N, sms);
@@ -1260,12 +1233,11 @@ cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, floa
   p.status = status;
   p.agg = agg;
   p.E = E;
-  p.phik = phik;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
   cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k1::SMEM);
   if (e != cudaSuccess) return e;
-  k1::aggregate_kernel<false><<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mphik, p, mbar_ns);
+  k1::aggregate_kernel<false><<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, p, mbar_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute pdl;
@@ -1336,7 +1308,7 @@ cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cud
                            (int)k1::SMEM);
   if (e != cudaSuccess) return e;
   // (the decayed aggregate kernel stores no phi(K): its third map is unused)
-  k1::aggregate_kernel<true><<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, mk, p, mbar_ns);
+  k1::aggregate_kernel<true><<<p.sp.G, 32 * k1::kWarps, k1::SMEM, stream>>>(mk, mv, p, mbar_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute pdl;
