@@ -17,8 +17,9 @@
 namespace {
 
 // 16 MiB of scratch per device: enough for la_prefill's workspace at
-// dk = dv = 64 up to e.g. 16 heads of 4096 tokens, at dk = dv = 128 up to e.g.
-// 4 heads of 2048 tokens.
+// dk = dv = 64 up to e.g. 16 heads of 4096 tokens (and, past 2048 chunks of
+// 128 tokens, where only each piece's state is kept, for a few hundred heads
+// of any length), at dk = dv = 128 up to e.g. 4 heads of 2048 tokens.
 constexpr size_t kScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_la_scratch[kScratchBytes];

@@ -39,9 +39,10 @@ def _inputs(B, H, N, d, dtype, seed):
 
 
 @pytest.mark.parametrize("case", [(2, 4, 4096, 64, torch.bfloat16),   # tensor-core path
+                                  (1, 4, 70000, 64, torch.bfloat16),  # d = 64, past 2048 chunks
                                   (2, 3, 1000, 128, torch.bfloat16),  # tensor-core, d = 128
                                   (1, 2, 300, 64, torch.float32)],    # CUDA-core path
-                         ids=["bf16_d64", "bf16_d128", "f32"])
+                         ids=["bf16_d64", "bf16_d64_long", "bf16_d128", "f32"])
 def test_noalloc_matches_prefill_two_calls_in_a_row(la, orc, case):
     B, H, N, d, dtype = case
     g = torch.Generator().manual_seed(77)
@@ -108,10 +109,11 @@ def test_noalloc_bounded_wait_reports_timeout(la, orc, monkeypatch):
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(la):
-    # 64 heads x 65536 tokens at d = 64 needs far more than the 16 MiB scratch
-    need = la.prefill_workspace_bytes(1, 64, 65536, 64, 64)
+    # 64 heads x 4096 tokens at d = 64 (2048 chunks, the two-launch form, which
+    # keeps a bf16 copy of phi(K)) needs more than the 16 MiB scratch
+    need = la.prefill_workspace_bytes(1, 64, 4096, 64, 64)
     assert need > (16 << 20)
-    q = torch.empty((1, 64, 65536, 64), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((1, 64, 4096, 64), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(la.LAError) as err:
         la.prefill_noalloc(q, q, q)
     assert err.value.status == 1  # LA_ERR_INVALID_ARG
