@@ -15,11 +15,13 @@
 //   K1 (aggregate): per piece, R^T = sum_c V_c^T phi(K_c) (TMEM lanes = value
 //      column j) and the key sum zeta = sum_c phi(K_c)^T 1 (lanes = key column
 //      i, an N = 16 product against an all-ones operand), stored to the
-//      piece's workspace slot as S^T rows and then z; phi(K) itself is stored
-//      (bf16, the layout of K) for K3.
+//      piece's workspace slot as S^T rows and then z.  phi(K) is not stored:
+//      K3 applies phi to K itself, so nothing per token goes through the
+//      workspace.
 //   K2 (scan): per head, each piece's entry state as the left fold S0 + R_0 +
 //      R_1 + ... in fp32 (the same order every run), and S_N, z_N.
-//   K3 (output): each piece replays its chunks from its entry state E.  phi(Q)
+//   K3 (output): each piece replays its chunks from its entry state E; phi is
+//      applied to each K tile in shared memory, in place.  phi(Q)
 //      lives in TMEM (the A operand of the two products that read it), so a
 //      chunk's Q tile frees its shared-memory slot as soon as it has been read;
 //      the running state S^T, z lives in TMEM, is snapshotted to bf16 for the
@@ -28,7 +30,7 @@
 //      phi(Q) phi(K)^T, P = causal mask (bf16, written back into TMEM),
 //      [num | den] = phi(Q) [S | z_hi | z_lo] + P [V | 1], o = num / (den + eps)
 //      stored through TMA.
-#include "prefill_tc_common.cuh"
+#include "prefill_scan.cuh"
 
 namespace la {
 namespace {
@@ -61,7 +63,6 @@ struct Params {
   unsigned* status;      // sticky error bits (the workspace header's)
   float* agg;            // [BH * MPH][SZ] piece totals, S^T rows then z
   float* E;              // [BH * MPH][SZ] entry states, same layout
-  __nv_bfloat16* phik;   // [BH][N][D], phi(K) written by K1
   int force_wait;        // test hook: K3 waits once on a barrier that nothing completes
 };
 
@@ -190,13 +191,13 @@ constexpr uint32_t STAGE = 2 * TILE;    // K | V
 constexpr uint32_t OFF_ONES = NS * STAGE;
 constexpr uint32_t OFF_BAR = OFF_ONES + ONES;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
-constexpr int kWarps = 10;  // 0 TMA, 1 MMA, 2-5 phi, 6-9 epilogue (thread 192 also stores phi(K))
+constexpr int kWarps = 10;  // 0 TMA, 1 MMA, 2-5 phi, 6-9 epilogue
 constexpr uint32_t kCols = 512;
 constexpr uint32_t RCOLS = 144;  // per buffer: R^T (128 columns), then zeta (16)
 
 struct Bars {
   uint64_t full[NS], xf[NS];
-  uint64_t empty[NS];  // the stage's MMA done and its phi(K) store read: 2 arrivals
+  uint64_t empty[NS];  // the stage's MMA done
   uint64_t racc[2];    // a piece's totals complete in buffer b  (MMA -> epilogue)
   uint64_t rfree[2];   // buffer b stored                       (epilogue -> MMA)
   uint64_t drain;
@@ -207,8 +208,7 @@ static_assert(sizeof(Bars) <= 256, "barrier area");
 
 __global__ void __launch_bounds__(32 * kWarps, 1)
 aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 const __grid_constant__ CUtensorMap tm_phik, const Params p,
-                 const unsigned long long mbar_ns) {
+                 const Params p, const unsigned long long mbar_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + OFF_BAR);
@@ -217,7 +217,7 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     for (int s = 0; s < NS; ++s) {
       mbar_init(&B->full[s], 1);
       mbar_init(&B->xf[s], 4);
-      mbar_init(&B->empty[s], 2);
+      mbar_init(&B->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&B->racc[b], 1);
@@ -228,21 +228,20 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     fence_mbar_init();
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_phik);
   }
   const Run run(p.sp, blockIdx.x);
-  // The run is walked backwards (last piece, last chunk first): the phi(K) and
-  // V it touches last are those of the run's first chunks, which the output
-  // kernel reads first, so they are still in L2.  A piece's total does not
-  // depend on the order.
+  // The run is walked backwards (last piece, last chunk first): the K and V it
+  // touches last are those of the run's first chunks, which the output kernel
+  // reads first, so they are still in L2.  A piece's total does not depend on
+  // the order.
   const int npieces = run.count(p.sp);
   auto walk = [&](int i, Piece* pc) { return i < npieces && run.piece(p.sp, npieces - 1 - i, pc); };
   auto chunk_of = [&](const Piece& pc, int c) { return pc.nch - 1 - c; };
   auto load_stage = [&](uint32_t s, int tok, int h) {
     uint8_t* st = smem + s * STAGE;
     mbar_arrive_expect_tx(&B->full[s], 2 * TILE);
-    tma_load_3d_ef(st, &tm_k, 0, tok, h, &B->full[s]);
-    tma_load_3d_ef(st + BLK, &tm_k, 64, tok, h, &B->full[s]);
+    tma_load_3d(st, &tm_k, 0, tok, h, &B->full[s]);
+    tma_load_3d(st + BLK, &tm_k, 64, tok, h, &B->full[s]);
     tma_load_3d(st + TILE, &tm_v, 0, tok, h, &B->full[s]);
     tma_load_3d(st + TILE + BLK, &tm_v, 64, tok, h, &B->full[s]);
   };
@@ -334,25 +333,8 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   } else {  // ---- epilogue: buffer b -> workspace slot (S^T rows, then z)
     const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 192;
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
-    uint32_t sj = 0;
     Piece pc;
     for (int i = 0; walk(i, &pc); ++i) {
-      if (et == 0) {  // phi(K) of the piece's chunks -> workspace; a stage is released
-                      // once the store of the chunk after it was issued and its own
-                      // store has read shared memory
-        for (int c = 0; c < pc.nch; ++c, ++sj) {
-          const uint32_t s = sj % NS;
-          if (!wait_b(x, &B->xf[s], (sj / NS) & 1)) continue;
-          uint8_t* st = smem + s * STAGE;
-          tma_store_3d(&tm_phik, st, 0, pc.tok0 + chunk_of(pc, c) * C, pc.h);
-          tma_store_3d(&tm_phik, st + BLK, 64, pc.tok0 + chunk_of(pc, c) * C, pc.h);
-          bulk_commit();
-          if (sj > 0) {
-            bulk_wait_read_but_one();
-            mbar_arrive(&B->empty[(sj - 1) % NS]);
-          }
-        }
-      }
       const int b = i % 2;
       wait_b(x, &B->racc[b], (i / 2) & 1);  // on a timeout the rest runs on, storing garbage
       __syncwarp();
@@ -377,10 +359,6 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       named_bar_sync(1, 128);
       if (et == 0) mbar_arrive(&B->rfree[b]);
     }
-    if (et == 0) {
-      bulk_wait_all();
-      if (sj > 0 && !*x.abort) mbar_arrive(&B->empty[(sj - 1) % NS]);
-    }
   }
   drain_and_free(x, warp, kCols);
 }
@@ -392,40 +370,10 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
 namespace k2 {
 
-constexpr int kThreads = 256;
-
-__global__ void __launch_bounds__(kThreads) scan_kernel(const Params p) {
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
   pdl_launch_dependents();  // the output kernel may be scheduled now
   pdl_wait();               // the totals of the aggregate kernel are complete
-  const int e = blockIdx.x * kThreads + threadIdx.x;  // slot element: row * 128 + i
-  const int h = blockIdx.y;
-  if (e >= SZ) return;
-  const Split& s = p.sp;
-  const int row = e / D, i = e % D;  // row < 128: S[i][row]; row 128: z[i]
-  float acc = 0.f;
-  if (row < D) {
-    if (p.S0) acc = p.S0[(size_t)h * D * D + i * D + row];
-  } else if (p.z0) {
-    acc = p.z0[(size_t)h * D + i];
-  }
-  const int first = s.owner((long long)h * s.NC);
-  const int npieces = s.owner((long long)(h + 1) * s.NC - 1) - first + 1;
-  const size_t base = (size_t)h * s.MPH * SZ + e;
-  constexpr int U = 8;
-  for (int w0 = 0; w0 < npieces; w0 += U) {
-    float a[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) a[u] = (w0 + u < npieces) ? __ldcg(p.agg + base + (size_t)(w0 + u) * SZ) : 0.f;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (w0 + u < npieces) {
-        __stcg(p.E + base + (size_t)(w0 + u) * SZ, acc);
-        acc += a[u];
-      }
-    }
-  }
-  if (row < D) p.S_N[(size_t)h * D * D + i * D + row] = acc;
-  else p.z_N[(size_t)h * D + i] = acc;
+  scan_fold<D, false>(p.sp, p.agg, p.E, nullptr, p.S0, p.z0, p.S_N, p.z_N);
 }
 
 }  // namespace k2
@@ -435,8 +383,8 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const Params p) {
 
 namespace k3 {
 
-constexpr int NS = 2;                         // phi(K), V stages (64 KB each)
-constexpr uint32_t STAGE = 2 * TILE;          // phi(K) | V
+constexpr int NS = 2;                         // K, V stages (64 KB each)
+constexpr uint32_t STAGE = 2 * TILE;          // K (phi applied in place) | V
 constexpr uint32_t OFF_Q = NS * STAGE;        // one Q slot: its rows go to TMEM as phi(Q)
 constexpr uint32_t OFF_SNAP = OFF_Q + TILE;   // the state snapshot
 constexpr uint32_t OFF_ONES = OFF_SNAP + SNAP;
@@ -445,8 +393,9 @@ constexpr uint32_t OFF_BAR = OFF_OUT + BLK;
 constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 static_assert(OFF_SNAP % 1024 == 0 && OFF_ONES % 1024 == 0 && OFF_OUT % 1024 == 0, "atom alignment");
-// 0 phi(K)/V producer, 1 MMA, 2-5 phi(Q), 6-9 P, 10-13 state snapshots and
-// output epilogue, 14 state chain, 15 Q producer: 512 threads, 128 registers
+// 0 K/V producer, 1 MMA, 2-5 phi (K in place, then Q into TMEM), 6-9 P,
+// 10-13 state snapshots and output epilogue, 14 state chain, 15 Q producer:
+// 512 threads, 128 registers
 constexpr int kWarps = 16;
 constexpr uint32_t kCols = 512;
 constexpr uint32_t TA = 0;    // scores, then P (packed bf16, columns 0..63)
@@ -457,6 +406,7 @@ constexpr uint32_t TZ = 464;  // running z (lane i = key column), 16 columns
 
 struct Bars {
   uint64_t full[NS], empty[NS];  // stage landed; stage free (MMA commit + state chain: 2 arrivals)
+  uint64_t xf[NS];               // phi applied to the stage's K        (phi warps -> MMA, state chain)
   uint64_t qfull, qempty;        // Q landed; Q read by the four phi(Q) warps
   uint64_t qready;               // phi(Q) in TMEM                     (phi(Q) warps -> MMA)
   uint64_t accS;                 // scores in A                         (MMA -> P warps)
@@ -491,6 +441,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int s = 0; s < NS; ++s) {
       mbar_init(&B->full[s], 1);
       mbar_init(&B->empty[s], 2);
+      mbar_init(&B->xf[s], 4);
     }
     mbar_init(&B->qfull, 1);
     mbar_init(&B->qempty, 4);
@@ -516,9 +467,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     tma_prefetch_desc(&tm_o);
   }
   const Run run(p.sp, blockIdx.x);
-  // The first stages' V tiles and the first Q tile go out before the rest of
-  // the set-up; each stage's barrier expects phi(K) too, which joins it once
-  // the aggregate kernel has finished.
+  // The first stages' K and V tiles and the first Q tile go out before the
+  // rest of the set-up (inputs only: the launches before this one have waited
+  // for whatever precedes the call on the stream).
   uint32_t pre = 0;
   bool any = false;
   if (threadIdx.x == 0) {
@@ -528,6 +479,8 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         uint8_t* st = smem + pre * STAGE;
         const int tok = pc.tok0 + c * C;
         mbar_arrive_expect_tx(&B->full[pre], 2 * TILE);
+        tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[pre]);
+        tma_load_3d_ef(st + BLK, &tm_k, 64, tok, pc.h, &B->full[pre]);
         tma_load_3d_ef(st + TILE, &tm_v, 0, tok, pc.h, &B->full[pre]);
         tma_load_3d_ef(st + TILE + BLK, &tm_v, 64, tok, pc.h, &B->full[pre]);
         if (pre == 0) {
@@ -556,7 +509,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const Ctx x{&p, &B->abort, *reinterpret_cast<volatile uint32_t*>(&B->tmem_slot), mbar_ns};
 
   if (warp == 0) {
-    if (lane == 0) {  // ---- phi(K), V producer (V of the first stages went out above)
+    if (lane == 0) {  // ---- K, V producer (the first stages went out above)
       uint32_t sj = 0, issued = pre;
       Piece pc;
       for (int i = 0; run.piece(p.sp, i, &pc); ++i)
@@ -564,12 +517,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const uint32_t s = sj % NS;
           uint8_t* st = smem + s * STAGE;
           const int tok = pc.tok0 + c * C;
-          if (sj < pre) {  // phi(K) is the aggregate kernel's output
-            if (sj == 0) pdl_wait();
-            tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[s]);
-            tma_load_3d_ef(st + BLK, &tm_k, 64, tok, pc.h, &B->full[s]);
-            continue;
-          }
+          if (sj < pre) continue;
           if (!wait_b(x, &B->empty[s], ((sj / NS) - 1) & 1)) break;
           mbar_arrive_expect_tx(&B->full[s], 2 * TILE);
           tma_load_3d_ef(st, &tm_k, 0, tok, pc.h, &B->full[s]);
@@ -609,7 +557,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int i = 0; ok && run.piece(p.sp, i, &pc); ++i)
         for (int c = 0; ok && c < pc.nch; ++c, ++g) {
           const uint32_t s = g % NS;
-          ok = wait_b(x, &B->qready, g & 1) && wait_b(x, &B->full[s], (g / NS) & 1) &&
+          ok = wait_b(x, &B->qready, g & 1) && wait_b(x, &B->xf[s], (g / NS) & 1) &&
                (g == 0 || wait_b(x, &B->afree, (g - 1) & 1));
           if (!ok) break;
           tc_fence_after();
@@ -647,7 +595,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
     }
     __syncwarp();
-  } else if (warp < 6) {  // ---- phi(Q) into TMEM (one query row per thread)
+  } else if (warp < 6) {  // ---- phi: K in place, then Q into TMEM (one row per thread)
     const int quad = warp % 4, row = 32 * quad + lane;
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
     uint32_t g = 0;
@@ -655,6 +603,15 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int i = 0; run.piece(p.sp, i, &pc); ++i)
       for (int c = 0; c < pc.nch; ++c, ++g) {
         const int valid = pc.tok1 - (pc.tok0 + c * C);
+        const uint32_t s = g % NS;
+        if (wait_w(x, &B->full[s], (g / NS) & 1)) {  // the chunk's K tile: phi in place
+          uint8_t* kt = smem + s * STAGE;
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) phi_row<4>(kt + (m / 2) * BLK, row, 4 * (m % 2), valid);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B->xf[s]);
+        }
         // Q landed, and the products of the chunk before have read phi(Q)
         if (!wait_w(x, &B->qfull, g & 1)) continue;
         if (g > 0 && !wait_w(x, &B->qsdone, (g - 1) & 1)) continue;
@@ -831,13 +788,14 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   } else {  // ---- the state chain: S^T += V^T phi(K), z += phi(K)^T 1, chunk by chunk
     if (lane == 0) {
       const uint64_t ones = sdesc_sw128(smem_u32(smem + OFF_ONES), 16, 1024);
-      // The advance of chunk j (its stage loaded; the running state read), or,
-      // for a piece's last chunk, which has none, just this issuer's share of
-      // the stage's release.  Chunk j is loaded, so its stage's previous use
-      // has been released and the release counts for chunk j.
+      // The advance of chunk j (its stage loaded and phi applied to its K; the
+      // running state read), or, for a piece's last chunk, which has none, just
+      // this issuer's share of the stage's release.  Chunk j is loaded, so its
+      // stage's previous use has been released and the release counts for
+      // chunk j.
       auto advance = [&](uint32_t j, bool any_adv) {
         const uint32_t s = j % NS;
-        if (!wait_b(x, &B->full[s], (j / NS) & 1)) return false;
+        if (!wait_b(x, &B->xf[s], (j / NS) & 1)) return false;
         if (!any_adv) {
           mbar_arrive(&B->empty[s]);
           return true;
@@ -880,10 +838,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
 }  // namespace
 
-// agg and E slots, then phi(K)
+// agg and E slots
 size_t prefill_chunked128_workspace_bytes(int B, int H, int N) {
   const Split s = make_split(B * H, N, sm_count());
-  return 2 * (size_t)s.BH * s.MPH * SZ * sizeof(float) + (size_t)s.BH * N * D * sizeof(__nv_bfloat16);
+  return 2 * (size_t)s.BH * s.MPH * SZ * sizeof(float);
 }
 
 cudaError_t launch_prefill_chunked128(const PrefillArgs& a, cudaStream_t stream) {
@@ -910,10 +868,6 @@ cudaError_t launch_prefill_chunked128(const PrefillArgs& a, cudaStream_t stream)
     return cudaErrorInvalidValue;
   p.agg = reinterpret_cast<float*>(ws + sizeof(WsHeader));
   p.E = p.agg + slots * SZ;
-  p.phik = reinterpret_cast<__nv_bfloat16*>(p.E + slots * SZ);
-  CUtensorMap mphik;
-  if (!make_map(&mphik, p.phik, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C))
-    return cudaErrorInvalidValue;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
 
@@ -936,17 +890,17 @@ cudaError_t launch_prefill_chunked128(const PrefillArgs& a, cudaStream_t stream)
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k1::kWarps);
   cfg.dynamicSmemBytes = k1::SMEM;
-  e = cudaLaunchKernelEx(&cfg, k1::aggregate_kernel, mk, mv, mphik, p, mbar_ns);
+  e = cudaLaunchKernelEx(&cfg, k1::aggregate_kernel, mk, mv, p, mbar_ns);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
-  cfg.blockDim = dim3(k2::kThreads);
+  cfg.gridDim = dim3(scan_blocks_per_head<D>(), BH);
+  cfg.blockDim = dim3(kScanThreads);
   cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, k2::scan_kernel, p);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k3::kWarps);
   cfg.dynamicSmemBytes = k3::SMEM;
-  return cudaLaunchKernelEx(&cfg, k3::output_kernel, mq, mphik, mv, mo, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, k3::output_kernel, mq, mk, mv, mo, p, mbar_ns);
 }
 
 }  // namespace la

@@ -28,7 +28,7 @@
 //      written back into TMEM), [num | den] = P [V | 1] + phi(Q) [S | z] as two
 //      N = 80 products, o = num / (den + eps) stored through TMA.
 // V and phi(K) are read again by K3 (from L2 when the workload fits in it).
-#include "prefill_tc_common.cuh"
+#include "prefill_scan.cuh"
 
 namespace la {
 namespace {
@@ -476,45 +476,12 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
 namespace k2 {
 
-constexpr int kThreads = 256;
-
 // DECAY: each piece first decays what came before it, E' = Gamma E + R.
 template <bool DECAY>
-__global__ void __launch_bounds__(kThreads) scan_kernel(const Params3 p) {
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params3 p) {
   pdl_launch_dependents();  // the output kernel may be scheduled now
   pdl_wait();               // the aggregates of the aggregate kernel are complete
-  const int e = blockIdx.x * kThreads + threadIdx.x;  // slot element: row * 64 + i
-  const int h = blockIdx.y;
-  if (e >= SZ) return;
-  const Split& s = p.sp;
-  const int row = e / D, i = e % D;  // row < 64: S[i][row]; row 64: z[i]
-  float acc = 0.f;
-  if (row < D) {
-    if (p.S0) acc = p.S0[(size_t)h * D * D + i * D + row];
-  } else if (p.z0) {
-    acc = p.z0[(size_t)h * D + i];
-  }
-  const int first = s.owner((long long)h * s.NC);
-  const int npieces = s.owner((long long)(h + 1) * s.NC - 1) - first + 1;
-  const size_t base = (size_t)h * s.MPH * SZ + e;
-  constexpr int U = 8;
-  for (int w0 = 0; w0 < npieces; w0 += U) {
-    float a[U], gm[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      a[u] = (w0 + u < npieces) ? __ldcg(p.agg + base + (size_t)(w0 + u) * SZ) : 0.f;
-      gm[u] = (DECAY && w0 + u < npieces) ? __ldcg(p.gam + (size_t)h * s.MPH + w0 + u) : 1.f;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (w0 + u < npieces) {
-        __stcg(p.E + base + (size_t)(w0 + u) * SZ, acc);
-        acc = DECAY ? fmaf(gm[u], acc, a[u]) : acc + a[u];
-      }
-    }
-  }
-  if (row < D) p.S_N[(size_t)h * D * D + i * D + row] = acc;
-  else p.z_N[(size_t)h * D + i] = acc;
+  scan_fold<D, DECAY>(p.sp, p.agg, p.E, p.gam, p.S0, p.z0, p.S_N, p.z_N);
 }
 
 }  // namespace k2
@@ -1186,8 +1153,8 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   cfg.dynamicSmemBytes = k1::SMEM;
   e = cudaLaunchKernelEx(&cfg, k1::aggregate_kernel<false>, mk, mv, p, mbar_ns);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
-  cfg.blockDim = dim3(k2::kThreads);
+  cfg.gridDim = dim3(scan_blocks_per_head<D>(), BH);
+  cfg.blockDim = dim3(kScanThreads);
   cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, k2::scan_kernel<false>, p);
   if (e != cudaSuccess) return e;
@@ -1247,8 +1214,8 @@ cudaError_t launch_prefill_entry_states64(const PrefillArgs& a, float* agg, floa
   cfg.stream = stream;
   cfg.attrs = &pdl;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
-  cfg.blockDim = dim3(k2::kThreads);
+  cfg.gridDim = dim3(scan_blocks_per_head<D>(), BH);
+  cfg.blockDim = dim3(kScanThreads);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, k2::scan_kernel<false>, p);
 }
@@ -1318,8 +1285,8 @@ cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cud
   cfg.stream = stream;
   cfg.attrs = &pdl;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3((SZ + k2::kThreads - 1) / k2::kThreads, BH);
-  cfg.blockDim = dim3(k2::kThreads);
+  cfg.gridDim = dim3(scan_blocks_per_head<D>(), BH);
+  cfg.blockDim = dim3(kScanThreads);
   cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, k2::scan_kernel<true>, p);
   if (e != cudaSuccess) return e;

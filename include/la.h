@@ -295,9 +295,9 @@ la_status delta_read_device_status(cudaStream_t stream);
  *   4096 tokens fit (10.3 MiB on a 152-SM GPU), 16 heads of 4096 just fit
  *   (15.2 MiB), 32 do not; past 2048 chunks (heads x chunks) the d = 64
  *   form keeps only two state slots per (head, block) pair, so 64 heads of
- *   65536 tokens take 8.1 MiB; at dk = dv = 128 the copy of phi(K) takes 256
- *   bytes per token and the slots are 66 KB: 4 heads of 2048 tokens fit
- *   (10.6 MiB), 8 do not.  The CUDA-core path's chunk slots take
+ *   65536 tokens take 8.1 MiB; at dk = dv = 128 the workspace is two arrays
+ *   of 66 KB slots, one per (head, block) pair: 4 heads of 2048 tokens fit
+ *   (8.6 MiB), 8 do not.  The CUDA-core path's chunk slots take
  *   (dk dv + dk + 1) * 4 bytes per chunk (1.2 MiB for 2 heads of 300 tokens
  *   at d = 64).  la_prefill_workspace_bytes gives the figure.
  *   Set-up: the first call on each device (with that device current) looks up

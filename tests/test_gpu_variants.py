@@ -273,9 +273,10 @@ def test_decay_prefill_tc_matches_oracle(la, orc, N, arange):
     assert la.delta_read_device_status() == 0
 
 
-# the decayed two-launch form over pieces: runs that cross heads, heads over
-# many blocks (entry states folded from earlier totals and decays)
-DECAY_SHAPES = [(2, 5, 3000), (3, 40, 333), (1, 2, 20000)]
+# the decayed forms over pieces: runs that cross heads, heads over many blocks
+# (entry states folded from earlier totals and decays); the last shape has
+# more than 2048 chunks, so it runs the three-launch form
+DECAY_SHAPES = [(2, 5, 3000), (3, 40, 333), (1, 2, 20000), (1, 4, 70000)]
 
 
 @pytest.mark.parametrize("shape", DECAY_SHAPES, ids=[str(s) for s in DECAY_SHAPES])
