@@ -59,7 +59,7 @@ def _args():
                    help="headline workload only (no long/decode/delta/e2e/cpu)")
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run "
-                        "(long,decode,delta,pr1,gated,decay,rbw,nc,backward,prefill128)")
+                        "(long,decode,delta,pr1,gated,decay,rbw,nc,backward,prefill128,rbw128,nc128)")
     p.add_argument("--profile-backward", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain la_prefill_backward calls and exit (for ncu)")
     p.add_argument("--profile-decay", type=int, default=0, metavar="CALLS",
@@ -593,14 +593,15 @@ def bench_backward(api, rank, world, reps=5):
             "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "peak_kind": f"of {kind}"}
 
 
-def bench_order_prefill(api, rank, world, mode, reps=12, sets=4):
+def bench_order_prefill(api, rank, world, mode, reps=12, sets=4, wname="prefill"):
     """la_prefill_variant in read-before-write or non-causal order (no decay)
-    on the headline prefill shape, on the tensor cores (read before write:
-    la_prefill's two launches with a strict mask; non-causal: the piece totals,
-    then one product per chunk against the head's final state), over `sets`
-    rotating input/output sets."""
+    on the headline prefill shape (wname "prefill") or its d = 128 twin
+    ("prefill128"), on the tensor cores (read before write: la_prefill's
+    launches with a strict mask; non-causal: the piece totals, then one product
+    per chunk against the head's final state), over `sets` rotating
+    input/output sets."""
     import torch
-    w = inputs_mod().WORKLOADS["prefill"]
+    w = inputs_mod().WORKLOADS[wname]
     dev = torch.device("cuda")
     bufs = []
     for r in range(sets):
@@ -621,10 +622,10 @@ def bench_order_prefill(api, rank, world, mode, reps=12, sets=4):
     _, per = _timed(fn, reps, stream, world)
     ms_calls = statistics.median(per)
     ms = _graph_ms(fn, 4 * sets, stream, world)
-    b = PREFILL_BYTES_PER_TOKEN * w.tokens
+    b = (2 * (w.dk + w.dk + w.dv) + 4 * w.dv) * w.tokens  # q, k, v bf16 in, o fp32 out
     hbm_peak, _, kind = _peaks()
     order = "read-before-write" if mode == api.LA_MODE_READ_BEFORE_WRITE else "non-causal"
-    return {"workload": f"{order} prefill: B=4 H=8 N=4096 dk=dv=64 bf16",
+    return {"workload": f"{order} prefill: B={w.B} H={w.H} N={w.N} dk=dv={w.dk} bf16",
             "ms_per_call": ms, "ms_per_python_call": ms_calls,
             "timing": f"{4 * sets} calls in one CUDA graph, replayed (device time per call); "
                       "ms_per_python_call: median of back-to-back calls from Python",
@@ -838,7 +839,7 @@ def main():
     e2e = None
     wanted = set(x for x in args.only.split(",") if x) or {"long", "decode", "delta", "pr1",
                                                              "gated", "decay", "rbw", "nc", "backward",
-                                                             "prefill128"}
+                                                             "prefill128", "rbw128", "nc128"}
     if not args.no_extra:
         if "long" in wanted:
             extra["long"] = bench_simple_prefill(api, "long", rank, world)
@@ -858,6 +859,12 @@ def main():
             extra["rbw_prefill"] = bench_order_prefill(api, rank, world, api.LA_MODE_READ_BEFORE_WRITE)
         if "nc" in wanted:
             extra["noncausal_prefill"] = bench_order_prefill(api, rank, world, api.LA_MODE_NONCAUSAL)
+        if "rbw128" in wanted:
+            extra["rbw_prefill_d128"] = bench_order_prefill(api, rank, world, api.LA_MODE_READ_BEFORE_WRITE,
+                                                            wname="prefill128")
+        if "nc128" in wanted:
+            extra["noncausal_prefill_d128"] = bench_order_prefill(api, rank, world, api.LA_MODE_NONCAUSAL,
+                                                                  wname="prefill128")
         if "backward" in wanted:
             extra["backward"] = bench_backward(api, rank, world)
         e_steps = min(max(args.steps // 4, 20), 200)  # at least 20 steps whatever --steps is

@@ -216,10 +216,19 @@ size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv, l
     return 0;
   if (decay && mode == LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 64 && dv == 64 && N > 0)
     return la::prefill_decay64_workspace_bytes(B, H, N);
-  if (!decay && mode != LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 64 && dv == 64 &&
-      la::prefill_prefix64_chosen(B, H, N))  // the tensor-core form, or the CUDA-core one if it cannot run
-    return std::max(la::prefill_prefix64_workspace_bytes(B, H, N),
-                    la::prefill_simt_workspace_bytes(B, H, N, dk, dv));
+  // no decay, another read order, bf16 at dk = dv = 64 or 128: the tensor-core
+  // form, or the CUDA-core one if it cannot run
+  if (!decay && mode != LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == dv && (dk == 64 || dk == 128) &&
+      N > 0) {
+    size_t tc = 0;
+    if (dk == 64 && la::prefill_prefix64_chosen(B, H, N))
+      tc = la::prefill_prefix64_workspace_bytes(B, H, N);
+    else if (mode == LA_MODE_READ_BEFORE_WRITE)
+      tc = sizeof(la::WsHeader) + la::prefill_tc_workspace_bytes(B, H, N, dk, 128);
+    else
+      tc = la::prefill_nc_workspace_bytes(B, H, N, dk);
+    return std::max(tc, la::prefill_simt_workspace_bytes(B, H, N, dk, dv));
+  }
   return la::prefill_simt_workspace_bytes(B, H, N, dk, dv);
 }
 
@@ -284,15 +293,29 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   // bf16 at dk = dv = 64, write then read with a decay: tensor cores
   if (alpha && mode == LA_MODE_CAUSAL && la::prefill_decay64_supported(a))
     return from_cuda(la::launch_prefill_decay64(a, alpha, stream));
-  // bf16 at dk = dv = 64, no decay, with a workspace: read before write in
-  // the two tensor-core launches of the prefill with a strict mask
+  // bf16 at dk = dv = 64 or 128, no decay, with a workspace: the tensor cores
   PrefillArgs tc = a;
   tc.chunk = 128;  // the tensor-core chunk
-  const bool tc64 = !alpha && dk == 64 && la::prefill_tc_supported(tc) && la::prefill_prefix64_chosen(B, H, N) &&
-                    workspace && ws_bytes >= la::prefill_prefix64_workspace_bytes(B, H, N);
-  if (tc64 && mode == LA_MODE_READ_BEFORE_WRITE) return from_cuda(la::launch_prefill_rbw64(a, stream));
-  // non-causal: the piece totals, then every query reads its head's final state
-  if (tc64 && mode == LA_MODE_NONCAUSAL) return from_cuda(la::launch_prefill_nc64(a, stream));
+  if (!alpha && mode != LA_MODE_CAUSAL && workspace && la::prefill_tc_supported(tc)) {
+    // d = 64, at most 2048 chunks: the prefill's two launches, read before
+    // write with a strict mask; non-causal from their piece totals
+    if (dk == 64 && la::prefill_prefix64_chosen(B, H, N) &&
+        ws_bytes >= la::prefill_prefix64_workspace_bytes(B, H, N))
+      return from_cuda(mode == LA_MODE_READ_BEFORE_WRITE ? la::launch_prefill_rbw64(a, stream)
+                                                         : la::launch_prefill_nc64(a, stream));
+    // otherwise the three-launch prefill of that width with a strict mask, or
+    // its aggregate launch and the reads of the final state
+    if (mode == LA_MODE_READ_BEFORE_WRITE &&
+        ws_bytes >= sizeof(la::WsHeader) + la::prefill_tc_workspace_bytes(B, H, N, dk, 128) &&
+        !(dk == 64 && la::prefill_prefix64_chosen(B, H, N))) {
+      tc.strict = true;
+      const cudaError_t e = la::library_status_word(&tc.status);
+      if (e != cudaSuccess) return from_cuda(e);
+      return from_cuda(dk == 64 ? la::launch_prefill_chunked64(tc, stream) : la::launch_prefill_chunked128(tc, stream));
+    }
+    if (mode == LA_MODE_NONCAUSAL && ws_bytes >= la::prefill_nc_workspace_bytes(B, H, N, dk))
+      return from_cuda(la::launch_prefill_nc(tc, stream));
+  }
   return from_cuda(la::launch_prefill_variant_simt(a, alpha, (int)mode, stream));
 }
 

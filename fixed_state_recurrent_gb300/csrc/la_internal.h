@@ -41,6 +41,7 @@ struct PrefillArgs {
   void* workspace;
   size_t ws_bytes;
   unsigned* status;  // where the tensor-core kernels record errors; NULL = the workspace header's word
+  bool strict;       // read before write: token t reads the state before its own write (keys s < t)
 };
 
 // la_prefill's argument checks, path choice and launches, with the status
@@ -143,10 +144,23 @@ cudaError_t launch_prefill_rbw64(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefix64_totals(const PrefillArgs& a, const Prefix64Buffers& b, cudaStream_t stream);
 // Non-causal order (la_prefill_variant's LA_MODE_NONCAUSAL) at bf16,
 // dk = dv = 64, for the calls prefill_prefix64_chosen takes: the piece totals,
-// then every query reads its head's final state (prefill_noncausal64.cu).
+// then every query reads its head's final state (prefill_noncausal.cu).
 // a.workspace of at least prefill_prefix64_workspace_bytes (no header);
 // bounded-wait failures go to the library status word.
 cudaError_t launch_prefill_nc64(const PrefillArgs& a, cudaStream_t stream);
+// The same order at bf16, dk = dv = 64 or 128, for calls of any length: the
+// totals from the aggregate kernel of the three-launch prefill, then the
+// reads.  a.workspace of at least prefill_nc_workspace_bytes (no header);
+// bounded-wait failures go to the library status word.
+size_t prefill_nc_workspace_bytes(int B, int H, int N, int d);
+cudaError_t launch_prefill_nc(const PrefillArgs& a, cudaStream_t stream);
+// The aggregate launch of the three-launch prefill alone: each piece's total
+// (without S0) into agg, in slots of make_split(B H, N, SMs); bounded-wait
+// failures go to `status`.  A programmatic dependent of what precedes it.
+size_t aggregate64_totals_bytes(int B, int H, int N);
+cudaError_t launch_aggregate64_totals(const PrefillArgs& a, float* agg, unsigned* status, cudaStream_t stream);
+size_t aggregate128_totals_bytes(int B, int H, int N);
+cudaError_t launch_aggregate128_totals(const PrefillArgs& a, float* agg, unsigned* status, cudaStream_t stream);
 // The decayed write-then-read form (alpha: [B][H][N]) in the same two launches,
 // for the calls prefill_prefix64_chosen takes: a.workspace of at least
 // prefill_prefix64_decay_workspace_bytes (no header); bounded-wait failures go

@@ -429,6 +429,9 @@ static_assert(sizeof(Bars) <= 512, "barrier area");
 // once per state advance), and single buffers (A, O, phi(Q), the snapshot, the
 // Q slot) are handed round in chunk order, so no waiter can fall two phases
 // behind: each completion needs the waiter of the one before to have passed.
+// STRICT: read before write (token t reads the state before its own write, so
+// the mask keeps keys s < t; the state handed between chunks is the same).
+template <bool STRICT>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -660,8 +663,9 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             } else {
 #pragma unroll
               for (int t = 0; t < 16; ++t)
-                w[t] = pack_bf16x2(2 * t <= lane ? __uint_as_float(r[2 * t]) : 0.f,
-                                   2 * t + 1 <= lane ? __uint_as_float(r[2 * t + 1]) : 0.f);
+                w[t] = pack_bf16x2((STRICT ? 2 * t < lane : 2 * t <= lane) ? __uint_as_float(r[2 * t]) : 0.f,
+                                   (STRICT ? 2 * t + 1 < lane : 2 * t + 1 <= lane) ? __uint_as_float(r[2 * t + 1])
+                                                                                  : 0.f);
             }
           }
           tmem_st16(base + 16 * q4, w);
@@ -873,9 +877,9 @@ cudaError_t launch_prefill_chunked128(const PrefillArgs& a, cudaStream_t stream)
 
   cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)k1::SMEM);
+  auto* const out = a.strict ? k3::output_kernel<true> : k3::output_kernel<false>;
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k3::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)k3::SMEM);
+    e = cudaFuncSetAttribute(out, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k3::SMEM);
   if (e != cudaSuccess) return e;
   // All three launches are programmatic dependents of what precedes them on
   // the stream: their blocks may start while the kernel before them runs, and
@@ -900,7 +904,43 @@ cudaError_t launch_prefill_chunked128(const PrefillArgs& a, cudaStream_t stream)
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k3::kWarps);
   cfg.dynamicSmemBytes = k3::SMEM;
-  return cudaLaunchKernelEx(&cfg, k3::output_kernel, mq, mk, mv, mo, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, out, mq, mk, mv, mo, p, mbar_ns);
+}
+
+size_t aggregate128_totals_bytes(int B, int H, int N) {
+  const Split s = make_split(B * H, N, sm_count());
+  return (size_t)s.BH * s.MPH * SZ * sizeof(float);
+}
+
+cudaError_t launch_aggregate128_totals(const PrefillArgs& a, float* agg, unsigned* status,
+                                       cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  CUtensorMap mk, mv;
+  if (!make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C))
+    return cudaErrorInvalidValue;
+  Params p = {};
+  p.sp = make_split(BH, a.N, sms);
+  p.eps = a.eps;
+  p.status = status;
+  p.agg = agg;
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)k1::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * k1::kWarps);
+  cfg.dynamicSmemBytes = k1::SMEM;
+  return cudaLaunchKernelEx(&cfg, k1::aggregate_kernel, mk, mv, p, mbar_ns);
 }
 
 }  // namespace la

@@ -573,7 +573,9 @@ __device__ __forceinline__ uint8_t* stage_ptr(uint8_t* smem, uint32_t s) { retur
 // two later products; the state warps scale the running state by gamma_C of
 // the next chunk before its advance, and after the last advance store S_N,
 // z_N.  All factors are at most 1 for alpha <= 1.
-template <bool DECAY>
+// STRICT (without DECAY): read before write, token t reads the state before
+// its own write, so the mask keeps keys s < t.
+template <bool DECAY, bool STRICT = false>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -831,7 +833,8 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                   a0 *= exp2_ftz(gt - g[32 * q4 + 2 * t]);
                   a1 *= exp2_ftz(gt - g[32 * q4 + 2 * t + 1]);
                 }
-                w[t] = pack_bf16x2(2 * t <= lane ? a0 : 0.f, 2 * t + 1 <= lane ? a1 : 0.f);
+                w[t] = pack_bf16x2((STRICT ? 2 * t < lane : 2 * t <= lane) ? a0 : 0.f,
+                                   (STRICT ? 2 * t + 1 < lane : 2 * t + 1 <= lane) ? a1 : 0.f);
               }
             }
           }
@@ -1134,9 +1137,9 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
 
   cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)k1::SMEM);
+  auto* const out = a.strict ? k3::output_kernel<false, true> : k3::output_kernel<false, false>;
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k3::output_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)k3::SMEM);
+    e = cudaFuncSetAttribute(out, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k3::SMEM);
   if (e != cudaSuccess) return e;
   // All three launches are programmatic dependents of what precedes them on
   // the stream: their blocks may start while the kernel before them runs, and
@@ -1161,7 +1164,43 @@ cudaError_t launch_prefill_chunked64(const PrefillArgs& a, cudaStream_t stream) 
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k3::kWarps);
   cfg.dynamicSmemBytes = k3::SMEM;
-  return cudaLaunchKernelEx(&cfg, k3::output_kernel<false>, mq, mk, mv, mo, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, out, mq, mk, mv, mo, p, mbar_ns);
+}
+
+size_t aggregate64_totals_bytes(int B, int H, int N) {
+  const Split s = make_split(B * H, N, sm_count());
+  return (size_t)s.BH * s.MPH * SZ * sizeof(float);
+}
+
+cudaError_t launch_aggregate64_totals(const PrefillArgs& a, float* agg, unsigned* status,
+                                      cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  CUtensorMap mk, mv;
+  if (!make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C))
+    return cudaErrorInvalidValue;
+  Params3 p = {};
+  p.sp = make_split(BH, a.N, sms);
+  p.eps = a.eps;
+  p.status = status;
+  p.agg = agg;
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)k1::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * k1::kWarps);
+  cfg.dynamicSmemBytes = k1::SMEM;
+  return cudaLaunchKernelEx(&cfg, k1::aggregate_kernel<false>, mk, mv, p, mbar_ns);
 }
 
 // the decayed form's slots: agg and E, then one decay factor per piece slot

@@ -16,7 +16,11 @@
 // totals and entry states move as 16-byte loads and stores, every piece's load
 // in flight at once.  S0 and S_N are stored [i][j] (the transpose of a slot's
 // rows); a block's share of them goes through shared memory so that their
-// global accesses are 16-byte runs too.
+// global accesses are 16-byte runs too.  A block reads its share of S0 before
+// it writes the same share of S_N, so S_N may be S0 (in place).
+//
+// Optionally the fold also writes each head's final state as the bf16
+// operand tile of a product phi(Q) [S_N | z_N]^T (StateTile below).
 #pragma once
 
 #include "prefill_tc_common.cuh"
@@ -26,6 +30,42 @@ namespace tcp {
 
 constexpr int kScanThreads = 256;
 
+// A state as the K-major bf16 B operand of an M = 128 product over N_S = D + 16
+// columns: D / 64 atoms (K = 64 each) of N_S rows of 128 swizzled bytes; row
+// j < D holds column j of S (a slot's S^T row j), row D bf16(z), row D + 1 the
+// rest of z (z - bf16(z), as bf16), the rows after that zero.
+template <int D>
+struct StateTile {
+  static constexpr int NS = D + 16;
+  static constexpr uint32_t XA = NS * 128;          // one atom
+  static constexpr uint32_t BYTES = (D / 64) * XA;  // the tile
+};
+
+// Four consecutive K positions (col .. col + 3) of tile row `row`.
+template <int D>
+__device__ __forceinline__ void state_tile_put4(uint8_t* tile, int row, int col, uint2 v) {
+  const int c = col % 64;
+  *reinterpret_cast<uint2*>(tile + (col / 64) * StateTile<D>::XA + tc::sw128_offset(row, c / 8) + (c % 8) * 2) = v;
+}
+
+// acc (four floats of slot row `row`, keys col .. col + 3) into the tile: S
+// rows as bf16, the z row as hi and lo rows.
+template <int D>
+__device__ __forceinline__ void state_tile_put(uint8_t* tile, int row, int col, float4 acc) {
+  uint2 hi;
+  hi.x = tc::pack_bf16x2(acc.x, acc.y);
+  hi.y = tc::pack_bf16x2(acc.z, acc.w);
+  if (row < D) {
+    state_tile_put4<D>(tile, row, col, hi);
+  } else {
+    uint2 lo;
+    lo.x = tc::pack_bf16x2(acc.x - __uint_as_float(hi.x << 16), acc.y - __uint_as_float(hi.x & 0xFFFF0000u));
+    lo.y = tc::pack_bf16x2(acc.z - __uint_as_float(hi.y << 16), acc.w - __uint_as_float(hi.y & 0xFFFF0000u));
+    state_tile_put4<D>(tile, D, col, hi);
+    state_tile_put4<D>(tile, D + 1, col, lo);
+  }
+}
+
 // Blocks per head: D * D / (4 kScanThreads) for the S rows, one for z.
 template <int D>
 constexpr int scan_blocks_per_head() {
@@ -33,12 +73,14 @@ constexpr int scan_blocks_per_head() {
 }
 
 // One block of the fold (blockIdx.x = part of the slot, blockIdx.y = head).
-// `gam` (DECAY only) holds one factor per piece slot.
+// `gam` (DECAY only) holds one factor per piece slot.  E (the entry states)
+// and `tiles` (per head a StateTile of S_N, z_N) may be NULL.
 template <int D, bool DECAY>
 __device__ __forceinline__ void scan_fold(const Split& s, const float* __restrict__ agg,
                                           float* __restrict__ E, const float* __restrict__ gam,
                                           const float* __restrict__ S0, const float* __restrict__ z0,
-                                          float* __restrict__ S_N, float* __restrict__ z_N) {
+                                          float* __restrict__ S_N, float* __restrict__ z_N,
+                                          uint8_t* __restrict__ tiles = nullptr) {
   static_assert((D * D) % (4 * kScanThreads) == 0 && D % 4 == 0 && D / 4 <= kScanThreads,
                 "slot split");
   constexpr int SZ = D * D + D;
@@ -93,7 +135,7 @@ __device__ __forceinline__ void scan_fold(const Split& s, const float* __restric
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (w0 + u < npieces) {
-          __stcg(reinterpret_cast<float4*>(E + base + (size_t)(w0 + u) * SZ), acc);
+          if (E) __stcg(reinterpret_cast<float4*>(E + base + (size_t)(w0 + u) * SZ), acc);
           if (DECAY) {
             acc.x = fmaf(g[u], acc.x, a[u].x);
             acc.y = fmaf(g[u], acc.y, a[u].y);
@@ -110,6 +152,16 @@ __device__ __forceinline__ void scan_fold(const Split& s, const float* __restric
     }
   }
 
+  if (tiles) {
+    uint8_t* tile = tiles + (size_t)h * StateTile<D>::BYTES;
+    if (mine) state_tile_put<D>(tile, row, i0, acc);
+    if (zpart) {  // the zero rows D + 2 .. N_S - 1 of every atom
+      constexpr int Z = (StateTile<D>::NS - D - 2) * 8;  // 16-byte units per atom
+      for (int u = t; u < (D / 64) * Z; u += kScanThreads)
+        *reinterpret_cast<uint4*>(tile + (u / Z) * StateTile<D>::XA + (D + 2) * 128 + (u % Z) * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+  }
   if (zpart) {
     if (mine) *reinterpret_cast<float4*>(z_N + (size_t)h * D + i0) = acc;
     return;

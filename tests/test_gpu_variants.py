@@ -173,6 +173,82 @@ def test_noncausal_tc_matches_oracle(la, orc, shape):
     assert la.delta_read_device_status() == 0
 
 
+# the other tensor-core forms of the two read orders: d = 128 (the three-launch
+# prefill with a strict mask; the aggregate launch, then the reads of the final
+# state), and d = 64 past 2048 chunks (the same at d = 64)
+WIDE_SHAPES = [(128, 1, 3, 1), (128, 1, 3, 129), (128, 1, 3, 300), (128, 2, 5, 3000),
+               (128, 3, 40, 333), (128, 1, 2, 20000), (64, 1, 4, 70000)]
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["rbw", "nc"])
+@pytest.mark.parametrize("shape", WIDE_SHAPES, ids=[str(s) for s in WIDE_SHAPES])
+def test_read_orders_tc_wide_match_oracle(la, orc, shape, mode):
+    from fixed_state_recurrent_gb300 import inputs
+    d, B, H, N = shape
+    q, k, v = inputs.la_inputs(B, H, N, d, d, torch.bfloat16, seed=180 + N % 79 + mode)
+    g = torch.Generator().manual_seed(181 + N + d)
+    S0 = torch.randn((B, H, d, d), generator=g) * 0.5
+    z0 = torch.rand((B, H, d), generator=g) * 4 + 0.5
+    la.delta_read_device_status()
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), None, mode, S0=S0.cuda(), z0=z0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), None, mode, S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["rbw", "nc"])
+@pytest.mark.parametrize("d,N", [(128, 3000), (64, 70000)], ids=["d128", "d64_long"])
+def test_read_orders_tc_wide_state_in_place(la, orc, d, N, mode):
+    # S_N, z_N written over S0, z0: every block of a head reads S0 while one of
+    # them writes S_N
+    from fixed_state_recurrent_gb300 import inputs
+    B, H = 1, 4
+    q, k, v = inputs.la_inputs(B, H, N, d, d, torch.bfloat16, seed=185 + mode)
+    g = torch.Generator().manual_seed(186 + d)
+    S0 = torch.randn((B, H, d, d), generator=g) * 0.5
+    z0 = torch.rand((B, H, d), generator=g) * 4 + 0.5
+    Sd, zd = S0.cuda(), z0.cuda()
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), None, mode, S0=Sd, z0=zd,
+                                 S_N=Sd, z_N=zd)
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), None, mode, S0=f64(S0), z0=f64(z0))
+    assert S.data_ptr() == Sd.data_ptr() and z.data_ptr() == zd.data_ptr()
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+
+
+@pytest.mark.parametrize("d,N", [(64, 1000), (128, 1000)], ids=["d64", "d128"])
+def test_noncausal_tc_bounded_wait_reports_timeout(la, orc, monkeypatch, d, N):
+    # the test hook makes the reads' first product wait on an mbarrier that
+    # nothing completes (2 ms limit): the launch finishes, the library status
+    # word says LA_ERR_TIMEOUT, reading clears it, and the next call is right
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 2, N, d, d, torch.bfloat16, seed=188)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    la.delta_read_device_status()
+    monkeypatch.setenv("LA_TEST_FORCE_WAIT", "1")
+    monkeypatch.setenv("LA_MBAR_TIMEOUT_NS", "2000000")
+    la.prefill_variant(qd, kd, vd, None, la.LA_MODE_NONCAUSAL)
+    assert la.delta_read_device_status() == 4  # LA_ERR_TIMEOUT
+    assert la.delta_read_device_status() == 0
+    monkeypatch.delenv("LA_TEST_FORCE_WAIT")
+    monkeypatch.delenv("LA_MBAR_TIMEOUT_NS")
+    o, S, z = la.prefill_variant(qd, kd, vd, None, la.LA_MODE_NONCAUSAL)
+    assert la.delta_read_device_status() == 0
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), None, 2)
+    assert relmax(f64(o), ro) <= TOL_BF16
+
+
+def test_read_before_write_tc_wide_first_read_is_zero(la):
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(2, 3, 300, 128, 128, torch.bfloat16, seed=187)
+    o, _, _ = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), None, la.LA_MODE_READ_BEFORE_WRITE)
+    assert torch.count_nonzero(o[:, :, 0]) == 0
+    assert torch.count_nonzero(o[:, :, 1]) > 0
+
+
 def test_noncausal_tc_queries_read_one_state(la):
     # every query of a head reads the same state: two equal queries far apart in
     # the sequence (other chunks, other blocks) give the same output
