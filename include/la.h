@@ -127,13 +127,14 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  * the outputs, each block folding its entry state from the earlier totals),
  * for larger ones three (decayed piece totals, the chained scan
  * E' = Gamma E + R, then the outputs); with NULL, one block per head.
- * LA_BF16 at dk = dv = 64 without a decay, with a workspace, for calls of at
- * most 2048 chunks of 128 tokens, also runs on the tensor cores:
- * LA_MODE_READ_BEFORE_WRITE as la_prefill's two launches with a strict mask
- * inside each chunk; LA_MODE_NONCAUSAL as la_prefill's first launch (the
- * totals of the heads' pieces), then every query reads its head's final state
- * (one product per chunk against a bf16 copy of it, z as hi + lo).  A bounded
- * wait of those kernels that gives up is reported by
+ * LA_BF16 at dk = dv = 64 or 128 without a decay, with a workspace, also
+ * runs on the tensor cores: LA_MODE_READ_BEFORE_WRITE as la_prefill's
+ * launches with a strict mask inside each chunk; LA_MODE_NONCAUSAL as the
+ * totals of the heads' pieces (la_prefill's first launch at dk = 64 for calls
+ * of at most 2048 chunks of 128 tokens, else its aggregate launch followed by
+ * one fold per head into S_N, z_N), then every query reads its head's final
+ * state (one product per chunk against a bf16 copy of it, z as hi + lo).  A
+ * bounded wait of those kernels that gives up is reported by
  * delta_read_device_status.  Everything else runs on the CUDA cores in fp32,
  * for LA_F32 and LA_BF16 inputs and any dk, dv <= 128: with a workspace of
  * la_prefill_variant_workspace_bytes, each head's sequence in up to 64
