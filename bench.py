@@ -59,7 +59,8 @@ def _args():
                    help="headline workload only (no long/decode/delta/e2e/cpu)")
     p.add_argument("--only", default="",
                    help="comma list of extra workloads to run "
-                        "(long,decode,delta,pr1,gated,decay,rbw,nc,backward,prefill128,rbw128,nc128)")
+                        "(long,decode,delta,pr1,gated,decay,rbw,nc,backward,prefill128,rbw128,nc128,"
+                        "decay128)")
     p.add_argument("--profile-backward", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain la_prefill_backward calls and exit (for ncu)")
     p.add_argument("--profile-decay", type=int, default=0, metavar="CALLS",
@@ -518,12 +519,13 @@ def bench_gated_delta(api, rank, world, reps=3):
             "fp32_tflops": 4.0 * w.dk * w.dv * tokens / (ms * 1e-3) / 1e12}
 
 
-def bench_decay_prefill(api, rank, world, reps=12, sets=4):
+def bench_decay_prefill(api, rank, world, reps=12, sets=4, wname="prefill"):
     """la_prefill_variant, write-then-read with a per-token decay, on the
-    headline prefill shape (tensor cores, the heads split over the SMs with a
-    workspace), over `sets` rotating input/output sets (~350 MB > L2)."""
+    headline prefill shape (wname "prefill") or its d = 128 twin
+    ("prefill128"), on the tensor cores (the heads split over the SMs with a
+    workspace), over `sets` rotating input/output sets (> L2)."""
     import torch
-    w = inputs_mod().WORKLOADS["prefill"]
+    w = inputs_mod().WORKLOADS[wname]
     dev = torch.device("cuda")
     bufs = []
     for r in range(sets):
@@ -546,11 +548,11 @@ def bench_decay_prefill(api, rank, world, reps=12, sets=4):
     _, per = _timed(fn, reps, stream, world)
     ms_calls = statistics.median(per)
     ms = _graph_ms(fn, 4 * sets, stream, world)
-    # algorithmic bytes: q, k, v in, o out (640 B/token), alpha (4 B/token), final state
-    b = (PREFILL_BYTES_PER_TOKEN + 4) * w.tokens + w.B * w.H * (w.dk * w.dv + w.dk) * 4
+    # algorithmic bytes: q, k, v bf16 in, o fp32 out, alpha (4 B/token), final state
+    b = (2 * (w.dk + w.dk + w.dv) + 4 * w.dv + 4) * w.tokens + w.B * w.H * (w.dk * w.dv + w.dk) * 4
     hbm_peak, _, kind = _peaks()
-    return {"workload": "decayed prefill: B=4 H=8 N=4096 dk=dv=64 bf16, alpha ~ U(0.9, 1), "
-                        "write then read", "ms_per_call": ms,
+    return {"workload": f"decayed prefill: B={w.B} H={w.H} N={w.N} dk=dv={w.dk} bf16, "
+                        "alpha ~ U(0.9, 1), write then read", "ms_per_call": ms,
             "ms_per_python_call": ms_calls,
             "timing": f"{4 * sets} calls in one CUDA graph, replayed (device time per call); "
                       "ms_per_python_call: median of back-to-back calls from Python",
@@ -839,7 +841,7 @@ def main():
     e2e = None
     wanted = set(x for x in args.only.split(",") if x) or {"long", "decode", "delta", "pr1",
                                                              "gated", "decay", "rbw", "nc", "backward",
-                                                             "prefill128", "rbw128", "nc128"}
+                                                             "prefill128", "rbw128", "nc128", "decay128"}
     if not args.no_extra:
         if "long" in wanted:
             extra["long"] = bench_simple_prefill(api, "long", rank, world)
@@ -855,6 +857,8 @@ def main():
             extra["gated_delta"] = bench_gated_delta(api, rank, world)
         if "decay" in wanted:
             extra["decay_prefill"] = bench_decay_prefill(api, rank, world)
+        if "decay128" in wanted:
+            extra["decay_prefill_d128"] = bench_decay_prefill(api, rank, world, wname="prefill128")
         if "rbw" in wanted:
             extra["rbw_prefill"] = bench_order_prefill(api, rank, world, api.LA_MODE_READ_BEFORE_WRITE)
         if "nc" in wanted:

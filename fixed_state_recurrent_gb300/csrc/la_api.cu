@@ -216,6 +216,9 @@ size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv, l
     return 0;
   if (decay && mode == LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 64 && dv == 64 && N > 0)
     return la::prefill_decay64_workspace_bytes(B, H, N);
+  if (decay && mode == LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 128 && dv == 128 && N > 0)
+    return std::max(la::prefill_decay128_workspace_bytes(B, H, N),
+                    la::prefill_simt_workspace_bytes(B, H, N, dk, dv));
   // no decay, another read order, bf16 at dk = dv = 64 or 128: the tensor-core
   // form, or the CUDA-core one if it cannot run
   if (!decay && mode != LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == dv && (dk == 64 || dk == 128) &&
@@ -296,6 +299,11 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   // bf16 at dk = dv = 64 or 128, no decay, with a workspace: the tensor cores
   PrefillArgs tc = a;
   tc.chunk = 128;  // the tensor-core chunk
+  // bf16 at dk = dv = 128, write then read with a decay, with a workspace: the
+  // three-launch tensor-core form with decay weights
+  if (alpha && mode == LA_MODE_CAUSAL && dk == 128 && workspace && la::prefill_tc_supported(tc) &&
+      ws_bytes >= la::prefill_decay128_workspace_bytes(B, H, N))
+    return from_cuda(la::launch_prefill_decay128(a, alpha, stream));
   if (!alpha && mode != LA_MODE_CAUSAL && workspace && la::prefill_tc_supported(tc)) {
     // d = 64, at most 2048 chunks: the prefill's two launches, read before
     // write with a strict mask; non-causal from their piece totals

@@ -160,6 +160,13 @@ cudaError_t launch_prefill_nc(const PrefillArgs& a, cudaStream_t stream);
 size_t aggregate64_totals_bytes(int B, int H, int N);
 cudaError_t launch_aggregate64_totals(const PrefillArgs& a, float* agg, unsigned* status, cudaStream_t stream);
 size_t aggregate128_totals_bytes(int B, int H, int N);
+// The decayed write-then-read form at bf16, dk = dv = 128 (alpha: [B][H][N]):
+// the three launches of prefill_chunked128.cu with decay weights (decayed
+// piece totals and decays, the scan E' = Gamma E + R, the outputs).
+// a.workspace of at least prefill_decay128_workspace_bytes (no header);
+// bounded-wait failures go to the library status word.
+size_t prefill_decay128_workspace_bytes(int B, int H, int N);
+cudaError_t launch_prefill_decay128(const PrefillArgs& a, const float* alpha, cudaStream_t stream);
 cudaError_t launch_aggregate128_totals(const PrefillArgs& a, float* agg, unsigned* status, cudaStream_t stream);
 // The decayed write-then-read form (alpha: [B][H][N]) in the same two launches,
 // for the calls prefill_prefix64_chosen takes: a.workspace of at least

@@ -30,6 +30,7 @@
 //      phi(Q) phi(K)^T, P = causal mask (bf16, written back into TMEM),
 //      [num | den] = phi(Q) [S | z_hi | z_lo] + P [V | 1], o = num / (den + eps)
 //      stored through TMA.
+#include "prefill_decay.cuh"
 #include "prefill_scan.cuh"
 
 namespace la {
@@ -63,6 +64,8 @@ struct Params {
   unsigned* status;      // sticky error bits (the workspace header's)
   float* agg;            // [BH * MPH][SZ] piece totals, S^T rows then z
   float* E;              // [BH * MPH][SZ] entry states, same layout
+  const float* alpha;    // decayed form: [BH][N] per-token decay of the state
+  float* gam;            // decayed form: [BH * MPH] the decay over each piece
   int force_wait;        // test hook: K3 waits once on a barrier that nothing completes
 };
 
@@ -203,9 +206,17 @@ struct Bars {
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
+  float part[4];       // decayed form: the phi warps' partial sums of log2 alpha
 };
 static_assert(sizeof(Bars) <= 256, "barrier area");
 
+// DECAY: the piece total with each token weighted by the decay from it to the
+// piece's end, R = sum_t 2^(G_end - G_t) [v_t | 1]^T phi(k_t) (G: running sum
+// of log2 alpha over the piece), so that the scan chains pieces as
+// E' = Gamma E + R with Gamma = 2^G_end (stored per piece slot).  The phi
+// warps first sum log2 alpha over the piece, then scale each phi(K) row by its
+// weight (at most 1) before the products read it; the run is walked forwards.
+template <bool DECAY>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const Params p, const unsigned long long mbar_ns) {
@@ -233,10 +244,13 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   // The run is walked backwards (last piece, last chunk first): the K and V it
   // touches last are those of the run's first chunks, which the output kernel
   // reads first, so they are still in L2.  A piece's total does not depend on
-  // the order.
-  const int npieces = run.count(p.sp);
-  auto walk = [&](int i, Piece* pc) { return i < npieces && run.piece(p.sp, npieces - 1 - i, pc); };
-  auto chunk_of = [&](const Piece& pc, int c) { return pc.nch - 1 - c; };
+  // the order.  (The decayed form walks forwards, the order of its weights.)
+  const int npieces = DECAY ? 0 : run.count(p.sp);
+  auto walk = [&](int i, Piece* pc) {
+    if (DECAY) return run.piece(p.sp, i, pc);
+    return i < npieces && run.piece(p.sp, npieces - 1 - i, pc);
+  };
+  auto chunk_of = [&](const Piece& pc, int c) { return DECAY ? c : pc.nch - 1 - c; };
   auto load_stage = [&](uint32_t s, int tok, int h) {
     uint8_t* st = smem + s * STAGE;
     mbar_arrive_expect_tx(&B->full[s], 2 * TILE);
@@ -315,21 +329,74 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
     __syncwarp();
   } else if (warp < 6) {  // ---- phi on K (one tile row per thread, a quarter row per iteration)
-    const int r = threadIdx.x - 64;
+    const int r = threadIdx.x - 64, w = r / 32;
     uint32_t sj = 0;
     Piece pc;
-    for (int i = 0; walk(i, &pc); ++i)
+    // decayed form: the four warps' total of v (both named barriers run on
+    // every call)
+    auto sum4 = [&](float v) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+      if (lane == 0) B->part[w] = v;
+      named_bar_sync(2, 128);
+      const float tot = (B->part[0] + B->part[1]) + (B->part[2] + B->part[3]);
+      named_bar_sync(2, 128);
+      return tot;
+    };
+    for (int i = 0; walk(i, &pc); ++i) {
+      float rem = 0.f;  // decayed form: log2 of the decay from the chunk's start to the piece's end
+      if (DECAY) {
+        const float* al = p.alpha + (size_t)pc.h * p.sp.N;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        int t = pc.tok0 + r;
+        for (; t + 7 * C < pc.tok1; t += 8 * C) {  // eight loads in flight
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] += __log2f(fmaxf(__ldg(al + t + u * C), kAlphaMin));
+        }
+        for (; t < pc.tok1; t += C) acc[0] += __log2f(fmaxf(__ldg(al + t), kAlphaMin));
+        rem = sum4(((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
+        if (r == 0) p.gam[pc.slot] = exp2_ftz(rem);
+      }
       for (int c = 0; c < pc.nch; ++c, ++sj) {
         const uint32_t s = sj % NS;
         const int valid = pc.tok1 - (pc.tok0 + chunk_of(pc, c) * C);
+        // decayed form: the row's weight 2^(rem - g_r), g_r the inclusive sum of
+        // log2 alpha over the chunk up to row r, found before the tile is waited for
+        float wt = 1.f;
+        if (DECAY) {
+          float la = r < valid ? __log2f(fmaxf(__ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 +
+                                                    chunk_of(pc, c) * C + r), kAlphaMin))
+                               : 0.f;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xFFFFFFFFu, la, off);
+            if (lane >= off) la += y;
+          }
+          if (lane == 31) B->part[w] = la;
+          named_bar_sync(2, 128);
+          float g = la, tot = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float pq = B->part[q];
+            if (q < w) g += pq;
+            tot += pq;
+          }
+          named_bar_sync(2, 128);
+          wt = exp2_ftz(rem - g);
+          rem -= tot;
+        }
         if (!wait_w(x, &B->full[s], (sj / NS) & 1)) continue;
         uint8_t* st = smem + s * STAGE;
 #pragma unroll 1
-        for (int m = 0; m < 4; ++m) phi_row<4>(st + (m / 2) * BLK, r, 4 * (m % 2), valid);
+        for (int m = 0; m < 4; ++m) {
+          if (DECAY) phi_scale_row<4>(st + (m / 2) * BLK, r, 4 * (m % 2), valid, wt);
+          else phi_row<4>(st + (m / 2) * BLK, r, 4 * (m % 2), valid);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&B->xf[s]);
       }
+    }
   } else {  // ---- epilogue: buffer b -> workspace slot (S^T rows, then z)
     const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 192;
     const uint32_t tl = x.tmem + ((uint32_t)(32 * quad) << 16);
@@ -370,10 +437,12 @@ aggregate_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
 namespace k2 {
 
+// DECAY: each piece first decays what came before it, E' = Gamma E + R.
+template <bool DECAY>
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
   pdl_launch_dependents();  // the output kernel may be scheduled now
   pdl_wait();               // the totals of the aggregate kernel are complete
-  scan_fold<D, false>(p.sp, p.agg, p.E, nullptr, p.S0, p.z0, p.S_N, p.z_N);
+  scan_fold<D, DECAY>(p.sp, p.agg, p.E, p.gam, p.S0, p.z0, p.S_N, p.z_N);
 }
 
 }  // namespace k2
@@ -390,7 +459,13 @@ constexpr uint32_t OFF_SNAP = OFF_Q + TILE;   // the state snapshot
 constexpr uint32_t OFF_ONES = OFF_SNAP + SNAP;
 constexpr uint32_t OFF_OUT = OFF_ONES + ONES;  // output staging: one [128 x 32] fp32 box
 constexpr uint32_t OFF_BAR = OFF_OUT + BLK;
-constexpr uint32_t SMEM = OFF_BAR + 512 + 1024;
+// decayed form, per stage: g_t (the inclusive sums of log2 alpha over the
+// chunk), the four warp totals, then the key factors 2^(g_e - g_s) (g_e the
+// sum at the last key of s's 32-key block)
+constexpr uint32_t OFF_G = OFF_BAR + 512;
+constexpr int GKF = C + 4;
+constexpr int GSTRIDE = 2 * C + 4;
+constexpr uint32_t SMEM = OFF_G + NS * GSTRIDE * 4 + 1024;
 static_assert(SMEM <= 227 * 1024, "shared memory per block");
 static_assert(OFF_SNAP % 1024 == 0 && OFF_ONES % 1024 == 0 && OFF_OUT % 1024 == 0, "atom alignment");
 // 0 K/V producer, 1 MMA, 2-5 phi (K in place, then Q into TMEM), 6-9 P,
@@ -422,8 +497,13 @@ struct Bars {
   uint32_t tmem_slot;
   int abort;
   unsigned epieces;  // entry states stored in TMEM so far, times 4 (state warps -> state chain)
+  unsigned pdone[4];  // decayed form: chunks whose K rows P warp q has rescaled (P warps -> state chain)
 };
 static_assert(sizeof(Bars) <= 512, "barrier area");
+
+__device__ __forceinline__ float* gsums(uint8_t* smem, uint32_t s) {
+  return reinterpret_cast<float*>(smem + OFF_G) + s * GSTRIDE;
+}
 
 // Every barrier of the chunk loop completes once per chunk (sacc and tsread
 // once per state advance), and single buffers (A, O, phi(Q), the snapshot, the
@@ -431,7 +511,17 @@ static_assert(sizeof(Bars) <= 512, "barrier area");
 // behind: each completion needs the waiter of the one before to have passed.
 // STRICT: read before write (token t reads the state before its own write, so
 // the mask keeps keys s < t; the state handed between chunks is the same).
-template <bool STRICT>
+// DECAY: S_t = alpha_t S_{t-1} + phi(k_t) v_t^T, z likewise.  With g_t the
+// inclusive sum of log2 alpha over the chunk up to t and gamma_t = 2^g_t, the
+// chunk's entry state reaches token t as gamma_t S and its own tokens s <= t
+// with weight 2^(g_t - g_s); after the chunk S <- gamma_C S + sum_s
+// 2^(g_C - g_s) phi(k_s) [v_s | 1]^T.  The phi warps scan log2 alpha; the P
+// warps weight each kept score by 2^(g_t - g_s) and, once the scores have read
+// them, rescale phi(Q) in TMEM by gamma_t (for phi(Q) [S | z], issued after
+// P) and the chunk's phi(K) rows by 2^(g_C - g_s) (for the advance); the state
+// warps write the running state back as gamma_C S (gamma_C of the next chunk)
+// when they snapshot it.  All factors are at most 1 for alpha <= 1.
+template <bool STRICT, bool DECAY>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -462,6 +552,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(&B->drain2, 1);
     mbar_init(&B->never, 1);
     B->epieces = 0;
+    for (int q = 0; q < 4; ++q) B->pdone[q] = 0;
     B->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -571,7 +662,8 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         sdesc_sw128(kt + (ks / 4) * BLK + (ks % 4) * 32, 16, 1024), ID_S,
                         ks > 0 ? 1u : 0u);
           mma_commit(&B->accS);
-          ok = wait_b(x, &B->sready, g & 1) && (g == 0 || wait_b(x, &B->ofree, (g - 1) & 1));
+          ok = wait_b(x, &B->sready, g & 1) && (g == 0 || wait_b(x, &B->ofree, (g - 1) & 1)) &&
+               (!DECAY || wait_b(x, &B->pready, g & 1));  // decayed: phi(Q) rescaled with P
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -580,7 +672,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         sdesc_sw128(aSnap + (ks / 4) * SNAP_ATOM + (ks % 4) * 32, 16, 1024), ID_QS,
                         ks > 0 ? 1u : 0u);
           mma_commit(&B->qsdone);
-          if (!(ok = wait_b(x, &B->pready, g & 1))) break;
+          if (!DECAY && !(ok = wait_b(x, &B->pready, g & 1))) break;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < C / 16; ++ks) {  // += P [V | 1], P from TMEM
@@ -607,10 +699,36 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int c = 0; c < pc.nch; ++c, ++g) {
         const int valid = pc.tok1 - (pc.tok0 + c * C);
         const uint32_t s = g % NS;
-        if (wait_w(x, &B->full[s], (g / NS) & 1)) {  // the chunk's K tile: phi in place
+        // decayed form: this row's alpha, loaded before the wait for the tiles
+        float av = 1.f;
+        if (DECAY && row < valid) av = __ldg(p.alpha + (size_t)pc.h * p.sp.N + pc.tok0 + c * C + row);
+        const bool got = wait_w(x, &B->full[s], (g / NS) & 1);
+        if (got) {  // the chunk's K tile: phi in place
           uint8_t* kt = smem + s * STAGE;
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) phi_row<4>(kt + (m / 2) * BLK, row, 4 * (m % 2), valid);
+        }
+        if (DECAY) {
+          // g_t: inclusive sums of log2 alpha over the chunk (alpha = 1 past the
+          // end); a warp scan, then the totals of the warps before.  The named
+          // barrier runs whether or not the wait succeeded, so that all four
+          // warps always meet it.
+          float la = 0.f;
+          if (got && row < valid) la = __log2f(fmaxf(av, kAlphaMin));
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xFFFFFFFFu, la, off);
+            if (lane >= off) la += y;
+          }
+          float* gs = gsums(smem, s);
+          // the key factor from the warp's own sums (the earlier warps' totals cancel)
+          gs[GKF + row] = exp2_ftz(__shfl_sync(0xFFFFFFFFu, la, 31) - la);
+          if (lane == 31) gs[C + quad] = la;
+          named_bar_sync(2, 128);
+          for (int w = 0; w < quad; ++w) la += gs[C + w];
+          gs[row] = la;
+        }
+        if (got) {
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B->xf[s]);
@@ -641,11 +759,16 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int c = 0; c < pc.nch; ++c, ++g) {
         if (!wait_w(x, &B->accS, g & 1)) continue;
         tc_fence_after();
+        const float* gs = gsums(smem, g % NS);
+        const float gt = DECAY ? gs[row] : 0.f;
         // this warp's query rows are 32 quad .. +31: key blocks before `quad`
         // are fully visible, block `quad` holds the diagonal (kept), later
         // blocks are zero.  Packed keys 32 q4 .. go to columns 16 q4 ..; block
         // q4 is read completely before its packed columns (in block q4 / 2 <=
-        // q4) are written.
+        // q4) are written.  Decayed form: kept scores are weighted by
+        // 2^(g_t - g_s); for a block before the diagonal that is
+        // 2^(g_t - g_e) 2^(g_e - g_s), g_e the sum at the block's last key (one
+        // exponential per block and row, the key factors from the phi warps).
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t w[16];
@@ -657,24 +780,67 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tmem_ld32(base + 32 * q4, r);
             tmem_ld_wait();
             if (q4 < quad) {
+              float rf = 1.f;
+              const float* ck = gs + GKF + 32 * q4;
+              if (DECAY) rf = exp2_ftz(gt - gs[32 * q4 + 31]);
 #pragma unroll
-              for (int t = 0; t < 16; ++t)
-                w[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
+              for (int t = 0; t < 16; ++t) {
+                float a0 = __uint_as_float(r[2 * t]), a1 = __uint_as_float(r[2 * t + 1]);
+                if (DECAY) {
+                  a0 *= rf * ck[2 * t];
+                  a1 *= rf * ck[2 * t + 1];
+                }
+                w[t] = pack_bf16x2(a0, a1);
+              }
             } else {
 #pragma unroll
-              for (int t = 0; t < 16; ++t)
-                w[t] = pack_bf16x2((STRICT ? 2 * t < lane : 2 * t <= lane) ? __uint_as_float(r[2 * t]) : 0.f,
-                                   (STRICT ? 2 * t + 1 < lane : 2 * t + 1 <= lane) ? __uint_as_float(r[2 * t + 1])
-                                                                                  : 0.f);
+              for (int t = 0; t < 16; ++t) {
+                float a0 = __uint_as_float(r[2 * t]), a1 = __uint_as_float(r[2 * t + 1]);
+                if (DECAY) {
+                  a0 *= exp2_ftz(gt - gs[32 * q4 + 2 * t]);
+                  a1 *= exp2_ftz(gt - gs[32 * q4 + 2 * t + 1]);
+                }
+                w[t] = pack_bf16x2((STRICT ? 2 * t < lane : 2 * t <= lane) ? a0 : 0.f,
+                                   (STRICT ? 2 * t + 1 < lane : 2 * t + 1 <= lane) ? a1 : 0.f);
+              }
             }
           }
           tmem_st16(base + 16 * q4, w);
         }
-        (void)row;
         tmem_st_wait();
+        if (DECAY) {
+          // The scores have read phi(Q) and phi(K): phi(Q) [S | z] takes phi(Q)
+          // times gamma_t (TMEM, packed bf16 pairs), the advance phi(K) rows
+          // times 2^(g_C - g_t) (shared memory).
+          const float gq = exp2_ftz(gt), gk = exp2_ftz(gs[C - 1] - gt);
+          const uint32_t tq = x.tmem + ((uint32_t)(32 * quad) << 16) + TQ;
+#pragma unroll 1
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t r[32];
+            tmem_ld32(tq + 32 * h2, r);
+            tmem_ld_wait();
+            uint32_t w0[16], w1[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              w0[t] = pack_bf16x2(__uint_as_float(r[t] << 16) * gq, __uint_as_float(r[t] & 0xFFFF0000u) * gq);
+              w1[t] = pack_bf16x2(__uint_as_float(r[16 + t] << 16) * gq,
+                                  __uint_as_float(r[16 + t] & 0xFFFF0000u) * gq);
+            }
+            tmem_st16(tq + 32 * h2, w0);
+            tmem_st16(tq + 32 * h2 + 16, w1);
+          }
+          tmem_st_wait();
+          uint8_t* kt = smem + (g % NS) * STAGE;
+          scale_row(kt, row, gk);
+          scale_row(kt + BLK, row, gk);
+          fence_proxy_async_smem();
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&B->pready);
+        if (lane == 0) {
+          mbar_arrive(&B->pready);
+          if (DECAY) red_add_release_cta(&B->pdone[quad], 1u);
+        }
       }
   } else if (warp < 14) {  // ---- state snapshots and output epilogue
     const int quad = warp % 4, row = 32 * quad + lane, et = threadIdx.x - 320;
@@ -689,6 +855,13 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       // once the products of the chunk before have read the snapshot (the
       // previous piece's advances were all waited for below).
       if (g == 0 || wait_w(x, &B->qsdone, (g - 1) & 1)) {
+        // decayed form: the running state enters the first advance as
+        // gamma_C E (gamma_C of the piece's first chunk); the snapshot is E
+        float gC = 1.f;
+        if (DECAY) {
+          wait_w(x, &B->xf[g % NS], (g / NS) & 1);  // the chunk's sums of log2 alpha
+          gC = exp2_ftz(gsums(smem, g % NS)[C - 1]);
+        }
         const float* src = p.E + (size_t)pc.slot * SZ;
 #pragma unroll 1
         for (int grp = 0; grp < 4; ++grp) {
@@ -704,8 +877,8 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           uint32_t w0[16], w1[16];
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
-            w0[t] = v[t];
-            w1[t] = v[16 + t];
+            w0[t] = DECAY ? __float_as_uint(__uint_as_float(v[t]) * gC) : v[t];
+            w1[t] = DECAY ? __float_as_uint(__uint_as_float(v[16 + t]) * gC) : v[16 + t];
           }
           tmem_st16(tl + TS + 32 * grp, w0);
           tmem_st16(tl + TS + 32 * grp + 16, w1);
@@ -715,7 +888,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         uint32_t wz[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) wz[t] = 0u;
-        wz[0] = __float_as_uint(z);
+        wz[0] = __float_as_uint(z * gC);
         tmem_st16(tl + TZ, wz);
         snap_z(snap, row, z);
         tmem_st_wait();
@@ -730,20 +903,42 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
       for (int c = 0; c < pc.nch; ++c, ++g) {
         if (c + 1 < pc.nch) {  // the snapshot of the state after chunk g, for chunk g + 1
-          const bool ok = wait_w(x, &B->sacc, nsa & 1) && wait_w(x, &B->qsdone, g & 1);
+          const bool ok = wait_w(x, &B->sacc, nsa & 1) && wait_w(x, &B->qsdone, g & 1) &&
+                          (!DECAY || wait_w(x, &B->xf[(g + 1) % NS], ((g + 1) / NS) & 1));
           ++nsa;
           if (ok) {
             tc_fence_after();
+            // decayed form: the next advance adds onto gamma_C S, gamma_C of
+            // the next chunk; the snapshot is S
+            const float gC = DECAY ? exp2_ftz(gsums(smem, (g + 1) % NS)[C - 1]) : 1.f;
 #pragma unroll 1
             for (int grp = 0; grp < 4; ++grp) {
               uint32_t v[32];
               tmem_ld32(tl + TS + 32 * grp, v);
               tmem_ld_wait();
+              if (DECAY) {
+                uint32_t w0[16], w1[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                  w0[t] = __float_as_uint(__uint_as_float(v[t]) * gC);
+                  w1[t] = __float_as_uint(__uint_as_float(v[16 + t]) * gC);
+                }
+                tmem_st16(tl + TS + 32 * grp, w0);
+                tmem_st16(tl + TS + 32 * grp + 16, w1);
+              }
               snap_store32(snap, row, grp, v);
             }
             uint32_t zz[2];
             tmem_ld2(tl + TZ, zz);
             tmem_ld_wait();
+            if (DECAY) {
+              uint32_t wz[16];
+#pragma unroll
+              for (int t = 0; t < 16; ++t) wz[t] = 0u;
+              wz[0] = __float_as_uint(__uint_as_float(zz[0]) * gC);
+              tmem_st16(tl + TZ, wz);
+              tmem_st_wait();
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&B->tsread);  // the running state may advance again
@@ -803,6 +998,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!any_adv) {
           mbar_arrive(&B->empty[s]);
           return true;
+        }
+        if (DECAY) {  // phi(K) of chunk j rescaled by all four P warps
+          for (int q = 0; q < 4; ++q)
+            if (!count_reached(x, &B->pdone[q], j + 1)) return false;
         }
         tc_fence_after();
         const uint32_t kt = smem_u32(smem + s * STAGE), vt = kt + TILE;
@@ -875,9 +1074,9 @@ cudaError_t launch_prefill_chunked128(const PrefillArgs& a, cudaStream_t stream)
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
 
-  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)k1::SMEM);
-  auto* const out = a.strict ? k3::output_kernel<true> : k3::output_kernel<false>;
+  auto* const out = a.strict ? k3::output_kernel<true, false> : k3::output_kernel<false, false>;
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(out, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k3::SMEM);
   if (e != cudaSuccess) return e;
@@ -894,17 +1093,80 @@ cudaError_t launch_prefill_chunked128(const PrefillArgs& a, cudaStream_t stream)
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k1::kWarps);
   cfg.dynamicSmemBytes = k1::SMEM;
-  e = cudaLaunchKernelEx(&cfg, k1::aggregate_kernel, mk, mv, p, mbar_ns);
+  e = cudaLaunchKernelEx(&cfg, k1::aggregate_kernel<false>, mk, mv, p, mbar_ns);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(scan_blocks_per_head<D>(), BH);
   cfg.blockDim = dim3(kScanThreads);
   cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, k2::scan_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, k2::scan_kernel<false>, p);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k3::kWarps);
   cfg.dynamicSmemBytes = k3::SMEM;
   return cudaLaunchKernelEx(&cfg, out, mq, mk, mv, mo, p, mbar_ns);
+}
+
+// the decayed form's slots: agg and E, then one decay factor per piece slot
+size_t prefill_decay128_workspace_bytes(int B, int H, int N) {
+  const Split s = make_split(B * H, N, sm_count());
+  const size_t slots = (size_t)s.BH * s.MPH;
+  return (2 * slots * SZ + slots) * sizeof(float);
+}
+
+cudaError_t launch_prefill_decay128(const PrefillArgs& a, const float* alpha, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  if (!a.workspace || a.ws_bytes < prefill_decay128_workspace_bytes(a.B, a.H, a.N)) return cudaErrorInvalidValue;
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, C) ||
+      !make_map(&mo, a.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, BH, 32, C))
+    return cudaErrorInvalidValue;
+  Params p = {};
+  p.sp = make_split(BH, a.N, sms);
+  p.eps = a.eps;
+  p.S0 = a.S0;
+  p.z0 = a.z0;
+  p.S_N = a.S_N;
+  p.z_N = a.z_N;
+  p.alpha = alpha;
+  const size_t slots = (size_t)BH * p.sp.MPH;
+  p.agg = static_cast<float*>(a.workspace);
+  p.E = p.agg + slots * SZ;
+  p.gam = p.E + slots * SZ;
+  cudaError_t e = library_status_word(&p.status);
+  if (e != cudaSuccess) return e;
+  const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
+  p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+  e = cudaFuncSetAttribute(k1::aggregate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k1::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k3::output_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)k3::SMEM);
+  if (e != cudaSuccess) return e;
+  // the three launches, each a programmatic dependent of what precedes it
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * k1::kWarps);
+  cfg.dynamicSmemBytes = k1::SMEM;
+  e = cudaLaunchKernelEx(&cfg, k1::aggregate_kernel<true>, mk, mv, p, mbar_ns);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(scan_blocks_per_head<D>(), BH);
+  cfg.blockDim = dim3(kScanThreads);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, k2::scan_kernel<true>, p);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(p.sp.G);
+  cfg.blockDim = dim3(32 * k3::kWarps);
+  cfg.dynamicSmemBytes = k3::SMEM;
+  return cudaLaunchKernelEx(&cfg, k3::output_kernel<false, true>, mq, mk, mv, mo, p, mbar_ns);
 }
 
 size_t aggregate128_totals_bytes(int B, int H, int N) {
@@ -927,7 +1189,7 @@ cudaError_t launch_aggregate128_totals(const PrefillArgs& a, float* agg, unsigne
   p.status = status;
   p.agg = agg;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
-  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(k1::aggregate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)k1::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute pdl;
@@ -940,7 +1202,7 @@ cudaError_t launch_aggregate128_totals(const PrefillArgs& a, float* agg, unsigne
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k1::kWarps);
   cfg.dynamicSmemBytes = k1::SMEM;
-  return cudaLaunchKernelEx(&cfg, k1::aggregate_kernel, mk, mv, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, k1::aggregate_kernel<false>, mk, mv, p, mbar_ns);
 }
 
 }  // namespace la

@@ -28,6 +28,7 @@
 //      written back into TMEM), [num | den] = P [V | 1] + phi(Q) [S | z] as two
 //      N = 80 products, o = num / (den + eps) stored through TMA.
 // V and phi(K) are read again by K3 (from L2 when the workload fits in it).
+#include "prefill_decay.cuh"
 #include "prefill_scan.cuh"
 
 namespace la {
@@ -38,7 +39,6 @@ using namespace tcp;
 
 constexpr int D = 64;
 constexpr int SZ = D * D + D;                // floats per state slot (R^T rows, then z)
-constexpr float kAlphaMin = 1e-30f;          // a zero decay is taken as this (its log2 stays finite)
 constexpr uint32_t BLK = 16384;              // [128 rows x 128 B] swizzled bf16 tile
 constexpr uint32_t SNAP = 80 * 128;          // K-major [80 x 64]: S^T rows, z hi, z lo, zeros
 
@@ -172,44 +172,6 @@ __device__ __forceinline__ void drain_and_free(const Ctx3& x, int warp, uint32_t
     tc_fence_after();
     tmem_dealloc(x.tmem, ncols);
   }
-}
-
-// Row r of a bf16 [128 x 64] swizzled tile, times f, rounded to bf16 again.
-__device__ __forceinline__ void scale_row(uint8_t* tile, int r, float f) {
-  uint4 v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, i));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t* w = reinterpret_cast<uint32_t*>(&v[i]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      w[j] = pack_bf16x2(__uint_as_float(w[j] << 16) * f, __uint_as_float(w[j] & 0xFFFF0000u) * f);
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(tile + sw128_offset(r, i)) = v[i];
-}
-
-// phi_row followed by scale_row on `nchunk` 16-byte chunks of row r from
-// chunk c0, in one pass (the same two roundings to bf16, one shared-memory
-// round trip).
-template <int NCH>
-__device__ __forceinline__ void phi_scale_row(uint8_t* tile, int r, int c0, int valid, float f) {
-  uint4 v[NCH];
-#pragma unroll
-  for (int i = 0; i < NCH; ++i) v[i] = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, c0 + i));
-  const uint32_t keep = r < valid ? 0xFFFFFFFFu : 0u;
-#pragma unroll
-  for (int i = 0; i < NCH; ++i) {
-    uint32_t* w = reinterpret_cast<uint32_t*>(&v[i]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t y = phi2(w[j]) & keep;
-      w[j] = pack_bf16x2(__uint_as_float(y << 16) * f, __uint_as_float(y & 0xFFFF0000u) * f);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < NCH; ++i) *reinterpret_cast<uint4*>(tile + sw128_offset(r, c0 + i)) = v[i];
 }
 
 // ===========================================================================

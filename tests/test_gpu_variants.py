@@ -376,6 +376,71 @@ def test_decay_prefill_tc_pieces_match_oracle(la, orc, shape, arange):
     assert la.delta_read_device_status() == 0
 
 
+# the decayed form at d = 128 (three launches with decay weights; a workspace)
+DECAY128_SHAPES = [(1, 3, 1), (1, 3, 129), (1, 3, 300), (2, 5, 3000), (3, 40, 333), (1, 2, 20000)]
+
+
+@pytest.mark.parametrize("shape", DECAY128_SHAPES, ids=[str(s) for s in DECAY128_SHAPES])
+@pytest.mark.parametrize("arange", [(0.9, 1.0), (0.3, 1.0), (0.02, 0.5)], ids=["mild", "strong", "severe"])
+def test_decay_prefill_tc_d128_matches_oracle(la, orc, shape, arange):
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N = shape
+    q, k, v = inputs.la_inputs(B, H, N, 128, 128, torch.bfloat16, seed=195 + N % 67)
+    g = torch.Generator().manual_seed(196 + N)
+    lo, hi = arange
+    alpha = lo + (hi - lo) * torch.rand((B, H, N), generator=g)
+    S0 = torch.randn((B, H, 128, 128), generator=g) * 0.5
+    z0 = torch.rand((B, H, 128), generator=g) * 4 + 0.5
+    la.delta_read_device_status()
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), alpha.cuda(), 0,
+                                 S0=S0.cuda(), z0=z0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha), 0, S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
+
+
+def test_decay_prefill_tc_d128_zero_alpha_and_alpha_one(la, orc):
+    # alpha = 0 at chunk edges forgets the state before them; alpha = 1 is
+    # la_prefill's recurrence (through other kernels: within the tolerance)
+    from fixed_state_recurrent_gb300 import inputs
+    N = 520
+    q, k, v = inputs.la_inputs(2, 2, N, 128, 128, torch.bfloat16, seed=197)
+    alpha = torch.full((2, 2, N), 0.97)
+    alpha[:, :, [0, 5, 127, 128, 255, 300, 519]] = 0.0
+    S0 = torch.randn((2, 2, 128, 128), generator=torch.Generator().manual_seed(198))
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, S, z = la.prefill_variant(qd, kd, vd, alpha.cuda(), 0, S0=S0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha), 0, S0=f64(S0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+    a = la.prefill_variant(qd, kd, vd, torch.ones((2, 2, N), device="cuda"), 0)
+    b = la.prefill(qd, kd, vd)
+    for x, y in zip(a, b):
+        assert relmax(f64(x), f64(y)) <= TOL_BF16
+
+
+def test_decay_prefill_tc_d128_bounded_wait_reports_timeout(la, orc, monkeypatch):
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 2, 600, 128, 128, torch.bfloat16, seed=199)
+    alpha = torch.full((1, 2, 600), 0.99, device="cuda")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    la.delta_read_device_status()
+    monkeypatch.setenv("LA_TEST_FORCE_WAIT", "1")
+    monkeypatch.setenv("LA_MBAR_TIMEOUT_NS", "2000000")
+    la.prefill_variant(qd, kd, vd, alpha, 0)
+    assert la.delta_read_device_status() == 4  # LA_ERR_TIMEOUT
+    assert la.delta_read_device_status() == 0
+    monkeypatch.delenv("LA_TEST_FORCE_WAIT")
+    monkeypatch.delenv("LA_MBAR_TIMEOUT_NS")
+    o, S, z = la.prefill_variant(qd, kd, vd, alpha, 0)
+    assert la.delta_read_device_status() == 0
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha.cpu()), 0)
+    assert relmax(f64(o), ro) <= TOL_BF16
+
+
 def test_decay_prefill_tc_zero_alpha_forgets(la, orc):
     # alpha = 0 at some tokens (taken as 1e-30 in the chunk factors): the state
     # before them is forgotten, including right at chunk edges
