@@ -127,6 +127,8 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  * the outputs, each block folding its entry state from the earlier totals),
  * for larger ones three (decayed piece totals, the chained scan
  * E' = Gamma E + R, then the outputs); with NULL, one block per head.
+ * LA_BF16 at dk = dv = 128 with a decay in LA_MODE_CAUSAL and a workspace
+ * runs the same three launches on the tensor cores at that width.
  * LA_BF16 at dk = dv = 64 or 128 without a decay, with a workspace, also
  * runs on the tensor cores: LA_MODE_READ_BEFORE_WRITE as la_prefill's
  * launches with a strict mask inside each chunk; LA_MODE_NONCAUSAL as the
