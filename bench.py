@@ -63,6 +63,9 @@ def _args():
                         "decay128)")
     p.add_argument("--profile-backward", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain la_prefill_backward calls and exit (for ncu)")
+    p.add_argument("--profile-order", type=int, default=0, metavar="MODE",
+                   help="with --profile N: la_prefill_variant calls in read order MODE "
+                        "(1 read before write, 2 non-causal) instead of la_prefill")
     p.add_argument("--profile-decay", type=int, default=0, metavar="CALLS",
                    help="run CALLS plain decayed-prefill calls and exit (for ncu)")
     p.add_argument("--profile-decode", type=int, default=0, metavar="CALLS",
@@ -384,11 +387,12 @@ def profile_decode_calls(api, calls):
     print(f"profiled {calls} decode steps", flush=True)
 
 
-def profile_decay_calls(api, calls, sets=4):
+def profile_decay_calls(api, calls, sets=4, wname="prefill"):
     """`calls` plain decayed-prefill calls (la_prefill_variant, alpha ~ U(0.9, 1))
-    on the headline prefill shape over rotating input sets, for profilers."""
+    on the headline prefill shape (or another prefill workload) over rotating
+    input sets, for profilers."""
     import torch
-    w = inputs_mod().WORKLOADS["prefill"]
+    w = inputs_mod().WORKLOADS[wname]
     dev = torch.device("cuda")
     bufs = []
     for r in range(sets):
@@ -400,6 +404,20 @@ def profile_decay_calls(api, calls, sets=4):
         api.prefill_variant(q, k, v, alpha, 0)
     torch.cuda.synchronize()
     print(f"profiled {calls} decayed prefill calls", flush=True)
+
+
+def profile_order_calls(api, calls, mode, sets=4, wname="prefill"):
+    """`calls` plain la_prefill_variant calls in another read order (no decay)
+    on a prefill workload over rotating input sets, for profilers."""
+    import torch
+    w = inputs_mod().WORKLOADS[wname]
+    dev = torch.device("cuda")
+    bufs = [_device_inputs(w, w.seed + r, dev) for r in range(sets)]
+    for i in range(calls):
+        q, k, v = bufs[i % sets]
+        api.prefill_variant(q, k, v, None, mode)
+    torch.cuda.synchronize()
+    print(f"profiled {calls} read-order {mode} calls", flush=True)
 
 
 def profile_backward_calls(api, calls):
@@ -818,7 +836,7 @@ def main():
         sampler.stop()
         return
     if args.profile_decay:
-        profile_decay_calls(api, args.profile_decay)
+        profile_decay_calls(api, args.profile_decay, wname=args.profile_workload)
         sampler.stop()
         return
     if args.profile_decode:
@@ -827,6 +845,10 @@ def main():
         return
     if args.profile_delta:
         profile_delta_calls(api, args.profile_delta)
+        sampler.stop()
+        return
+    if args.profile and args.profile_order:
+        profile_order_calls(api, args.profile, args.profile_order, wname=args.profile_workload)
         sampler.stop()
         return
     if args.profile:

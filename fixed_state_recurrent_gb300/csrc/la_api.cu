@@ -214,9 +214,11 @@ size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv, l
   if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return 0;
   if (mode != LA_MODE_CAUSAL && mode != LA_MODE_READ_BEFORE_WRITE && mode != LA_MODE_NONCAUSAL)
     return 0;
-  if (decay && mode == LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 64 && dv == 64 && N > 0)
+  // with a decay (write then read, or read before write), bf16 at dk = dv = 64
+  // or 128: the decayed tensor-core forms
+  if (decay && in_dtype == LA_BF16 && dk == 64 && dv == 64 && N > 0)
     return la::prefill_decay64_workspace_bytes(B, H, N);
-  if (decay && mode == LA_MODE_CAUSAL && in_dtype == LA_BF16 && dk == 128 && dv == 128 && N > 0)
+  if (decay && in_dtype == LA_BF16 && dk == 128 && dv == 128 && N > 0)
     return std::max(la::prefill_decay128_workspace_bytes(B, H, N),
                     la::prefill_simt_workspace_bytes(B, H, N, dk, dv));
   // no decay, another read order, bf16 at dk = dv = 64 or 128: the tensor-core
@@ -293,17 +295,23 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   a.chunk = 0;
   a.workspace = workspace;
   a.ws_bytes = workspace ? ws_bytes : 0;
-  // bf16 at dk = dv = 64, write then read with a decay: tensor cores
-  if (alpha && mode == LA_MODE_CAUSAL && la::prefill_decay64_supported(a))
-    return from_cuda(la::launch_prefill_decay64(a, alpha, stream));
+  // bf16 at dk = dv = 64 with a decay: tensor cores (read before write in the
+  // three-launch form with a strict mask, or one block per head)
+  if (alpha && la::prefill_decay64_supported(a)) {
+    PrefillArgs d = a;
+    d.strict = mode == LA_MODE_READ_BEFORE_WRITE;
+    return from_cuda(la::launch_prefill_decay64(d, alpha, stream));
+  }
   // bf16 at dk = dv = 64 or 128, no decay, with a workspace: the tensor cores
   PrefillArgs tc = a;
   tc.chunk = 128;  // the tensor-core chunk
   // bf16 at dk = dv = 128, write then read with a decay, with a workspace: the
   // three-launch tensor-core form with decay weights
-  if (alpha && mode == LA_MODE_CAUSAL && dk == 128 && workspace && la::prefill_tc_supported(tc) &&
-      ws_bytes >= la::prefill_decay128_workspace_bytes(B, H, N))
-    return from_cuda(la::launch_prefill_decay128(a, alpha, stream));
+  if (alpha && dk == 128 && workspace && la::prefill_tc_supported(tc) &&
+      ws_bytes >= la::prefill_decay128_workspace_bytes(B, H, N)) {
+    tc.strict = mode == LA_MODE_READ_BEFORE_WRITE;
+    return from_cuda(la::launch_prefill_decay128(tc, alpha, stream));
+  }
   if (!alpha && mode != LA_MODE_CAUSAL && workspace && la::prefill_tc_supported(tc)) {
     // d = 64, at most 2048 chunks: the prefill's two launches, read before
     // write with a strict mask; non-causal from their piece totals

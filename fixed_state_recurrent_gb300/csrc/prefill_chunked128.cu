@@ -510,7 +510,9 @@ __device__ __forceinline__ float* gsums(uint8_t* smem, uint32_t s) {
 // Q slot) are handed round in chunk order, so no waiter can fall two phases
 // behind: each completion needs the waiter of the one before to have passed.
 // STRICT: read before write (token t reads the state before its own write, so
-// the mask keeps keys s < t; the state handed between chunks is the same).
+// the mask keeps keys s < t; the state handed between chunks is the same; with
+// DECAY that state is S_{t-1}, so the query side takes g_{t-1}, 0 for the
+// chunk's first token, in place of g_t).
 // DECAY: S_t = alpha_t S_{t-1} + phi(k_t) v_t^T, z likewise.  With g_t the
 // inclusive sum of log2 alpha over the chunk up to t and gamma_t = 2^g_t, the
 // chunk's entry state reaches token t as gamma_t S and its own tokens s <= t
@@ -760,7 +762,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!wait_w(x, &B->accS, g & 1)) continue;
         tc_fence_after();
         const float* gs = gsums(smem, g % NS);
-        const float gt = DECAY ? gs[row] : 0.f;
+        // decayed form: gt the query side's sum (g_t, or g_{t-1} before write),
+        // gkey the key side's (g_s for key s = row)
+        const float gkey = DECAY ? gs[row] : 0.f;
+        const float gt = !DECAY ? 0.f : !STRICT ? gkey : row > 0 ? gs[row - 1] : 0.f;
         // this warp's query rows are 32 quad .. +31: key blocks before `quad`
         // are fully visible, block `quad` holds the diagonal (kept), later
         // blocks are zero.  Packed keys 32 q4 .. go to columns 16 q4 ..; block
@@ -812,7 +817,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           // The scores have read phi(Q) and phi(K): phi(Q) [S | z] takes phi(Q)
           // times gamma_t (TMEM, packed bf16 pairs), the advance phi(K) rows
           // times 2^(g_C - g_t) (shared memory).
-          const float gq = exp2_ftz(gt), gk = exp2_ftz(gs[C - 1] - gt);
+          const float gq = exp2_ftz(gt), gk = exp2_ftz(gs[C - 1] - gkey);
           const uint32_t tq = x.tmem + ((uint32_t)(32 * quad) << 16) + TQ;
 #pragma unroll 1
           for (int h2 = 0; h2 < 2; ++h2) {
@@ -1140,10 +1145,9 @@ cudaError_t launch_prefill_decay128(const PrefillArgs& a, const float* alpha, cu
   if (e != cudaSuccess) return e;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
+  auto* const out = a.strict ? k3::output_kernel<true, true> : k3::output_kernel<false, true>;
   e = cudaFuncSetAttribute(k1::aggregate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k1::SMEM);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k3::output_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)k3::SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(out, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k3::SMEM);
   if (e != cudaSuccess) return e;
   // the three launches, each a programmatic dependent of what precedes it
   cudaLaunchAttribute pdl;
@@ -1166,7 +1170,7 @@ cudaError_t launch_prefill_decay128(const PrefillArgs& a, const float* alpha, cu
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k3::kWarps);
   cfg.dynamicSmemBytes = k3::SMEM;
-  return cudaLaunchKernelEx(&cfg, k3::output_kernel<false, true>, mq, mk, mv, mo, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, out, mq, mk, mv, mo, p, mbar_ns);
 }
 
 size_t aggregate128_totals_bytes(int B, int H, int N) {

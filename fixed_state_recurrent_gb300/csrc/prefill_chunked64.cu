@@ -535,8 +535,9 @@ __device__ __forceinline__ uint8_t* stage_ptr(uint8_t* smem, uint32_t s) { retur
 // two later products; the state warps scale the running state by gamma_C of
 // the next chunk before its advance, and after the last advance store S_N,
 // z_N.  All factors are at most 1 for alpha <= 1.
-// STRICT (without DECAY): read before write, token t reads the state before
-// its own write, so the mask keeps keys s < t.
+// STRICT: read before write, token t reads the state before its own write,
+// so the mask keeps keys s < t; with DECAY that state is S_{t-1}, so the query
+// side takes g_{t-1} (0 for the chunk's first token) in place of g_t.
 template <bool DECAY, bool STRICT = false>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -753,7 +754,10 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t base = tl + TA + 128 * b;
         const int row = 32 * quad + lane;
         const float* g = gsums(smem, aj % NS);
-        const float gt = DECAY ? g[row] : 0.f;
+        // decayed form: gt the query side's sum (g_t, or g_{t-1} before write),
+        // gk the key side's (g_s for key s = row)
+        const float gk = DECAY ? g[row] : 0.f;
+        const float gt = !DECAY ? 0.f : !STRICT ? gk : row > 0 ? g[row - 1] : 0.f;
         // this warp's query rows are 32 quad .. +31: key blocks before `quad` are
         // fully visible, block `quad` holds the diagonal, later blocks are zero;
         // packed keys 32 q4.. go to columns 16 q4..  One key block at a time
@@ -807,7 +811,7 @@ output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           uint8_t* st = stage_ptr(smem, aj % NS);
           // phi(Q) [S | z]: gamma_t; the advance: phi(K) by 2^(g_C - g_t)
 #pragma unroll 1
-          for (int m = 0; m < 2; ++m) scale_row(st + m * BLK, row, exp2_ftz(m ? g[C - 1] - gt : gt));
+          for (int m = 0; m < 2; ++m) scale_row(st + m * BLK, row, exp2_ftz(m ? g[C - 1] - gk : gt));
           fence_proxy_async_smem();
         }
         tc_fence_before();
@@ -1235,7 +1239,7 @@ bool prefill_decay64_supported(const PrefillArgs& a) {
 cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cudaStream_t stream) {
   const int BH = a.B * a.H;
   // calls whose re-read data stays in L2: the two launches of prefill_prefix64.cu
-  if (a.workspace && prefill_prefix64_chosen(a.B, a.H, a.N) &&
+  if (!a.strict && a.workspace && prefill_prefix64_chosen(a.B, a.H, a.N) &&
       a.ws_bytes >= prefill_prefix64_decay_workspace_bytes(a.B, a.H, a.N))
     return launch_prefill_prefix64_decay(a, alpha, stream);
   CUtensorMap mq, mk, mv, mo;
@@ -1265,11 +1269,11 @@ cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cud
   if (e != cudaSuccess) return e;
   const unsigned long long mbar_ns = env_ull("LA_MBAR_TIMEOUT_NS", 2000000000ull);
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
-  e = cudaFuncSetAttribute(k3::output_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)k3::SMEM);
+  auto* const out = a.strict ? k3::output_kernel<true, true> : k3::output_kernel<true, false>;
+  e = cudaFuncSetAttribute(out, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k3::SMEM);
   if (e != cudaSuccess) return e;
   if (!pieces) {
-    k3::output_kernel<true><<<p.sp.G, 32 * k3::kWarps, k3::SMEM, stream>>>(mq, mk, mv, mo, p, mbar_ns);
+    out<<<p.sp.G, 32 * k3::kWarps, k3::SMEM, stream>>>(mq, mk, mv, mo, p, mbar_ns);
     return cudaGetLastError();
   }
   e = cudaFuncSetAttribute(k1::aggregate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1294,7 +1298,7 @@ cudaError_t launch_prefill_decay64(const PrefillArgs& a, const float* alpha, cud
   cfg.gridDim = dim3(p.sp.G);
   cfg.blockDim = dim3(32 * k3::kWarps);
   cfg.dynamicSmemBytes = k3::SMEM;
-  return cudaLaunchKernelEx(&cfg, k3::output_kernel<true>, mq, mk, mv, mo, p, mbar_ns);
+  return cudaLaunchKernelEx(&cfg, out, mq, mk, mv, mo, p, mbar_ns);
 }
 
 }  // namespace la

@@ -128,7 +128,11 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  * for larger ones three (decayed piece totals, the chained scan
  * E' = Gamma E + R, then the outputs); with NULL, one block per head.
  * LA_BF16 at dk = dv = 128 with a decay in LA_MODE_CAUSAL and a workspace
- * runs the same three launches on the tensor cores at that width.
+ * runs the same three launches on the tensor cores at that width.  With a
+ * decay in LA_MODE_READ_BEFORE_WRITE, LA_BF16 at dk = dv = 64 (any
+ * workspace, or none) and at 128 (with one) runs the three-launch forms (at
+ * 64 without a workspace, one block per head) with a strict mask, each token
+ * reading S_{t-1}.
  * LA_BF16 at dk = dv = 64 or 128 without a decay, with a workspace, also
  * runs on the tensor cores: LA_MODE_READ_BEFORE_WRITE as la_prefill's
  * launches with a strict mask inside each chunk; LA_MODE_NONCAUSAL as the

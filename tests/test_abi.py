@@ -148,14 +148,18 @@ def test_prefill_variant_rejects_invalid_arguments(lib, kw):
 
 
 def test_prefill_variant_workspace_bytes(lib):
-    # bf16 at d = 64 with a decay, write then read: the tensor-core split over
-    # the SMs; every other form the CUDA-core chunk slots (dk dv + dk + 1 floats
-    # per chunk), when its heads are few enough to be worth cutting
+    # bf16 at d = 64 with a decay, write then read or read before write: the
+    # tensor-core split over the SMs (the same workspace for both orders);
+    # without a decay in causal order, and fp32, the CUDA-core chunk slots
+    # (dk dv + dk + 1 floats per chunk), when its heads are few enough to be
+    # worth cutting
     assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 0, 1) > 0
+    assert (lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 1, 1) ==
+            lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 0, 1))
     slots = 32 * 10 * (64 * 64 + 64 + 1) * 4  # 32 heads: 10 chunks each fill ~2 blocks per SM
     assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 0, 0) == slots
     assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 0, 0, 1) == slots
-    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 1, 1, 1) == slots
+    assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 64, 64, 0, 1, 1) == slots
     assert lib.la_prefill_variant_workspace_bytes(1, 1, 256, 64, 64, 0, 2, 0) == 32 * (64 * 64 + 64 + 1) * 4
     assert lib.la_prefill_variant_workspace_bytes(4, 8, 4096, 128, 128, 1, 0, 1) > 0
     assert lib.la_prefill_variant_workspace_bytes(1, 1, 8, 64, 64, 0, 0, 0) == 0   # one chunk

@@ -441,6 +441,38 @@ def test_decay_prefill_tc_d128_bounded_wait_reports_timeout(la, orc, monkeypatch
     assert relmax(f64(o), ro) <= TOL_BF16
 
 
+# read before write with a decay on the tensor cores: the three-launch forms
+# with a strict mask and the query side decayed to the token before (and, at
+# d = 64 without a workspace, one block per head)
+RBW_DECAY_SHAPES = [(64, 1, 3, 1), (64, 1, 3, 300), (64, 2, 5, 3000), (64, 3, 40, 333),
+                    (128, 1, 3, 129), (128, 2, 5, 3000), (128, 3, 40, 333)]
+
+
+@pytest.mark.parametrize("shape", RBW_DECAY_SHAPES, ids=[str(s) for s in RBW_DECAY_SHAPES])
+@pytest.mark.parametrize("arange", [(0.9, 1.0), (0.02, 0.5)], ids=["mild", "severe"])
+@pytest.mark.parametrize("ws", [None, False], ids=["ws", "nows"])
+def test_decay_read_before_write_tc_matches_oracle(la, orc, shape, arange, ws):
+    from fixed_state_recurrent_gb300 import inputs
+    d, B, H, N = shape
+    if ws is False and d == 128:
+        pytest.skip("d = 128 without a workspace runs on the CUDA cores")
+    q, k, v = inputs.la_inputs(B, H, N, d, d, torch.bfloat16, seed=205 + N % 53)
+    g = torch.Generator().manual_seed(206 + N + d)
+    lo, hi = arange
+    alpha = lo + (hi - lo) * torch.rand((B, H, N), generator=g)
+    alpha[:, :, ::97] = 0.0  # some tokens forget everything before them
+    S0 = torch.randn((B, H, d, d), generator=g) * 0.5
+    z0 = torch.rand((B, H, d), generator=g) * 4 + 0.5
+    la.delta_read_device_status()
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), alpha.cuda(), la.LA_MODE_READ_BEFORE_WRITE,
+                                 S0=S0.cuda(), z0=z0.cuda(), ws=ws)
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha), 1, S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
+
+
 def test_decay_prefill_tc_zero_alpha_forgets(la, orc):
     # alpha = 0 at some tokens (taken as 1e-30 in the chunk factors): the state
     # before them is forgotten, including right at chunk edges
