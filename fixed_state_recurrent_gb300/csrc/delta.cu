@@ -165,7 +165,7 @@ cudaError_t launch_delta_prefill(const void* k, const void* v, bool bf16,
   // tensor-core form (delta_chunked128.cu); everything else runs token by
   // token here.
   if (delta_chunked_supported(bf16, dk, dv))
-    return launch_delta_chunked(k, v, beta, alpha, B, H, N, S0, reads, S_N, stream);
+    return launch_delta_chunked(k, v, beta, alpha, B, H, N, dk, S0, reads, S_N, stream);
   const unsigned blocks = (unsigned)((size_t)B * H);
   // P lanes per column (a power of two, at most 4): enough that a lane holds
   // at most 32 rows.  rows = ceil(dk / P) <= 32 and P * kPad <= 4 * kPad, so

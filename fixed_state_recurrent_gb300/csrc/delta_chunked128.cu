@@ -107,6 +107,7 @@ constexpr uint32_t ID_S = idesc_bf16_f32(128, D, 0, 1);     // UB x K_c   (B MN-
 
 struct Params {
   int BH, N;
+  int d;               // dk = dv of the call (64, 96 or 128); the kernel works at 128 with zeros past d
   const float* beta;
   const float* alpha;  // gated form: per-token forgetting (kernel instantiated with GATED)
   const float* S0;
@@ -632,12 +633,16 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       uint32_t w[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        w[q] = __float_as_uint(p.S0 ? p.S0[((size_t)head * D + 16 * h + q) * D + j] : 0.f);
+        w[q] = __float_as_uint(p.S0 && 16 * h + q < p.d && j < p.d
+                                   ? p.S0[((size_t)head * p.d + 16 * h + q) * p.d + j] : 0.f);
       tmem_st16(tl + ST + 16 * h, w);
     }
     tmem_st_wait();
     const uint32_t nchunks = 2u * (uint32_t)npairs;
-    float* reads_j = p.reads + (size_t)head * p.N * D + j;
+    // value column j of the reads (lanes j >= d hold the zero columns of a
+    // narrower call and store nothing)
+    const bool jout = j < p.d;
+    float* reads_j = p.reads + (size_t)head * p.N * p.d + (jout ? j : 0);
     for (uint32_t ch = 0; ch < nchunks; ++ch) {
       const uint8_t* vt = smem + OFF_V + (ch % NV) * VSLOT;
       // gated: the pair's gamma factors are published with its T (tready)
@@ -689,7 +694,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
           tmem_ld_wait();
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            if (t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * D] = __uint_as_float(f[q]);
+            if (jout && t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * p.d] = __uint_as_float(f[q]);
         }
       }
       // V of the chunk, column j, into registers (token pairs packed)
@@ -778,7 +783,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 32; ++q)
-          if (t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * D] = __uint_as_float(f[q]);
+          if (jout && t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * p.d] = __uint_as_float(f[q]);
       }
       waitd_warp(x, &B->sready, (nchunks - 1) & 1);
       tc_fence_after();
@@ -788,7 +793,8 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       tmem_ld32(tl + ST + 32 * h, f);
       tmem_ld_wait();
 #pragma unroll
-      for (int q = 0; q < 32; ++q) p.S_N[((size_t)head * D + 32 * h + q) * D + j] = __uint_as_float(f[q]);
+      for (int q = 0; q < 32; ++q)
+        if (jout && 32 * h + q < p.d) p.S_N[((size_t)head * p.d + 32 * h + q) * p.d + j] = __uint_as_float(f[q]);
     }
   }
   tc_fence_before();
@@ -806,23 +812,31 @@ __device__ unsigned g_delta_status;
 }  // namespace dc
 }  // namespace
 
-bool delta_chunked_supported(bool bf16, int dk, int dv) { return bf16 && dk == 128 && dv == 128; }
+// dk = dv = 64 and 96 run the same kernel: the K and V maps are as wide as the
+// call, so the column blocks past it load as zeros (TMA fills what lies
+// outside a tensor), and with zero key and value columns the state's rows and
+// columns past d stay exactly zero; only the first d columns are stored.
+bool delta_chunked_supported(bool bf16, int dk, int dv) {
+  return bf16 && dk == dv && (dk == 64 || dk == 96 || dk == 128);
+}
 
 cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, const float* alpha,
-                                 int B, int H, int N, const float* S0, float* reads, float* S_N,
+                                 int B, int H, int N, int d, const float* S0, float* reads, float* S_N,
                                  cudaStream_t stream) {
   using namespace dc;
+  if (!delta_chunked_supported(true, d, d)) return cudaErrorInvalidValue;
   unsigned* status = nullptr;
   cudaError_t se = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_delta_status);
   if (se != cudaSuccess) return se;
   const int BH = B * H;
   CUtensorMap mk, mv;
-  if (!make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, PT) ||
-      !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 64, CH))
+  if (!make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, PT) ||
+      !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, CH))
     return cudaErrorInvalidValue;
   Params p;
   p.BH = BH;
   p.N = N;
+  p.d = d;
   p.beta = beta;
   p.alpha = alpha;
   p.S0 = S0;

@@ -199,11 +199,12 @@ cudaError_t launch_decode_step(const void* q, const void* k, const void* v,
                                float eps, float* S, float* z, float* o,
                                cudaStream_t stream);
 
-// Tensor-core chunked delta rule (bf16, dk = dv = 128; delta_chunked128.cu).
+// Tensor-core chunked delta rule (bf16, dk = dv = 64, 96 or 128;
+// delta_chunked128.cu).
 bool delta_chunked_supported(bool bf16, int dk, int dv);
-// alpha: per-token forgetting of the gated form, or NULL.
+// alpha: per-token forgetting of the gated form, or NULL; d = dk = dv.
 cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta, const float* alpha,
-                                 int B, int H, int N, const float* S0, float* reads, float* S_N,
+                                 int B, int H, int N, int d, const float* S0, float* reads, float* S_N,
                                  cudaStream_t stream);
 // The status word of the kernels whose calls take no workspace (the chunked
 // delta kernels, the decayed tensor-core prefill): its device address, and

@@ -232,9 +232,10 @@ la_status la_decode_step(const void* q, const void* k, const void* v, la_dtype i
  *   k [B][H][N][dk], v [B][H][N][dv] in in_dtype;  beta [B][H][N] float32
  *   S0 initial memory or NULL (zero); S_N may alias S0
  *   reads [B][H][N][dv], S_N [B][H][dk][dv] float32
- * bf16 inputs at dk = dv = 128 run chunkwise on the tensor cores (64-token
- * chunks; the state enters the products as a bf16 copy of the fp32 state);
- * other inputs run token by token in fp32.  A bounded wait of the chunkwise
+ * bf16 inputs at dk = dv = 64, 96 or 128 run chunkwise on the tensor cores
+ * (64-token chunks; the state enters the products as a bf16 copy of the fp32
+ * state; widths below 128 run the width-128 kernel with the columns past dk
+ * zero, so they take about as long); other inputs run token by token in fp32.  A bounded wait of the chunkwise
  * kernel that gives up is reported by delta_read_device_status.
  */
 la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const float* beta,
@@ -248,8 +249,8 @@ la_status delta_prefill(const void* k, const void* v, la_dtype in_dtype, const f
  * memory decays first, then the correction uses the decayed prediction:
  *   D = alpha_t S_{t-1};  reads[t] = k_t^T D;  S_t = D + beta_t k_t (v_t - reads[t])^T
  *   alpha [B][H][N] float32, or NULL (alpha_t = 1: exactly delta_prefill).
- * Other arguments as delta_prefill.  bf16 inputs at dk = dv = 128 run
- * chunkwise on the tensor cores (decay factors inside each 64-token chunk,
+ * Other arguments as delta_prefill.  bf16 inputs at dk = dv = 64, 96 or 128
+ * run chunkwise on the tensor cores (decay factors inside each 64-token chunk,
  * status through delta_read_device_status); everything else runs token by
  * token in fp32 on the CUDA cores.
  */
@@ -274,8 +275,9 @@ la_status la_read_device_status(const void* workspace, cudaStream_t stream);
 
 /* Synchronizes `stream`, then returns and clears the status word of the
  * tensor-core kernels whose calls take no workspace: delta_prefill and
- * gated_delta_prefill with bf16 inputs at dk = dv = 128, la_prefill_variant
- * with a decay and la_prefill_backward on bf16 inputs at dk = dv = 64 (also
+ * gated_delta_prefill with bf16 inputs at dk = dv = 64, 96 or 128, the
+ * tensor-core forms of la_prefill_variant and la_prefill_backward on bf16
+ * inputs (also
  * when they are given a workspace), and la_prefill_noalloc.  LA_ERR_TIMEOUT if one of their
  * bounded waits gave up since the last read, otherwise LA_OK; LA_ERR_CUDA if
  * the synchronization or copy fails.  The word belongs to the current device

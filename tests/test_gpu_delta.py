@@ -134,6 +134,30 @@ def test_delta_chunked_ragged(la, orc, N):
     assert relmax(f64(S), rS) <= TOL_BF16
 
 
+@pytest.mark.parametrize("gated", [False, True], ids=["plain", "gated"])
+@pytest.mark.parametrize("N", [1, 65, 129, 385, 1000])
+@pytest.mark.parametrize("d", [64, 96])
+def test_delta_chunked_narrow(la, orc, d, N, gated):
+    # bf16 at dk = dv = 64 and 96 runs the chunkwise kernel with the columns
+    # past d zero: the reads and the state match the oracle, with S_N written
+    # over S0
+    from fixed_state_recurrent_gb300 import inputs
+    k, v, beta = inputs.delta_inputs(2, 3, N, d, d, torch.bfloat16, seed=520 + N + d)
+    g = torch.Generator().manual_seed(N + d)
+    S0 = torch.randn((2, 3, d, d), generator=g) * 0.5
+    alpha = (0.8 + 0.2 * torch.rand((2, 3, N), generator=g)) if gated else None
+    Sd = S0.cuda()
+    la.delta_read_device_status()
+    reads, S = la.gated_delta_prefill(k.cuda(), v.cuda(), beta.cuda(),
+                                      None if alpha is None else alpha.cuda(), S0=Sd, S_N=Sd)
+    rr, rS = orc.gated_delta(f64(k), f64(v), f64(beta), None if alpha is None else f64(alpha),
+                             S0=f64(S0))
+    assert S.data_ptr() == Sd.data_ptr()
+    assert relmax(f64(reads), rr) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
+
+
 def test_delta_chunked_repeatable(la, orc):
     # A few blocks (three heads) leave the SMs lightly loaded, which is where
     # an ordering hole between the kernel's roles shows up; the kernel has no
