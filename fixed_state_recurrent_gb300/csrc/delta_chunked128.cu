@@ -107,7 +107,6 @@ constexpr uint32_t ID_S = idesc_bf16_f32(128, D, 0, 1);     // UB x K_c   (B MN-
 
 struct Params {
   int BH, N;
-  int d;               // dk = dv of the call (64, 96 or 128); the kernel works at 128 with zeros past d
   const float* beta;
   const float* alpha;  // gated form: per-token forgetting (kernel instantiated with GATED)
   const float* S0;
@@ -350,7 +349,9 @@ __device__ __forceinline__ void solve_t(float* S, const float* bs, uint8_t* ttil
   }
 }
 
-template <bool GATED>
+// DW: dk = dv of the call (64, 96 or 128, a compile-time stride for the
+// stores); the kernel works at 128 with the key and value columns past DW zero.
+template <bool GATED, int DW>
 __global__ void __launch_bounds__(32 * kWarps, 1)
 delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const Params p, const unsigned long long mbar_ns) {
@@ -633,16 +634,16 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       uint32_t w[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        w[q] = __float_as_uint(p.S0 && 16 * h + q < p.d && j < p.d
-                                   ? p.S0[((size_t)head * p.d + 16 * h + q) * p.d + j] : 0.f);
+        w[q] = __float_as_uint(p.S0 && 16 * h + q < DW && j < DW
+                                   ? p.S0[((size_t)head * DW + 16 * h + q) * DW + j] : 0.f);
       tmem_st16(tl + ST + 16 * h, w);
     }
     tmem_st_wait();
     const uint32_t nchunks = 2u * (uint32_t)npairs;
     // value column j of the reads (lanes j >= d hold the zero columns of a
     // narrower call and store nothing)
-    const bool jout = j < p.d;
-    float* reads_j = p.reads + (size_t)head * p.N * p.d + (jout ? j : 0);
+    const bool jout = j < DW;
+    float* reads_j = p.reads + (size_t)head * p.N * DW + (jout ? j : 0);
     for (uint32_t ch = 0; ch < nchunks; ++ch) {
       const uint8_t* vt = smem + OFF_V + (ch % NV) * VSLOT;
       // gated: the pair's gamma factors are published with its T (tready)
@@ -694,7 +695,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
           tmem_ld_wait();
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            if (jout && t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * p.d] = __uint_as_float(f[q]);
+            if (jout && t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * DW] = __uint_as_float(f[q]);
         }
       }
       // V of the chunk, column j, into registers (token pairs packed)
@@ -783,7 +784,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 32; ++q)
-          if (jout && t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * p.d] = __uint_as_float(f[q]);
+          if (jout && t0 + 32 * h + q < p.N) reads_j[(size_t)(t0 + 32 * h + q) * DW] = __uint_as_float(f[q]);
       }
       waitd_warp(x, &B->sready, (nchunks - 1) & 1);
       tc_fence_after();
@@ -794,7 +795,7 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       tmem_ld_wait();
 #pragma unroll
       for (int q = 0; q < 32; ++q)
-        if (jout && 32 * h + q < p.d) p.S_N[((size_t)head * p.d + 32 * h + q) * p.d + j] = __uint_as_float(f[q]);
+        if (jout && 32 * h + q < DW) p.S_N[((size_t)head * DW + 32 * h + q) * DW + j] = __uint_as_float(f[q]);
     }
   }
   tc_fence_before();
@@ -836,7 +837,6 @@ cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta
   Params p;
   p.BH = BH;
   p.N = N;
-  p.d = d;
   p.beta = beta;
   p.alpha = alpha;
   p.S0 = S0;
@@ -851,7 +851,9 @@ cudaError_t launch_delta_chunked(const void* k, const void* v, const float* beta
     kern<<<BH, 32 * kWarps, SMEM, stream>>>(mk, mv, p, mbar_ns);
     return cudaGetLastError();
   };
-  return alpha ? go(delta_chunked_kernel<true>) : go(delta_chunked_kernel<false>);
+  if (d == 64) return alpha ? go(delta_chunked_kernel<true, 64>) : go(delta_chunked_kernel<false, 64>);
+  if (d == 96) return alpha ? go(delta_chunked_kernel<true, 96>) : go(delta_chunked_kernel<false, 96>);
+  return alpha ? go(delta_chunked_kernel<true, 128>) : go(delta_chunked_kernel<false, 128>);
 }
 
 cudaError_t library_status_word(unsigned** out) {
