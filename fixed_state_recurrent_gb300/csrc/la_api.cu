@@ -227,7 +227,8 @@ size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv, l
       N > 0) {
     size_t tc = 0;
     if (dk == 64 && la::prefill_prefix64_chosen(B, H, N))
-      tc = la::prefill_prefix64_workspace_bytes(B, H, N);
+      tc = mode == LA_MODE_NONCAUSAL ? la::prefill_nc64_workspace_bytes(B, H, N)
+                                     : la::prefill_prefix64_workspace_bytes(B, H, N);
     else if (mode == LA_MODE_READ_BEFORE_WRITE)
       tc = sizeof(la::WsHeader) + la::prefill_tc_workspace_bytes(B, H, N, dk, 128);
     else
@@ -315,10 +316,12 @@ la_status la_prefill_variant(const void* q, const void* k, const void* v, la_dty
   if (!alpha && mode != LA_MODE_CAUSAL && workspace && la::prefill_tc_supported(tc)) {
     // d = 64, at most 2048 chunks: the prefill's two launches, read before
     // write with a strict mask; non-causal from their piece totals
-    if (dk == 64 && la::prefill_prefix64_chosen(B, H, N) &&
+    if (dk == 64 && la::prefill_prefix64_chosen(B, H, N) && mode == LA_MODE_READ_BEFORE_WRITE &&
         ws_bytes >= la::prefill_prefix64_workspace_bytes(B, H, N))
-      return from_cuda(mode == LA_MODE_READ_BEFORE_WRITE ? la::launch_prefill_rbw64(a, stream)
-                                                         : la::launch_prefill_nc64(a, stream));
+      return from_cuda(la::launch_prefill_rbw64(a, stream));
+    if (dk == 64 && la::prefill_prefix64_chosen(B, H, N) && mode == LA_MODE_NONCAUSAL &&
+        ws_bytes >= la::prefill_nc64_workspace_bytes(B, H, N))
+      return from_cuda(la::launch_prefill_nc64(a, stream));
     // otherwise the three-launch prefill of that width with a strict mask, or
     // its aggregate launch and the reads of the final state
     if (mode == LA_MODE_READ_BEFORE_WRITE &&

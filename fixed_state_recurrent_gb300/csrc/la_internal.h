@@ -145,8 +145,9 @@ cudaError_t launch_prefix64_totals(const PrefillArgs& a, const Prefix64Buffers& 
 // Non-causal order (la_prefill_variant's LA_MODE_NONCAUSAL) at bf16,
 // dk = dv = 64, for the calls prefill_prefix64_chosen takes: the piece totals,
 // then every query reads its head's final state (prefill_noncausal.cu).
-// a.workspace of at least prefill_prefix64_workspace_bytes (no header);
+// a.workspace of at least prefill_nc64_workspace_bytes (no header);
 // bounded-wait failures go to the library status word.
+size_t prefill_nc64_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prefill_nc64(const PrefillArgs& a, cudaStream_t stream);
 // The same order at bf16, dk = dv = 64 or 128, for calls of any length: the
 // totals from the aggregate kernel of the three-launch prefill, then the

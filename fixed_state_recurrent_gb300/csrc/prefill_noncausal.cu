@@ -5,24 +5,19 @@
 // reads the state over the whole sequence,
 //   o_t = phi(q_t)^T S_N / (phi(q_t)^T z_N + eps),
 //   S_N = S0 + sum_t phi(k_t) v_t^T,  z_N = z0 + sum_t phi(k_t).
-// Over splits of prefill_tc_common.cuh, either
-//   (d = 64, calls of at most 2048 chunks) two launches:
-//   1. the prefill's prefix kernel (prefill_prefix64.cu) for the piece totals
-//      R, which carry S0 in a piece that starts its head;
-//   2. nc_kernel<64>: per piece of the block's run, S_N of its head as the sum
-//      of the head's totals in slot order (fp32), as the operand tile of
-//      prefill_scan.cuh (StateTile); per chunk phi(Q) in place, then
-//      [num | den] = phi(Q) [S_N | z_N]^T as one product of N_S = D + 16
-//      columns, o = num / (den + eps) staged for TMA stores.  The block that
-//      holds a head's last chunk writes S_N, z_N;
-//   or (d = 64 past 2048 chunks, d = 128) three launches:
-//   1. the aggregate kernel of the three-launch prefill at that width
-//      (prefill_chunked64.cu, prefill_chunked128.cu) for the piece totals,
-//      without S0;
-//   2. the fold of prefill_scan.cuh, once per head: S_N = S0 + the totals in
-//      slot order, stored as S_N, z_N and as the head's operand tile;
-//   3. nc_kernel<D> as above, with each piece's tile brought in by one bulk
-//      copy instead of being summed by every block of the head.
+// Three launches over splits of prefill_tc_common.cuh:
+//   1. the piece totals R: at d = 64, for calls of at most 2048 chunks, the
+//      prefill's prefix kernel (prefill_prefix64.cu), whose totals carry S0 in
+//      a piece that starts its head; otherwise the aggregate kernel of the
+//      three-launch prefill at that width (prefill_chunked64.cu,
+//      prefill_chunked128.cu), whose totals do not;
+//   2. the fold of prefill_scan.cuh, once per head: S_N = S0 (unless the
+//      totals carry it) + the totals in slot order, stored as S_N, z_N and as
+//      the head's bf16 operand tile (StateTile, z as hi + lo rows);
+//   3. nc_kernel<D>: per piece of the block's run, its head's tile by one bulk
+//      copy; per chunk phi(Q) in place, then [num | den] = phi(Q) [S_N | z_N]^T
+//      as one product of N_S = D + 16 columns, o = num / (den + eps) staged
+//      for TMA stores.
 // At d = 64 a block takes 77 KB of shared memory and the split has two blocks
 // per SM; at d = 128 it takes 133 KB and one.  Every wait is bounded; one that
 // gives up records a timeout in the library status word and the kernel
@@ -61,10 +56,7 @@ struct Params {
   Split sp;           // this kernel's runs
   Split sr;           // the split of the launch whose slots hold the piece totals
   float eps;
-  const float* R;     // [BH * sr.MPH][SZ] piece totals (slot layout: S^T rows, then z)
-  const uint8_t* tiles;  // [BH] operand tiles of S_N, z_N (StateTile); NULL: summed here from R
-  float* S_N;
-  float* z_N;
+  const uint8_t* tiles;  // [BH] operand tiles of S_N, z_N (StateTile), from the fold
   unsigned* status;
   int force_wait;     // test hook: the first product waits once on a barrier that nothing completes
 };
@@ -174,45 +166,12 @@ nc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   Piece pc;
   for (int i = 0; run.piece(sp, i, &pc); ++i) {
     const int h = pc.h;
-    if (p.tiles) {  // the head's tile, folded once per head by the launch before
-      if (t == 0 && !aborted()) {
-        mbar_arrive_expect_tx(&B->tile, L::XT);
-        bulk_copy_in(stile, p.tiles + (size_t)h * L::XT, L::XT, &B->tile);
-      }
-      waitb(x, &B->tile, i & 1);
-    } else {
-      // S_N of the piece's head: the sum of all its slots, in slot order
-      const Split& sr = p.sr;
-      const int nb = sr.owner((long long)h * NC + NC - 1) - sr.owner((long long)h * NC) + 1;
-      const bool last = pc.tok1 == N;  // this block holds the head's last chunk: it writes S_N, z_N
-      const float4* Rh = reinterpret_cast<const float4*>(p.R + (size_t)h * sr.MPH * SZ);
-      for (int f = t; f < SZ / 4; f += kThreads) {
-        const int row = f / (D / 4), col = 4 * (f % (D / 4));  // slot row j holds column j of S
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        constexpr int U = 4;
-        for (int k0 = 0; k0 < nb; k0 += U) {
-          float4 r[U];
-#pragma unroll
-          for (int u = 0; u < U; ++u)
-            r[u] = k0 + u < nb ? __ldcg(Rh + (size_t)(k0 + u) * (SZ / 4) + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            acc.x += r[u].x; acc.y += r[u].y; acc.z += r[u].z; acc.w += r[u].w;
-          }
-        }
-        state_tile_put<D>(stile, row, col, acc);
-        if (last && !aborted()) {
-          if (row < D) {
-            p.S_N[((size_t)h * D + col + 0) * D + row] = acc.x;
-            p.S_N[((size_t)h * D + col + 1) * D + row] = acc.y;
-            p.S_N[((size_t)h * D + col + 2) * D + row] = acc.z;
-            p.S_N[((size_t)h * D + col + 3) * D + row] = acc.w;
-          } else {
-            reinterpret_cast<float4*>(p.z_N + (size_t)h * D)[col / 4] = acc;
-          }
-        }
-      }
+    // the head's tile, folded once per head by the launch before
+    if (t == 0 && !aborted()) {
+      mbar_arrive_expect_tx(&B->tile, L::XT);
+      bulk_copy_in(stile, p.tiles + (size_t)h * L::XT, L::XT, &B->tile);
     }
+    waitb(x, &B->tile, i & 1);
     fence_proxy_async_smem();
     __syncthreads();
 
@@ -325,31 +284,47 @@ cudaError_t launch_nc_kernel(const PrefillArgs& a, const Params& p, cudaStream_t
 
 }  // namespace
 
+size_t prefill_nc64_workspace_bytes(int B, int H, int N) {
+  return prefill_prefix64_workspace_bytes(B, H, N) + (size_t)B * H * StateTile<64>::BYTES;
+}
+
 cudaError_t launch_prefill_nc64(const PrefillArgs& a, cudaStream_t stream) {
   constexpr int D = 64;
   const int BH = a.B * a.H;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const Split sr = make_split(BH, a.N, sms);
-  if (!a.workspace || prefill_prefix64_workspace_bytes(a.B, a.H, a.N) > a.ws_bytes)
-    return cudaErrorInvalidValue;
-  // the prefill's workspace layout: piece totals, prefix tiles, phi(K)
+  if (!a.workspace || prefill_nc64_workspace_bytes(a.B, a.H, a.N) > a.ws_bytes) return cudaErrorInvalidValue;
+  // the prefill's workspace layout (piece totals, prefix tiles, phi(K); only
+  // the totals are written), then one state tile per head
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   Prefix64Buffers b = {};
   b.R = reinterpret_cast<float*>(ws);
   b.P = reinterpret_cast<uint8_t*>(b.R + (size_t)BH * sr.MPH * Nc<D>::SZ);
   b.phik = reinterpret_cast<__nv_bfloat16*>(b.P + (size_t)sr.TC() * 66 * 128);
+  uint8_t* tiles = ws + prefill_prefix64_workspace_bytes(a.B, a.H, a.N);
   cudaError_t e = library_status_word(&b.status);
   if (e != cudaSuccess) return e;
   e = launch_prefix64_totals(a, b, stream);
+  if (e != cudaSuccess) return e;
+  // the fold (S0 is in the totals already), a programmatic dependent
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kScanThreads);
+  cfg.gridDim = dim3(scan_blocks_per_head<D>(), BH);
+  e = cudaLaunchKernelEx(&cfg, fold_kernel<D>, sr, (const float*)b.R, (const float*)nullptr,
+                         (const float*)nullptr, a.S_N, a.z_N, tiles);
   if (e != cudaSuccess) return e;
   Params p = {};
   p.sp = make_split(BH, a.N, Nc<D>::SPLIT * sms);
   p.sr = sr;
   p.eps = a.eps;
-  p.R = b.R;  // S0 is in the totals
-  p.S_N = a.S_N;
-  p.z_N = a.z_N;
+  p.tiles = tiles;
   p.status = b.status;
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
   return launch_nc_kernel<D>(a, p, stream);
@@ -373,10 +348,7 @@ cudaError_t launch_prefill_nc(const PrefillArgs& a, cudaStream_t stream) {
   float* R = reinterpret_cast<float*>(ws);
   uint8_t* tiles = ws + (d == 64 ? aggregate64_totals_bytes(a.B, a.H, a.N) : aggregate128_totals_bytes(a.B, a.H, a.N));
   Params p = {};
-  p.R = R;
   p.tiles = tiles;
-  p.S_N = a.S_N;
-  p.z_N = a.z_N;
   p.sr = make_split(BH, a.N, sms);
   p.eps = a.eps;
   p.force_wait = (int)env_ull("LA_TEST_FORCE_WAIT", 0);
