@@ -184,7 +184,7 @@ constexpr uint32_t STAGE = 2 * BLK;  // K | V
 constexpr uint32_t OFF_ONES = NS * STAGE;
 constexpr uint32_t OFF_BAR = OFF_ONES + BLK;
 constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
-constexpr int kWarps = 10;  // 0 TMA, 1 MMA, 2-5 phi, 6-9 epilogue (thread 192 also stores phi(K))
+constexpr int kWarps = 10;  // 0 TMA, 1 MMA, 2-5 phi, 6-9 epilogue
 constexpr uint32_t kCols = 128;
 
 struct Bars {
