@@ -14,15 +14,26 @@
 //   dS0 = G_0, dz0 = g_0,  dq = dphi(q) phi'(q), dk = dphi(k) phi'(k)
 // with phi'(u) = 1 for u > 0 and exp(u) for u <= 0.
 //
-// One block per head, fp32.  As in the CUDA-core prefill, thread (row group,
-// column group) owns a (rows x 4) slice of S -- and in the reverse sweep the
-// same slice of G.  Per token the block reduces num and den over row groups,
-// dden over columns and dphi(q) over column groups through shared memory;
-// the forward sweep parks dnum_t in dv's row t and dden_t in dk's row t
-// (element 0), and the reverse sweep reads them back before overwriting those
-// rows with the gradients.  Tokens are staged TB at a time.  This is the
-// plain form of the backward pass (a token-serial chain per head); it is not
-// a tensor-core kernel.
+// fp32.  As in the CUDA-core prefill, thread (row group, column group) owns a
+// (rows x 4) slice of S -- and in the reverse sweep the same slice of G.  Per
+// token the block reduces num and den over row groups, dden over columns and
+// dphi(q) over column groups through shared memory; the forward sweep parks
+// dnum_t in dv's row t and dden_t in dk's row t (element 0), and the reverse
+// sweep reads them back before overwriting those rows with the gradients.
+// Tokens are staged TB at a time.  Not a tensor-core kernel.
+//
+// Without a workspace one block walks a whole head, both sweeps (PASS 0).
+// With one the heads are cut into the CUDA-core prefill's chunks and five
+// launches run them in parallel:
+//   1-2. the prefill's chunk increments and scan: the state before every
+//        chunk (prefill_simt.cu);
+//   3. PASS 1, per chunk: the forward sweep from the state before the chunk,
+//      and the chunk's gradient-state increment
+//      dG_c = sum_{t in c} phi(q_t) dnum_t^T, dg_c = sum_{t in c} dden_t phi(q_t);
+//   4. per head, the gradient state after every chunk as the right fold
+//      dS_N + dG_{c+1} + dG_{c+2} + ... (always in this order), and dS0, dz0;
+//   5. PASS 2, per chunk: the reverse sweep from the gradient state after the
+//      chunk.
 #include "la_internal.h"
 
 namespace la {
@@ -55,8 +66,16 @@ struct BwdArgs {
   float eps;
   const float *S0, *z0, *dO, *dS_N, *dz_N;
   float *dq, *dk_out, *dv_out, *dS0, *dz0;
+  // chunked form: NC chunks of L tokens per head; per (head, chunk) a slot of
+  // dk dv + dk floats (row-major [i][j], then the dk vector)
+  int NC, L;
+  const float* E;  // the state before every chunk
+  float* Gs;       // PASS 1: the gradient-state increments; PASS 2: the gradient state after every chunk
 };
 
+// PASS 0: a whole head, both sweeps; 1: one chunk's forward sweep; 2: one
+// chunk's reverse sweep (see the top of the file).
+template <int PASS>
 __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a) {
   extern __shared__ float sm[];
   const Shape sh = bshape(a.dk, a.dv);
@@ -76,7 +95,12 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
   const int g = tid % sh.G, rg = tid / sh.G;
   const bool active = rg < sh.R;
   const int col0 = 4 * g;
-  const size_t head = blockIdx.x;
+  const size_t head = PASS == 0 ? blockIdx.x : blockIdx.y;
+  const int chunk = PASS == 0 ? 0 : blockIdx.x;
+  const int tb = PASS == 0 ? 0 : chunk * a.L;             // this block's tokens [tb, te)
+  const int te = PASS == 0 ? N : min(N, tb + a.L);
+  const size_t slot_sz = (size_t)dk * dv + dk;
+  const size_t slot = (head * a.NC + chunk) * slot_sz;
 
   float S[kMaxRows][4];
   float z[kMaxRows];
@@ -86,27 +110,38 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
 #pragma unroll
     for (int c = 0; c < 4; ++c) S[r][c] = 0.f;
   }
-  if (active) {
+  // PASS 1: the chunk's gradient-state increment, this thread's slice
+  float dG[kMaxRows][4];
+  float dg[kMaxRows];
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) {
+    dg[r] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dG[r][c] = 0.f;
+  }
+  if (PASS != 2 && active) {  // the state before the block's first token
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) {
       const int i = rg + r * sh.R;
       if (i < dk) {
-        if (a.S0) {
+        const float* Si = PASS == 0 ? (a.S0 ? a.S0 + (head * dk + i) * dv : nullptr) : a.E + slot + (size_t)i * dv;
+        const float* zi = PASS == 0 ? (a.z0 ? a.z0 + head * dk + i : nullptr) : a.E + slot + (size_t)dk * dv + i;
+        if (Si) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            if (col0 + c < dv) S[r][c] = a.S0[(head * dk + i) * dv + col0 + c];
+            if (col0 + c < dv) S[r][c] = Si[col0 + c];
         }
-        if (a.z0) z[r] = a.z0[head * dk + i];
+        if (zi) z[r] = *zi;
       }
     }
   }
 
   // ---------------------------------------------------------------- forward
-  for (int t0 = 0; t0 < N; t0 += kTB) {
+  for (int t0 = tb; PASS != 2 && t0 < te; t0 += kTB) {
     for (int e = tid; e < kTB * kMaxD; e += kThreads) {
       const int t = e / kMaxD, i = e % kMaxD;
       const int tok = t0 + t;
-      const bool in = tok < N;
+      const bool in = tok < te;
       float qv = 0.f;
       if (in && i < dk) qv = load_in(a.q, (head * N + tok) * dk + i, a.bf16);
       fq[e] = (in && i < dk) ? phi_f32(qv) : 0.f;
@@ -116,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
       gv[e] = (in && i < dv) ? a.dO[(head * N + tok) * dv + i] : 0.f;
     }
     __syncthreads();
-    const int nt = min(kTB, N - t0);
+    const int nt = min(kTB, te - t0);
     for (int t = 0; t < nt; ++t) {
       const size_t tok = head * N + t0 + t;
       // write, then the partial read over this thread's rows
@@ -186,6 +221,14 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
             float s = S[r][0] * dn.x + S[r][1] * dn.y + S[r][2] * dn.z + S[r][3] * dn.w;
             if (g == 0) s += dden * z[r];
             rpart[i * sh.G + g] = s;
+            if (PASS == 1) {  // phi(q_t) dnum_t^T and dden_t phi(q_t)
+              const float qq = fq[t * kMaxD + i];
+              dG[r][0] += qq * dn.x;
+              dG[r][1] += qq * dn.y;
+              dG[r][2] += qq * dn.z;
+              dG[r][3] += qq * dn.w;
+              dg[r] += dden * qq;
+            }
           }
         }
       }
@@ -200,6 +243,22 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
     }
   }
 
+  if (PASS == 1) {  // the chunk's gradient-state increment
+    if (active) {
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        const int i = rg + r * sh.R;
+        if (i < dk) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (col0 + c < dv) a.Gs[slot + (size_t)i * dv + col0 + c] = dG[r][c];
+          if (g == 0) a.Gs[slot + (size_t)dk * dv + i] = dg[r];
+        }
+      }
+    }
+    return;
+  }
+
   // ---------------------------------------------------------------- reverse
   // S and z become G and g
 #pragma unroll
@@ -208,24 +267,26 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
 #pragma unroll
     for (int c = 0; c < 4; ++c) S[r][c] = 0.f;
   }
-  if (active) {
+  if (active) {  // the gradient state after the block's last token
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) {
       const int i = rg + r * sh.R;
       if (i < dk) {
-        if (a.dS_N) {
+        const float* Gi = PASS == 0 ? (a.dS_N ? a.dS_N + (head * dk + i) * dv : nullptr) : a.Gs + slot + (size_t)i * dv;
+        const float* gi = PASS == 0 ? (a.dz_N ? a.dz_N + head * dk + i : nullptr) : a.Gs + slot + (size_t)dk * dv + i;
+        if (Gi) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            if (col0 + c < dv) S[r][c] = a.dS_N[(head * dk + i) * dv + col0 + c];
+            if (col0 + c < dv) S[r][c] = Gi[col0 + c];
         }
-        if (a.dz_N) z[r] = a.dz_N[head * dk + i];
+        if (gi) z[r] = *gi;
       }
     }
   }
-  const int nstage = (N + kTB - 1) / kTB;
+  const int nstage = (te - tb + kTB - 1) / kTB;
   for (int sidx = nstage - 1; sidx >= 0; --sidx) {
-    const int t0 = sidx * kTB;
-    const int nt = min(kTB, N - t0);
+    const int t0 = tb + sidx * kTB;
+    const int nt = min(kTB, te - t0);
     __syncthreads();  // the previous stage's reads of the staging arrays are done
     for (int e = tid; e < kTB * kMaxD; e += kThreads) {
       const int t = e / kMaxD, i = e % kMaxD;
@@ -288,7 +349,7 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
       __syncthreads();
     }
   }
-  if (active) {
+  if (PASS == 0 && active) {
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) {
       const int i = rg + r * sh.R;
@@ -304,27 +365,79 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
   }
 }
 
+// Per head and state element: the gradient state after every chunk, in
+// place of the chunk's increment, as the right fold from dS_N (dz_N) taken
+// from the last chunk back to the first, and dS0, dz0.
+__global__ void __launch_bounds__(kThreads) bwd_gscan_kernel(const BwdArgs a) {
+  const size_t head = blockIdx.y;
+  const int e = blockIdx.x * kThreads + threadIdx.x;
+  const int nS = a.dk * a.dv;
+  if (e >= nS + a.dk) return;
+  float acc = e < nS ? (a.dS_N ? a.dS_N[head * nS + e] : 0.f) : (a.dz_N ? a.dz_N[head * a.dk + e - nS] : 0.f);
+  const size_t sz = (size_t)nS + a.dk;
+  float* col = a.Gs + head * a.NC * sz + e;
+  for (int c = a.NC - 1; c >= 0; --c) {
+    const float d = col[c * sz];
+    col[c * sz] = acc;
+    acc += d;
+  }
+  if (e < nS) {
+    if (a.dS0) a.dS0[head * nS + e] = acc;
+  } else if (a.dz0) {
+    a.dz0[head * a.dk + e - nS] = acc;
+  }
+}
+
 }  // namespace
+
+// the chunked form: the state before every chunk, the gradient states, and
+// S_N, z_N of the prefill's scan (unused)
+size_t backward_simt_workspace_bytes(int B, int H, int N, int dk, int dv) {
+  int L = 0;
+  const int nc = simt_chunking(B * H, N, dk, dv, &L);
+  if (nc < 2) return 0;
+  return (size_t)B * H * (2 * (size_t)nc + 1) * ((size_t)dk * dv + dk) * sizeof(float);
+}
 
 cudaError_t launch_prefill_backward(const PrefillArgs& p, const float* dO, const float* dS_N,
                                     const float* dz_N, float* dq, float* dk, float* dv,
                                     float* dS0, float* dz0, cudaStream_t stream) {
   const Shape sh = bshape(p.dk, p.dv);
   if ((p.dk + sh.R - 1) / sh.R > kMaxRows) return cudaErrorInvalidValue;
-  BwdArgs a;
+  BwdArgs a = {};
   a.q = p.q; a.k = p.k; a.v = p.v; a.bf16 = p.bf16;
   a.N = p.N; a.dk = p.dk; a.dv = p.dv; a.eps = p.eps;
   a.S0 = p.S0; a.z0 = p.z0; a.dO = dO; a.dS_N = dS_N; a.dz_N = dz_N;
   a.dq = dq; a.dk_out = dk; a.dv_out = dv; a.dS0 = dS0; a.dz0 = dz0;
   const size_t smem = sizeof(float) * (5 * kTB * kMaxD + kTB + sh.R * sh.dvp + kMaxD * sh.G +
                                        kMaxD + 8);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(backward_simt_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto prep = [&](auto kern) -> cudaError_t {
+    if (smem > 48 * 1024)
+      return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return cudaSuccess;
+  };
+  const unsigned BH = (unsigned)((size_t)p.B * p.H);
+  const size_t need = backward_simt_workspace_bytes(p.B, p.H, p.N, p.dk, p.dv);
+  if (!p.workspace || need == 0 || p.ws_bytes < need) {  // one block per head
+    cudaError_t e = prep(backward_simt_kernel<0>);
     if (e != cudaSuccess) return e;
+    backward_simt_kernel<0><<<BH, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
   }
-  const unsigned blocks = (unsigned)((size_t)p.B * p.H);
-  backward_simt_kernel<<<blocks, kThreads, smem, stream>>>(a);
+  a.NC = simt_chunking((int)BH, p.N, p.dk, p.dv, &a.L);
+  const size_t sz = (size_t)p.dk * p.dv + p.dk;
+  float* E = static_cast<float*>(p.workspace);
+  a.E = E;
+  a.Gs = E + (size_t)BH * a.NC * sz;
+  float* SN = a.Gs + (size_t)BH * a.NC * sz;
+  cudaError_t e = launch_simt_entry_states(p, E, SN, SN + (size_t)BH * p.dk * p.dv, stream);
+  if (e == cudaSuccess) e = prep(backward_simt_kernel<1>);
+  if (e == cudaSuccess) e = prep(backward_simt_kernel<2>);
+  if (e != cudaSuccess) return e;
+  const dim3 cgrid((unsigned)a.NC, BH);
+  backward_simt_kernel<1><<<cgrid, kThreads, smem, stream>>>(a);
+  bwd_gscan_kernel<<<dim3((unsigned)((sz + kThreads - 1) / kThreads), BH), kThreads, 0, stream>>>(a);
+  backward_simt_kernel<2><<<cgrid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -342,7 +342,7 @@ size_t la_prefill_backward_workspace_bytes(int B, int H, int N, int dk, int dv, 
   if (!dtype_ok(in_dtype) || !dims_ok(B, H, N, dk, dv)) return 0;
   if (in_dtype == LA_BF16 && dk == 64 && dv == 64 && N > 0)
     return la::backward_tc64_workspace_bytes(B, H, N);
-  return 0;
+  return la::backward_simt_workspace_bytes(B, H, N, dk, dv);  // the CUDA cores' chunks (0: none)
 }
 
 la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dtype in_dtype,

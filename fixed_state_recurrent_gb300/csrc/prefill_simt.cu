@@ -349,6 +349,39 @@ size_t prefill_simt_workspace_bytes(int B, int H, int N, int dk, int dv) {
   return (size_t)BH * nc * ((size_t)dk * dv + dk + 1) * sizeof(float);
 }
 
+int simt_chunking(int BH, int N, int dk, int dv, int* L) {
+  (void)dk;
+  (void)dv;
+  int nc = simt_chunks(BH, N);
+  if (nc < 2) return 1;
+  *L = ((N + nc - 1) / nc + kTB - 1) / kTB * kTB;
+  return (N + *L - 1) / *L;
+}
+
+cudaError_t launch_simt_entry_states(const PrefillArgs& a, float* slots, float* S_N, float* z_N,
+                                     cudaStream_t stream) {
+  const SimtShape sh = simt_shape(a.dk, a.dv);
+  if ((a.dk + sh.R - 1) / sh.R > kMaxRows) return cudaErrorInvalidValue;
+  const int BH = a.B * a.H;
+  SimtChunks ck = {};
+  ck.NC = simt_chunking(BH, a.N, a.dk, a.dv, &ck.L);
+  if (ck.NC < 2) return cudaErrorInvalidValue;
+  ck.slots = slots;
+  const size_t smem = sizeof(float) * (3 * kTB * kMaxD + kTB * sh.R * sh.dvp + kTB * sh.R + kTB);
+  auto kern = prefill_simt_kernel<0, false, 1>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<dim3((unsigned)ck.NC, (unsigned)BH), kThreads, smem, stream>>>(
+      a.q, a.k, a.v, a.bf16, a.N, a.dk, a.dv, a.eps, nullptr, a.S0, a.z0, nullptr, S_N, z_N, ck);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const dim3 sgrid((unsigned)((a.dk * a.dv + a.dk + kThreads - 1) / kThreads), (unsigned)BH);
+  simt_scan_kernel<false><<<sgrid, kThreads, 0, stream>>>(a.dk, a.dv, a.S0, a.z0, S_N, z_N, ck);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream) {
   return launch_prefill_variant_simt(a, nullptr, 0, stream);
 }

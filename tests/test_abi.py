@@ -167,10 +167,15 @@ def test_prefill_variant_workspace_bytes(lib):
     assert lib.la_prefill_variant_workspace_bytes(0, 8, 4096, 64, 64, 1, 0, 1) == 0
     # la_prefill's CUDA-core path: the same slots after the 256-byte header
     assert lib.la_prefill_workspace_bytes(1, 1, 256, 64, 64, 0, 0) == 256 + 32 * (64 * 64 + 64 + 1) * 4
-    # the backward splits its heads over the SMs only on the tensor-core form
+    # the backward splits its heads over the SMs on the tensor-core form and,
+    # elsewhere, into the CUDA-core prefill's chunks: the state before every
+    # chunk, the gradient state after it, and one scratch state per head
     assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 1) > 0
-    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 0) == 0
-    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 128, 128, 1) == 0
+    slot = 64 * 64 + 64
+    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 0) == 32 * (2 * 10 + 1) * slot * 4
+    slot = 128 * 128 + 128
+    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 128, 128, 1) == 32 * (2 * 10 + 1) * slot * 4
+    assert lib.la_prefill_backward_workspace_bytes(8, 64, 4096, 128, 128, 1) == 0  # 512 heads: whole heads
     assert lib.la_prefill_backward_workspace_bytes(4, 8, 0, 64, 64, 1) == 0
     assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 129, 64, 1) == 0
     # it grows with the tokens (the parked phi(K) rows) and covers at least them

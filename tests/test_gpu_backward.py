@@ -20,13 +20,17 @@ def la():
 
 
 SHAPES = [(1, 1, 1, 4, 3), (2, 3, 37, 5, 3), (1, 2, 100, 64, 64), (1, 2, 129, 128, 128),
-          (1, 1, 77, 33, 7)]
+          (1, 1, 77, 33, 7), (1, 2, 1500, 128, 128), (2, 2, 999, 96, 40)]
 
 
+# with a workspace (the binding's default) the CUDA-core form cuts the heads
+# into chunks run in parallel (and bf16 at d = 64 runs on the tensor cores);
+# without one, one block per head
+@pytest.mark.parametrize("ws", [None, False], ids=["ws", "nows"])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("with_state", [False, True], ids=["zero", "state"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
-def test_backward_matches_oracle(la, orc, dtype, with_state, shape):
+def test_backward_matches_oracle(la, orc, dtype, with_state, shape, ws):
     from fixed_state_recurrent_gb300 import inputs
     B, H, N, dk, dv = shape
     q, k, v = inputs.la_inputs(B, H, N, dk, dv, dtype, seed=160 + N)
@@ -40,7 +44,7 @@ def test_backward_matches_oracle(la, orc, dtype, with_state, shape):
         dz = torch.randn((B, H, dk), generator=g)
     cu = lambda t: None if t is None else t.cuda()
     got = la.prefill_backward(q.cuda(), k.cuda(), v.cuda(), dO.cuda(), S0=cu(S0), z0=cu(z0),
-                              dS_N=cu(dS), dz_N=cu(dz))
+                              dS_N=cu(dS), dz_N=cu(dz), ws=ws)
     f = lambda t: None if t is None else f64(t)
     want = orc.la_backward(f64(q), f64(k), f64(v), f64(dO), S0=f(S0), z0=f(z0), dS_N=f(dS),
                            dz_N=f(dz))
@@ -54,6 +58,18 @@ def test_backward_matches_oracle(la, orc, dtype, with_state, shape):
             assert np.max(np.abs(f64(a) - b)) <= 1e-5, name
             continue
         assert relmax(f64(a), b) <= tol, name
+
+
+def test_backward_simt_chunked_repeatable(la):
+    # the chunked CUDA-core form sums in a fixed order: bit for bit from run to run
+    from fixed_state_recurrent_gb300 import inputs
+    q, k, v = inputs.la_inputs(1, 3, 1000, 128, 128, torch.float32, seed=170)
+    dO = torch.randn((1, 3, 1000, 128), generator=torch.Generator().manual_seed(171)).cuda()
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    first = la.prefill_backward(qd, kd, vd, dO)
+    for _ in range(5):
+        again = la.prefill_backward(qd, kd, vd, dO)
+        assert all(torch.equal(a, b) for a, b in zip(first, again))
 
 
 def test_backward_zero_length_passes_state_gradient(la):
