@@ -390,11 +390,16 @@ __global__ void __launch_bounds__(kThreads) bwd_gscan_kernel(const BwdArgs a) {
 
 }  // namespace
 
+// Chunks of the chunked form: about four blocks per SM of a 152-SM GPU (the
+// forward sweep holds one block per SM, the reverse sweep two), so that the
+// sweeps run in whole waves.
+constexpr int kBwdBlocks = 4 * 152;
+
 // the chunked form: the state before every chunk, the gradient states, and
 // S_N, z_N of the prefill's scan (unused)
 size_t backward_simt_workspace_bytes(int B, int H, int N, int dk, int dv) {
   int L = 0;
-  const int nc = simt_chunking(B * H, N, dk, dv, &L);
+  const int nc = simt_chunking(B * H, N, kBwdBlocks, &L);
   if (nc < 2) return 0;
   return (size_t)B * H * (2 * (size_t)nc + 1) * ((size_t)dk * dv + dk) * sizeof(float);
 }
@@ -424,13 +429,13 @@ cudaError_t launch_prefill_backward(const PrefillArgs& p, const float* dO, const
     backward_simt_kernel<0><<<BH, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
   }
-  a.NC = simt_chunking((int)BH, p.N, p.dk, p.dv, &a.L);
+  a.NC = simt_chunking((int)BH, p.N, kBwdBlocks, &a.L);
   const size_t sz = (size_t)p.dk * p.dv + p.dk;
   float* E = static_cast<float*>(p.workspace);
   a.E = E;
   a.Gs = E + (size_t)BH * a.NC * sz;
   float* SN = a.Gs + (size_t)BH * a.NC * sz;
-  cudaError_t e = launch_simt_entry_states(p, E, SN, SN + (size_t)BH * p.dk * p.dv, stream);
+  cudaError_t e = launch_simt_entry_states(p, a.NC, a.L, E, SN, SN + (size_t)BH * p.dk * p.dv, stream);
   if (e == cudaSuccess) e = prep(backward_simt_kernel<1>);
   if (e == cudaSuccess) e = prep(backward_simt_kernel<2>);
   if (e != cudaSuccess) return e;

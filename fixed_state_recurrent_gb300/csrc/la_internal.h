@@ -72,13 +72,15 @@ size_t backward_simt_workspace_bytes(int B, int H, int N, int dk, int dv);
 cudaError_t launch_prefill_backward(const PrefillArgs& p, const float* dO, const float* dS_N,
                                     const float* dz_N, float* dq, float* dk, float* dv,
                                     float* dS0, float* dz0, cudaStream_t stream);
-// The CUDA-core prefill's chunking (prefill_simt.cu): the number of chunks per
-// head (1: whole heads) and their length *L; and its first two launches, the
-// state before every chunk into slots ([B H][NC][dk dv + dk], S row-major then
-// z), S_N and z_N into the given buffers.
-int simt_chunking(int BH, int N, int dk, int dv, int* L);
-cudaError_t launch_simt_entry_states(const PrefillArgs& a, float* slots, float* S_N, float* z_N,
-                                     cudaStream_t stream);
+// The CUDA-core prefill's chunking (prefill_simt.cu) for about `blocks`
+// blocks: the number of chunks per head (1: whole heads) and their length *L
+// (a multiple of the 8-token stage); and its first two launches over NC
+// chunks of L tokens, the state before every chunk into slots
+// ([B H][NC][dk dv + dk], S row-major then z), S_N and z_N into the given
+// buffers.
+int simt_chunking(int BH, int N, int blocks, int* L);
+cudaError_t launch_simt_entry_states(const PrefillArgs& a, int NC, int L, float* slots, float* S_N,
+                                     float* z_N, cudaStream_t stream);
 // The same gradient on the tensor cores for bf16 inputs at dk = dv = 64
 // (backward_tc64.cu): a forward and a reverse sweep over 128-token chunks (it
 // parks bf16 data in dv until the reverse sweep overwrites it); bounded-wait

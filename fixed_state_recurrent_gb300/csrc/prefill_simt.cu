@@ -349,23 +349,27 @@ size_t prefill_simt_workspace_bytes(int B, int H, int N, int dk, int dv) {
   return (size_t)BH * nc * ((size_t)dk * dv + dk + 1) * sizeof(float);
 }
 
-int simt_chunking(int BH, int N, int dk, int dv, int* L) {
-  (void)dk;
-  (void)dv;
-  int nc = simt_chunks(BH, N);
+int simt_chunking(int BH, int N, int blocks, int* L) {
+  // as simt_chunks, with a target block count of the caller's
+  const int by_len = (N + kTB - 1) / kTB;
+  const int by_sm = (blocks + BH - 1) / BH;
+  int nc = by_len < by_sm ? by_len : by_sm;
+  nc = nc < 128 ? nc : 128;
   if (nc < 2) return 1;
   *L = ((N + nc - 1) / nc + kTB - 1) / kTB * kTB;
   return (N + *L - 1) / *L;
 }
 
-cudaError_t launch_simt_entry_states(const PrefillArgs& a, float* slots, float* S_N, float* z_N,
-                                     cudaStream_t stream) {
+cudaError_t launch_simt_entry_states(const PrefillArgs& a, int NC, int L, float* slots, float* S_N,
+                                     float* z_N, cudaStream_t stream) {
   const SimtShape sh = simt_shape(a.dk, a.dv);
   if ((a.dk + sh.R - 1) / sh.R > kMaxRows) return cudaErrorInvalidValue;
   const int BH = a.B * a.H;
   SimtChunks ck = {};
-  ck.NC = simt_chunking(BH, a.N, a.dk, a.dv, &ck.L);
-  if (ck.NC < 2) return cudaErrorInvalidValue;
+  ck.NC = NC;
+  ck.L = L;
+  if (NC < 2 || L % kTB != 0 || (long long)NC * L < a.N || (long long)(NC - 1) * L >= a.N)
+    return cudaErrorInvalidValue;
   ck.slots = slots;
   const size_t smem = sizeof(float) * (3 * kTB * kMaxD + kTB * sh.R * sh.dvp + kTB * sh.R + kTB);
   auto kern = prefill_simt_kernel<0, false, 1>;

@@ -171,11 +171,11 @@ def test_prefill_variant_workspace_bytes(lib):
     # elsewhere, into the CUDA-core prefill's chunks: the state before every
     # chunk, the gradient state after it, and one scratch state per head
     assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 1) > 0
-    slot = 64 * 64 + 64
-    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 0) == 32 * (2 * 10 + 1) * slot * 4
+    slot = 64 * 64 + 64  # 32 heads: 19 chunks each make about four blocks per SM
+    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 64, 64, 0) == 32 * (2 * 19 + 1) * slot * 4
     slot = 128 * 128 + 128
-    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 128, 128, 1) == 32 * (2 * 10 + 1) * slot * 4
-    assert lib.la_prefill_backward_workspace_bytes(8, 64, 4096, 128, 128, 1) == 0  # 512 heads: whole heads
+    assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 128, 128, 1) == 32 * (2 * 19 + 1) * slot * 4
+    assert lib.la_prefill_backward_workspace_bytes(8, 128, 4096, 128, 128, 1) == 0  # 1024 heads: whole heads
     assert lib.la_prefill_backward_workspace_bytes(4, 8, 0, 64, 64, 1) == 0
     assert lib.la_prefill_backward_workspace_bytes(4, 8, 4096, 129, 64, 1) == 0
     # it grows with the tokens (the parked phi(K) rows) and covers at least them
