@@ -53,7 +53,7 @@ extern "C" {
 typedef enum {
   LA_OK = 0,
   LA_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment, aliasing or eps */
-  LA_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no sm_103a device) */
+  LA_ERR_UNSUPPORTED = 2,  /* valid request the library cannot run here (e.g. no sm_103a device) */
   LA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
   LA_ERR_TIMEOUT = 4       /* a kernel's bounded inter-block wait gave up */
 } la_status;
