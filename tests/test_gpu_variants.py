@@ -268,6 +268,19 @@ def test_prefill_variant_zero_length_copies_state(la):
     assert torch.equal(S, S0) and torch.equal(z, z0)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mode,decay", [(0, True), (1, False), (1, True), (2, False)],
+                         ids=["causal_decay", "rbw", "rbw_decay", "nc"])
+def test_prefill_variant_tc_zero_length_copies_state(la, d, mode, decay):
+    # bf16 at the tensor-core widths, every order: no tokens, the state passes through
+    e = torch.empty((1, 2, 0, d), dtype=torch.bfloat16, device="cuda")
+    S0 = torch.rand((1, 2, d, d), device="cuda")
+    z0 = torch.rand((1, 2, d), device="cuda")
+    alpha = torch.empty((1, 2, 0), device="cuda") if decay else None
+    o, S, z = la.prefill_variant(e, e, e, alpha, mode, S0=S0, z0=z0)
+    assert torch.equal(S, S0) and torch.equal(z, z0)
+
+
 # gated delta on the tensor cores (bf16, dk = dv = 128): chunkwise with decay factors
 GATED_N = [1, 64, 65, 129, 300, 1000]
 
