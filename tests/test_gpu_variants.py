@@ -580,3 +580,25 @@ def test_decay_prefill_tc_split_and_per_head_agree(la, orc, shape):
         assert relmax(f64(got[0]), ro) <= TOL_BF16
         assert relmax(f64(got[1]), rS) <= TOL_BF16
         assert relmax(f64(got[2]), rz) <= TOL_BF16
+
+
+# The variant workloads the bench times, at full size (B=4 H=8 N=4096, bf16,
+# the bench's seeds and alpha ~ U(0.9, 1)): every head against the oracle, in
+# the launch configuration the bench uses (a workspace from the binding).
+@pytest.mark.parametrize("wname", ["prefill", "prefill128"])
+@pytest.mark.parametrize("mode,decay", [(0, True), (1, False), (2, False)], ids=["decay", "rbw", "nc"])
+def test_variant_bench_workloads_full(la, orc, wname, mode, decay):
+    from fixed_state_recurrent_gb300 import inputs
+    w = inputs.WORKLOADS[wname]
+    q, k, v = inputs.la_inputs(w.B, w.H, w.N, w.dk, w.dv, w.dtype, w.seed)
+    alpha = None
+    if decay:
+        g = torch.Generator().manual_seed(6)
+        alpha = 0.9 + 0.1 * torch.rand((w.B, w.H, w.N), generator=g)
+    la.delta_read_device_status()
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), None if alpha is None else alpha.cuda(), mode)
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), None if alpha is None else f64(alpha), mode)
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+    assert relmax(f64(z), rz) <= TOL_BF16
+    assert la.delta_read_device_status() == 0
