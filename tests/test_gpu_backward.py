@@ -198,12 +198,14 @@ def test_backward_tc_bounded_wait_reports_timeout(la, orc, monkeypatch, ws):
         assert relmax(f64(a), b) <= tol_for(torch.bfloat16)
 
 
-def test_backward_d128_bench_shape_full(la, orc):
-    # B=4 H=8 N=4096 dk=dv=128, bf16 (the CUDA-core form in parallel chunks):
-    # every head against the oracle
+@pytest.mark.parametrize("d,seed", [(64, 1), (128, 5)], ids=["d64", "d128"])
+def test_backward_bench_shape_full(la, orc, d, seed):
+    # B=4 H=8 N=4096, bf16 (d = 64: the chunk-parallel tensor-core form the
+    # bench times; d = 128: the CUDA-core form in parallel chunks): every head
+    # against the oracle
     from fixed_state_recurrent_gb300 import inputs
-    q, k, v = inputs.la_inputs(4, 8, 4096, 128, 128, torch.bfloat16, 5)
-    dO = torch.randn((4, 8, 4096, 128), generator=torch.Generator().manual_seed(9))
+    q, k, v = inputs.la_inputs(4, 8, 4096, d, d, torch.bfloat16, seed)
+    dO = torch.randn((4, 8, 4096, d), generator=torch.Generator().manual_seed(9))
     got = la.prefill_backward(q.cuda(), k.cuda(), v.cuda(), dO.cuda())
     want = orc.la_backward(f64(q), f64(k), f64(v), f64(dO))
     for name, a, b in zip(("dq", "dk", "dv", "dS0", "dz0"), got, want):
