@@ -27,12 +27,14 @@
 // launches run them in parallel:
 //   1-2. the prefill's chunk increments and scan: the state before every
 //        chunk (prefill_simt.cu);
-//   3. PASS 1, per chunk: the forward sweep from the state before the chunk,
-//      and the chunk's gradient-state increment
-//      dG_c = sum_{t in c} phi(q_t) dnum_t^T, dg_c = sum_{t in c} dden_t phi(q_t);
-//   4. per head, the gradient state after every chunk as the right fold
+//   3. PASS 1, per chunk: the forward sweep from the state before the chunk
+//      (dq; dnum and dden parked);
+//   4. per chunk, its gradient-state increment from the parked rows,
+//      dG_c = sum_{t in c} phi(q_t) dnum_t^T, dg_c = sum_{t in c} dden_t phi(q_t)
+//      (a product over the chunk's tokens, no per-token reductions);
+//   5. per head, the gradient state after every chunk as the right fold
 //      dS_N + dG_{c+1} + dG_{c+2} + ... (always in this order), and dS0, dz0;
-//   5. PASS 2, per chunk: the reverse sweep from the gradient state after the
+//   6. PASS 2, per chunk: the reverse sweep from the gradient state after the
 //      chunk.
 #include "la_internal.h"
 
@@ -109,15 +111,6 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
     z[r] = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) S[r][c] = 0.f;
-  }
-  // PASS 1: the chunk's gradient-state increment, this thread's slice
-  float dG[kMaxRows][4];
-  float dg[kMaxRows];
-#pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) {
-    dg[r] = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) dG[r][c] = 0.f;
   }
   if (PASS != 2 && active) {  // the state before the block's first token
 #pragma unroll
@@ -221,14 +214,6 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
             float s = S[r][0] * dn.x + S[r][1] * dn.y + S[r][2] * dn.z + S[r][3] * dn.w;
             if (g == 0) s += dden * z[r];
             rpart[i * sh.G + g] = s;
-            if (PASS == 1) {  // phi(q_t) dnum_t^T and dden_t phi(q_t)
-              const float qq = fq[t * kMaxD + i];
-              dG[r][0] += qq * dn.x;
-              dG[r][1] += qq * dn.y;
-              dG[r][2] += qq * dn.z;
-              dG[r][3] += qq * dn.w;
-              dg[r] += dden * qq;
-            }
           }
         }
       }
@@ -243,21 +228,7 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
     }
   }
 
-  if (PASS == 1) {  // the chunk's gradient-state increment
-    if (active) {
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
-        const int i = rg + r * sh.R;
-        if (i < dk) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (col0 + c < dv) a.Gs[slot + (size_t)i * dv + col0 + c] = dG[r][c];
-          if (g == 0) a.Gs[slot + (size_t)dk * dv + i] = dg[r];
-        }
-      }
-    }
-    return;
-  }
+  if (PASS == 1) return;
 
   // ---------------------------------------------------------------- reverse
   // S and z become G and g
@@ -365,6 +336,77 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
   }
 }
 
+// Per chunk (blockIdx.x) of head blockIdx.y: dG_c = sum_t phi(q_t) dnum_t^T
+// and dg_c = sum_t dden_t phi(q_t) over the chunk's tokens, from the rows the
+// forward sweep parked in dv_out (dnum) and dk_out (dden, element 0), into
+// the chunk's slot of Gs.  Thread (row group, column group) owns the same
+// (rows x 4) slice as in the sweeps.
+__global__ void __launch_bounds__(kThreads) bwd_increment_kernel(const BwdArgs a) {
+  extern __shared__ float sm[];
+  const Shape sh = bshape(a.dk, a.dv);
+  const int N = a.N, dk = a.dk, dv = a.dv;
+  float* fq = sm;                  // [kTB][kMaxD] phi(q)
+  float* dn = fq + kTB * kMaxD;    // [kTB][kMaxD] dnum
+  float* dd = dn + kTB * kMaxD;    // [kTB] dden
+  const int tid = threadIdx.x;
+  const int g = tid % sh.G, rg = tid / sh.G;
+  const bool active = rg < sh.R;
+  const int col0 = 4 * g;
+  const size_t head = blockIdx.y;
+  const int chunk = blockIdx.x;
+  const int tb = chunk * a.L, te = min(N, tb + a.L);
+  const size_t slot = (head * a.NC + chunk) * ((size_t)dk * dv + dk);
+  float G[kMaxRows][4], gz[kMaxRows];
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) {
+    gz[r] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) G[r][c] = 0.f;
+  }
+  for (int t0 = tb; t0 < te; t0 += kTB) {
+    const int nt = min(kTB, te - t0);
+    __syncthreads();  // the previous stage has been read
+    for (int e = tid; e < kTB * kMaxD; e += kThreads) {
+      const int t = e / kMaxD, i = e % kMaxD;
+      const bool in = t < nt;
+      fq[e] = (in && i < dk) ? phi_f32(load_in(a.q, (head * N + t0 + t) * dk + i, a.bf16)) : 0.f;
+      dn[e] = (in && i < dv) ? a.dv_out[(head * N + t0 + t) * dv + i] : 0.f;
+    }
+    if (tid < kTB) dd[tid] = tid < nt ? a.dk_out[(head * N + t0 + tid) * dk] : 0.f;
+    __syncthreads();
+    if (active) {
+      for (int t = 0; t < nt; ++t) {
+        const float4 d4 = *reinterpret_cast<const float4*>(&dn[t * kMaxD + col0]);
+        const float de = dd[t];
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          const int i = rg + r * sh.R;
+          if (i < dk) {
+            const float qq = fq[t * kMaxD + i];
+            G[r][0] += qq * d4.x;
+            G[r][1] += qq * d4.y;
+            G[r][2] += qq * d4.z;
+            G[r][3] += qq * d4.w;
+            gz[r] += de * qq;
+          }
+        }
+      }
+    }
+  }
+  if (active) {
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      const int i = rg + r * sh.R;
+      if (i < dk) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (col0 + c < dv) a.Gs[slot + (size_t)i * dv + col0 + c] = G[r][c];
+        if (g == 0) a.Gs[slot + (size_t)dk * dv + i] = gz[r];
+      }
+    }
+  }
+}
+
 // Per head and state element: the gradient state after every chunk, in
 // place of the chunk's increment, as the right fold from dS_N (dz_N) taken
 // from the last chunk back to the first, and dS0, dz0.
@@ -391,8 +433,7 @@ __global__ void __launch_bounds__(kThreads) bwd_gscan_kernel(const BwdArgs a) {
 }  // namespace
 
 // Chunks of the chunked form: about four blocks per SM of a 152-SM GPU (the
-// forward sweep holds one block per SM, the reverse sweep two), so that the
-// sweeps run in whole waves.
+// sweeps hold two blocks per SM), so that they run in whole waves.
 constexpr int kBwdBlocks = 4 * 152;
 
 // the chunked form: the state before every chunk, the gradient states, and
@@ -441,6 +482,7 @@ cudaError_t launch_prefill_backward(const PrefillArgs& p, const float* dO, const
   if (e != cudaSuccess) return e;
   const dim3 cgrid((unsigned)a.NC, BH);
   backward_simt_kernel<1><<<cgrid, kThreads, smem, stream>>>(a);
+  bwd_increment_kernel<<<cgrid, kThreads, sizeof(float) * (2 * kTB * kMaxD + kTB), stream>>>(a);
   bwd_gscan_kernel<<<dim3((unsigned)((sz + kThreads - 1) / kThreads), BH), kThreads, 0, stream>>>(a);
   backward_simt_kernel<2><<<cgrid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();

@@ -353,8 +353,7 @@ int simt_chunking(int BH, int N, int blocks, int* L) {
   // as simt_chunks, with a target block count of the caller's
   const int by_len = (N + kTB - 1) / kTB;
   const int by_sm = (blocks + BH - 1) / BH;
-  int nc = by_len < by_sm ? by_len : by_sm;
-  nc = nc < 128 ? nc : 128;
+  const int nc = by_len < by_sm ? by_len : by_sm;
   if (nc < 2) return 1;
   *L = ((N + nc - 1) / nc + kTB - 1) / kTB * kTB;
   return (N + *L - 1) / *L;

@@ -194,11 +194,10 @@ size_t la_prefill_variant_workspace_bytes(int B, int H, int N, int dk, int dv,
  * With NULL, one block per head, both sweeps.  A bounded wait of those kernels
  * that gives up is reported by delta_read_device_status.  Everything else runs
  * on the CUDA cores in fp32, any dk, dv <= 128: with a workspace, each head
- * cut into the CUDA-core prefill's chunks, run in parallel (the state before
- * every chunk from the prefill's first two launches, a forward sweep per chunk
- * that also sums the chunk's gradient-state increment, a reverse scan per
- * head, a reverse sweep per chunk); with NULL, one block per head, token by
- * token.
+ * cut into chunks run in parallel (the state before every chunk from the
+ * CUDA-core prefill's first two launches, a forward sweep per chunk, each
+ * chunk's gradient-state increment, a reverse scan per head, a reverse sweep
+ * per chunk); with NULL, one block per head, token by token.
  */
 la_status la_prefill_backward(const void* q, const void* k, const void* v, la_dtype in_dtype,
                               int B, int H, int N, int dk, int dv, float eps,
