@@ -649,9 +649,12 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
       // gated: the pair's gamma factors are published with its T (tready)
       const float* gam = reinterpret_cast<const float*>(smem + OFF_GAM) + (((ch / 2) & 1) * 2 + (ch & 1)) * 2 * CH;
       if (GATED && (ch & 1) == 0) waitd_warp(x, &B->tready[(ch / 2) & 1], ((ch / 2) >> 1) & 1);
-      // SB = bf16(S^T) once S has advanced past chunk ch - 1
+      // SB = bf16(S^T) once S has advanced past chunk ch - 1; gated: in the
+      // same pass S <- gamma_C S for this chunk's state product (issued after
+      // ubready), while SB keeps S itself for K S
       if (ch > 0) waitd_warp(x, &B->sready, (ch - 1) & 1);
       tc_fence_after();
+      const float gc = GATED ? gam[CH - 1] : 1.f;
 #pragma unroll 1
       for (int h = 0; h < 4; ++h) {
         uint32_t f[32], w[16];
@@ -660,18 +663,8 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 #pragma unroll
         for (int q = 0; q < 16; ++q) w[q] = pack_bf16x2(__uint_as_float(f[2 * q]), __uint_as_float(f[2 * q + 1]));
         tmem_st16(tl + SB + 16 * h, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B->sbready);
-      if (GATED) {  // S <- gamma_C S before this chunk's state product (after ubready)
-        const float gc = gam[CH - 1];
-#pragma unroll 1
-        for (int h = 0; h < 4; ++h) {
-          uint32_t f[32], w0[16], w1[16];
-          tmem_ld32(tl + ST + 32 * h, f);
-          tmem_ld_wait();
+        if (GATED) {
+          uint32_t w0[16], w1[16];
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             w0[q] = __float_as_uint(gc * __uint_as_float(f[q]));
@@ -680,8 +673,11 @@ delta_chunked_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
           tmem_st16(tl + ST + 32 * h, w0);
           tmem_st16(tl + ST + 32 * h + 16, w1);
         }
-        tmem_st_wait();
       }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B->sbready);
       // reads of chunk ch - 1 (R^T in its KR region, which this chunk's U^T
       // overwrites only after xready below)
       if (ch > 0) {
