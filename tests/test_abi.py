@@ -226,3 +226,43 @@ def test_backward_rejects_invalid_arguments(lib):
     assert call(ws=BASE + 8 * MB + 8, wsb=need) == 1       # misaligned workspace
     assert call(ws=BASE + 6 * MB, wsb=need) == 1           # workspace overlaps dv
     assert call(ws=BASE + 2 * MB - 16, wsb=need) == 1      # workspace overlaps v
+
+
+def _split(BH, N, sms=152):
+    """The work split of the tensor-core kernels (piece slots per head), as the
+    header describes it: G = min(chunks, SMs) runs, MPH = ceil(NC / L) + 1."""
+    NC = (N + 127) // 128
+    tc = BH * NC
+    G = min(tc, sms)
+    L = tc // G
+    return NC, tc, (NC + L - 1) // L + 1
+
+
+def test_tensor_core_variant_workspace_sizes(lib):
+    # the workspace of each tensor-core form, from the split alone (the CPU has
+    # no device, so the library takes a 152-SM GPU)
+    B, H, N = 4, 8, 4096
+    BH = B * H
+    NC, tc, mph = _split(BH, N)
+    slot64, slot128 = (64 * 64 + 64) * 4, (128 * 128 + 128) * 4
+    simt = lambda d: lib.la_prefill_variant_workspace_bytes(B, H, N, d, d, 0, 1, 0)  # fp32: CUDA cores
+    prefix64 = BH * mph * slot64 + tc * 66 * 128 + BH * N * 64 * 2
+    # la_prefill: header, then the two-launch form's totals, prefix tiles and phi(K)
+    assert lib.la_prefill_workspace_bytes(B, H, N, 64, 64, 1, 0) == 256 + prefix64
+    # d = 128: header, then two slot arrays (no phi(K) copy)
+    assert lib.la_prefill_workspace_bytes(B, H, N, 128, 128, 1, 0) == 256 + 2 * BH * mph * slot128
+    # read before write at d = 64 (two-launch form): the prefill's workspace, no header
+    assert lib.la_prefill_variant_workspace_bytes(B, H, N, 64, 64, 1, 1, 0) == max(prefix64, simt(64))
+    # non-causal at d = 64: that plus one [80 x 64] bf16 state tile per head
+    assert lib.la_prefill_variant_workspace_bytes(B, H, N, 64, 64, 1, 2, 0) == max(prefix64 + BH * 80 * 128,
+                                                                                 simt(64))
+    # non-causal at d = 128: the totals, then one [144 x 128] bf16 tile per head
+    assert lib.la_prefill_variant_workspace_bytes(B, H, N, 128, 128, 1, 2, 0) == max(
+        BH * mph * slot128 + BH * 2 * 144 * 128, simt(128))
+    # read before write at d = 128: the three-launch prefill's workspace with its header
+    assert lib.la_prefill_variant_workspace_bytes(B, H, N, 128, 128, 1, 1, 0) == max(
+        256 + 2 * BH * mph * slot128, simt(128))
+    # decayed at d = 128, either order: totals, entry states and one decay per slot
+    dec128 = (2 * BH * mph * (128 * 128 + 128) + BH * mph) * 4
+    assert lib.la_prefill_variant_workspace_bytes(B, H, N, 128, 128, 1, 0, 1) == max(dec128, simt(128))
+    assert lib.la_prefill_variant_workspace_bytes(B, H, N, 128, 128, 1, 1, 1) == max(dec128, simt(128))
