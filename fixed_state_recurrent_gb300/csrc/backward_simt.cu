@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) backward_simt_kernel(const BwdArgs a
     }
   }
 
-  if (PASS == 1) return;
+  if (PASS == 1) return;  // (the reverse sweep below is then unreachable)
 
   // ---------------------------------------------------------------- reverse
   // S and z become G and g

@@ -35,7 +35,6 @@ constexpr int kThreads = 128;     // one thread per chunk row / TMEM lane
 
 template <int D>
 struct Nc {
-  static constexpr int SZ = D * D + D;                        // floats per state slot
   static constexpr int NS = StateTile<D>::NS;                 // state operand rows (N of the product)
   static constexpr uint32_t QT = (D / 64) * BLK;              // a Q tile: D / 64 column blocks
   static constexpr uint32_t XA = StateTile<D>::XA;            // one K-atom of the state operand
@@ -110,7 +109,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 nc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
           const Params p, const unsigned long long mbar_ns) {
   using L = Nc<D>;
-  constexpr int SZ = L::SZ;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* B = reinterpret_cast<Bars*>(smem + L::OFF_BAR);
@@ -118,7 +116,7 @@ nc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   uint8_t* out = smem + L::OFF_OUT;
   const int t = threadIdx.x, warp = t / 32;
   const Split& sp = p.sp;
-  const int N = sp.N, NC = sp.NC;
+  const int NC = sp.NC;
   const Run run(sp, blockIdx.x);
   const uint32_t total = (uint32_t)(run.b - run.a);
   if (t == 0) {
@@ -300,7 +298,7 @@ cudaError_t launch_prefill_nc64(const PrefillArgs& a, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   Prefix64Buffers b = {};
   b.R = reinterpret_cast<float*>(ws);
-  b.P = reinterpret_cast<uint8_t*>(b.R + (size_t)BH * sr.MPH * Nc<D>::SZ);
+  b.P = reinterpret_cast<uint8_t*>(b.R + (size_t)BH * sr.MPH * (D * D + D));  // slots of D D + D floats
   b.phik = reinterpret_cast<__nv_bfloat16*>(b.P + (size_t)sr.TC() * 66 * 128);
   uint8_t* tiles = ws + prefill_prefix64_workspace_bytes(a.B, a.H, a.N);
   cudaError_t e = library_status_word(&b.status);
