@@ -486,6 +486,24 @@ def test_decay_read_before_write_tc_matches_oracle(la, orc, shape, arange, ws):
     assert la.delta_read_device_status() == 0
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decay_read_before_write_tc_large_eps(la, orc, d):
+    # with a large eps a stray alpha_t on the read would show: token t reads
+    # S_{t-1} (decayed only up to token t - 1), numerator and denominator alike
+    from fixed_state_recurrent_gb300 import inputs
+    B, H, N = 1, 3, 700
+    q, k, v = inputs.la_inputs(B, H, N, d, d, torch.bfloat16, seed=215 + d)
+    g = torch.Generator().manual_seed(216 + d)
+    alpha = 0.2 + 0.8 * torch.rand((B, H, N), generator=g)
+    S0 = torch.randn((B, H, d, d), generator=g) * 0.5
+    z0 = torch.rand((B, H, d), generator=g) * 4 + 0.5
+    o, S, z = la.prefill_variant(q.cuda(), k.cuda(), v.cuda(), alpha.cuda(), la.LA_MODE_READ_BEFORE_WRITE,
+                                 eps=0.5, S0=S0.cuda(), z0=z0.cuda())
+    ro, rS, rz = orc.la_variant(f64(q), f64(k), f64(v), f64(alpha), 1, eps=0.5, S0=f64(S0), z0=f64(z0))
+    assert relmax(f64(o), ro) <= TOL_BF16
+    assert relmax(f64(S), rS) <= TOL_BF16
+
+
 def test_decay_prefill_tc_zero_alpha_forgets(la, orc):
     # alpha = 0 at some tokens (taken as 1e-30 in the chunk factors): the state
     # before them is forgotten, including right at chunk edges

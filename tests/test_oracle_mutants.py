@@ -61,6 +61,10 @@ MUTANTS = [
      "S[i * dv + j] = at * (S[i * dv + j] + fk[i] * vt[j]);"),
     ("variant_rbw_reads_after_write", "      if (a->mode == 1) var_read(fq, S, z, dk, dv, a->eps, ot);",
      "      if (a->mode == 1) {}"),
+    ("variant_rbw_reads_decayed_state", "      if (a->mode == 1) var_read(fq, S, z, dk, dv, a->eps, ot);",
+     "      if (a->mode == 1) { for (int e = 0; e < dk * dv; ++e) S[e] *= at; for (int i = 0; i < dk; ++i) z[i] *= at;"
+     " var_read(fq, S, z, dk, dv, a->eps, ot); for (int e = 0; e < dk * dv; ++e) S[e] /= at;"
+     " for (int i = 0; i < dk; ++i) z[i] /= at; }"),
     ("variant_noncausal_reads_prefix",
      "    /* then every query reads it */\n    for (int t = 0; t < N; ++t) {",
      "    /* then every query reads it */\n    for (int t = 0; t < N && 0; ++t) {"),
@@ -96,6 +100,8 @@ def _pin_functions():
             out.append(lambda orc, f=fn: [f(orc, c) for c in (1, 3, 16, 101)])
         elif name == "test_variant_recurrence_equals_explicit_weights":
             out.append(lambda orc, f=fn: [f(orc, m) for m in (0, 1, 2)])
+        elif name == "test_decayed_read_before_write_reads_the_state_one_token_late":
+            out.append(lambda orc, f=fn: [f(orc, e) for e in (1e-6, 0.5)])
         elif name == "test_backward_matches_finite_differences":
             out.append(lambda orc, f=fn: [f(orc, w) for w in (False, True)])
     return out

@@ -473,6 +473,32 @@ def test_read_before_write_first_read_is_zero_and_strictly_past(orc):
     np.testing.assert_allclose(o[:, :, 1:], oc, rtol=1e-13, atol=1e-15)
 
 
+@pytest.mark.parametrize("eps", [1e-6, 0.5])
+def test_decayed_read_before_write_reads_the_state_one_token_late(orc, eps):
+    # read before write with a decay: token t reads S_{t-1}, the state after
+    # token t - 1's own decay and write, not yet decayed by alpha_t.  So with
+    # the query held fixed it is the write-then-read output of the sequence
+    # shifted by one token.  (A large eps exposes a stray alpha_t on the read:
+    # such a factor scales numerator and denominator alike and cancels against
+    # all but eps.)
+    q, k, v = _rand_la(80, 2, 2, 13, 4, 3)
+    r = _rng(81)
+    alpha = r.uniform(0.2, 1.0, size=(2, 2, 13))
+    S0 = r.uniform(size=(2, 2, 4, 3))
+    z0 = r.uniform(size=(2, 2, 4)) + 0.5
+    o, S, z = orc.la_variant(q, k, v, alpha, orc.MODE_READ_BEFORE_WRITE, eps=eps, S0=S0, z0=z0)
+    oc, _, _ = orc.la_variant(q[:, :, 1:], k[:, :, :-1], v[:, :, :-1], alpha[:, :, :-1],
+                              orc.MODE_CAUSAL, eps=eps, S0=S0, z0=z0)
+    np.testing.assert_allclose(o[:, :, 1:], oc, rtol=1e-12, atol=1e-15)
+    fq = orc.phi(q[:, :, 0])  # the first read is the initial state's
+    want0 = np.einsum("bhi,bhij->bhj", fq, S0) / (np.einsum("bhi,bhi->bh", fq, z0)[..., None] + eps)
+    np.testing.assert_allclose(o[:, :, 0], want0, rtol=1e-12)
+    # the final state is the write-then-read one
+    _, Sc, zc = orc.la_variant(q, k, v, alpha, orc.MODE_CAUSAL, eps=eps, S0=S0, z0=z0)
+    np.testing.assert_allclose(S, Sc, rtol=1e-13)
+    np.testing.assert_allclose(z, zc, rtol=1e-13)
+
+
 def test_decay_zero_attends_to_the_current_token_only(orc):
     q, k, v = _rand_la(76, 1, 2, 7, 4, 3)
     eps = 1e-6
