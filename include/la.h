@@ -137,9 +137,9 @@ la_status la_prefill(const void* q, const void* k, const void* v, la_dtype in_dt
  * runs on the tensor cores: LA_MODE_READ_BEFORE_WRITE as la_prefill's
  * launches with a strict mask inside each chunk; LA_MODE_NONCAUSAL as the
  * totals of the heads' pieces (la_prefill's first launch at dk = 64 for calls
- * of at most 2048 chunks of 128 tokens, else its aggregate launch followed by
- * one fold per head into S_N, z_N), then every query reads its head's final
- * state (one product per chunk against a bf16 copy of it, z as hi + lo).  A
+ * of at most 2048 chunks of 128 tokens, else the aggregate launch of its
+ * three-launch form), one fold per head into S_N, z_N and a bf16 copy of that
+ * state (z as hi + lo), then every query reads it (one product per chunk).  A
  * bounded wait of those kernels that gives up is reported by
  * delta_read_device_status.  Everything else runs on the CUDA cores in fp32,
  * for LA_F32 and LA_BF16 inputs and any dk, dv <= 128: with a workspace of
